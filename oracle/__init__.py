@@ -1,0 +1,239 @@
+"""CPU oracle for the sparse-decode hot path.  TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package.  It wraps ``sd_oracle.c`` (plain C, double accumulation,
+built with ``-ffp-contract=off``), which shares no code with the CUDA library.
+Every function takes and returns numpy arrays; bf16 tensors travel as their
+uint16 bit patterns.
+
+Pins (tests/test_oracle_pins.py) tie each function to something other than
+itself: the HashAttention worked example, the bit-plane prefix invariant, brute
+force over all bf16 values, brute-force water-filling, the Quest bound,
+brute-force top-k, dense softmax attention at k = n.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sd_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+PLAN_WATERFILL, PLAN_FIXED, PLAN_FULL = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so next to its source."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _l():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            p, i64, i32, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+            lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
+            lib.orc_f32_to_f16.restype = ctypes.c_uint16
+            lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.orc_f16_to_f32.restype = ctypes.c_float
+            lib.orc_reconstruct.argtypes = [i32, i32, d]
+            lib.orc_reconstruct.restype = d
+            lib.orc_sig_encode.argtypes = [p, i64, i32, p, p, i32, p, p, p]
+            lib.orc_sig_encode.restype = i32
+            lib.orc_hamming_score.argtypes = [p, i64, i32, i32, i64, p, p]
+            lib.orc_hamming_score.restype = None
+            lib.orc_plane_build.argtypes = [p, i64, i32, i64, i32, p, p]
+            lib.orc_plane_build.restype = i32
+            lib.orc_plan.argtypes = [p, p, i64, i32, i32, i32, i32, i32, p]
+            lib.orc_plan.restype = i32
+            lib.orc_plane_score.argtypes = [p, p, p, p, i64, i32, i32, i64, i32, p]
+            lib.orc_plane_score.restype = None
+            lib.orc_plane_score_l1.argtypes = [p, p, p, p, i64, i32, i32, i64, i32, p]
+            lib.orc_plane_score_l1.restype = None
+            lib.orc_minmax_build.argtypes = [p, i64, i32, i64, i32, p]
+            lib.orc_minmax_build.restype = None
+            lib.orc_quest_score.argtypes = [p, p, i64, i32, i32, i64, i32, p, p]
+            lib.orc_quest_score.restype = None
+            lib.orc_topk.argtypes = [p, i32, i64, i64, i32, i32, i32, i32, i64, p, i64, p]
+            lib.orc_topk.restype = None
+            lib.orc_gather_attend.argtypes = [p, p, p, i64, i32, i32, i64, i32, p, i64, p, d,
+                                              p, p]
+            lib.orc_gather_attend.restype = None
+            lib.orc_prefix_copy.argtypes = [p, p, p, i64, i32, i64, i32, p, p]
+            lib.orc_prefix_copy.restype = None
+            _lib = lib
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+def f32_to_f16(x: float) -> int:
+    return int(_l().orc_f32_to_f16(float(x)))
+
+
+def f16_to_f32(h: int) -> float:
+    return float(_l().orc_f16_to_f32(int(h)))
+
+
+def reconstruct(prefix: int, t: int, s: float) -> float:
+    return float(_l().orc_reconstruct(int(prefix), int(t), float(s)))
+
+
+def sig_encode(x_bf16: np.ndarray, W1, b1, W2=None, b2=None) -> np.ndarray:
+    """32-bit signatures of the rows of x (last dim d)."""
+    x, px = _c(x_bf16, np.uint16)
+    d = x.shape[-1]
+    rows = x.size // d
+    W1, pW1 = _c(W1, np.float32)
+    b1, pb1 = _c(b1, np.float32)
+    hidden = 0
+    pW2 = pb2 = None
+    if W2 is not None:
+        hidden = W1.shape[0]
+        W2, pW2 = _c(W2, np.float32)
+        b2, pb2 = _c(b2, np.float32)
+    out = np.empty(rows, np.uint32)
+    rc = _l().orc_sig_encode(px, rows, d, pW1, pb1, hidden, pW2, pb2, out.ctypes.data)
+    if rc:
+        raise ValueError("orc_sig_encode: unsupported size")
+    return out.reshape(x.shape[:-1])
+
+
+def hamming_score(sig: np.ndarray, qsig: np.ndarray) -> np.ndarray:
+    """sig uint32 [B][Hkv][n], qsig uint32 [B][Hq] -> int32 [B][Hkv][n]."""
+    sig, ps = _c(sig, np.uint32)
+    qsig, pq = _c(qsig, np.uint32)
+    B, Hkv, n = sig.shape
+    Hq = qsig.shape[1]
+    out = np.empty((B, Hkv, n), np.int32)
+    _l().orc_hamming_score(ps, B, Hq, Hkv, n, pq, out.ctypes.data)
+    return out
+
+
+def plane_build(K: np.ndarray):
+    """K bf16 [B][Hkv][n][d] -> planes uint32 [B][Hkv][d][4][n/32], scales f16 bits
+    uint16 [B][Hkv][d][n/64]."""
+    K, pk = _c(K, np.uint16)
+    B, Hkv, n, d = K.shape
+    planes = np.empty((B, Hkv, d, 4, n // 32), np.uint32)
+    scales = np.empty((B, Hkv, d, n // 64), np.uint16)
+    if _l().orc_plane_build(pk, B, Hkv, n, d, planes.ctypes.data, scales.ctypes.data):
+        raise ValueError("plane_build needs n % 64 == 0")
+    return planes, scales
+
+
+def plan(q: np.ndarray, sigma2: np.ndarray, Hkv: int, mode: int, budget: int) -> np.ndarray:
+    """q bf16 [B][Hq][d], sigma2 f32 [Hkv][d] -> plan uint8 [B][Hkv][d]."""
+    q, pq = _c(q, np.uint16)
+    s2, ps = _c(sigma2, np.float32)
+    B, Hq, d = q.shape
+    out = np.empty((B, Hkv, d), np.uint8)
+    if _l().orc_plan(pq, ps, B, Hq, Hkv, d, mode, budget, out.ctypes.data):
+        raise ValueError("plan: bad mode/budget")
+    return out
+
+
+def plane_score(planes, scales, plan_, q, with_l1: bool = False):
+    planes, pp = _c(planes, np.uint32)
+    scales, psc = _c(scales, np.uint16)
+    plan_, ppl = _c(plan_, np.uint8)
+    q, pq = _c(q, np.uint16)
+    B, Hkv, d, _, nw = planes.shape
+    n = nw * 32
+    Hq = q.shape[1]
+    out = np.empty((B, Hkv, n), np.float64)
+    _l().orc_plane_score(pp, psc, ppl, pq, B, Hq, Hkv, n, d, out.ctypes.data)
+    if not with_l1:
+        return out
+    l1 = np.empty((B, Hkv, n), np.float64)
+    _l().orc_plane_score_l1(pp, psc, ppl, pq, B, Hq, Hkv, n, d, l1.ctypes.data)
+    return out, l1
+
+
+def minmax_build(K: np.ndarray) -> np.ndarray:
+    """K bf16 [B][Hkv][n][d] -> summ bf16 [B][Hkv][ceil(n/16)][2][d]."""
+    K, pk = _c(K, np.uint16)
+    B, Hkv, n, d = K.shape
+    nblk = (n + 15) // 16
+    out = np.empty((B, Hkv, nblk, 2, d), np.uint16)
+    _l().orc_minmax_build(pk, B, Hkv, n, d, out.ctypes.data)
+    return out
+
+
+def quest_score(summ, q, with_l1: bool = False):
+    summ, ps = _c(summ, np.uint16)
+    q, pq = _c(q, np.uint16)
+    B, Hkv, nblk, _, d = summ.shape
+    Hq = q.shape[1]
+    U = np.empty((B, Hkv, nblk), np.float64)
+    l1 = np.empty((B, Hkv, nblk), np.float64)
+    _l().orc_quest_score(ps, pq, B, Hq, Hkv, nblk, d, U.ctypes.data, l1.ctypes.data)
+    return (U, l1) if with_l1 else U
+
+
+def topk(scores: np.ndarray, k: int, sink: int = 0, local: int = 0, block: int = 1,
+         n_tokens: int = None):
+    """scores [rows..., n_units] (int32, float32 or float64) -> (idx int32
+    [rows..., max_count] padded with -1, count int32 [rows...])."""
+    kind = {np.dtype(np.int32): 0, np.dtype(np.float32): 1, np.dtype(np.float64): 2}[
+        np.asarray(scores).dtype]
+    s = np.ascontiguousarray(scores)
+    lead_shape = s.shape[:-1]
+    n_units = s.shape[-1]
+    rows = int(np.prod(lead_shape)) if lead_shape else 1
+    if n_tokens is None:
+        n_tokens = n_units * block
+    max_units = min(n_units, sink + local + k)
+    stride = max(1, max_units * block)
+    idx = np.full((rows, stride), -1, np.int32)
+    count = np.empty(rows, np.int32)
+    _l().orc_topk(s.ctypes.data, kind, rows, n_units, k, sink, local, block, n_tokens,
+                  idx.ctypes.data, stride, count.ctypes.data)
+    return idx.reshape(lead_shape + (stride,)), count.reshape(lead_shape)
+
+
+def gather_attend(q, K, V, idx, count, scale: float):
+    """-> (o float64 [B][Hq][d], lse float64 [B][Hq])."""
+    q, pq = _c(q, np.uint16)
+    K, pk = _c(K, np.uint16)
+    V, pv = _c(V, np.uint16)
+    idx, pi = _c(idx, np.int32)
+    count, pc = _c(count, np.int32)
+    B, Hq, d = q.shape
+    Hkv, n = K.shape[1], K.shape[2]
+    stride = idx.shape[-1]
+    out = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    _l().orc_gather_attend(pq, pk, pv, B, Hq, Hkv, n, d, pi, stride, pc, float(scale),
+                           out.ctypes.data, lse.ctypes.data)
+    return out, lse
+
+
+def prefix_copy(src_planes, src_scales, plan_, dst_planes, dst_scales):
+    """Copy the planned prefixes (and the active channels' scales) into dst in place."""
+    src_planes, pp = _c(src_planes, np.uint32)
+    src_scales, ps = _c(src_scales, np.uint16)
+    plan_, ppl = _c(plan_, np.uint8)
+    assert dst_planes.flags["C_CONTIGUOUS"] and dst_scales.flags["C_CONTIGUOUS"]
+    B, Hkv, d, _, nw = src_planes.shape
+    _l().orc_prefix_copy(pp, ps, ppl, B, Hkv, nw * 32, d, dst_planes.ctypes.data,
+                         dst_scales.ctypes.data)

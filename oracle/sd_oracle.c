@@ -1,0 +1,558 @@
+/*
+ * CPU ORACLE for the sparse-decode hot path (SCORE -> TOPK -> GATHER-ATT).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the CUDA library computes.  Only the tests, the smoke check
+ * and the benchmark's CPU-baseline leg may load it.  It shares no code, header,
+ * table or helper with the CUDA library; each side was written from the pages.
+ *
+ * Arithmetic: double unless the method fixes fp32 (signature chains, water-filling
+ * gains, quantiser division), built with -ffp-contract=off so that no FMA is
+ * formed behind our back.  OpenMP runs independent (sequence, KV head) units in
+ * parallel; no result depends on the thread count.
+ *
+ * Sources (page title, section/equation):
+ *   [HA]  HashAttention: Semantic Sparsity for Faster Inference
+ *         (2.1 inputs/outputs and the three stages; 2.2 eq. phi(x), SCORE, H;
+ *          2.2 worked example; 2.5 page size 1; 3.1 fixed 128+128 positions)
+ *   [FA]  Fathom: Per-Query Read Depth for Sparse Decoding over Offloaded KV Caches
+ *         (paragraph "store as bit planes per channel"; paragraph "per-query
+ *          reverse water-filling"; paragraph "host planes are channel-contiguous")
+ *   [OK]  OasisKV: Scaling In-Decode KV Cache Beyond HBM with Lookahead Sparse
+ *         Prefetching (prerequisites: "sparse attention (Quest-style block
+ *         summaries)"; core method; method details: 129 blocks incl. 1 local)
+ *
+ * Readings of points the pages leave open are marked READING below.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------------ */
+/* number formats                                                                  */
+/* ------------------------------------------------------------------------------ */
+
+/* bf16 -> float: the bf16 pattern is the top half of the float pattern. */
+static float bf16_to_f32(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static uint32_t f32_bits(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return u;
+}
+
+/* IEEE binary32 -> binary16, round to nearest, ties to even (hand-written). */
+uint16_t orc_f32_to_f16(float f) {
+  uint32_t x = f32_bits(f);
+  uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+  uint32_t ax = x & 0x7FFFFFFFu;
+  if (ax >= 0x7F800000u) return sign | (ax > 0x7F800000u ? 0x7E00u : 0x7C00u);
+  int e = (int)(ax >> 23) - 127;         /* unbiased exponent */
+  uint32_t mant = ax & 0x7FFFFFu;
+  if (e >= -14) {                         /* normal binary16 range (or overflow) */
+    if (e > 15) return sign | 0x7C00u;
+    uint32_t v = ((uint32_t)(e + 15) << 10) | (mant >> 13);
+    uint32_t rem = mant & 0x1FFFu;
+    if (rem > 0x1000u || (rem == 0x1000u && (v & 1u))) v += 1; /* may carry to inf */
+    return sign | (uint16_t)v;
+  }
+  /* subnormal binary16: value = m * 2^(e-23) with m the 24-bit significand,
+     counted in units of 2^-24 it is m * 2^(e+1); shift right by -(e+1). */
+  if (ax == 0) return sign;
+  uint32_t m = mant | 0x800000u;
+  int shift = -(e + 1);
+  if (shift > 25) return sign;
+  uint32_t q = m >> shift;
+  uint32_t rem = m & ((1u << shift) - 1u);
+  uint32_t half = 1u << (shift - 1);
+  if (rem > half || (rem == half && (q & 1u))) q += 1;
+  return sign | (uint16_t)q;
+}
+
+/* binary16 -> binary32 (exact). */
+float orc_f16_to_f32(uint16_t h) {
+  uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+  uint32_t e = (h >> 10) & 0x1Fu, m = h & 0x3FFu;
+  uint32_t u;
+  if (e == 0x1F) u = sign | 0x7F800000u | (m << 13);
+  else if (e != 0) u = sign | ((e + 112u) << 23) | (m << 13);
+  else if (m == 0) u = sign;
+  else { /* subnormal: m * 2^-24 */
+    float f = (float)m * (1.0f / 16777216.0f);
+    u = sign | f32_bits(f);
+  }
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static int popcount32(uint32_t x) {
+  int c = 0;
+  while (x) { x &= x - 1u; ++c; }
+  return c;
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S1  signatures  [HA 2.2, eq. phi(x) = ReLU(sign(F(x)))]                         */
+/* ------------------------------------------------------------------------------ */
+/*
+ * One 32-bit code per input row.  F is either one fp32 projection W1[32][d]
+ * (+ b1) or a two-layer MLP: hidden u = max(0, W1[u].x + b1[u]) (hidden units),
+ * output o = W2[o].hidden + b2[o].  Bit o of the packed word is 1 iff F_o > 0
+ * (ReLU(sign(0)) = 0, so +-0 give 0).
+ * Each dot product is the canonical fp32 chain acc = fmaf(w_j, x_j, acc) for
+ * j = 0..len-1 from acc = +0, then acc = acc + bias (fmaf is correctly rounded,
+ * so any correct implementation of this chain gives the same bits).
+ * READING: the pages give no MLP activation or bias; ReLU hidden units and zero
+ * biases in the synthetic encoders.
+ */
+static float fp32_chain(const float* w, const float* x, int len, float bias) {
+  float acc = 0.0f;
+  for (int j = 0; j < len; ++j) acc = fmaf(w[j], x[j], acc);
+  return acc + bias;
+}
+
+int orc_sig_encode(const uint16_t* x_bf16, int64_t rows, int d, const float* W1,
+                   const float* b1, int hidden, const float* W2, const float* b2,
+                   uint32_t* out) {
+  if (d < 1 || d > 512 || hidden < 0 || hidden > 1024) return -1;
+#pragma omp parallel for schedule(dynamic, 256)
+  for (int64_t r = 0; r < rows; ++r) {
+    float x[512], hbuf[1024];
+    for (int j = 0; j < d; ++j) x[j] = bf16_to_f32(x_bf16[r * d + j]);
+    uint32_t word = 0;
+    if (hidden == 0) {
+      for (int o = 0; o < 32; ++o)
+        if (fp32_chain(W1 + (int64_t)o * d, x, d, b1 ? b1[o] : 0.0f) > 0.0f) word |= 1u << o;
+    } else {
+      for (int u = 0; u < hidden; ++u) {
+        float a = fp32_chain(W1 + (int64_t)u * d, x, d, b1 ? b1[u] : 0.0f);
+        hbuf[u] = a > 0.0f ? a : 0.0f;
+      }
+      for (int o = 0; o < 32; ++o)
+        if (fp32_chain(W2 + (int64_t)o * hidden, hbuf, hidden, b2 ? b2[o] : 0.0f) > 0.0f)
+          word |= 1u << o;
+    }
+    out[r] = word;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S5a  Hamming score  [HA 2.2, SCORE = -H(phi_kv(k), phi_q(q)), H = popcount(XOR)] */
+/* ------------------------------------------------------------------------------ */
+/*
+ * score[b][h][i] = - sum over the query heads g of KV head h of
+ *                  popcount(sig[b][h][i] XOR qsig[b][g]).
+ * READING: one selection per KV head; the group's per-head scores are summed.
+ */
+void orc_hamming_score(const uint32_t* sig, int64_t B, int Hq, int Hkv, int64_t n,
+                       const uint32_t* qsig, int32_t* score) {
+  int G = Hq / Hkv;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      const uint32_t* s = sig + (b * Hkv + h) * n;
+      int32_t* out = score + (b * Hkv + h) * n;
+      for (int64_t i = 0; i < n; ++i) {
+        int acc = 0;
+        for (int g = 0; g < G; ++g) acc += popcount32(s[i] ^ qsig[b * Hq + h * G + g]);
+        out[i] = -acc;
+      }
+    }
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S2  bit-plane index  [FA "store as bit planes per channel"]                     */
+/* ------------------------------------------------------------------------------ */
+/*
+ * Per (sequence, KV head, channel j, 64-token block c):
+ *   s = f16_rn(absmax / 7) in fp32 arithmetic, replaced by 1 when it is 0;
+ *   code_i = clamp(rint(k_ij / s) + 8, 0, 15)  (fp32 IEEE divide, ties-to-even);
+ *   plane p (0 = MSB) holds bit (3 - p) of the code.
+ * Layout: planes uint32 [B][Hkv][d][4][n/32] (token i is bit i%32 of word i/32),
+ *         scales f16   [B][Hkv][d][n/64].
+ * READING: the pages fix a 4-bit uniform code with an fp16 scale per channel per
+ * 64-token block; absmax/7 with offset 8 is the symmetric [-8, 7] reading.
+ */
+int orc_plane_build(const uint16_t* K, int64_t B, int Hkv, int64_t n, int d,
+                    uint32_t* planes, uint16_t* scales) {
+  if (n % 64) return -1;
+  int64_t nw = n / 32, nb = n / 64;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      const uint16_t* Kh = K + (b * Hkv + h) * n * d;
+      for (int j = 0; j < d; ++j) {
+        uint32_t* pl = planes + (((b * Hkv + h) * d + j) * 4) * nw;
+        memset(pl, 0, sizeof(uint32_t) * 4 * nw);
+        for (int64_t c = 0; c < nb; ++c) {
+          float amax = 0.0f;
+          for (int t = 0; t < 64; ++t) {
+            float v = fabsf(bf16_to_f32(Kh[(c * 64 + t) * d + j]));
+            if (v > amax) amax = v;
+          }
+          uint16_t s16 = orc_f32_to_f16(amax / 7.0f);
+          if ((s16 & 0x7FFFu) == 0) s16 = 0x3C00u; /* scale 0 -> 1 */
+          scales[((b * Hkv + h) * d + j) * nb + c] = s16;
+          float s = orc_f16_to_f32(s16);
+          for (int t = 0; t < 64; ++t) {
+            int64_t i = c * 64 + t;
+            float r = rintf(bf16_to_f32(Kh[i * d + j]) / s);
+            int code = r <= -8.0f ? 0 : (r >= 7.0f ? 15 : (int)r + 8);
+            for (int p = 0; p < 4; ++p)
+              if ((code >> (3 - p)) & 1) pl[p * nw + i / 32] |= 1u << (i % 32);
+          }
+        }
+      }
+    }
+  return 0;
+}
+
+/* t-bit reconstruction from the first t planes (prefix = code >> (4-t) << (4-t)).
+ * READING: bin midpoint of [-8s, 8s) split into 2^t bins, i.e.
+ *   khat_t = s * (prefix + 2^(3-t) - 8) for t < 4 (0 when t = 0),
+ *   khat_4 = s * (code - 8). */
+double orc_reconstruct(int prefix, int t, double s) {
+  double h = t < 4 ? (double)(1 << (3 - t)) : 0.0;
+  return s * ((double)prefix + h - 8.0);
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S4  read plan  [FA "per-query reverse water-filling"]                           */
+/* ------------------------------------------------------------------------------ */
+/*
+ * mode 0 WATERFILL(budget): gain w_j = fl32(fl32(sum_g q_gj^2) * sigma2_j) (sum
+ *   over the GQA group in ascending g).  Starting from b = 0, repeat budget times:
+ *   give one more bit to the channel with the largest w_j * 4^-b_j among b_j < 4
+ *   (lowest j on ties).  Every b_j = 4 once budget >= 4d.
+ * mode 1 FIXED(r): the r channels with the largest sigma2_j (lowest j on ties)
+ *   get 4 bits, the others 0.
+ * mode 2 FULL: every channel gets 4 bits.
+ * One plan per (sequence, KV head): the query heads of a group share it.
+ * READING: "average budget B" is sum_j b_j = B bits per token per KV head.
+ */
+int orc_plan(const uint16_t* q, const float* sigma2, int64_t B, int Hq, int Hkv, int d,
+             int mode, int budget, uint8_t* plan) {
+  int G = Hq / Hkv;
+  if (budget < 0 || mode < 0 || mode > 2 || d < 1 || d > 512) return -1;
+  if (mode == 1 && budget > d) return -1;
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      uint8_t* pb = plan + (b * Hkv + h) * d;
+      const float* s2 = sigma2 + (int64_t)h * d;
+      if (mode == 2) { memset(pb, 4, d); continue; }
+      memset(pb, 0, d);
+      if (mode == 1) {
+        for (int r = 0; r < budget; ++r) {
+          int best = -1;
+          for (int j = 0; j < d; ++j)
+            if (pb[j] == 0 && (best < 0 || s2[j] > s2[best])) best = j;
+          pb[best] = 4;
+        }
+        continue;
+      }
+      float w[512];
+      for (int j = 0; j < d; ++j) {
+        float acc = 0.0f;
+        for (int g = 0; g < G; ++g) {
+          float x = bf16_to_f32(q[(b * Hq + h * G + g) * d + j]);
+          float sq = x * x;
+          acc = acc + sq;
+        }
+        w[j] = acc * s2[j];
+      }
+      int steps = budget < 4 * d ? budget : 4 * d;
+      for (int st = 0; st < steps; ++st) {
+        int best = -1;
+        float bestg = 0.0f;
+        for (int j = 0; j < d; ++j) {
+          if (pb[j] >= 4) continue;
+          float gj = ldexpf(w[j], -2 * pb[j]);
+          if (best < 0 || gj > bestg) { best = j; bestg = gj; }
+        }
+        pb[best] += 1;
+      }
+    }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S5b  bit-plane prefix score  [FA "store as bit planes", "water-filling"]        */
+/* ------------------------------------------------------------------------------ */
+/*
+ * score[b][h][i] = sum_g sum_j q_gj * khat_ij(t = plan_j), khat from the first
+ * plan_j planes of channel j and the block's scale (orc_reconstruct), in double.
+ */
+void orc_plane_score(const uint32_t* planes, const uint16_t* scales, const uint8_t* plan,
+                     const uint16_t* q, int64_t B, int Hq, int Hkv, int64_t n, int d,
+                     double* score) {
+  int G = Hq / Hkv;
+  int64_t nw = n / 32, nb = n / 64;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      const uint8_t* pb = plan + (b * Hkv + h) * d;
+      for (int64_t i = 0; i < n; ++i) {
+        double acc = 0.0;
+        for (int g = 0; g < G; ++g) {
+          const uint16_t* qg = q + (b * Hq + h * G + g) * d;
+          for (int j = 0; j < d; ++j) {
+            int t = pb[j];
+            const uint32_t* pl = planes + (((b * Hkv + h) * d + j) * 4) * nw;
+            int prefix = 0;
+            for (int p = 0; p < t; ++p)
+              if ((pl[p * nw + i / 32] >> (i % 32)) & 1u) prefix |= 1 << (3 - p);
+            double s = (double)orc_f16_to_f32(scales[((b * Hkv + h) * d + j) * nb + i / 64]);
+            acc += (double)bf16_to_f32(qg[j]) * orc_reconstruct(prefix, t, s);
+          }
+        }
+        score[(b * Hkv + h) * n + i] = acc;
+      }
+    }
+}
+
+/* Sum of |terms| of each plane score, the scale of its rounding tolerance. */
+void orc_plane_score_l1(const uint32_t* planes, const uint16_t* scales, const uint8_t* plan,
+                        const uint16_t* q, int64_t B, int Hq, int Hkv, int64_t n, int d,
+                        double* l1) {
+  int G = Hq / Hkv;
+  int64_t nw = n / 32, nb = n / 64;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      const uint8_t* pb = plan + (b * Hkv + h) * d;
+      for (int64_t i = 0; i < n; ++i) {
+        double acc = 0.0;
+        for (int g = 0; g < G; ++g)
+          for (int j = 0; j < d; ++j) {
+            int t = pb[j];
+            const uint32_t* pl = planes + (((b * Hkv + h) * d + j) * 4) * nw;
+            int prefix = 0;
+            for (int p = 0; p < t; ++p)
+              if ((pl[p * nw + i / 32] >> (i % 32)) & 1u) prefix |= 1 << (3 - p);
+            double s = (double)orc_f16_to_f32(scales[((b * Hkv + h) * d + j) * nb + i / 64]);
+            acc += fabs((double)bf16_to_f32(q[(b * Hq + h * G + g) * d + j]) *
+                        orc_reconstruct(prefix, t, s));
+          }
+        l1[(b * Hkv + h) * n + i] = acc;
+      }
+    }
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S3 / S5c  block min/max summaries and block bound  [OK "Quest-style summaries"] */
+/* ------------------------------------------------------------------------------ */
+/*
+ * summ[b][h][c][0][j] = min, summ[b][h][c][1][j] = max of k_ij over the tokens of
+ * 16-token block c (the last block may be short).  Values are the exact bf16
+ * keys.  READING: -0.0 orders below +0.0 so that min/max are unique bit patterns.
+ */
+static int bf16_less(uint16_t a, uint16_t b) { /* total order, -0 < +0 */
+  uint32_t ka = (a & 0x8000u) ? (uint32_t)(~a & 0xFFFFu) : (uint32_t)(a | 0x8000u);
+  uint32_t kb = (b & 0x8000u) ? (uint32_t)(~b & 0xFFFFu) : (uint32_t)(b | 0x8000u);
+  return ka < kb;
+}
+
+void orc_minmax_build(const uint16_t* K, int64_t B, int Hkv, int64_t n, int d,
+                      uint16_t* summ) {
+  int64_t nblk = (n + 15) / 16;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      const uint16_t* Kh = K + (b * Hkv + h) * n * d;
+      for (int64_t c = 0; c < nblk; ++c) {
+        uint16_t* out = summ + ((b * Hkv + h) * nblk + c) * 2 * d;
+        int64_t t1 = (c + 1) * 16 < n ? (c + 1) * 16 : n;
+        for (int j = 0; j < d; ++j) {
+          uint16_t mn = Kh[c * 16 * d + j], mx = mn;
+          for (int64_t t = c * 16 + 1; t < t1; ++t) {
+            uint16_t v = Kh[t * d + j];
+            if (bf16_less(v, mn)) mn = v;
+            if (bf16_less(mx, v)) mx = v;
+          }
+          out[j] = mn;
+          out[d + j] = mx;
+        }
+      }
+    }
+}
+
+/* U[b][h][c] = sum_g sum_j max(q_gj * min_cj, q_gj * max_cj), in double. */
+void orc_quest_score(const uint16_t* summ, const uint16_t* q, int64_t B, int Hq, int Hkv,
+                     int64_t nblk, int d, double* U, double* l1) {
+  int G = Hq / Hkv;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h)
+      for (int64_t c = 0; c < nblk; ++c) {
+        const uint16_t* s = summ + ((b * Hkv + h) * nblk + c) * 2 * d;
+        double acc = 0.0, mass = 0.0;
+        for (int g = 0; g < G; ++g)
+          for (int j = 0; j < d; ++j) {
+            double qq = bf16_to_f32(q[(b * Hq + h * G + g) * d + j]);
+            double lo = qq * bf16_to_f32(s[j]), hi = qq * bf16_to_f32(s[d + j]);
+            double m = lo > hi ? lo : hi;
+            acc += m;
+            mass += fabs(m);
+          }
+        U[(b * Hkv + h) * nblk + c] = acc;
+        if (l1) l1[(b * Hkv + h) * nblk + c] = mass;
+      }
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S6  exact top-k with forced windows  [HA 2.1 TOPK; HA 3.1; OK method details]  */
+/* ------------------------------------------------------------------------------ */
+/*
+ * Per row of n_units scores (units are tokens when block == 1, blocks of `block`
+ * tokens otherwise):
+ *   forced units: [0, sink) and [n_units - local, n_units);
+ *   candidates:   the units in between; if there are at most k of them all are
+ *                 taken, else the first k in the order (score desc, unit asc);
+ *   output:       the union in ascending order, each unit expanded to its tokens
+ *                 [u*block, min((u+1)*block, n_tokens)).
+ * count[row] = number of tokens written; -1 if the row holds a NaN score.
+ * READING: the retrieval budget k is counted apart from the forced windows.
+ */
+typedef struct { double s; int64_t u; } cand_t;
+
+static int cand_cmp(const void* a, const void* b) {
+  const cand_t* x = (const cand_t*)a;
+  const cand_t* y = (const cand_t*)b;
+  if (x->s > y->s) return -1;
+  if (x->s < y->s) return 1;
+  return (x->u > y->u) - (x->u < y->u);
+}
+
+static int i64_cmp(const void* a, const void* b) {
+  int64_t x = *(const int64_t*)a, y = *(const int64_t*)b;
+  return (x > y) - (x < y);
+}
+
+/* kind: 0 = int32 scores, 1 = float32 scores, 2 = double scores */
+void orc_topk(const void* scores, int kind, int64_t rows, int64_t n_units, int k, int sink,
+              int local, int block, int64_t n_tokens, int32_t* idx, int64_t idx_stride,
+              int32_t* count) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < rows; ++r) {
+    cand_t* c = (cand_t*)malloc(sizeof(cand_t) * (size_t)(n_units > 0 ? n_units : 1));
+    int64_t* sel = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n_units > 0 ? n_units : 1));
+    int bad = 0;
+    int64_t lead = sink < n_units ? sink : n_units;
+    int64_t tail = n_units - local > lead ? n_units - local : lead;
+    int64_t nc = 0, ns = 0;
+    for (int64_t u = lead; u < tail; ++u) {
+      double s;
+      if (kind == 0) s = ((const int32_t*)scores)[r * n_units + u];
+      else if (kind == 1) s = ((const float*)scores)[r * n_units + u];
+      else s = ((const double*)scores)[r * n_units + u];
+      if (s != s) bad = 1;
+      c[nc].s = s;
+      c[nc].u = u;
+      ++nc;
+    }
+    if (bad) {
+      count[r] = -1;
+      free(c);
+      free(sel);
+      continue;
+    }
+    for (int64_t u = 0; u < lead; ++u) sel[ns++] = u;
+    if (nc <= k) {
+      for (int64_t i = 0; i < nc; ++i) sel[ns++] = c[i].u;
+    } else {
+      qsort(c, (size_t)nc, sizeof(cand_t), cand_cmp);
+      for (int i = 0; i < k; ++i) sel[ns++] = c[i].u;
+    }
+    for (int64_t u = tail; u < n_units; ++u) sel[ns++] = u;
+    qsort(sel, (size_t)ns, sizeof(int64_t), i64_cmp);
+    int64_t w = 0;
+    for (int64_t i = 0; i < ns; ++i) {
+      int64_t t0 = sel[i] * block, t1 = (sel[i] + 1) * block;
+      if (t1 > n_tokens) t1 = n_tokens;
+      for (int64_t t = t0; t < t1; ++t) idx[r * idx_stride + w++] = (int32_t)t;
+    }
+    count[r] = (int32_t)w;
+    free(c);
+    free(sel);
+  }
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S7  gather-attend  [HA 2.1: o_hat over the selected set, corrected denominator; */
+/*                     HA 2.5: rows read in place, page size 1]                   */
+/* ------------------------------------------------------------------------------ */
+/*
+ * For query head g of sequence b (KV head h = g / G), over I = idx[b][h][0..count):
+ *   z_i = scale * <q_g, k_i>,  o = sum_i e^{z_i - m} v_i / sum_i e^{z_i - m},
+ *   lse = m + log(sum_i e^{z_i - m}),  m = max_i z_i;
+ * an empty set gives o = 0 and lse = -inf.  Double throughout.
+ */
+void orc_gather_attend(const uint16_t* q, const uint16_t* K, const uint16_t* V, int64_t B,
+                       int Hq, int Hkv, int64_t n, int d, const int32_t* idx,
+                       int64_t idx_stride, const int32_t* count, double scale, double* out,
+                       double* lse) {
+  int G = Hq / Hkv;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int64_t b = 0; b < B; ++b)
+    for (int g = 0; g < Hq; ++g) {
+      int h = g / G;
+      const int32_t* I = idx + (b * Hkv + h) * idx_stride;
+      int64_t c = count[b * Hkv + h];
+      const uint16_t* qg = q + (b * Hq + g) * d;
+      double* o = out + (b * Hq + g) * d;
+      for (int j = 0; j < d; ++j) o[j] = 0.0;
+      if (c <= 0) { lse[b * Hq + g] = -INFINITY; continue; }
+      double* z = (double*)malloc(sizeof(double) * (size_t)c);
+      double m = -INFINITY;
+      for (int64_t i = 0; i < c; ++i) {
+        const uint16_t* kr = K + ((b * Hkv + h) * n + I[i]) * d;
+        double acc = 0.0;
+        for (int j = 0; j < d; ++j) acc += (double)bf16_to_f32(qg[j]) * bf16_to_f32(kr[j]);
+        z[i] = scale * acc;
+        if (z[i] > m) m = z[i];
+      }
+      double l = 0.0;
+      for (int64_t i = 0; i < c; ++i) {
+        double a = exp(z[i] - m);
+        l += a;
+        const uint16_t* vr = V + ((b * Hkv + h) * n + I[i]) * d;
+        for (int j = 0; j < d; ++j) o[j] += a * bf16_to_f32(vr[j]);
+      }
+      for (int j = 0; j < d; ++j) o[j] /= l;
+      lse[b * Hq + g] = m + log(l);
+      free(z);
+    }
+}
+
+/* ------------------------------------------------------------------------------ */
+/* S8  planned-prefix copy  [FA "host planes are channel-contiguous; one gather    */
+/*                           copies the active channels' prefixes"]                */
+/* ------------------------------------------------------------------------------ */
+/*
+ * For every (sequence, KV head, channel j) with plan_j > 0: the first plan_j
+ * planes of channel j (plan_j * n/32 words) and channel j's scales are copied
+ * from src to dst; everything else in dst is left as it was.
+ */
+void orc_prefix_copy(const uint32_t* src_planes, const uint16_t* src_scales,
+                     const uint8_t* plan, int64_t B, int Hkv, int64_t n, int d,
+                     uint32_t* dst_planes, uint16_t* dst_scales) {
+  int64_t nw = n / 32, nb = n / 64;
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h)
+      for (int j = 0; j < d; ++j) {
+        int t = plan[(b * Hkv + h) * d + j];
+        if (t == 0) continue;
+        int64_t base = ((b * Hkv + h) * d + j);
+        memcpy(dst_planes + base * 4 * nw, src_planes + base * 4 * nw,
+               sizeof(uint32_t) * (size_t)(t * nw));
+        memcpy(dst_scales + base * nb, src_scales + base * nb, sizeof(uint16_t) * (size_t)nb);
+      }
+}

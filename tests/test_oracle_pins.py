@@ -1,0 +1,463 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test ties an oracle function to something other than itself: a worked
+example printed on a page, a closed form or bound, a textbook or library routine
+(sort, numpy float16 rounding, dense softmax), or brute force on tiny inputs.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bits_to_word(s: str) -> int:
+    return sum(1 << i for i, ch in enumerate(s) if ch == "1")
+
+
+# ---------------------------------------------------------------------------------
+# Hamming score: HashAttention 2.2 worked example (T1)
+# ---------------------------------------------------------------------------------
+def test_hamming_worked_example():
+    g = json.load(open(os.path.join(GOLD, "hamming_worked_example.json")))
+    q = bits_to_word(g["query"])
+    keys = [bits_to_word(k) for k in g["keys"]]
+    for k, x in zip(keys, g["xor"]):
+        assert (k ^ q) == bits_to_word(x)
+    sig = np.array(keys, np.uint32).reshape(1, 1, -1)
+    qsig = np.array([[q]], np.uint32)
+    score = oracle.hamming_score(sig, qsig)
+    assert (-score[0, 0]).tolist() == g["hamming"]
+    idx, cnt = oracle.topk(score.reshape(1, -1), k=g["budget"])
+    assert cnt[0] == g["budget"]
+    assert idx[0, : cnt[0]].tolist() == g["selected"]
+
+
+def test_hamming_matches_library_popcount_and_group_sum():
+    rng_sig = (synth.uniform(7, 1, 3 * 2 * 300) * 2**32).astype(np.uint64).astype(np.uint32)
+    rng_q = (synth.uniform(7, 2, 3 * 8) * 2**32).astype(np.uint64).astype(np.uint32)
+    sig = rng_sig.reshape(3, 2, 300)
+    qsig = rng_q.reshape(3, 8)  # G = 4
+    s = oracle.hamming_score(sig, qsig)
+    for b in range(3):
+        for h in range(2):
+            x = sig[b, h][:, None] ^ qsig[b, h * 4:(h + 1) * 4][None, :]
+            ref = -np.bitwise_count(x).astype(np.int64).sum(axis=1)
+            assert np.array_equal(s[b, h], ref)
+    assert s.min() >= -32 * 4 and s.max() <= 0
+
+
+# ---------------------------------------------------------------------------------
+# Signatures: bits agree with a float64 evaluation wherever the margin exceeds the
+# fp32 chain's error bound (HashAttention 2.2, eq. phi)
+# ---------------------------------------------------------------------------------
+@pytest.mark.parametrize("hidden", [0, 16])
+def test_signature_bits_match_exact_sign(hidden):
+    d = 128
+    x = synth.normal_bf16(11, 1, 400, d)
+    xf = synth.bf16_to_f64(x)
+    if hidden == 0:
+        W1 = synth.normal_f32(11, 2, (32, d), 1.0)
+        b1 = synth.normal_f32(11, 3, (32,), 0.5)
+        sig = oracle.sig_encode(x, W1, b1)
+        pre = xf @ W1.astype(np.float64).T + b1
+        mass = np.abs(xf) @ np.abs(W1.astype(np.float64)).T + np.abs(b1)
+        rel = d * 2.0**-23
+    else:
+        W1 = synth.normal_f32(11, 4, (hidden, d), 1 / math.sqrt(d))
+        b1 = synth.normal_f32(11, 5, (hidden,), 0.1)
+        W2 = synth.normal_f32(11, 6, (32, hidden), 1 / math.sqrt(hidden))
+        b2 = synth.normal_f32(11, 7, (32,), 0.1)
+        sig = oracle.sig_encode(x, W1, b1, W2, b2)
+        hid = np.maximum(xf @ W1.astype(np.float64).T + b1, 0.0)
+        pre = hid @ W2.astype(np.float64).T + b2
+        mass = (np.abs(xf) @ np.abs(W1.astype(np.float64)).T + np.abs(b1)) @ \
+            np.abs(W2.astype(np.float64)).T + np.abs(b2)
+        rel = (d + hidden) * 2.0**-22
+    bits = ((sig[:, None] >> np.arange(32, dtype=np.uint32)[None, :]) & 1).astype(bool)
+    sure = np.abs(pre) > rel * mass
+    assert sure.mean() > 0.99
+    assert np.array_equal(bits[sure], (pre > 0)[sure])
+
+
+def test_signature_zero_gives_zero_bit():
+    d = 128
+    x = np.zeros((2, d), np.uint16)
+    x[1] = 0x8000  # -0.0
+    W1 = synth.normal_f32(3, 1, (32, d), 1.0)
+    sig = oracle.sig_encode(x, W1, np.zeros(32, np.float32))
+    assert sig.tolist() == [0, 0]
+
+
+# ---------------------------------------------------------------------------------
+# Bit planes (Fathom "bit planes per channel")
+# ---------------------------------------------------------------------------------
+def test_f16_rounding_matches_numpy():
+    u = synth.uniform(5, 1, 200000)
+    # magnitudes from 2^-30 to 2^17 so subnormal, normal and overflow paths are hit
+    x = (np.exp2(u * 47 - 30) * np.where(synth.uniform(5, 2, 200000) < 0.5, -1, 1)).astype(np.float32)
+    extra = np.array([0.0, -0.0, 65504.0, 65519.99, 65520.0, 2**-24, 2**-25, 1.5 * 2**-25,
+                      2**-14, 6.1e-5, 1.0 + 2**-11, 1.0 + 3 * 2**-11], np.float32)
+    x = np.concatenate([x, extra])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f32_to_f16(float(v)) for v in x], np.uint16)
+    assert np.array_equal(got, ref)
+    back = np.array([oracle.f16_to_f32(int(h)) for h in ref[:2000]], np.float32)
+    assert np.array_equal(back, ref[:2000].view(np.float16).astype(np.float32))
+
+
+def _decode_codes(planes):
+    return ((planes[..., 0, :, None] >> np.arange(32, dtype=np.uint32)) & 1) * 8 + \
+        ((planes[..., 1, :, None] >> np.arange(32, dtype=np.uint32)) & 1) * 4 + \
+        ((planes[..., 2, :, None] >> np.arange(32, dtype=np.uint32)) & 1) * 2 + \
+        ((planes[..., 3, :, None] >> np.arange(32, dtype=np.uint32)) & 1)
+
+
+def test_plane_codes_are_nearest_grid_points_all_bf16():
+    """Brute force over every finite bf16 value in range against one scale: the
+    code is the nearest point of the grid s*(c-8), ties to the even rint."""
+    all_bf16 = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        vals = synth.bf16_to_f64(all_bf16)
+    finite = np.isfinite(vals)
+    # one 64-token block per channel: put the block absmax 7*s at token 0
+    s_target = 0.375  # exact in f16; absmax = 2.625 is exact in bf16
+    amax = np.float64(7 * s_target)
+    sel = all_bf16[finite & (np.abs(vals) <= amax)]
+    n_tok = 64 * ((len(sel) + 62) // 63)
+    d = 1
+    K = np.zeros((1, 1, n_tok, d), np.uint16)
+    flat = K.reshape(-1)
+    # each block: token 0 holds +absmax, the other 63 hold values under test
+    vals_iter = list(sel)
+    pos = 0
+    for blk in range(n_tok // 64):
+        flat[blk * 64] = synth.to_bf16(np.array([amax]))[0]
+        for t in range(1, 64):
+            flat[blk * 64 + t] = vals_iter[pos] if pos < len(vals_iter) else 0
+            pos += 1
+    planes, scales = oracle.plane_build(K)
+    assert np.all(scales == np.float16(s_target).view(np.uint16))
+    codes = _decode_codes(planes)[0, 0, 0].reshape(-1)
+    k = synth.bf16_to_f64(flat)
+    grid = s_target * (np.arange(16) - 8.0)
+    dist = np.abs(k[:, None] - grid[None, :])
+    best = dist.min(axis=1)
+    assert np.all(dist[np.arange(len(k)), codes] == best)
+    tie = (dist == best[:, None]).sum(axis=1) > 1
+    # ties only between two neighbours: rint picks the even (k/s) integer, i.e. even code
+    assert np.all(codes[tie] % 2 == 0)
+
+
+def test_plane_scale_rule_and_prefix_invariant():
+    cfg = synth.config(0, n=256)
+    inp = synth.make_inputs(cfg, with_v=False)
+    planes, scales = oracle.plane_build(inp.K)
+    K = synth.bf16_to_f64(inp.K)[0, 0]  # [n][d]
+    n, d = K.shape
+    # scale = f16_rn(absmax/7) computed in fp32, via numpy's own float16 rounding
+    amax = np.abs(K.reshape(n // 64, 64, d)).max(axis=1).astype(np.float32)  # [nb][d]
+    s_ref = (amax / np.float32(7)).astype(np.float16)
+    s_ref[s_ref == 0] = 1
+    assert np.array_equal(scales[0, 0].T, s_ref.view(np.uint16))
+    codes = _decode_codes(planes)[0, 0].reshape(d, n)
+    s = np.repeat(s_ref.astype(np.float64), 64, axis=0).T  # [d][n]
+    # 4-bit dequantisation error bound |k - s(c-8)| <= s/2 (inside the clamp range)
+    assert np.all(np.abs(K.T - s * (codes - 8.0)) <= s / 2 * (1 + 1e-12))
+    # prefix invariant: the first t planes are the t-bit code, and the midpoint
+    # reconstruction of [-8s, 8s) cut into 2^t bins stays within half a t-bit step
+    for t in range(5):
+        pref = (codes >> (4 - t)) << (4 - t)
+        for c, p, sv in [(int(codes[j, i]), int(pref[j, i]), float(s[j, i]))
+                         for j in (0, 5, 77) for i in (0, 63, 64, 200)]:
+            khat = oracle.reconstruct(p, t, sv)
+            khat4 = oracle.reconstruct(c, 4, sv)
+            assert khat4 == sv * (c - 8)
+            if t == 0:
+                assert khat == 0.0
+            if t < 4:
+                width = sv * 2 ** (4 - t)
+                assert khat == pytest.approx(-8 * sv + (p >> (4 - t)) * width + width / 2)
+                assert abs(khat - khat4) <= sv * 2 ** (3 - t)
+
+
+def test_plane_zero_block_scale_is_one():
+    K = np.zeros((1, 1, 64, 128), np.uint16)
+    planes, scales = oracle.plane_build(K)
+    assert np.all(scales == 0x3C00)
+    codes = _decode_codes(planes)[0, 0]
+    assert np.all(codes == 8)
+
+
+# ---------------------------------------------------------------------------------
+# Water-filling plan (Fathom "per-query reverse water-filling")
+# ---------------------------------------------------------------------------------
+def _brute_plan_objective(w, B):
+    best = -1.0
+    for alloc in itertools.product(range(5), repeat=len(w)):
+        if sum(alloc) != B:
+            continue
+        val = sum(wj * (1 - 4.0 ** -bj) for wj, bj in zip(w, alloc))
+        best = max(best, val)
+    return best
+
+
+def _gains(q, sigma2, h, G):
+    qf = synth.bf16_to_f64(q).astype(np.float32)
+    acc = np.zeros(q.shape[-1], np.float32)
+    for g in range(G):
+        acc = acc + qf[0, h * G + g] * qf[0, h * G + g]
+    return (acc * sigma2[h]).astype(np.float64)
+
+
+@pytest.mark.parametrize("d,G", [(4, 1), (5, 2), (6, 4)])
+def test_waterfill_is_optimal_by_brute_force(d, G):
+    for trial in range(3):
+        q = synth.normal_bf16(100 + trial, 1, G, d).reshape(1, G, d)
+        sigma2 = (synth.uniform(100 + trial, 2, d) * 4 + 0.01).astype(np.float32).reshape(1, d)
+        w = _gains(q, sigma2, 0, G)
+        prev = np.zeros(d, np.int64)
+        for B in range(0, 4 * d + 3):
+            p = oracle.plan(q, sigma2, 1, oracle.PLAN_WATERFILL, B)[0, 0].astype(np.int64)
+            assert p.sum() == min(B, 4 * d) and p.max() <= 4
+            assert np.all(p >= prev)  # nested in B
+            prev = p
+            if B <= 4 * d:
+                val = float(np.sum(w * (1 - 4.0 ** -p)))
+                assert val == pytest.approx(_brute_plan_objective(w, B), rel=1e-12, abs=1e-300)
+
+
+def test_waterfill_ties_go_to_lower_channel():
+    d = 4
+    q = np.zeros((1, 1, d), np.uint16)
+    q[0, 0] = synth.to_bf16(np.array([1.0, 1.0, 2.0, 0.0]))
+    sigma2 = np.array([[1.0, 1.0, 0.25, 3.0]], np.float32)  # gains 1, 1, 1, 0
+    got = [oracle.plan(q, sigma2, 1, oracle.PLAN_WATERFILL, B)[0, 0].tolist() for B in range(8)]
+    assert got[1] == [1, 0, 0, 0]
+    assert got[3] == [1, 1, 1, 0]
+    assert got[4] == [2, 1, 1, 0]
+    assert got[7] == [3, 2, 2, 0]
+    # an exact tie between a second bit of channel 0 (w/4) and a first bit of channel 1
+    q[0, 0] = synth.to_bf16(np.array([2.0, 1.0, 0.0, 0.0]))
+    sigma2 = np.array([[1.0, 1.0, 1.0, 1.0]], np.float32)  # gains 4, 1, 0, 0
+    assert oracle.plan(q, sigma2, 1, oracle.PLAN_WATERFILL, 2)[0, 0].tolist() == [2, 0, 0, 0]
+    assert oracle.plan(q, sigma2, 1, oracle.PLAN_WATERFILL, 3)[0, 0].tolist() == [2, 1, 0, 0]
+    # zero gains: bits go to the lowest channels, 4 at a time
+    q[:] = 0
+    assert oracle.plan(q, sigma2, 1, oracle.PLAN_WATERFILL, 6)[0, 0].tolist() == [4, 2, 0, 0]
+
+
+def test_fixed_and_full_plans():
+    cfg = synth.config(4, n=64, B=2)
+    inp = synth.make_inputs(cfg, with_v=False)
+    p = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, oracle.PLAN_FIXED, 32)
+    for h in range(cfg.Hkv):
+        top = np.argsort(-inp.sigma2[h].astype(np.float64), kind="stable")[:32]
+        ref = np.zeros(cfg.d, np.uint8)
+        ref[top] = 4
+        assert np.array_equal(p[0, h], ref) and np.array_equal(p[1, h], ref)
+    f = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, oracle.PLAN_FULL, 0)
+    assert np.all(f == 4)
+
+
+# ---------------------------------------------------------------------------------
+# Bit-plane score
+# ---------------------------------------------------------------------------------
+def test_plane_score_full_plan_is_dequantised_dot_and_bounded():
+    cfg = synth.config(0, n=512)
+    inp = synth.make_inputs(cfg, with_v=False)
+    planes, scales = oracle.plane_build(inp.K)
+    full = oracle.plan(inp.q, inp.sigma2, 1, oracle.PLAN_FULL, 0)
+    sc = oracle.plane_score(planes, scales, full, inp.q)[0, 0]
+    qf = synth.bf16_to_f64(inp.q)[0]          # [G][d]
+    Kf = synth.bf16_to_f64(inp.K)[0, 0]       # [n][d]
+    sv = np.repeat(scales[0, 0].view(np.float16).astype(np.float64), 64, axis=1).T  # [n][d]
+    exact = Kf @ qf.sum(axis=0)
+    bound = (sv / 2) @ np.abs(qf).sum(axis=0)
+    assert np.all(np.abs(sc - exact) <= bound * (1 + 1e-9))
+    zero = oracle.plan(inp.q, inp.sigma2, 1, oracle.PLAN_WATERFILL, 0)
+    assert np.all(oracle.plane_score(planes, scales, zero, inp.q) == 0.0)
+
+
+def test_plane_score_single_channel_prefix():
+    cfg = synth.config(0, n=128)
+    inp = synth.make_inputs(cfg, with_v=False)
+    planes, scales = oracle.plane_build(inp.K)
+    qf = synth.bf16_to_f64(inp.q)[0]
+    codes = _decode_codes(planes)[0, 0].reshape(cfg.d, cfg.n)
+    for j, t in [(3, 1), (9, 2), (40, 3), (127, 4)]:
+        p = np.zeros((1, 1, cfg.d), np.uint8)
+        p[0, 0, j] = t
+        sc = oracle.plane_score(planes, scales, p, inp.q)[0, 0]
+        sv = np.repeat(scales[0, 0, j].view(np.float16).astype(np.float64), 64)
+        pref = (codes[j] >> (4 - t)) << (4 - t)
+        width = sv * 2.0 ** (4 - t)
+        if t < 4:   # midpoint of bin (pref >> (4-t)) of [-8s, 8s) cut into 2^t bins
+            mid = -8 * sv + (pref >> (4 - t)) * width + width / 2
+        else:       # the 4-bit grid value
+            mid = sv * (codes[j] - 8.0)
+        assert np.allclose(sc, qf[:, j].sum() * mid, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------
+# Quest bound (OasisKV prerequisites: Quest-style block summaries)
+# ---------------------------------------------------------------------------------
+def test_minmax_matches_library_reductions():
+    cfg = synth.config(0, n=200)  # ragged tail block
+    inp = synth.make_inputs(cfg, with_v=False)
+    summ = oracle.minmax_build(inp.K)
+    Kf = synth.bf16_to_f64(inp.K)[0, 0]
+    for c in range(summ.shape[2]):
+        blk = Kf[c * 16: min((c + 1) * 16, cfg.n)]
+        assert np.array_equal(synth.bf16_to_f64(summ[0, 0, c, 0]), blk.min(axis=0))
+        assert np.array_equal(synth.bf16_to_f64(summ[0, 0, c, 1]), blk.max(axis=0))
+
+
+def test_minmax_signed_zero_rule():
+    K = np.zeros((1, 1, 16, 128), np.uint16)
+    K[0, 0, 3, 0] = 0x8000  # one -0.0 among +0.0
+    summ = oracle.minmax_build(K)
+    assert summ[0, 0, 0, 0, 0] == 0x8000 and summ[0, 0, 0, 1, 0] == 0x0000
+
+
+def test_quest_bound_dominates_every_in_block_dot():
+    cfg = synth.config(3, B=2, Hkv=2, Hq=8, n=16 * 40 + 5, planted=3)
+    inp = synth.make_inputs(cfg, with_v=False)
+    summ = oracle.minmax_build(inp.K)
+    U = oracle.quest_score(summ, inp.q)
+    qf = synth.bf16_to_f64(inp.q)
+    Kf = synth.bf16_to_f64(inp.K)
+    G = cfg.G
+    for b in range(cfg.B):
+        for h in range(cfg.Hkv):
+            qs = qf[b, h * G:(h + 1) * G].sum(axis=0)
+            dots = Kf[b, h] @ qs
+            for c in range(U.shape[2]):
+                blk = dots[c * 16: min((c + 1) * 16, cfg.n)]
+                assert np.all(blk <= U[b, h, c] + 1e-9 * (1 + abs(U[b, h, c])))
+    # tightness: a block of identical keys gives exactly their dot
+    K1 = np.repeat(inp.K[:1, :1, :1], 16, axis=2)
+    U1 = oracle.quest_score(oracle.minmax_build(K1), inp.q[:1, :G])
+    assert U1[0, 0, 0] == pytest.approx(float(Kf[0, 0, 0] @ qf[0, :G].sum(axis=0)), rel=1e-12)
+
+
+# ---------------------------------------------------------------------------------
+# Top-k with forced windows (HashAttention 2.1 TOPK, 3.1; OasisKV method details)
+# ---------------------------------------------------------------------------------
+def _brute_topk(s, k, sink, local, block, n_tokens):
+    n = len(s)
+    lead = min(sink, n)
+    tail = max(n - local, lead)
+    cand = list(range(lead, tail))
+    if len(cand) > k:
+        cand = sorted(cand, key=lambda u: (-float(s[u]), u))[:k]
+    units = sorted(list(range(lead)) + cand + list(range(tail, n)))
+    out = []
+    for u in units:
+        out.extend(range(u * block, min((u + 1) * block, n_tokens)))
+    return out
+
+
+@pytest.mark.parametrize("kind", ["f32", "f32ties", "int", "const"])
+def test_topk_brute_force_small(kind):
+    for n in [1, 5, 17, 40, 130]:
+        s = synth.make_scores(31 + n, 4, n, kind, levels=5)
+        for k, sink, local in [(1, 0, 0), (3, 2, 2), (8, 0, 4), (50, 4, 4), (200, 1, 1)]:
+            idx, cnt = oracle.topk(s, k, sink, local)
+            for r in range(4):
+                ref = _brute_topk(s[r], k, sink, local, 1, n)
+                assert cnt[r] == len(ref)
+                assert idx[r, :cnt[r]].tolist() == ref
+
+
+def test_topk_block_mode_and_ragged_tail():
+    s = synth.make_scores(5, 3, 21, "f32").astype(np.float64)
+    n_tokens = 16 * 20 + 7
+    idx, cnt = oracle.topk(s, k=4, sink=0, local=1, block=16, n_tokens=n_tokens)
+    for r in range(3):
+        ref = _brute_topk(s[r], 4, 0, 1, 16, n_tokens)
+        assert cnt[r] == 4 * 16 + 7 and idx[r, :cnt[r]].tolist() == ref
+
+
+def test_topk_all_ties_take_lowest_indices_and_signed_zero():
+    s = np.zeros((2, 100), np.float32)
+    s[1, ::2] = np.float32(-0.0)
+    idx, cnt = oracle.topk(s, k=10)
+    assert idx[0, :10].tolist() == list(range(10)) and idx[1, :10].tolist() == list(range(10))
+
+
+def test_topk_nan_row_reports_error():
+    s = np.zeros((2, 50), np.float32)
+    s[1, 7] = np.nan
+    _, cnt = oracle.topk(s, k=5)
+    assert cnt[0] == 5 and cnt[1] == -1
+
+
+def test_budget_arithmetic_hashattention_and_oasiskv():
+    g = json.load(open(os.path.join(GOLD, "byte_model.json")))
+    n, m, fixed = g["n"], g["m"], g["fixed"]
+    assert n // g["sparsity"] == m
+    s = synth.make_scores(9, 1, n, "f32")
+    _, cnt = oracle.topk(s, k=m, sink=fixed // 2, local=fixed // 2)
+    assert cnt[0] == g["total"]
+    assert round(100.0 * cnt[0] / n, 2) == g["read_fraction_pct"]
+    nblk = 1024
+    sb = synth.make_scores(10, 1, nblk, "f32")
+    _, cb = oracle.topk(sb, k=g["blocks"] - 1, local=1, block=g["block_tokens"],
+                        n_tokens=nblk * 16)
+    assert cb[0] == g["tokens_per_head"]
+
+
+# ---------------------------------------------------------------------------------
+# Gather-attend (HashAttention 2.1, corrected o_hat)
+# ---------------------------------------------------------------------------------
+def test_gather_attend_full_set_equals_dense_softmax():
+    cfg = synth.config(0, n=300, Hq=8, Hkv=2)
+    inp = synth.make_inputs(cfg)
+    B, Hkv, n = cfg.B, cfg.Hkv, cfg.n
+    idx = np.tile(np.arange(n, dtype=np.int32), (B, Hkv, 1))
+    cnt = np.full((B, Hkv), n, np.int32)
+    scale = 1 / math.sqrt(cfg.d)
+    o, lse = oracle.gather_attend(inp.q, inp.K, inp.V, idx, cnt, scale)
+    qf, Kf, Vf = (synth.bf16_to_f64(x) for x in (inp.q, inp.K, inp.V))
+    for g in range(cfg.Hq):
+        h = g // cfg.G
+        z = Kf[0, h] @ qf[0, g] * scale
+        a = np.exp(z - z.max())
+        ref = (a / a.sum()) @ Vf[0, h]
+        assert np.allclose(o[0, g], ref, rtol=1e-12, atol=1e-12)
+        assert lse[0, g] == pytest.approx(z.max() + math.log(a.sum()), rel=1e-12)
+
+
+def test_gather_attend_single_row_and_empty():
+    cfg = synth.config(0, n=64)
+    inp = synth.make_inputs(cfg)
+    idx = np.array([[[17, -1]]], np.int32)
+    o, lse = oracle.gather_attend(inp.q, inp.K, inp.V, idx, np.array([[1]], np.int32), 0.1)
+    v = synth.bf16_to_f64(inp.V)[0, 0, 17]
+    assert np.array_equal(o[0, 0], v) and np.array_equal(o[0, 3], v)
+    o, lse = oracle.gather_attend(inp.q, inp.K, inp.V, idx, np.array([[0]], np.int32), 0.1)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+def test_prefix_copy_copies_exactly_the_planned_prefix():
+    cfg = synth.config(0, n=128)
+    inp = synth.make_inputs(cfg, with_v=False)
+    planes, scales = oracle.plane_build(inp.K)
+    p = oracle.plan(inp.q, inp.sigma2, 1, oracle.PLAN_WATERFILL, 56)
+    dp = np.zeros_like(planes)
+    ds = np.zeros_like(scales)
+    oracle.prefix_copy(planes, scales, p, dp, ds)
+    for j in range(cfg.d):
+        t = int(p[0, 0, j])
+        assert np.array_equal(dp[0, 0, j, :t], planes[0, 0, j, :t])
+        assert np.all(dp[0, 0, j, t:] == 0)
+        assert np.array_equal(ds[0, 0, j], scales[0, 0, j] if t else np.zeros_like(ds[0, 0, j]))
