@@ -1,0 +1,221 @@
+/*
+ * sd.h -- C ABI of libsd, the per-decode-step hot path of top-k sparse attention
+ * (SCORE -> TOPK -> GATHER-ATT) for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (page title, section / equation):
+ *   HashAttention: Semantic Sparsity for Faster Inference
+ *     2.1 "inputs, outputs and the three stages" (z_i, softmax, the corrected
+ *         sparse output o_hat over a selected set);
+ *     2.2 "binary codes and GPU scoring" (phi(x) = ReLU(sign(F(x))), key and
+ *         query encoders, SCORE = -Hamming, popcount of XOR, worked example);
+ *     2.5 "why token-level sparsity runs efficiently" (page size 1: rows read
+ *         in place by index; cost T = T_qmap + T_scan + T_topk + T_att);
+ *     3.1 "protocol" (first 128 and last 128 tokens kept; budget counted apart).
+ *   Fathom: Per-Query Read Depth for Sparse Decoding over Offloaded KV Caches
+ *     paragraph "store as bit planes per channel" (4-bit codes, fp16 scale per
+ *         channel per 64-token block, 4 channel-major planes, t-plane prefix is
+ *         a t-bit quantiser);
+ *     paragraph "per-query reverse water-filling" (gain q_j^2 sigma_j^2, each bit
+ *         divides the remaining error by ~4, 0..4 bits per channel under a budget,
+ *         one plan per KV head);
+ *     paragraph "host planes are channel-contiguous" (one gather copies the
+ *         active channels' prefixes into HBM before the scan).
+ *   OasisKV: Scaling In-Decode KV Cache Beyond HBM with Lookahead Sparse Prefetching
+ *     prerequisites, "sparse attention (Quest-style block summaries)" (per-block
+ *         per-channel min/max, block importance, top-K blocks);
+ *     method details (129 blocks of 16 tokens incl. 1 local block per KV head;
+ *         UVA gather kernel from pinned CPU memory on side streams).
+ *
+ * Conventions (every entry point):
+ *   - Ownership: the caller allocates every buffer.  libsd never allocates;
+ *     scratch needs are reported by *_workspace_size().
+ *   - Device pointers unless stated; 16-byte aligned.  bf16 data travel as raw
+ *     bit patterns (uint16).  All layouts are row-major, last index fastest.
+ *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t passed as void*,
+ *     NULL = legacy default stream) and the call returns without synchronising.
+ *   - Errors: the return value is SD_OK or a negative SD_ERR_*; nothing is
+ *     enqueued when an argument check fails.  sd_last_error() returns a
+ *     thread-local message for the last failing call on this thread.
+ *   - Shapes: sd_shape.d must be 128; hq % hkv == 0 and G = hq / hkv must be
+ *     1, 2, 4 or 8.  n is the number of valid tokens per sequence, n_cap
+ *     (>= n; 0 means n) the allocated tokens per (sequence, KV head): the
+ *     stride of K, V and every per-token index buffer.
+ */
+#ifndef SD_H_
+#define SD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SD_OK 0
+#define SD_ERR_INVALID_ARG (-1) /* null pointer, bad size, bad enum, bad alignment */
+#define SD_ERR_UNSUPPORTED (-2) /* a valid request outside this build (d != 128, ...) */
+#define SD_ERR_CUDA (-3)        /* a CUDA call or launch failed; see sd_last_error() */
+#define SD_ERR_TIMEOUT (-4)     /* a bounded wait ran out */
+#define SD_ERR_WORKSPACE (-5)   /* workspace too small */
+
+typedef struct sd_shape {
+  int32_t batch; /* B: sequences in the decode batch */
+  int32_t hq;    /* query heads per sequence */
+  int32_t hkv;   /* KV heads per sequence */
+  int32_t d;     /* head dimension (128) */
+  int64_t n;     /* valid cached tokens per sequence */
+  int64_t n_cap; /* allocated tokens per (sequence, KV head); 0 = n */
+} sd_shape;
+
+/* Signature encoder F (fp32, device).  hidden = 0: one projection W1 [32][d]
+ * (+ b1 [32]).  hidden in {32, 64, 128}: W1 [hidden][d], b1 [hidden], ReLU,
+ * W2 [32][hidden], b2 [32].  Null biases are zero. */
+typedef struct sd_encoder {
+  const float* W1;
+  const float* b1;
+  int32_t hidden;
+  const float* W2;
+  const float* b2;
+} sd_encoder;
+
+typedef enum { SD_IDX_SIG = 0, SD_IDX_PLANES = 1, SD_IDX_MINMAX = 2 } sd_index_kind;
+typedef enum { SD_PLAN_WATERFILL = 0, SD_PLAN_FIXED = 1, SD_PLAN_FULL = 2 } sd_plan_mode;
+typedef enum { SD_SCORE_I32 = 0, SD_SCORE_F32 = 1 } sd_score_type;
+
+/*
+ * sd_build_index -- key-side index, built on the KV-write path.
+ *   K: bf16 [B][hkv][n_cap][d] (tokens [0, n) are read).
+ *   SD_IDX_SIG (HashAttention 2.2, eq. phi): out0 = uint32 [B][hkv][n_cap]
+ *     signatures; bit o = 1 iff F_o(k) > 0.  Every dot product is the fp32 chain
+ *     acc = fma(w_j, x_j, acc), j ascending from +0, then acc + bias, so the
+ *     bits are reproducible on any IEEE machine.  enc is required; out1 unused.
+ *   SD_IDX_PLANES (Fathom, bit planes): requires n % 64 == 0 and n_cap % 64 == 0.
+ *     out0 = uint32 planes [B][hkv][d][4][n_cap/32] (token i = bit i%32 of word
+ *     i/32; plane 0 = MSB), out1 = fp16 scales [B][hkv][d][n_cap/64] with
+ *     s = f16_rn(absmax/7) (1 if that is 0) and code = clamp(rint(k/s)+8, 0, 15).
+ *   SD_IDX_MINMAX (OasisKV, Quest-style summaries): out0 = bf16 summaries
+ *     [B][hkv][ceil(n_cap/16)][2][d]: per 16-token block the channel min row then
+ *     the max row (exact keys; -0.0 orders below +0.0; the last block may be
+ *     short).  out1 unused.
+ */
+int sd_build_index(int kind, const sd_shape* shape, const void* K, const sd_encoder* enc,
+                   void* out0, void* out1, void* stream);
+
+/*
+ * sd_encode_query -- query signatures phi_q(q) (HashAttention 2.2), the
+ * "query map" stage of the per-step cost.  q: bf16 [B][hq][d]; qsig: uint32
+ * [B][hq].  Same fp32 chain as SD_IDX_SIG.
+ */
+int sd_encode_query(const sd_shape* shape, const void* q, const sd_encoder* enc,
+                    uint32_t* qsig, void* stream);
+
+/*
+ * sd_plan -- per-query read plan (Fathom, reverse water-filling), one per
+ * (sequence, KV head), shared by the group's query heads.
+ *   q: bf16 [B][hq][d]; sigma2: fp32 [hkv][d] calibration variances;
+ *   plan: uint8 [B][hkv][d], bits per channel in 0..4.
+ *   SD_PLAN_WATERFILL, budget B in [0, 4d]: gain w_j = (sum_g q_gj^2) * sigma2_j
+ *     in fp32 (g ascending, no fused multiply-add); the result equals giving B
+ *     bits one at a time to the channel with the largest w_j * 4^-b_j among
+ *     b_j < 4, lowest j on ties; sum_j plan_j = min(B, 4d).
+ *   SD_PLAN_FIXED, budget r in [0, d]: the r channels with the largest sigma2_j
+ *     (lowest j on ties) get 4 bits, the others 0.
+ *   SD_PLAN_FULL: every channel gets 4 bits (budget ignored).
+ */
+int sd_plan(const sd_shape* shape, const void* q, const float* sigma2, int mode, int budget,
+            uint8_t* plan, void* stream);
+
+/*
+ * sd_score -- SCORE of every cached key (or block) of every (sequence, KV head).
+ * Output rows are contiguous: scores [B*hkv][n] (or [B*hkv][ceil(n/16)]).
+ *   SD_IDX_SIG (HashAttention 2.2): index0 = signatures, q_or_qsig = uint32
+ *     qsig [B][hq]; scores int32 = -sum_{g in group} popcount(sig XOR qsig_g).
+ *   SD_IDX_PLANES (Fathom): index0 = planes, index1 = scales, plan required,
+ *     q_or_qsig = bf16 q [B][hq][d]; scores fp32 = sum_g sum_j q_gj *
+ *     khat_ij(plan_j) with khat_t = s*(prefix_t + 2^(3-t) - 8) for t < 4 (0 for
+ *     t = 0) and s*(code - 8) for t = 4, prefix_t = the code with its low 4-t
+ *     bits cleared.  Only the first plan_j planes of channel j are read.
+ *   SD_IDX_MINMAX (OasisKV/Quest bound): index0 = summaries, q_or_qsig = bf16
+ *     q; scores fp32 [B*hkv][ceil(n/16)] = sum_g sum_j max(q_gj min_j, q_gj max_j).
+ */
+int sd_score(int kind, const sd_shape* shape, const void* index0, const void* index1,
+             const void* q_or_qsig, const uint8_t* plan, void* scores, void* stream);
+
+/*
+ * sd_topk -- exact top-k per row with forced windows (HashAttention 2.1 TOPK and
+ * 3.1 fixed positions; OasisKV method details: top-K blocks + 1 local block).
+ *   scores: rows x n_units, SD_SCORE_I32 or SD_SCORE_F32, contiguous rows.
+ *   Units are tokens (sel.block == 1) or blocks of sel.block tokens.
+ *   Forced units: [0, sink) and [n_units - local, n_units).  Of the units in
+ *   between, all are taken if there are at most k, else the first k in the
+ *   order (score descending, unit ascending); -0.0 equals +0.0.
+ *   Output: idx int32 [rows][idx_stride] holds the union in ascending order,
+ *   each unit expanded to tokens [u*block, min((u+1)*block, n_tokens));
+ *   count int32 [rows] = tokens written (-1 if the row holds a NaN score).
+ *   Entries past count are not written.  idx_stride must be at least
+ *   min(n_units, sink + local + k) * block.  Limits: 1 <= k <= 4096.
+ *   Workspace: sd_topk_workspace_size() bytes (device), contents need not be
+ *   initialised; calls sharing a workspace must not overlap.
+ */
+typedef struct sd_select {
+  int32_t k;
+  int32_t sink;
+  int32_t local;
+  int32_t block;
+} sd_select;
+
+size_t sd_topk_workspace_size(int64_t rows, int64_t n_units, const sd_select* sel);
+int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
+            int64_t n_tokens, const sd_select* sel, int32_t* idx, int64_t idx_stride,
+            int32_t* count, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * sd_gather_attend -- GATHER-ATT (HashAttention 2.1, corrected o_hat; 2.5 page
+ * size 1): for query head g of sequence b, KV head h = g / G, over the rows
+ * I = idx[b*hkv + h][0..count): z_i = scale * <q_g, k_i>,
+ * out = sum_i e^{z_i - m} v_i / sum_i e^{z_i - m}, lse = m + log(sum e^{z_i - m}).
+ *   q bf16 [B][hq][d]; K, V bf16 [B][hkv][n_cap][d]; idx int32 [B*hkv][idx_stride]
+ *   (token indices < n, any order); count int32 [B*hkv] (<= max_count);
+ *   out fp32 [B][hq][d]; lse fp32 [B][hq] or NULL.  An empty set gives out = 0,
+ *   lse = -inf.  The set is split across CTAs and merged by an online-softmax
+ *   combine.  Workspace: sd_gather_attend_workspace_size() bytes (device).
+ */
+size_t sd_gather_attend_workspace_size(const sd_shape* shape, int64_t max_count);
+int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const void* V,
+                     const int32_t* idx, int64_t idx_stride, const int32_t* count,
+                     int64_t max_count, float scale, float* out, float* lse, void* workspace,
+                     size_t ws_bytes, void* stream);
+
+/*
+ * sd_offload_gather -- copy each (sequence, KV head, channel j)'s planned
+ * prefix (the first plan_j planes, contiguous in the channel-major layout)
+ * and channel j's scales from pinned host memory into HBM, with device loads
+ * over the host link (Fathom, host planes; OasisKV, UVA gather on a side stream).
+ *   host_planes / host_scales: pinned host memory (cudaHostAlloc or registered)
+ *   in the SD_IDX_PLANES layout; plan: device uint8 [B][hkv][d];
+ *   dev_planes / dev_scales: device buffers in the same layout.  Channels with
+ *   plan_j = 0 and planes past the prefix are not written.  Typically enqueued
+ *   on a side stream; the caller orders the scan after it with an event.
+ */
+int sd_offload_gather(const sd_shape* shape, const uint32_t* host_planes,
+                      const uint16_t* host_scales, const uint8_t* plan, uint32_t* dev_planes,
+                      uint16_t* dev_scales, void* stream);
+
+/*
+ * sd_event_wait -- host-side bounded wait on a cudaEvent_t (passed as void*):
+ * polls until the event completes or timeout_us microseconds pass
+ * (SD_ERR_TIMEOUT).  Lets a caller bound its wait for an offload copy.
+ */
+int sd_event_wait(void* event, int64_t timeout_us);
+
+/* Thread-local message of the last failing call on this thread ("" if none). */
+const char* sd_last_error(void);
+
+/* ABI version (major * 100 + minor). */
+int sd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SD_H_ */

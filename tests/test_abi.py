@@ -1,0 +1,113 @@
+"""The C-ABI library loads and exports every entry point include/sd.h declares;
+argument checks fail with the documented codes before anything reaches CUDA.
+No GPU needed: every call here is rejected by the host-side checks."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sd():
+    from top_sparse_decode_gb300 import build as b
+    b.build()
+    import top_sparse_decode_gb300 as sdmod
+    sdmod.lib()
+    return sdmod
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "sd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[\w\s\*]+?\b(sd_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_path():
+    names = header_functions()
+    for must in ["sd_build_index", "sd_encode_query", "sd_plan", "sd_score", "sd_topk",
+                 "sd_gather_attend", "sd_offload_gather", "sd_last_error"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(sd):
+    lib = sd.lib()
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    from top_sparse_decode_gb300 import _abi
+    assert sorted(_abi.SIGNATURES) == header_functions()
+    for name in header_functions():
+        assert callable(getattr(sd, name)), name
+    assert sd.sd_version() == 100
+
+
+def test_shape_checks(sd):
+    bad = [sd.make_shape(1, 4, 1, 4096, d=64),      # d != 128
+           sd.make_shape(1, 12, 4, 4096),           # G = 3
+           sd.make_shape(1, 4, 3, 4096),            # hq % hkv
+           sd.make_shape(0, 4, 1, 4096),            # batch 0
+           sd.make_shape(1, 4, 1, 4096, n_cap=100)]  # n_cap < n
+    codes = [sd.SD_ERR_UNSUPPORTED, sd.SD_ERR_UNSUPPORTED, sd.SD_ERR_INVALID_ARG,
+             sd.SD_ERR_INVALID_ARG, sd.SD_ERR_INVALID_ARG]
+    lib = sd.lib()
+    for shp, code in zip(bad, codes):
+        rc = lib.sd_plan(ctypes.byref(shp), 16, 16, 0, 56, 16, None)
+        assert rc == code, (shp.d, shp.hq, shp.hkv, rc)
+        assert sd.sd_last_error()
+
+
+def test_argument_checks(sd):
+    lib = sd.lib()
+    shp = sd.make_shape(1, 4, 1, 4096)
+    P = 1 << 20  # a fake, aligned address; never dereferenced
+    # planes need n % 64 == 0
+    shp_r = sd.make_shape(1, 4, 1, 4000)
+    assert lib.sd_build_index(1, ctypes.byref(shp_r), P, None, P, P, None) == sd.SD_ERR_UNSUPPORTED
+    # misaligned K
+    assert lib.sd_build_index(2, ctypes.byref(shp), P + 2, None, P, None, None) == sd.SD_ERR_INVALID_ARG
+    # unknown kind
+    assert lib.sd_build_index(7, ctypes.byref(shp), P, None, P, None, None) == sd.SD_ERR_INVALID_ARG
+    # signatures need an encoder; hidden 100 unsupported
+    assert lib.sd_build_index(0, ctypes.byref(shp), P, None, P, None, None) == sd.SD_ERR_INVALID_ARG
+    enc = sd._abi.SdEncoder(P, None, 100, P, None)
+    assert lib.sd_build_index(0, ctypes.byref(shp), P, ctypes.byref(enc), P, None, None) == \
+        sd.SD_ERR_UNSUPPORTED
+    # plan budgets
+    assert lib.sd_plan(ctypes.byref(shp), P, P, 0, 513, P, None) == sd.SD_ERR_INVALID_ARG
+    assert lib.sd_plan(ctypes.byref(shp), P, P, 1, 129, P, None) == sd.SD_ERR_INVALID_ARG
+    assert lib.sd_plan(ctypes.byref(shp), P, P, 5, 1, P, None) == sd.SD_ERR_INVALID_ARG
+    # top-k limits and strides
+    sel = sd.make_select(5000)
+    assert lib.sd_topk(1, P, 1, 100, 100, ctypes.byref(sel), P, 5000, P, None, 0, None) == \
+        sd.SD_ERR_UNSUPPORTED
+    sel = sd.make_select(10, 2, 2)
+    assert lib.sd_topk(1, P, 1, 100, 100, ctypes.byref(sel), P, 13, P, None, 0, None) == \
+        sd.SD_ERR_INVALID_ARG
+    assert lib.sd_topk(3, P, 1, 100, 100, ctypes.byref(sel), P, 14, P, None, 0, None) == \
+        sd.SD_ERR_INVALID_ARG
+    # long rows need a workspace
+    need = sd.sd_topk_workspace_size(2, 100000, sel)
+    assert need > 0 and sd.sd_topk_workspace_size(2, 1000, sel) == 0
+    assert lib.sd_topk(1, P, 2, 100000, 100000, ctypes.byref(sel), P, 14, P, P, need - 1, None) \
+        == sd.SD_ERR_WORKSPACE
+    # block mode: n_tokens must match n_units * block
+    selb = sd.make_select(4, 0, 1, 16)
+    assert lib.sd_topk(1, P, 1, 10, 200, ctypes.byref(selb), P, 80, P, None, 0, None) == \
+        sd.SD_ERR_INVALID_ARG
+    # gather-attend workspace
+    wsz = sd.sd_gather_attend_workspace_size(shp, 200)
+    assert wsz > 0
+    assert lib.sd_gather_attend(ctypes.byref(shp), P, P, P, P, 200, P, 200, 0.1, P, None, P,
+                                wsz - 1, None) == sd.SD_ERR_WORKSPACE
+    assert lib.sd_gather_attend(ctypes.byref(shp), P, P, P, P, 100, P, 200, 0.1, P, None, P,
+                                wsz, None) == sd.SD_ERR_INVALID_ARG
+    assert lib.sd_event_wait(None, 10) == sd.SD_ERR_INVALID_ARG
+
+
+def test_python_binding_raises_with_message(sd):
+    shp = sd.make_shape(1, 4, 1, 4096, d=64)
+    with pytest.raises(sd.SdError) as ei:
+        sd.sd_plan(shp, 16, 16, 0, 56, 16, stream=0)
+    assert ei.value.code == sd.SD_ERR_UNSUPPORTED and "d = 64" in str(ei.value)

@@ -1,0 +1,161 @@
+"""top_sparse_decode_gb300 -- Python binding of libsd (include/sd.h).
+
+Every function has the name of the C entry point it calls and only marshals
+arguments: tensors become device pointers, the stream defaults to torch's
+current stream.  Every step of the path runs in libsd's CUDA kernels; there is
+no Python or CPU fallback, and a missing libsd.so raises at first use.
+
+bf16 tensors may be passed as torch.bfloat16 or as their int16/uint16 bit
+patterns.  Layouts are those of include/sd.h (row-major, contiguous).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import (SD_ERR_CUDA, SD_ERR_INVALID_ARG, SD_ERR_TIMEOUT, SD_ERR_UNSUPPORTED,  # noqa: F401
+                   SD_ERR_WORKSPACE, SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_OK,
+                   SD_PLAN_FIXED, SD_PLAN_FULL, SD_PLAN_WATERFILL, SD_SCORE_F32, SD_SCORE_I32,
+                   SdEncoder, SdSelect, SdShape)
+
+__all__ = [
+    "SdError", "make_shape", "make_encoder", "make_select", "lib",
+    "sd_build_index", "sd_encode_query", "sd_plan", "sd_score", "sd_topk_workspace_size",
+    "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend", "sd_offload_gather",
+    "sd_event_wait", "sd_last_error", "sd_version",
+]
+
+
+class SdError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def lib():
+    return _abi.load()
+
+
+def _check(rc: int, name: str) -> None:
+    if rc != SD_OK:
+        msg = (lib().sd_last_error() or b"").decode(errors="replace")
+        raise SdError(rc, f"{name}: {msg}")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("libsd takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_shape(batch: int, hq: int, hkv: int, n: int, d: int = 128, n_cap: int = 0) -> SdShape:
+    return SdShape(batch, hq, hkv, d, n, n_cap)
+
+
+class _Encoder:
+    """sd_encoder plus references that keep its weight tensors alive."""
+
+    def __init__(self, W1, b1=None, W2=None, b2=None):
+        self.tensors = (W1, b1, W2, b2)
+        hidden = 0 if W2 is None else int(W1.shape[0])
+        self.c = SdEncoder(_ptr(W1), _ptr(b1), hidden, _ptr(W2), _ptr(b2))
+
+
+def make_encoder(W1, b1=None, W2=None, b2=None) -> _Encoder:
+    """Device fp32 weights: W1 [32][d] (single projection) or W1 [hidden][d] and
+    W2 [32][hidden] (two layers)."""
+    return _Encoder(W1, b1, W2, b2)
+
+
+def make_select(k: int, sink: int = 0, local: int = 0, block: int = 1) -> SdSelect:
+    return SdSelect(k, sink, local, block)
+
+
+def sd_version() -> int:
+    return int(lib().sd_version())
+
+
+def sd_last_error() -> str:
+    return (lib().sd_last_error() or b"").decode(errors="replace")
+
+
+def sd_build_index(kind: int, shape: SdShape, K, enc: Optional[_Encoder], out0, out1=None,
+                   stream=None) -> None:
+    e = ctypes.byref(enc.c) if enc is not None else None
+    _check(lib().sd_build_index(kind, ctypes.byref(shape), _ptr(K), e, _ptr(out0), _ptr(out1),
+                                _stream(stream)), "sd_build_index")
+
+
+def sd_encode_query(shape: SdShape, q, enc: _Encoder, qsig, stream=None) -> None:
+    _check(lib().sd_encode_query(ctypes.byref(shape), _ptr(q), ctypes.byref(enc.c), _ptr(qsig),
+                                 _stream(stream)), "sd_encode_query")
+
+
+def sd_plan(shape: SdShape, q, sigma2, mode: int, budget: int, plan, stream=None) -> None:
+    _check(lib().sd_plan(ctypes.byref(shape), _ptr(q), _ptr(sigma2), mode, budget, _ptr(plan),
+                         _stream(stream)), "sd_plan")
+
+
+def sd_score(kind: int, shape: SdShape, index0, index1, q_or_qsig, plan, scores,
+             stream=None) -> None:
+    _check(lib().sd_score(kind, ctypes.byref(shape), _ptr(index0), _ptr(index1),
+                          _ptr(q_or_qsig), _ptr(plan), _ptr(scores), _stream(stream)),
+           "sd_score")
+
+
+def sd_topk_workspace_size(rows: int, n_units: int, sel: SdSelect) -> int:
+    return int(lib().sd_topk_workspace_size(rows, n_units, ctypes.byref(sel)))
+
+
+def sd_topk(score_type: int, scores, rows: int, n_units: int, n_tokens: int, sel: SdSelect,
+            idx, idx_stride: int, count, workspace=None, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().sd_topk(score_type, _ptr(scores), rows, n_units, n_tokens, ctypes.byref(sel),
+                         _ptr(idx), idx_stride, _ptr(count), _ptr(workspace), ws_bytes,
+                         _stream(stream)), "sd_topk")
+
+
+def sd_gather_attend_workspace_size(shape: SdShape, max_count: int) -> int:
+    return int(lib().sd_gather_attend_workspace_size(ctypes.byref(shape), max_count))
+
+
+def sd_gather_attend(shape: SdShape, q, K, V, idx, idx_stride: int, count, max_count: int,
+                     scale: float, out, lse=None, workspace=None, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().sd_gather_attend(ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V), _ptr(idx),
+                                  idx_stride, _ptr(count), max_count, float(scale), _ptr(out),
+                                  _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)),
+           "sd_gather_attend")
+
+
+def sd_offload_gather(shape: SdShape, host_planes, host_scales, plan, dev_planes, dev_scales,
+                      stream=None) -> None:
+    _check(lib().sd_offload_gather(ctypes.byref(shape), _ptr(host_planes), _ptr(host_scales),
+                                   _ptr(plan), _ptr(dev_planes), _ptr(dev_scales),
+                                   _stream(stream)), "sd_offload_gather")
+
+
+def sd_event_wait(event, timeout_us: int) -> None:
+    handle = event if isinstance(event, int) else event.cuda_event
+    _check(lib().sd_event_wait(handle, int(timeout_us)), "sd_event_wait")
+
+
+def default_scale(d: int = 128) -> float:
+    """1/sqrt(d), the softmax scale of z_i = <q, k_i> / sqrt(d)."""
+    return 1.0 / math.sqrt(d)

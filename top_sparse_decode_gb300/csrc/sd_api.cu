@@ -1,0 +1,265 @@
+// C-ABI entry points of libsd: argument checks, then one launcher per operation.
+// Nothing is enqueued when a check fails.
+#include <stdarg.h>
+#include <string.h>
+
+#include <chrono>
+#include <thread>
+
+#include "sd_internal.cuh"
+
+namespace sd {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+}
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return SD_OK;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Validates a shape and fills Dims.  need_n64: planes layout constraint.
+static int check_shape(const sd_shape* sh, Dims* out, bool need_n64 = false) {
+  if (!sh) return fail(SD_ERR_INVALID_ARG, "shape is NULL");
+  if (sh->batch < 1 || sh->hq < 1 || sh->hkv < 1 || sh->n < 1)
+    return fail(SD_ERR_INVALID_ARG, "shape: batch, hq, hkv and n must be positive");
+  if (sh->hq % sh->hkv)
+    return fail(SD_ERR_INVALID_ARG, "shape: hq (%d) is not a multiple of hkv (%d)", sh->hq,
+                sh->hkv);
+  int G = sh->hq / sh->hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(SD_ERR_UNSUPPORTED, "shape: group size %d (supported: 1, 2, 4, 8)", G);
+  if (sh->d != kD) return fail(SD_ERR_UNSUPPORTED, "shape: d = %d (supported: 128)", sh->d);
+  int64_t ncap = sh->n_cap ? sh->n_cap : sh->n;
+  if (ncap < sh->n) return fail(SD_ERR_INVALID_ARG, "shape: n_cap < n");
+  if (sh->n >= (int64_t)1 << 31 || ncap >= (int64_t)1 << 31)
+    return fail(SD_ERR_UNSUPPORTED, "shape: n >= 2^31");
+  if ((int64_t)sh->batch * sh->hkv > 65535)
+    return fail(SD_ERR_UNSUPPORTED, "shape: batch * hkv > 65535");
+  if (need_n64 && (sh->n % 64 || ncap % 64))
+    return fail(SD_ERR_UNSUPPORTED, "bit planes need n and n_cap to be multiples of 64");
+  *out = Dims{sh->batch, sh->hq, sh->hkv, G, sh->n, ncap};
+  return SD_OK;
+}
+
+static int check_encoder(const sd_encoder* enc) {
+  if (!enc || !enc->W1) return fail(SD_ERR_INVALID_ARG, "encoder: W1 is NULL");
+  if (enc->hidden != 0 && enc->hidden != 32 && enc->hidden != 64 && enc->hidden != 128)
+    return fail(SD_ERR_UNSUPPORTED, "encoder: hidden = %d (supported: 0, 32, 64, 128)",
+                enc->hidden);
+  if (enc->hidden && !enc->W2) return fail(SD_ERR_INVALID_ARG, "encoder: W2 is NULL");
+  return SD_OK;
+}
+
+}  // namespace sd
+
+using namespace sd;
+
+extern "C" {
+
+int sd_version(void) { return 100; }
+
+const char* sd_last_error(void) { return g_err; }
+
+int sd_build_index(int kind, const sd_shape* shape, const void* K, const sd_encoder* enc,
+                   void* out0, void* out1, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s, kind == SD_IDX_PLANES);
+  if (rc) return rc;
+  if (!K || !out0) return fail(SD_ERR_INVALID_ARG, "sd_build_index: K or out0 is NULL");
+  if (!aligned16(K) || !aligned16(out0))
+    return fail(SD_ERR_INVALID_ARG, "sd_build_index: K and out0 must be 16-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  switch (kind) {
+    case SD_IDX_SIG:
+      if ((rc = check_encoder(enc))) return rc;
+      return launch_sig_build(s, (const uint16_t*)K, *enc, (uint32_t*)out0, st);
+    case SD_IDX_PLANES:
+      if (!out1) return fail(SD_ERR_INVALID_ARG, "sd_build_index: scales (out1) is NULL");
+      return launch_plane_build(s, (const uint16_t*)K, (uint32_t*)out0, (uint16_t*)out1, st);
+    case SD_IDX_MINMAX:
+      return launch_minmax_build(s, (const uint16_t*)K, (uint16_t*)out0, st);
+    default:
+      return fail(SD_ERR_INVALID_ARG, "sd_build_index: unknown kind %d", kind);
+  }
+}
+
+int sd_encode_query(const sd_shape* shape, const void* q, const sd_encoder* enc, uint32_t* qsig,
+                    void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s);
+  if (rc) return rc;
+  if ((rc = check_encoder(enc))) return rc;
+  if (!q || !qsig) return fail(SD_ERR_INVALID_ARG, "sd_encode_query: q or qsig is NULL");
+  return launch_encode_query(s, (const uint16_t*)q, *enc, qsig, (cudaStream_t)stream);
+}
+
+int sd_plan(const sd_shape* shape, const void* q, const float* sigma2, int mode, int budget,
+            uint8_t* plan, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s);
+  if (rc) return rc;
+  if (!plan || (mode != SD_PLAN_FULL && !sigma2) || (mode == SD_PLAN_WATERFILL && !q))
+    return fail(SD_ERR_INVALID_ARG, "sd_plan: NULL input");
+  if (mode < 0 || mode > 2) return fail(SD_ERR_INVALID_ARG, "sd_plan: unknown mode %d", mode);
+  if (mode == SD_PLAN_WATERFILL && (budget < 0 || budget > 4 * kD))
+    return fail(SD_ERR_INVALID_ARG, "sd_plan: budget %d outside [0, %d]", budget, 4 * kD);
+  if (mode == SD_PLAN_FIXED && (budget < 0 || budget > kD))
+    return fail(SD_ERR_INVALID_ARG, "sd_plan: fixed width %d outside [0, %d]", budget, kD);
+  return launch_plan(s, (const uint16_t*)q, sigma2, mode, budget, plan, (cudaStream_t)stream);
+}
+
+int sd_score(int kind, const sd_shape* shape, const void* index0, const void* index1,
+             const void* q_or_qsig, const uint8_t* plan, void* scores, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s, kind == SD_IDX_PLANES);
+  if (rc) return rc;
+  if (!index0 || !q_or_qsig || !scores) return fail(SD_ERR_INVALID_ARG, "sd_score: NULL input");
+  if (!aligned16(index0) || !aligned16(scores))
+    return fail(SD_ERR_INVALID_ARG, "sd_score: index0 and scores must be 16-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  switch (kind) {
+    case SD_IDX_SIG:
+      return launch_score_hamming(s, (const uint32_t*)index0, (const uint32_t*)q_or_qsig,
+                                  (int32_t*)scores, st);
+    case SD_IDX_PLANES:
+      if (!index1 || !plan) return fail(SD_ERR_INVALID_ARG, "sd_score: scales or plan NULL");
+      return launch_score_planes(s, (const uint32_t*)index0, (const uint16_t*)index1, plan,
+                                 (const uint16_t*)q_or_qsig, (float*)scores, st);
+    case SD_IDX_MINMAX:
+      return launch_score_quest(s, (const uint16_t*)index0, (const uint16_t*)q_or_qsig,
+                                (float*)scores, st);
+    default:
+      return fail(SD_ERR_INVALID_ARG, "sd_score: unknown kind %d", kind);
+  }
+}
+
+size_t sd_topk_workspace_size(int64_t rows, int64_t n_units, const sd_select* sel) {
+  if (!sel || rows < 1 || n_units < 1) return 0;
+  return topk_workspace_bytes(rows, n_units, *sel);
+}
+
+int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
+            int64_t n_tokens, const sd_select* sel, int32_t* idx, int64_t idx_stride,
+            int32_t* count, void* workspace, size_t ws_bytes, void* stream) {
+  if (!sel || !scores || !idx || !count) return fail(SD_ERR_INVALID_ARG, "sd_topk: NULL input");
+  if (score_type != SD_SCORE_I32 && score_type != SD_SCORE_F32)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk: unknown score type %d", score_type);
+  if (rows < 1 || n_units < 1 || n_units >= ((int64_t)1 << 31) || rows >= ((int64_t)1 << 31))
+    return fail(SD_ERR_INVALID_ARG, "sd_topk: bad rows / n_units");
+  if (sel->k < 1 || sel->k > kMaxTopK)
+    return fail(SD_ERR_UNSUPPORTED, "sd_topk: k = %d outside [1, %d]", sel->k, kMaxTopK);
+  if (sel->sink < 0 || sel->local < 0 || sel->block < 1)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk: negative window or block < 1");
+  if (n_tokens < 1 || n_tokens > n_units * (int64_t)sel->block ||
+      n_tokens <= (n_units - 1) * (int64_t)sel->block)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk: n_tokens does not match n_units * block");
+  int64_t max_units = n_units < (int64_t)sel->sink + sel->local + sel->k
+                          ? n_units : (int64_t)sel->sink + sel->local + sel->k;
+  if (idx_stride < max_units * sel->block)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk: idx_stride %lld < %lld", (long long)idx_stride,
+                (long long)(max_units * sel->block));
+  if (n_units > kSmallRow && rows > 65535)
+    return fail(SD_ERR_UNSUPPORTED, "sd_topk: more than 65535 rows of over %d units", kSmallRow);
+  size_t need = topk_workspace_bytes(rows, n_units, *sel);
+  if (need && (!workspace || ws_bytes < need))
+    return fail(SD_ERR_WORKSPACE, "sd_topk: workspace %zu < %zu bytes", ws_bytes, need);
+  return launch_topk(score_type, scores, rows, n_units, n_tokens, *sel, idx, idx_stride, count,
+                     workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+size_t sd_gather_attend_workspace_size(const sd_shape* shape, int64_t max_count) {
+  Dims s;
+  if (check_shape(shape, &s) || max_count < 0) return 0;
+  return attend_workspace_bytes(s, max_count);
+}
+
+int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const void* V,
+                     const int32_t* idx, int64_t idx_stride, const int32_t* count,
+                     int64_t max_count, float scale, float* out, float* lse, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s);
+  if (rc) return rc;
+  if (!q || !K || !V || !idx || !count || !out)
+    return fail(SD_ERR_INVALID_ARG, "sd_gather_attend: NULL input");
+  if (!aligned16(K) || !aligned16(V))
+    return fail(SD_ERR_INVALID_ARG, "sd_gather_attend: K and V must be 16-byte aligned");
+  if (max_count < 0 || idx_stride < max_count)
+    return fail(SD_ERR_INVALID_ARG, "sd_gather_attend: bad max_count / idx_stride");
+  size_t need = attend_workspace_bytes(s, max_count);
+  if (need && (!workspace || ws_bytes < need))
+    return fail(SD_ERR_WORKSPACE, "sd_gather_attend: workspace %zu < %zu bytes", ws_bytes,
+                need);
+  return launch_gather_attend(s, (const uint16_t*)q, (const uint16_t*)K, (const uint16_t*)V, idx,
+                              idx_stride, count, max_count, scale, out, lse, workspace, ws_bytes,
+                              (cudaStream_t)stream);
+}
+
+int sd_offload_gather(const sd_shape* shape, const uint32_t* host_planes,
+                      const uint16_t* host_scales, const uint8_t* plan, uint32_t* dev_planes,
+                      uint16_t* dev_scales, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s, true);
+  if (rc) return rc;
+  if (!host_planes || !host_scales || !plan || !dev_planes || !dev_scales)
+    return fail(SD_ERR_INVALID_ARG, "sd_offload_gather: NULL input");
+  if (!aligned16(host_planes) || !aligned16(dev_planes))
+    return fail(SD_ERR_INVALID_ARG, "sd_offload_gather: planes must be 16-byte aligned");
+  // the host buffers must be pinned and mapped into the device address space
+  const void* hp[2] = {host_planes, host_scales};
+  const void* dp[2] = {nullptr, nullptr};
+  for (int i = 0; i < 2; ++i) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, hp[i]);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(SD_ERR_INVALID_ARG, "sd_offload_gather: cannot query host pointer: %s",
+                  cudaGetErrorString(e));
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer)
+      return fail(SD_ERR_INVALID_ARG,
+                  "sd_offload_gather: host buffers must be pinned (cudaHostAlloc/Register)");
+    dp[i] = a.devicePointer;
+  }
+  return launch_offload_gather(s, (const uint32_t*)dp[0], (const uint16_t*)dp[1], plan,
+                               dev_planes, dev_scales, (cudaStream_t)stream);
+}
+
+int sd_event_wait(void* event, int64_t timeout_us) {
+  if (!event || timeout_us < 0) return fail(SD_ERR_INVALID_ARG, "sd_event_wait: bad argument");
+  auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    cudaError_t e = cudaEventQuery((cudaEvent_t)event);
+    if (e == cudaSuccess) return SD_OK;
+    if (e != cudaErrorNotReady) {
+      cudaGetLastError();
+      return fail(SD_ERR_CUDA, "sd_event_wait: %s", cudaGetErrorString(e));
+    }
+    auto us = std::chrono::duration_cast<std::chrono::microseconds>(
+                  std::chrono::steady_clock::now() - t0).count();
+    if (us >= timeout_us)
+      return fail(SD_ERR_TIMEOUT, "sd_event_wait: not complete after %lld us",
+                  (long long)timeout_us);
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+}
+
+}  // extern "C"

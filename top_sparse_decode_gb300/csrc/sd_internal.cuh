@@ -1,0 +1,74 @@
+// Internal declarations shared by libsd's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "sd.h"
+
+namespace sd {
+
+constexpr int kD = 128;          // head dimension supported by this build
+constexpr int kMaxTopK = 4096;   // largest retrieval budget of sd_topk
+constexpr int kSmallRow = 8192;  // rows up to this many units are selected by one CTA
+
+// ---- error reporting -------------------------------------------------------------
+void set_error(const char* fmt, ...);
+int fail(int code, const char* fmt, ...);
+int check_launch(const char* what);
+
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// ---- number formats ----------------------------------------------------------------
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+// low / high bf16 of a packed pair
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// order-preserving 32-bit keys: larger score -> larger key
+__device__ __forceinline__ uint32_t key_of_f32(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0.0 ranks with +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t key_of_i32(int32_t x) { return (uint32_t)x ^ 0x80000000u; }
+
+// ---- launchers (each returns SD_OK or an SD_ERR_*) ---------------------------------
+struct Dims {
+  int B, Hq, Hkv, G;
+  int64_t n, ncap;
+};
+
+int launch_sig_build(const Dims& s, const uint16_t* K, const sd_encoder& enc, uint32_t* sig,
+                     cudaStream_t st);
+int launch_encode_query(const Dims& s, const uint16_t* q, const sd_encoder& enc, uint32_t* qsig,
+                        cudaStream_t st);
+int launch_plane_build(const Dims& s, const uint16_t* K, uint32_t* planes, uint16_t* scales,
+                       cudaStream_t st);
+int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaStream_t st);
+int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode, int budget,
+                uint8_t* plan, cudaStream_t st);
+int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsig,
+                         int32_t* scores, cudaStream_t st);
+int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
+                        const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st);
+int launch_score_quest(const Dims& s, const uint16_t* summ, const uint16_t* q, float* scores,
+                       cudaStream_t st);
+size_t topk_workspace_bytes(int64_t rows, int64_t n_units, const sd_select& sel);
+int launch_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
+                int64_t n_tokens, const sd_select& sel, int32_t* idx, int64_t idx_stride,
+                int32_t* count, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t attend_workspace_bytes(const Dims& s, int64_t max_count);
+int launch_gather_attend(const Dims& s, const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                         const int32_t* idx, int64_t idx_stride, const int32_t* count,
+                         int64_t max_count, float scale, float* out, float* lse, void* ws,
+                         size_t ws_bytes, cudaStream_t st);
+int launch_offload_gather(const Dims& s, const uint32_t* host_planes, const uint16_t* host_scales,
+                          const uint8_t* plan, uint32_t* dev_planes, uint16_t* dev_scales,
+                          cudaStream_t st);
+
+}  // namespace sd
