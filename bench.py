@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of one sparse-decode step (SCORE -> TOPK -> GATHER-ATT) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (default): the long-context stress configuration -- one sequence of
+n = 1,048,576 cached tokens, 32 query heads on 8 KV heads, d = 128, bf16 K/V
+resident in HBM; Fathom bit-plane scan at a 56-bit water-filled budget, exact
+top-512 per KV head, gather-attend over the 512 selected rows.  A step is one
+layer's whole hot path for all heads: read plan -> bit-plane scan -> top-k ->
+gather-attend (the KV-write-path index build is done once, untimed).
+
+Timing: W untimed warm-up steps, then exactly K steps, each timed with CUDA
+events on the launching stream; L2 (129 MB) is flushed before every timed step
+by writing a 256 MB buffer, outside the events.  `value` = keys scored per
+second = (B * Hkv * n) / step time, summed over ranks (independent replicas,
+weak scaling).  One JSON line is printed by rank 0.
+
+--impl reference times the CPU oracle on the host cores on a bounded sample
+of the same workload per step (one KV head x 262,144 tokens).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "keys scored/s (sparse-decode step, 1M-token context)"
+UNIT = "keys/s"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-variants", action="store_true", help="skip the other scorers")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--n", type=int, default=0, help="override n (testing only)")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(nm)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dev_tensor(x, torch):
+    x = np.ascontiguousarray(x)
+    v = {np.dtype(np.uint16): np.int16, np.dtype(np.uint32): np.int32}.get(x.dtype, x.dtype)
+    return torch.from_numpy(x.view(v)).cuda()
+
+
+# ------------------------------------------------------------------------------------
+def timed_steps(torch, fn, steps, warmup, flush_buf, ws=1):
+    """Runs fn() warmup + steps times; returns per-step device ms of the timed ones.
+    The L2 flush before each step sits outside the events."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush_buf.zero_()
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush_buf.zero_()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def capture_graph(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def launches_per_step(step) -> int:
+    """Kernels of libsd one step launches (per the stage implementations)."""
+    from top_sparse_decode_gb300 import SD_IDX_MINMAX
+    c = step.cfg
+    prep = 0 if c.kind == SD_IDX_MINMAX else 1
+    topk = 1 if c.n_units <= 8192 else 4
+    return prep + 1 + topk + 2
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------
+def oracle_sample(inp, heads, n_tok):
+    """Oracle inputs for a sample of the step: the first `heads` KV heads of
+    sequence 0 over the first n_tok tokens, with its planes (KV-write path)."""
+    import oracle
+    G = inp.cfg.G
+    qh = np.ascontiguousarray(inp.q[:1, : heads * G])
+    Kh = np.ascontiguousarray(inp.K[:1, :heads, :n_tok])
+    Vh = np.ascontiguousarray(inp.V[:1, :heads, :n_tok])
+    s2 = np.ascontiguousarray(inp.sigma2[:heads])
+    planes, scales = oracle.plane_build(Kh)
+    return dict(q=qh, K=Kh, V=Vh, s2=s2, planes=planes, scales=scales, heads=heads, n=n_tok)
+
+
+def oracle_step(smp, k, d=128):
+    """The oracle, as it stands: plan -> bit-plane score -> top-k -> gather-attend.
+    Returns seconds."""
+    import oracle
+    h = smp["heads"]
+    t0 = time.perf_counter()
+    plan = oracle.plan(smp["q"], smp["s2"], h, oracle.PLAN_WATERFILL, 56)
+    sc = oracle.plane_score(smp["planes"], smp["scales"], plan, smp["q"])
+    idx, cnt = oracle.topk(sc.reshape(h, -1), k, 0, 0)
+    oracle.gather_attend(smp["q"], smp["K"], smp["V"], idx.reshape(1, h, -1),
+                         cnt.reshape(1, h), 1 / math.sqrt(d))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, cfg, heads=None):
+    """CPU baseline leg: the oracle on the same 1M-token step (all KV heads)."""
+    import oracle
+    heads = heads or cfg.Hkv
+    smp = oracle_sample(inp, heads, cfg.n)
+    dt = oracle_step(smp, cfg.k, cfg.d)
+    return {"value": heads * cfg.n / dt, "unit": UNIT, "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{heads} of {cfg.Hkv} KV heads x {cfg.n} tokens of the step (plan, "
+                      f"bit-plane score, top-{cfg.k}, gather-attend) in {dt:.2f} s"}
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the CPU oracle on the same workload; each step is a bounded
+    sample (1 KV head x 262,144 tokens) so that K steps take well under a minute
+    or two on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    n = args.n or (1 << 20)
+    cfg = synth.config(4, n=n)
+    cfg_s = synth.config(4, B=1, Hkv=1, Hq=cfg.G, n=n)
+    inp = synth.make_inputs(cfg_s)
+    n_tok = min(n, 1 << 18)
+    smp = oracle_sample(inp, 1, n_tok)
+    for _ in range(args.warmup):
+        oracle_step(smp, cfg.k, cfg.d)
+    times = [oracle_step(smp, cfg.k, cfg.d) for _ in range(args.steps)]
+    t = statistics.mean(times)
+    v = n_tok / t
+    sample = (f"1 of {cfg.Hkv} KV heads x {n_tok} of {n} tokens per step (plan, bit-plane "
+              f"score, top-{cfg.k}, gather-attend)")
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": f"longctx-1m: B=1, Hq=32, Hkv=8, d=128, n={n}; 56-bit "
+                                   f"water-filled bit-plane scan, top-{cfg.k}, gather-attend "
+                                   f"(oracle on a per-step sample)", "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle.threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------
+def main():
+    args = parse()
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    import torch
+
+    import synth
+    import top_sparse_decode_gb300 as sd
+    from top_sparse_decode_gb300 import build as sdbuild
+    from top_sparse_decode_gb300 import roofline as rl
+    from top_sparse_decode_gb300.pipeline import DecodeStep, StepConfig, build_index
+
+    if rank == 0:
+        sdbuild.build()
+    barrier(ws)
+    torch.cuda.set_device(local)
+    sd.lib()
+    cfg = synth.config(4) if not args.n else synth.config(4, n=args.n)
+    t_gen = time.perf_counter()
+    inp = synth.make_inputs(cfg)
+    log(f"[bench] inputs generated in {time.perf_counter() - t_gen:.1f} s")
+    q = dev_tensor(inp.q, torch)
+    K = dev_tensor(inp.K, torch)
+    V = dev_tensor(inp.V, torch)
+    sigma2 = dev_tensor(inp.sigma2, torch)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    B, Hq, Hkv, n = cfg.B, cfg.Hq, cfg.Hkv, cfg.n
+    keys = B * Hkv * n
+
+    # headline step: 56-bit water-filled bit-plane scan
+    sc = StepConfig(sd.SD_IDX_PLANES, B, Hq, Hkv, n, k=cfg.k, plan_mode=sd.SD_PLAN_WATERFILL,
+                    budget=56)
+    index = build_index(sc, K)
+    step = DecodeStep(sc, K, V, index, sigma2=sigma2)
+    step.run(q)
+    torch.cuda.synchronize()
+    plan_np = step.plan.cpu().numpy()
+    counts_np = step.count.cpu().numpy()
+    scan_bytes = rl.plane_scan_bytes(plan_np, n)
+    gath_bytes = rl.gather_bytes(counts_np)
+    alg_bytes = scan_bytes + gath_bytes
+
+    # graph-captured step (falls back to eager if capture is refused)
+    try:
+        graph = capture_graph(torch, lambda: step.run(q))
+        run = graph.replay
+        mode = "cuda-graph"
+    except Exception as e:  # noqa: BLE001
+        log(f"[bench] graph capture failed ({e}); timing eager launches")
+        run = lambda: step.run(q)  # noqa: E731
+        mode = "eager"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    times = timed_steps(torch, run, args.steps, args.warmup, flush, ws)
+    ck = clocks.stop()
+    t_step = statistics.mean(times)
+    t_step_max = max_over_ranks(t_step, ws)
+    value = keys * ws / (t_step_max * 1e-3)
+
+    # per-stage and dominant-kernel timings (eager, each stage alone, cold L2)
+    K_st = max(10, min(args.steps, 100))
+    st_prep = statistics.mean(timed_steps(torch, lambda: step.stage_prep(q), K_st, 3, flush))
+    st_score = statistics.mean(timed_steps(torch, lambda: step.stage_score(q), K_st, 3, flush))
+    st_topk = statistics.mean(timed_steps(torch, lambda: step.stage_topk(), K_st, 3, flush))
+    st_att = statistics.mean(timed_steps(torch, lambda: step.stage_attend(q), K_st, 3, flush))
+    eager = statistics.mean(timed_steps(torch, lambda: step.run(q), K_st, 3, flush))
+    peak_gbs, peak_kind = peaks()
+    scan_gbs = scan_bytes / (st_score * 1e-3) / 1e9
+    alu_ops = rl.plane_scan_alu_ops(plan_np, n)
+
+    # e2e: pinned host q in, result out, through the public API, each step
+    q_host = torch.from_numpy(inp.q.view(np.int16)).pin_memory()
+    out_host = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    lse_host = torch.empty(step.lse.shape, dtype=torch.float32).pin_memory()
+    q_dev = torch.empty_like(q)
+
+    def e2e_step():
+        q_dev.copy_(q_host, non_blocking=True)
+        step.run(q_dev)
+        out_host.copy_(step.out, non_blocking=True)
+        lse_host.copy_(step.lse, non_blocking=True)
+
+    e2e_t = statistics.mean(timed_steps(torch, e2e_step, max(args.steps // 2, 10), 3, flush))
+    e2e_val = keys * ws / (max_over_ranks(e2e_t, ws) * 1e-3)
+    torch.cuda.synchronize()
+    assert np.array_equal(out_host.numpy(), step.out.cpu().numpy())
+
+    variants = {}
+    if not args.no_variants:
+        # fixed 32-channel full-depth scan (the "136-bit" class) on the same planes
+        scf = StepConfig(sd.SD_IDX_PLANES, B, Hq, Hkv, n, k=cfg.k, plan_mode=sd.SD_PLAN_FIXED,
+                         budget=32)
+        stf = DecodeStep(scf, K, V, index, sigma2=sigma2)
+        stf.run(q)
+        torch.cuda.synchronize()
+        pf = stf.plan.cpu().numpy()
+        tf = statistics.mean(timed_steps(torch, lambda: stf.run(q), K_st, 3, flush))
+        tfs = statistics.mean(timed_steps(torch, lambda: stf.stage_score(q), K_st, 3, flush))
+        bf = rl.plane_scan_bytes(pf, n)
+        variants["fixed32x4"] = {"us_per_step": tf * 1e3, "keys_per_s": keys / (tf * 1e-3),
+                                 "scan_us": tfs * 1e3, "scan_bytes": bf,
+                                 "scan_GBps": bf / (tfs * 1e-3) / 1e9,
+                                 "scan_frac_hbm": bf / (tfs * 1e-3) / 1e9 / peak_gbs}
+        del stf
+        # 32-bit Hamming (random projection), query map included
+        sch = StepConfig(sd.SD_IDX_SIG, B, Hq, Hkv, n, k=cfg.k)
+        enc = sd.make_encoder(dev_tensor(inp.W1, torch), dev_tensor(inp.b1, torch))
+        ih = build_index(sch, K, enc)
+        sth = DecodeStep(sch, K, V, ih, enc=enc)
+        sth.run(q)
+        torch.cuda.synchronize()
+        th = statistics.mean(timed_steps(torch, lambda: sth.run(q), K_st, 3, flush))
+        ths = statistics.mean(timed_steps(torch, lambda: sth.stage_score(q), K_st, 3, flush))
+        bh = rl.hamming_scan_bytes(B, Hkv, n)
+        variants["hamming32"] = {"us_per_step": th * 1e3, "keys_per_s": keys / (th * 1e-3),
+                                 "scan_us": ths * 1e3, "scan_bytes": bh,
+                                 "scan_GBps": bh / (ths * 1e-3) / 1e9,
+                                 "scan_frac_hbm": bh / (ths * 1e-3) / 1e9 / peak_gbs}
+        del sth, ih
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, cfg)
+
+    # ALU peak: 152 SMs x 128 lanes x the median SM clock seen under load
+    sm_mhz = ck.get("sm_mhz") or 1920.0
+    alu_peak = 152 * 128 * sm_mhz * 1e6
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"longctx-1m: B={B}, Hq={Hq}, Hkv={Hkv}, d={cfg.d}, n={n}; "
+                               f"56-bit water-filled bit-plane scan, top-{cfg.k}, "
+                               f"gather-attend over bf16 K/V in HBM",
+                   "l2": "flushed (256 MB write) before every timed step", "launch": mode,
+                   "parallelism": f"replicas x{ws}"},
+        "us_per_step": t_step_max * 1e3,
+        "stages_us": {"plan": st_prep * 1e3, "scan": st_score * 1e3, "topk": st_topk * 1e3,
+                      "gather_attend": st_att * 1e3, "step_eager": eager * 1e3},
+        "roofline": {"bound": "hbm", "kernel": "score_planes_kernel",
+                     "achieved": scan_gbs, "peak": peak_gbs, "unit": "GB/s",
+                     "frac": scan_gbs / peak_gbs, "traffic": None,
+                     "peak_kind": peak_kind,
+                     "alg_bytes_per_launch": scan_bytes},
+        "roofline_alu": {"bound": "alu", "kernel": "score_planes_kernel",
+                         "achieved": alu_ops / (st_score * 1e-3) / 1e12,
+                         "peak": alu_peak / 1e12, "unit": "Tops/s",
+                         "frac": alu_ops / (st_score * 1e-3) / alu_peak,
+                         "ops_per_launch": alu_ops},
+        "step_bytes": {"algorithmic": alg_bytes, "scan": scan_bytes, "gather": gath_bytes,
+                       "score_buffer": rl.score_buffer_bytes(B, Hkv, n),
+                       "step_GBps": alg_bytes / (t_step_max * 1e-3) / 1e9},
+        "plan_bits_per_token": rl.plane_scan_bits_per_token(plan_np),
+        "e2e": {"value": e2e_val, "unit": UNIT,
+                "h2d_bytes_per_step": int(q_host.numel() * q_host.element_size()),
+                "d2h_bytes_per_step": int(out_host.numel() * 4 + lse_host.numel() * 4)},
+        "gpu_launches": launches_per_step(step) * args.steps,
+        "clocks": ck,
+        "variants": variants,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -52,6 +52,8 @@ def _l():
             lib.orc_f32_to_f16.restype = ctypes.c_uint16
             lib.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
             lib.orc_f16_to_f32.restype = ctypes.c_float
+            lib.orc_threads.argtypes = []
+            lib.orc_threads.restype = i32
             lib.orc_reconstruct.argtypes = [i32, i32, d]
             lib.orc_reconstruct.restype = d
             lib.orc_sig_encode.argtypes = [p, i64, i32, p, p, i32, p, p, p]
@@ -84,6 +86,10 @@ def _l():
 def _c(a, dtype):
     a = np.ascontiguousarray(a, dtype=dtype)
     return a, a.ctypes.data
+
+
+def threads() -> int:
+    return int(_l().orc_threads())
 
 
 def f32_to_f16(x: float) -> int:

@@ -25,6 +25,7 @@
  * Readings of points the pages leave open are marked READING below.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -92,6 +93,9 @@ float orc_f16_to_f32(uint16_t h) {
   return f;
 }
 
+/* threads the oracle's parallel loops use (for reporting a CPU baseline) */
+int orc_threads(void) { return omp_get_max_threads(); }
+
 static int popcount32(uint32_t x) {
   int c = 0;
   while (x) { x &= x - 1u; ++c; }
@@ -155,17 +159,15 @@ int orc_sig_encode(const uint16_t* x_bf16, int64_t rows, int d, const float* W1,
 void orc_hamming_score(const uint32_t* sig, int64_t B, int Hq, int Hkv, int64_t n,
                        const uint32_t* qsig, int32_t* score) {
   int G = Hq / Hkv;
-#pragma omp parallel for collapse(2) schedule(static)
+#pragma omp parallel for collapse(3) schedule(static)
   for (int64_t b = 0; b < B; ++b)
-    for (int h = 0; h < Hkv; ++h) {
-      const uint32_t* s = sig + (b * Hkv + h) * n;
-      int32_t* out = score + (b * Hkv + h) * n;
+    for (int h = 0; h < Hkv; ++h)
       for (int64_t i = 0; i < n; ++i) {
+        const uint32_t* s = sig + (b * Hkv + h) * n;
         int acc = 0;
         for (int g = 0; g < G; ++g) acc += popcount32(s[i] ^ qsig[b * Hq + h * G + g]);
-        out[i] = -acc;
+        score[(b * Hkv + h) * n + i] = -acc;
       }
-    }
 }
 
 /* ------------------------------------------------------------------------------ */
@@ -295,11 +297,11 @@ void orc_plane_score(const uint32_t* planes, const uint16_t* scales, const uint8
                      double* score) {
   int G = Hq / Hkv;
   int64_t nw = n / 32, nb = n / 64;
-#pragma omp parallel for collapse(2) schedule(static)
+#pragma omp parallel for collapse(3) schedule(static)
   for (int64_t b = 0; b < B; ++b)
-    for (int h = 0; h < Hkv; ++h) {
-      const uint8_t* pb = plan + (b * Hkv + h) * d;
+    for (int h = 0; h < Hkv; ++h)
       for (int64_t i = 0; i < n; ++i) {
+        const uint8_t* pb = plan + (b * Hkv + h) * d;
         double acc = 0.0;
         for (int g = 0; g < G; ++g) {
           const uint16_t* qg = q + (b * Hq + h * G + g) * d;
@@ -315,7 +317,6 @@ void orc_plane_score(const uint32_t* planes, const uint16_t* scales, const uint8
         }
         score[(b * Hkv + h) * n + i] = acc;
       }
-    }
 }
 
 /* Sum of |terms| of each plane score, the scale of its rounding tolerance. */
@@ -324,11 +325,11 @@ void orc_plane_score_l1(const uint32_t* planes, const uint16_t* scales, const ui
                         double* l1) {
   int G = Hq / Hkv;
   int64_t nw = n / 32, nb = n / 64;
-#pragma omp parallel for collapse(2) schedule(static)
+#pragma omp parallel for collapse(3) schedule(static)
   for (int64_t b = 0; b < B; ++b)
-    for (int h = 0; h < Hkv; ++h) {
-      const uint8_t* pb = plan + (b * Hkv + h) * d;
+    for (int h = 0; h < Hkv; ++h)
       for (int64_t i = 0; i < n; ++i) {
+        const uint8_t* pb = plan + (b * Hkv + h) * d;
         double acc = 0.0;
         for (int g = 0; g < G; ++g)
           for (int j = 0; j < d; ++j) {
@@ -343,7 +344,6 @@ void orc_plane_score_l1(const uint32_t* planes, const uint16_t* scales, const ui
           }
         l1[(b * Hkv + h) * n + i] = acc;
       }
-    }
 }
 
 /* ------------------------------------------------------------------------------ */

@@ -4,7 +4,10 @@
 #include <string.h>
 
 #include <chrono>
+#include <map>
+#include <mutex>
 #include <thread>
+#include <utility>
 
 #include "sd_internal.cuh"
 
@@ -30,6 +33,22 @@ int fail(int code, const char* fmt, ...) {
 int check_launch(const char* what) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return SD_OK;
+}
+
+int set_smem_limit(const void* kernel, size_t bytes, const char* what) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return check_launch(what);
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_pair(dev, kernel);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return SD_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return check_launch(what);
+  done[key] = bytes;
   return SD_OK;
 }
 

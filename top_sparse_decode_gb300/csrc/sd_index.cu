@@ -188,8 +188,7 @@ static int sig_build_t(const Dims& s, const uint16_t* K, const sd_encoder& e, ui
   constexpr int H1 = HID ? HID : 32;
   size_t smem = sizeof(float) * (kD * H1 + H1 + HID * 32 + 32);
   auto kern = sig_build_kernel<HID>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))
-    return check_launch("sig_build: smem attribute");
+  if (int rc_ = set_smem_limit((const void*)kern, smem, "sig_build: smem attribute")) return rc_;
   int64_t rows = (int64_t)s.B * s.Hkv * s.n;
   unsigned grid = (unsigned)((rows + 127) / 128);
   kern<<<grid, 128, smem, st>>>(K, s.n, s.ncap, rows, e.W1, e.b1, e.W2, e.b2, sig);
@@ -203,8 +202,7 @@ static int encode_query_t(const Dims& s, const uint16_t* q, const sd_encoder& e,
   size_t smem = sizeof(float) * (H1 * (kD + 1) + (HID ? 32 * (HID + 1) : 0) + kQRows * kD +
                                  kQRows * HID);
   auto kern = encode_query_kernel<HID>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))
-    return check_launch("encode_query: smem attribute");
+  if (int rc_ = set_smem_limit((const void*)kern, smem, "encode_query: smem attribute")) return rc_;
   int rows = s.B * s.Hq;
   kern<<<(rows + kQRows - 1) / kQRows, 128, smem, st>>>(q, rows, e.W1, e.b1, e.W2, e.b2, qsig);
   return check_launch("encode_query");
@@ -303,9 +301,7 @@ plane_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap,
 int launch_plane_build(const Dims& s, const uint16_t* K, uint32_t* planes, uint16_t* scales,
                        cudaStream_t st) {
   size_t smem = 64 * kPbPitch * 2 + kD * 4 * 32 * 4 + kD * 16 * 2;
-  if (cudaFuncSetAttribute(plane_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem))
-    return check_launch("plane_build: smem attribute");
+  if (int rc_ = set_smem_limit((const void*)plane_build_kernel, smem, "plane_build: smem attribute")) return rc_;
   dim3 grid((unsigned)((s.n + kPbTile - 1) / kPbTile), (unsigned)(s.B * s.Hkv));
   plane_build_kernel<<<grid, 256, smem, st>>>(K, s.n, s.ncap, planes, scales);
   return check_launch("plane_build");

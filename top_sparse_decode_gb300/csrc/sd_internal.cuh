@@ -17,6 +17,10 @@ constexpr int kSmallRow = 8192;  // rows up to this many units are selected by o
 void set_error(const char* fmt, ...);
 int fail(int code, const char* fmt, ...);
 int check_launch(const char* what);
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per (device,
+// kernel): later calls, including those made while a stream is being captured
+// into a CUDA graph, issue no CUDA call.
+int set_smem_limit(const void* kernel, size_t bytes, const char* what);
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }

@@ -497,8 +497,7 @@ static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
   const size_t smem = sizeof(FinSmem);
   if (g.n_units <= kSmallRow) {
     auto kern = topk_small_kernel<F32>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))
-      return check_launch("topk: smem attribute");
+    if (int rc_ = set_smem_limit((const void*)kern, smem, "topk: smem attribute")) return rc_;
     kern<<<(unsigned)rows, kFinThreads, smem, st>>>(scores, g, idx, idx_stride, count);
     return check_launch("topk_small");
   }
@@ -511,8 +510,7 @@ static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
   topk_hist_kernel<F32><<<grid, 256, 0, st>>>(scores, g, ws, max(nchunks, 1u));
   topk_filter_kernel<F32><<<grid, 256, 0, st>>>(scores, g, ws);
   auto fin = topk_finish_kernel<F32>;
-  if (cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))
-    return check_launch("topk: smem attribute");
+  if (int rc_ = set_smem_limit((const void*)fin, smem, "topk: smem attribute")) return rc_;
   fin<<<(unsigned)rows, kFinThreads, smem, st>>>(scores, g, ws, idx, idx_stride, count);
   return check_launch("topk");
 }

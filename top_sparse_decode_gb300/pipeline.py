@@ -1,0 +1,141 @@
+"""One decode step of the sparse-decode hot path, composed from the C-ABI calls.
+
+This module owns buffers and call order only; every value is computed by
+libsd's kernels.  A step for one layer, all heads and the whole batch is
+
+    query map (Hamming) or read plan (bit planes)  ->  sd_score  ->  sd_topk
+        ->  sd_gather_attend
+
+and the per-stage split T = T_qmap + T_scan + T_topk + T_att follows
+HashAttention: Semantic Sparsity for Faster Inference, 2.5.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+from . import (SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_SCORE_F32,
+               SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
+               sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_score, sd_topk,
+               sd_topk_workspace_size)
+
+KIND_NAMES = {SD_IDX_SIG: "hamming", SD_IDX_PLANES: "planes", SD_IDX_MINMAX: "quest"}
+
+
+@dataclasses.dataclass
+class StepConfig:
+    kind: int                 # SD_IDX_SIG, SD_IDX_PLANES or SD_IDX_MINMAX
+    B: int
+    Hq: int
+    Hkv: int
+    n: int
+    d: int = 128
+    k: int = 512              # tokens (token mode) or blocks (block mode, kind MINMAX)
+    sink: int = 0             # forced leading units
+    local: int = 0            # forced trailing units
+    plan_mode: int = SD_PLAN_WATERFILL
+    budget: int = 56          # bits per token per KV head (water-filling) or r (fixed)
+
+    @property
+    def block(self) -> int:
+        return 16 if self.kind == SD_IDX_MINMAX else 1
+
+    @property
+    def n_units(self) -> int:
+        return (self.n + 15) // 16 if self.kind == SD_IDX_MINMAX else self.n
+
+    @property
+    def max_count(self) -> int:
+        return min(self.n_units, self.sink + self.local + self.k) * self.block
+
+
+def index_buffers(cfg: StepConfig, device="cuda") -> dict:
+    """Allocates the key-side index of cfg.kind (uninitialised)."""
+    B, H, n, d = cfg.B, cfg.Hkv, cfg.n, cfg.d
+    if cfg.kind == SD_IDX_SIG:
+        return {"sig": torch.empty((B, H, n), dtype=torch.int32, device=device)}
+    if cfg.kind == SD_IDX_PLANES:
+        return {"planes": torch.empty((B, H, d, 4, n // 32), dtype=torch.int32, device=device),
+                "scales": torch.empty((B, H, d, n // 64), dtype=torch.int16, device=device)}
+    nblk = (n + 15) // 16
+    return {"summ": torch.empty((B, H, nblk, 2, d), dtype=torch.int16, device=device)}
+
+
+def build_index(cfg: StepConfig, K: torch.Tensor, enc=None, stream=None) -> dict:
+    """Runs sd_build_index for cfg.kind (the KV-write path) and returns the index."""
+    shp = make_shape(cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.d)
+    idx = index_buffers(cfg, K.device)
+    if cfg.kind == SD_IDX_SIG:
+        sd_build_index(SD_IDX_SIG, shp, K, enc, idx["sig"], None, stream)
+    elif cfg.kind == SD_IDX_PLANES:
+        sd_build_index(SD_IDX_PLANES, shp, K, None, idx["planes"], idx["scales"], stream)
+    else:
+        sd_build_index(SD_IDX_MINMAX, shp, K, None, idx["summ"], None, stream)
+    return idx
+
+
+class DecodeStep:
+    """Preallocated buffers and the call sequence of one decode step."""
+
+    def __init__(self, cfg: StepConfig, K: torch.Tensor, V: torch.Tensor, index: dict,
+                 enc=None, sigma2: Optional[torch.Tensor] = None,
+                 scale: Optional[float] = None):
+        self.cfg = cfg
+        self.K, self.V, self.index, self.enc, self.sigma2 = K, V, index, enc, sigma2
+        self.scale = 1.0 / math.sqrt(cfg.d) if scale is None else scale
+        dev = K.device
+        c = cfg
+        self.shape = make_shape(c.B, c.Hq, c.Hkv, c.n, c.d)
+        self.rows = c.B * c.Hkv
+        self.sel = make_select(c.k, c.sink, c.local, c.block)
+        sdt = torch.int32 if c.kind == SD_IDX_SIG else torch.float32
+        self.scores = torch.empty((self.rows, c.n_units), dtype=sdt, device=dev)
+        self.qsig = torch.empty((c.B, c.Hq), dtype=torch.int32, device=dev)
+        self.plan = torch.empty((c.B, c.Hkv, c.d), dtype=torch.uint8, device=dev)
+        self.idx = torch.empty((self.rows, c.max_count), dtype=torch.int32, device=dev)
+        self.count = torch.empty((self.rows,), dtype=torch.int32, device=dev)
+        tws = sd_topk_workspace_size(self.rows, c.n_units, self.sel)
+        self.topk_ws = torch.empty(tws, dtype=torch.uint8, device=dev) if tws else None
+        aws = sd_gather_attend_workspace_size(self.shape, c.max_count)
+        self.att_ws = torch.empty(max(aws, 256), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((c.B, c.Hq, c.d), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((c.B, c.Hq), dtype=torch.float32, device=dev)
+
+    # the four stages, separately callable for per-stage timing
+    def stage_prep(self, q, stream=None):
+        c = self.cfg
+        if c.kind == SD_IDX_SIG:
+            sd_encode_query(self.shape, q, self.enc, self.qsig, stream)
+        elif c.kind == SD_IDX_PLANES:
+            sd_plan(self.shape, q, self.sigma2, c.plan_mode, c.budget, self.plan, stream)
+
+    def stage_score(self, q, stream=None):
+        c, ix = self.cfg, self.index
+        if c.kind == SD_IDX_SIG:
+            sd_score(SD_IDX_SIG, self.shape, ix["sig"], None, self.qsig, None, self.scores, stream)
+        elif c.kind == SD_IDX_PLANES:
+            sd_score(SD_IDX_PLANES, self.shape, ix["planes"], ix["scales"], q, self.plan,
+                     self.scores, stream)
+        else:
+            sd_score(SD_IDX_MINMAX, self.shape, ix["summ"], None, q, None, self.scores, stream)
+
+    def stage_topk(self, stream=None):
+        c = self.cfg
+        st = SD_SCORE_I32 if c.kind == SD_IDX_SIG else SD_SCORE_F32
+        sd_topk(st, self.scores, self.rows, c.n_units, c.n, self.sel, self.idx, c.max_count,
+                self.count, self.topk_ws, stream)
+
+    def stage_attend(self, q, stream=None):
+        c = self.cfg
+        sd_gather_attend(self.shape, q, self.K, self.V, self.idx, c.max_count, self.count,
+                         c.max_count, self.scale, self.out, self.lse, self.att_ws, stream)
+
+    def run(self, q, stream=None):
+        self.stage_prep(q, stream)
+        self.stage_score(q, stream)
+        self.stage_topk(stream)
+        self.stage_attend(q, stream)
+        return self.out
