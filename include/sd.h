@@ -187,6 +187,28 @@ int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const 
                      size_t ws_bytes, void* stream);
 
 /*
+ * sd_gather_attend_noalloc -- sd_gather_attend for callers that cannot allocate
+ * device memory: code running while its stream is captured into a CUDA graph,
+ * engines whose host framework owns every device allocation, real-time loops
+ * that must not take allocator locks.  (The pages have no counterpart: this is
+ * a property of the library, not of the method.)
+ *   Same arguments, layouts and results as sd_gather_attend, without the
+ *   workspace: the split-n partials live in a 4 MiB file-scope device array
+ *   that every GPU loading libsd holds until the process exits.  Requests whose
+ *   partials need more (sd_gather_attend_workspace_size() > 4 MiB) are rejected
+ *   with SD_ERR_UNSUPPORTED before anything is enqueued.  Allocates nothing.
+ *   The first call on each device looks up that device's copy of the array
+ *   (cudaGetSymbolAddress, with the device current); make that first call before
+ *   any stream capture.  All calls on a device share the array and it keeps the
+ *   last call's contents (every partial is written before it is read, so no
+ *   clearing is needed); calls that overlap on the GPU race on it.
+ */
+int sd_gather_attend_noalloc(const sd_shape* shape, const void* q, const void* K, const void* V,
+                             const int32_t* idx, int64_t idx_stride, const int32_t* count,
+                             int64_t max_count, float scale, float* out, float* lse,
+                             void* stream);
+
+/*
  * sd_offload_gather -- copy each (sequence, KV head, channel j)'s planned
  * prefix (the first plan_j planes, contiguous in the channel-major layout)
  * and channel j's scales from pinned host memory into HBM, with device loads

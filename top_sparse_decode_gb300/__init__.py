@@ -25,7 +25,8 @@ from ._abi import (SD_ERR_CUDA, SD_ERR_INVALID_ARG, SD_ERR_TIMEOUT, SD_ERR_UNSUP
 __all__ = [
     "SdError", "make_shape", "make_encoder", "make_select", "lib",
     "sd_build_index", "sd_encode_query", "sd_plan", "sd_score", "sd_topk_workspace_size",
-    "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend", "sd_offload_gather",
+    "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
+    "sd_gather_attend_noalloc", "sd_offload_gather",
     "sd_event_wait", "sd_last_error", "sd_version",
 ]
 
@@ -142,6 +143,16 @@ def sd_gather_attend(shape: SdShape, q, K, V, idx, idx_stride: int, count, max_c
                                   idx_stride, _ptr(count), max_count, float(scale), _ptr(out),
                                   _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)),
            "sd_gather_attend")
+
+
+def sd_gather_attend_noalloc(shape: SdShape, q, K, V, idx, idx_stride: int, count,
+                             max_count: int, scale: float, out, lse=None, stream=None) -> None:
+    """sd_gather_attend without a workspace (for callers that cannot allocate):
+    partials live in libsd's 4 MiB per-GPU static array; see include/sd.h."""
+    _check(lib().sd_gather_attend_noalloc(ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V),
+                                          _ptr(idx), idx_stride, _ptr(count), max_count,
+                                          float(scale), _ptr(out), _ptr(lse), _stream(stream)),
+           "sd_gather_attend_noalloc")
 
 
 def sd_offload_gather(shape: SdShape, host_planes, host_scales, plan, dev_planes, dev_scales,

@@ -47,6 +47,8 @@ SIGNATURES = {
     "sd_gather_attend_workspace_size": (_sz, [_PS, _i64]),
     "sd_gather_attend": (_i, [_PS, _p, _p, _p, _p, _i64, _p, _i64, ctypes.c_float, _p, _p, _p,
                               _sz, _p]),
+    "sd_gather_attend_noalloc": (_i, [_PS, _p, _p, _p, _p, _i64, _p, _i64, ctypes.c_float, _p,
+                                      _p, _p]),
     "sd_offload_gather": (_i, [_PS, _p, _p, _p, _p, _p, _p]),
     "sd_event_wait": (_i, [_p, _i64]),
     "sd_last_error": (ctypes.c_char_p, []),
