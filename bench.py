@@ -186,8 +186,8 @@ def launches_per_step(step) -> int:
     from top_sparse_decode_gb300 import SD_IDX_MINMAX
     c = step.cfg
     prep = 0 if c.kind == SD_IDX_MINMAX else 1
-    topk = 1 if c.n_units <= 8192 else 4
-    return prep + 1 + topk + 2
+    topk = 1 if c.n_units <= 8192 else 3   # one CTA per row, or sample + filter + finish
+    return prep + 1 + topk + 1             # + gather-attend (partials merged in-kernel)
 
 
 def peaks():

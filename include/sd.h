@@ -200,8 +200,9 @@ int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const 
  *   The first call on each device looks up that device's copy of the array
  *   (cudaGetSymbolAddress, with the device current); make that first call before
  *   any stream capture.  All calls on a device share the array and it keeps the
- *   last call's contents (every partial is written before it is read, so no
- *   clearing is needed); calls that overlap on the GPU race on it.
+ *   last call's contents: each call first clears the per-row counters that
+ *   must start at zero (partials are written before they are read); calls that
+ *   overlap on the GPU race on it.
  */
 int sd_gather_attend_noalloc(const sd_shape* shape, const void* q, const void* K, const void* V,
                              const int32_t* idx, int64_t idx_stride, const int32_t* count,

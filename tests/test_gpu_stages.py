@@ -145,17 +145,24 @@ def test_plan_bit_exact(sd, G):
 # --------------------------------------------------------------------------------------
 # S5b bit-plane scan and S5c Quest bound: within 1e-5 of the L1 mass
 # --------------------------------------------------------------------------------------
-@pytest.mark.parametrize("budget,mode", [(56, 0), (47, 0), (92, 0), (0, 0), (32, 1), (0, 2)])
-def test_plane_scores(sd, budget, mode):
+@pytest.mark.parametrize("budget,mode,ncap", [(56, 0, 0), (47, 0, 0), (92, 0, 0), (0, 0, 0),
+                                               (32, 1, 0), (0, 2, 0), (56, 0, 4608),
+                                               (0, 2, 4608)])
+def test_plane_scores(sd, budget, mode, ncap):
+    # n = 4288: one full 4096-token tile and a last tile of 6 words / 3 scale
+    # blocks; ncap = 4608 (a multiple of 512) takes the 16-byte staging path
     cfg = synth.config(2, B=2, Hq=8, Hkv=2, n=2 * 2048 + 3 * 64)
     inp = synth.make_inputs(cfg, with_v=False)
-    shp = shape_of(sd, cfg)
+    ncap = ncap or cfg.n
+    shp = shape_of(sd, cfg, n_cap=ncap)
     ref_p, ref_s = oracle.plane_build(inp.K)
     plan_ref = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, mode, budget)
     ref, l1 = oracle.plane_score(ref_p, ref_s, plan_ref, inp.q, with_l1=True)
-    planes = empty(ref_p.shape, np.uint32)
-    scales = empty(ref_s.shape, np.uint16)
-    sd.sd_build_index(sd.SD_IDX_PLANES, shp, dev(inp.K), None, planes, scales)
+    Kp = np.zeros((cfg.B, cfg.Hkv, ncap, cfg.d), np.uint16)
+    Kp[:, :, :cfg.n] = inp.K
+    planes = empty((cfg.B, cfg.Hkv, cfg.d, 4, ncap // 32), np.uint32)
+    scales = empty((cfg.B, cfg.Hkv, cfg.d, ncap // 64), np.uint16)
+    sd.sd_build_index(sd.SD_IDX_PLANES, shp, dev(Kp), None, planes, scales)
     plan = empty(plan_ref.shape, np.uint8)
     q = dev(inp.q)
     sd.sd_plan(shp, q, dev(inp.sigma2), mode, budget, plan)
@@ -224,6 +231,35 @@ def test_topk_bit_exact_on_shared_scores(sd, rows, n, kind, levels, k, sink, loc
     for r in range(rows):
         assert gc[r] == rc[r], (r, gc[r], rc[r])
         assert np.array_equal(gi[r, :gc[r]], ri[r, :rc[r]]), r
+
+
+def test_topk_estimate_misses_fall_back_to_exact(sd):
+    # Long rows: the threshold is estimated from an evenly spaced sample of up to
+    # 16,384 scores.  (a) 200 large scores, all on sampled positions: the estimate
+    # admits fewer than k candidates.  (b) every sampled position large: more
+    # candidates than the finishing CTA holds.  Both must still be exact.
+    M, S = 100000, 16384
+    pos = (np.arange(S, dtype=np.int64) * M) // S
+    a = np.zeros((1, M), np.float32)
+    a[0, pos[::37][:200]] = 1.0
+    b = np.zeros((1, M), np.float32)
+    b[0, pos] = 2.0
+    b[0, 5] = 3.0
+    for s in (a, b):
+        gi, gc = run_topk(sd, s, 512, 0, 0)
+        ri, rc = oracle.topk(s, 512, 0, 0)
+        assert gc[0] == rc[0] and np.array_equal(gi[0, :gc[0]], ri[0, :rc[0]])
+
+
+def test_topk_clustered_winners(sd):
+    # the top k sit in one narrow index range (sorting falls back to bitonic)
+    s = synth.make_scores(3, 2, 200000, "f32")
+    s[:, 50000:53000] += 100.0
+    for k in (512, 3000, 4096):
+        gi, gc = run_topk(sd, s, k, 1, 1)
+        ri, rc = oracle.topk(s, k, 1, 1)
+        for r in range(2):
+            assert gc[r] == rc[r] and np.array_equal(gi[r, :gc[r]], ri[r, :rc[r]])
 
 
 def test_topk_block_mode_bit_exact(sd):

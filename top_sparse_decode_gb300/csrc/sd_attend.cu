@@ -5,14 +5,16 @@
 //
 // Split-n: CTA (chunk, row) handles up to kAtChunk selected tokens of one
 // (sequence, KV head) for all G query heads of the group, so every K/V row is
-// read once per group.  It writes (m, l, o~) partials; a combine kernel merges
-// them with the usual rescaling e^{m_c - m}.
+// read once per group.  It writes (m, l, o~) partials; the last CTA of a row to
+// finish (a per-row ticket) merges the row's partials in chunk order with the
+// usual rescaling e^{m_c - m}, so the result does not depend on which CTA is last.
 #include "sd_internal.cuh"
 
 namespace sd {
 
-constexpr int kAtChunk = 64;
+constexpr int kAtChunk = 32;
 constexpr int kAtPitch = kD + 8;  // bf16 pitch of staged rows (breaks bank alignment)
+constexpr int kQPitch = 36;       // fp32 pitch of a quarter of q (conflict-free LDS.128)
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -26,42 +28,72 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 static int64_t attend_chunks(int64_t max_count) { return (max_count + kAtChunk - 1) / kAtChunk; }
 
+struct AttWs {
+  uint32_t* ticket;  // [rows], zeroed at the start of every call
+  float* part_o;     // [rows][nch][G][kD]
+  float2* part_ml;   // [rows][nch][G]
+};
+
+static AttWs carve_att(void* ws, int64_t rows, int64_t nch, int G) {
+  uint8_t* p = (uint8_t*)ws;
+  AttWs w;
+  w.ticket = (uint32_t*)p;
+  p += align256(sizeof(uint32_t) * rows);
+  w.part_o = (float*)p;
+  p += align256(sizeof(float) * rows * nch * G * kD);
+  w.part_ml = (float2*)p;
+  return w;
+}
+
 size_t attend_workspace_bytes(const Dims& s, int64_t max_count) {
   int64_t nch = attend_chunks(max_count);
   int64_t rows = (int64_t)s.B * s.Hkv;
-  return align256(sizeof(float) * rows * nch * s.G * kD) + align256(sizeof(float2) * rows * nch * s.G);
+  return align256(sizeof(uint32_t) * rows) + align256(sizeof(float) * rows * nch * s.G * kD) +
+         align256(sizeof(float2) * rows * nch * s.G);
 }
 
 template <int G>
 __global__ void __launch_bounds__(128)
-attend_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ K,
-                      const uint16_t* __restrict__ V, const int32_t* __restrict__ idx,
-                      int64_t idx_stride, const int32_t* __restrict__ count, int Hq, int Hkv,
-                      int64_t n, int64_t ncap, int max_count, float scale, int nchunks,
-                      float* __restrict__ part_o, float2* __restrict__ part_ml) {
+attend_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ K,
+              const uint16_t* __restrict__ V, const int32_t* __restrict__ idx,
+              int64_t idx_stride, const int32_t* __restrict__ count, int Hq, int Hkv, int64_t n,
+              int64_t ncap, int max_count, float scale, int nchunks, AttWs ws,
+              float* __restrict__ out, float* __restrict__ lse) {
   __shared__ __align__(16) uint16_t Ks[kAtChunk][kAtPitch];
   __shared__ __align__(16) uint16_t Vs[kAtChunk][kAtPitch];
-  __shared__ __align__(16) float qs[G][2][68];
+  __shared__ __align__(16) float qs[G][4][kQPitch];
   __shared__ float zs[G][kAtChunk];
   __shared__ float2 ml[G];
   __shared__ int valid[kAtChunk];
+  __shared__ bool last;
 
   const int64_t row = blockIdx.y;
   const int b = (int)(row / Hkv), h = (int)(row % Hkv);
   const int c = min(count[row], max_count);
+  const int t = threadIdx.x;
   const int t0 = blockIdx.x * kAtChunk;
+  if (c <= 0) {  // empty set: o = 0, lse = -inf, written once per row
+    if (blockIdx.x == 0) {
+      for (int g = 0; g < G; ++g) {
+        const int64_t bq = (int64_t)b * Hq + h * G + g;
+        out[bq * kD + t] = 0.0f;
+        if (lse && t == 0) lse[bq] = -INFINITY;
+      }
+    }
+    return;
+  }
   if (t0 >= c) return;
   const int nt = min(kAtChunk, c - t0);
-  const int t = threadIdx.x;
+  const int nch_row = (c + kAtChunk - 1) / kAtChunk;
 
   for (int e = t; e < G * kD; e += 128) {
-    int g = e / kD, j = e % kD;
-    qs[g][j >> 6][j & 63] = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]);
+    const int g = e / kD, j = e % kD;
+    qs[g][j >> 5][j & 31] = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]);
   }
   if (t < kAtChunk) {
     int ok = 0;
     if (t < nt) {
-      int tok = idx[row * idx_stride + t0 + t];
+      const int tok = idx[row * idx_stride + t0 + t];
       ok = (tok >= 0 && tok < n) ? tok + 1 : 0;  // out-of-range indices are skipped
     }
     valid[t] = ok;
@@ -70,10 +102,10 @@ attend_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
   const uint16_t* Kr = K + row * ncap * kD;
   const uint16_t* Vr = V + row * ncap * kD;
   for (int e = t; e < nt * 16; e += 128) {
-    int r = e >> 4, seg = e & 15;
-    int ok = valid[r];
+    const int r = e >> 4, seg = e & 15;
+    const int ok = valid[r];
     if (ok) {
-      int64_t tok = ok - 1;
+      const int64_t tok = ok - 1;
       cp_async16(&Ks[r][seg * 8], Kr + tok * kD + seg * 8);
       cp_async16(&Vs[r][seg * 8], Vr + tok * kD + seg * 8);
     }
@@ -81,22 +113,23 @@ attend_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
   cp_async_wait_all();
   __syncthreads();
 
-  // z for token tt, split over two threads by halves of d
+  // z for token tt, split over four threads by quarters of d
   {
-    const int tt = t >> 1, half = t & 1;
+    const int tt = t >> 2, qq = t & 3;
     float dot[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) dot[g] = 0.0f;
-    if (tt < nt && valid[tt]) {
+    const bool ok = tt < nt && valid[tt];
+    if (ok) {
 #pragma unroll
-      for (int c8 = 0; c8 < 64; c8 += 8) {
-        uint4 kv = *reinterpret_cast<const uint4*>(&Ks[tt][half * 64 + c8]);
-        float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
-                       bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
+      for (int c8 = 0; c8 < 32; c8 += 8) {
+        const uint4 kv = *reinterpret_cast<const uint4*>(&Ks[tt][qq * 32 + c8]);
+        const float kf[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
+                             bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float4 qa = *reinterpret_cast<const float4*>(&qs[g][half][c8]);
-          float4 qb = *reinterpret_cast<const float4*>(&qs[g][half][c8 + 4]);
+          const float4 qa = *reinterpret_cast<const float4*>(&qs[g][qq][c8]);
+          const float4 qb = *reinterpret_cast<const float4*>(&qs[g][qq][c8 + 4]);
           dot[g] = fmaf(qa.x, kf[0], dot[g]);
           dot[g] = fmaf(qa.y, kf[1], dot[g]);
           dot[g] = fmaf(qa.z, kf[2], dot[g]);
@@ -109,27 +142,27 @@ attend_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
       }
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) dot[g] += __shfl_xor_sync(0xFFFFFFFFu, dot[g], 1);
-    if (half == 0) {
-      const bool ok = tt < nt && valid[tt];
+    for (int g = 0; g < G; ++g) {
+      dot[g] += __shfl_xor_sync(0xFFFFFFFFu, dot[g], 1);
+      dot[g] += __shfl_xor_sync(0xFFFFFFFFu, dot[g], 2);
+    }
+    if (qq == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g) zs[g][tt] = ok ? dot[g] * scale : -INFINITY;
     }
   }
   __syncthreads();
-  // per-head chunk max and exponentials
+  // per-head chunk max and exponentials: warp w handles heads w, w + 4
   {
     const int warp = t >> 5, lane = t & 31;
     for (int g = warp; g < G; g += 4) {
-      float z0 = zs[g][lane], z1 = zs[g][lane + 32];
-      float m = fmaxf(z0, z1);
+      const float z = zs[g][lane];
+      float m = z;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      float p0 = z0 == -INFINITY ? 0.0f : expf(z0 - m);
-      float p1 = z1 == -INFINITY ? 0.0f : expf(z1 - m);
-      zs[g][lane] = p0;
-      zs[g][lane + 32] = p1;
-      float l = p0 + p1;
+      const float p = z == -INFINITY ? 0.0f : expf(z - m);
+      zs[g][lane] = p;
+      float l = p;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
       if (lane == 0) ml[g] = make_float2(m, l);
@@ -141,46 +174,38 @@ attend_partial_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
 #pragma unroll
   for (int g = 0; g < G; ++g) acc[g] = 0.0f;
   for (int r = 0; r < nt; ++r) {
-    if (!valid[r]) continue;
-    float v = bf16_to_f32(Vs[r][t]);
+    if (!valid[r]) continue;  // skipped rows were not staged
+    const float v = bf16_to_f32(Vs[r][t]);
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = fmaf(zs[g][r], v, acc[g]);
   }
   const int64_t pbase = (row * nchunks + blockIdx.x) * G;
 #pragma unroll
-  for (int g = 0; g < G; ++g) part_o[(pbase + g) * kD + t] = acc[g];
-  if (t < G) part_ml[pbase + t] = ml[t];
-}
+  for (int g = 0; g < G; ++g) ws.part_o[(pbase + g) * kD + t] = acc[g];
+  if (t < G) ws.part_ml[pbase + t] = ml[t];
 
-template <int G>
-__global__ void __launch_bounds__(128)
-attend_combine_kernel(const int32_t* __restrict__ count, int Hq, int Hkv, int max_count,
-                      int nchunks, const float* __restrict__ part_o,
-                      const float2* __restrict__ part_ml, float* __restrict__ out,
-                      float* __restrict__ lse) {
-  const int64_t bq = blockIdx.x;  // b * Hq + query head
-  const int b = (int)(bq / Hq), hq = (int)(bq % Hq);
-  const int64_t row = (int64_t)b * Hkv + hq / G;
-  const int g = hq % G;
-  const int c = min(count[row], max_count);
-  const int nch = (c + kAtChunk - 1) / kAtChunk;
-  const int t = threadIdx.x;
-  if (c <= 0) {
-    out[bq * kD + t] = 0.0f;
-    if (lse && t == 0) lse[bq] = -INFINITY;
-    return;
+  // the last CTA of the row merges the partials in chunk order
+  __threadfence();
+  __syncthreads();
+  if (t == 0) last = atomicAdd(&ws.ticket[row], 1u) == (uint32_t)(nch_row - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int64_t rbase = row * nchunks * G;
+  for (int g = 0; g < G; ++g) {
+    float m = -INFINITY;
+    for (int ch = 0; ch < nch_row; ++ch) m = fmaxf(m, __ldcg(&ws.part_ml[rbase + ch * G + g].x));
+    float l = 0.0f, o = 0.0f;
+    for (int ch = 0; ch < nch_row; ++ch) {
+      const float2 p = __ldcg(&ws.part_ml[rbase + ch * G + g]);
+      const float wgt = p.x == -INFINITY ? 0.0f : expf(p.x - m);
+      l = fmaf(p.y, wgt, l);
+      o = fmaf(__ldcg(&ws.part_o[(rbase + ch * G + g) * kD + t]), wgt, o);
+    }
+    const int64_t bq = (int64_t)b * Hq + h * G + g;
+    out[bq * kD + t] = l > 0.0f ? o / l : 0.0f;
+    if (lse && t == 0) lse[bq] = l > 0.0f ? m + logf(l) : -INFINITY;
   }
-  float m = -INFINITY;
-  for (int ch = 0; ch < nch; ++ch) m = fmaxf(m, part_ml[(row * nchunks + ch) * G + g].x);
-  float l = 0.0f, o = 0.0f;
-  for (int ch = 0; ch < nch; ++ch) {
-    float2 p = part_ml[(row * nchunks + ch) * G + g];
-    float w = p.x == -INFINITY ? 0.0f : expf(p.x - m);
-    l = fmaf(p.y, w, l);
-    o = fmaf(part_o[((row * nchunks + ch) * G + g) * kD + t], w, o);
-  }
-  out[bq * kD + t] = l > 0.0f ? o / l : 0.0f;
-  if (lse && t == 0) lse[bq] = l > 0.0f ? m + logf(l) : -INFINITY;
 }
 
 template <int G>
@@ -190,19 +215,14 @@ static int attend_t(const Dims& s, const uint16_t* q, const uint16_t* K, const u
                     cudaStream_t st) {
   const int64_t rows = (int64_t)s.B * s.Hkv;
   const int nch = (int)attend_chunks(max_count);
-  float* part_o = (float*)ws;
-  float2* part_ml = (float2*)((uint8_t*)ws + align256(sizeof(float) * rows * nch * G * kD));
-  if (nch > 0) {
-    dim3 grid((unsigned)nch, (unsigned)rows);
-    attend_partial_kernel<G><<<grid, 128, 0, st>>>(q, K, V, idx, idx_stride, count, s.Hq, s.Hkv,
-                                                   s.n, s.ncap, (int)max_count, scale, nch,
-                                                   part_o, part_ml);
-    int rc = check_launch("attend_partial");
-    if (rc) return rc;
-  }
-  attend_combine_kernel<G><<<(unsigned)(s.B * s.Hq), 128, 0, st>>>(
-      count, s.Hq, s.Hkv, (int)max_count, nch, part_o, part_ml, out, lse);
-  return check_launch("attend_combine");
+  AttWs w = carve_att(ws, rows, nch, G);
+  if (cudaMemsetAsync(w.ticket, 0, sizeof(uint32_t) * rows, st) != cudaSuccess)
+    return check_launch("attend: ticket clear");
+  dim3 grid((unsigned)(nch > 0 ? nch : 1), (unsigned)rows);
+  attend_kernel<G><<<grid, 128, 0, st>>>(q, K, V, idx, idx_stride, count, s.Hq, s.Hkv, s.n,
+                                         s.ncap, (int)max_count, scale, nch > 0 ? nch : 1, w,
+                                         out, lse);
+  return check_launch("attend");
 }
 
 int launch_gather_attend(const Dims& s, const uint16_t* q, const uint16_t* K, const uint16_t* V,

@@ -9,9 +9,9 @@
 //
 // The array is a module global: every GPU that loads libsd holds its
 // kNoallocScratchBytes until the process exits, and every call on a GPU shares
-// that GPU's copy.  The array keeps the previous call's contents; the kernels
-// write every partial before they read it, so nothing needs clearing between
-// calls.  Calls whose work overlaps on the GPU (different streams without
+// that GPU's copy.  The array keeps the previous call's contents; every call
+// first clears the per-row counters that must start at zero (with a memset on the
+// caller's stream), and the kernels write every partial before they read it.  Calls whose work overlaps on the GPU (different streams without
 // ordering, or host threads) race on the array.
 #include <mutex>
 

@@ -80,153 +80,286 @@ int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsi
 //   sum_j W'_j * (prefix_ij + h(t_j) - 8)
 //     = C_blk + sum over active planes (j, p < t_j) of (W'_j * 2^(3-p)) * bit_jpi,
 //   C_blk = sum_j W'_j * (h(t_j) - 8),  h(t) = 2^(3-t) (t < 4), 0 (t = 4).
-// So each active plane costs one bit test and one predicated add per token.
-// A CTA scores 2048 tokens (64 words per plane, 32 scale blocks) of one
-// (sequence, KV head); planes are staged 32 at a time in shared memory.
-// Warp w owns words 8w..8w+7 and lane l owns bit l of each.
+// So each planned plane costs one bit test and one predicated add per token --
+// the in-HBM scan is bound by these operations, as the Fathom page notes.
+//
+// A CTA scores tiles of 4096 tokens (128 words per plane, 64 scale blocks) of one
+// (sequence, KV head); the grid is persistent (3 CTAs per SM), each CTA taking a
+// contiguous range of tiles so the per-row prologue (group-summed query, active
+// plane list) is paid once per row change.  Per tile: the active channels' scales
+// are staged once; planes are staged 32 at a time with cp.async into a double
+// buffer while the previous 32 are consumed; folded weights are built per stage.
+// Warp w owns words 16w..16w+15 (blocks 8w..8w+7); lane l owns bit l of each.
 // =====================================================================================
-constexpr int kPsTile = 2048;
-constexpr int kPsWords = kPsTile / 32;   // 64
-constexpr int kPsBlocks = kPsTile / 64;  // 32
-constexpr int kPsChunk = 32;
+constexpr int kPsTile = 4096;
+constexpr int kPsWords = kPsTile / 32;   // 128
+constexpr int kPsBlocks = kPsTile / 64;  // 64
+constexpr int kPsChunk = 32;             // planes per stage
+constexpr int kPsThreads = 256;
+constexpr int kPsCtasPerSm = 3;
 
-template <int G>
-__global__ void __launch_bounds__(256)
+struct PsSmem {
+  uint32_t words[2][kPsChunk][kPsWords];  // 32 KB
+  float Wt[2][kPsChunk][kPsBlocks];       // 16 KB
+  uint16_t sc[kD][kPsBlocks];             // 16 KB: scales of the active channels (by slot)
+  float red[4][kPsBlocks];
+  float Cs[kPsBlocks];
+  float qt[kD];
+  float offs[kD];                         // h(t) - 8 per slot
+  int tb[kD];
+  int slot_of[kD];
+  int chan[kD];                           // channel of each slot
+  uint16_t act[4 * kD];                   // active entries j * 4 + p, j ascending
+  int nact, nch;
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  unsigned d = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  unsigned d = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// Issues the copies of planes [e0, e0 + ne) of the tile into words[buf].
+template <bool A16>
+__device__ __forceinline__ void ps_stage_words(PsSmem& S, int buf, int e0, int ne,
+                                               const uint32_t* pl_tile, int64_t wstride,
+                                               int nwv) {
+  if (A16) {
+    // whole 16-byte segments inside the valid words, then an 8-byte remainder
+    // (nwv is even): no copy reads past the last valid word of a plane row
+    for (int x = threadIdx.x; x < ne * (kPsWords / 4); x += kPsThreads) {
+      const int e = x / (kPsWords / 4), seg = x % (kPsWords / 4);
+      const uint32_t* src = pl_tile + (int64_t)S.act[e0 + e] * wstride + seg * 4;
+      if (seg * 4 + 4 <= nwv)
+        cp_async16(&S.words[buf][e][seg * 4], src);
+      else if (seg * 4 + 2 == nwv)
+        cp_async8(&S.words[buf][e][seg * 4], src);
+    }
+  } else {
+    for (int x = threadIdx.x; x < ne * (kPsWords / 2); x += kPsThreads) {
+      const int e = x / (kPsWords / 2), seg = x % (kPsWords / 2);
+      if (seg * 2 < nwv)
+        cp_async8(&S.words[buf][e][seg * 2], pl_tile + (int64_t)S.act[e0 + e] * wstride + seg * 2);
+    }
+  }
+  cp_async_commit();
+}
+
+// Folded weights of planes [e0, e0 + ne): Wt = (q~_j * s_j,blk) * 2^(3-p).
+__device__ __forceinline__ void ps_weights(PsSmem& S, int buf, int e0, int ne, int nbv) {
+  for (int x = threadIdx.x; x < ne * kPsBlocks; x += kPsThreads) {
+    const int e = x / kPsBlocks, blk = x % kPsBlocks;
+    const int ent = S.act[e0 + e];
+    const int j = ent >> 2, p = ent & 3;
+    float wv = 0.0f;
+    if (blk < nbv) {
+      const float sv = __half2float(__ushort_as_half(S.sc[S.slot_of[j]][blk]));
+      wv = __fmul_rn(__fmul_rn(S.qt[j], sv), (float)(8 >> p));
+    }
+    S.Wt[buf][e][blk] = wv;
+  }
+}
+
+template <int G, bool A16>
+__global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm)
 score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
                     const uint8_t* __restrict__ plan, const uint16_t* __restrict__ q, int Hq,
-                    int Hkv, int64_t n, int64_t ncap, float* __restrict__ scores) {
-  __shared__ float qt[kD];
-  __shared__ int tb[kD];
-  __shared__ uint16_t act[4 * kD];
-  __shared__ int nact_s;
-  __shared__ float Cs[kPsBlocks];
-  __shared__ __align__(16) uint32_t words[kPsChunk][kPsWords];
-  __shared__ __align__(16) float Ws[kPsChunk][kPsBlocks];
-
-  const int64_t bh = blockIdx.y;
-  const int b = (int)(bh / Hkv), h = (int)(bh % Hkv);
-  const int64_t tok0 = (int64_t)blockIdx.x * kPsTile;
-  const int nwv = (int)imin64(kPsWords, (n - tok0) / 32);  // valid words
-  const int nbv = nwv / 2;                                        // valid blocks
+                    int Hkv, int64_t n, int64_t ncap, int64_t tiles_per_row, int64_t total_tiles,
+                    float* __restrict__ scores) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  PsSmem& S = *reinterpret_cast<PsSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lanemask = 1u << lane;
   const int64_t wstride = ncap / 32, sstride = ncap / 64;
-  const uint16_t* sc_bh = scales + bh * kD * sstride + tok0 / 64;
+  const int64_t t_begin = (int64_t)blockIdx.x * total_tiles / gridDim.x;
+  const int64_t t_end = (int64_t)(blockIdx.x + 1) * total_tiles / gridDim.x;
+  int64_t cur_bh = -1;
 
-  if (threadIdx.x < kD) {
-    const int j = threadIdx.x;
-    float acc = 0.0f;
+  for (int64_t tile = t_begin; tile < t_end; ++tile) {
+    const int64_t bh = tile / tiles_per_row;
+    const int64_t tok0 = (tile % tiles_per_row) * kPsTile;
+    if (bh != cur_bh) {  // per-row prologue
+      cur_bh = bh;
+      const int b = (int)(bh / Hkv), h = (int)(bh % Hkv);
+      if (threadIdx.x < kD) {
+        const int j = threadIdx.x;
+        float acc = 0.0f;
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      acc = __fadd_rn(acc, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]));
-    qt[j] = acc;
-    tb[j] = min((int)plan[bh * kD + j], 4);  // a plan holds 0..4 bits per channel
-  }
-  __syncthreads();
-  // active plane list (j ascending, p ascending) by a warp scan over channels
-  if (warp == 0) {
-    int c[4], tot = 0;
+        for (int g = 0; g < G; ++g)
+          acc = __fadd_rn(acc, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]));
+        S.qt[j] = acc;
+        S.tb[j] = min((int)plan[bh * kD + j], 4);  // a plan holds 0..4 bits per channel
+      }
+      __syncthreads();
+      if (warp == 0) {  // active entries and channel slots, j ascending
+        int c[4], tot = 0, chs = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) { c[k] = tb[lane * 4 + k]; tot += c[k]; }
-    int incl = tot;
+        for (int k = 0; k < 4; ++k) {
+          c[k] = S.tb[lane * 4 + k];
+          tot += c[k];
+          chs += c[k] > 0;
+        }
+        int incl = tot, inclc = chs;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-      if (lane >= off) incl += y;
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          const int yc = __shfl_up_sync(0xFFFFFFFFu, inclc, off);
+          if (lane >= off) { incl += y; inclc += yc; }
+        }
+        int pos = incl - tot, slot = inclc - chs;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = lane * 4 + k;
+          for (int p = 0; p < c[k]; ++p) S.act[pos++] = (uint16_t)(j * 4 + p);
+          if (c[k] > 0) {
+            S.slot_of[j] = slot;
+            S.chan[slot] = j;
+            S.offs[slot] = c[k] < 4 ? (float)((1 << (3 - c[k])) - 8) : -8.0f;
+            ++slot;
+          } else {
+            S.slot_of[j] = 0;
+          }
+        }
+        if (lane == 31) { S.nact = incl; S.nch = inclc; }
+      }
+      __syncthreads();
     }
-    int pos = incl - tot;
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      for (int p = 0; p < c[k]; ++p) act[pos++] = (uint16_t)((lane * 4 + k) * 4 + p);
-    if (lane == 31) nact_s = incl;
-  }
-  // per-block constants: warp w handles blocks 4w..4w+3
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int blk = warp * 4 + k;
-    float part = 0.0f;
-    if (blk < nbv) {
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int j = lane + 32 * jj;
-        const int t = tb[j];
-        if (t > 0) {
-          float s = __half2float(__ushort_as_half(sc_bh[j * sstride + blk]));
-          float wp = __fmul_rn(qt[j], s);
-          float off = t < 4 ? (float)((1 << (3 - t)) - 8) : -8.0f;
-          part = __fadd_rn(part, __fmul_rn(wp, off));
+    const int nact = S.nact, nch = S.nch;
+    const int nwv = (int)imin64(kPsWords, (n - tok0) / 32);  // valid words (even)
+    const int nbv = nwv / 2;                                  // valid scale blocks
+    const uint32_t* pl_tile = planes + bh * kD * 4 * wstride + tok0 / 32;
+    const uint16_t* sc_tile = scales + bh * kD * sstride + tok0 / 64;
+
+    // stage the active channels' scales and the first chunk of planes
+    if (A16) {
+      // whole 16-byte segments (8 blocks) inside the valid blocks, the rest singly
+      for (int x = threadIdx.x; x < nch * 8; x += kPsThreads) {
+        const int sl = x >> 3, seg = x & 7;
+        const uint16_t* src = sc_tile + (int64_t)S.chan[sl] * sstride + seg * 8;
+        if (seg * 8 + 8 <= nbv) {
+          cp_async16(&S.sc[sl][seg * 8], src);
+        } else {
+          for (int k = 0; seg * 8 + k < nbv; ++k) S.sc[sl][seg * 8 + k] = src[k];
         }
       }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xFFFFFFFFu, part, o));
-    if (lane == 0) Cs[blk] = part;
-  }
-  __syncthreads();
-
-  float acc[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-  const uint32_t lanemask = 1u << lane;
-  const int nact = nact_s;
-  const uint32_t* pl_bh = planes + bh * kD * 4 * wstride + tok0 / 32;
-
-  for (int e0 = 0; e0 < nact; e0 += kPsChunk) {
-    const int ne = min(kPsChunk, nact - e0);
-    // stage the chunk's words (8-byte loads) and folded weights
-    for (int x = threadIdx.x; x < ne * (kPsWords / 2); x += 256) {
-      const int e = x / (kPsWords / 2), seg = x % (kPsWords / 2);
-      const int ent = act[e0 + e];
-      uint2 v = make_uint2(0u, 0u);
-      if (seg * 2 < nwv)
-        v = __ldg(reinterpret_cast<const uint2*>(pl_bh + (int64_t)ent * wstride) + seg);
-      *reinterpret_cast<uint2*>(&words[e][seg * 2]) = v;
-    }
-    for (int x = threadIdx.x; x < ne * kPsBlocks; x += 256) {
-      const int e = x / kPsBlocks, blk = x % kPsBlocks;
-      const int ent = act[e0 + e];
-      const int j = ent >> 2, p = ent & 3;
-      float wv = 0.0f;
-      if (blk < nbv) {
-        float s = __half2float(__ushort_as_half(sc_bh[j * sstride + blk]));
-        wv = __fmul_rn(__fmul_rn(qt[j], s), (float)(8 >> p));
+    } else {
+      for (int x = threadIdx.x; x < nch * kPsBlocks; x += kPsThreads) {
+        const int sl = x / kPsBlocks, blk = x % kPsBlocks;
+        if (blk < nbv) S.sc[sl][blk] = sc_tile[(int64_t)S.chan[sl] * sstride + blk];
       }
-      Ws[e][blk] = wv;
     }
+    const int ne0 = min(kPsChunk, nact);
+    ps_stage_words<A16>(S, 0, 0, ne0, pl_tile, wstride, nwv);
+    cp_async_wait_all();
     __syncthreads();
-#pragma unroll 2
-    for (int e = 0; e < ne; ++e) {
-      const uint4 wa = *reinterpret_cast<const uint4*>(&words[e][warp * 8]);
-      const uint4 wb = *reinterpret_cast<const uint4*>(&words[e][warp * 8 + 4]);
-      const float4 wt = *reinterpret_cast<const float4*>(&Ws[e][warp * 4]);
-      if (wa.x & lanemask) acc[0] += wt.x;
-      if (wa.y & lanemask) acc[1] += wt.x;
-      if (wa.z & lanemask) acc[2] += wt.y;
-      if (wa.w & lanemask) acc[3] += wt.y;
-      if (wb.x & lanemask) acc[4] += wt.z;
-      if (wb.y & lanemask) acc[5] += wt.z;
-      if (wb.z & lanemask) acc[6] += wt.w;
-      if (wb.w & lanemask) acc[7] += wt.w;
+    // per-block constants C_blk (four partial sums per block) and the first weights
+    {
+      const int blk = threadIdx.x & (kPsBlocks - 1), part = threadIdx.x >> 6;
+      float acc = 0.0f;
+      if (blk < nbv)
+        for (int sl = part; sl < nch; sl += 4) {
+          const float sv = __half2float(__ushort_as_half(S.sc[sl][blk]));
+          acc = __fadd_rn(acc, __fmul_rn(__fmul_rn(S.qt[S.chan[sl]], sv), S.offs[sl]));
+        }
+      S.red[part][blk] = acc;
     }
+    ps_weights(S, 0, 0, ne0, nbv);
     __syncthreads();
-  }
-  float* orow = scores + bh * n + tok0;
+    if (threadIdx.x < kPsBlocks)
+      S.Cs[threadIdx.x] = __fadd_rn(__fadd_rn(S.red[0][threadIdx.x], S.red[1][threadIdx.x]),
+                                    __fadd_rn(S.red[2][threadIdx.x], S.red[3][threadIdx.x]));
+
+    float acc[16];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int w = warp * 8 + k;
-    if (w < nwv) orow[w * 32 + lane] = acc[k] + Cs[w >> 1];
+    for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+    for (int e0 = 0, buf = 0; e0 < nact; e0 += kPsChunk, buf ^= 1) {
+      const int ne = min(kPsChunk, nact - e0);
+      const int e1 = e0 + kPsChunk;
+      const int ne1 = min(kPsChunk, nact - e1);
+      if (ne1 > 0) ps_stage_words<A16>(S, buf ^ 1, e1, ne1, pl_tile, wstride, nwv);
+#pragma unroll 2
+      for (int e = 0; e < ne; ++e) {
+        const uint4 a = *reinterpret_cast<const uint4*>(&S.words[buf][e][warp * 16]);
+        const uint4 b = *reinterpret_cast<const uint4*>(&S.words[buf][e][warp * 16 + 4]);
+        const uint4 c = *reinterpret_cast<const uint4*>(&S.words[buf][e][warp * 16 + 8]);
+        const uint4 d = *reinterpret_cast<const uint4*>(&S.words[buf][e][warp * 16 + 12]);
+        const float4 wa = *reinterpret_cast<const float4*>(&S.Wt[buf][e][warp * 8]);
+        const float4 wb = *reinterpret_cast<const float4*>(&S.Wt[buf][e][warp * 8 + 4]);
+        if (a.x & lanemask) acc[0] += wa.x;
+        if (a.y & lanemask) acc[1] += wa.x;
+        if (a.z & lanemask) acc[2] += wa.y;
+        if (a.w & lanemask) acc[3] += wa.y;
+        if (b.x & lanemask) acc[4] += wa.z;
+        if (b.y & lanemask) acc[5] += wa.z;
+        if (b.z & lanemask) acc[6] += wa.w;
+        if (b.w & lanemask) acc[7] += wa.w;
+        if (c.x & lanemask) acc[8] += wb.x;
+        if (c.y & lanemask) acc[9] += wb.x;
+        if (c.z & lanemask) acc[10] += wb.y;
+        if (c.w & lanemask) acc[11] += wb.y;
+        if (d.x & lanemask) acc[12] += wb.z;
+        if (d.y & lanemask) acc[13] += wb.z;
+        if (d.z & lanemask) acc[14] += wb.w;
+        if (d.w & lanemask) acc[15] += wb.w;
+      }
+      if (ne1 > 0) ps_weights(S, buf ^ 1, e1, ne1, nbv);
+      cp_async_wait_all();
+      __syncthreads();
+    }
+    if (nact == 0) __syncthreads();  // Cs written above must be visible
+    float* orow = scores + bh * n + tok0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int w = warp * 16 + k;
+      if (w < nwv) orow[w * 32 + lane] = acc[k] + S.Cs[w >> 1];
+    }
+    __syncthreads();  // buffers are reused by the next tile
   }
+}
+
+static int sm_count() {
+  static int cnt[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (!cnt[dev]) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+      c = 152;
+    cnt[dev] = c;
+  }
+  return cnt[dev];
+}
+
+template <int G, bool A16>
+static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scales,
+                    const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st) {
+  auto kern = score_planes_kernel<G, A16>;
+  if (int rc = set_smem_limit((const void*)kern, sizeof(PsSmem), "score_planes: smem attribute"))
+    return rc;
+  const int64_t tiles_per_row = (s.n + kPsTile - 1) / kPsTile;
+  const int64_t total = tiles_per_row * s.B * s.Hkv;
+  const int64_t grid = imin64(total, (int64_t)sm_count() * kPsCtasPerSm);
+  kern<<<(unsigned)grid, kPsThreads, sizeof(PsSmem), st>>>(planes, scales, plan, q, s.Hq, s.Hkv,
+                                                          s.n, s.ncap, tiles_per_row, total,
+                                                          scores);
+  return check_launch("score_planes");
 }
 
 int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
                         const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st) {
-  dim3 grid((unsigned)((s.n + kPsTile - 1) / kPsTile), (unsigned)(s.B * s.Hkv));
+  const bool a16 = (s.ncap % 512 == 0) && ((uintptr_t)planes % 16 == 0) &&
+                   ((uintptr_t)scales % 16 == 0);
   switch (s.G) {
-    case 1: score_planes_kernel<1><<<grid, 256, 0, st>>>(planes, scales, plan, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
-    case 2: score_planes_kernel<2><<<grid, 256, 0, st>>>(planes, scales, plan, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
-    case 4: score_planes_kernel<4><<<grid, 256, 0, st>>>(planes, scales, plan, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
-    default: score_planes_kernel<8><<<grid, 256, 0, st>>>(planes, scales, plan, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
+    case 1: return a16 ? planes_t<1, true>(s, planes, scales, plan, q, scores, st) : planes_t<1, false>(s, planes, scales, plan, q, scores, st);
+    case 2: return a16 ? planes_t<2, true>(s, planes, scales, plan, q, scores, st) : planes_t<2, false>(s, planes, scales, plan, q, scores, st);
+    case 4: return a16 ? planes_t<4, true>(s, planes, scales, plan, q, scores, st) : planes_t<4, false>(s, planes, scales, plan, q, scores, st);
+    default: return a16 ? planes_t<8, true>(s, planes, scales, plan, q, scores, st) : planes_t<8, false>(s, planes, scales, plan, q, scores, st);
   }
-  return check_launch("score_planes");
 }
 
 // =====================================================================================

@@ -3,52 +3,47 @@
 //   3.1 (first and last tokens always kept, budget counted apart);
 //   OasisKV: ..., method details (top-K blocks plus the active local block).
 //
-// Order: score descending, unit ascending.  Each candidate u in [lead, tail)
+// Order: score descending, unit ascending.  Within a set of candidates, unit u
 // gets a unique 64-bit composite key
 //     C(u) = (key(u) - kmin) << bI  |  (M - 1 - (u - lead))
-// (key = order-preserving 32-bit image of the score, kmin its row minimum,
-// M = tail - lead candidates, bI = bits of M - 1), so "top-k by C" is exactly
-// the required order with no ties left.  Rows of up to kSmallRow units are
-// selected by one CTA in shared memory.  Longer rows:
-//   1. row min/max of the keys (multi-CTA);
-//   2. one 11-bit histogram pass over the top digit of C (multi-CTA; the
-//      last CTA of a row picks the digit holding the k-th largest);
-//   3. compaction: units with a larger digit go to an "above" list (< k of
-//      them), units with that digit to a candidate list;
-//   4. one CTA per row finishes the radix select among the candidates in
-//      shared memory, merges with the above list, sorts ascending and writes
-//      the forced and selected units expanded to tokens.
-// If the chosen digit holds more than kCap candidates (only for rows with
-// enormous runs of near-equal scores), step 4 resolves the remaining digits
-// by passes over the row in global memory: slower, same result.
+// (key = order-preserving 32-bit image of the score, kmin the candidates' minimum,
+// M = tail - lead candidates, bI = bits of M - 1), so "top-k by C" is exactly the
+// required order with no ties left, and a radix select over C needs no tie pass.
+// Rows of up to kSmallRow units are selected by one CTA in shared memory.
+// Longer rows take three kernels:
+//   1. sample: one CTA per row reads an evenly spaced sample of up to 16K keys
+//      and takes T_est = its r-th largest key, r = mu + 5 sqrt(mu) + 2 with
+//      mu = k * sample / M the expected number of top-k members in the sample;
+//   2. filter: one pass over the row appends (key, unit) of every key >= T_est
+//      to the row's candidate list (warp-aggregated atomics);
+//   3. finish: one CTA per row selects the top k of the candidates by C in
+//      shared memory, sorts them ascending and writes the forced and selected
+//      units expanded to tokens.
+// The result is exact whatever the sample: if at least k keys are >= T_est, every
+// member of the top k (and every key tied with the k-th) is a candidate.  When
+// the estimate misses (fewer than k, or more than kCap candidates) the finishing
+// CTA selects over the whole row itself: slower, same result.
 #include "sd_internal.cuh"
 
 namespace sd {
 
 constexpr int kCap = 8192;          // candidates a finishing CTA holds in shared memory
-constexpr int kFinThreads = 1024;
+constexpr int kFinThreads = 256;
 constexpr int kChunk = 8192;        // units per CTA in the multi-CTA steps
 constexpr int kDigit = 11;
 constexpr int kBins = 1 << kDigit;
 
-struct RowState {
-  uint32_t inv_min;  // ~(row min key), via atomicMax (zero-initialised)
-  uint32_t max_key;  // row max key, via atomicMax
-  uint32_t nan;      // a NaN was seen
-  uint32_t ticket;   // CTAs done with the histogram pass
-  uint32_t digit;    // chosen top digit
-  uint32_t need;     // how many of the digit's units to take
-  uint32_t bucket;   // units with that digit
-  uint32_t nabove;   // units with a larger digit (compaction counter)
-  uint32_t ncand;    // compaction counter of the candidate list
-  uint32_t pad[7];
-  uint32_t hist[kBins];
+struct RowState {   // written by the sample CTA before the filter reads it
+  uint32_t nan;      // a NaN was seen (sample or filter)
+  uint32_t thresh;   // estimate (T_key, i_max): unit u = lead + i is a candidate iff
+  uint32_t imax;     //   key > T_key, or key == T_key and i <= i_max
+  uint32_t ncand;    // candidates appended by the filter (may exceed kCap)
+  uint32_t pad[12];
 };
 
 struct Ws {
   RowState* st;      // [rows]
-  uint32_t* above;   // [rows][kMaxTopK]
-  uint64_t* cand;    // [rows][kCap]
+  uint64_t* cand;    // [rows][kCap]: (key << 32) | unit
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -58,16 +53,13 @@ static Ws carve(void* base, int64_t rows) {
   Ws w;
   w.st = (RowState*)p;
   p += align256(sizeof(RowState) * rows);
-  w.above = (uint32_t*)p;
-  p += align256(sizeof(uint32_t) * kMaxTopK * rows);
   w.cand = (uint64_t*)p;
   return w;
 }
 
 size_t topk_workspace_bytes(int64_t rows, int64_t n_units, const sd_select&) {
   if (n_units <= kSmallRow) return 0;
-  return align256(sizeof(RowState) * rows) + align256(sizeof(uint32_t) * kMaxTopK * rows) +
-         align256(sizeof(uint64_t) * kCap * rows);
+  return align256(sizeof(RowState) * rows) + align256(sizeof(uint64_t) * kCap * rows);
 }
 
 struct Geo {  // per-row candidate geometry
@@ -155,20 +147,107 @@ __device__ void bitonic_sort_u32(uint32_t* a, int n2) {
   }
 }
 
+// hist[bin] += 1 for every lane with `in`, one shared-memory atomic per distinct
+// bin per warp (score distributions crowd a few bins; this avoids serialising
+// on them).  All 32 lanes must call it.
+__device__ __forceinline__ void hist_add(uint32_t* hist, bool in, uint32_t bin) {
+  const uint32_t act = __ballot_sync(0xFFFFFFFFu, in);
+  if (!act) return;
+  const uint32_t peers = __match_any_sync(0xFFFFFFFFu, in ? bin : 0xFFFFFFFFu) & act;
+  const int lane = threadIdx.x & 31;
+  if (in && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
+// Sorts the nsel distinct units sel[0..nsel) (all < 2^ubits) ascending: a counting
+// sort on the top 10 bits (1024 buckets), then each bucket -- usually 0 to 2
+// units -- sorted by one thread.  tmp holds >= 2048 words, out >= nsel words.
+template <int NT>
+__device__ void sort_units(uint32_t* sel, int nsel, int ubits, uint32_t* tmp, uint32_t* out) {
+  constexpr int kB = 1024;
+  const int shift = ubits > 10 ? ubits - 10 : 0;
+  uint32_t* cnt = tmp;         // [kB] counts, then running cursors
+  uint32_t* start = tmp + kB;  // [kB] bucket starts
+  __shared__ uint32_t wsum[NT / 32];
+  for (int b = threadIdx.x; b < kB; b += NT) cnt[b] = 0;
+  __syncthreads();
+  for (int e = threadIdx.x; e < nsel; e += NT) atomicAdd(&cnt[sel[e] >> shift], 1u);
+  __syncthreads();
+  // exclusive scan of cnt into start: each thread owns kB / NT consecutive buckets
+  constexpr int PER = kB / NT;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t loc[PER], tot = 0, most = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    loc[i] = cnt[threadIdx.x * PER + i];
+    tot += loc[i];
+    most = max(most, loc[i]);
+  }
+  if (__syncthreads_or(most > 32)) {  // clustered units: bitonic sort instead
+    int n2 = 1;
+    while (n2 < nsel) n2 <<= 1;
+    for (int i = nsel + threadIdx.x; i < n2; i += NT) sel[i] = 0xFFFFFFFFu;
+    __syncthreads();
+    bitonic_sort_u32<NT>(sel, n2);
+    return;
+  }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  uint32_t run = incl - tot;
+  for (int w = 0; w < warp; ++w) run += wsum[w];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    start[threadIdx.x * PER + i] = run;
+    cnt[threadIdx.x * PER + i] = run;
+    run += loc[i];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < nsel; e += NT) {
+    const uint32_t u = sel[e];
+    out[atomicAdd(&cnt[u >> shift], 1u)] = u;
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kB; b += NT) {  // cnt[b] is now the bucket's end
+    const int s0 = (int)start[b], s1 = (int)cnt[b];
+    for (int i = s0 + 1; i < s1; ++i) {  // insertion sort of a short bucket
+      const uint32_t x = out[i];
+      int j = i - 1;
+      while (j >= s0 && out[j] > x) { out[j + 1] = out[j]; --j; }
+      out[j + 1] = x;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < nsel; e += NT) sel[e] = out[e];
+  __syncthreads();
+}
+
 // Finds T such that exactly `need` of the c unique values C[0..c) are >= T,
 // given that all of them equal `prefix` in the bits above `pos`.
-template <int NT>
-__device__ uint64_t radix_threshold(const uint64_t* C, int c, uint32_t need, uint64_t prefix,
-                                    int pos, uint32_t* hist, uint32_t* scratch, uint32_t* out) {
+template <int NT, typename KT>
+__device__ uint64_t radix_threshold(const KT* C, int c, uint32_t need, uint64_t prefix,
+                                    int pos, uint32_t* hist, uint32_t* scratch, uint32_t* out,
+                                    int max_passes = 64) {
   uint32_t r = need;
-  while (pos > 0) {
+  for (int pass = 0; pos > 0 && pass < max_passes; ++pass) {
     const int w = min(kDigit, pos);
     const int npos = pos - w;
     for (int b = threadIdx.x; b < kBins; b += NT) hist[b] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < c; i += NT) {
-      uint64_t x = C[i];
-      if ((x >> pos) == prefix) atomicAdd(&hist[(uint32_t)(x >> npos) & ((1u << w) - 1)], 1u);
+    for (int i0 = 0; i0 < c; i0 += NT) {  // warp-uniform trip count for the match below
+      const int i = i0 + threadIdx.x;
+      bool in = false;
+      uint32_t bin = 0;
+      if (i < c) {
+        const uint64_t x = (uint64_t)C[i];
+        in = (x >> pos) == prefix;
+        bin = (uint32_t)(x >> npos) & ((1u << w) - 1);
+      }
+      hist_add(hist, in, bin);
     }
     __syncthreads();
     pick_digit<NT>(hist, r, scratch, out);
@@ -189,17 +268,20 @@ __device__ void write_units(const Geo& g, const uint32_t* sel, int nsel, int32_t
                             int32_t* count_row) {
   const int ntail = (int)(g.n_units - g.tail);
   const int nunits = g.lead + nsel + ntail;
-  const int64_t total = (int64_t)nunits * g.block;
-  for (int64_t p = threadIdx.x; p < total; p += NT) {
-    int ui = (int)(p / g.block), off = (int)(p % g.block);
-    int64_t u = ui < g.lead ? ui : (ui < g.lead + nsel ? (int64_t)sel[ui - g.lead]
-                                                      : (int64_t)g.tail + (ui - g.lead - nsel));
-    int64_t tok = u * g.block + off;
-    if (tok < g.n_tokens) idx_row[p] = (int32_t)tok;
+  const int blk = g.block;
+  const int total = nunits * blk;  // <= idx_stride < 2^31
+  const int ntok = (int)g.n_tokens;
+  for (int p = threadIdx.x; p < total; p += NT) {
+    const int ui = blk == 1 ? p : p / blk;
+    const int off = p - ui * blk;
+    const int u = ui < g.lead ? ui : (ui < g.lead + nsel ? (int)sel[ui - g.lead]
+                                                        : g.tail + (ui - g.lead - nsel));
+    const int tok = u * blk + off;
+    if (tok < ntok) idx_row[p] = tok;
   }
   if (threadIdx.x == 0) {
-    bool last_in = ntail > 0 || (nsel > 0 && (int64_t)sel[nsel - 1] == g.n_units - 1) ||
-                   (nsel == 0 && ntail == 0 && g.lead == g.n_units);
+    const bool last_in = ntail > 0 || (nsel > 0 && (int64_t)sel[nsel - 1] == g.n_units - 1) ||
+                         (nsel == 0 && ntail == 0 && g.lead == g.n_units);
     int64_t cnt = total;
     if (last_in) cnt -= (g.n_units * g.block - g.n_tokens);
     *count_row = (int32_t)cnt;
@@ -271,143 +353,190 @@ topk_small_kernel(const void* __restrict__ scores, Geo g, int32_t* __restrict__ 
   }
   __syncthreads();
   const int nsel = (int)S.nsel;
-  int n2 = 1;
-  while (n2 < nsel) n2 <<= 1;
-  for (int i = nsel + threadIdx.x; i < n2; i += kFinThreads) S.sel[i] = 0xFFFFFFFFu;
-  __syncthreads();
-  bitonic_sort_u32<kFinThreads>(S.sel, n2);
+  sort_units<kFinThreads>(S.sel, nsel, bits_of((uint32_t)(g.n_units - 1)), S.hist,
+                          reinterpret_cast<uint32_t*>(S.C));
   write_units<kFinThreads>(g, S.sel, nsel, idx_row, count + row);
 }
 
 // --------------------------------------------------------------------------------------
-// Long rows.
+// Long rows: sample -> filter -> finish.
 // --------------------------------------------------------------------------------------
+// The sample CTA estimates a threshold T_est with at least k keys >= T_est from an
+// evenly spaced sample; the filter appends every key >= T_est (with its unit) to
+// the row's candidate list; the finishing CTA selects exactly among them.  When
+// the estimate misses (fewer than k or more than kCap candidates) the finishing
+// CTA selects over the whole row itself.  Only speed depends on the sample.
+constexpr int kSample = 8192;  // largest sample (composite keys held in shared memory)
+
+__host__ __device__ inline int sample_size(const Geo& g) {
+  int64_t s = g.k * 4 > 4096 ? (int64_t)g.k * 4 : 4096;
+  if (s > kSample) s = kSample;
+  return (int)imin64(g.M, s);
+}
+
+// The estimate is taken on composite keys (unique, ties broken by index), so the
+// candidate count stays near r * M / sample even when a huge group of units ties
+// on one score (integer Hamming scores do).  Two 11-bit radix passes suffice: the
+// lower bound of the bucket that holds the r-th largest sample is a valid estimate
+// (at least r sampled keys are >= it).
 template <bool F32>
-__global__ void __launch_bounds__(256)
-topk_minmax_kernel(const void* __restrict__ scores, Geo g, Ws ws) {
-  const int64_t row = blockIdx.y;
+__global__ void __launch_bounds__(kFinThreads)
+topk_sample_kernel(const void* __restrict__ scores, Geo g, Ws ws) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint64_t* C = reinterpret_cast<uint64_t*>(smem_raw);  // [kSample]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(C + kSample);  // [kBins]
+  __shared__ uint32_t scratch[32], out[4], kmin_s, kmax_s;
+  __shared__ int nan_s;
+  const int64_t row = blockIdx.x;
   RowState& st = ws.st[row];
-  const int64_t i0 = (int64_t)blockIdx.x * kChunk;
-  const int64_t i1 = imin64(i0 + kChunk, g.M);
+  if (threadIdx.x == 0) { nan_s = 0; kmin_s = 0xFFFFFFFFu; kmax_s = 0; }
+  __syncthreads();
+  const int S = sample_size(g);
+  // sample i sits at unit lead + floor(i * step), step = M / S in 32.32 fixed point
+  const uint64_t step = ((uint64_t)g.M << 32) / (uint64_t)S;
+  const float* fs = reinterpret_cast<const float*>(scores) + row * g.n_units + g.lead;
+  const int32_t* is = reinterpret_cast<const int32_t*>(scores) + row * g.n_units + g.lead;
   bool nan = false;
   uint32_t mn = 0xFFFFFFFFu, mx = 0;
-  for (int64_t i = i0 + threadIdx.x; i < i1; i += 256) {
-    uint32_t kk = load_key<F32>(scores, row * g.n_units + g.lead + i, nan);
-    mn = min(mn, kk);
-    mx = max(mx, kk);
-  }
+  constexpr int kBatch = 8;  // independent loads in flight per thread
+  for (int i0 = 0; i0 < S; i0 += kFinThreads * kBatch) {
+    uint32_t v[kBatch];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * kFinThreads + threadIdx.x;
+      if (i < S) {
+        const uint32_t iu = (uint32_t)(((uint64_t)i * step) >> 32);
+        if (F32) {
+          const float f = __ldg(fs + iu);
+          if ((__float_as_uint(f) & 0x7FFFFFFFu) > 0x7F800000u) nan = true;
+          v[u] = key_of_f32(f);
+        } else {
+          v[u] = key_of_i32(__ldg(is + iu));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * kFinThreads + threadIdx.x;
+      if (i < S) {
+        C[i] = v[u];
+        mn = min(mn, v[u]);
+        mx = max(mx, v[u]);
+      }
+    }
   }
-  if (__any_sync(0xFFFFFFFFu, nan) && (threadIdx.x & 31) == 0) atomicOr(&st.nan, 1u);
-  if ((threadIdx.x & 31) == 0) {
-    atomicMax(&st.inv_min, ~mn);
-    atomicMax(&st.max_key, mx);
+  if (nan) nan_s = 1;
+  atomicMin(&kmin_s, mn);
+  atomicMax(&kmax_s, mx);
+  __syncthreads();
+  const double mu = (double)g.k * S / (double)g.M;
+  const int r = (int)fmin((double)S, ceil(mu + 5.0 * sqrt(mu) + 2.0));
+  uint32_t T_key = 0, imax = (uint32_t)g.M;  // default: every unit is a candidate
+  if (!nan_s && g.M > g.k && r < S) {
+    const uint32_t kmin = kmin_s;
+    const int bI = bits_of((uint32_t)(g.M - 1));
+    const int nb = bits_of(kmax_s - kmin) + bI;
+    for (int i = threadIdx.x; i < S; i += kFinThreads) {
+      const uint32_t iu = (uint32_t)(((uint64_t)i * step) >> 32);  // sampled unit - lead
+      C[i] = ((uint64_t)((uint32_t)C[i] - kmin) << bI) | (uint64_t)((uint32_t)(g.M - 1) - iu);
+    }
+    __syncthreads();
+    const uint64_t T = radix_threshold<kFinThreads>(C, S, (uint32_t)r, 0, nb, hist, scratch, out, 2);
+    T_key = kmin + (uint32_t)(T >> bI);
+    imax = (uint32_t)(g.M - 1) - (uint32_t)(T & ((1ull << bI) - 1));
+  }
+  if (threadIdx.x == 0) {
+    st.nan = nan_s;
+    st.thresh = T_key;
+    st.imax = imax;
+    st.ncand = 0;
   }
 }
 
-struct Comp {  // composite-key geometry of a row
-  uint32_t kmin;
-  int bI, nb, w0, shift0;
-};
-
-__device__ __forceinline__ Comp row_comp(const RowState& st, const Geo& g) {
-  Comp c;
-  c.kmin = ~st.inv_min;
-  c.bI = bits_of((uint32_t)(g.M - 1));
-  c.nb = bits_of(st.max_key - c.kmin) + c.bI;
-  c.w0 = min(kDigit, c.nb);
-  c.shift0 = c.nb - c.w0;
-  return c;
-}
-
-__device__ __forceinline__ uint64_t composite(uint32_t key, int64_t i, const Comp& c, int M) {
-  return ((uint64_t)(key - c.kmin) << c.bI) | (uint64_t)(M - 1 - i);
-}
+// One pass over the row: every unit with (key, index) at or above the estimate
+// is appended with its key; 8 groups of 4 units per thread are loaded up front.
+constexpr int kFilterGroups = kChunk / (256 * 4);
 
 template <bool F32>
 __global__ void __launch_bounds__(256)
-topk_hist_kernel(const void* __restrict__ scores, Geo g, Ws ws, unsigned nchunks) {
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t scratch[32];
-  __shared__ uint32_t out[4];
-  __shared__ bool last;
+topk_filter_kernel(const void* __restrict__ scores, Geo g, Ws ws, bool vec) {
   const int64_t row = blockIdx.y;
   RowState& st = ws.st[row];
   if (st.nan || g.M <= g.k) return;
-  const Comp c = row_comp(st, g);
-  for (int b = threadIdx.x; b < kBins; b += 256) hist[b] = 0;
-  __syncthreads();
-  const int64_t i0 = (int64_t)blockIdx.x * kChunk;
-  const int64_t i1 = imin64(i0 + kChunk, g.M);
-  bool nan = false;
-  for (int64_t i = i0 + threadIdx.x; i < i1; i += 256) {
-    uint32_t kk = load_key<F32>(scores, row * g.n_units + g.lead + i, nan);
-    atomicAdd(&hist[(uint32_t)(composite(kk, i, c, g.M) >> c.shift0)], 1u);
-  }
-  __syncthreads();
-  for (int b = threadIdx.x; b < kBins; b += 256)
-    if (hist[b]) atomicAdd(&st.hist[b], hist[b]);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = (atomicAdd(&st.ticket, 1u) == nchunks - 1);
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  for (int b = threadIdx.x; b < kBins; b += 256) hist[b] = __ldcg(&st.hist[b]);
-  __syncthreads();
-  pick_digit<256>(hist, (uint32_t)g.k, scratch, out);
-  if (threadIdx.x == 0) {
-    st.digit = out[0];
-    st.need = (uint32_t)g.k - out[1];
-    st.bucket = hist[out[0]];
-  }
-}
-
-template <bool F32>
-__global__ void __launch_bounds__(256)
-topk_filter_kernel(const void* __restrict__ scores, Geo g, Ws ws) {
-  const int64_t row = blockIdx.y;
-  const RowState& st = ws.st[row];
-  if (st.nan || g.M <= g.k) return;
-  const Comp c = row_comp(st, g);
-  const uint32_t d = st.digit;
-  const bool keep_cand = st.bucket <= (uint32_t)kCap;
-  uint32_t* above = ws.above + row * kMaxTopK;
+  const uint32_t T = st.thresh;
+  const uint32_t imax = st.imax;
   uint64_t* cand = ws.cand + row * kCap;
-  RowState& stw = ws.st[row];
   const int lane = threadIdx.x & 31;
-  const int64_t i0 = (int64_t)blockIdx.x * kChunk;
-  const int64_t i1 = imin64(i0 + kChunk, g.M);
+  const float* frow = reinterpret_cast<const float*>(scores) + row * g.n_units;
+  const int32_t* irow = reinterpret_cast<const int32_t*>(scores) + row * g.n_units;
+  const int lead = g.lead, tail = g.tail, nu = (int)g.n_units;
+  const int a0 = (lead & ~3) + (int)blockIdx.x * kChunk;  // aligned chunk start
+  uint32_t kk[kFilterGroups][4];
   bool nan = false;
-  for (int64_t ib = i0; ib < i1; ib += 256) {
-    const int64_t i = ib + threadIdx.x;
-    uint64_t x = 0;
-    uint32_t dig = 0;
-    bool valid = i < i1;
-    if (valid) {
-      x = composite(load_key<F32>(scores, row * g.n_units + g.lead + i, nan), i, c, g.M);
-      dig = (uint32_t)(x >> c.shift0);
+#pragma unroll
+  for (int gi = 0; gi < kFilterGroups; ++gi) {
+    const int gs = a0 + (gi * 256 + (int)threadIdx.x) * 4;
+    if (vec && gs + 4 <= nu) {
+      if (F32) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(frow + gs));
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kk[gi][e] = key_of_f32(f[e]);
+          if ((__float_as_uint(f[e]) & 0x7FFFFFFFu) > 0x7F800000u && gs + e >= lead && gs + e < tail)
+            nan = true;
+        }
+      } else {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(irow + gs));
+        kk[gi][0] = key_of_i32(v.x); kk[gi][1] = key_of_i32(v.y);
+        kk[gi][2] = key_of_i32(v.z); kk[gi][3] = key_of_i32(v.w);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        kk[gi][e] = 0u;
+        if (gs + e >= lead && gs + e < tail) {
+          if (F32) {
+            const float f = __ldg(frow + gs + e);
+            if ((__float_as_uint(f) & 0x7FFFFFFFu) > 0x7F800000u) nan = true;
+            kk[gi][e] = key_of_f32(f);
+          } else {
+            kk[gi][e] = key_of_i32(__ldg(irow + gs + e));
+          }
+        }
+      }
     }
-    const bool up = valid && dig > d;
-    const bool eq = valid && keep_cand && dig == d;
-    // warp-aggregated appends
-    uint32_t mu = __ballot_sync(0xFFFFFFFFu, up);
-    if (mu) {
-      uint32_t basep = 0;
-      if (lane == 0) basep = atomicAdd(&stw.nabove, __popc(mu));
-      basep = __shfl_sync(0xFFFFFFFFu, basep, 0);
-      if (up) above[basep + __popc(mu & ((1u << lane) - 1))] = (uint32_t)(g.lead + i);
+  }
+  if (nan) atomicOr(&st.nan, 1u);
+#pragma unroll
+  for (int gi = 0; gi < kFilterGroups; ++gi) {
+    const int gs = a0 + (gi * 256 + (int)threadIdx.x) * 4;
+    uint32_t hit = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int u = gs + e;
+      const bool inr = u >= lead && u < tail;
+      const uint32_t k = kk[gi][e];
+      if (inr && (k > T || (k == T && (uint32_t)(u - lead) <= imax))) hit |= 1u << e;
     }
-    uint32_t me = __ballot_sync(0xFFFFFFFFu, eq);
-    if (me) {
-      uint32_t basep = 0;
-      if (lane == 0) basep = atomicAdd(&stw.ncand, __popc(me));
-      basep = __shfl_sync(0xFFFFFFFFu, basep, 0);
-      if (eq) cand[basep + __popc(me & ((1u << lane) - 1))] = x;
+    if (!__any_sync(0xFFFFFFFFu, hit != 0)) continue;
+    const uint32_t mine = __popc(hit);
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
     }
+    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    uint32_t basep = 0;
+    if (lane == 31) basep = atomicAdd(&st.ncand, tot);
+    basep = __shfl_sync(0xFFFFFFFFu, basep, 31) + incl - mine;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (hit & (1u << e)) {
+        if (basep < (uint32_t)kCap) cand[basep] = ((uint64_t)kk[gi][e] << 32) | (uint32_t)(gs + e);
+        ++basep;
+      }
   }
 }
 
@@ -424,44 +553,68 @@ topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __res
     if (threadIdx.x == 0) count[row] = -1;
     return;
   }
-  if (threadIdx.x == 0) S.nsel = 0;
+  if (threadIdx.x == 0) { S.nsel = 0; S.kmin = 0xFFFFFFFFu; S.kmax = 0; }
   if (g.M <= g.k) {
     for (int i = threadIdx.x; i < g.M; i += kFinThreads) S.sel[i] = g.lead + i;
     __syncthreads();
     write_units<kFinThreads>(g, S.sel, g.M, idx_row, count + row);
     return;
   }
-  const Comp c = row_comp(st, g);
-  const uint32_t d = st.digit, need = st.need, bucket = st.bucket, nabove = st.nabove;
-  const uint32_t* above = ws.above + row * kMaxTopK;
-  for (uint32_t i = threadIdx.x; i < nabove; i += kFinThreads) S.sel[i] = above[i];
-  if (threadIdx.x == 0) S.nsel = nabove;
   __syncthreads();
-  if (bucket <= (uint32_t)kCap) {
+  const uint32_t c = st.ncand;
+  const int bI = bits_of((uint32_t)(g.M - 1));
+  const uint64_t imask = (1ull << bI) - 1;
+  if (c >= (uint32_t)g.k && c <= (uint32_t)kCap) {
     const uint64_t* cand = ws.cand + row * kCap;
-    for (uint32_t i = threadIdx.x; i < bucket; i += kFinThreads) S.C[i] = cand[i];
+    uint32_t mn = 0xFFFFFFFFu, mx = 0;
+    for (uint32_t i = threadIdx.x; i < c; i += kFinThreads) {
+      uint64_t x = cand[i];
+      S.C[i] = x;
+      mn = min(mn, (uint32_t)(x >> 32));
+      mx = max(mx, (uint32_t)(x >> 32));
+    }
+    atomicMin(&S.kmin, mn);
+    atomicMax(&S.kmax, mx);
     __syncthreads();
-    const uint64_t T = radix_threshold<kFinThreads>(S.C, (int)bucket, need, d, c.shift0,
-                                                    S.hist, S.scratch, S.out);
-    for (uint32_t i = threadIdx.x; i < bucket; i += kFinThreads) {
+    const uint32_t kmin = S.kmin;
+    const int nb = bits_of(S.kmax - kmin) + bI;
+    for (uint32_t i = threadIdx.x; i < c; i += kFinThreads) {
       uint64_t x = S.C[i];
-      if (x >= T)
-        S.sel[atomicAdd(&S.nsel, 1u)] =
-            g.lead + (g.M - 1 - (uint32_t)(x & ((1ull << c.bI) - 1)));
+      uint32_t u = (uint32_t)x;
+      S.C[i] = ((uint64_t)((uint32_t)(x >> 32) - kmin) << bI) | (uint64_t)(g.M - 1 - (u - g.lead));
+    }
+    __syncthreads();
+    const uint64_t T = radix_threshold<kFinThreads>(S.C, (int)c, (uint32_t)g.k, 0, nb, S.hist,
+                                                    S.scratch, S.out);
+    for (uint32_t i = threadIdx.x; i < c; i += kFinThreads) {
+      uint64_t x = S.C[i];
+      if (x >= T) S.sel[atomicAdd(&S.nsel, 1u)] = g.lead + (g.M - 1 - (uint32_t)(x & imask));
     }
   } else {
-    // Slow path: resolve the remaining digits with passes over the row.
-    uint64_t prefix = d;
-    int pos = c.shift0;
-    uint32_t r = need;
+    // The estimate missed: exact selection over the whole row in this CTA.
     bool nan = false;
+    uint32_t mn = 0xFFFFFFFFu, mx = 0;
+    for (int64_t i = threadIdx.x; i < g.M; i += kFinThreads) {
+      uint32_t kk = load_key<F32>(scores, row * g.n_units + g.lead + i, nan);
+      mn = min(mn, kk);
+      mx = max(mx, kk);
+    }
+    atomicMin(&S.kmin, mn);
+    atomicMax(&S.kmax, mx);
+    __syncthreads();
+    const uint32_t kmin = S.kmin;
+    const int nb = bits_of(S.kmax - kmin) + bI;
+    uint64_t prefix = 0;
+    int pos = nb;
+    uint32_t r = (uint32_t)g.k;
     while (pos > 0) {
       const int w = min(kDigit, pos);
       const int npos = pos - w;
       for (int b = threadIdx.x; b < kBins; b += kFinThreads) S.hist[b] = 0;
       __syncthreads();
       for (int64_t i = threadIdx.x; i < g.M; i += kFinThreads) {
-        uint64_t x = composite(load_key<F32>(scores, row * g.n_units + g.lead + i, nan), i, c, g.M);
+        uint32_t kk = load_key<F32>(scores, row * g.n_units + g.lead + i, nan);
+        uint64_t x = ((uint64_t)(kk - kmin) << bI) | (uint64_t)(g.M - 1 - i);
         if ((x >> pos) == prefix) atomicAdd(&S.hist[(uint32_t)(x >> npos) & ((1u << w) - 1)], 1u);
       }
       __syncthreads();
@@ -474,26 +627,22 @@ topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __res
       if (inb == r) break;
     }
     const uint64_t T = prefix << pos;
-    const uint64_t lo_d = (uint64_t)d << c.shift0, hi_d = ((uint64_t)d + 1) << c.shift0;
     for (int64_t i = threadIdx.x; i < g.M; i += kFinThreads) {
-      uint64_t x = composite(load_key<F32>(scores, row * g.n_units + g.lead + i, nan), i, c, g.M);
-      if (x >= lo_d && x < hi_d && x >= T) S.sel[atomicAdd(&S.nsel, 1u)] = (uint32_t)(g.lead + i);
+      uint32_t kk = load_key<F32>(scores, row * g.n_units + g.lead + i, nan);
+      uint64_t x = ((uint64_t)(kk - kmin) << bI) | (uint64_t)(g.M - 1 - i);
+      if (x >= T) S.sel[atomicAdd(&S.nsel, 1u)] = (uint32_t)(g.lead + i);
     }
   }
   __syncthreads();
   const int nsel = (int)S.nsel;
-  int n2 = 1;
-  while (n2 < nsel) n2 <<= 1;
-  for (int i = nsel + threadIdx.x; i < n2; i += kFinThreads) S.sel[i] = 0xFFFFFFFFu;
-  __syncthreads();
-  bitonic_sort_u32<kFinThreads>(S.sel, n2);
+  sort_units<kFinThreads>(S.sel, nsel, bits_of((uint32_t)(g.n_units - 1)), S.hist,
+                          reinterpret_cast<uint32_t*>(S.C));
   write_units<kFinThreads>(g, S.sel, nsel, idx_row, count + row);
 }
 
 template <bool F32>
 static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
-                  int64_t idx_stride, int32_t* count, void* wsp, size_t ws_bytes,
-                  cudaStream_t st) {
+                  int64_t idx_stride, int32_t* count, void* wsp, cudaStream_t st) {
   const size_t smem = sizeof(FinSmem);
   if (g.n_units <= kSmallRow) {
     auto kern = topk_small_kernel<F32>;
@@ -502,13 +651,13 @@ static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
     return check_launch("topk_small");
   }
   Ws ws = carve(wsp, rows);
-  if (cudaMemsetAsync(ws.st, 0, sizeof(RowState) * rows, st) != cudaSuccess)
-    return check_launch("topk: workspace clear");
-  const unsigned nchunks = (unsigned)((g.M + kChunk - 1) / kChunk);
-  dim3 grid(max(nchunks, 1u), (unsigned)rows);
-  topk_minmax_kernel<F32><<<grid, 256, 0, st>>>(scores, g, ws);
-  topk_hist_kernel<F32><<<grid, 256, 0, st>>>(scores, g, ws, max(nchunks, 1u));
-  topk_filter_kernel<F32><<<grid, 256, 0, st>>>(scores, g, ws);
+  const size_t smem_s = (size_t)kSample * 8 + kBins * 4;
+  auto samp = topk_sample_kernel<F32>;
+  if (int rc_ = set_smem_limit((const void*)samp, smem_s, "topk: smem attribute")) return rc_;
+  samp<<<(unsigned)rows, kFinThreads, smem_s, st>>>(scores, g, ws);
+  const unsigned nchunks = (unsigned)((g.tail - (g.lead & ~3) + kChunk - 1) / kChunk);
+  const bool vec = ((uintptr_t)scores % 16 == 0) && (g.n_units % 4 == 0);
+  topk_filter_kernel<F32><<<dim3(nchunks, (unsigned)rows), 256, 0, st>>>(scores, g, ws, vec);
   auto fin = topk_finish_kernel<F32>;
   if (int rc_ = set_smem_limit((const void*)fin, smem, "topk: smem attribute")) return rc_;
   fin<<<(unsigned)rows, kFinThreads, smem, st>>>(scores, g, ws, idx, idx_stride, count);
@@ -517,11 +666,11 @@ static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
 
 int launch_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
                 int64_t n_tokens, const sd_select& sel, int32_t* idx, int64_t idx_stride,
-                int32_t* count, void* ws, size_t ws_bytes, cudaStream_t st) {
+                int32_t* count, void* ws, size_t, cudaStream_t st) {
   Geo g = make_geo(n_units, n_tokens, sel);
   if (score_type == SD_SCORE_F32)
-    return topk_t<true>(scores, rows, g, idx, idx_stride, count, ws, ws_bytes, st);
-  return topk_t<false>(scores, rows, g, idx, idx_stride, count, ws, ws_bytes, st);
+    return topk_t<true>(scores, rows, g, idx, idx_stride, count, ws, st);
+  return topk_t<false>(scores, rows, g, idx, idx_stride, count, ws, st);
 }
 
 }  // namespace sd
