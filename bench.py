@@ -342,6 +342,22 @@ def main():
     st_topk = statistics.mean(timed_steps(torch, lambda: step.stage_topk(), K_st, 3, flush))
     st_att = statistics.mean(timed_steps(torch, lambda: step.stage_attend(q), K_st, 3, flush))
     eager = statistics.mean(timed_steps(torch, lambda: step.run(q), K_st, 3, flush))
+
+    # marginal stage costs inside the step: cumulative prefixes, L2 flushed before each
+    def upto(nst):
+        def f():
+            step.stage_prep(q)
+            if nst > 1:
+                step.stage_score(q)
+            if nst > 2:
+                step.stage_topk()
+            if nst > 3:
+                step.stage_attend(q)
+        return f
+
+    cum = [statistics.mean(timed_steps(torch, upto(i), K_st, 3, flush)) for i in (1, 2, 3, 4)]
+    marginal = {"plan": cum[0] * 1e3, "scan": (cum[1] - cum[0]) * 1e3,
+                "topk": (cum[2] - cum[1]) * 1e3, "gather_attend": (cum[3] - cum[2]) * 1e3}
     peak_gbs, peak_kind = peaks()
     scan_gbs = scan_bytes / (st_score * 1e-3) / 1e9
     alu_ops = rl.plane_scan_alu_ops(plan_np, n)
@@ -396,6 +412,34 @@ def main():
                                  "scan_frac_hbm": bh / (ths * 1e-3) / 1e9 / peak_gbs}
         del sth, ih
 
+        # index in pinned host memory: gather the planned prefixes over the host link
+        # (NVLink-C2C on a Grace host), then scan, select and attend
+        hp = index["planes"].cpu().pin_memory()
+        hs = index["scales"].cpu().pin_memory()
+        dpl = torch.empty_like(index["planes"])
+        dsc = torch.empty_like(index["scales"])
+        shp = sd.make_shape(B, Hq, Hkv, n)
+        sto = DecodeStep(sc, K, V, {"planes": dpl, "scales": dsc}, sigma2=sigma2)
+
+        def offload_only():
+            sd.sd_offload_gather(shp, hp, hs, step.plan, dpl, dsc)
+
+        def offload_step():
+            sto.stage_prep(q)
+            sd.sd_offload_gather(shp, hp, hs, sto.plan, dpl, dsc)
+            sto.stage_score(q)
+            sto.stage_topk()
+            sto.stage_attend(q)
+
+        to = statistics.mean(timed_steps(torch, offload_only, K_st, 3, flush))
+        tos = statistics.mean(timed_steps(torch, offload_step, K_st, 3, flush))
+        torch.cuda.synchronize()
+        assert np.array_equal(sto.out.cpu().numpy(), step.out.cpu().numpy())
+        variants["offload56"] = {"gather_us": to * 1e3, "gather_bytes": scan_bytes,
+                                 "host_link_GBps": scan_bytes / (to * 1e-3) / 1e9,
+                                 "us_per_step": tos * 1e3, "keys_per_s": keys / (tos * 1e-3)}
+        del hp, hs, dpl, dsc, sto
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, cfg)
@@ -415,6 +459,7 @@ def main():
         "us_per_step": t_step_max * 1e3,
         "stages_us": {"plan": st_prep * 1e3, "scan": st_score * 1e3, "topk": st_topk * 1e3,
                       "gather_attend": st_att * 1e3, "step_eager": eager * 1e3},
+        "stages_in_step_us": marginal,
         "roofline": {"bound": "hbm", "kernel": "score_planes_kernel",
                      "achieved": scan_gbs, "peak": peak_gbs, "unit": "GB/s",
                      "frac": scan_gbs / peak_gbs, "traffic": None,

@@ -234,17 +234,21 @@ def test_topk_bit_exact_on_shared_scores(sd, rows, n, kind, levels, k, sink, loc
 
 
 def test_topk_estimate_misses_fall_back_to_exact(sd):
-    # Long rows: the threshold is estimated from an evenly spaced sample of up to
-    # 16,384 scores.  (a) 200 large scores, all on sampled positions: the estimate
-    # admits fewer than k candidates.  (b) every sampled position large: more
-    # candidates than the finishing CTA holds.  Both must still be exact.
-    M, S = 100000, 16384
-    pos = (np.arange(S, dtype=np.int64) * M) // S
+    # Long rows: the threshold is estimated from up to 8192 evenly spaced units
+    # (unit floor(s * step) with step = M / 8192 in 32.32 fixed point).  (a) 200
+    # large scores, all on sampled units: the estimate admits fewer than k
+    # candidates.  (b) every unsampled unit large: far more candidates than the
+    # selection holds.  Both must still be exact.
+    M = 100000
+    Ssz = min(M, 8192)
+    step = (M << 32) // Ssz
+    pos = (np.arange(Ssz, dtype=np.uint64) * np.uint64(step)) >> np.uint64(32)
+    pos = pos.astype(np.int64)
     a = np.zeros((1, M), np.float32)
     a[0, pos[::37][:200]] = 1.0
-    b = np.zeros((1, M), np.float32)
-    b[0, pos] = 2.0
-    b[0, 5] = 3.0
+    b = np.full((1, M), 5.0, np.float32)
+    b[0, pos] = 1.0
+    b[0, 7] = 9.0
     for s in (a, b):
         gi, gc = run_topk(sd, s, 512, 0, 0)
         ri, rc = oracle.topk(s, 512, 0, 0)
@@ -286,9 +290,9 @@ def test_topk_nan_row(sd):
 # --------------------------------------------------------------------------------------
 # S7 gather-attend on identical generated index lists: 2e-3 absolute
 # --------------------------------------------------------------------------------------
-@pytest.mark.parametrize("G,max_count", [(4, 1152), (8, 2064), (1, 63), (2, 200)])
+@pytest.mark.parametrize("G,max_count", [(4, 1152), (8, 2064), (1, 63), (2, 200), (4, 9000)])
 def test_gather_attend(sd, G, max_count):
-    cfg = synth.config(1, B=2, Hq=3 * G, Hkv=3, n=5000)
+    cfg = synth.config(1, B=2, Hq=3 * G, Hkv=3, n=max(5000, max_count + 100))
     inp = synth.make_inputs(cfg)
     rows = cfg.B * cfg.Hkv
     counts = np.array([max_count, 1, 0, 65, max_count - 1, 64][:rows])

@@ -223,6 +223,7 @@ int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const 
     return fail(SD_ERR_INVALID_ARG, "sd_gather_attend: K and V must be 16-byte aligned");
   if (max_count < 0 || idx_stride < max_count)
     return fail(SD_ERR_INVALID_ARG, "sd_gather_attend: bad max_count / idx_stride");
+
   size_t need = attend_workspace_bytes(s, max_count);
   if (need && (!workspace || ws_bytes < need))
     return fail(SD_ERR_WORKSPACE, "sd_gather_attend: workspace %zu < %zu bytes", ws_bytes,

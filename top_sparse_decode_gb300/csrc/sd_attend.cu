@@ -15,6 +15,7 @@ namespace sd {
 constexpr int kAtChunk = 32;
 constexpr int kAtPitch = kD + 8;  // bf16 pitch of staged rows (breaks bank alignment)
 constexpr int kQPitch = 36;       // fp32 pitch of a quarter of q (conflict-free LDS.128)
+constexpr int kMergeMax = 256;    // chunks whose merge weights are staged at once
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -191,20 +192,61 @@ attend_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ K,
   __syncthreads();
   if (!last) return;
   __threadfence();
+  // merge: the row max m, then per window of up to kMergeMax chunks their weights
+  // e^{m_c - m} staged in shared memory; o accumulates with 8 loads in flight
+  __shared__ float wts[G][kMergeMax];
+  __shared__ float lsum[G], mrow[G];
   const int64_t rbase = row * nchunks * G;
-  for (int g = 0; g < G; ++g) {
+  const int warp = t >> 5, lane = t & 31;
+  for (int g = warp; g < G; g += 4) {
     float m = -INFINITY;
-    for (int ch = 0; ch < nch_row; ++ch) m = fmaxf(m, __ldcg(&ws.part_ml[rbase + ch * G + g].x));
-    float l = 0.0f, o = 0.0f;
-    for (int ch = 0; ch < nch_row; ++ch) {
-      const float2 p = __ldcg(&ws.part_ml[rbase + ch * G + g]);
-      const float wgt = p.x == -INFINITY ? 0.0f : expf(p.x - m);
-      l = fmaf(p.y, wgt, l);
-      o = fmaf(__ldcg(&ws.part_o[(rbase + ch * G + g) * kD + t]), wgt, o);
+    for (int ch = lane; ch < nch_row; ch += 32) m = fmaxf(m, __ldcg(&ws.part_ml[rbase + ch * G + g].x));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) { mrow[g] = m; lsum[g] = 0.0f; }
+  }
+  float o_acc[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) o_acc[g] = 0.0f;
+  for (int c0 = 0; c0 < nch_row; c0 += kMergeMax) {
+    const int nw = min(kMergeMax, nch_row - c0);
+    __syncthreads();  // mrow ready; the previous window's weights consumed
+    for (int g = warp; g < G; g += 4) {
+      const float m = mrow[g];
+      float l = 0.0f;
+      for (int i = lane; i < nw; i += 32) {
+        const float2 p = __ldcg(&ws.part_ml[rbase + (c0 + i) * G + g]);
+        const float wgt = p.x == -INFINITY ? 0.0f : expf(p.x - m);
+        wts[g][i] = wgt;
+        l = fmaf(p.y, wgt, l);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+      if (lane == 0) lsum[g] += l;
     }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float o = o_acc[g];
+      int i = 0;
+      for (; i + 8 <= nw; i += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(&ws.part_o[(rbase + (c0 + i + u) * G + g) * kD + t]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) o = fmaf(v[u], wts[g][i + u], o);
+      }
+      for (; i < nw; ++i) o = fmaf(__ldcg(&ws.part_o[(rbase + (c0 + i) * G + g) * kD + t]), wts[g][i], o);
+      o_acc[g] = o;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float l = lsum[g];
     const int64_t bq = (int64_t)b * Hq + h * G + g;
-    out[bq * kD + t] = l > 0.0f ? o / l : 0.0f;
-    if (lse && t == 0) lse[bq] = l > 0.0f ? m + logf(l) : -INFINITY;
+    out[bq * kD + t] = l > 0.0f ? o_acc[g] / l : 0.0f;
+    if (lse && t == 0) lse[bq] = l > 0.0f ? mrow[g] + logf(l) : -INFINITY;
   }
 }
 

@@ -23,6 +23,8 @@
 // member of the top k (and every key tied with the k-th) is a candidate.  When
 // the estimate misses (fewer than k, or more than kCap candidates) the finishing
 // CTA selects over the whole row itself: slower, same result.
+#include <cooperative_groups.h>
+
 #include "sd_internal.cuh"
 
 namespace sd {
@@ -147,15 +149,11 @@ __device__ void bitonic_sort_u32(uint32_t* a, int n2) {
   }
 }
 
-// hist[bin] += 1 for every lane with `in`, one shared-memory atomic per distinct
-// bin per warp (score distributions crowd a few bins; this avoids serialising
-// on them).  All 32 lanes must call it.
+// hist[bin] += 1 for every lane with `in` (all 32 lanes call it).  Plain shared
+// atomics: measured faster here than aggregating equal bins with match.any, whose
+// cost grows with the number of distinct bins in the warp.
 __device__ __forceinline__ void hist_add(uint32_t* hist, bool in, uint32_t bin) {
-  const uint32_t act = __ballot_sync(0xFFFFFFFFu, in);
-  if (!act) return;
-  const uint32_t peers = __match_any_sync(0xFFFFFFFFu, in ? bin : 0xFFFFFFFFu) & act;
-  const int lane = threadIdx.x & 31;
-  if (in && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+  if (in) atomicAdd(&hist[bin], 1u);
 }
 
 // Sorts the nsel distinct units sel[0..nsel) (all < 2^ubits) ascending: a counting
@@ -640,6 +638,465 @@ topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __res
   write_units<kFinThreads>(g, S.sel, nsel, idx_row, count + row);
 }
 
+// --------------------------------------------------------------------------------------
+// Long rows, one launch: a thread-block cluster of CS CTAs per row.
+// --------------------------------------------------------------------------------------
+// The same three steps as above, but the CTAs of a row share distributed shared
+// memory and cluster barriers instead of global memory and kernel boundaries:
+//   1. each CTA samples its share of the evenly spaced positions; the composite
+//      keys are gathered in CTA 0, which picks the estimate (T_key, i_max);
+//   2. each CTA filters its slice of the row into a local candidate list; the
+//      lists are gathered in CTA 0, which selects exactly (radix over composite
+//      keys) and broadcasts the exact threshold;
+//   3. each CTA keeps its own candidates above the threshold, sorts them (they lie
+//      in its slice, so the slices' lists concatenate in ascending order) and
+//      writes them at the offset given by the ranks before it.
+// If the estimate admits fewer than k or too many candidates, step 2 is replaced
+// by an exact radix select over the whole row, distributed over the cluster (each
+// CTA histograms its slice, the histograms are summed in CTA 0).
+namespace cg = cooperative_groups;
+constexpr int kLocCap = 2048;  // local candidates per CTA of a cluster
+constexpr int kClBuf = kCap;   // CTA 0's gather buffer (samples, then candidates)
+
+struct ClSmem {
+  uint64_t buf[kClBuf];    // CTA 0: gathered samples, then gathered candidates / row histogram
+  uint64_t cand[kLocCap];  // local candidates (key << 32 | unit); samples in step 1
+  uint32_t sel[kMaxTopK];  // local selected units
+  uint32_t hist[kBins];
+  uint32_t scratch[32], out[4];
+  uint32_t kmin, kmax, nan, nbuf, ovf, ncand, nsel, mode;
+  uint32_t T_key, imax;
+  uint32_t cnt[16];
+};
+
+// 4096 samples (2k for large k) keep the candidates near 3K at k = 512 and under
+// kCap up to k = 4096, while the estimate's serial radix stays short
+// 4096 samples (2k for large k) keep the candidates near 3K at k = 512 and within
+// the gather buffer up to k = 4096, while the estimate's serial radix stays short
+__host__ __device__ inline int cluster_sample_size(const Geo& g) {
+  const int64_t s = g.k * 2 > 4096 ? (int64_t)g.k * 2 : 4096;
+  return (int)imin64(g.M, imin64(s, kClBuf));
+}
+
+template <bool F32>
+__device__ __forceinline__ uint32_t key_at(const float* frow, const int32_t* irow, int64_t u,
+                                           bool& nan) {
+  if (F32) {
+    const float f = __ldg(frow + u);
+    if ((__float_as_uint(f) & 0x7FFFFFFFu) > 0x7F800000u) nan = true;
+    return key_of_f32(f);
+  }
+  return key_of_i32(__ldg(irow + u));
+}
+
+constexpr int kClThreads = 512;
+
+template <bool F32, int CS>
+__global__ void __launch_bounds__(kClThreads)
+topk_cluster_kernel(const void* __restrict__ scores, Geo g, int32_t* __restrict__ idx,
+                    int64_t idx_stride, int32_t* __restrict__ count) {
+  constexpr int NT = kClThreads;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  ClSmem& S = *reinterpret_cast<ClSmem*>(smem_raw);
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  ClSmem* S0 = cl.map_shared_rank(&S, 0);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t row = blockIdx.y;
+  const float* frow = reinterpret_cast<const float*>(scores) + row * g.n_units;
+  const int32_t* irow = reinterpret_cast<const int32_t*>(scores) + row * g.n_units;
+  int32_t* idx_row = idx + row * idx_stride;
+  const int M = g.M, lead = g.lead, k = g.k, blk = g.block;
+  const int ntail = (int)(g.n_units - g.tail);
+  const int i_lo = (int)(((int64_t)rank * M) / CS), i_hi = (int)(((int64_t)(rank + 1) * M) / CS);
+  const int bI = bits_of((uint32_t)(M - 1));
+  const uint32_t imask = (uint32_t)((1ull << bI) - 1);
+
+  if (tid == 0) {
+    S.kmin = 0xFFFFFFFFu; S.kmax = 0; S.nan = 0; S.nbuf = 0; S.ovf = 0;
+    S.ncand = 0; S.nsel = 0; S.mode = 0;
+  }
+  cl.sync();
+
+  // ---- step 1: sample ----
+  const int Ssz = cluster_sample_size(g);
+  const uint64_t step = ((uint64_t)M << 32) / (uint64_t)Ssz;
+  const int s_lo = (int)(((int64_t)rank * Ssz) / CS), s_hi = (int)(((int64_t)(rank + 1) * Ssz) / CS);
+  {
+    bool nan = false;
+    uint32_t mn = 0xFFFFFFFFu, mx = 0;
+    for (int s0 = s_lo; s0 < s_hi; s0 += NT * 4) {
+      uint32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sidx = s0 + u * NT + tid;
+        if (sidx < s_hi) v[u] = key_at<F32>(frow, irow, lead + (int64_t)(((uint64_t)sidx * step) >> 32), nan);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int sidx = s0 + u * NT + tid;
+        if (sidx < s_hi) {
+          S.cand[sidx - s_lo] = v[u];
+          mn = min(mn, v[u]);
+          mx = max(mx, v[u]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+      mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    if (lane == 0) {
+      atomicMin(&S0->kmin, mn);
+      atomicMax(&S0->kmax, mx);
+    }
+    if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) atomicOr(&S0->nan, 1u);
+  }
+  cl.sync();
+  if (S0->nan) {  // uniform over the cluster
+    if (rank == 0 && tid == 0) count[row] = -1;
+    cl.sync();
+    return;
+  }
+  {
+    const uint32_t kmin = S0->kmin;
+    for (int sidx = s_lo + tid; sidx < s_hi; sidx += NT) {
+      const uint32_t iu = (uint32_t)(((uint64_t)sidx * step) >> 32);
+      S0->buf[sidx] = ((uint64_t)((uint32_t)S.cand[sidx - s_lo] - kmin) << bI) |
+                      (uint64_t)((uint32_t)(M - 1) - iu);
+    }
+  }
+  cl.sync();
+  if (rank == 0) {
+    const double mu = (double)k * Ssz / (double)M;
+    const int r = (int)fmin((double)Ssz, ceil(mu + 5.0 * sqrt(mu) + 2.0));
+    uint32_t T_key = 0, imax = (uint32_t)M;
+    if (r < Ssz) {
+      const int nb = bits_of(S.kmax - S.kmin) + bI;
+      const uint64_t T = radix_threshold<NT>(S.buf, Ssz, (uint32_t)r, 0, nb, S.hist, S.scratch,
+                                             S.out, 2);
+      T_key = S.kmin + (uint32_t)(T >> bI);
+      imax = (uint32_t)(M - 1) - (uint32_t)(T & imask);
+    }
+    if (tid == 0) { S.T_key = T_key; S.imax = imax; }
+  }
+  cl.sync();
+
+  // ---- step 2: filter this CTA's slice ----
+  {
+    const uint32_t T = S0->T_key, imax = S0->imax;
+    // the threshold in the score domain (the key map preserves order, -0 == +0)
+    const float Tf = __uint_as_float((T & 0x80000000u) ? (T & 0x7FFFFFFFu) : ~T);
+    const int32_t Ti = (int32_t)(T ^ 0x80000000u);
+    const bool take_all = T == 0;  // key 0 is below every score's key
+    bool nan = false;
+    const int u_lo = lead + i_lo, u_hi = lead + i_hi;
+    const int a_lo = u_lo & ~3;
+    const int nu = (int)g.n_units;
+    const bool vec = ((uintptr_t)frow % 16 == 0) && (nu % 4 == 0);
+    constexpr int kG = 8;  // groups of 4 units in flight per thread
+    for (int b0 = a_lo; b0 < u_hi; b0 += NT * 4 * kG) {  // uniform trip count
+      // issue every load first, convert afterwards: a value used right after its
+      // own load would serialise the loads into round trips
+      uint4 raw[kG];
+#pragma unroll
+      for (int gi = 0; gi < kG; ++gi) {
+        const int gs = b0 + (gi * NT + tid) * 4;
+        if (vec && gs >= u_lo && gs + 4 <= u_hi) {
+          raw[gi] = __ldg(reinterpret_cast<const uint4*>(F32 ? (const void*)(frow + gs) : (const void*)(irow + gs)));
+        } else {
+          const uint32_t* src = F32 ? reinterpret_cast<const uint32_t*>(frow) : reinterpret_cast<const uint32_t*>(irow);
+          raw[gi].x = (gs + 0 >= u_lo && gs + 0 < u_hi) ? __ldg(src + gs + 0) : 0u;
+          raw[gi].y = (gs + 1 >= u_lo && gs + 1 < u_hi) ? __ldg(src + gs + 1) : 0u;
+          raw[gi].z = (gs + 2 >= u_lo && gs + 2 < u_hi) ? __ldg(src + gs + 2) : 0u;
+          raw[gi].w = (gs + 3 >= u_lo && gs + 3 < u_hi) ? __ldg(src + gs + 3) : 0u;
+        }
+      }
+#pragma unroll
+      for (int gi = 0; gi < kG; ++gi) {
+        const int gs = b0 + (gi * NT + tid) * 4;
+        const uint32_t rv[4] = {raw[gi].x, raw[gi].y, raw[gi].z, raw[gi].w};
+        const bool inner = gs >= u_lo && gs + 4 <= u_hi;
+        uint32_t hit = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          bool above, equal;
+          if (F32) {
+            const float f = __uint_as_float(rv[e]);
+            nan |= f != f;  // masked units read 0
+            above = f > Tf;
+            equal = f == Tf;
+          } else {
+            const int32_t x = (int32_t)rv[e];
+            above = x > Ti;
+            equal = x == Ti;
+          }
+          const int u = gs + e;
+          const bool in = inner || (u >= u_lo && u < u_hi);
+          if (in && (take_all || above || (equal && (uint32_t)(u - lead) <= imax))) hit |= 1u << e;
+        }
+        if (!__any_sync(0xFFFFFFFFu, hit != 0)) continue;
+        const uint32_t mine = __popc(hit);
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        uint32_t basep = 0;
+        if (lane == 31) basep = atomicAdd(&S.ncand, tot);
+        basep = __shfl_sync(0xFFFFFFFFu, basep, 31) + incl - mine;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (hit & (1u << e)) {
+            const uint32_t key = F32 ? key_of_f32(__uint_as_float(rv[e])) : key_of_i32((int32_t)rv[e]);
+            if (basep < (uint32_t)kLocCap) S.cand[basep] = ((uint64_t)key << 32) | (uint32_t)(gs + e);
+            ++basep;
+          }
+      }
+    }
+    if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) atomicOr(&S.nan, 1u);
+  }
+  __syncthreads();
+  const uint32_t nloc = S.ncand;
+  const uint32_t nkeep = min(nloc, (uint32_t)kLocCap);
+  if (tid == 0) {
+    if (S.nan) atomicOr(&S0->nan, 1u);
+    if (nloc > (uint32_t)kLocCap) atomicOr(&S0->ovf, 1u);
+    S.out[3] = atomicAdd(&S0->nbuf, nkeep);
+  }
+  __syncthreads();
+  {
+    const uint32_t base = S.out[3];
+    for (uint32_t j = tid; j < nkeep; j += NT)
+      if (base + j < (uint32_t)kClBuf) S0->buf[base + j] = S.cand[j];
+  }
+  cl.sync();
+  if (rank == 0) {  // decide: 0 exact among candidates, 1 whole-row fallback, 2 NaN
+    uint32_t mode = 0;
+    const uint32_t total = S.nbuf;
+    if (S.nan) mode = 2;
+    else if (S.ovf || total > (uint32_t)kClBuf || total < (uint32_t)k) mode = 1;
+    if (mode == 0) {
+      if (tid == 0) { S.kmin = 0xFFFFFFFFu; S.kmax = 0; }
+      __syncthreads();
+      uint32_t mn = 0xFFFFFFFFu, mx = 0;
+      for (uint32_t j = tid; j < total; j += NT) {
+        const uint32_t kk = (uint32_t)(S.buf[j] >> 32);
+        mn = min(mn, kk);
+        mx = max(mx, kk);
+      }
+      atomicMin(&S.kmin, mn);
+      atomicMax(&S.kmax, mx);
+      __syncthreads();
+      const uint32_t kmin = S.kmin;
+      const int nb = bits_of(S.kmax - kmin) + bI;
+      for (uint32_t j = tid; j < total; j += NT) {
+        const uint64_t x = S.buf[j];
+        S.buf[j] = ((uint64_t)((uint32_t)(x >> 32) - kmin) << bI) |
+                   (uint64_t)((uint32_t)(M - 1) - ((uint32_t)x - (uint32_t)lead));
+      }
+      __syncthreads();
+      const uint64_t T = radix_threshold<NT>(S.buf, (int)total, (uint32_t)k, 0, nb, S.hist,
+                                             S.scratch, S.out);
+      if (tid == 0) {
+        S.T_key = kmin + (uint32_t)(T >> bI);
+        S.imax = (uint32_t)(M - 1) - (uint32_t)(T & imask);
+      }
+    } else if (mode == 1) {
+      uint32_t* gh = reinterpret_cast<uint32_t*>(S.buf);
+      for (int b = tid; b < kBins; b += NT) gh[b] = 0;
+      if (tid == 0) { S.kmin = 0xFFFFFFFFu; S.kmax = 0; }
+    }
+    if (tid == 0) S.mode = mode;
+  }
+  cl.sync();
+  const uint32_t mode = S0->mode;
+  if (mode == 2) {
+    if (rank == 0 && tid == 0) count[row] = -1;
+    cl.sync();
+    return;
+  }
+  uint32_t T_key, imax;
+  if (mode == 0) {
+    T_key = S0->T_key;
+    imax = S0->imax;
+  } else {
+    // exact radix select over the whole row, distributed over the cluster
+    const int u_lo = lead + i_lo, u_hi = lead + i_hi;
+    bool nan = false;
+    {
+      uint32_t mn = 0xFFFFFFFFu, mx = 0;
+      for (int u = u_lo + tid; u < u_hi; u += NT) {
+        const uint32_t kk = key_at<F32>(frow, irow, u, nan);
+        mn = min(mn, kk);
+        mx = max(mx, kk);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      }
+      if (lane == 0) { atomicMin(&S0->kmin, mn); atomicMax(&S0->kmax, mx); }
+    }
+    cl.sync();
+    const uint32_t kmin = S0->kmin;
+    const int nb = bits_of(S0->kmax - kmin) + bI;
+    uint32_t* gh0 = reinterpret_cast<uint32_t*>(S0->buf);
+    uint64_t prefix = 0;
+    int pos = nb;
+    uint32_t r = (uint32_t)k;
+    while (pos > 0) {
+      const int w = min(kDigit, pos);
+      const int npos = pos - w;
+      for (int b = tid; b < kBins; b += NT) S.hist[b] = 0;
+      __syncthreads();
+      for (int u0 = u_lo; u0 < u_hi; u0 += NT) {  // uniform trip count
+        const int u = u0 + tid;
+        bool in = false;
+        uint32_t bin = 0;
+        if (u < u_hi) {
+          const uint64_t x = ((uint64_t)(key_at<F32>(frow, irow, u, nan) - kmin) << bI) |
+                             (uint64_t)((uint32_t)(M - 1) - (uint32_t)(u - lead));
+          in = (x >> pos) == prefix;
+          bin = (uint32_t)(x >> npos) & ((1u << w) - 1);
+        }
+        hist_add(S.hist, in, bin);
+      }
+      __syncthreads();
+      for (int b = tid; b < kBins; b += NT)
+        if (S.hist[b]) atomicAdd(&gh0[b], S.hist[b]);
+      cl.sync();
+      if (rank == 0) {
+        pick_digit<NT>(gh0, r, S.scratch, S.out);
+        if (tid == 0) S.out[2] = gh0[S.out[0]];
+        __syncthreads();
+        for (int b = tid; b < kBins; b += NT) gh0[b] = 0;
+      }
+      cl.sync();
+      const uint32_t d = S0->out[0], above = S0->out[1], inb = S0->out[2];
+      r -= above;
+      prefix = (prefix << w) | d;
+      pos = npos;
+      if (inb == r) break;
+    }
+    const uint64_t T = prefix << pos;
+    T_key = kmin + (uint32_t)(T >> bI);
+    imax = (uint32_t)(M - 1) - (uint32_t)(T & imask);
+  }
+
+  // ---- step 3: keep, sort and write this CTA's share ----
+  if (mode == 0) {
+    for (uint32_t j = tid; j < nkeep; j += NT) {
+      const uint64_t x = S.cand[j];
+      const uint32_t kk = (uint32_t)(x >> 32), u = (uint32_t)x;
+      if (kk > T_key || (kk == T_key && u - (uint32_t)lead <= imax))
+        S.sel[atomicAdd(&S.nsel, 1u)] = u;
+    }
+  } else {
+    bool nan = false;
+    for (int u = lead + i_lo + tid; u < lead + i_hi; u += NT) {
+      const uint32_t kk = key_at<F32>(frow, irow, u, nan);
+      if (kk > T_key || (kk == T_key && (uint32_t)(u - lead) <= imax))
+        S.sel[atomicAdd(&S.nsel, 1u)] = (uint32_t)u;
+    }
+  }
+  __syncthreads();
+  const int nsel = (int)S.nsel;
+  if (tid == 0) S0->cnt[rank] = (uint32_t)nsel;
+  sort_units<NT>(S.sel, nsel, bits_of((uint32_t)(g.n_units - 1)), S.hist,
+                 reinterpret_cast<uint32_t*>(S.cand));
+  cl.sync();
+  int off = 0, ktot = 0;
+  for (int q = 0; q < CS; ++q) {
+    const int c = (int)S0->cnt[q];
+    if (q < rank) off += c;
+    ktot += c;
+  }
+  // units at output positions: lead units, then ranks' selections, then tail units
+  for (int p = tid; p < nsel * blk; p += NT) {
+    const int j = blk == 1 ? p : p / blk, o = p - j * blk;
+    const int tok = (int)S.sel[j] * blk + o;
+    if (tok < (int)g.n_tokens) idx_row[(int64_t)(lead + off + j) * blk + o] = tok;
+  }
+  if (rank == 0)
+    for (int p = tid; p < lead * blk; p += NT) idx_row[p] = p;  // lead units are full blocks
+  if (rank == CS - 1) {
+    for (int p = tid; p < ntail * blk; p += NT) {
+      const int tok = g.tail * blk + p;
+      if (tok < (int)g.n_tokens) idx_row[(int64_t)(lead + ktot) * blk + p] = tok;
+    }
+    if (tid == 0) {
+      const bool last_in = ntail > 0 || (nsel > 0 && (int64_t)S.sel[nsel - 1] == g.n_units - 1);
+      int64_t cnt = (int64_t)(lead + ktot + ntail) * blk;
+      if (last_in) cnt -= (g.n_units * g.block - g.n_tokens);
+      count[row] = (int32_t)cnt;
+    }
+  }
+  cl.sync();  // CTA 0's shared memory stays alive until every rank has read it
+}
+
+// How many clusters of CS CTAs can be resident at once on this device (0 if the
+// configuration cannot run), cached per device.  GB300 places at most a few
+// 16-CTA clusters at a time, so the launcher picks the largest CS whose clusters
+// all fit in one wave.
+template <bool F32, int CS>
+static int cluster_capacity() {
+  static int cap[64];
+  static bool known[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!known[dev]) {
+    auto kern = topk_cluster_kernel<F32, CS>;
+    int n = 0;
+    bool yes = set_smem_limit((const void*)kern, sizeof(ClSmem), "topk cluster") == SD_OK;
+    if (yes && CS > 8)
+      yes = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess;
+    if (yes) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(CS, 1, 1);
+      cfg.blockDim = dim3(kClThreads, 1, 1);
+      cfg.dynamicSmemBytes = sizeof(ClSmem);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = CS;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cap[dev] = n;
+    known[dev] = true;
+  }
+  return cap[dev];
+}
+
+template <bool F32, int CS>
+static int launch_cluster(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
+                          int64_t idx_stride, int32_t* count, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CS, (unsigned)rows, 1);
+  cfg.blockDim = dim3(kClThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(ClSmem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel<F32, CS>, scores, g, idx, idx_stride, count) !=
+      cudaSuccess)
+    return check_launch("topk_cluster");
+  return check_launch("topk_cluster");
+}
+
 template <bool F32>
 static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
                   int64_t idx_stride, int32_t* count, void* wsp, cudaStream_t st) {
@@ -649,6 +1106,17 @@ static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
     if (int rc_ = set_smem_limit((const void*)kern, smem, "topk: smem attribute")) return rc_;
     kern<<<(unsigned)rows, kFinThreads, smem, st>>>(scores, g, idx, idx_stride, count);
     return check_launch("topk_small");
+  }
+  if (g.M > g.k && g.M >= 4 * 16 && rows <= 65535) {
+    // the largest cluster whose row-clusters are all resident in one wave
+    if (rows <= cluster_capacity<F32, 16>())
+      return launch_cluster<F32, 16>(scores, rows, g, idx, idx_stride, count, st);
+    if (rows <= cluster_capacity<F32, 8>())
+      return launch_cluster<F32, 8>(scores, rows, g, idx, idx_stride, count, st);
+    if (rows <= cluster_capacity<F32, 4>())
+      return launch_cluster<F32, 4>(scores, rows, g, idx, idx_stride, count, st);
+    if (cluster_capacity<F32, 2>() > 0)
+      return launch_cluster<F32, 2>(scores, rows, g, idx, idx_stride, count, st);
   }
   Ws ws = carve(wsp, rows);
   const size_t smem_s = (size_t)kSample * 8 + kBins * 4;
