@@ -101,7 +101,9 @@ constexpr int kPsCtasPerSm = 3;
 struct PsSmem {
   uint32_t words[2][kPsChunk][kPsWords];  // 32 KB
   float Wt[2][kPsChunk][kPsBlocks];       // 16 KB
-  uint16_t sc[kD][kPsBlocks];             // 16 KB: scales of the active channels (by slot)
+  uint16_t sc[2][kD / 2][kPsBlocks];      // 16 KB: active channels' scales by slot: two
+                                          // 64-slot halves (current / prefetched tile),
+                                          // or one flat 128-slot buffer
   float red[4][kPsBlocks];
   float Cs[kPsBlocks];
   float qt[kD];
@@ -110,6 +112,8 @@ struct PsSmem {
   int slot_of[kD];
   int chan[kD];                           // channel of each slot
   uint16_t act[4 * kD];                   // active entries j * 4 + p, j ascending
+  uint8_t eslot[4 * kD];                  // slot of each entry's channel
+  float qp[4 * kD];                       // q~_j * 2^(3-p) per entry (exact scaling)
   int nact, nch;
 };
 
@@ -150,18 +154,43 @@ __device__ __forceinline__ void ps_stage_words(PsSmem& S, int buf, int e0, int n
   cp_async_commit();
 }
 
-// Folded weights of planes [e0, e0 + ne): Wt = (q~_j * s_j,blk) * 2^(3-p).
-__device__ __forceinline__ void ps_weights(PsSmem& S, int buf, int e0, int ne, int nbv) {
+// Folded weights of planes [e0, e0 + ne): Wt = (q~_j * 2^(3-p)) * s_j,blk, which
+// equals fl(q~_j * s_j,blk) * 2^(3-p) exactly (power-of-two scaling commutes with
+// rounding).
+__device__ __forceinline__ void ps_weights(PsSmem& S, const uint16_t* scb, int buf, int e0, int ne,
+                                           int nbv) {
   for (int x = threadIdx.x; x < ne * kPsBlocks; x += kPsThreads) {
     const int e = x / kPsBlocks, blk = x % kPsBlocks;
-    const int ent = S.act[e0 + e];
-    const int j = ent >> 2, p = ent & 3;
     float wv = 0.0f;
-    if (blk < nbv) {
-      const float sv = __half2float(__ushort_as_half(S.sc[S.slot_of[j]][blk]));
-      wv = __fmul_rn(__fmul_rn(S.qt[j], sv), (float)(8 >> p));
-    }
+    if (blk < nbv)
+      wv = __fmul_rn(S.qp[e0 + e],
+                     __half2float(__ushort_as_half(scb[S.eslot[e0 + e] * kPsBlocks + blk])));
     S.Wt[buf][e][blk] = wv;
+  }
+}
+
+// Issues the copies of a tile's active-channel scales into scb (one group with
+// the tile's first chunk of planes, which the caller stages).
+template <bool A16>
+__device__ __forceinline__ void ps_stage_scales(PsSmem& S, uint16_t* scb, const uint16_t* sc_tile,
+                                                int64_t sstride, int nch, int nbv) {
+  if (A16) {
+    // whole 16-byte segments (8 blocks) inside the valid blocks, the rest singly
+    for (int x = threadIdx.x; x < nch * 8; x += kPsThreads) {
+      const int sl = x >> 3, seg = x & 7;
+      const uint16_t* src = sc_tile + (int64_t)S.chan[sl] * sstride + seg * 8;
+      uint16_t* dst = scb + sl * kPsBlocks + seg * 8;
+      if (seg * 8 + 8 <= nbv) {
+        cp_async16(dst, src);
+      } else {
+        for (int k = 0; seg * 8 + k < nbv; ++k) dst[k] = src[k];
+      }
+    }
+  } else {
+    for (int x = threadIdx.x; x < nch * kPsBlocks; x += kPsThreads) {
+      const int sl = x / kPsBlocks, blk = x % kPsBlocks;
+      if (blk < nbv) scb[sl * kPsBlocks + blk] = sc_tile[(int64_t)S.chan[sl] * sstride + blk];
+    }
   }
 }
 
@@ -179,12 +208,16 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
   const int64_t t_begin = (int64_t)blockIdx.x * total_tiles / gridDim.x;
   const int64_t t_end = (int64_t)(blockIdx.x + 1) * total_tiles / gridDim.x;
   int64_t cur_bh = -1;
+  bool staged = false;  // this tile's scales and first chunk are already in flight
+  int sbuf = 0;         // scale half of this tile (double-buffered mode)
+  int wb0 = 0;          // words buffer holding this tile's first chunk
 
   for (int64_t tile = t_begin; tile < t_end; ++tile) {
     const int64_t bh = tile / tiles_per_row;
     const int64_t tok0 = (tile % tiles_per_row) * kPsTile;
     if (bh != cur_bh) {  // per-row prologue
       cur_bh = bh;
+      staged = false;
       const int b = (int)(bh / Hkv), h = (int)(bh % Hkv);
       if (threadIdx.x < kD) {
         const int j = threadIdx.x;
@@ -228,33 +261,24 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
         if (lane == 31) { S.nact = incl; S.nch = inclc; }
       }
       __syncthreads();
+      for (int e = threadIdx.x; e < S.nact; e += kPsThreads) {
+        const int ent = S.act[e], j = ent >> 2, p = ent & 3;
+        S.eslot[e] = (uint8_t)S.slot_of[j];
+        S.qp[e] = ldexpf(S.qt[j], 3 - p);
+      }
+      __syncthreads();
     }
     const int nact = S.nact, nch = S.nch;
+    const bool dbl = nch <= kD / 2;  // scales fit one half: prefetch the next tile
+    uint16_t* scb = dbl ? &S.sc[sbuf][0][0] : &S.sc[0][0][0];
     const int nwv = (int)imin64(kPsWords, (n - tok0) / 32);  // valid words (even)
     const int nbv = nwv / 2;                                  // valid scale blocks
     const uint32_t* pl_tile = planes + bh * kD * 4 * wstride + tok0 / 32;
-    const uint16_t* sc_tile = scales + bh * kD * sstride + tok0 / 64;
-
-    // stage the active channels' scales and the first chunk of planes
-    if (A16) {
-      // whole 16-byte segments (8 blocks) inside the valid blocks, the rest singly
-      for (int x = threadIdx.x; x < nch * 8; x += kPsThreads) {
-        const int sl = x >> 3, seg = x & 7;
-        const uint16_t* src = sc_tile + (int64_t)S.chan[sl] * sstride + seg * 8;
-        if (seg * 8 + 8 <= nbv) {
-          cp_async16(&S.sc[sl][seg * 8], src);
-        } else {
-          for (int k = 0; seg * 8 + k < nbv; ++k) S.sc[sl][seg * 8 + k] = src[k];
-        }
-      }
-    } else {
-      for (int x = threadIdx.x; x < nch * kPsBlocks; x += kPsThreads) {
-        const int sl = x / kPsBlocks, blk = x % kPsBlocks;
-        if (blk < nbv) S.sc[sl][blk] = sc_tile[(int64_t)S.chan[sl] * sstride + blk];
-      }
-    }
     const int ne0 = min(kPsChunk, nact);
-    ps_stage_words<A16>(S, 0, 0, ne0, pl_tile, wstride, nwv);
+    if (!staged) {
+      ps_stage_scales<A16>(S, scb, scales + bh * kD * sstride + tok0 / 64, sstride, nch, nbv);
+      ps_stage_words<A16>(S, wb0, 0, ne0, pl_tile, wstride, nwv);
+    }
     cp_async_wait_all();
     __syncthreads();
     // per-block constants C_blk (four partial sums per block) and the first weights
@@ -263,33 +287,47 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
       float acc = 0.0f;
       if (blk < nbv)
         for (int sl = part; sl < nch; sl += 4) {
-          const float sv = __half2float(__ushort_as_half(S.sc[sl][blk]));
+          const float sv = __half2float(__ushort_as_half(scb[sl * kPsBlocks + blk]));
           acc = __fadd_rn(acc, __fmul_rn(__fmul_rn(S.qt[S.chan[sl]], sv), S.offs[sl]));
         }
       S.red[part][blk] = acc;
     }
-    ps_weights(S, 0, 0, ne0, nbv);
+    ps_weights(S, scb, wb0, 0, ne0, nbv);
     __syncthreads();
     if (threadIdx.x < kPsBlocks)
       S.Cs[threadIdx.x] = __fadd_rn(__fadd_rn(S.red[0][threadIdx.x], S.red[1][threadIdx.x]),
                                     __fadd_rn(S.red[2][threadIdx.x], S.red[3][threadIdx.x]));
 
+    // the next tile of the same row can be staged during this tile's last chunk
+    const bool pref = dbl && tile + 1 < t_end && (tile + 1) / tiles_per_row == bh;
+    bool staged_next = false;
+    int next_wb0 = 0;
     float acc[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
-    for (int e0 = 0, buf = 0; e0 < nact; e0 += kPsChunk, buf ^= 1) {
+    int buf = wb0;
+    for (int e0 = 0; e0 < nact; e0 += kPsChunk, buf ^= 1) {
       const int ne = min(kPsChunk, nact - e0);
       const int e1 = e0 + kPsChunk;
       const int ne1 = min(kPsChunk, nact - e1);
-      if (ne1 > 0) ps_stage_words<A16>(S, buf ^ 1, e1, ne1, pl_tile, wstride, nwv);
-#pragma unroll 2
-      for (int e = 0; e < ne; ++e) {
-        const uint4 a = *reinterpret_cast<const uint4*>(&S.words[buf][e][warp * 16]);
-        const uint4 b = *reinterpret_cast<const uint4*>(&S.words[buf][e][warp * 16 + 4]);
-        const uint4 c = *reinterpret_cast<const uint4*>(&S.words[buf][e][warp * 16 + 8]);
-        const uint4 d = *reinterpret_cast<const uint4*>(&S.words[buf][e][warp * 16 + 12]);
-        const float4 wa = *reinterpret_cast<const float4*>(&S.Wt[buf][e][warp * 8]);
-        const float4 wb = *reinterpret_cast<const float4*>(&S.Wt[buf][e][warp * 8 + 4]);
+      if (ne1 > 0) {
+        ps_stage_words<A16>(S, buf ^ 1, e1, ne1, pl_tile, wstride, nwv);
+      } else if (pref) {
+        const int64_t ntok0 = tok0 + kPsTile;
+        const int nnwv = (int)imin64(kPsWords, (n - ntok0) / 32);
+        ps_stage_scales<A16>(S, &S.sc[sbuf ^ 1][0][0], scales + bh * kD * sstride + ntok0 / 64,
+                             sstride, nch, nnwv / 2);
+        ps_stage_words<A16>(S, buf ^ 1, 0, ne0, planes + bh * kD * 4 * wstride + ntok0 / 32,
+                            wstride, nnwv);
+        staged_next = true;
+        next_wb0 = buf ^ 1;
+      }
+      const uint4* wp = reinterpret_cast<const uint4*>(&S.words[buf][0][warp * 16]);
+      const float4* tp = reinterpret_cast<const float4*>(&S.Wt[buf][0][warp * 8]);
+#pragma unroll 4
+      for (int e = 0; e < ne; ++e, wp += kPsWords / 4, tp += kPsBlocks / 4) {
+        const uint4 a = wp[0], b = wp[1], c = wp[2], d = wp[3];
+        const float4 wa = tp[0], wb = tp[1];
         if (a.x & lanemask) acc[0] += wa.x;
         if (a.y & lanemask) acc[1] += wa.x;
         if (a.z & lanemask) acc[2] += wa.y;
@@ -307,11 +345,18 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
         if (d.z & lanemask) acc[14] += wb.w;
         if (d.w & lanemask) acc[15] += wb.w;
       }
-      if (ne1 > 0) ps_weights(S, buf ^ 1, e1, ne1, nbv);
-      cp_async_wait_all();
+      if (ne1 > 0) {
+        ps_weights(S, scb, buf ^ 1, e1, ne1, nbv);
+        cp_async_wait_all();  // the next chunk (nothing else is in flight)
+      }
       __syncthreads();
     }
-    if (nact == 0) __syncthreads();  // Cs written above must be visible
+    if (nact == 0) {
+      if (pref) {  // nothing to prefetch but the (empty) tile bookkeeping
+        staged_next = false;
+      }
+      __syncthreads();  // Cs written above must be visible
+    }
     float* orow = scores + bh * n + tok0;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
@@ -319,7 +364,15 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
       if (w < nwv) orow[w * 32 + lane] = acc[k] + S.Cs[w >> 1];
     }
     __syncthreads();  // buffers are reused by the next tile
+    staged = staged_next;
+    if (staged_next) {
+      sbuf ^= 1;
+      wb0 = next_wb0;
+    } else {
+      wb0 = 0;
+    }
   }
+  cp_async_wait_all();  // nothing may be left in flight at exit
 }
 
 static int sm_count() {
