@@ -25,6 +25,8 @@
 // CTA selects over the whole row itself: slower, same result.
 #include <cooperative_groups.h>
 
+#include <cmath>
+
 #include "sd_internal.cuh"
 
 namespace sd {
@@ -67,7 +69,19 @@ size_t topk_workspace_bytes(int64_t rows, int64_t n_units, const sd_select&) {
 struct Geo {  // per-row candidate geometry
   int64_t n_units, n_tokens;
   int lead, tail, M, k, block;
+  int r_sample;   // sample rank of the estimate (sample kernel), computed on the host
+  int r_cluster;  // the same for the cluster kernel's sample
 };
+
+// Rank in a sample of S (out of M candidates) whose key is a safe estimate of the
+// k-th largest: mu = k S / M members of the top k are expected in the sample, and
+// r = mu + 5 sqrt(mu) + 2 exceeds their count except with negligible probability.
+// Host-side: this GPU's double-precision rate is far too low for per-thread use.
+static int sample_rank(int64_t k, int64_t S, int64_t M) {
+  const double mu = (double)k * (double)S / (double)M;
+  const double r = std::ceil(mu + 5.0 * std::sqrt(mu) + 2.0);
+  return (int)(r < (double)S ? r : (double)S);
+}
 
 __host__ __device__ inline Geo make_geo(int64_t n_units, int64_t n_tokens, const sd_select& s) {
   Geo g;
@@ -78,6 +92,7 @@ __host__ __device__ inline Geo make_geo(int64_t n_units, int64_t n_tokens, const
   g.M = g.tail - g.lead;
   g.k = s.k;
   g.block = s.block;
+  g.r_sample = g.r_cluster = 0;
   return g;
 }
 
@@ -427,8 +442,7 @@ topk_sample_kernel(const void* __restrict__ scores, Geo g, Ws ws) {
   atomicMin(&kmin_s, mn);
   atomicMax(&kmax_s, mx);
   __syncthreads();
-  const double mu = (double)g.k * S / (double)g.M;
-  const int r = (int)fmin((double)S, ceil(mu + 5.0 * sqrt(mu) + 2.0));
+  const int r = g.r_sample;
   uint32_t T_key = 0, imax = (uint32_t)g.M;  // default: every unit is a candidate
   if (!nan_s && g.M > g.k && r < S) {
     const uint32_t kmin = kmin_s;
@@ -656,6 +670,7 @@ topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __res
 // CTA histograms its slice, the histograms are summed in CTA 0).
 namespace cg = cooperative_groups;
 constexpr int kLocCap = 2048;  // local candidates per CTA of a cluster
+constexpr int kClThreads = 1024;
 constexpr int kClBuf = kCap;   // CTA 0's gather buffer (samples, then candidates)
 
 struct ClSmem {
@@ -667,6 +682,7 @@ struct ClSmem {
   uint32_t kmin, kmax, nan, nbuf, ovf, ncand, nsel, mode;
   uint32_t T_key, imax;
   uint32_t cnt[16];
+  uint32_t pwh[(kClThreads / 32) * 256];  // per-warp radix histograms
 };
 
 // 4096 samples (2k for large k) keep the candidates near 3K at k = 512 and under
@@ -676,6 +692,13 @@ struct ClSmem {
 __host__ __device__ inline int cluster_sample_size(const Geo& g) {
   const int64_t s = g.k * 2 > 4096 ? (int64_t)g.k * 2 : 4096;
   return (int)imin64(g.M, imin64(s, kClBuf));
+}
+
+// max that propagates NaN (PTX max.NaN), so one compare screens four scores
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
 template <bool F32>
@@ -689,7 +712,64 @@ __device__ __forceinline__ uint32_t key_at(const float* frow, const int32_t* iro
   return key_of_i32(__ldg(irow + u));
 }
 
-constexpr int kClThreads = 512;
+// Radix select over 8-bit digits with per-warp private histograms (pwh: one
+// 256-bin table per warp), so crowded score ranges do not serialise on shared
+// atomics.  Finds T with at least `need` of C[0..c) >= T, all C < 2^nb; exact
+// (exactly `need` values >= T, C unique) unless max_passes stops it first, in
+// which case T is the lower bound of the bucket holding the need-th value.
+template <int NT>
+__device__ uint64_t radix_select_pw(const uint64_t* C, int c, uint32_t need, int nb,
+                                    int max_passes, uint32_t* pwh, uint32_t* out) {
+  constexpr int NW = NT / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* mine = pwh + warp * 256;
+  uint64_t prefix = 0;
+  int pos = nb;
+  uint32_t r = need;
+  for (int pass = 0; pos > 0 && pass < max_passes; ++pass) {
+    const int w = min(8, pos), npos = pos - w;
+    const uint32_t mask = (1u << w) - 1;
+#pragma unroll
+    for (int b = lane; b < 256; b += 32) mine[b] = 0;
+    __syncwarp();
+    for (int i = threadIdx.x; i < c; i += NT) {
+      const uint64_t x = C[i];
+      if ((x >> pos) == prefix) atomicAdd(&mine[(uint32_t)(x >> npos) & mask], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 8l..8l+7 (summed over the warps); suffix scan over lanes
+      uint32_t h[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t v = 0;
+        for (int ww = 0; ww < NW; ++ww) v += pwh[ww * 256 + lane * 8 + i];
+        h[i] = v;
+        tot += v;
+      }
+      uint32_t suf = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+        if (lane + o < 32) suf += y;
+      }
+      uint32_t above = suf - tot;  // bins of higher lanes
+#pragma unroll
+      for (int i = 7; i >= 0; --i) {
+        if (above < r && r <= above + h[i]) { out[0] = lane * 8 + i; out[1] = above; out[2] = h[i]; }
+        above += h[i];
+      }
+    }
+    __syncthreads();
+    const uint32_t d = out[0], ab = out[1], inb = out[2];
+    __syncthreads();
+    r -= ab;
+    prefix = (prefix << w) | d;
+    pos = npos;
+    if (inb == r) break;
+  }
+  return prefix << pos;
+}
 
 template <bool F32, int CS>
 __global__ void __launch_bounds__(kClThreads)
@@ -769,13 +849,11 @@ topk_cluster_kernel(const void* __restrict__ scores, Geo g, int32_t* __restrict_
   }
   cl.sync();
   if (rank == 0) {
-    const double mu = (double)k * Ssz / (double)M;
-    const int r = (int)fmin((double)Ssz, ceil(mu + 5.0 * sqrt(mu) + 2.0));
+    const int r = g.r_cluster;
     uint32_t T_key = 0, imax = (uint32_t)M;
     if (r < Ssz) {
       const int nb = bits_of(S.kmax - S.kmin) + bI;
-      const uint64_t T = radix_threshold<NT>(S.buf, Ssz, (uint32_t)r, 0, nb, S.hist, S.scratch,
-                                             S.out, 2);
+      const uint64_t T = radix_select_pw<NT>(S.buf, Ssz, (uint32_t)r, nb, 3, S.pwh, S.out);
       T_key = S.kmin + (uint32_t)(T >> bI);
       imax = (uint32_t)(M - 1) - (uint32_t)(T & imask);
     }
@@ -795,28 +873,45 @@ topk_cluster_kernel(const void* __restrict__ scores, Geo g, int32_t* __restrict_
     const int a_lo = u_lo & ~3;
     const int nu = (int)g.n_units;
     const bool vec = ((uintptr_t)frow % 16 == 0) && (nu % 4 == 0);
-    constexpr int kG = 8;  // groups of 4 units in flight per thread
-    for (int b0 = a_lo; b0 < u_hi; b0 += NT * 4 * kG) {  // uniform trip count
-      // issue every load first, convert afterwards: a value used right after its
-      // own load would serialise the loads into round trips
-      uint4 raw[kG];
+    constexpr int kG = 4;  // groups of 4 units per thread per batch
+    // Batches are software-pipelined: batch i+1's loads are issued before batch i
+    // is tested, so every thread keeps 8 to 16 loads in flight.
+    const uint32_t* src = F32 ? reinterpret_cast<const uint32_t*>(frow) : reinterpret_cast<const uint32_t*>(irow);
+    auto load_batch = [&](int b0, uint4 (&raw)[kG]) {
 #pragma unroll
       for (int gi = 0; gi < kG; ++gi) {
         const int gs = b0 + (gi * NT + tid) * 4;
         if (vec && gs >= u_lo && gs + 4 <= u_hi) {
-          raw[gi] = __ldg(reinterpret_cast<const uint4*>(F32 ? (const void*)(frow + gs) : (const void*)(irow + gs)));
+          raw[gi] = __ldg(reinterpret_cast<const uint4*>(src + gs));
         } else {
-          const uint32_t* src = F32 ? reinterpret_cast<const uint32_t*>(frow) : reinterpret_cast<const uint32_t*>(irow);
           raw[gi].x = (gs + 0 >= u_lo && gs + 0 < u_hi) ? __ldg(src + gs + 0) : 0u;
           raw[gi].y = (gs + 1 >= u_lo && gs + 1 < u_hi) ? __ldg(src + gs + 1) : 0u;
           raw[gi].z = (gs + 2 >= u_lo && gs + 2 < u_hi) ? __ldg(src + gs + 2) : 0u;
           raw[gi].w = (gs + 3 >= u_lo && gs + 3 < u_hi) ? __ldg(src + gs + 3) : 0u;
         }
       }
+    };
+    constexpr int kBatch = NT * 4 * kG;
+    uint4 cur[kG], nxt[kG];
+    if (a_lo < u_hi) load_batch(a_lo, cur);
+    for (int b0 = a_lo; b0 < u_hi; b0 += kBatch) {  // uniform trip count
+      if (b0 + kBatch < u_hi) load_batch(b0 + kBatch, nxt);
 #pragma unroll
       for (int gi = 0; gi < kG; ++gi) {
         const int gs = b0 + (gi * NT + tid) * 4;
-        const uint32_t rv[4] = {raw[gi].x, raw[gi].y, raw[gi].z, raw[gi].w};
+        const uint32_t rv[4] = {cur[gi].x, cur[gi].y, cur[gi].z, cur[gi].w};
+        // group pre-test: almost every group lies below the threshold; only a
+        // group whose maximum reaches it (or holds a NaN) is examined unit by unit
+        bool maybe;
+        if (F32) {
+          const float m = fmax_nan(fmax_nan(__uint_as_float(rv[0]), __uint_as_float(rv[1])),
+                                   fmax_nan(__uint_as_float(rv[2]), __uint_as_float(rv[3])));
+          maybe = !(m < Tf);  // true for m >= Tf and for NaN
+        } else {
+          const int32_t m = max(max((int32_t)rv[0], (int32_t)rv[1]), max((int32_t)rv[2], (int32_t)rv[3]));
+          maybe = m >= Ti;
+        }
+        if (!__any_sync(0xFFFFFFFFu, maybe || take_all)) continue;
         const bool inner = gs >= u_lo && gs + 4 <= u_hi;
         uint32_t hit = 0;
 #pragma unroll
@@ -856,6 +951,8 @@ topk_cluster_kernel(const void* __restrict__ scores, Geo g, int32_t* __restrict_
             ++basep;
           }
       }
+#pragma unroll
+      for (int gi = 0; gi < kG; ++gi) cur[gi] = nxt[gi];
     }
     if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) atomicOr(&S.nan, 1u);
   }
@@ -1136,6 +1233,10 @@ int launch_topk(int score_type, const void* scores, int64_t rows, int64_t n_unit
                 int64_t n_tokens, const sd_select& sel, int32_t* idx, int64_t idx_stride,
                 int32_t* count, void* ws, size_t, cudaStream_t st) {
   Geo g = make_geo(n_units, n_tokens, sel);
+  if (g.M > 0) {
+    g.r_sample = sample_rank(g.k, sample_size(g), g.M);
+    g.r_cluster = sample_rank(g.k, cluster_sample_size(g), g.M);
+  }
   if (score_type == SD_SCORE_F32)
     return topk_t<true>(scores, rows, g, idx, idx_stride, count, ws, st);
   return topk_t<false>(scores, rows, g, idx, idx_stride, count, ws, st);
