@@ -172,6 +172,28 @@ def test_plane_scores(sd, budget, mode, ncap):
     check_scores(host(scores, np.float32), ref, l1, "plane scores")
 
 
+@pytest.mark.parametrize("B,Hkv,n,budget,mode", [(1, 8, 262144, 56, 0), (2, 4, 300 * 512 + 192, 56, 0),
+                                                 (1, 8, 262144, 80, 1)])
+def test_plane_scores_long_ranges(sd, B, Hkv, n, budget, mode):
+    # more 512-token units than resident CTAs: each CTA walks several tiles, ranges
+    # cross row ends, the next tile is prefetched (at most 64 active channels) or
+    # not (80 channels of the fixed plan), and a row may end in a partial unit
+    cfg = synth.config(4, B=B, Hq=4 * Hkv, Hkv=Hkv, n=n)
+    inp = synth.make_inputs(cfg, with_v=False)
+    shp = shape_of(sd, cfg)
+    ref_p, ref_s = oracle.plane_build(inp.K)
+    plan_ref = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, mode, budget)
+    ref, l1 = oracle.plane_score(ref_p, ref_s, plan_ref, inp.q, with_l1=True)
+    q = dev(inp.q)
+    plan = empty(plan_ref.shape, np.uint8)
+    sd.sd_plan(shp, q, dev(inp.sigma2), mode, budget, plan)
+    scores = empty((cfg.B, cfg.Hkv, cfg.n), np.float32)
+    sd.sd_score(sd.SD_IDX_PLANES, shp, dev(ref_p), dev(ref_s), q, plan, scores)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(plan, np.uint8), plan_ref)
+    check_scores(host(scores, np.float32), ref, l1, "plane scores")
+
+
 @pytest.mark.parametrize("G,n", [(4, 16 * 1024), (8, 16 * 100 + 9), (1, 16 * 33)])
 def test_quest_scores(sd, G, n):
     cfg = synth.config(3, B=3, Hq=2 * G, Hkv=2, n=n, planted=4)

@@ -83,15 +83,23 @@ int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsi
 // So each planned plane costs one bit test and one predicated add per token --
 // the in-HBM scan is bound by these operations, as the Fathom page notes.
 //
-// A CTA scores tiles of 4096 tokens (128 words per plane, 64 scale blocks) of one
-// (sequence, KV head); the grid is persistent (3 CTAs per SM), each CTA taking a
-// contiguous range of tiles so the per-row prologue (group-summed query, active
-// plane list) is paid once per row change.  Per tile: the active channels' scales
+// A CTA scores tiles of up to 4096 tokens (128 words per plane, 64 scale blocks) of
+// one (sequence, KV head); the grid is persistent (3 CTAs per SM).  The rows' tokens
+// are cut into 512-token units and each CTA takes an equal contiguous range of
+// units (so every CTA has the same work to within one unit), walked as tiles of at
+// most 8 units that end at row ends; the per-row prologue (group-summed query,
+// active plane list) is paid once per row change.  Per tile: the active channels' scales
 // are staged once; planes are staged 32 at a time with cp.async into a double
 // buffer while the previous 32 are consumed; folded weights are built per stage.
-// Warp w owns words 16w..16w+15 (blocks 8w..8w+7); lane l owns bit l of each.
+// Each lane owns one word (32 tokens, one scale block) of the tile: lane l of warp
+// w holds word 32 (w mod 4) + l, so per plane a warp reads 32 distinct words and
+// 16 distinct weights (one shared-memory wavefront each) and then runs 32 bit
+// tests and predicated adds on registers.  Warps 0-3 take the even planes of each
+// stage, warps 4-7 the odd ones; the two partial sums meet in shared memory once
+// per tile.
 // =====================================================================================
 constexpr int kPsTile = 4096;
+constexpr int kPsUnit = 512;             // work split granularity (16-byte aligned copies)
 constexpr int kPsWords = kPsTile / 32;   // 128
 constexpr int kPsBlocks = kPsTile / 64;  // 64
 constexpr int kPsChunk = 32;             // planes per stage
@@ -104,10 +112,10 @@ struct PsSmem {
   uint16_t sc[2][kD / 2][kPsBlocks];      // 16 KB: active channels' scales by slot: two
                                           // 64-slot halves (current / prefetched tile),
                                           // or one flat 128-slot buffer
-  float red[4][kPsBlocks];
+  float red[8][kPsBlocks];
   float Cs[kPsBlocks];
   float qt[kD];
-  float offs[kD];                         // h(t) - 8 per slot
+  float qo[kD];                           // q~_j * (h(t_j) - 8) per slot
   int tb[kD];
   int slot_of[kD];
   int chan[kD];                           // channel of each slot
@@ -116,6 +124,25 @@ struct PsSmem {
   float qp[4 * kD];                       // q~_j * 2^(3-p) per entry (exact scaling)
   int nact, nch;
 };
+
+// The tile starting at unit u of a CTA's range [.., u_end): its row, first token
+// and unit count.
+struct PsTile {
+  int64_t bh, tok0;
+  int nu;
+};
+__device__ __forceinline__ PsTile ps_tile_at(int64_t u, int64_t u_end, int64_t upr) {
+  PsTile t;
+  t.bh = u / upr;
+  const int64_t ur = u - t.bh * upr;
+  t.tok0 = ur * kPsUnit;
+  t.nu = (int)imin64(imin64(kPsTile / kPsUnit, upr - ur), u_end - u);
+  return t;
+}
+// valid words of a tile (even: n is a multiple of 64)
+__device__ __forceinline__ int ps_valid_words(const PsTile& t, int64_t n) {
+  return (int)imin64(t.nu * (kPsUnit / 32), (n - t.tok0) / 32);
+}
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   unsigned d = (unsigned)__cvta_generic_to_shared(smem);
@@ -133,22 +160,20 @@ template <bool A16>
 __device__ __forceinline__ void ps_stage_words(PsSmem& S, int buf, int e0, int ne,
                                                const uint32_t* pl_tile, int64_t wstride,
                                                int nwv) {
-  if (A16) {
-    // whole 16-byte segments inside the valid words, then an 8-byte remainder
-    // (nwv is even): no copy reads past the last valid word of a plane row
-    for (int x = threadIdx.x; x < ne * (kPsWords / 4); x += kPsThreads) {
-      const int e = x / (kPsWords / 4), seg = x % (kPsWords / 4);
-      const uint32_t* src = pl_tile + (int64_t)S.act[e0 + e] * wstride + seg * 4;
-      if (seg * 4 + 4 <= nwv)
-        cp_async16(&S.words[buf][e][seg * 4], src);
-      else if (seg * 4 + 2 == nwv)
-        cp_async8(&S.words[buf][e][seg * 4], src);
-    }
-  } else {
-    for (int x = threadIdx.x; x < ne * (kPsWords / 2); x += kPsThreads) {
-      const int e = x / (kPsWords / 2), seg = x % (kPsWords / 2);
-      if (seg * 2 < nwv)
-        cp_async8(&S.words[buf][e][seg * 2], pl_tile + (int64_t)S.act[e0 + e] * wstride + seg * 2);
+  // one warp per plane row
+  const int lane = threadIdx.x & 31;
+  for (int e = threadIdx.x >> 5; e < ne; e += kPsThreads / 32) {
+    const uint32_t* src = pl_tile + (int64_t)S.act[e0 + e] * wstride;
+    uint32_t* dst = &S.words[buf][e][0];
+    if (A16) {
+      // whole 16-byte segments inside the valid words, then an 8-byte remainder
+      // (nwv is even): no copy reads past the last valid word of a plane row
+      if (lane * 4 + 4 <= nwv)
+        cp_async16(dst + lane * 4, src + lane * 4);
+      else if (lane * 4 + 2 == nwv)
+        cp_async8(dst + lane * 4, src + lane * 4);
+    } else {
+      for (int sg = lane; sg * 2 < nwv; sg += 32) cp_async8(dst + sg * 2, src + sg * 2);
     }
   }
   cp_async_commit();
@@ -157,15 +182,19 @@ __device__ __forceinline__ void ps_stage_words(PsSmem& S, int buf, int e0, int n
 // Folded weights of planes [e0, e0 + ne): Wt = (q~_j * 2^(3-p)) * s_j,blk, which
 // equals fl(q~_j * s_j,blk) * 2^(3-p) exactly (power-of-two scaling commutes with
 // rounding).
+// Only valid blocks are written: the other weights are read only by lanes whose
+// words lie past the tile's end, whose sums are never stored.
 __device__ __forceinline__ void ps_weights(PsSmem& S, const uint16_t* scb, int buf, int e0, int ne,
                                            int nbv) {
-  for (int x = threadIdx.x; x < ne * kPsBlocks; x += kPsThreads) {
-    const int e = x / kPsBlocks, blk = x % kPsBlocks;
-    float wv = 0.0f;
-    if (blk < nbv)
-      wv = __fmul_rn(S.qp[e0 + e],
-                     __half2float(__ushort_as_half(scb[S.eslot[e0 + e] * kPsBlocks + blk])));
-    S.Wt[buf][e][blk] = wv;
+  // blocks b2, b2 + 1; for odd nbv the last pair's second weight is not valid (and
+  // is read only by lanes past the end)
+  const int b2 = (threadIdx.x & 31) * 2;
+  if (b2 >= nbv) return;
+  for (int e = threadIdx.x >> 5; e < ne; e += kPsThreads / 32) {
+    const float qp = S.qp[e0 + e];
+    const __half2 sv = *reinterpret_cast<const __half2*>(&scb[S.eslot[e0 + e] * kPsBlocks + b2]);
+    const float2 f = __half22float2(sv);
+    *reinterpret_cast<float2*>(&S.Wt[buf][e][b2]) = make_float2(__fmul_rn(qp, f.x), __fmul_rn(qp, f.y));
   }
 }
 
@@ -198,23 +227,22 @@ template <int G, bool A16>
 __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm)
 score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
                     const uint8_t* __restrict__ plan, const uint16_t* __restrict__ q, int Hq,
-                    int Hkv, int64_t n, int64_t ncap, int64_t tiles_per_row, int64_t total_tiles,
+                    int Hkv, int64_t n, int64_t ncap, int64_t units_per_row, int64_t total_units,
                     float* __restrict__ scores) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PsSmem& S = *reinterpret_cast<PsSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t lanemask = 1u << lane;
   const int64_t wstride = ncap / 32, sstride = ncap / 64;
-  const int64_t t_begin = (int64_t)blockIdx.x * total_tiles / gridDim.x;
-  const int64_t t_end = (int64_t)(blockIdx.x + 1) * total_tiles / gridDim.x;
+  const int64_t u_begin = (int64_t)blockIdx.x * total_units / gridDim.x;
+  const int64_t u_end = (int64_t)(blockIdx.x + 1) * total_units / gridDim.x;
   int64_t cur_bh = -1;
   bool staged = false;  // this tile's scales and first chunk are already in flight
   int sbuf = 0;         // scale half of this tile (double-buffered mode)
   int wb0 = 0;          // words buffer holding this tile's first chunk
 
-  for (int64_t tile = t_begin; tile < t_end; ++tile) {
-    const int64_t bh = tile / tiles_per_row;
-    const int64_t tok0 = (tile % tiles_per_row) * kPsTile;
+  for (int64_t u = u_begin; u < u_end;) {
+    const PsTile T = ps_tile_at(u, u_end, units_per_row);
+    const int64_t bh = T.bh, tok0 = T.tok0, u_next = u + T.nu;
     if (bh != cur_bh) {  // per-row prologue
       cur_bh = bh;
       staged = false;
@@ -252,7 +280,7 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
           if (c[k] > 0) {
             S.slot_of[j] = slot;
             S.chan[slot] = j;
-            S.offs[slot] = c[k] < 4 ? (float)((1 << (3 - c[k])) - 8) : -8.0f;
+            S.qo[slot] = __fmul_rn(S.qt[j], c[k] < 4 ? (float)((1 << (3 - c[k])) - 8) : -8.0f);
             ++slot;
           } else {
             S.slot_of[j] = 0;
@@ -271,8 +299,8 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
     const int nact = S.nact, nch = S.nch;
     const bool dbl = nch <= kD / 2;  // scales fit one half: prefetch the next tile
     uint16_t* scb = dbl ? &S.sc[sbuf][0][0] : &S.sc[0][0][0];
-    const int nwv = (int)imin64(kPsWords, (n - tok0) / 32);  // valid words (even)
-    const int nbv = nwv / 2;                                  // valid scale blocks
+    const int nwv = ps_valid_words(T, n);  // valid words (even)
+    const int nbv = nwv / 2;               // valid scale blocks
     const uint32_t* pl_tile = planes + bh * kD * 4 * wstride + tok0 / 32;
     const int ne0 = min(kPsChunk, nact);
     if (!staged) {
@@ -283,28 +311,35 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
     __syncthreads();
     // per-block constants C_blk (four partial sums per block) and the first weights
     {
-      const int blk = threadIdx.x & (kPsBlocks - 1), part = threadIdx.x >> 6;
-      float acc = 0.0f;
-      if (blk < nbv)
-        for (int sl = part; sl < nch; sl += 4) {
-          const float sv = __half2float(__ushort_as_half(scb[sl * kPsBlocks + blk]));
-          acc = __fadd_rn(acc, __fmul_rn(__fmul_rn(S.qt[S.chan[sl]], sv), S.offs[sl]));
+      const int b2 = (threadIdx.x & 31) * 2, part = threadIdx.x >> 5;
+      float a0 = 0.0f, a1 = 0.0f;
+      if (b2 < nbv)
+        for (int sl = part; sl < nch; sl += kPsThreads / 32) {
+          const float2 f =
+              __half22float2(*reinterpret_cast<const __half2*>(&scb[sl * kPsBlocks + b2]));
+          const float qo = S.qo[sl];
+          a0 = __fadd_rn(a0, __fmul_rn(qo, f.x));
+          a1 = __fadd_rn(a1, __fmul_rn(qo, f.y));
         }
-      S.red[part][blk] = acc;
+      *reinterpret_cast<float2*>(&S.red[part][b2]) = make_float2(a0, a1);
     }
     ps_weights(S, scb, wb0, 0, ne0, nbv);
     __syncthreads();
-    if (threadIdx.x < kPsBlocks)
-      S.Cs[threadIdx.x] = __fadd_rn(__fadd_rn(S.red[0][threadIdx.x], S.red[1][threadIdx.x]),
-                                    __fadd_rn(S.red[2][threadIdx.x], S.red[3][threadIdx.x]));
+    if (threadIdx.x < kPsBlocks) {
+      float c = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) c = __fadd_rn(c, S.red[k][threadIdx.x]);
+      S.Cs[threadIdx.x] = c;
+    }
 
     // the next tile of the same row can be staged during this tile's last chunk
-    const bool pref = dbl && tile + 1 < t_end && (tile + 1) / tiles_per_row == bh;
+    const bool pref = dbl && u_next < u_end && u_next / units_per_row == bh;
     bool staged_next = false;
     int next_wb0 = 0;
-    float acc[16];
+    const int half = warp >> 2, wl = (warp & 3) * 32 + lane;  // plane parity, word
+    float acc[32];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.0f;
+    for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
     int buf = wb0;
     for (int e0 = 0; e0 < nact; e0 += kPsChunk, buf ^= 1) {
       const int ne = min(kPsChunk, nact - e0);
@@ -313,8 +348,9 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
       if (ne1 > 0) {
         ps_stage_words<A16>(S, buf ^ 1, e1, ne1, pl_tile, wstride, nwv);
       } else if (pref) {
-        const int64_t ntok0 = tok0 + kPsTile;
-        const int nnwv = (int)imin64(kPsWords, (n - ntok0) / 32);
+        const PsTile NT = ps_tile_at(u_next, u_end, units_per_row);
+        const int64_t ntok0 = NT.tok0;
+        const int nnwv = ps_valid_words(NT, n);
         ps_stage_scales<A16>(S, &S.sc[sbuf ^ 1][0][0], scales + bh * kD * sstride + ntok0 / 64,
                              sstride, nch, nnwv / 2);
         ps_stage_words<A16>(S, buf ^ 1, 0, ne0, planes + bh * kD * 4 * wstride + ntok0 / 32,
@@ -322,28 +358,16 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
         staged_next = true;
         next_wb0 = buf ^ 1;
       }
-      const uint4* wp = reinterpret_cast<const uint4*>(&S.words[buf][0][warp * 16]);
-      const float4* tp = reinterpret_cast<const float4*>(&S.Wt[buf][0][warp * 8]);
-#pragma unroll 4
-      for (int e = 0; e < ne; ++e, wp += kPsWords / 4, tp += kPsBlocks / 4) {
-        const uint4 a = wp[0], b = wp[1], c = wp[2], d = wp[3];
-        const float4 wa = tp[0], wb = tp[1];
-        if (a.x & lanemask) acc[0] += wa.x;
-        if (a.y & lanemask) acc[1] += wa.x;
-        if (a.z & lanemask) acc[2] += wa.y;
-        if (a.w & lanemask) acc[3] += wa.y;
-        if (b.x & lanemask) acc[4] += wa.z;
-        if (b.y & lanemask) acc[5] += wa.z;
-        if (b.z & lanemask) acc[6] += wa.w;
-        if (b.w & lanemask) acc[7] += wa.w;
-        if (c.x & lanemask) acc[8] += wb.x;
-        if (c.y & lanemask) acc[9] += wb.x;
-        if (c.z & lanemask) acc[10] += wb.y;
-        if (c.w & lanemask) acc[11] += wb.y;
-        if (d.x & lanemask) acc[12] += wb.z;
-        if (d.y & lanemask) acc[13] += wb.z;
-        if (d.z & lanemask) acc[14] += wb.w;
-        if (d.w & lanemask) acc[15] += wb.w;
+      const uint32_t* wp = &S.words[buf][half][wl];
+      const float* tp = &S.Wt[buf][half][wl >> 1];
+      const int ne_w = (warp & 3) * 32 < nwv ? ne : 0;  // warps past the tile's end idle
+#pragma unroll 2
+      for (int e = half; e < ne_w; e += 2, wp += 2 * kPsWords, tp += 2 * kPsBlocks) {
+        const uint32_t w = *wp;
+        const float wt = *tp;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (w & (1u << i)) acc[i] += wt;
       }
       if (ne1 > 0) {
         ps_weights(S, scb, buf ^ 1, e1, ne1, nbv);
@@ -357,13 +381,29 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
       }
       __syncthreads();  // Cs written above must be visible
     }
-    float* orow = scores + bh * n + tok0;
+    // odd-plane partial sums through the (now idle) weight buffers: lane l's eight
+    // float4s go to 16-byte slots k ^ (l & 7), so each quarter-warp hits 8 distinct
+    // bank groups
+    float4* red = reinterpret_cast<float4*>(&S.Wt[0][0][0]) + ((warp & 3) * 32 + lane) * 8;
+    const int sw = lane & 7;
+    if (half == 1) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int w = warp * 16 + k;
-      if (w < nwv) orow[w * 32 + lane] = acc[k] + S.Cs[w >> 1];
+      for (int k = 0; k < 8; ++k)
+        red[k ^ sw] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+    }
+    __syncthreads();
+    if (half == 0 && wl < nwv) {
+      const float c = S.Cs[wl >> 1];
+      float4* orow = reinterpret_cast<float4*>(scores + bh * n + tok0 + wl * 32);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 o = red[k ^ sw];
+        orow[k] = make_float4((acc[4 * k] + o.x) + c, (acc[4 * k + 1] + o.y) + c,
+                              (acc[4 * k + 2] + o.z) + c, (acc[4 * k + 3] + o.w) + c);
+      }
     }
     __syncthreads();  // buffers are reused by the next tile
+    u = u_next;
     staged = staged_next;
     if (staged_next) {
       sbuf ^= 1;
@@ -394,11 +434,11 @@ static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scale
   auto kern = score_planes_kernel<G, A16>;
   if (int rc = set_smem_limit((const void*)kern, sizeof(PsSmem), "score_planes: smem attribute"))
     return rc;
-  const int64_t tiles_per_row = (s.n + kPsTile - 1) / kPsTile;
-  const int64_t total = tiles_per_row * s.B * s.Hkv;
+  const int64_t units_per_row = (s.n + kPsUnit - 1) / kPsUnit;
+  const int64_t total = units_per_row * s.B * s.Hkv;
   const int64_t grid = imin64(total, (int64_t)sm_count() * kPsCtasPerSm);
   kern<<<(unsigned)grid, kPsThreads, sizeof(PsSmem), st>>>(planes, scales, plan, q, s.Hq, s.Hkv,
-                                                          s.n, s.ncap, tiles_per_row, total,
+                                                          s.n, s.ncap, units_per_row, total,
                                                           scores);
   return check_launch("score_planes");
 }
