@@ -83,187 +83,274 @@ int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsi
 // So each planned plane costs one bit test and one predicated add per token --
 // the in-HBM scan is bound by these operations, as the Fathom page notes.
 //
-// A CTA scores tiles of up to 4096 tokens (128 words per plane, 64 scale blocks) of
-// one (sequence, KV head); the grid is persistent (3 CTAs per SM).  The rows' tokens
-// are cut into 512-token units and each CTA takes an equal contiguous range of
-// units (so every CTA has the same work to within one unit), walked as tiles of at
-// most 8 units that end at row ends; the per-row prologue (group-summed query,
-// active plane list) is paid once per row change.  Per tile: the active channels' scales
-// are staged once; planes are staged 32 at a time with cp.async into a double
-// buffer while the previous 32 are consumed; folded weights are built per stage.
-// Each lane owns one word (32 tokens, one scale block) of the tile: lane l of warp
-// w holds word 32 (w mod 4) + l, so per plane a warp reads 32 distinct words and
-// 16 distinct weights (one shared-memory wavefront each) and then runs 32 bit
-// tests and predicated adds on registers.  Warps 0-3 take the even planes of each
-// stage, warps 4-7 the odd ones; the two partial sums meet in shared memory once
-// per tile.
+// Work split.  The rows' tokens are cut into 512-token units and each CTA takes an
+// equal contiguous range of units (every CTA has the same work to within one unit),
+// walked as tiles of at most 8 units (4096 tokens: 128 words per plane, 64 scale
+// blocks) that end at row ends.  A tile's active planes are consumed in chunks of
+// up to 32.
+//
+// Warp roles (384 threads, 2 CTAs per SM).  Four helper warps stage each chunk's
+// plane words with cp.async into a ring of three slots and write its folded
+// weights (and, for a tile's first chunk, stage the tile's scales and form its
+// per-block constants), then hand the slot over.  Eight compute warps only run the
+// bit tests and adds: lane l of compute warp w owns word 32 (w mod 4) + l of the
+// tile (32 tokens of one scale block), so per plane a warp reads 32 distinct words
+// and 16 distinct weights and runs 32 bit tests and predicated adds on registers.
+// Warps 0-3 take a chunk's even planes, warps 4-7 its odd ones; the two partial
+// sums meet in shared memory at the tile's end.  Slots are handed over with named
+// barriers: FULL[s] (helpers arrive, compute warps wait) and EMPTY[s] (compute warps
+// arrive, helpers wait); a last FULL carries an end marker.
 // =====================================================================================
 constexpr int kPsTile = 4096;
 constexpr int kPsUnit = 512;             // work split granularity (16-byte aligned copies)
 constexpr int kPsWords = kPsTile / 32;   // 128
 constexpr int kPsBlocks = kPsTile / 64;  // 64
-constexpr int kPsChunk = 32;             // planes per stage
-constexpr int kPsThreads = 256;
-constexpr int kPsCtasPerSm = 3;
+constexpr int kPsChunk = 32;             // planes per slot
+constexpr int kPsSlots = 3;
+constexpr int kPsCompute = 256, kPsHelpers = 128;
+constexpr int kPsThreads = kPsCompute + kPsHelpers;
+constexpr int kPsCtasPerSm = 2;
+// named barrier ids (0 is __syncthreads, which the kernel does not use)
+constexpr int kBarFull = 1, kBarEmpty = kBarFull + kPsSlots, kBarHelp = kBarEmpty + kPsSlots,
+              kBarComp = kBarHelp + 1;
+constexpr int kSlotFirst = 1, kSlotLast = 2, kSlotEnd = 4;
+
+struct PsSlot {
+  int ne;     // planes in the chunk (0 for a tile with no active plane)
+  int flags;  // kSlotFirst / kSlotLast of its tile, kSlotEnd
+  int cs;     // the tile's entry in the Cs ring
+  int nwv;    // the tile's valid words
+  int64_t out;  // the tile's first score
+};
 
 struct PsSmem {
-  uint32_t words[2][kPsChunk][kPsWords];  // 32 KB
-  float Wt[2][kPsChunk][kPsBlocks];       // 16 KB
-  uint16_t sc[2][kD / 2][kPsBlocks];      // 16 KB: active channels' scales by slot: two
-                                          // 64-slot halves (current / prefetched tile),
-                                          // or one flat 128-slot buffer
-  float red[8][kPsBlocks];
-  float Cs[kPsBlocks];
+  uint32_t words[kPsSlots][kPsChunk][kPsWords];  // 48 KB
+  float Wt[kPsSlots][kPsChunk][kPsBlocks];       // 24 KB
+  float4 red[kPsWords * 8];                      // 16 KB: odd-plane partial sums
+  uint16_t sc[kD][kPsBlocks];                    // 16 KB: active channels' scales by slot:
+                                                 // two 64-slot halves (alternate tiles) or,
+                                                 // past 64 active channels, one flat buffer
+  float Cs[4][kPsBlocks];                        // per-block constants of 4 tiles in flight
+  float hred[4][kPsBlocks];
+  PsSlot slot[kPsSlots];
   float qt[kD];
-  float qo[kD];                           // q~_j * (h(t_j) - 8) per slot
+  float qo[kD];                                  // q~_j * (h(t_j) - 8) per slot
   int tb[kD];
   int slot_of[kD];
-  int chan[kD];                           // channel of each slot
-  uint16_t act[4 * kD];                   // active entries j * 4 + p, j ascending
-  uint8_t eslot[4 * kD];                  // slot of each entry's channel
-  float qp[4 * kD];                       // q~_j * 2^(3-p) per entry (exact scaling)
+  int chan[kD];                                  // channel of each slot
+  uint16_t act[4 * kD];                          // active entries j * 4 + p, j ascending
+  uint8_t eslot[4 * kD];                         // slot of each entry's channel
+  float qp[4 * kD];                              // q~_j * 2^(3-p) per entry (exact scaling)
   int nact, nch;
 };
 
-// The tile starting at unit u of a CTA's range [.., u_end): its row, first token
-// and unit count.
-struct PsTile {
-  int64_t bh, tok0;
-  int nu;
-};
-__device__ __forceinline__ PsTile ps_tile_at(int64_t u, int64_t u_end, int64_t upr) {
-  PsTile t;
-  t.bh = u / upr;
-  const int64_t ur = u - t.bh * upr;
-  t.tok0 = ur * kPsUnit;
-  t.nu = (int)imin64(imin64(kPsTile / kPsUnit, upr - ur), u_end - u);
-  return t;
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
-// valid words of a tile (even: n is a multiple of 64)
-__device__ __forceinline__ int ps_valid_words(const PsTile& t, int64_t n) {
-  return (int)imin64(t.nu * (kPsUnit / 32), (n - t.tok0) / 32);
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src));
 }
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  unsigned d = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem));
-}
-__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
-  unsigned d = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(gmem));
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ void nb_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void nb_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
 
-// Issues the copies of planes [e0, e0 + ne) of the tile into words[buf].
-template <bool A16>
-__device__ __forceinline__ void ps_stage_words(PsSmem& S, int buf, int e0, int ne,
-                                               const uint32_t* pl_tile, int64_t wstride,
-                                               int nwv) {
-  // one warp per plane row
-  const int lane = threadIdx.x & 31;
-  for (int e = threadIdx.x >> 5; e < ne; e += kPsThreads / 32) {
-    const uint32_t* src = pl_tile + (int64_t)S.act[e0 + e] * wstride;
-    uint32_t* dst = &S.words[buf][e][0];
-    if (A16) {
-      // whole 16-byte segments inside the valid words, then an 8-byte remainder
-      // (nwv is even): no copy reads past the last valid word of a plane row
-      if (lane * 4 + 4 <= nwv)
-        cp_async16(dst + lane * 4, src + lane * 4);
-      else if (lane * 4 + 2 == nwv)
-        cp_async8(dst + lane * 4, src + lane * 4);
-    } else {
-      for (int sg = lane; sg * 2 < nwv; sg += 32) cp_async8(dst + sg * 2, src + sg * 2);
+// acc[i] += wt for every set bit i of w (a bit test and a predicated add per bit)
+__device__ __forceinline__ void ps_bits(float (&acc)[32], uint32_t w, float wt) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    asm("{\n\t.reg .pred p;\n\t.reg .b32 t;\n\tand.b32 t, %1, %2;\n\tsetp.ne.b32 p, t, 0;\n\t"
+        "@p add.f32 %0, %0, %3;\n\t}"
+        : "+f"(acc[i])
+        : "r"(w), "r"(1u << i), "f"(wt));
+}
+
+// Compute warps: consume slots until the end marker.
+__device__ __forceinline__ void ps_compute(PsSmem& S, float* __restrict__ scores) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = warp >> 2, wl = (warp & 3) * 32 + lane;  // plane parity, word
+  float4* red = &S.red[wl * 8];
+  const int sw = lane & 7;
+  float acc[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
+  for (int c = 0;; ++c) {
+    const int s = c % kPsSlots;
+    nb_sync(kBarFull + s, kPsThreads);
+    const PsSlot m = S.slot[s];
+    if (m.flags & kSlotEnd) break;
+    if (m.flags & kSlotFirst) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
     }
-  }
-  cp_async_commit();
-}
-
-// Folded weights of planes [e0, e0 + ne): Wt = (q~_j * 2^(3-p)) * s_j,blk, which
-// equals fl(q~_j * s_j,blk) * 2^(3-p) exactly (power-of-two scaling commutes with
-// rounding).
-// Only valid blocks are written: the other weights are read only by lanes whose
-// words lie past the tile's end, whose sums are never stored.
-__device__ __forceinline__ void ps_weights(PsSmem& S, const uint16_t* scb, int buf, int e0, int ne,
-                                           int nbv) {
-  // blocks b2, b2 + 1; for odd nbv the last pair's second weight is not valid (and
-  // is read only by lanes past the end)
-  const int b2 = (threadIdx.x & 31) * 2;
-  if (b2 >= nbv) return;
-  for (int e = threadIdx.x >> 5; e < ne; e += kPsThreads / 32) {
-    const float qp = S.qp[e0 + e];
-    const __half2 sv = *reinterpret_cast<const __half2*>(&scb[S.eslot[e0 + e] * kPsBlocks + b2]);
-    const float2 f = __half22float2(sv);
-    *reinterpret_cast<float2*>(&S.Wt[buf][e][b2]) = make_float2(__fmul_rn(qp, f.x), __fmul_rn(qp, f.y));
-  }
-}
-
-// Issues the copies of a tile's active-channel scales into scb (one group with
-// the tile's first chunk of planes, which the caller stages).
-template <bool A16>
-__device__ __forceinline__ void ps_stage_scales(PsSmem& S, uint16_t* scb, const uint16_t* sc_tile,
-                                                int64_t sstride, int nch, int nbv) {
-  if (A16) {
-    // whole 16-byte segments (8 blocks) inside the valid blocks, the rest singly
-    for (int x = threadIdx.x; x < nch * 8; x += kPsThreads) {
-      const int sl = x >> 3, seg = x & 7;
-      const uint16_t* src = sc_tile + (int64_t)S.chan[sl] * sstride + seg * 8;
-      uint16_t* dst = scb + sl * kPsBlocks + seg * 8;
-      if (seg * 8 + 8 <= nbv) {
-        cp_async16(dst, src);
-      } else {
-        for (int k = 0; seg * 8 + k < nbv; ++k) dst[k] = src[k];
+    if ((warp & 3) * 32 < m.nwv) {  // warps whose words all lie past the end idle
+      const uint32_t* wp = &S.words[s][half][wl];
+      const float* tp = &S.Wt[s][half][wl >> 1];
+#pragma unroll 2
+      for (int e = half; e < m.ne; e += 2, wp += 2 * kPsWords, tp += 2 * kPsBlocks)
+        ps_bits(acc, *wp, *tp);
+    }
+    nb_arrive(kBarEmpty + s, kPsThreads);
+    if (m.flags & kSlotLast) {
+      // odd-plane partial sums: lane l's eight float4s go to 16-byte slots k ^ (l & 7),
+      // so each quarter-warp hits 8 distinct bank groups.  (The next tile's writes to
+      // red come after a FULL wait that every compute thread joins only once done
+      // reading it here.)
+      if (half == 1) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          red[k ^ sw] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+      }
+      nb_sync(kBarComp, kPsCompute);
+      if (half == 0 && wl < m.nwv) {
+        const float cb = S.Cs[m.cs][wl >> 1];
+        float4* orow = reinterpret_cast<float4*>(scores + m.out + wl * 32);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 o = red[k ^ sw];
+          orow[k] = make_float4((acc[4 * k] + o.x) + cb, (acc[4 * k + 1] + o.y) + cb,
+                                (acc[4 * k + 2] + o.z) + cb, (acc[4 * k + 3] + o.w) + cb);
+        }
       }
     }
-  } else {
-    for (int x = threadIdx.x; x < nch * kPsBlocks; x += kPsThreads) {
-      const int sl = x / kPsBlocks, blk = x % kPsBlocks;
-      if (blk < nbv) scb[sl * kPsBlocks + blk] = sc_tile[(int64_t)S.chan[sl] * sstride + blk];
-    }
   }
 }
 
+// Helper-side record of a chunk whose copies are in flight.
+struct PsPending {
+  PsSlot m;
+  int e0;  // first entry of the chunk
+  int sb;  // scale buffer: 0 / 1 (halves) or 2 (flat)
+};
+
+__device__ __forceinline__ const uint16_t* ps_scales(const PsSmem& S, int sb) {
+  return sb == 1 ? &S.sc[kD / 2][0] : &S.sc[0][0];
+}
+
+// Finishes the oldest pending chunk (slot d % kPsSlots): waits for its copies (the
+// `newer` chunks issued after it may stay in flight), forms the tile's per-block
+// constants if it is the tile's first chunk, writes its folded weights and hands
+// the slot to the compute warps.
+__device__ __forceinline__ void ps_finish(PsSmem& S, const PsPending& pd, int d, int newer) {
+  const int ht = threadIdx.x - kPsCompute, hw = ht >> 5, lane = threadIdx.x & 31;
+  if (newer > 0)
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+  else
+    cp_async_wait_all();
+  nb_sync(kBarHelp, kPsHelpers);  // every helper's copies of the chunk have landed
+  const int s = d % kPsSlots;
+  const uint16_t* scb = ps_scales(S, pd.sb);
+  const int nbv = pd.m.nwv / 2;
+  // blocks b4..b4+3 (a group that reaches past nbv holds blocks past the end: their
+  // values are read only by lanes whose sums are not stored)
+  const int b4 = (lane & 15) * 4;
+  if (pd.m.flags & kSlotFirst) {
+    // per-block constants C_blk: half-warps take alternate slots, a shuffle joins
+    // the halves, then the four warps' partial sums are added
+    float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (b4 < nbv) {
+      for (int sl = 2 * hw + (lane >> 4); sl < S.nch; sl += 2 * (kPsHelpers / 32)) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(scb + sl * kPsBlocks + b4);
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        const float qo = S.qo[sl];
+        a.x = __fadd_rn(a.x, __fmul_rn(qo, f0.x));
+        a.y = __fadd_rn(a.y, __fmul_rn(qo, f0.y));
+        a.z = __fadd_rn(a.z, __fmul_rn(qo, f1.x));
+        a.w = __fadd_rn(a.w, __fmul_rn(qo, f1.y));
+      }
+    }
+    a.x = __fadd_rn(a.x, __shfl_xor_sync(0xFFFFFFFFu, a.x, 16));
+    a.y = __fadd_rn(a.y, __shfl_xor_sync(0xFFFFFFFFu, a.y, 16));
+    a.z = __fadd_rn(a.z, __shfl_xor_sync(0xFFFFFFFFu, a.z, 16));
+    a.w = __fadd_rn(a.w, __shfl_xor_sync(0xFFFFFFFFu, a.w, 16));
+    if (lane < 16) *reinterpret_cast<float4*>(&S.hred[hw][b4]) = a;
+    nb_sync(kBarHelp, kPsHelpers);
+    if (ht < kPsBlocks)
+      S.Cs[pd.m.cs][ht] = __fadd_rn(__fadd_rn(S.hred[0][ht], S.hred[1][ht]),
+                                    __fadd_rn(S.hred[2][ht], S.hred[3][ht]));
+  }
+  // folded weights Wt = (q~_j * 2^(3-p)) * s_j,blk, which equals
+  // fl(q~_j * s_j,blk) * 2^(3-p) exactly (power-of-two scaling commutes with rounding);
+  // half-warps take alternate planes, each lane four blocks
+  if (b4 < nbv) {
+#pragma unroll 2
+    for (int e = 2 * hw + (lane >> 4); e < pd.m.ne; e += 2 * (kPsHelpers / 32)) {
+      const float qv = S.qp[pd.e0 + e];
+      const uint2 raw = *reinterpret_cast<const uint2*>(scb + S.eslot[pd.e0 + e] * kPsBlocks + b4);
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+      const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+      *reinterpret_cast<float4*>(&S.Wt[s][e][b4]) =
+          make_float4(__fmul_rn(qv, f0.x), __fmul_rn(qv, f0.y), __fmul_rn(qv, f1.x),
+                      __fmul_rn(qv, f1.y));
+    }
+  }
+  if (ht == 0) S.slot[s] = pd.m;
+  nb_arrive(kBarFull + s, kPsThreads);
+}
+
+// Helper warps: walk the CTA's tiles and keep up to two chunks' copies in flight:
+// chunk c is issued once the compute warps release its slot, right after chunk
+// c - 2 is finished and handed over.  The pipeline drains before a row change
+// (the row tables are rebuilt) and, past 64 active channels, before each tile
+// (one flat scale buffer); then the end marker is posted.
 template <int G, bool A16>
-__global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm)
-score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
-                    const uint8_t* __restrict__ plan, const uint16_t* __restrict__ q, int Hq,
-                    int Hkv, int64_t n, int64_t ncap, int64_t units_per_row, int64_t total_units,
-                    float* __restrict__ scores) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  PsSmem& S = *reinterpret_cast<PsSmem*>(smem_raw);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t wstride = ncap / 32, sstride = ncap / 64;
+__device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ planes,
+                                        const uint16_t* __restrict__ scales,
+                                        const uint8_t* __restrict__ plan,
+                                        const uint16_t* __restrict__ q, int Hq, int Hkv, int64_t n,
+                                        int64_t ncap, int upr, int64_t total_units) {
+  const int ht = threadIdx.x - kPsCompute, hw = ht >> 5, lane = threadIdx.x & 31;
+  const uint32_t wstride = (uint32_t)(ncap / 32), sstride = (uint32_t)(ncap / 64);
+  // this CTA's units, walked as (row bh, unit ur) without dividing; rows <= 65535
+  // and a CTA holds fewer than 2^30 units, so 32-bit counters suffice
   const int64_t u_begin = (int64_t)blockIdx.x * total_units / gridDim.x;
   const int64_t u_end = (int64_t)(blockIdx.x + 1) * total_units / gridDim.x;
-  int64_t cur_bh = -1;
-  bool staged = false;  // this tile's scales and first chunk are already in flight
-  int sbuf = 0;         // scale half of this tile (double-buffered mode)
-  int wb0 = 0;          // words buffer holding this tile's first chunk
-
-  for (int64_t u = u_begin; u < u_end;) {
-    const PsTile T = ps_tile_at(u, u_end, units_per_row);
-    const int64_t bh = T.bh, tok0 = T.tok0, u_next = u + T.nu;
-    if (bh != cur_bh) {  // per-row prologue
+  int left = (int)(u_end - u_begin);
+  int bh = (int)(u_begin / upr);
+  int ur = (int)(u_begin - (int64_t)bh * upr);
+  int cur_bh = -1;
+  int c = 0, d = 0;  // chunks issued, chunks handed over
+  PsPending p0, p1;  // pending chunks, oldest first (registers: indexed statically)
+  int np = 0;
+  const int n32 = (int)(n / 32);  // words per row (n < 2^31)
+  for (int tcount = 0; left > 0; ++tcount) {
+    const int nu = min(min(kPsTile / kPsUnit, upr - ur), left);
+    const int64_t tok0 = (int64_t)ur * kPsUnit;
+    const int nwv = min(nu * (kPsUnit / 32), n32 - ur * (kPsUnit / 32));  // valid words (even)
+    const int nbv = nwv / 2;                                             // valid scale blocks
+    if (bh != cur_bh) {  // per-row tables: drain, then rebuild
+      for (; np > 0; --np, ++d) {
+        ps_finish(S, p0, d, np - 1);
+        p0 = p1;
+      }
+      nb_sync(kBarHelp, kPsHelpers);  // every helper is done with the old tables
       cur_bh = bh;
-      staged = false;
-      const int b = (int)(bh / Hkv), h = (int)(bh % Hkv);
-      if (threadIdx.x < kD) {
-        const int j = threadIdx.x;
-        float acc = 0.0f;
+      const int b = bh / Hkv, h = bh % Hkv;
+      {
+        const int j = ht;
+        float a = 0.0f;
 #pragma unroll
         for (int g = 0; g < G; ++g)
-          acc = __fadd_rn(acc, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]));
-        S.qt[j] = acc;
-        S.tb[j] = min((int)plan[bh * kD + j], 4);  // a plan holds 0..4 bits per channel
+          a = __fadd_rn(a, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]));
+        S.qt[j] = a;
+        S.tb[j] = min((int)plan[(int64_t)bh * kD + j], 4);  // a plan holds 0..4 bits per channel
       }
-      __syncthreads();
-      if (warp == 0) {  // active entries and channel slots, j ascending
-        int c[4], tot = 0, chs = 0;
+      nb_sync(kBarHelp, kPsHelpers);
+      if (hw == 0) {  // active entries and channel slots, j ascending
+        int cnt[4], tot = 0, chs = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          c[k] = S.tb[lane * 4 + k];
-          tot += c[k];
-          chs += c[k] > 0;
+          cnt[k] = S.tb[lane * 4 + k];
+          tot += cnt[k];
+          chs += cnt[k] > 0;
         }
         int incl = tot, inclc = chs;
 #pragma unroll
@@ -276,11 +363,11 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int j = lane * 4 + k;
-          for (int p = 0; p < c[k]; ++p) S.act[pos++] = (uint16_t)(j * 4 + p);
-          if (c[k] > 0) {
+          for (int p = 0; p < cnt[k]; ++p) S.act[pos++] = (uint16_t)(j * 4 + p);
+          if (cnt[k] > 0) {
             S.slot_of[j] = slot;
             S.chan[slot] = j;
-            S.qo[slot] = __fmul_rn(S.qt[j], c[k] < 4 ? (float)((1 << (3 - c[k])) - 8) : -8.0f);
+            S.qo[slot] = __fmul_rn(S.qt[j], cnt[k] < 4 ? (float)((1 << (3 - cnt[k])) - 8) : -8.0f);
             ++slot;
           } else {
             S.slot_of[j] = 0;
@@ -288,131 +375,122 @@ score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restr
         }
         if (lane == 31) { S.nact = incl; S.nch = inclc; }
       }
-      __syncthreads();
-      for (int e = threadIdx.x; e < S.nact; e += kPsThreads) {
+      nb_sync(kBarHelp, kPsHelpers);
+      for (int e = ht; e < S.nact; e += kPsHelpers) {
         const int ent = S.act[e], j = ent >> 2, p = ent & 3;
         S.eslot[e] = (uint8_t)S.slot_of[j];
         S.qp[e] = ldexpf(S.qt[j], 3 - p);
       }
-      __syncthreads();
+      nb_sync(kBarHelp, kPsHelpers);
     }
     const int nact = S.nact, nch = S.nch;
-    const bool dbl = nch <= kD / 2;  // scales fit one half: prefetch the next tile
-    uint16_t* scb = dbl ? &S.sc[sbuf][0][0] : &S.sc[0][0][0];
-    const int nwv = ps_valid_words(T, n);  // valid words (even)
-    const int nbv = nwv / 2;               // valid scale blocks
-    const uint32_t* pl_tile = planes + bh * kD * 4 * wstride + tok0 / 32;
-    const int ne0 = min(kPsChunk, nact);
-    if (!staged) {
-      ps_stage_scales<A16>(S, scb, scales + bh * kD * sstride + tok0 / 64, sstride, nch, nbv);
-      ps_stage_words<A16>(S, wb0, 0, ne0, pl_tile, wstride, nwv);
+    const int nck = max(1, (nact + kPsChunk - 1) / kPsChunk);
+    const int sb = nch <= kD / 2 ? (tcount & 1) : 2;
+    if (sb == 2) {  // one flat scale buffer: drain first
+      for (; np > 0; --np, ++d) {
+        ps_finish(S, p0, d, np - 1);
+        p0 = p1;
+      }
     }
-    cp_async_wait_all();
-    __syncthreads();
-    // per-block constants C_blk (four partial sums per block) and the first weights
-    {
-      const int b2 = (threadIdx.x & 31) * 2, part = threadIdx.x >> 5;
-      float a0 = 0.0f, a1 = 0.0f;
-      if (b2 < nbv)
-        for (int sl = part; sl < nch; sl += kPsThreads / 32) {
-          const float2 f =
-              __half22float2(*reinterpret_cast<const __half2*>(&scb[sl * kPsBlocks + b2]));
-          const float qo = S.qo[sl];
-          a0 = __fadd_rn(a0, __fmul_rn(qo, f.x));
-          a1 = __fadd_rn(a1, __fmul_rn(qo, f.y));
+    uint16_t* scb = const_cast<uint16_t*>(ps_scales(S, sb));
+    const uint32_t* pl_tile = planes + (int64_t)bh * kD * 4 * wstride + tok0 / 32;
+    const uint16_t* sc_tile = scales + (int64_t)bh * kD * sstride + tok0 / 64;
+    for (int k = 0; k < nck; ++k, ++c) {
+      if (np == 2) {  // hand over chunk c - 2 before waiting for a slot
+        ps_finish(S, p0, d, 1);
+        p0 = p1;
+        --np;
+        ++d;
+      }
+      const int s = c % kPsSlots;
+      if (c >= kPsSlots) nb_sync(kBarEmpty + s, kPsThreads);  // compute is done with slot s
+      const int e0 = k * kPsChunk, ne = max(0, min(kPsChunk, nact - e0));
+      if (k == 0) {  // the tile's active-channel scales
+        nb_sync(kBarHelp, kPsHelpers);  // every helper is done reading this scale buffer
+        if (A16) {
+          // whole 16-byte segments (8 blocks) inside the valid blocks, the rest singly
+          for (int x = ht; x < nch * 8; x += kPsHelpers) {
+            const int sl = x >> 3, sg = x & 7;
+            const uint16_t* src = sc_tile + (uint64_t)S.chan[sl] * sstride + sg * 8;
+            uint16_t* dst = scb + sl * kPsBlocks + sg * 8;
+            if (sg * 8 + 8 <= nbv) {
+              cp_async16(smem_u32(dst), src);
+            } else {
+              for (int i = 0; sg * 8 + i < nbv; ++i) dst[i] = src[i];
+            }
+          }
+        } else {
+          for (int x = ht; x < nch * kPsBlocks; x += kPsHelpers) {
+            const int sl = x / kPsBlocks, blk = x % kPsBlocks;
+            if (blk < nbv) scb[sl * kPsBlocks + blk] = sc_tile[(uint64_t)S.chan[sl] * sstride + blk];
+          }
         }
-      *reinterpret_cast<float2*>(&S.red[part][b2]) = make_float2(a0, a1);
-    }
-    ps_weights(S, scb, wb0, 0, ne0, nbv);
-    __syncthreads();
-    if (threadIdx.x < kPsBlocks) {
-      float c = 0.0f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) c = __fadd_rn(c, S.red[k][threadIdx.x]);
-      S.Cs[threadIdx.x] = c;
-    }
-
-    // the next tile of the same row can be staged during this tile's last chunk
-    const bool pref = dbl && u_next < u_end && u_next / units_per_row == bh;
-    bool staged_next = false;
-    int next_wb0 = 0;
-    const int half = warp >> 2, wl = (warp & 3) * 32 + lane;  // plane parity, word
-    float acc[32];
-#pragma unroll
-    for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
-    int buf = wb0;
-    for (int e0 = 0; e0 < nact; e0 += kPsChunk, buf ^= 1) {
-      const int ne = min(kPsChunk, nact - e0);
-      const int e1 = e0 + kPsChunk;
-      const int ne1 = min(kPsChunk, nact - e1);
-      if (ne1 > 0) {
-        ps_stage_words<A16>(S, buf ^ 1, e1, ne1, pl_tile, wstride, nwv);
-      } else if (pref) {
-        const PsTile NT = ps_tile_at(u_next, u_end, units_per_row);
-        const int64_t ntok0 = NT.tok0;
-        const int nnwv = ps_valid_words(NT, n);
-        ps_stage_scales<A16>(S, &S.sc[sbuf ^ 1][0][0], scales + bh * kD * sstride + ntok0 / 64,
-                             sstride, nch, nnwv / 2);
-        ps_stage_words<A16>(S, buf ^ 1, 0, ne0, planes + bh * kD * 4 * wstride + ntok0 / 32,
-                            wstride, nnwv);
-        staged_next = true;
-        next_wb0 = buf ^ 1;
       }
-      const uint32_t* wp = &S.words[buf][half][wl];
-      const float* tp = &S.Wt[buf][half][wl >> 1];
-      const int ne_w = (warp & 3) * 32 < nwv ? ne : 0;  // warps past the tile's end idle
-#pragma unroll 2
-      for (int e = half; e < ne_w; e += 2, wp += 2 * kPsWords, tp += 2 * kPsBlocks) {
-        const uint32_t w = *wp;
-        const float wt = *tp;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (w & (1u << i)) acc[i] += wt;
+      // the chunk's plane words: one warp per plane row
+      const uint32_t wdst = smem_u32(&S.words[s][0][0]);
+      if (A16) {
+        // whole 16-byte segments inside the valid words, then an 8-byte remainder
+        // (nwv is even): no copy reads past the last valid word of a plane row
+        const int seg = lane * 4 + 4 <= nwv ? 16 : (lane * 4 + 2 == nwv ? 8 : 0);
+        if (seg) {
+          for (int e = hw; e < ne; e += kPsHelpers / 32) {
+            const uint32_t* src = pl_tile + (uint64_t)S.act[e0 + e] * wstride + lane * 4;
+            const uint32_t dd = wdst + e * (kPsWords * 4) + lane * 16;
+            if (seg == 16) cp_async16(dd, src);
+            else cp_async8(dd, src);
+          }
+        }
+      } else {
+        for (int e = hw; e < ne; e += kPsHelpers / 32) {
+          const uint32_t* src = pl_tile + (uint64_t)S.act[e0 + e] * wstride;
+          for (int sg = lane; sg * 2 < nwv; sg += 32)
+            cp_async8(wdst + e * (kPsWords * 4) + sg * 8, src + sg * 2);
+        }
       }
-      if (ne1 > 0) {
-        ps_weights(S, scb, buf ^ 1, e1, ne1, nbv);
-        cp_async_wait_all();  // the next chunk (nothing else is in flight)
-      }
-      __syncthreads();
+      cp_async_commit();
+      PsPending pd;
+      pd.m.ne = ne;
+      pd.m.flags = (k == 0 ? kSlotFirst : 0) | (k == nck - 1 ? kSlotLast : 0);
+      pd.m.cs = tcount & 3;
+      pd.m.nwv = nwv;
+      pd.m.out = (int64_t)bh * n + tok0;
+      pd.e0 = e0;
+      pd.sb = sb;
+      if (np == 0) p0 = pd;
+      else p1 = pd;
+      ++np;
     }
-    if (nact == 0) {
-      if (pref) {  // nothing to prefetch but the (empty) tile bookkeeping
-        staged_next = false;
-      }
-      __syncthreads();  // Cs written above must be visible
-    }
-    // odd-plane partial sums through the (now idle) weight buffers: lane l's eight
-    // float4s go to 16-byte slots k ^ (l & 7), so each quarter-warp hits 8 distinct
-    // bank groups
-    float4* red = reinterpret_cast<float4*>(&S.Wt[0][0][0]) + ((warp & 3) * 32 + lane) * 8;
-    const int sw = lane & 7;
-    if (half == 1) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        red[k ^ sw] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
-    }
-    __syncthreads();
-    if (half == 0 && wl < nwv) {
-      const float c = S.Cs[wl >> 1];
-      float4* orow = reinterpret_cast<float4*>(scores + bh * n + tok0 + wl * 32);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 o = red[k ^ sw];
-        orow[k] = make_float4((acc[4 * k] + o.x) + c, (acc[4 * k + 1] + o.y) + c,
-                              (acc[4 * k + 2] + o.z) + c, (acc[4 * k + 3] + o.w) + c);
-      }
-    }
-    __syncthreads();  // buffers are reused by the next tile
-    u = u_next;
-    staged = staged_next;
-    if (staged_next) {
-      sbuf ^= 1;
-      wb0 = next_wb0;
-    } else {
-      wb0 = 0;
-    }
+    // the next tile of the range
+    left -= nu;
+    ur += nu;
+    if (ur == upr) { ur = 0; ++bh; }
   }
-  cp_async_wait_all();  // nothing may be left in flight at exit
+  for (; np > 0; --np, ++d) {
+    ps_finish(S, p0, d, np - 1);
+    p0 = p1;
+  }
+  // end marker, then wait out the compute warps' releases of the last slots
+  {
+    const int s = c % kPsSlots;
+    if (c >= kPsSlots) nb_sync(kBarEmpty + s, kPsThreads);
+    if (ht == 0) S.slot[s].flags = kSlotEnd;
+    nb_arrive(kBarFull + s, kPsThreads);
+  }
+  for (int x = max(0, c - kPsSlots + 1); x < c; ++x) nb_sync(kBarEmpty + x % kPsSlots, kPsThreads);
+}
+
+template <int G, bool A16>
+__global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm)
+score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
+                    const uint8_t* __restrict__ plan, const uint16_t* __restrict__ q, int Hq,
+                    int Hkv, int64_t n, int64_t ncap, int upr, int64_t total_units,
+                    float* __restrict__ scores) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  PsSmem& S = *reinterpret_cast<PsSmem*>(smem_raw);
+  if (threadIdx.x < kPsCompute)
+    ps_compute(S, scores);
+  else
+    ps_help<G, A16>(S, planes, scales, plan, q, Hq, Hkv, n, ncap, upr, total_units);
 }
 
 static int sm_count() {
@@ -434,12 +512,11 @@ static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scale
   auto kern = score_planes_kernel<G, A16>;
   if (int rc = set_smem_limit((const void*)kern, sizeof(PsSmem), "score_planes: smem attribute"))
     return rc;
-  const int64_t units_per_row = (s.n + kPsUnit - 1) / kPsUnit;
-  const int64_t total = units_per_row * s.B * s.Hkv;
+  const int upr = (int)((s.n + kPsUnit - 1) / kPsUnit);  // units per row (n < 2^31)
+  const int64_t total = (int64_t)upr * s.B * s.Hkv;
   const int64_t grid = imin64(total, (int64_t)sm_count() * kPsCtasPerSm);
   kern<<<(unsigned)grid, kPsThreads, sizeof(PsSmem), st>>>(planes, scales, plan, q, s.Hq, s.Hkv,
-                                                          s.n, s.ncap, units_per_row, total,
-                                                          scores);
+                                                          s.n, s.ncap, upr, total, scores);
   return check_launch("score_planes");
 }
 
