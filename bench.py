@@ -48,7 +48,7 @@ def log(*a):
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=10000)  # ~1 s timed: clocks sampled within
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-variants", action="store_true", help="skip the other scorers")
@@ -181,13 +181,38 @@ def capture_graph(torch, fn):
     return g
 
 
-def launches_per_step(step) -> int:
-    """Kernels of libsd one step launches (per the stage implementations)."""
-    from top_sparse_decode_gb300 import SD_IDX_MINMAX
-    c = step.cfg
-    prep = 0 if c.kind == SD_IDX_MINMAX else 1
-    topk = 1 if c.n_units <= 8192 else 3   # one CTA per row, or sample + filter + finish
-    return prep + 1 + topk + 1             # + gather-attend (partials merged in-kernel)
+def launches_per_step(step, q) -> int:
+    """Kernels of libsd one eager step launches, counted by the library itself
+    (a graph replay of the step launches the same kernels)."""
+    import torch
+    import top_sparse_decode_gb300 as sd
+    torch.cuda.synchronize()
+    before = sd.sd_launch_count()
+    step.run(q)
+    torch.cuda.synchronize()
+    return sd.sd_launch_count() - before
+
+
+def scan_traffic(workload: str):
+    """DRAM bytes per launch of the scan kernel from the committed ncu summary,
+    or None when the kernel source changed since that capture."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "score_planes_longctx-262k.md")
+    src = os.path.join(ROOT, "top_sparse_decode_gb300", "csrc", "sd_score.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    text = open(prof).read()
+    code = open(src).read()
+    i, j = code.find("// Bit-plane prefix scan."), code.find("static int sm_count()")
+    if i < 0 or j < i:
+        return None
+    sha = hashlib.sha256(code[i:j].encode()).hexdigest()  # the scan's device code
+    if sha not in text:
+        return None
+    for line in text.splitlines():
+        if line.startswith(f"traffic_bytes_per_launch[{workload}]"):
+            return int(line.split("=")[1].split()[0])
+    return None
 
 
 def peaks():
@@ -460,16 +485,19 @@ def main():
         "stages_us": {"plan": st_prep * 1e3, "scan": st_score * 1e3, "topk": st_topk * 1e3,
                       "gather_attend": st_att * 1e3, "step_eager": eager * 1e3},
         "stages_in_step_us": marginal,
-        "roofline": {"bound": "hbm", "kernel": "score_planes_kernel",
-                     "achieved": scan_gbs, "peak": peak_gbs, "unit": "GB/s",
-                     "frac": scan_gbs / peak_gbs, "traffic": None,
-                     "peak_kind": peak_kind,
-                     "alg_bytes_per_launch": scan_bytes},
-        "roofline_alu": {"bound": "alu", "kernel": "score_planes_kernel",
-                         "achieved": alu_ops / (st_score * 1e-3) / 1e12,
-                         "peak": alu_peak / 1e12, "unit": "Tops/s",
-                         "frac": alu_ops / (st_score * 1e-3) / alu_peak,
-                         "ops_per_launch": alu_ops},
+        # the scan is bound by one bit test and one predicated FP32 add per planned
+        # token-plane: the peak is the FP32 pipe (128 lanes per SM per clock)
+        "roofline": {"bound": "alu", "kernel": "score_planes_kernel",
+                     "achieved": alu_ops / (st_score * 1e-3) / 1e12,
+                     "peak": alu_peak / 1e12, "unit": "T token-planes/s",
+                     "frac": alu_ops / (st_score * 1e-3) / alu_peak,
+                     "traffic": scan_traffic("longctx-1m") if n == 1048576 else None,
+                     "ops_per_launch": alu_ops, "alg_bytes_per_launch": scan_bytes,
+                     "peak_kind": "derived: 152 SMs x 128 FP32 lanes x median SM clock"},
+        "roofline_hbm": {"bound": "hbm", "kernel": "score_planes_kernel",
+                         "achieved": scan_gbs, "peak": peak_gbs, "unit": "GB/s",
+                         "frac": scan_gbs / peak_gbs, "peak_kind": peak_kind,
+                         "alg_bytes_per_launch": scan_bytes},
         "step_bytes": {"algorithmic": alg_bytes, "scan": scan_bytes, "gather": gath_bytes,
                        "score_buffer": rl.score_buffer_bytes(B, Hkv, n),
                        "step_GBps": alg_bytes / (t_step_max * 1e-3) / 1e9},
@@ -477,7 +505,7 @@ def main():
         "e2e": {"value": e2e_val, "unit": UNIT,
                 "h2d_bytes_per_step": int(q_host.numel() * q_host.element_size()),
                 "d2h_bytes_per_step": int(out_host.numel() * 4 + lse_host.numel() * 4)},
-        "gpu_launches": launches_per_step(step) * args.steps,
+        "gpu_launches": launches_per_step(step, q) * args.steps,
         "clocks": ck,
         "variants": variants,
         "cpu_baseline": cpu,

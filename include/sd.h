@@ -237,6 +237,14 @@ const char* sd_last_error(void);
 /* ABI version (major * 100 + minor). */
 int sd_version(void);
 
+/*
+ * sd_launch_count -- number of kernels this library has launched in this
+ * process (all devices and threads; a graph replay launches nothing through
+ * the library and is not counted).  Read it before and after a call to count
+ * that call's launches.
+ */
+int64_t sd_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,7 @@ __all__ = [
     "sd_build_index", "sd_encode_query", "sd_plan", "sd_score", "sd_topk_workspace_size",
     "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
     "sd_gather_attend_noalloc", "sd_offload_gather",
-    "sd_event_wait", "sd_last_error", "sd_version",
+    "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
 ]
 
 
@@ -90,6 +90,10 @@ def make_select(k: int, sink: int = 0, local: int = 0, block: int = 1) -> SdSele
 
 def sd_version() -> int:
     return int(lib().sd_version())
+
+
+def sd_launch_count() -> int:
+    return int(lib().sd_launch_count())
 
 
 def sd_last_error() -> str:

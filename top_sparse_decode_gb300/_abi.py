@@ -53,6 +53,7 @@ SIGNATURES = {
     "sd_event_wait": (_i, [_p, _i64]),
     "sd_last_error": (ctypes.c_char_p, []),
     "sd_version": (_i, []),
+    "sd_launch_count": (_i64, []),
 }
 
 _lib = None

@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <string.h>
 
+#include <atomic>
 #include <chrono>
 #include <map>
 #include <mutex>
@@ -29,6 +30,10 @@ int fail(int code, const char* fmt, ...) {
   va_end(ap);
   return code;
 }
+
+static std::atomic<long long> g_launches{0};
+void note_launches(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+static long long launch_total() { return g_launches.load(std::memory_order_relaxed); }
 
 int check_launch(const char* what) {
   cudaError_t e = cudaGetLastError();
@@ -94,6 +99,8 @@ using namespace sd;
 extern "C" {
 
 int sd_version(void) { return 100; }
+
+int64_t sd_launch_count(void) { return (int64_t)launch_total(); }
 
 const char* sd_last_error(void) { return g_err; }
 

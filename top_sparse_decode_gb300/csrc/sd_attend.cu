@@ -264,6 +264,7 @@ static int attend_t(const Dims& s, const uint16_t* q, const uint16_t* K, const u
   attend_kernel<G><<<grid, 128, 0, st>>>(q, K, V, idx, idx_stride, count, s.Hq, s.Hkv, s.n,
                                          s.ncap, (int)max_count, scale, nch > 0 ? nch : 1, w,
                                          out, lse);
+  note_launches(1);
   return check_launch("attend");
 }
 

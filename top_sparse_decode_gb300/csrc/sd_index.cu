@@ -192,6 +192,7 @@ static int sig_build_t(const Dims& s, const uint16_t* K, const sd_encoder& e, ui
   int64_t rows = (int64_t)s.B * s.Hkv * s.n;
   unsigned grid = (unsigned)((rows + 127) / 128);
   kern<<<grid, 128, smem, st>>>(K, s.n, s.ncap, rows, e.W1, e.b1, e.W2, e.b2, sig);
+  note_launches(1);
   return check_launch("sig_build");
 }
 
@@ -205,6 +206,7 @@ static int encode_query_t(const Dims& s, const uint16_t* q, const sd_encoder& e,
   if (int rc_ = set_smem_limit((const void*)kern, smem, "encode_query: smem attribute")) return rc_;
   int rows = s.B * s.Hq;
   kern<<<(rows + kQRows - 1) / kQRows, 128, smem, st>>>(q, rows, e.W1, e.b1, e.W2, e.b2, qsig);
+  note_launches(1);
   return check_launch("encode_query");
 }
 
@@ -304,6 +306,7 @@ int launch_plane_build(const Dims& s, const uint16_t* K, uint32_t* planes, uint1
   if (int rc_ = set_smem_limit((const void*)plane_build_kernel, smem, "plane_build: smem attribute")) return rc_;
   dim3 grid((unsigned)((s.n + kPbTile - 1) / kPbTile), (unsigned)(s.B * s.Hkv));
   plane_build_kernel<<<grid, 256, smem, st>>>(K, s.n, s.ncap, planes, scales);
+  note_launches(1);
   return check_launch("plane_build");
 }
 
@@ -359,6 +362,7 @@ int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaSt
   int64_t nblk = (s.n + 15) / 16;
   dim3 grid((unsigned)((nblk + 7) / 8), (unsigned)(s.B * s.Hkv));
   minmax_build_kernel<<<grid, 256, 0, st>>>(K, s.n, s.ncap, summ);
+  note_launches(1);
   return check_launch("minmax_build");
 }
 

@@ -17,6 +17,8 @@ constexpr int kSmallRow = 8192;  // rows up to this many units are selected by o
 void set_error(const char* fmt, ...);
 int fail(int code, const char* fmt, ...);
 int check_launch(const char* what);
+// counts kernel launches made by the library (sd_launch_count)
+void note_launches(int k);
 // Raises a kernel's dynamic shared-memory limit to `bytes`, once per (device,
 // kernel): later calls, including those made while a stream is being captured
 // into a CUDA graph, issue no CUDA call.

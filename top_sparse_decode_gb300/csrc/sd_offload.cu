@@ -63,6 +63,7 @@ int launch_offload_gather(const Dims& s, const uint32_t* host_planes, const uint
             (unsigned)((max_bytes + kOgBytesPerCta - 1) / kOgBytesPerCta));
   offload_gather_kernel<<<grid, kOgThreads, 0, st>>>(host_planes, host_scales, plan, s.ncap,
                                                      dev_planes, dev_scales);
+  note_launches(1);
   return check_launch("offload_gather");
 }
 

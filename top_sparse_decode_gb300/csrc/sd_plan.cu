@@ -103,6 +103,7 @@ plan_kernel(const uint16_t* __restrict__ q, const float* __restrict__ sigma2, in
 int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode, int budget,
                 uint8_t* plan, cudaStream_t st) {
   plan_kernel<<<s.B * s.Hkv, 4 * kD, 0, st>>>(q, sigma2, s.Hq, s.Hkv, s.G, mode, budget, plan);
+  note_launches(1);
   return check_launch("plan");
 }
 

@@ -60,6 +60,7 @@ static void hamming_t(const Dims& s, const uint32_t* sig, const uint32_t* qsig, 
   bool vec = (s.n % 4 == 0) && (s.ncap % 4 == 0);
   dim3 grid((unsigned)((s.n + 1023) / 1024), (unsigned)(s.B * s.Hkv));
   score_hamming_kernel<G><<<grid, 256, 0, st>>>(sig, qsig, s.Hq, s.Hkv, s.n, s.ncap, vec, out);
+  note_launches(1);
 }
 
 int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsig,
@@ -517,6 +518,7 @@ static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scale
   const int64_t grid = imin64(total, (int64_t)sm_count() * kPsCtasPerSm);
   kern<<<(unsigned)grid, kPsThreads, sizeof(PsSmem), st>>>(planes, scales, plan, q, s.Hq, s.Hkv,
                                                           s.n, s.ncap, upr, total, scores);
+  note_launches(1);
   return check_launch("score_planes");
 }
 
@@ -605,6 +607,7 @@ int launch_score_quest(const Dims& s, const uint16_t* summ, const uint16_t* q, f
     case 4: score_quest_kernel<4><<<grid, 256, 0, st>>>(summ, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
     default: score_quest_kernel<8><<<grid, 256, 0, st>>>(summ, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
   }
+  note_launches(1);
   return check_launch("score_quest");
 }
 

@@ -1191,6 +1191,7 @@ static int launch_cluster(const void* scores, int64_t rows, const Geo& g, int32_
   if (cudaLaunchKernelEx(&cfg, topk_cluster_kernel<F32, CS>, scores, g, idx, idx_stride, count) !=
       cudaSuccess)
     return check_launch("topk_cluster");
+  note_launches(1);
   return check_launch("topk_cluster");
 }
 
@@ -1202,6 +1203,7 @@ static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
     auto kern = topk_small_kernel<F32>;
     if (int rc_ = set_smem_limit((const void*)kern, smem, "topk: smem attribute")) return rc_;
     kern<<<(unsigned)rows, kFinThreads, smem, st>>>(scores, g, idx, idx_stride, count);
+    note_launches(1);
     return check_launch("topk_small");
   }
   if (g.M > g.k && g.M >= 4 * 16 && rows <= 65535) {
@@ -1226,6 +1228,7 @@ static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
   auto fin = topk_finish_kernel<F32>;
   if (int rc_ = set_smem_limit((const void*)fin, smem, "topk: smem attribute")) return rc_;
   fin<<<(unsigned)rows, kFinThreads, smem, st>>>(scores, g, ws, idx, idx_stride, count);
+  note_launches(3);
   return check_launch("topk");
 }
 

@@ -62,6 +62,8 @@ def score_buffer_bytes(B: int, Hkv: int, n_units: int) -> int:
 
 
 def plane_scan_alu_ops(plan: np.ndarray, n: int) -> int:
-    """One bit test and one predicated add per planned plane per token per KV
-    head (the in-HBM bit-plane scan is bound by these, as the Fathom page notes)."""
-    return int(2 * plan.astype(np.int64).sum() * n)
+    """Planned token-planes: each costs one bit test and one predicated FP32 add
+    per token per KV head (the in-HBM bit-plane scan is bound by these, as the
+    Fathom page notes); counted once, against the FP32 pipe's one add per lane
+    per clock."""
+    return int(plan.astype(np.int64).sum() * n)
