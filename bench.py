@@ -366,23 +366,23 @@ def main():
     st_score = statistics.mean(timed_steps(torch, lambda: step.stage_score(q), K_st, 3, flush))
     st_topk = statistics.mean(timed_steps(torch, lambda: step.stage_topk(), K_st, 3, flush))
     st_att = statistics.mean(timed_steps(torch, lambda: step.stage_attend(q), K_st, 3, flush))
+    st_fused = (statistics.mean(timed_steps(torch, lambda: step.stage_score_topk(q), K_st, 3,
+                                            flush)) if step.fused else None)
     eager = statistics.mean(timed_steps(torch, lambda: step.run(q), K_st, 3, flush))
 
     # marginal stage costs inside the step: cumulative prefixes, L2 flushed before each
+    stages = step.stages()
+
     def upto(nst):
         def f():
-            step.stage_prep(q)
-            if nst > 1:
-                step.stage_score(q)
-            if nst > 2:
-                step.stage_topk()
-            if nst > 3:
-                step.stage_attend(q)
+            for _, fn in stages[:nst]:
+                fn(q)
         return f
 
-    cum = [statistics.mean(timed_steps(torch, upto(i), K_st, 3, flush)) for i in (1, 2, 3, 4)]
-    marginal = {"plan": cum[0] * 1e3, "scan": (cum[1] - cum[0]) * 1e3,
-                "topk": (cum[2] - cum[1]) * 1e3, "gather_attend": (cum[3] - cum[2]) * 1e3}
+    cum = [statistics.mean(timed_steps(torch, upto(i), K_st, 3, flush))
+           for i in range(1, len(stages) + 1)]
+    marginal = {name: (cum[i] - (cum[i - 1] if i else 0.0)) * 1e3
+                for i, (name, _) in enumerate(stages)}
     peak_gbs, peak_kind = peaks()
     scan_gbs = scan_bytes / (st_score * 1e-3) / 1e9
     alu_ops = rl.plane_scan_alu_ops(plan_np, n)
@@ -452,9 +452,8 @@ def main():
         def offload_step():
             sto.stage_prep(q)
             sd.sd_offload_gather(shp, hp, hs, sto.plan, dpl, dsc)
-            sto.stage_score(q)
-            sto.stage_topk()
-            sto.stage_attend(q)
+            for _, fn in sto.stages()[1:]:
+                fn(q)
 
         to = statistics.mean(timed_steps(torch, offload_only, K_st, 3, flush))
         tos = statistics.mean(timed_steps(torch, offload_step, K_st, 3, flush))
@@ -483,6 +482,7 @@ def main():
                    "parallelism": f"replicas x{ws}"},
         "us_per_step": t_step_max * 1e3,
         "stages_us": {"plan": st_prep * 1e3, "scan": st_score * 1e3, "topk": st_topk * 1e3,
+                      "scan_topk": None if st_fused is None else st_fused * 1e3,
                       "gather_attend": st_att * 1e3, "step_eager": eager * 1e3},
         "stages_in_step_us": marginal,
         # the scan is bound by one bit test and one predicated FP32 add per planned

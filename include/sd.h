@@ -170,6 +170,32 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
             int32_t* count, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * sd_score_topk -- sd_score(SD_IDX_PLANES) then sd_topk(SD_SCORE_F32) on those
+ * scores, in one call (Fathom's bit-plane scan feeding HashAttention 2.1's TOPK):
+ * writes exactly the scores, idx and count the two calls would.
+ *   Arguments as sd_score with kind SD_IDX_PLANES (planes, scales, q, plan;
+ *   scores fp32 [B*hkv][n]) and as sd_topk with rows = batch * hkv and
+ *   n_units = n_tokens = n; sel.block must be 1.
+ *   Rows of at least 65536 competing tokens (n - sink - local) with n_cap a
+ *   multiple of 512 and 16-byte aligned planes and scales take a fused path: a
+ *   sample of each row (512 runs of 32 tokens, scored with the plan) sets a
+ *   threshold below the row's k-th score with high probability, the scan marks
+ *   every competing token that reaches it (one bit per token), and the top k are
+ *   drawn from the marked tokens instead of from a second pass over the scores;
+ *   a row with fewer than k marks, more than the selection can gather, or a NaN
+ *   is selected from its full score row.  Other calls run the scan, then
+ *   sd_topk's kernels.
+ *   Workspace: sd_score_topk_workspace_size() bytes of device memory, 256-byte
+ *   aligned; contents need not be initialised; calls sharing a workspace must
+ *   not overlap.
+ */
+size_t sd_score_topk_workspace_size(const sd_shape* shape, const sd_select* sel);
+int sd_score_topk(const sd_shape* shape, const void* planes, const void* scales, const void* q,
+                  const uint8_t* plan, const sd_select* sel, float* scores, int32_t* idx,
+                  int64_t idx_stride, int32_t* count, void* workspace, size_t ws_bytes,
+                  void* stream);
+
+/*
  * sd_gather_attend -- GATHER-ATT (HashAttention 2.1, corrected o_hat; 2.5 page
  * size 1): for query head g of sequence b, KV head h = g / G, over the rows
  * I = idx[b*hkv + h][0..count): z_i = scale * <q_g, k_i>,

@@ -28,6 +28,7 @@ __all__ = [
     "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
     "sd_gather_attend_noalloc", "sd_offload_gather",
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
+    "sd_score_topk_workspace_size", "sd_score_topk",
 ]
 
 
@@ -134,6 +135,19 @@ def sd_topk(score_type: int, scores, rows: int, n_units: int, n_tokens: int, sel
     _check(lib().sd_topk(score_type, _ptr(scores), rows, n_units, n_tokens, ctypes.byref(sel),
                          _ptr(idx), idx_stride, _ptr(count), _ptr(workspace), ws_bytes,
                          _stream(stream)), "sd_topk")
+
+
+def sd_score_topk_workspace_size(shape: SdShape, sel: SdSelect) -> int:
+    return int(lib().sd_score_topk_workspace_size(ctypes.byref(shape), ctypes.byref(sel)))
+
+
+def sd_score_topk(shape: SdShape, planes, scales, q, plan, sel: SdSelect, scores, idx,
+                  idx_stride: int, count, workspace=None, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().sd_score_topk(ctypes.byref(shape), _ptr(planes), _ptr(scales), _ptr(q),
+                               _ptr(plan), ctypes.byref(sel), _ptr(scores), _ptr(idx),
+                               idx_stride, _ptr(count), _ptr(workspace), ws_bytes,
+                               _stream(stream)), "sd_score_topk")
 
 
 def sd_gather_attend_workspace_size(shape: SdShape, max_count: int) -> int:

@@ -211,6 +211,43 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
                      workspace, ws_bytes, (cudaStream_t)stream);
 }
 
+size_t sd_score_topk_workspace_size(const sd_shape* shape, const sd_select* sel) {
+  Dims s;
+  if (!sel || check_shape(shape, &s, true)) return 0;
+  return score_topk_workspace_bytes((int64_t)s.B * s.Hkv, s.n, *sel);
+}
+
+int sd_score_topk(const sd_shape* shape, const void* planes, const void* scales, const void* q,
+                  const uint8_t* plan, const sd_select* sel, float* scores, int32_t* idx,
+                  int64_t idx_stride, int32_t* count, void* workspace, size_t ws_bytes,
+                  void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s, true);
+  if (rc) return rc;
+  if (!planes || !scales || !q || !plan || !sel || !scores || !idx || !count)
+    return fail(SD_ERR_INVALID_ARG, "sd_score_topk: NULL input");
+  if (!aligned16(planes) || !aligned16(scores))
+    return fail(SD_ERR_INVALID_ARG, "sd_score_topk: planes and scores must be 16-byte aligned");
+  if (sel->k < 1 || sel->k > kMaxTopK)
+    return fail(SD_ERR_UNSUPPORTED, "sd_score_topk: k = %d outside [1, %d]", sel->k, kMaxTopK);
+  if (sel->sink < 0 || sel->local < 0 || sel->block != 1)
+    return fail(SD_ERR_INVALID_ARG, "sd_score_topk: negative window or block != 1");
+  const int64_t rows = (int64_t)s.B * s.Hkv;
+  const int64_t max_units = s.n < (int64_t)sel->sink + sel->local + sel->k
+                                ? s.n : (int64_t)sel->sink + sel->local + sel->k;
+  if (idx_stride < max_units)
+    return fail(SD_ERR_INVALID_ARG, "sd_score_topk: idx_stride %lld < %lld",
+                (long long)idx_stride, (long long)max_units);
+  const size_t need = score_topk_workspace_bytes(rows, s.n, *sel);
+  if (!workspace || ws_bytes < need)
+    return fail(SD_ERR_WORKSPACE, "sd_score_topk: workspace %zu < %zu bytes", ws_bytes, need);
+  if ((uintptr_t)workspace % 256)
+    return fail(SD_ERR_INVALID_ARG, "sd_score_topk: workspace must be 256-byte aligned");
+  return launch_score_topk(s, (const uint32_t*)planes, (const uint16_t*)scales, plan,
+                           (const uint16_t*)q, *sel, scores, idx, idx_stride, count, workspace,
+                           (cudaStream_t)stream);
+}
+
 size_t sd_gather_attend_workspace_size(const sd_shape* shape, int64_t max_count) {
   Dims s;
   if (check_shape(shape, &s) || max_count < 0) return 0;

@@ -9,6 +9,8 @@
 
 namespace sd {
 
+struct PsCand;  // sd_planes.cuh
+
 constexpr int kD = 128;          // head dimension supported by this build
 constexpr int kMaxTopK = 4096;   // largest retrieval budget of sd_topk
 constexpr int kSmallRow = 8192;  // rows up to this many units are selected by one CTA
@@ -42,6 +44,12 @@ __device__ __forceinline__ uint32_t key_of_f32(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ uint32_t key_of_i32(int32_t x) { return (uint32_t)x ^ 0x80000000u; }
+// max that propagates NaN (PTX max.NaN), so one compare screens several scores
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
 
 // ---- launchers (each returns SD_OK or an SD_ERR_*) ---------------------------------
 struct Dims {
@@ -60,11 +68,20 @@ int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode,
                 uint8_t* plan, cudaStream_t st);
 int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsig,
                          int32_t* scores, cudaStream_t st);
+// (cand: the fused scan + top-k's candidate list, or null)
+bool planes_aligned(const Dims& s, const void* planes, const void* scales);
 int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
-                        const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st);
+                        const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st,
+                        const PsCand* cand = nullptr);
 int launch_score_quest(const Dims& s, const uint16_t* summ, const uint16_t* q, float* scores,
                        cudaStream_t st);
 size_t topk_workspace_bytes(int64_t rows, int64_t n_units, const sd_select& sel);
+// fused bit-plane scan + top-k (sd_score_topk)
+size_t score_topk_workspace_bytes(int64_t rows, int64_t n, const sd_select& sel);
+int launch_score_topk(const Dims& s, const uint32_t* planes, const uint16_t* scales,
+                      const uint8_t* plan, const uint16_t* q, const sd_select& sel, float* scores,
+                      int32_t* idx, int64_t idx_stride, int32_t* count, void* ws,
+                      cudaStream_t st);
 int launch_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
                 int64_t n_tokens, const sd_select& sel, int32_t* idx, int64_t idx_stride,
                 int32_t* count, void* ws, size_t ws_bytes, cudaStream_t st);

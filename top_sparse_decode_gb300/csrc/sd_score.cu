@@ -11,6 +11,7 @@
 #include <cuda_fp16.h>
 
 #include "sd_internal.cuh"
+#include "sd_planes.cuh"
 
 namespace sd {
 
@@ -117,12 +118,21 @@ constexpr int kBarFull = 1, kBarEmpty = kBarFull + kPsSlots, kBarHelp = kBarEmpt
 constexpr int kSlotFirst = 1, kSlotLast = 2, kSlotEnd = 4;
 
 struct PsSlot {
-  int ne;     // planes in the chunk (0 for a tile with no active plane)
-  int flags;  // kSlotFirst / kSlotLast of its tile, kSlotEnd
-  int cs;     // the tile's entry in the Cs ring
-  int nwv;    // the tile's valid words
-  int64_t out;  // the tile's first score
+  int64_t tok0;  // the tile's first token
+  int row;       // the tile's (sequence, KV head) row
+  uint32_t thr;  // the row's candidate threshold key (fused scan + top-k)
+  // planes in the chunk (bits 0-7; 0 for a tile with no active plane), the tile's
+  // valid words (8-15), kSlotFirst / kSlotLast / kSlotEnd (16-19), the tile's
+  // entry in the Cs ring (20-21)
+  int info;
+  __host__ __device__ int ne() const { return info & 255; }
+  __host__ __device__ int nwv() const { return (info >> 8) & 255; }
+  __host__ __device__ int flags() const { return (info >> 16) & 15; }
+  __host__ __device__ int cs() const { return (info >> 20) & 3; }
 };
+__device__ __forceinline__ int slot_info(int ne, int nwv, int flags, int cs) {
+  return ne | (nwv << 8) | (flags << 16) | (cs << 20);
+}
 
 struct PsSmem {
   uint32_t words[kPsSlots][kPsChunk][kPsWords];  // 48 KB
@@ -134,15 +144,7 @@ struct PsSmem {
   float Cs[4][kPsBlocks];                        // per-block constants of 4 tiles in flight
   float hred[4][kPsBlocks];
   PsSlot slot[kPsSlots];
-  float qt[kD];
-  float qo[kD];                                  // q~_j * (h(t_j) - 8) per slot
-  int tb[kD];
-  int slot_of[kD];
-  int chan[kD];                                  // channel of each slot
-  uint16_t act[4 * kD];                          // active entries j * 4 + p, j ascending
-  uint8_t eslot[4 * kD];                         // slot of each entry's channel
-  float qp[4 * kD];                              // q~_j * 2^(3-p) per entry (exact scaling)
-  int nact, nch;
+  PsRow row;                                     // the current row's tables
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -163,18 +165,42 @@ __device__ __forceinline__ void nb_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
-// acc[i] += wt for every set bit i of w (a bit test and a predicated add per bit)
-__device__ __forceinline__ void ps_bits(float (&acc)[32], uint32_t w, float wt) {
+// Marks this lane's competing scores that reach the row's threshold in the hit
+// masks (warp-collective: every lane of the warp calls it).
+__device__ __forceinline__ void ps_mark(const PsCand& cd, int row, uint32_t T, int64_t tok,
+                                        bool valid, const float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+  const bool all = T == 0;  // key 0 lies below every score's key
+  const float Tf = __uint_as_float((T & 0x80000000u) ? (T & 0x7FFFFFFFu) : ~T);
+  float t[16];  // the maximum of the 32 scores as a tree (depth 5)
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    asm("{\n\t.reg .pred p;\n\t.reg .b32 t;\n\tand.b32 t, %1, %2;\n\tsetp.ne.b32 p, t, 0;\n\t"
-        "@p add.f32 %0, %0, %3;\n\t}"
-        : "+f"(acc[i])
-        : "r"(w), "r"(1u << i), "f"(wt));
+  for (int i = 0; i < 16; ++i) t[i] = fmax_nan(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmax_nan(t[i], t[i + w]);
+  const float mx = t[0];
+  // almost every lane lies below the threshold: one compare screens its 32 scores
+  const bool maybe = valid && (all || !(mx < Tf));  // reaches it, or holds a NaN
+  uint32_t hit = 0;
+  bool nan = false;
+  if (maybe) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const bool in = tok + i >= cd.lead && tok + i < cd.tail;
+      nan |= in && v[i] != v[i];
+      if (in && (all || v[i] >= Tf)) hit |= 1u << i;
+    }
+  }
+  if (valid) cd.hits[(int64_t)row * cd.n32 + tok / 32] = hit;  // every word, every call
+  if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) atomicOr(cd.nan + row, 1u);
 }
 
-// Compute warps: consume slots until the end marker.
-__device__ __forceinline__ void ps_compute(PsSmem& S, float* __restrict__ scores) {
+// Compute warps: consume slots until the end marker; with CAND, also append the
+// row's candidates (see PsCand).
+template <bool CAND>
+__device__ __forceinline__ void ps_compute(PsSmem& S, float* __restrict__ scores, int64_t n,
+                                           const PsCand& cd) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = warp >> 2, wl = (warp & 3) * 32 + lane;  // plane parity, word
   float4* red = &S.red[wl * 8];
@@ -186,20 +212,21 @@ __device__ __forceinline__ void ps_compute(PsSmem& S, float* __restrict__ scores
     const int s = c % kPsSlots;
     nb_sync(kBarFull + s, kPsThreads);
     const PsSlot m = S.slot[s];
-    if (m.flags & kSlotEnd) break;
-    if (m.flags & kSlotFirst) {
+    const int flags = m.flags(), nwv = m.nwv();
+    if (flags & kSlotEnd) break;
+    if (flags & kSlotFirst) {
 #pragma unroll
       for (int k = 0; k < 32; ++k) acc[k] = 0.0f;
     }
-    if ((warp & 3) * 32 < m.nwv) {  // warps whose words all lie past the end idle
+    if ((warp & 3) * 32 < nwv) {  // warps whose words all lie past the end idle
       const uint32_t* wp = &S.words[s][half][wl];
       const float* tp = &S.Wt[s][half][wl >> 1];
 #pragma unroll 2
-      for (int e = half; e < m.ne; e += 2, wp += 2 * kPsWords, tp += 2 * kPsBlocks)
+      for (int e = half, ne = m.ne(); e < ne; e += 2, wp += 2 * kPsWords, tp += 2 * kPsBlocks)
         ps_bits(acc, *wp, *tp);
     }
     nb_arrive(kBarEmpty + s, kPsThreads);
-    if (m.flags & kSlotLast) {
+    if (flags & kSlotLast) {
       // odd-plane partial sums: lane l's eight float4s go to 16-byte slots k ^ (l & 7),
       // so each quarter-warp hits 8 distinct bank groups.  (The next tile's writes to
       // red come after a FULL wait that every compute thread joins only once done
@@ -210,15 +237,20 @@ __device__ __forceinline__ void ps_compute(PsSmem& S, float* __restrict__ scores
           red[k ^ sw] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
       }
       nb_sync(kBarComp, kPsCompute);
-      if (half == 0 && wl < m.nwv) {
-        const float cb = S.Cs[m.cs][wl >> 1];
-        float4* orow = reinterpret_cast<float4*>(scores + m.out + wl * 32);
+      if (half == 0) {
+        const bool valid = wl < nwv;
+        const float cb = S.Cs[m.cs()][wl >> 1];
+        float4* orow = reinterpret_cast<float4*>(scores + (int64_t)m.row * n + m.tok0 + wl * 32);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const float4 o = red[k ^ sw];
-          orow[k] = make_float4((acc[4 * k] + o.x) + cb, (acc[4 * k + 1] + o.y) + cb,
-                                (acc[4 * k + 2] + o.z) + cb, (acc[4 * k + 3] + o.w) + cb);
+          acc[4 * k] = (acc[4 * k] + o.x) + cb;
+          acc[4 * k + 1] = (acc[4 * k + 1] + o.y) + cb;
+          acc[4 * k + 2] = (acc[4 * k + 2] + o.z) + cb;
+          acc[4 * k + 3] = (acc[4 * k + 3] + o.w) + cb;
+          if (valid) orow[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
         }
+        if (CAND) ps_mark(cd, m.row, m.thr, m.tok0 + wl * 32, valid, acc);
       }
     }
   }
@@ -248,20 +280,20 @@ __device__ __forceinline__ void ps_finish(PsSmem& S, const PsPending& pd, int d,
   nb_sync(kBarHelp, kPsHelpers);  // every helper's copies of the chunk have landed
   const int s = d % kPsSlots;
   const uint16_t* scb = ps_scales(S, pd.sb);
-  const int nbv = pd.m.nwv / 2;
+  const int nbv = pd.m.nwv() / 2;
   // blocks b4..b4+3 (a group that reaches past nbv holds blocks past the end: their
   // values are read only by lanes whose sums are not stored)
   const int b4 = (lane & 15) * 4;
-  if (pd.m.flags & kSlotFirst) {
+  if (pd.m.flags() & kSlotFirst) {
     // per-block constants C_blk: half-warps take alternate slots, a shuffle joins
     // the halves, then the four warps' partial sums are added
     float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (b4 < nbv) {
-      for (int sl = 2 * hw + (lane >> 4); sl < S.nch; sl += 2 * (kPsHelpers / 32)) {
+      for (int sl = 2 * hw + (lane >> 4); sl < S.row.nch; sl += 2 * (kPsHelpers / 32)) {
         const uint2 raw = *reinterpret_cast<const uint2*>(scb + sl * kPsBlocks + b4);
         const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
         const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        const float qo = S.qo[sl];
+        const float qo = S.row.qo[sl];
         a.x = __fadd_rn(a.x, __fmul_rn(qo, f0.x));
         a.y = __fadd_rn(a.y, __fmul_rn(qo, f0.y));
         a.z = __fadd_rn(a.z, __fmul_rn(qo, f1.x));
@@ -275,7 +307,7 @@ __device__ __forceinline__ void ps_finish(PsSmem& S, const PsPending& pd, int d,
     if (lane < 16) *reinterpret_cast<float4*>(&S.hred[hw][b4]) = a;
     nb_sync(kBarHelp, kPsHelpers);
     if (ht < kPsBlocks)
-      S.Cs[pd.m.cs][ht] = __fadd_rn(__fadd_rn(S.hred[0][ht], S.hred[1][ht]),
+      S.Cs[pd.m.cs()][ht] = __fadd_rn(__fadd_rn(S.hred[0][ht], S.hred[1][ht]),
                                     __fadd_rn(S.hred[2][ht], S.hred[3][ht]));
   }
   // folded weights Wt = (q~_j * 2^(3-p)) * s_j,blk, which equals
@@ -283,9 +315,9 @@ __device__ __forceinline__ void ps_finish(PsSmem& S, const PsPending& pd, int d,
   // half-warps take alternate planes, each lane four blocks
   if (b4 < nbv) {
 #pragma unroll 2
-    for (int e = 2 * hw + (lane >> 4); e < pd.m.ne; e += 2 * (kPsHelpers / 32)) {
-      const float qv = S.qp[pd.e0 + e];
-      const uint2 raw = *reinterpret_cast<const uint2*>(scb + S.eslot[pd.e0 + e] * kPsBlocks + b4);
+    for (int e = 2 * hw + (lane >> 4), ne = pd.m.ne(); e < ne; e += 2 * (kPsHelpers / 32)) {
+      const float qv = S.row.qp[pd.e0 + e];
+      const uint2 raw = *reinterpret_cast<const uint2*>(scb + S.row.eslot[pd.e0 + e] * kPsBlocks + b4);
       const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
       const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
       *reinterpret_cast<float4*>(&S.Wt[s][e][b4]) =
@@ -302,12 +334,13 @@ __device__ __forceinline__ void ps_finish(PsSmem& S, const PsPending& pd, int d,
 // c - 2 is finished and handed over.  The pipeline drains before a row change
 // (the row tables are rebuilt) and, past 64 active channels, before each tile
 // (one flat scale buffer); then the end marker is posted.
-template <int G, bool A16>
+template <int G, bool A16, bool CAND>
 __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ planes,
                                         const uint16_t* __restrict__ scales,
                                         const uint8_t* __restrict__ plan,
                                         const uint16_t* __restrict__ q, int Hq, int Hkv, int64_t n,
-                                        int64_t ncap, int upr, int64_t total_units) {
+                                        int64_t ncap, int upr, int64_t total_units,
+                                        const PsCand& cd) {
   const int ht = threadIdx.x - kPsCompute, hw = ht >> 5, lane = threadIdx.x & 31;
   const uint32_t wstride = (uint32_t)(ncap / 32), sstride = (uint32_t)(ncap / 64);
   // this CTA's units, walked as (row bh, unit ur) without dividing; rows <= 65535
@@ -318,6 +351,7 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
   int bh = (int)(u_begin / upr);
   int ur = (int)(u_begin - (int64_t)bh * upr);
   int cur_bh = -1;
+  uint32_t row_thr = 0;
   int c = 0, d = 0;  // chunks issued, chunks handed over
   PsPending p0, p1;  // pending chunks, oldest first (registers: indexed statically)
   int np = 0;
@@ -334,57 +368,11 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
       }
       nb_sync(kBarHelp, kPsHelpers);  // every helper is done with the old tables
       cur_bh = bh;
-      const int b = bh / Hkv, h = bh % Hkv;
-      {
-        const int j = ht;
-        float a = 0.0f;
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-          a = __fadd_rn(a, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]));
-        S.qt[j] = a;
-        S.tb[j] = min((int)plan[(int64_t)bh * kD + j], 4);  // a plan holds 0..4 bits per channel
-      }
-      nb_sync(kBarHelp, kPsHelpers);
-      if (hw == 0) {  // active entries and channel slots, j ascending
-        int cnt[4], tot = 0, chs = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          cnt[k] = S.tb[lane * 4 + k];
-          tot += cnt[k];
-          chs += cnt[k] > 0;
-        }
-        int incl = tot, inclc = chs;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-          const int yc = __shfl_up_sync(0xFFFFFFFFu, inclc, off);
-          if (lane >= off) { incl += y; inclc += yc; }
-        }
-        int pos = incl - tot, slot = inclc - chs;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int j = lane * 4 + k;
-          for (int p = 0; p < cnt[k]; ++p) S.act[pos++] = (uint16_t)(j * 4 + p);
-          if (cnt[k] > 0) {
-            S.slot_of[j] = slot;
-            S.chan[slot] = j;
-            S.qo[slot] = __fmul_rn(S.qt[j], cnt[k] < 4 ? (float)((1 << (3 - cnt[k])) - 8) : -8.0f);
-            ++slot;
-          } else {
-            S.slot_of[j] = 0;
-          }
-        }
-        if (lane == 31) { S.nact = incl; S.nch = inclc; }
-      }
-      nb_sync(kBarHelp, kPsHelpers);
-      for (int e = ht; e < S.nact; e += kPsHelpers) {
-        const int ent = S.act[e], j = ent >> 2, p = ent & 3;
-        S.eslot[e] = (uint8_t)S.slot_of[j];
-        S.qp[e] = ldexpf(S.qt[j], 3 - p);
-      }
-      nb_sync(kBarHelp, kPsHelpers);
+      ps_build_row<G>(S.row, ht, q, plan, bh / Hkv, bh % Hkv, Hq, (int64_t)bh,
+                      [] { nb_sync(kBarHelp, kPsHelpers); });
+      if (CAND) row_thr = __ldg(cd.thr + bh);
     }
-    const int nact = S.nact, nch = S.nch;
+    const int nact = S.row.nact, nch = S.row.nch;
     const int nck = max(1, (nact + kPsChunk - 1) / kPsChunk);
     const int sb = nch <= kD / 2 ? (tcount & 1) : 2;
     if (sb == 2) {  // one flat scale buffer: drain first
@@ -412,7 +400,7 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
           // whole 16-byte segments (8 blocks) inside the valid blocks, the rest singly
           for (int x = ht; x < nch * 8; x += kPsHelpers) {
             const int sl = x >> 3, sg = x & 7;
-            const uint16_t* src = sc_tile + (uint64_t)S.chan[sl] * sstride + sg * 8;
+            const uint16_t* src = sc_tile + (uint64_t)S.row.chan[sl] * sstride + sg * 8;
             uint16_t* dst = scb + sl * kPsBlocks + sg * 8;
             if (sg * 8 + 8 <= nbv) {
               cp_async16(smem_u32(dst), src);
@@ -423,7 +411,7 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
         } else {
           for (int x = ht; x < nch * kPsBlocks; x += kPsHelpers) {
             const int sl = x / kPsBlocks, blk = x % kPsBlocks;
-            if (blk < nbv) scb[sl * kPsBlocks + blk] = sc_tile[(uint64_t)S.chan[sl] * sstride + blk];
+            if (blk < nbv) scb[sl * kPsBlocks + blk] = sc_tile[(uint64_t)S.row.chan[sl] * sstride + blk];
           }
         }
       }
@@ -435,7 +423,7 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
         const int seg = lane * 4 + 4 <= nwv ? 16 : (lane * 4 + 2 == nwv ? 8 : 0);
         if (seg) {
           for (int e = hw; e < ne; e += kPsHelpers / 32) {
-            const uint32_t* src = pl_tile + (uint64_t)S.act[e0 + e] * wstride + lane * 4;
+            const uint32_t* src = pl_tile + (uint64_t)S.row.act[e0 + e] * wstride + lane * 4;
             const uint32_t dd = wdst + e * (kPsWords * 4) + lane * 16;
             if (seg == 16) cp_async16(dd, src);
             else cp_async8(dd, src);
@@ -443,18 +431,18 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
         }
       } else {
         for (int e = hw; e < ne; e += kPsHelpers / 32) {
-          const uint32_t* src = pl_tile + (uint64_t)S.act[e0 + e] * wstride;
+          const uint32_t* src = pl_tile + (uint64_t)S.row.act[e0 + e] * wstride;
           for (int sg = lane; sg * 2 < nwv; sg += 32)
             cp_async8(wdst + e * (kPsWords * 4) + sg * 8, src + sg * 2);
         }
       }
       cp_async_commit();
       PsPending pd;
-      pd.m.ne = ne;
-      pd.m.flags = (k == 0 ? kSlotFirst : 0) | (k == nck - 1 ? kSlotLast : 0);
-      pd.m.cs = tcount & 3;
-      pd.m.nwv = nwv;
-      pd.m.out = (int64_t)bh * n + tok0;
+      pd.m.info = slot_info(ne, nwv, (k == 0 ? kSlotFirst : 0) | (k == nck - 1 ? kSlotLast : 0),
+                            tcount & 3);
+      pd.m.tok0 = tok0;
+      pd.m.row = bh;
+      pd.m.thr = row_thr;
       pd.e0 = e0;
       pd.sb = sb;
       if (np == 0) p0 = pd;
@@ -474,24 +462,24 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
   {
     const int s = c % kPsSlots;
     if (c >= kPsSlots) nb_sync(kBarEmpty + s, kPsThreads);
-    if (ht == 0) S.slot[s].flags = kSlotEnd;
+    if (ht == 0) S.slot[s].info = slot_info(0, 0, kSlotEnd, 0);
     nb_arrive(kBarFull + s, kPsThreads);
   }
   for (int x = max(0, c - kPsSlots + 1); x < c; ++x) nb_sync(kBarEmpty + x % kPsSlots, kPsThreads);
 }
 
-template <int G, bool A16>
+template <int G, bool A16, bool CAND>
 __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm)
 score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
                     const uint8_t* __restrict__ plan, const uint16_t* __restrict__ q, int Hq,
                     int Hkv, int64_t n, int64_t ncap, int upr, int64_t total_units,
-                    float* __restrict__ scores) {
+                    float* __restrict__ scores, PsCand cd) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PsSmem& S = *reinterpret_cast<PsSmem*>(smem_raw);
   if (threadIdx.x < kPsCompute)
-    ps_compute(S, scores);
+    ps_compute<CAND>(S, scores, n, cd);
   else
-    ps_help<G, A16>(S, planes, scales, plan, q, Hq, Hkv, n, ncap, upr, total_units);
+    ps_help<G, A16, CAND>(S, planes, scales, plan, q, Hq, Hkv, n, ncap, upr, total_units, cd);
 }
 
 static int sm_count() {
@@ -507,30 +495,46 @@ static int sm_count() {
   return cnt[dev];
 }
 
-template <int G, bool A16>
+template <int G, bool A16, bool CAND>
 static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scales,
-                    const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st) {
-  auto kern = score_planes_kernel<G, A16>;
+                    const uint8_t* plan, const uint16_t* q, float* scores, const PsCand& cd,
+                    cudaStream_t st) {
+  auto kern = score_planes_kernel<G, A16, CAND>;
   if (int rc = set_smem_limit((const void*)kern, sizeof(PsSmem), "score_planes: smem attribute"))
     return rc;
   const int upr = (int)((s.n + kPsUnit - 1) / kPsUnit);  // units per row (n < 2^31)
   const int64_t total = (int64_t)upr * s.B * s.Hkv;
   const int64_t grid = imin64(total, (int64_t)sm_count() * kPsCtasPerSm);
   kern<<<(unsigned)grid, kPsThreads, sizeof(PsSmem), st>>>(planes, scales, plan, q, s.Hq, s.Hkv,
-                                                          s.n, s.ncap, upr, total, scores);
+                                                          s.n, s.ncap, upr, total, scores, cd);
   note_launches(1);
   return check_launch("score_planes");
 }
 
+bool planes_aligned(const Dims& s, const void* planes, const void* scales) {
+  return (s.ncap % 512 == 0) && ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
+}
+
 int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
-                        const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st) {
-  const bool a16 = (s.ncap % 512 == 0) && ((uintptr_t)planes % 16 == 0) &&
-                   ((uintptr_t)scales % 16 == 0);
+                        const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st,
+                        const PsCand* cand) {
+  const bool a16 = planes_aligned(s, planes, scales);
+  if (cand) {  // the fused scan + top-k path (16-byte aligned layouts only)
+    if (!a16) return fail(SD_ERR_INVALID_ARG, "score_planes: candidates need n_cap %% 512 == 0 "
+                                              "and 16-byte aligned planes and scales");
+    switch (s.G) {
+      case 1: return planes_t<1, true, true>(s, planes, scales, plan, q, scores, *cand, st);
+      case 2: return planes_t<2, true, true>(s, planes, scales, plan, q, scores, *cand, st);
+      case 4: return planes_t<4, true, true>(s, planes, scales, plan, q, scores, *cand, st);
+      default: return planes_t<8, true, true>(s, planes, scales, plan, q, scores, *cand, st);
+    }
+  }
+  const PsCand none{};
   switch (s.G) {
-    case 1: return a16 ? planes_t<1, true>(s, planes, scales, plan, q, scores, st) : planes_t<1, false>(s, planes, scales, plan, q, scores, st);
-    case 2: return a16 ? planes_t<2, true>(s, planes, scales, plan, q, scores, st) : planes_t<2, false>(s, planes, scales, plan, q, scores, st);
-    case 4: return a16 ? planes_t<4, true>(s, planes, scales, plan, q, scores, st) : planes_t<4, false>(s, planes, scales, plan, q, scores, st);
-    default: return a16 ? planes_t<8, true>(s, planes, scales, plan, q, scores, st) : planes_t<8, false>(s, planes, scales, plan, q, scores, st);
+    case 1: return a16 ? planes_t<1, true, false>(s, planes, scales, plan, q, scores, none, st) : planes_t<1, false, false>(s, planes, scales, plan, q, scores, none, st);
+    case 2: return a16 ? planes_t<2, true, false>(s, planes, scales, plan, q, scores, none, st) : planes_t<2, false, false>(s, planes, scales, plan, q, scores, none, st);
+    case 4: return a16 ? planes_t<4, true, false>(s, planes, scales, plan, q, scores, none, st) : planes_t<4, false, false>(s, planes, scales, plan, q, scores, none, st);
+    default: return a16 ? planes_t<8, true, false>(s, planes, scales, plan, q, scores, none, st) : planes_t<8, false, false>(s, planes, scales, plan, q, scores, none, st);
   }
 }
 

@@ -28,6 +28,7 @@
 #include <cmath>
 
 #include "sd_internal.cuh"
+#include "sd_planes.cuh"
 
 namespace sd {
 
@@ -552,53 +553,39 @@ topk_filter_kernel(const void* __restrict__ scores, Geo g, Ws ws, bool vec) {
   }
 }
 
-template <bool F32>
-__global__ void __launch_bounds__(kFinThreads)
-topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __restrict__ idx,
-                   int64_t idx_stride, int32_t* __restrict__ count) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  FinSmem& S = *reinterpret_cast<FinSmem*>(smem_raw);
-  const int64_t row = blockIdx.x;
-  const RowState& st = ws.st[row];
-  int32_t* idx_row = idx + row * idx_stride;
-  if (st.nan) {
-    if (threadIdx.x == 0) count[row] = -1;
-    return;
-  }
-  if (threadIdx.x == 0) { S.nsel = 0; S.kmin = 0xFFFFFFFFu; S.kmax = 0; }
-  if (g.M <= g.k) {
-    for (int i = threadIdx.x; i < g.M; i += kFinThreads) S.sel[i] = g.lead + i;
-    __syncthreads();
-    write_units<kFinThreads>(g, S.sel, g.M, idx_row, count + row);
-    return;
-  }
-  __syncthreads();
-  const uint32_t c = st.ncand;
+// Finishes a row whose c candidates (key << 32 | unit) are in S.C: the exact top k
+// among them when c >= k and they all fit (c <= kCap), else an exact selection
+// over the whole row in this CTA; then sorts and writes the units.  (Every
+// thread of the CTA calls it; S.nsel is zero and M > k.)
+template <bool F32, int NT>
+__device__ void finish_row(FinSmem& S, const void* __restrict__ scores, const Geo& g,
+                           int64_t row, uint32_t c, int32_t* __restrict__ idx_row,
+                           int32_t* __restrict__ count_row) {
   const int bI = bits_of((uint32_t)(g.M - 1));
   const uint64_t imask = (1ull << bI) - 1;
+  if (threadIdx.x == 0) { S.kmin = 0xFFFFFFFFu; S.kmax = 0; }
+  __syncthreads();
   if (c >= (uint32_t)g.k && c <= (uint32_t)kCap) {
-    const uint64_t* cand = ws.cand + row * kCap;
     uint32_t mn = 0xFFFFFFFFu, mx = 0;
-    for (uint32_t i = threadIdx.x; i < c; i += kFinThreads) {
-      uint64_t x = cand[i];
-      S.C[i] = x;
-      mn = min(mn, (uint32_t)(x >> 32));
-      mx = max(mx, (uint32_t)(x >> 32));
+    for (uint32_t i = threadIdx.x; i < c; i += NT) {
+      const uint32_t kk = (uint32_t)(S.C[i] >> 32);
+      mn = min(mn, kk);
+      mx = max(mx, kk);
     }
     atomicMin(&S.kmin, mn);
     atomicMax(&S.kmax, mx);
     __syncthreads();
     const uint32_t kmin = S.kmin;
     const int nb = bits_of(S.kmax - kmin) + bI;
-    for (uint32_t i = threadIdx.x; i < c; i += kFinThreads) {
+    for (uint32_t i = threadIdx.x; i < c; i += NT) {
       uint64_t x = S.C[i];
       uint32_t u = (uint32_t)x;
       S.C[i] = ((uint64_t)((uint32_t)(x >> 32) - kmin) << bI) | (uint64_t)(g.M - 1 - (u - g.lead));
     }
     __syncthreads();
-    const uint64_t T = radix_threshold<kFinThreads>(S.C, (int)c, (uint32_t)g.k, 0, nb, S.hist,
-                                                    S.scratch, S.out);
-    for (uint32_t i = threadIdx.x; i < c; i += kFinThreads) {
+    const uint64_t T = radix_threshold<NT>(S.C, (int)c, (uint32_t)g.k, 0, nb, S.hist, S.scratch,
+                                           S.out);
+    for (uint32_t i = threadIdx.x; i < c; i += NT) {
       uint64_t x = S.C[i];
       if (x >= T) S.sel[atomicAdd(&S.nsel, 1u)] = g.lead + (g.M - 1 - (uint32_t)(x & imask));
     }
@@ -606,7 +593,7 @@ topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __res
     // The estimate missed: exact selection over the whole row in this CTA.
     bool nan = false;
     uint32_t mn = 0xFFFFFFFFu, mx = 0;
-    for (int64_t i = threadIdx.x; i < g.M; i += kFinThreads) {
+    for (int64_t i = threadIdx.x; i < g.M; i += NT) {
       uint32_t kk = load_key<F32>(scores, row * g.n_units + g.lead + i, nan);
       mn = min(mn, kk);
       mx = max(mx, kk);
@@ -622,15 +609,15 @@ topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __res
     while (pos > 0) {
       const int w = min(kDigit, pos);
       const int npos = pos - w;
-      for (int b = threadIdx.x; b < kBins; b += kFinThreads) S.hist[b] = 0;
+      for (int b = threadIdx.x; b < kBins; b += NT) S.hist[b] = 0;
       __syncthreads();
-      for (int64_t i = threadIdx.x; i < g.M; i += kFinThreads) {
+      for (int64_t i = threadIdx.x; i < g.M; i += NT) {
         uint32_t kk = load_key<F32>(scores, row * g.n_units + g.lead + i, nan);
         uint64_t x = ((uint64_t)(kk - kmin) << bI) | (uint64_t)(g.M - 1 - i);
         if ((x >> pos) == prefix) atomicAdd(&S.hist[(uint32_t)(x >> npos) & ((1u << w) - 1)], 1u);
       }
       __syncthreads();
-      pick_digit<kFinThreads>(S.hist, r, S.scratch, S.out);
+      pick_digit<NT>(S.hist, r, S.scratch, S.out);
       const uint32_t dd = S.out[0], ab = S.out[1], inb = S.hist[dd];
       __syncthreads();
       r -= ab;
@@ -639,7 +626,7 @@ topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __res
       if (inb == r) break;
     }
     const uint64_t T = prefix << pos;
-    for (int64_t i = threadIdx.x; i < g.M; i += kFinThreads) {
+    for (int64_t i = threadIdx.x; i < g.M; i += NT) {
       uint32_t kk = load_key<F32>(scores, row * g.n_units + g.lead + i, nan);
       uint64_t x = ((uint64_t)(kk - kmin) << bI) | (uint64_t)(g.M - 1 - i);
       if (x >= T) S.sel[atomicAdd(&S.nsel, 1u)] = (uint32_t)(g.lead + i);
@@ -647,9 +634,73 @@ topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __res
   }
   __syncthreads();
   const int nsel = (int)S.nsel;
-  sort_units<kFinThreads>(S.sel, nsel, bits_of((uint32_t)(g.n_units - 1)), S.hist,
-                          reinterpret_cast<uint32_t*>(S.C));
-  write_units<kFinThreads>(g, S.sel, nsel, idx_row, count + row);
+  sort_units<NT>(S.sel, nsel, bits_of((uint32_t)(g.n_units - 1)), S.hist,
+                 reinterpret_cast<uint32_t*>(S.C));
+  write_units<NT>(g, S.sel, nsel, idx_row, count_row);
+}
+
+template <bool F32>
+__global__ void __launch_bounds__(kFinThreads)
+topk_finish_kernel(const void* __restrict__ scores, Geo g, Ws ws, int32_t* __restrict__ idx,
+                   int64_t idx_stride, int32_t* __restrict__ count) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  FinSmem& S = *reinterpret_cast<FinSmem*>(smem_raw);
+  const int64_t row = blockIdx.x;
+  const RowState& st = ws.st[row];
+  int32_t* idx_row = idx + row * idx_stride;
+  if (st.nan) {
+    if (threadIdx.x == 0) count[row] = -1;
+    return;
+  }
+  if (threadIdx.x == 0) S.nsel = 0;
+  if (g.M <= g.k) {
+    for (int i = threadIdx.x; i < g.M; i += kFinThreads) S.sel[i] = g.lead + i;
+    __syncthreads();
+    write_units<kFinThreads>(g, S.sel, g.M, idx_row, count + row);
+    return;
+  }
+  const uint32_t c = st.ncand;
+  if (c >= (uint32_t)g.k && c <= (uint32_t)kCap) {
+    const uint64_t* cand = ws.cand + row * kCap;
+    for (uint32_t i = threadIdx.x; i < c; i += kFinThreads) S.C[i] = cand[i];
+  }
+  finish_row<F32, kFinThreads>(S, scores, g, row, c, idx_row, count + row);
+}
+
+// The fused scan + top-k's selection: one CTA per row gathers the units the scan
+// marked (PsCand hit masks) as its candidates, then finishes the row.
+constexpr int kMarkThreads = 1024;
+
+template <bool F32>
+__global__ void __launch_bounds__(kMarkThreads)
+topk_marked_kernel(const void* __restrict__ scores, Geo g, const uint32_t* __restrict__ hits,
+                   const uint32_t* __restrict__ cnan, int64_t n32, int32_t* __restrict__ idx,
+                   int64_t idx_stride, int32_t* __restrict__ count) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  FinSmem& S = *reinterpret_cast<FinSmem*>(smem_raw);
+  const int64_t row = blockIdx.x;
+  int32_t* idx_row = idx + row * idx_stride;
+  if (__ldg(cnan + row)) {
+    if (threadIdx.x == 0) count[row] = -1;
+    return;
+  }
+  if (threadIdx.x == 0) { S.nsel = 0; S.flag = 0; }
+  __syncthreads();
+  const float* frow = reinterpret_cast<const float*>(scores) + row * g.n_units;
+  const int32_t* irow = reinterpret_cast<const int32_t*>(scores) + row * g.n_units;
+  const uint32_t* hrow = hits + row * n32;
+  for (int64_t w = threadIdx.x; w < n32; w += kMarkThreads) {
+    uint32_t m = __ldg(hrow + w);
+    while (m) {
+      const uint32_t u = (uint32_t)(w * 32) + (uint32_t)(__ffs(m) - 1);
+      m &= m - 1;
+      const uint32_t key = F32 ? key_of_f32(__ldg(frow + u)) : key_of_i32(__ldg(irow + u));
+      const uint32_t p = atomicAdd(&S.flag, 1u);
+      if (p < (uint32_t)kCap) S.C[p] = ((uint64_t)key << 32) | u;
+    }
+  }
+  __syncthreads();
+  finish_row<F32, kMarkThreads>(S, scores, g, row, S.flag, idx_row, count + row);
 }
 
 // --------------------------------------------------------------------------------------
@@ -685,8 +736,6 @@ struct ClSmem {
   uint32_t pwh[(kClThreads / 32) * 256];  // per-warp radix histograms
 };
 
-// 4096 samples (2k for large k) keep the candidates near 3K at k = 512 and under
-// kCap up to k = 4096, while the estimate's serial radix stays short
 // 4096 samples (2k for large k) keep the candidates near 3K at k = 512 and within
 // the gather buffer up to k = 4096, while the estimate's serial radix stays short
 __host__ __device__ inline int cluster_sample_size(const Geo& g) {
@@ -694,12 +743,6 @@ __host__ __device__ inline int cluster_sample_size(const Geo& g) {
   return (int)imin64(g.M, imin64(s, kClBuf));
 }
 
-// max that propagates NaN (PTX max.NaN), so one compare screens four scores
-__device__ __forceinline__ float fmax_nan(float a, float b) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-  return r;
-}
 
 template <bool F32>
 __device__ __forceinline__ uint32_t key_at(const float* frow, const int32_t* irow, int64_t u,
@@ -717,8 +760,8 @@ __device__ __forceinline__ uint32_t key_at(const float* frow, const int32_t* iro
 // atomics.  Finds T with at least `need` of C[0..c) >= T, all C < 2^nb; exact
 // (exactly `need` values >= T, C unique) unless max_passes stops it first, in
 // which case T is the lower bound of the bucket holding the need-th value.
-template <int NT>
-__device__ uint64_t radix_select_pw(const uint64_t* C, int c, uint32_t need, int nb,
+template <int NT, typename KT>
+__device__ uint64_t radix_select_pw(const KT* C, int c, uint32_t need, int nb,
                                     int max_passes, uint32_t* pwh, uint32_t* out) {
   constexpr int NW = NT / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -734,18 +777,24 @@ __device__ uint64_t radix_select_pw(const uint64_t* C, int c, uint32_t need, int
     __syncwarp();
     for (int i = threadIdx.x; i < c; i += NT) {
       const uint64_t x = C[i];
-      if ((x >> pos) == prefix) atomicAdd(&mine[(uint32_t)(x >> npos) & mask], 1u);
+      if (pos >= 64 || (x >> pos) == prefix) atomicAdd(&mine[(uint32_t)(x >> npos) & mask], 1u);
+    }
+    __syncthreads();
+    // bin totals over the warps' tables, one bin per thread, into warp 0's table
+    for (int b = threadIdx.x; b < 256; b += NT) {
+      uint32_t v = 0;
+#pragma unroll 8
+      for (int ww = 0; ww < NW; ++ww) v += pwh[ww * 256 + b];
+      pwh[b] = v;
     }
     __syncthreads();
     if (warp == 0) {
-      // lane l owns bins 8l..8l+7 (summed over the warps); suffix scan over lanes
+      // lane l owns bins 8l..8l+7; suffix scan over lanes
       uint32_t h[8], tot = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        uint32_t v = 0;
-        for (int ww = 0; ww < NW; ++ww) v += pwh[ww * 256 + lane * 8 + i];
-        h[i] = v;
-        tot += v;
+        h[i] = pwh[lane * 8 + i];
+        tot += h[i];
       }
       uint32_t suf = tot;
 #pragma unroll
@@ -1195,6 +1244,29 @@ static int launch_cluster(const void* scores, int64_t rows, const Geo& g, int32_
   return check_launch("topk_cluster");
 }
 
+// The largest cluster size whose row-clusters are all resident in one wave (0:
+// no cluster configuration applies).
+template <bool F32>
+static int pick_cluster(int64_t rows, const Geo& g) {
+  if (!(g.M > g.k && g.M >= 4 * 16 && rows <= 65535)) return 0;
+  if (rows <= cluster_capacity<F32, 16>()) return 16;
+  if (rows <= cluster_capacity<F32, 8>()) return 8;
+  if (rows <= cluster_capacity<F32, 4>()) return 4;
+  if (cluster_capacity<F32, 2>() > 0) return 2;
+  return 0;
+}
+
+template <bool F32>
+static int launch_cluster_cs(int cs, const void* scores, int64_t rows, const Geo& g, int32_t* idx,
+                             int64_t idx_stride, int32_t* count, cudaStream_t st) {
+  switch (cs) {
+    case 16: return launch_cluster<F32, 16>(scores, rows, g, idx, idx_stride, count, st);
+    case 8: return launch_cluster<F32, 8>(scores, rows, g, idx, idx_stride, count, st);
+    case 4: return launch_cluster<F32, 4>(scores, rows, g, idx, idx_stride, count, st);
+    default: return launch_cluster<F32, 2>(scores, rows, g, idx, idx_stride, count, st);
+  }
+}
+
 template <bool F32>
 static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
                   int64_t idx_stride, int32_t* count, void* wsp, cudaStream_t st) {
@@ -1206,17 +1278,8 @@ static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
     note_launches(1);
     return check_launch("topk_small");
   }
-  if (g.M > g.k && g.M >= 4 * 16 && rows <= 65535) {
-    // the largest cluster whose row-clusters are all resident in one wave
-    if (rows <= cluster_capacity<F32, 16>())
-      return launch_cluster<F32, 16>(scores, rows, g, idx, idx_stride, count, st);
-    if (rows <= cluster_capacity<F32, 8>())
-      return launch_cluster<F32, 8>(scores, rows, g, idx, idx_stride, count, st);
-    if (rows <= cluster_capacity<F32, 4>())
-      return launch_cluster<F32, 4>(scores, rows, g, idx, idx_stride, count, st);
-    if (cluster_capacity<F32, 2>() > 0)
-      return launch_cluster<F32, 2>(scores, rows, g, idx, idx_stride, count, st);
-  }
+  if (const int cs = pick_cluster<F32>(rows, g))
+    return launch_cluster_cs<F32>(cs, scores, rows, g, idx, idx_stride, count, st);
   Ws ws = carve(wsp, rows);
   const size_t smem_s = (size_t)kSample * 8 + kBins * 4;
   auto samp = topk_sample_kernel<F32>;
@@ -1243,6 +1306,247 @@ int launch_topk(int score_type, const void* scores, int64_t rows, int64_t n_unit
   if (score_type == SD_SCORE_F32)
     return topk_t<true>(scores, rows, g, idx, idx_stride, count, ws, st);
   return topk_t<false>(scores, rows, g, idx, idx_stride, count, ws, st);
+}
+
+// =====================================================================================
+// Fused bit-plane scan + top-k (sd_score_topk).
+//
+// Filtering 32 MB of scores after the scan costs a full read per step.  Instead,
+// a short kernel first scores a sample of every row -- kSmpRuns runs of 32
+// consecutive tokens (one word of each planned plane), spread evenly over the
+// competing tokens, with the scan's folded weights -- and takes a threshold key
+// below the row's k-th score with high probability (the r-th largest sample key,
+// r from the same margin as the other estimates, widened because the 32 tokens of
+// a run are not independent: mu = k S / M, r = mu + 5 sqrt(8 mu) + 2).  The scan
+// then appends every competing token whose key reaches the threshold to the row's
+// candidate list (and still writes all scores), and the cluster top-k draws the
+// exact top k from that list.  A row whose list holds fewer than k entries,
+// overflows, or holds a NaN is selected again from its full score row, so the
+// result is always that of sd_score followed by sd_topk.
+// =====================================================================================
+constexpr int kSmpRuns = 256;                   // sampled runs of 32 tokens per row
+constexpr int kSmpSplit = 16;                   // CTAs per row
+constexpr int kSmpRunsCta = kSmpRuns / kSmpSplit;  // 16
+constexpr int kSmpPer = 8;                      // threads per run (adjacent lanes)
+constexpr int kSmpThreads = kSmpRunsCta * kSmpPer;  // 128
+constexpr int kSmpTok = kSmpRuns * 32;          // sampled tokens per row
+constexpr int kFusedCap = kCap;                 // candidates the selecting CTA holds
+constexpr int64_t kFusedMinM = 65536;           // shorter rows: scan, then sd_topk
+
+struct SmpSmem {
+  PsRow row;
+  uint32_t wsum[kSmpThreads / 32];
+  uint32_t last;
+};
+
+// The largest key T with at least r of the calling CTA's keys (K per thread, in
+// registers) >= T: a bitwise search, one CTA-wide count per bit.  (r is small and
+// the keys of a row's scores crowd a few high-order digits, so this beats a radix
+// histogram with its serialised shared-memory atomics.)
+template <int NT, int K>
+__device__ uint32_t kth_largest_bits(const uint32_t (&key)[K], uint32_t r, uint32_t* wsum) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < K; ++i) c += key[i] >= cand;
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    if (lane == 0) wsum[warp] = c;
+    __syncthreads();
+    uint32_t tot = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) tot += wsum[w];
+    __syncthreads();
+    if (tot >= r) T = cand;
+  }
+  return T;
+}
+
+// Sample keys of a row's runs [32 b, 32 b + 32), b = blockIdx.x: keys[row][...] in
+// the workspace; the row's last CTA to finish (ticket) selects the threshold.
+template <int G>
+__global__ void __launch_bounds__(kSmpThreads)
+plane_sample_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
+                    const uint8_t* __restrict__ plan, const uint16_t* __restrict__ q, int Hq,
+                    int Hkv, int64_t ncap, int64_t lead, int64_t tail, int r,
+                    uint32_t* __restrict__ skeys, uint32_t* __restrict__ ticket,
+                    uint32_t* __restrict__ thr, uint32_t* __restrict__ cnan) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SmpSmem& S = *reinterpret_cast<SmpSmem*>(smem_raw);
+  const int t = threadIdx.x;
+  const int row = blockIdx.y;
+  ps_build_row<G>(S.row, t, q, plan, row / Hkv, row % Hkv, Hq, (int64_t)row,
+                  [] { __syncthreads(); });
+  const int run = blockIdx.x * kSmpRunsCta + t / kSmpPer, eg = t % kSmpPer;
+  // the run's word, evenly spaced over the words that hold competing tokens
+  const int64_t w0 = lead / 32, w1 = (tail + 31) / 32;
+  const int64_t w = w0 + ((2 * (int64_t)run + 1) * (w1 - w0)) / (2 * kSmpRuns);
+  const uint32_t wstride = (uint32_t)(ncap / 32), sstride = (uint32_t)(ncap / 64);
+  const uint32_t* prow = planes + (int64_t)row * kD * 4 * wstride + w;
+  const uint16_t* srow = scales + (int64_t)row * kD * sstride + (w >> 1);
+  const int nact = S.row.nact, nch = S.row.nch;
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+  float cp = 0.0f;
+  // this thread's planes e = eg + 8u and slots sl = eg + 8u: loads issued 8 planes
+  // and 8 slots at a time, then the bits and the block constant's terms
+  const int nb = max(nact, nch);
+  for (int e0 = eg; e0 < nb; e0 += 8 * kSmpPer) {
+    uint32_t wv[8];
+    float sv[8], cv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * kSmpPer;
+      if (e < nact) {
+        const int ent = S.row.act[e];
+        wv[u] = __ldg(prow + (int64_t)ent * wstride);
+        sv[u] = __half2float(__ushort_as_half(__ldg(srow + (int64_t)(ent >> 2) * sstride)));
+      }
+      if (e < nch)
+        cv[u] = __half2float(__ushort_as_half(__ldg(srow + (int64_t)S.row.chan[e] * sstride)));
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = e0 + u * kSmpPer;
+      if (e < nact) ps_bits(acc, wv[u], __fmul_rn(S.row.qp[e], sv[u]));
+      if (e < nch) cp = __fadd_rn(cp, __fmul_rn(S.row.qo[e], cv[u]));
+    }
+  }
+  // the run's eight partial sums meet by shuffles: each round halves what a lane
+  // keeps; lane eg ends with the totals of 4 tokens
+  float h16[16], h8[8], h4[4];
+  {
+    const bool b = eg & 1;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float keep = b ? acc[16 + i] : acc[i], give = b ? acc[i] : acc[16 + i];
+      h16[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, 1);
+    }
+  }
+  {
+    const bool b = eg & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float keep = b ? h16[8 + i] : h16[i], give = b ? h16[i] : h16[8 + i];
+      h8[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, 2);
+    }
+  }
+  {
+    const bool b = eg & 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float keep = b ? h8[4 + i] : h8[i], give = b ? h8[i] : h8[4 + i];
+      h4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, 4);
+    }
+  }
+  cp += __shfl_xor_sync(0xFFFFFFFFu, cp, 1);
+  cp += __shfl_xor_sync(0xFFFFFFFFu, cp, 2);
+  cp += __shfl_xor_sync(0xFFFFFFFFu, cp, 4);
+  const int tk0 = ((eg & 1) ? 16 : 0) + ((eg & 2) ? 8 : 0) + ((eg & 4) ? 4 : 0);
+  uint32_t* krow = skeys + (int64_t)row * kSmpTok;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float v = h4[i] + cp;
+    const int64_t tok = w * 32 + tk0 + i;
+    const bool in = tok >= lead && tok < tail && v == v;  // competing, not NaN
+    krow[run * 32 + tk0 + i] = in ? key_of_f32(v) : 0u;
+  }
+  // the row's last CTA selects
+  __threadfence();
+  __syncthreads();
+  if (t == 0) S.last = atomicAdd(ticket + row, 1u) == kSmpSplit - 1;
+  __syncthreads();
+  if (!S.last) return;
+  __threadfence();
+  constexpr int KPT = kSmpTok / kSmpThreads;  // keys per thread
+  uint32_t key[KPT];
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) key[i] = __ldcg(krow + i * kSmpThreads + t);
+  const uint32_t T = kth_largest_bits<kSmpThreads, KPT>(key, (uint32_t)r, S.wsum);
+  if (t == 0) {
+    thr[row] = (uint32_t)T;
+    cnan[row] = 0u;
+    ticket[row] = 0u;  // ready for the next call
+  }
+}
+
+static int fused_rank(int64_t k, int64_t S, int64_t M) {
+  const double mu = (double)k * (double)S / (double)M;
+  const double r = std::ceil(mu + 5.0 * std::sqrt(8.0 * mu) + 2.0);
+  return (int)(r < (double)S ? r : (double)S);
+}
+
+size_t score_topk_workspace_bytes(int64_t rows, int64_t n, const sd_select& sel) {
+  return align256(topk_workspace_bytes(rows, n, sel)) + align256(sizeof(uint32_t) * 3 * rows) +
+         align256(sizeof(uint32_t) * rows * kSmpTok) + align256(sizeof(uint32_t) * rows * (n / 32));
+}
+
+template <int G>
+static int sample_t(const Dims& s, const uint32_t* planes, const uint16_t* scales,
+                    const uint8_t* plan, const uint16_t* q, const Geo& g, int r, uint32_t* skeys,
+                    uint32_t* ticket, uint32_t* thr, uint32_t* cnan, cudaStream_t st) {
+  auto kern = plane_sample_kernel<G>;
+  if (int rc = set_smem_limit((const void*)kern, sizeof(SmpSmem), "plane sample: smem attribute"))
+    return rc;
+  const int64_t rows = (int64_t)s.B * s.Hkv;
+  if (cudaMemsetAsync(ticket, 0, sizeof(uint32_t) * rows, st) != cudaSuccess)
+    return check_launch("plane sample: ticket clear");
+  kern<<<dim3(kSmpSplit, (unsigned)rows), kSmpThreads, sizeof(SmpSmem), st>>>(
+      planes, scales, plan, q, s.Hq, s.Hkv, s.ncap, (int64_t)g.lead, (int64_t)g.tail, r, skeys,
+      ticket, thr, cnan);
+  note_launches(1);
+  return check_launch("plane sample");
+}
+
+int launch_score_topk(const Dims& s, const uint32_t* planes, const uint16_t* scales,
+                      const uint8_t* plan, const uint16_t* q, const sd_select& sel, float* scores,
+                      int32_t* idx, int64_t idx_stride, int32_t* count, void* ws,
+                      cudaStream_t st) {
+  const int64_t rows = (int64_t)s.B * s.Hkv;
+  Geo g = make_geo(s.n, s.n, sel);
+  if (g.M > 0) {
+    g.r_sample = sample_rank(g.k, sample_size(g), g.M);
+    g.r_cluster = sample_rank(g.k, cluster_sample_size(g), g.M);
+  }
+  // fused where the threshold keeps the expected candidates within 3/5 of what the
+  // selecting CTA holds (the count's spread is about sqrt of it)
+  int r = 0;
+  bool fused = false;
+  if (sel.block == 1 && g.M >= kFusedMinM && g.M > g.k && planes_aligned(s, planes, scales)) {
+    r = fused_rank(g.k, kSmpTok, g.M);
+    fused = (int64_t)r * (g.M / kSmpTok) <= kFusedCap * 3 / 5;
+  }
+  if (!fused) {  // scan, then the standalone top-k
+    if (int rc = launch_score_planes(s, planes, scales, plan, q, scores, st)) return rc;
+    return topk_t<true>(scores, rows, g, idx, idx_stride, count, ws, st);
+  }
+  uint8_t* p = static_cast<uint8_t*>(ws) + align256(topk_workspace_bytes(rows, s.n, sel));
+  uint32_t* thr = reinterpret_cast<uint32_t*>(p);
+  uint32_t* cnan = thr + rows;
+  uint32_t* ticket = cnan + rows;
+  p += align256(sizeof(uint32_t) * 3 * rows);
+  uint32_t* skeys = reinterpret_cast<uint32_t*>(p);
+  uint32_t* hits = reinterpret_cast<uint32_t*>(p + align256(sizeof(uint32_t) * rows * kSmpTok));
+  int rc;
+  switch (s.G) {
+    case 1: rc = sample_t<1>(s, planes, scales, plan, q, g, r, skeys, ticket, thr, cnan, st); break;
+    case 2: rc = sample_t<2>(s, planes, scales, plan, q, g, r, skeys, ticket, thr, cnan, st); break;
+    case 4: rc = sample_t<4>(s, planes, scales, plan, q, g, r, skeys, ticket, thr, cnan, st); break;
+    default: rc = sample_t<8>(s, planes, scales, plan, q, g, r, skeys, ticket, thr, cnan, st); break;
+  }
+  if (rc) return rc;
+  const PsCand cd{thr, hits, cnan, s.n / 32, (int64_t)g.lead, (int64_t)g.tail};
+  if ((rc = launch_score_planes(s, planes, scales, plan, q, scores, st, &cd))) return rc;
+  auto sel_k = topk_marked_kernel<true>;
+  if ((rc = set_smem_limit((const void*)sel_k, sizeof(FinSmem), "topk marked: smem attribute")))
+    return rc;
+  sel_k<<<(unsigned)rows, kMarkThreads, sizeof(FinSmem), st>>>(scores, g, hits, cnan, s.n / 32,
+                                                                idx, idx_stride, count);
+  note_launches(1);
+  return check_launch("topk marked");
 }
 
 }  // namespace sd

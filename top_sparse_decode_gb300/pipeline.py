@@ -7,7 +7,9 @@ libsd's kernels.  A step for one layer, all heads and the whole batch is
         ->  sd_gather_attend
 
 and the per-stage split T = T_qmap + T_scan + T_topk + T_att follows
-HashAttention: Semantic Sparsity for Faster Inference, 2.5.
+HashAttention: Semantic Sparsity for Faster Inference, 2.5.  With
+StepConfig.fused, bit planes run the scan and the top-k as one call
+(sd_score_topk, same results).
 """
 from __future__ import annotations
 
@@ -19,8 +21,8 @@ import torch
 
 from . import (SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_SCORE_F32,
                SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
-               sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_score, sd_topk,
-               sd_topk_workspace_size)
+               sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_score,
+               sd_score_topk, sd_score_topk_workspace_size, sd_topk, sd_topk_workspace_size)
 
 KIND_NAMES = {SD_IDX_SIG: "hamming", SD_IDX_PLANES: "planes", SD_IDX_MINMAX: "quest"}
 
@@ -38,6 +40,7 @@ class StepConfig:
     local: int = 0            # forced trailing units
     plan_mode: int = SD_PLAN_WATERFILL
     budget: int = 56          # bits per token per KV head (water-filling) or r (fixed)
+    fused: bool = False       # bit planes: scan and top-k in one call (sd_score_topk)
 
     @property
     def block(self) -> int:
@@ -99,6 +102,10 @@ class DecodeStep:
         self.count = torch.empty((self.rows,), dtype=torch.int32, device=dev)
         tws = sd_topk_workspace_size(self.rows, c.n_units, self.sel)
         self.topk_ws = torch.empty(tws, dtype=torch.uint8, device=dev) if tws else None
+        self.fused = c.fused and c.kind == SD_IDX_PLANES
+        if self.fused:
+            fws = sd_score_topk_workspace_size(self.shape, self.sel)
+            self.fused_ws = torch.empty(max(fws, 256), dtype=torch.uint8, device=dev)
         aws = sd_gather_attend_workspace_size(self.shape, c.max_count)
         self.att_ws = torch.empty(max(aws, 256), dtype=torch.uint8, device=dev)
         self.out = torch.empty((c.B, c.Hq, c.d), dtype=torch.float32, device=dev)
@@ -128,14 +135,30 @@ class DecodeStep:
         sd_topk(st, self.scores, self.rows, c.n_units, c.n, self.sel, self.idx, c.max_count,
                 self.count, self.topk_ws, stream)
 
+    def stage_score_topk(self, q, stream=None):
+        """Bit planes: the scan and the top-k in one call (same results as
+        stage_score followed by stage_topk)."""
+        ix = self.index
+        sd_score_topk(self.shape, ix["planes"], ix["scales"], q, self.plan, self.sel,
+                      self.scores, self.idx, self.cfg.max_count, self.count, self.fused_ws,
+                      stream)
+
     def stage_attend(self, q, stream=None):
         c = self.cfg
         sd_gather_attend(self.shape, q, self.K, self.V, self.idx, c.max_count, self.count,
                          c.max_count, self.scale, self.out, self.lse, self.att_ws, stream)
 
+    def stages(self):
+        """(name, fn(q, stream)) of the step's stages in call order."""
+        if self.fused:
+            return [("plan", self.stage_prep), ("scan_topk", self.stage_score_topk),
+                    ("gather_attend", self.stage_attend)]
+        first = "plan" if self.cfg.kind == SD_IDX_PLANES else "prep"
+        return [(first, self.stage_prep), ("scan", self.stage_score),
+                ("topk", lambda q, stream=None: self.stage_topk(stream)),
+                ("gather_attend", self.stage_attend)]
+
     def run(self, q, stream=None):
-        self.stage_prep(q, stream)
-        self.stage_score(q, stream)
-        self.stage_topk(stream)
-        self.stage_attend(q, stream)
+        for _, fn in self.stages():
+            fn(q, stream)
         return self.out
