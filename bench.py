@@ -368,6 +368,8 @@ def main():
     st_att = statistics.mean(timed_steps(torch, lambda: step.stage_attend(q), K_st, 3, flush))
     st_fused = (statistics.mean(timed_steps(torch, lambda: step.stage_score_topk(q), K_st, 3,
                                             flush)) if step.fused else None)
+    st_plan_scan = statistics.mean(timed_steps(torch, lambda: step.stage_plan_score(q), K_st, 3,
+                                               flush))
     eager = statistics.mean(timed_steps(torch, lambda: step.run(q), K_st, 3, flush))
 
     # marginal stage costs inside the step: cumulative prefixes, L2 flushed before each
@@ -449,11 +451,12 @@ def main():
         def offload_only():
             sd.sd_offload_gather(shp, hp, hs, step.plan, dpl, dsc)
 
-        def offload_step():
+        def offload_step():  # the plan must exist before the gather: plan, gather, scan
             sto.stage_prep(q)
             sd.sd_offload_gather(shp, hp, hs, sto.plan, dpl, dsc)
-            for _, fn in sto.stages()[1:]:
-                fn(q)
+            sto.stage_score(q)
+            sto.stage_topk()
+            sto.stage_attend(q)
 
         to = statistics.mean(timed_steps(torch, offload_only, K_st, 3, flush))
         tos = statistics.mean(timed_steps(torch, offload_step, K_st, 3, flush))
@@ -483,6 +486,7 @@ def main():
         "us_per_step": t_step_max * 1e3,
         "stages_us": {"plan": st_prep * 1e3, "scan": st_score * 1e3, "topk": st_topk * 1e3,
                       "scan_topk": None if st_fused is None else st_fused * 1e3,
+                      "plan_scan": st_plan_scan * 1e3,
                       "gather_attend": st_att * 1e3, "step_eager": eager * 1e3},
         "stages_in_step_us": marginal,
         # the scan is bound by one bit test and one predicated FP32 add per planned

@@ -170,6 +170,17 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
             int32_t* count, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * sd_plan_score -- sd_plan then sd_score(SD_IDX_PLANES) in one launch (Fathom's
+ * per-query plan and bit-plane scan): the scan computes each row's plan from q
+ * and sigma2 itself, with sd_plan's arithmetic, and writes exactly the scores the
+ * two calls would.  Arguments as sd_plan (q, sigma2, mode, budget; plan may be
+ * NULL, else it receives the plan) and sd_score (planes, scales, scores).
+ */
+int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales, const void* q,
+                  const float* sigma2, int mode, int budget, uint8_t* plan, float* scores,
+                  void* stream);
+
+/*
  * sd_score_topk -- sd_score(SD_IDX_PLANES) then sd_topk(SD_SCORE_F32) on those
  * scores, in one call (Fathom's bit-plane scan feeding HashAttention 2.1's TOPK):
  * writes exactly the scores, idx and count the two calls would.

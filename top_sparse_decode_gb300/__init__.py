@@ -28,7 +28,7 @@ __all__ = [
     "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
     "sd_gather_attend_noalloc", "sd_offload_gather",
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
-    "sd_score_topk_workspace_size", "sd_score_topk",
+    "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score",
 ]
 
 
@@ -135,6 +135,13 @@ def sd_topk(score_type: int, scores, rows: int, n_units: int, n_tokens: int, sel
     _check(lib().sd_topk(score_type, _ptr(scores), rows, n_units, n_tokens, ctypes.byref(sel),
                          _ptr(idx), idx_stride, _ptr(count), _ptr(workspace), ws_bytes,
                          _stream(stream)), "sd_topk")
+
+
+def sd_plan_score(shape: SdShape, planes, scales, q, sigma2, mode: int, budget: int, plan,
+                  scores, stream=None) -> None:
+    _check(lib().sd_plan_score(ctypes.byref(shape), _ptr(planes), _ptr(scales), _ptr(q),
+                               _ptr(sigma2), mode, budget, _ptr(plan), _ptr(scores),
+                               _stream(stream)), "sd_plan_score")
 
 
 def sd_score_topk_workspace_size(shape: SdShape, sel: SdSelect) -> int:

@@ -11,6 +11,7 @@
 #include <utility>
 
 #include "sd_internal.cuh"
+#include "sd_planes.cuh"
 
 namespace sd {
 
@@ -209,6 +210,27 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
     return fail(SD_ERR_WORKSPACE, "sd_topk: workspace %zu < %zu bytes", ws_bytes, need);
   return launch_topk(score_type, scores, rows, n_units, n_tokens, *sel, idx, idx_stride, count,
                      workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales, const void* q,
+                  const float* sigma2, int mode, int budget, uint8_t* plan, float* scores,
+                  void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s, true);
+  if (rc) return rc;
+  if (!planes || !scales || !q || !sigma2 || !scores)
+    return fail(SD_ERR_INVALID_ARG, "sd_plan_score: NULL input");
+  if (!aligned16(planes) || !aligned16(scores))
+    return fail(SD_ERR_INVALID_ARG, "sd_plan_score: planes and scores must be 16-byte aligned");
+  if (mode != SD_PLAN_WATERFILL && mode != SD_PLAN_FIXED && mode != SD_PLAN_FULL)
+    return fail(SD_ERR_INVALID_ARG, "sd_plan_score: unknown plan mode %d", mode);
+  if (mode == SD_PLAN_WATERFILL && (budget < 0 || budget > 4 * kD))
+    return fail(SD_ERR_INVALID_ARG, "sd_plan_score: budget %d outside [0, %d]", budget, 4 * kD);
+  if (mode == SD_PLAN_FIXED && (budget < 0 || budget > kD))
+    return fail(SD_ERR_INVALID_ARG, "sd_plan_score: fixed width %d outside [0, %d]", budget, kD);
+  const PsPlanIn pl{sigma2, mode, budget, plan};
+  return launch_score_planes(s, (const uint32_t*)planes, (const uint16_t*)scales, nullptr,
+                             (const uint16_t*)q, scores, (cudaStream_t)stream, nullptr, &pl);
 }
 
 size_t sd_score_topk_workspace_size(const sd_shape* shape, const sd_select* sel) {

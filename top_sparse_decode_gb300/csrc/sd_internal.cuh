@@ -9,7 +9,8 @@
 
 namespace sd {
 
-struct PsCand;  // sd_planes.cuh
+struct PsCand;    // sd_planes.cuh
+struct PsPlanIn;  // sd_planes.cuh
 
 constexpr int kD = 128;          // head dimension supported by this build
 constexpr int kMaxTopK = 4096;   // largest retrieval budget of sd_topk
@@ -68,11 +69,12 @@ int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode,
                 uint8_t* plan, cudaStream_t st);
 int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsig,
                          int32_t* scores, cudaStream_t st);
-// (cand: the fused scan + top-k's candidate list, or null)
+// (cand: the fused scan + top-k's candidate marks, or null; plan_in: compute the
+// read plan in the scan instead of reading `plan`, or null)
 bool planes_aligned(const Dims& s, const void* planes, const void* scales);
 int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
                         const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st,
-                        const PsCand* cand = nullptr);
+                        const PsCand* cand = nullptr, const PsPlanIn* plan_in = nullptr);
 int launch_score_quest(const Dims& s, const uint16_t* summ, const uint16_t* q, float* scores,
                        cudaStream_t st);
 size_t topk_workspace_bytes(int64_t rows, int64_t n_units, const sd_select& sel);

@@ -28,14 +28,112 @@ struct PsRow {
   int nact, nch;
 };
 
+// The read plan of one row computed by a group of kD threads (thread t: channel
+// j = t and its pairs (j, 0..3)), with the same arithmetic and tie order as
+// plan_kernel (sd_plan.cu): the budget largest pairs w_j * 4^-b, ties to the
+// lower 4j + b (water-filling), the budget channels of largest sigma2 (fixed), or
+// 4 bits everywhere (full).  Returns channel t's bits.  sums: 2 * (kD / 32) words
+// of shared memory; bar() synchronises the group (threads t >= kD hold no keys).
+template <int G, class Bar>
+__device__ __forceinline__ int ps_plan_row(int t, const uint16_t* __restrict__ q,
+                                           const float* __restrict__ sigma2, int b, int h,
+                                           int Hq, int mode, int budget, int* sums, Bar bar) {
+  constexpr int NW = kD / 32;
+  const int lane = t & 31, warp = t >> 5;
+  if (mode == SD_PLAN_FULL) return 4;
+  const int nkeys = (mode == SD_PLAN_FIXED ? 1 : 4) * kD;
+  if (budget >= nkeys) return 4;
+  if (budget <= 0) return 0;
+  const int npairs = t >= kD ? 0 : (mode == SD_PLAN_FIXED ? 1 : 4);  // keys of this thread
+  if (t >= kD) t = 0;  // (loads in bounds; its keys are not counted)
+  uint32_t key[4] = {0u, 0u, 0u, 0u};
+  if (mode == SD_PLAN_FIXED) {
+    key[0] = key_of_f32(sigma2[(int64_t)h * kD + t]);
+  } else {
+    float acc = 0.0f;  // gains in fp32, group sum in ascending g, no fused multiply-add
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float x = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + t]);
+      acc = __fadd_rn(acc, __fmul_rn(x, x));
+    }
+    const float w = __fmul_rn(acc, sigma2[(int64_t)h * kD + t]);
+    const float scale4[4] = {1.0f, 0.25f, 0.0625f, 0.015625f};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) key[p] = key_of_f32(__fmul_rn(w, scale4[p]));
+  }
+  // group-wide count of keys satisfying pred, through two alternating tables
+  int parity = 0;
+  auto count = [&](auto pred) {
+    int c = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) c += p < npairs && pred(key[p]);
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    int* tab = sums + parity * NW;
+    parity ^= 1;
+    if (lane == 0 && warp < NW) tab[warp] = c;
+    bar();
+    int tot = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot += tab[w];
+    return tot;
+  };
+  // T: the largest key value with at least `budget` keys >= it
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    if (count([&](uint32_t k) { return k >= cand; }) >= budget) T = cand;
+  }
+  const int above = count([&](uint32_t k) { return k > T; });
+  // rank of each key equal to T among the equal keys, in pair order 4j + p
+  int eq = 0;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) eq += p < npairs && key[p] == T;
+  int incl = eq;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int* tab = sums + parity * NW;
+  if (lane == 31 && warp < NW) tab[warp] = incl;
+  bar();
+  int before = incl - eq;
+  for (int w = 0; w < warp && w < NW; ++w) before += tab[w];
+  int taken = 0;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    if (p >= npairs) break;
+    const bool e = key[p] == T;
+    if (key[p] > T || (e && before < budget - above)) ++taken;
+    before += e;
+  }
+  return mode == SD_PLAN_FIXED ? (taken ? 4 : 0) : taken;
+}
+
 // Builds R for row bh = b * Hkv + h.  Every thread of the calling group runs it
 // and `bar()` synchronises exactly that group; threads t < kD (t = the thread's
 // index within the group) do the per-channel work, warp t / 32 == 0 the scan.
+// With pl.sigma2 set, the row's plan is computed here (ps_plan_row) instead of
+// read from `plan`, and written to pl.out when pl.write.
+struct PsPlanIn {
+  const float* sigma2;
+  int mode, budget;
+  uint8_t* out;
+};
+
 template <int G, class Bar>
 __device__ __noinline__ void ps_build_row(PsRow& R, int t, const uint16_t* __restrict__ q,
                                           const uint8_t* __restrict__ plan, int b, int h, int Hq,
-                                          int64_t bh, Bar bar) {
+                                          int64_t bh, Bar bar, const PsPlanIn& pl = PsPlanIn{},
+                                          bool write_plan = false) {
   const int lane = t & 31;
+  int tb = 0;
+  if (pl.sigma2) {  // every thread of the group takes part in the plan's counts
+    tb = ps_plan_row<G>(t, q, pl.sigma2, b, h, Hq, pl.mode, pl.budget,
+                        reinterpret_cast<int*>(R.slot_of), bar);
+    bar();  // slot_of served as the plan's scratch
+    if (write_plan && t < kD && pl.out) pl.out[bh * kD + t] = (uint8_t)tb;
+  }
   if (t < kD) {
     const int j = t;
     float a = 0.0f;
@@ -43,7 +141,7 @@ __device__ __noinline__ void ps_build_row(PsRow& R, int t, const uint16_t* __res
     for (int g = 0; g < G; ++g)
       a = __fadd_rn(a, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]));
     R.qt[j] = a;
-    R.tb[j] = min((int)plan[bh * kD + j], 4);  // a plan holds 0..4 bits per channel
+    R.tb[j] = pl.sigma2 ? tb : min((int)plan[bh * kD + j], 4);  // 0..4 bits per channel
   }
   bar();
   if ((t >> 5) == 0) {  // active entries and channel slots, j ascending

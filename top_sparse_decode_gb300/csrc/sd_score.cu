@@ -340,7 +340,7 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
                                         const uint8_t* __restrict__ plan,
                                         const uint16_t* __restrict__ q, int Hq, int Hkv, int64_t n,
                                         int64_t ncap, int upr, int64_t total_units,
-                                        const PsCand& cd) {
+                                        const PsCand& cd, const PsPlanIn& pl) {
   const int ht = threadIdx.x - kPsCompute, hw = ht >> 5, lane = threadIdx.x & 31;
   const uint32_t wstride = (uint32_t)(ncap / 32), sstride = (uint32_t)(ncap / 64);
   // this CTA's units, walked as (row bh, unit ur) without dividing; rows <= 65535
@@ -368,8 +368,9 @@ __device__ __forceinline__ void ps_help(PsSmem& S, const uint32_t* __restrict__ 
       }
       nb_sync(kBarHelp, kPsHelpers);  // every helper is done with the old tables
       cur_bh = bh;
+      // (the CTA whose range holds the row's first unit writes a computed plan)
       ps_build_row<G>(S.row, ht, q, plan, bh / Hkv, bh % Hkv, Hq, (int64_t)bh,
-                      [] { nb_sync(kBarHelp, kPsHelpers); });
+                      [] { nb_sync(kBarHelp, kPsHelpers); }, pl, ur == 0);
       if (CAND) row_thr = __ldg(cd.thr + bh);
     }
     const int nact = S.row.nact, nch = S.row.nch;
@@ -473,13 +474,13 @@ __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm)
 score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
                     const uint8_t* __restrict__ plan, const uint16_t* __restrict__ q, int Hq,
                     int Hkv, int64_t n, int64_t ncap, int upr, int64_t total_units,
-                    float* __restrict__ scores, PsCand cd) {
+                    float* __restrict__ scores, PsCand cd, PsPlanIn pl) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PsSmem& S = *reinterpret_cast<PsSmem*>(smem_raw);
   if (threadIdx.x < kPsCompute)
     ps_compute<CAND>(S, scores, n, cd);
   else
-    ps_help<G, A16, CAND>(S, planes, scales, plan, q, Hq, Hkv, n, ncap, upr, total_units, cd);
+    ps_help<G, A16, CAND>(S, planes, scales, plan, q, Hq, Hkv, n, ncap, upr, total_units, cd, pl);
 }
 
 static int sm_count() {
@@ -498,7 +499,7 @@ static int sm_count() {
 template <int G, bool A16, bool CAND>
 static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scales,
                     const uint8_t* plan, const uint16_t* q, float* scores, const PsCand& cd,
-                    cudaStream_t st) {
+                    const PsPlanIn& pl, cudaStream_t st) {
   auto kern = score_planes_kernel<G, A16, CAND>;
   if (int rc = set_smem_limit((const void*)kern, sizeof(PsSmem), "score_planes: smem attribute"))
     return rc;
@@ -506,7 +507,7 @@ static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scale
   const int64_t total = (int64_t)upr * s.B * s.Hkv;
   const int64_t grid = imin64(total, (int64_t)sm_count() * kPsCtasPerSm);
   kern<<<(unsigned)grid, kPsThreads, sizeof(PsSmem), st>>>(planes, scales, plan, q, s.Hq, s.Hkv,
-                                                          s.n, s.ncap, upr, total, scores, cd);
+                                                          s.n, s.ncap, upr, total, scores, cd, pl);
   note_launches(1);
   return check_launch("score_planes");
 }
@@ -517,24 +518,25 @@ bool planes_aligned(const Dims& s, const void* planes, const void* scales) {
 
 int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
                         const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st,
-                        const PsCand* cand) {
+                        const PsCand* cand, const PsPlanIn* plan_in) {
   const bool a16 = planes_aligned(s, planes, scales);
+  const PsPlanIn pl = plan_in ? *plan_in : PsPlanIn{};
   if (cand) {  // the fused scan + top-k path (16-byte aligned layouts only)
     if (!a16) return fail(SD_ERR_INVALID_ARG, "score_planes: candidates need n_cap %% 512 == 0 "
                                               "and 16-byte aligned planes and scales");
     switch (s.G) {
-      case 1: return planes_t<1, true, true>(s, planes, scales, plan, q, scores, *cand, st);
-      case 2: return planes_t<2, true, true>(s, planes, scales, plan, q, scores, *cand, st);
-      case 4: return planes_t<4, true, true>(s, planes, scales, plan, q, scores, *cand, st);
-      default: return planes_t<8, true, true>(s, planes, scales, plan, q, scores, *cand, st);
+      case 1: return planes_t<1, true, true>(s, planes, scales, plan, q, scores, *cand, pl, st);
+      case 2: return planes_t<2, true, true>(s, planes, scales, plan, q, scores, *cand, pl, st);
+      case 4: return planes_t<4, true, true>(s, planes, scales, plan, q, scores, *cand, pl, st);
+      default: return planes_t<8, true, true>(s, planes, scales, plan, q, scores, *cand, pl, st);
     }
   }
   const PsCand none{};
   switch (s.G) {
-    case 1: return a16 ? planes_t<1, true, false>(s, planes, scales, plan, q, scores, none, st) : planes_t<1, false, false>(s, planes, scales, plan, q, scores, none, st);
-    case 2: return a16 ? planes_t<2, true, false>(s, planes, scales, plan, q, scores, none, st) : planes_t<2, false, false>(s, planes, scales, plan, q, scores, none, st);
-    case 4: return a16 ? planes_t<4, true, false>(s, planes, scales, plan, q, scores, none, st) : planes_t<4, false, false>(s, planes, scales, plan, q, scores, none, st);
-    default: return a16 ? planes_t<8, true, false>(s, planes, scales, plan, q, scores, none, st) : planes_t<8, false, false>(s, planes, scales, plan, q, scores, none, st);
+    case 1: return a16 ? planes_t<1, true, false>(s, planes, scales, plan, q, scores, none, pl, st) : planes_t<1, false, false>(s, planes, scales, plan, q, scores, none, pl, st);
+    case 2: return a16 ? planes_t<2, true, false>(s, planes, scales, plan, q, scores, none, pl, st) : planes_t<2, false, false>(s, planes, scales, plan, q, scores, none, pl, st);
+    case 4: return a16 ? planes_t<4, true, false>(s, planes, scales, plan, q, scores, none, pl, st) : planes_t<4, false, false>(s, planes, scales, plan, q, scores, none, pl, st);
+    default: return a16 ? planes_t<8, true, false>(s, planes, scales, plan, q, scores, none, pl, st) : planes_t<8, false, false>(s, planes, scales, plan, q, scores, none, pl, st);
   }
 }
 

@@ -7,9 +7,10 @@ libsd's kernels.  A step for one layer, all heads and the whole batch is
         ->  sd_gather_attend
 
 and the per-stage split T = T_qmap + T_scan + T_topk + T_att follows
-HashAttention: Semantic Sparsity for Faster Inference, 2.5.  With
-StepConfig.fused, bit planes run the scan and the top-k as one call
-(sd_score_topk, same results).
+HashAttention: Semantic Sparsity for Faster Inference, 2.5.  For bit planes the
+read plan is computed inside the scan (sd_plan_score, same results) unless
+StepConfig.plan_in_scan is False; with StepConfig.fused the scan and the top-k
+run as one call instead (sd_score_topk, same results).
 """
 from __future__ import annotations
 
@@ -21,8 +22,9 @@ import torch
 
 from . import (SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_SCORE_F32,
                SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
-               sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_score,
-               sd_score_topk, sd_score_topk_workspace_size, sd_topk, sd_topk_workspace_size)
+               sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_plan_score,
+               sd_score, sd_score_topk, sd_score_topk_workspace_size, sd_topk,
+               sd_topk_workspace_size)
 
 KIND_NAMES = {SD_IDX_SIG: "hamming", SD_IDX_PLANES: "planes", SD_IDX_MINMAX: "quest"}
 
@@ -41,6 +43,7 @@ class StepConfig:
     plan_mode: int = SD_PLAN_WATERFILL
     budget: int = 56          # bits per token per KV head (water-filling) or r (fixed)
     fused: bool = False       # bit planes: scan and top-k in one call (sd_score_topk)
+    plan_in_scan: bool = True  # bit planes: the plan computed by the scan (sd_plan_score)
 
     @property
     def block(self) -> int:
@@ -135,6 +138,13 @@ class DecodeStep:
         sd_topk(st, self.scores, self.rows, c.n_units, c.n, self.sel, self.idx, c.max_count,
                 self.count, self.topk_ws, stream)
 
+    def stage_plan_score(self, q, stream=None):
+        """Bit planes: the read plan computed inside the scan (same plan and scores
+        as stage_prep followed by stage_score)."""
+        c, ix = self.cfg, self.index
+        sd_plan_score(self.shape, ix["planes"], ix["scales"], q, self.sigma2, c.plan_mode,
+                      c.budget, self.plan, self.scores, stream)
+
     def stage_score_topk(self, q, stream=None):
         """Bit planes: the scan and the top-k in one call (same results as
         stage_score followed by stage_topk)."""
@@ -150,12 +160,15 @@ class DecodeStep:
 
     def stages(self):
         """(name, fn(q, stream)) of the step's stages in call order."""
+        topk = ("topk", lambda q, stream=None: self.stage_topk(stream))
         if self.fused:
             return [("plan", self.stage_prep), ("scan_topk", self.stage_score_topk),
                     ("gather_attend", self.stage_attend)]
+        if self.cfg.kind == SD_IDX_PLANES and self.cfg.plan_in_scan:
+            return [("plan_scan", self.stage_plan_score), topk,
+                    ("gather_attend", self.stage_attend)]
         first = "plan" if self.cfg.kind == SD_IDX_PLANES else "prep"
-        return [(first, self.stage_prep), ("scan", self.stage_score),
-                ("topk", lambda q, stream=None: self.stage_topk(stream)),
+        return [(first, self.stage_prep), ("scan", self.stage_score), topk,
                 ("gather_attend", self.stage_attend)]
 
     def run(self, q, stream=None):
