@@ -175,10 +175,29 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
  * and sigma2 itself, with sd_plan's arithmetic, and writes exactly the scores the
  * two calls would.  Arguments as sd_plan (q, sigma2, mode, budget; plan may be
  * NULL, else it receives the plan) and sd_score (planes, scales, scores).
+ *   wmax: NULL, or fp32 [B*hkv][n / 32], 4-byte aligned, receiving each 32-token
+ *   word's largest score (NaN if one of the 32 is NaN): the input of sd_topk_wmax.
  */
 int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales, const void* q,
                   const float* sigma2, int mode, int budget, uint8_t* plan, float* scores,
-                  void* stream);
+                  float* wmax, void* stream);
+
+/*
+ * sd_topk_wmax -- sd_topk(SD_SCORE_F32, sel.block == 1) for score rows whose
+ * 32-unit maxima are known (HashAttention 2.1 TOPK over the scores of the Fathom
+ * bit-plane scan): the same idx and count, drawn from the words whose maximum
+ * reaches a sampled threshold instead of from every score of the row.
+ *   scores fp32 [rows][n], 16-byte aligned; wmax fp32 [rows][n / 32] with
+ *   wmax[r][w] the largest of scores[r][32w .. 32w + 31], NaN if one of them is
+ *   NaN (as sd_plan_score writes it); n a multiple of 32.  Other arguments and
+ *   limits as sd_topk with n_units = n_tokens = n.  Calls outside the one-CTA
+ *   path (k > 1024, more than 36,864 words meeting [sink, n - local), rows of at
+ *   most 8192 units, or n - sink - local <= k) run sd_topk's kernels, so the
+ *   workspace is sd_topk_workspace_size(rows, n, sel) bytes.
+ */
+int sd_topk_wmax(const float* scores, const float* wmax, int64_t rows, int64_t n,
+                 const sd_select* sel, int32_t* idx, int64_t idx_stride, int32_t* count,
+                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * sd_score_topk -- sd_score(SD_IDX_PLANES) then sd_topk(SD_SCORE_F32) on those

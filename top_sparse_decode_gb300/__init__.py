@@ -28,7 +28,7 @@ __all__ = [
     "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
     "sd_gather_attend_noalloc", "sd_offload_gather",
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
-    "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score",
+    "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax",
 ]
 
 
@@ -138,10 +138,18 @@ def sd_topk(score_type: int, scores, rows: int, n_units: int, n_tokens: int, sel
 
 
 def sd_plan_score(shape: SdShape, planes, scales, q, sigma2, mode: int, budget: int, plan,
-                  scores, stream=None) -> None:
+                  scores, wmax=None, stream=None) -> None:
     _check(lib().sd_plan_score(ctypes.byref(shape), _ptr(planes), _ptr(scales), _ptr(q),
                                _ptr(sigma2), mode, budget, _ptr(plan), _ptr(scores),
-                               _stream(stream)), "sd_plan_score")
+                               _ptr(wmax), _stream(stream)), "sd_plan_score")
+
+
+def sd_topk_wmax(scores, wmax, rows: int, n: int, sel: SdSelect, idx, idx_stride: int, count,
+                 workspace=None, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().sd_topk_wmax(_ptr(scores), _ptr(wmax), rows, n, ctypes.byref(sel), _ptr(idx),
+                              idx_stride, _ptr(count), _ptr(workspace), ws_bytes,
+                              _stream(stream)), "sd_topk_wmax")
 
 
 def sd_score_topk_workspace_size(shape: SdShape, sel: SdSelect) -> int:

@@ -214,7 +214,7 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
 
 int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales, const void* q,
                   const float* sigma2, int mode, int budget, uint8_t* plan, float* scores,
-                  void* stream) {
+                  float* wmax, void* stream) {
   Dims s;
   int rc = check_shape(shape, &s, true);
   if (rc) return rc;
@@ -222,6 +222,8 @@ int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales,
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: NULL input");
   if (!aligned16(planes) || !aligned16(scores))
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: planes and scores must be 16-byte aligned");
+  if ((uintptr_t)wmax % 4)
+    return fail(SD_ERR_INVALID_ARG, "sd_plan_score: wmax must be 4-byte aligned");
   if (mode != SD_PLAN_WATERFILL && mode != SD_PLAN_FIXED && mode != SD_PLAN_FULL)
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: unknown plan mode %d", mode);
   if (mode == SD_PLAN_WATERFILL && (budget < 0 || budget > 4 * kD))
@@ -230,7 +232,42 @@ int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales,
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: fixed width %d outside [0, %d]", budget, kD);
   const PsPlanIn pl{sigma2, mode, budget, plan};
   return launch_score_planes(s, (const uint32_t*)planes, (const uint16_t*)scales, nullptr,
-                             (const uint16_t*)q, scores, (cudaStream_t)stream, nullptr, &pl);
+                             (const uint16_t*)q, scores, (cudaStream_t)stream, nullptr, &pl, wmax);
+}
+
+int sd_topk_wmax(const float* scores, const float* wmax, int64_t rows, int64_t n,
+                 const sd_select* sel, int32_t* idx, int64_t idx_stride, int32_t* count,
+                 void* workspace, size_t ws_bytes, void* stream) {
+  if (!scores || !wmax)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: NULL input");
+  if (!sel || sel->block != 1)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: sel is NULL or sel.block != 1");
+  if (n < 32 || n % 32)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: n = %lld is not a positive multiple of 32",
+                (long long)n);
+  if (!aligned16(scores) || (uintptr_t)wmax % 4)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: scores must be 16-byte, wmax 4-byte aligned");
+  // the remaining checks are sd_topk's
+  if (!idx || !count) return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: NULL input");
+  if (rows < 1 || n >= ((int64_t)1 << 31) || rows >= ((int64_t)1 << 31))
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: bad rows / n");
+  if (sel->k < 1 || sel->k > kMaxTopK)
+    return fail(SD_ERR_UNSUPPORTED, "sd_topk_wmax: k = %d outside [1, %d]", sel->k, kMaxTopK);
+  if (sel->sink < 0 || sel->local < 0)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: negative window");
+  const int64_t max_units = n < (int64_t)sel->sink + sel->local + sel->k
+                                ? n : (int64_t)sel->sink + sel->local + sel->k;
+  if (idx_stride < max_units)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: idx_stride %lld < %lld",
+                (long long)idx_stride, (long long)max_units);
+  if (n > kSmallRow && rows > 65535)
+    return fail(SD_ERR_UNSUPPORTED, "sd_topk_wmax: more than 65535 rows of over %d units",
+                kSmallRow);
+  const size_t need = topk_workspace_bytes(rows, n, *sel);
+  if (need && (!workspace || ws_bytes < need))
+    return fail(SD_ERR_WORKSPACE, "sd_topk_wmax: workspace %zu < %zu bytes", ws_bytes, need);
+  return launch_topk_wmax(scores, wmax, rows, n, *sel, idx, idx_stride, count, workspace,
+                          ws_bytes, (cudaStream_t)stream);
 }
 
 size_t sd_score_topk_workspace_size(const sd_shape* shape, const sd_select* sel) {

@@ -74,7 +74,8 @@ int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsi
 bool planes_aligned(const Dims& s, const void* planes, const void* scales);
 int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
                         const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st,
-                        const PsCand* cand = nullptr, const PsPlanIn* plan_in = nullptr);
+                        const PsCand* cand = nullptr, const PsPlanIn* plan_in = nullptr,
+                        float* wmax = nullptr);
 int launch_score_quest(const Dims& s, const uint16_t* summ, const uint16_t* q, float* scores,
                        cudaStream_t st);
 size_t topk_workspace_bytes(int64_t rows, int64_t n_units, const sd_select& sel);
@@ -87,6 +88,9 @@ int launch_score_topk(const Dims& s, const uint32_t* planes, const uint16_t* sca
 int launch_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
                 int64_t n_tokens, const sd_select& sel, int32_t* idx, int64_t idx_stride,
                 int32_t* count, void* ws, size_t ws_bytes, cudaStream_t st);
+int launch_topk_wmax(const float* scores, const float* wmax, int64_t rows, int64_t n,
+                     const sd_select& sel, int32_t* idx, int64_t idx_stride, int32_t* count,
+                     void* ws, size_t ws_bytes, cudaStream_t st);
 size_t attend_workspace_bytes(const Dims& s, int64_t max_count);
 int launch_gather_attend(const Dims& s, const uint16_t* q, const uint16_t* K, const uint16_t* V,
                          const int32_t* idx, int64_t idx_stride, const int32_t* count,

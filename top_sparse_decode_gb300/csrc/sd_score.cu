@@ -196,11 +196,12 @@ __device__ __forceinline__ void ps_mark(const PsCand& cd, int row, uint32_t T, i
   if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) atomicOr(cd.nan + row, 1u);
 }
 
-// Compute warps: consume slots until the end marker; with CAND, also append the
-// row's candidates (see PsCand).
+// Compute warps: consume slots until the end marker; with CAND, also mark the
+// row's candidates (see PsCand); with wmax, also write each 32-token word's
+// maximum score (NaN if one of them is NaN) to wmax[row][word].
 template <bool CAND>
 __device__ __forceinline__ void ps_compute(PsSmem& S, float* __restrict__ scores, int64_t n,
-                                           const PsCand& cd) {
+                                           const PsCand& cd, float* __restrict__ wmax) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = warp >> 2, wl = (warp & 3) * 32 + lane;  // plane parity, word
   float4* red = &S.red[wl * 8];
@@ -250,7 +251,15 @@ __device__ __forceinline__ void ps_compute(PsSmem& S, float* __restrict__ scores
           acc[4 * k + 3] = (acc[4 * k + 3] + o.w) + cb;
           if (valid) orow[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
         }
-        if (CAND) ps_mark(cd, m.row, m.thr, m.tok0 + wl * 32, valid, acc);
+        if (CAND) {
+          ps_mark(cd, m.row, m.thr, m.tok0 + wl * 32, valid, acc);
+        } else if (wmax) {  // a tree of depth 5 in place: acc is reset by the next tile
+#pragma unroll
+          for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) acc[i] = fmax_nan(acc[i], acc[i + w]);
+          if (valid) wmax[(int64_t)m.row * (n >> 5) + (m.tok0 >> 5) + wl] = acc[0];
+        }
       }
     }
   }
@@ -474,11 +483,12 @@ __global__ void __launch_bounds__(kPsThreads, kPsCtasPerSm)
 score_planes_kernel(const uint32_t* __restrict__ planes, const uint16_t* __restrict__ scales,
                     const uint8_t* __restrict__ plan, const uint16_t* __restrict__ q, int Hq,
                     int Hkv, int64_t n, int64_t ncap, int upr, int64_t total_units,
-                    float* __restrict__ scores, PsCand cd, PsPlanIn pl) {
+                    float* __restrict__ scores, PsCand cd, PsPlanIn pl,
+                    float* __restrict__ wmax) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   PsSmem& S = *reinterpret_cast<PsSmem*>(smem_raw);
   if (threadIdx.x < kPsCompute)
-    ps_compute<CAND>(S, scores, n, cd);
+    ps_compute<CAND>(S, scores, n, cd, wmax);
   else
     ps_help<G, A16, CAND>(S, planes, scales, plan, q, Hq, Hkv, n, ncap, upr, total_units, cd, pl);
 }
@@ -499,7 +509,7 @@ static int sm_count() {
 template <int G, bool A16, bool CAND>
 static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scales,
                     const uint8_t* plan, const uint16_t* q, float* scores, const PsCand& cd,
-                    const PsPlanIn& pl, cudaStream_t st) {
+                    const PsPlanIn& pl, float* wmax, cudaStream_t st) {
   auto kern = score_planes_kernel<G, A16, CAND>;
   if (int rc = set_smem_limit((const void*)kern, sizeof(PsSmem), "score_planes: smem attribute"))
     return rc;
@@ -507,7 +517,8 @@ static int planes_t(const Dims& s, const uint32_t* planes, const uint16_t* scale
   const int64_t total = (int64_t)upr * s.B * s.Hkv;
   const int64_t grid = imin64(total, (int64_t)sm_count() * kPsCtasPerSm);
   kern<<<(unsigned)grid, kPsThreads, sizeof(PsSmem), st>>>(planes, scales, plan, q, s.Hq, s.Hkv,
-                                                          s.n, s.ncap, upr, total, scores, cd, pl);
+                                                          s.n, s.ncap, upr, total, scores, cd, pl,
+                                                          wmax);
   note_launches(1);
   return check_launch("score_planes");
 }
@@ -518,25 +529,25 @@ bool planes_aligned(const Dims& s, const void* planes, const void* scales) {
 
 int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
                         const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st,
-                        const PsCand* cand, const PsPlanIn* plan_in) {
+                        const PsCand* cand, const PsPlanIn* plan_in, float* wmax) {
   const bool a16 = planes_aligned(s, planes, scales);
   const PsPlanIn pl = plan_in ? *plan_in : PsPlanIn{};
   if (cand) {  // the fused scan + top-k path (16-byte aligned layouts only)
     if (!a16) return fail(SD_ERR_INVALID_ARG, "score_planes: candidates need n_cap %% 512 == 0 "
                                               "and 16-byte aligned planes and scales");
     switch (s.G) {
-      case 1: return planes_t<1, true, true>(s, planes, scales, plan, q, scores, *cand, pl, st);
-      case 2: return planes_t<2, true, true>(s, planes, scales, plan, q, scores, *cand, pl, st);
-      case 4: return planes_t<4, true, true>(s, planes, scales, plan, q, scores, *cand, pl, st);
-      default: return planes_t<8, true, true>(s, planes, scales, plan, q, scores, *cand, pl, st);
+      case 1: return planes_t<1, true, true>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, st);
+      case 2: return planes_t<2, true, true>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, st);
+      case 4: return planes_t<4, true, true>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, st);
+      default: return planes_t<8, true, true>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, st);
     }
   }
   const PsCand none{};
   switch (s.G) {
-    case 1: return a16 ? planes_t<1, true, false>(s, planes, scales, plan, q, scores, none, pl, st) : planes_t<1, false, false>(s, planes, scales, plan, q, scores, none, pl, st);
-    case 2: return a16 ? planes_t<2, true, false>(s, planes, scales, plan, q, scores, none, pl, st) : planes_t<2, false, false>(s, planes, scales, plan, q, scores, none, pl, st);
-    case 4: return a16 ? planes_t<4, true, false>(s, planes, scales, plan, q, scores, none, pl, st) : planes_t<4, false, false>(s, planes, scales, plan, q, scores, none, pl, st);
-    default: return a16 ? planes_t<8, true, false>(s, planes, scales, plan, q, scores, none, pl, st) : planes_t<8, false, false>(s, planes, scales, plan, q, scores, none, pl, st);
+    case 1: return a16 ? planes_t<1, true, false>(s, planes, scales, plan, q, scores, none, pl, wmax, st) : planes_t<1, false, false>(s, planes, scales, plan, q, scores, none, pl, wmax, st);
+    case 2: return a16 ? planes_t<2, true, false>(s, planes, scales, plan, q, scores, none, pl, wmax, st) : planes_t<2, false, false>(s, planes, scales, plan, q, scores, none, pl, wmax, st);
+    case 4: return a16 ? planes_t<4, true, false>(s, planes, scales, plan, q, scores, none, pl, wmax, st) : planes_t<4, false, false>(s, planes, scales, plan, q, scores, none, pl, wmax, st);
+    default: return a16 ? planes_t<8, true, false>(s, planes, scales, plan, q, scores, none, pl, wmax, st) : planes_t<8, false, false>(s, planes, scales, plan, q, scores, none, pl, wmax, st);
   }
 }
 

@@ -1308,6 +1308,754 @@ int launch_topk(int score_type, const void* scores, int64_t rows, int64_t n_unit
   return topk_t<false>(scores, rows, g, idx, idx_stride, count, ws, st);
 }
 
+// --------------------------------------------------------------------------------------
+// fp32 rows with known 32-unit maxima (sd_topk_wmax): one CTA per row.
+// --------------------------------------------------------------------------------------
+// A word is 32 consecutive units; its competing maximum is the largest score of its
+// units inside [lead, tail).  If at least k competing units have key >= T, the
+// k-th largest key is >= T, so every member of the top k has key >= T and lies in a
+// word whose competing maximum is >= T.  Per row:
+//   1. the keys of the words' competing maxima go to shared memory (coalesced loads;
+//      the at most two words cut by lead or tail are recomputed from their scores;
+//      a NaN anywhere marks the row);
+//   2. T_est = a lower bound of the r-th largest key of an evenly spaced sample of
+//      words (r as for the sampled top-k, mu = k S / W; two radix digits), and the
+//      words whose key is >= T_est are listed in ascending order (each thread owns
+//      a contiguous run of words; one block-wide scan gives the offsets);
+//   3. those words' scores are read (one warp per word, one coalesced 128-byte
+//      line) and every competing unit with key >= T_est becomes a candidate,
+//      named by its position in the word list (list entry * 32 + unit in word),
+//      which orders candidates as their units;
+//   4. with at least k candidates, a radix select over (key, position descending)
+//      marks the top k in a bit mask per listed word; one block-wide scan over the
+//      masks' populations places them, so the units come out ascending unsorted.
+// When the estimate leaves fewer than k candidates, or a list overflows, an exact
+// path replaces 3-4: the k largest words by (key descending, word ascending) hold
+// the top k (a unit outside them is beaten by each of their maxima: a larger key,
+// or an equal key at a lower unit), and a radix select over those words' units,
+// reading their scores at every pass, picks the top k; a counting sort orders them.
+constexpr int kWmThreads = 1024;
+constexpr int kWmWords = 36864;   // words per row (n <= ~1.18M): at most 36 per thread
+constexpr int kWmMaxK = 1024;     // largest k of this path
+constexpr int kWmSample = 2048;   // sampled words
+constexpr int kWmCandWords = 4096;
+constexpr int kWmCand = 4096;     // candidate units
+
+struct WmSmem {
+  // word keys at wpos(i); on the estimate path the selection masks (one per listed
+  // word) reuse its start once the keys are no longer read
+  uint32_t wk[kWmWords];  // padded runs end below kWmWords: PER + padw <= 36 per thread
+  uint32_t cw[kWmCandWords];        // listed words (exact path: the k selected words)
+  uint64_t ct[kWmCand];             // candidates (key << 32 | position); the sample in
+                                    // step 2; the exact path's sort scratch
+  uint32_t sel[kWmMaxK];
+  uint32_t hist[kBins];
+  uint32_t scratch[32], out[4], wsum[32];
+  uint32_t nan, nct, nsel, nlist, kmin, kmax;
+};
+
+// Exclusive prefix of v over the block's threads (in thread order) and the total.
+// Uses wsum[32]; contains two __syncthreads.
+template <int NT>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wsum, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  uint32_t w = lane < NT / 32 ? wsum[lane] : 0u, wincl = w;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, wincl, o);
+    if (lane >= o) wincl += y;
+  }
+  total = __shfl_sync(0xFFFFFFFFu, wincl, 31);
+  const uint32_t before = __shfl_sync(0xFFFFFFFFu, wincl - w, warp);
+  __syncthreads();
+  return before + incl - v;
+}
+
+// Radix select of the `need` largest of c unique 64-bit values produced by
+// get(i, x) (false: i holds no value), all < 2^nb: returns T with exactly `need`
+// values >= T.  11-bit digits; get is called once per value and pass.
+template <int NT, class Get>
+__device__ uint64_t radix_select_fn(int c, Get get, uint32_t need, int nb, uint32_t* hist,
+                                    uint32_t* scratch, uint32_t* out) {
+  uint64_t prefix = 0;
+  int pos = nb;
+  uint32_t r = need;
+  while (pos > 0) {
+    const int w = min(kDigit, pos), npos = pos - w;
+    for (int b = threadIdx.x; b < kBins; b += NT) hist[b] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < c; i += NT) {
+      uint64_t x;
+      if (get(i, x) && (pos >= 64 || (x >> pos) == prefix))
+        atomicAdd(&hist[(uint32_t)(x >> npos) & ((1u << w) - 1)], 1u);
+    }
+    __syncthreads();
+    pick_digit<NT>(hist, r, scratch, out);
+    const uint32_t d = out[0], above = out[1], inb = hist[d];
+    __syncthreads();
+    r -= above;
+    prefix = (prefix << w) | d;
+    pos = npos;
+    if (inb == r) break;
+  }
+  return prefix << pos;
+}
+
+__global__ void __launch_bounds__(kWmThreads)
+topk_wmax_kernel(const float* __restrict__ scores, const float* __restrict__ wmax, Geo g,
+                 int32_t* __restrict__ idx, int64_t idx_stride, int32_t* __restrict__ count) {
+  constexpr int NT = kWmThreads;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  WmSmem& S = *reinterpret_cast<WmSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x;
+  const int64_t n = g.n_units, nw = n >> 5;
+  const float* srow = scores + row * n;
+  int32_t* idx_row = idx + row * idx_stride;
+  const int lead = g.lead, tail = g.tail, M = g.M, k = g.k;
+  const int w0 = lead >> 5, W = ((tail - 1) >> 5) - w0 + 1;  // words meeting [lead, tail)
+  // step 2 gives each thread a run of PER words, read as 16-byte vectors; runs are
+  // padded to an odd number of vectors so that a quarter warp's reads hit distinct banks
+  const int PER = 4 * ((W + 4 * NT - 1) / (4 * NT));  // <= 36
+  const int padw = ((PER >> 2) & 1) ? 0 : 4;          // PER + padw <= 36
+  const uint32_t magic = (uint32_t)((0x100000000ull + PER - 1) / PER);  // i / PER, i < 2^16
+  auto wpos = [&](int i) { return i + (int)__umulhi((uint32_t)i, magic) * padw; };
+  const bool cut0 = (lead & 31) != 0, cut1 = (tail & 31) != 0;
+  if (tid == 0) { S.nan = 0; S.nct = 0; S.nsel = 0; S.kmin = 0xFFFFFFFFu; S.kmax = 0; }
+
+  // ---- 1. word keys ----
+  {
+    // the cut words' scores (warps 0 and 1), in flight with the maxima
+    const bool cw0 = warp == 0 && cut0;
+    const bool cw1 = warp == 1 && cut1 && !(cut0 && W == 1);  // W == 1: warp 0 covers both
+    float xc = -INFINITY;
+    if (cw0 || cw1) {
+      const int u = (w0 + (cw0 ? 0 : W - 1)) * 32 + lane;
+      if (u >= lead && u < tail) xc = __ldg(srow + u);
+    }
+    const float* base = wmax + row * nw + w0;
+    constexpr int kL = kWmWords / NT;  // coalesced 4-byte loads per thread, all in flight
+    float v[kL];
+#pragma unroll
+    for (int j = 0; j < kL; ++j) {
+      const int i = j * NT + tid;
+      v[j] = i < W ? __ldg(base + i) : 0.f;
+    }
+    bool nan = false;
+#pragma unroll
+    for (int j = 0; j < kL; ++j) {
+      const int i = j * NT + tid;
+      if (i < W) {
+        if (!((i == 0 && cut0) || (i == W - 1 && cut1))) nan |= v[j] != v[j];
+        S.wk[wpos(i)] = key_of_f32(v[j]);
+      }
+    }
+    __syncthreads();
+    if (cw0 || cw1) {
+      nan |= xc != xc;
+      float m = xc;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      if (lane == 0) S.wk[wpos(cw0 ? 0 : W - 1)] = key_of_f32(m);
+    }
+    if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) atomicOr(&S.nan, 1u);
+    __syncthreads();
+  }
+  if (S.nan) {
+    if (tid == 0) count[row] = -1;
+    return;
+  }
+
+  // ---- 2. estimate and listed words ----
+  bool exact = true;
+  {
+    const int Ssz = min(W, kWmSample);
+    uint32_t* samp = reinterpret_cast<uint32_t*>(S.ct);
+    for (int s = tid; s < Ssz; s += NT) samp[s] = S.wk[wpos((int)(((int64_t)s * W) / Ssz))];
+    __syncthreads();
+    // two 11-bit digits: T is the low end of the 22-bit bin holding the r-th largest
+    const uint32_t T = (uint32_t)radix_threshold<NT, uint32_t>(
+        samp, Ssz, (uint32_t)min(g.r_sample, Ssz), 0, 32, S.hist, S.scratch, S.out, 2);
+    const int i0 = tid * PER;
+    const uint32_t* run = &S.wk[tid * (PER + padw)];
+    uint64_t hitm = 0;
+    for (int m = 0; 4 * m < PER; ++m) {
+      const uint4 x = *reinterpret_cast<const uint4*>(run + 4 * m);
+      const int i = i0 + 4 * m;
+      const uint32_t b = (uint32_t)(x.x >= T && i < W) | ((uint32_t)(x.y >= T && i + 1 < W) << 1) |
+                         ((uint32_t)(x.z >= T && i + 2 < W) << 2) |
+                         ((uint32_t)(x.w >= T && i + 3 < W) << 3);
+      hitm |= (uint64_t)b << (4 * m);
+    }
+    uint32_t ncw;
+    uint32_t p = block_excl_scan<NT>((uint32_t)__popcll(hitm), S.wsum, ncw);
+    if (ncw <= (uint32_t)kWmCandWords)
+      for (uint64_t h = hitm; h; h &= h - 1) S.cw[p++] = (uint32_t)(i0 + __ffsll((long long)h) - 1);
+    __syncthreads();
+
+    if (ncw <= (uint32_t)kWmCandWords) {
+      // ---- 3. candidates: one warp per listed word, eight words in flight ----
+      uint32_t mn = 0xFFFFFFFFu, mx = 0;
+      for (int c0 = warp * 8; c0 < (int)ncw; c0 += 8 * (NT / 32)) {  // warp-uniform
+        float x[8];
+        int ub[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + u;
+          ub[u] = c < (int)ncw ? (w0 + (int)S.cw[c]) * 32 : -64;
+          x[u] = c < (int)ncw ? __ldg(srow + ub[u] + lane) : -INFINITY;
+        }
+        uint32_t msk[8], tot = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int un = ub[u] + lane;
+          msk[u] = __ballot_sync(0xFFFFFFFFu, un >= lead && un < tail && key_of_f32(x[u]) >= T);
+          tot += __popc(msk[u]);
+        }
+        uint32_t basep = 0;
+        if (lane == 0 && tot) basep = atomicAdd(&S.nct, tot);
+        basep = __shfl_sync(0xFFFFFFFFu, basep, 0);
+        const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if ((msk[u] >> lane) & 1u) {
+            const uint32_t slot = basep + __popc(msk[u] & below);
+            const uint32_t key = key_of_f32(x[u]);
+            if (slot < (uint32_t)kWmCand)
+              S.ct[slot] = ((uint64_t)key << 32) | (uint32_t)((c0 + u) * 32 + lane);
+            mn = min(mn, key);
+            mx = max(mx, key);
+          }
+          basep += __popc(msk[u]);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      }
+      if (lane == 0 && mn <= mx) { atomicMin(&S.kmin, mn); atomicMax(&S.kmax, mx); }
+      __syncthreads();
+      const uint32_t nct = S.nct;
+      exact = nct < (uint32_t)k || nct > (uint32_t)kWmCand;
+      if (!exact) {
+        // ---- 4. the top k of the candidates, marked per listed word ----
+        const uint32_t kmin = S.kmin;
+        const uint32_t plast = ncw * 32 - 1;  // positions are < ncw * 32
+        const int bC = bits_of(plast);
+        const int nb = bits_of(S.kmax - kmin) + bC;
+        uint32_t* selm = S.wk;  // the word keys are no longer read
+        for (int c = tid; c < (int)ncw; c += NT) selm[c] = 0;
+        for (uint32_t j = tid; j < nct; j += NT) {
+          const uint64_t e = S.ct[j];
+          S.ct[j] = ((uint64_t)((uint32_t)(e >> 32) - kmin) << bC) | (uint64_t)(plast - (uint32_t)e);
+        }
+        __syncthreads();
+        const uint64_t Tc = nct == (uint32_t)k
+                                ? 0
+                                : radix_threshold<NT, uint64_t>(S.ct, (int)nct, (uint32_t)k, 0,
+                                                                nb, S.hist, S.scratch, S.out);
+        const uint64_t pmask = (1ull << bC) - 1;
+        for (uint32_t j = tid; j < nct; j += NT) {
+          const uint64_t e = S.ct[j];
+          if (e >= Tc) {
+            const uint32_t pp = plast - (uint32_t)(e & pmask);
+            atomicOr(&selm[pp >> 5], 1u << (pp & 31));
+          }
+        }
+        __syncthreads();
+        // ---- 5. ascending placement: each thread a run of q listed words ----
+        const int q = ((int)ncw + NT - 1) / NT;  // <= 4
+        uint32_t cnt = 0;
+        for (int e = 0; e < q; ++e) {
+          const int c = tid * q + e;
+          if (c < (int)ncw) cnt += __popc(selm[c]);
+        }
+        uint32_t total;
+        uint32_t off = block_excl_scan<NT>(cnt, S.wsum, total);
+        int32_t* sel_out = idx_row + lead;
+        for (int e = 0; e < q; ++e) {
+          const int c = tid * q + e;
+          if (c < (int)ncw) {
+            const int ubase = (w0 + (int)S.cw[c]) * 32;
+            for (uint32_t b = selm[c]; b; b &= b - 1) sel_out[off++] = ubase + __ffs((int)b) - 1;
+          }
+        }
+        for (int p2 = tid; p2 < lead; p2 += NT) idx_row[p2] = p2;
+        const int ntail = (int)(n - tail);
+        for (int p2 = tid; p2 < ntail; p2 += NT) idx_row[lead + k + p2] = tail + p2;
+        if (tid == 0) count[row] = lead + k + ntail;
+      }
+    }
+    __syncthreads();
+  }
+  if (!exact) return;
+
+  // ---- the exact path: the k largest words, then their units ----
+  const int kw = min(k, W);
+  const int bW = bits_of((uint32_t)(W - 1));
+  const int bI = bits_of((uint32_t)(M - 1));
+  auto wkey = [&](int i) { return ((uint64_t)S.wk[wpos(i)] << bW) | (uint64_t)(W - 1 - i); };
+  uint64_t Tw = 0;
+  if (W > k)
+    Tw = radix_select_fn<NT>(W, [&](int i, uint64_t& x) { x = wkey(i); return true; },
+                             (uint32_t)k, 32 + bW, S.hist, S.scratch, S.out);
+  if (tid == 0) S.nlist = 0;
+  __syncthreads();
+  for (int i = tid; i < W; i += NT)
+    if (wkey(i) >= Tw) S.cw[atomicAdd(&S.nlist, 1u)] = (uint32_t)i;
+  __syncthreads();
+  // units of the kw words: entry e = 32 * (word's list position) + unit in word
+  auto unit_of = [&](int e) { return (w0 + (int)S.cw[e >> 5]) * 32 + (e & 31); };
+  auto get = [&](int e, uint64_t& x) {
+    const int u = unit_of(e);
+    if (u < lead || u >= tail) return false;
+    x = ((uint64_t)key_of_f32(__ldg(srow + u)) << bI) |
+        (uint64_t)((uint32_t)(M - 1) - (uint32_t)(u - lead));
+    return true;
+  };
+  const uint64_t Tu = radix_select_fn<NT>(kw * 32, get, (uint32_t)k, 32 + bI, S.hist,
+                                          S.scratch, S.out);
+  for (int e = tid; e < kw * 32; e += NT) {
+    uint64_t x;
+    if (get(e, x) && x >= Tu) S.sel[atomicAdd(&S.nsel, 1u)] = (uint32_t)unit_of(e);
+  }
+  __syncthreads();
+  const int nsel = (int)S.nsel;
+  uint32_t* tmp = reinterpret_cast<uint32_t*>(S.ct);
+  sort_units<NT>(S.sel, nsel, bits_of((uint32_t)(n - 1)), tmp, tmp + 2048);
+  write_units<NT>(g, S.sel, nsel, idx_row, count + row);
+}
+
+// --------------------------------------------------------------------------------------
+// The same selection, one thread-block cluster of CS CTAs per row (sd_topk_wmax on
+// few long rows): a row's words are split evenly over the cluster's CTAs.
+// --------------------------------------------------------------------------------------
+//   1. each CTA loads its words' maxima (coalesced; the cut words recomputed) and
+//      the same evenly spaced sample of the row's maxima, and takes T_est from the
+//      sample as the single-CTA kernel does (every CTA the same T_est, no exchange);
+//   2. each CTA lists its words with key >= T_est, reads their scores (one warp per
+//      word, one 128-byte line), and sends every competing unit with key >= T_est
+//      to CTA 0 as (key << 21 | 2^21 - 1 - unit): unique, and larger for a larger
+//      key or, at equal keys, a lower unit;
+//   3. with at least k candidates in all, CTA 0 radix-selects the k largest, counts
+//      the selected units each CTA sent and hands every CTA the threshold and its
+//      output offset; each CTA marks its selected units in a bit mask per word and
+//      writes them ascending from its offset.
+// Two cluster barriers in all (after the sends, after the hand-out).  NaN rows are
+// reported through CTA 0.  An estimate that leaves fewer than k candidates, or
+// candidates beyond the buffers (heavy ties), sends CTA 0 alone down the single-CTA
+// kernel's exact path (word keys read from wmax).
+constexpr int kWcThreads = 512;
+constexpr int kWcWords = kWmWords / 8;  // words per CTA at CS >= 8 (9 per thread)
+constexpr int kWcLocal = 3072;          // candidates a CTA holds
+constexpr int kWcGather = 4096;         // candidates CTA 0 gathers
+
+struct WcSmem {
+  uint32_t wk[kWcWords];    // word keys; then the selection masks per word
+  uint32_t lw[kWcWords];    // listed words; the exact path's word list
+  uint64_t lc[kWcLocal];    // this CTA's candidates; the sample before them
+  uint64_t gb[kWcGather];   // CTA 0: everyone's candidates; the exact path's sort scratch
+  uint32_t pwh[(kWcThreads / 32) * 256];  // radix tables (per warp); the exact
+                                          // path's histogram [0, 2048), units
+                                          // [2048, 3072) and scratch [3072, 3104)
+  uint32_t cbase[16], clen[16];  // CTA 0: where each CTA's candidates went
+  uint32_t wsum[32], out[4];
+  unsigned long long tc;      // CTA 0 -> all: the k-th largest candidate
+  uint32_t mode;              // CTA 0 -> all: 0 thresholds, 1 the exact path, 2 NaN row
+  uint32_t off;               // CTA 0 -> all: the CTA's first output slot
+  uint32_t nan, nlc, ngb, ovf, kmax, nsel, nlist;
+};
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+template <int CS>
+__global__ void __launch_bounds__(kWcThreads, 2)
+topk_wmax_cluster_kernel(const float* __restrict__ scores, const float* __restrict__ wmax, Geo g,
+                         int32_t* __restrict__ idx, int64_t idx_stride,
+                         int32_t* __restrict__ count) {
+  constexpr int NT = kWcThreads;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  WcSmem& S = *reinterpret_cast<WcSmem*>(smem_raw);
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.y;
+  const int64_t n = g.n_units, nw = n >> 5;
+  const float* srow = scores + row * n;
+  int32_t* idx_row = idx + row * idx_stride;
+  const int lead = g.lead, tail = g.tail, k = g.k;
+  const int w0 = lead >> 5, W = ((tail - 1) >> 5) - w0 + 1;  // words meeting [lead, tail)
+  const int wlo = (int)(((int64_t)rank * W) / CS), whi = (int)(((int64_t)(rank + 1) * W) / CS);
+  const int Wc = whi - wlo;                                  // this CTA's words
+  const bool cut0 = (lead & 31) != 0, cut1 = (tail & 31) != 0;
+  if (tid == 0) { S.nan = 0; S.nlc = 0; S.ngb = 0; S.ovf = 0; S.kmax = 0; }
+  // remote accesses start after every CTA has started and set its counters: the
+  // arrival is here, the wait just before the first remote access
+  cluster_arrive_release();
+
+  // ---- 1. word keys, the sample, T_est ----
+  const float* wrow = wmax + row * nw + w0;
+  const int Ssz = min(W, kWmSample);
+  uint32_t* samp = reinterpret_cast<uint32_t*>(S.lc);
+  {
+    // a cut word's competing maximum, from its scores (warps 0 and 1 of its owner)
+    const bool own0 = rank == 0 && warp == 0 && cut0;
+    const bool own1 = rank == CS - 1 && warp == 1 && cut1 && !(cut0 && W == 1);
+    float xc = -INFINITY;
+    if (own0 || own1) {
+      const int u = (w0 + (own0 ? 0 : W - 1)) * 32 + lane;
+      if (u >= lead && u < tail) xc = __ldg(srow + u);
+    }
+    constexpr int kL = kWcWords / NT;
+    constexpr int kS = kWmSample / NT;
+    float v[kL], sv[kS];
+#pragma unroll
+    for (int j = 0; j < kL; ++j) {
+      const int i = j * NT + tid;
+      v[j] = i < Wc ? __ldg(wrow + wlo + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+      const int s = j * NT + tid;
+      sv[j] = s < Ssz ? __ldg(wrow + (int)(((int64_t)s * W) / Ssz)) : 0.f;
+    }
+    bool nan = false;
+#pragma unroll
+    for (int j = 0; j < kL; ++j) {
+      const int i = j * NT + tid, wi = wlo + i;
+      if (i < Wc) {
+        if (!((wi == 0 && cut0) || (wi == W - 1 && cut1))) nan |= v[j] != v[j];
+        S.wk[i] = key_of_f32(v[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kS; ++j) {
+      const int s = j * NT + tid;
+      if (s < Ssz) samp[s] = key_of_f32(sv[j]);
+    }
+    __syncthreads();
+    if (own0 || own1) {
+      nan |= xc != xc;
+      float m = xc;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      if (lane == 0) S.wk[own0 ? 0 : Wc - 1] = key_of_f32(m);
+    }
+    if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) S.nan = 1;
+  }
+  __syncthreads();
+  // two 8-bit digits: T is the low end of the 16-bit bin holding the r-th largest
+  const uint32_t T = (uint32_t)radix_select_pw<NT, uint32_t>(
+      samp, Ssz, (uint32_t)min(g.r_sample, Ssz), 32, 2, S.pwh, S.out);
+
+  // ---- 2. listed words and their candidates, sent to CTA 0 ----
+  {
+    constexpr int kR = (kWcWords + NT - 1) / NT;  // words per thread run (<= 9)
+    const int R = (Wc + NT - 1) / NT, i0 = tid * R;
+    uint32_t hitm = 0;
+#pragma unroll
+    for (int j = 0; j < kR; ++j)
+      if (j < R && i0 + j < Wc && S.wk[i0 + j] >= T) hitm |= 1u << j;
+    uint32_t nl;
+    uint32_t p = block_excl_scan<NT>((uint32_t)__popc(hitm), S.wsum, nl);
+    for (uint32_t h = hitm; h; h &= h - 1) S.lw[p++] = (uint32_t)(wlo + i0 + __ffs((int)h) - 1);
+    __syncthreads();
+    uint32_t mx = 0;
+    for (int c0 = warp * 8; c0 < (int)nl; c0 += 8 * (NT / 32)) {  // warp-uniform
+      float x[8];
+      int ub[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u;
+        ub[u] = c < (int)nl ? (w0 + (int)S.lw[c]) * 32 : -64;
+        x[u] = c < (int)nl ? __ldg(srow + ub[u] + lane) : -INFINITY;
+      }
+      uint32_t msk[8], tot = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int un = ub[u] + lane;
+        msk[u] = __ballot_sync(0xFFFFFFFFu, un >= lead && un < tail && key_of_f32(x[u]) >= T);
+        tot += __popc(msk[u]);
+      }
+      uint32_t basep = 0;
+      if (lane == 0 && tot) basep = atomicAdd(&S.nlc, tot);
+      basep = __shfl_sync(0xFFFFFFFFu, basep, 0);
+      const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if ((msk[u] >> lane) & 1u) {
+          const uint32_t slot = basep + __popc(msk[u] & below);
+          const uint32_t key = key_of_f32(x[u]);
+          if (slot < (uint32_t)kWcLocal)
+            S.lc[slot] = ((uint64_t)key << 21) | (uint64_t)(0x1FFFFFu - (uint32_t)(ub[u] + lane));
+          mx = max(mx, key);
+        }
+        basep += __popc(msk[u]);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (lane == 0 && mx) atomicMax(&S.kmax, mx);
+    __syncthreads();
+    cluster_wait_acquire();  // every CTA has started
+    const uint32_t nlc = S.nlc;
+    WcSmem* S0 = cl.map_shared_rank(&S, 0);
+    if (tid == 0) {
+      uint32_t gbase = 0xFFFFFFFFu;
+      if (S.nan) atomicOr(&S0->nan, 1u);
+      if (nlc > (uint32_t)kWcLocal) {
+        atomicOr(&S0->ovf, 1u);
+      } else {
+        gbase = nlc ? atomicAdd(&S0->ngb, nlc) : 0u;
+        if (gbase + nlc > (uint32_t)kWcGather) gbase = 0xFFFFFFFFu;  // CTA 0 sees ngb > cap
+        atomicMax(&S0->kmax, S.kmax);
+      }
+      S0->cbase[rank] = gbase;
+      S0->clen[rank] = nlc;
+      S.out[2] = gbase;
+    }
+    __syncthreads();
+    const uint32_t gbase = S.out[2];
+    if (gbase != 0xFFFFFFFFu)
+      for (uint32_t i = tid; i < nlc; i += NT) S0->gb[gbase + i] = S.lc[i];
+  }
+  __syncthreads();
+  cl.sync();  // B1: CTA 0 holds the candidates (or knows that they overflowed)
+
+  // ---- 3. CTA 0: the k-th largest candidate, counts and offsets, handed out ----
+  if (rank == 0) {
+    const uint32_t ngb = S.ngb;
+    uint32_t mode = S.nan ? 2u : (S.ovf || ngb > (uint32_t)kWcGather || ngb < (uint32_t)k) ? 1u : 0u;
+    uint64_t tc = 0;
+    if (mode == 0) {
+      // keys are >= T: subtract T's place so that the select starts at the bits that differ
+      const uint64_t base = (uint64_t)T << 21;
+      for (uint32_t i = tid; i < ngb; i += NT) S.gb[i] -= base;
+      __syncthreads();
+      const int nb = bits_of(S.kmax - T) + 21;
+      if (ngb > (uint32_t)k)
+        tc = radix_select_pw<NT, uint64_t>(S.gb, (int)ngb, (uint32_t)k, nb, 64, S.pwh, S.out);
+      // selected units per sending CTA (warp r counts CTA r's candidates)
+      if (warp < CS) {
+        const uint32_t b0 = S.cbase[warp], len = S.clen[warp];
+        uint32_t c = 0;
+        for (uint32_t i = lane; i < len; i += 32) c += S.gb[b0 + i] >= tc ? 1u : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+        if (lane == 0) S.pwh[warp] = c;  // the select is done with the tables
+      }
+      __syncthreads();
+      tc += base;
+    }
+    if (tid < CS) {
+      uint32_t off = 0;
+      for (int r = 0; r < tid; ++r) off += mode == 0 ? S.pwh[r] : 0u;
+      WcSmem* Sr = cl.map_shared_rank(&S, tid);
+      Sr->tc = tc;
+      Sr->mode = mode;
+      Sr->off = off;
+    }
+  }
+  __syncthreads();
+  cl.sync();  // B2: no shared memory is accessed remotely after this
+
+  if (S.mode == 2) {  // a NaN among the competing scores
+    if (rank == 0 && tid == 0) count[row] = -1;
+    return;
+  }
+  if (S.mode == 0) {
+    // ---- 4. mark and write ----
+    const uint64_t tc = S.tc;
+    const uint32_t nlc = S.nlc;
+    uint32_t* selm = S.wk;  // one mask per word of this CTA
+    for (int i = tid; i < Wc; i += NT) selm[i] = 0;
+    __syncthreads();
+    for (uint32_t i = tid; i < nlc; i += NT) {
+      const uint64_t e = S.lc[i];
+      if (e >= tc) {
+        const uint32_t u = 0x1FFFFFu - (uint32_t)(e & 0x1FFFFFu);
+        atomicOr(&selm[(int)(u >> 5) - w0 - wlo], 1u << (u & 31));
+      }
+    }
+    __syncthreads();
+    constexpr int kR = (kWcWords + NT - 1) / NT;
+    const int R = (Wc + NT - 1) / NT, i0 = tid * R;
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int j = 0; j < kR; ++j)
+      if (j < R && i0 + j < Wc) cnt += __popc(selm[i0 + j]);
+    uint32_t mine;
+    uint32_t off = S.off + block_excl_scan<NT>(cnt, S.wsum, mine);
+    int32_t* sel_out = idx_row + lead;
+#pragma unroll
+    for (int j = 0; j < kR; ++j) {
+      if (j < R && i0 + j < Wc) {
+        const int ubase = (w0 + wlo + i0 + j) * 32;
+        for (uint32_t b = selm[i0 + j]; b; b &= b - 1) sel_out[off++] = ubase + __ffs((int)b) - 1;
+      }
+    }
+    const int ntail = (int)(n - tail);
+    if (rank == 0) {
+      for (int p2 = tid; p2 < lead; p2 += NT) idx_row[p2] = p2;
+      if (tid == 0) count[row] = lead + k + ntail;
+    }
+    if (rank == CS - 1)
+      for (int p2 = tid; p2 < ntail; p2 += NT) idx_row[lead + k + p2] = tail + p2;
+    return;
+  }
+  if (rank != 0) return;
+
+  // ---- the exact path (CTA 0 alone): the k largest words, then their units ----
+  // word keys from wmax, the cut words' competing maxima recomputed
+  uint32_t* hist = S.pwh;
+  uint32_t* sel = S.pwh + 2048;
+  uint32_t* scratch = S.pwh + 3072;
+  if (warp < 2) {
+    const int i = warp == 0 ? 0 : W - 1;
+    const int u = (w0 + i) * 32 + lane;
+    float m = u >= lead && u < tail ? __ldg(srow + u) : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) S.out[2 + warp] = key_of_f32(m);
+  }
+  if (tid == 0) { S.nlist = 0; S.nsel = 0; }
+  __syncthreads();
+  const uint32_t kc0 = S.out[2], kc1 = S.out[3];
+  const int M = g.M;
+  const int kw = min(k, W);
+  const int bW = bits_of((uint32_t)(W - 1));
+  const int bI = bits_of((uint32_t)(M - 1));
+  auto wkey = [&](int i) {
+    const uint32_t key = (i == 0 && cut0) ? kc0
+                       : (i == W - 1 && cut1) ? kc1 : key_of_f32(__ldg(wrow + i));
+    return ((uint64_t)key << bW) | (uint64_t)(W - 1 - i);
+  };
+  uint64_t Tw = 0;
+  if (W > k)
+    Tw = radix_select_fn<NT>(W, [&](int i, uint64_t& x) { x = wkey(i); return true; },
+                             (uint32_t)k, 32 + bW, hist, scratch, S.out);
+  for (int i = tid; i < W; i += NT)
+    if (wkey(i) >= Tw) S.lw[atomicAdd(&S.nlist, 1u)] = (uint32_t)i;
+  __syncthreads();
+  auto unit_of = [&](int e) { return (w0 + (int)S.lw[e >> 5]) * 32 + (e & 31); };
+  auto get = [&](int e, uint64_t& x) {
+    const int u = unit_of(e);
+    if (u < lead || u >= tail) return false;
+    x = ((uint64_t)key_of_f32(__ldg(srow + u)) << bI) |
+        (uint64_t)((uint32_t)(M - 1) - (uint32_t)(u - lead));
+    return true;
+  };
+  const uint64_t Tu = radix_select_fn<NT>(kw * 32, get, (uint32_t)k, 32 + bI, hist, scratch,
+                                          S.out);
+  for (int e = tid; e < kw * 32; e += NT) {
+    uint64_t x;
+    if (get(e, x) && x >= Tu) sel[atomicAdd(&S.nsel, 1u)] = (uint32_t)unit_of(e);
+  }
+  __syncthreads();
+  const int nsel = (int)S.nsel;
+  uint32_t* tmp = reinterpret_cast<uint32_t*>(S.gb);
+  sort_units<NT>(sel, nsel, bits_of((uint32_t)(n - 1)), tmp, tmp + 2048);
+  write_units<NT>(g, sel, nsel, idx_row, count + row);
+}
+
+
+// Resident clusters of CS CTAs of topk_wmax_cluster_kernel (0: cannot run), per device.
+template <int CS>
+static int wmax_cluster_capacity() {
+  static int cap[64];
+  static bool known[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!known[dev]) {
+    auto kern = topk_wmax_cluster_kernel<CS>;
+    int nc = 0;
+    bool yes = set_smem_limit((const void*)kern, sizeof(WcSmem), "topk_wmax cluster") == SD_OK;
+    if (yes && CS > 8)
+      yes = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess;
+    if (yes) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(CS, 1, 1);
+      cfg.blockDim = dim3(kWcThreads, 1, 1);
+      cfg.dynamicSmemBytes = sizeof(WcSmem);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = CS;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
+    }
+    cudaGetLastError();
+    cap[dev] = nc;
+    known[dev] = true;
+  }
+  return cap[dev];
+}
+
+template <int CS>
+static int launch_wmax_cluster(const float* scores, const float* wmax, int64_t rows,
+                               const Geo& g, int32_t* idx, int64_t idx_stride, int32_t* count,
+                               cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CS, (unsigned)rows, 1);
+  cfg.blockDim = dim3(kWcThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(WcSmem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, topk_wmax_cluster_kernel<CS>, scores, wmax, g, idx, idx_stride,
+                         count) != cudaSuccess)
+    return check_launch("topk_wmax cluster");
+  note_launches(1);
+  return check_launch("topk_wmax cluster");
+}
+
+int launch_topk_wmax(const float* scores, const float* wmax, int64_t rows, int64_t n,
+                     const sd_select& sel, int32_t* idx, int64_t idx_stride, int32_t* count,
+                     void* ws, size_t ws_bytes, cudaStream_t st) {
+  Geo g = make_geo(n, n, sel);
+  const int64_t W = g.M > 0 ? ((g.tail - 1) >> 5) - (g.lead >> 5) + 1 : 0;
+  if (!(n > kSmallRow && g.M > g.k && g.k <= kWmMaxK && W <= kWmWords &&
+        (uintptr_t)scores % 16 == 0))
+    return launch_topk(SD_SCORE_F32, scores, rows, n, n, sel, idx, idx_stride, count, ws,
+                       ws_bytes, st);
+  g.r_sample = sample_rank(g.k, imin64(W, kWmSample), W);
+  // few rows: a cluster per row spreads the row's reads over CS SMs
+  if (n <= (1 << 21) && W > g.k && W >= 64 * 16 && rows <= 65535) {
+    if (rows <= wmax_cluster_capacity<16>())
+      return launch_wmax_cluster<16>(scores, wmax, rows, g, idx, idx_stride, count, st);
+    if (rows <= wmax_cluster_capacity<8>())
+      return launch_wmax_cluster<8>(scores, wmax, rows, g, idx, idx_stride, count, st);
+  }
+  if (int rc = set_smem_limit((const void*)topk_wmax_kernel, sizeof(WmSmem), "topk_wmax"))
+    return rc;
+  topk_wmax_kernel<<<(unsigned)rows, kWmThreads, sizeof(WmSmem), st>>>(scores, wmax, g, idx,
+                                                                        idx_stride, count);
+  note_launches(1);
+  return check_launch("topk_wmax");
+}
+
 // =====================================================================================
 // Fused bit-plane scan + top-k (sd_score_topk).
 //

@@ -9,8 +9,10 @@ libsd's kernels.  A step for one layer, all heads and the whole batch is
 and the per-stage split T = T_qmap + T_scan + T_topk + T_att follows
 HashAttention: Semantic Sparsity for Faster Inference, 2.5.  For bit planes the
 read plan is computed inside the scan (sd_plan_score, same results) unless
-StepConfig.plan_in_scan is False; with StepConfig.fused the scan and the top-k
-run as one call instead (sd_score_topk, same results).
+StepConfig.plan_in_scan is False, and the scan also writes each 32-token word's
+maximum score, from which sd_topk_wmax draws the same top-k as sd_topk unless
+StepConfig.wmax is False; with StepConfig.fused the scan and the top-k run as one
+call instead (sd_score_topk, same results).
 """
 from __future__ import annotations
 
@@ -24,7 +26,7 @@ from . import (SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_S
                SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
                sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_plan_score,
                sd_score, sd_score_topk, sd_score_topk_workspace_size, sd_topk,
-               sd_topk_workspace_size)
+               sd_topk_wmax, sd_topk_workspace_size)
 
 KIND_NAMES = {SD_IDX_SIG: "hamming", SD_IDX_PLANES: "planes", SD_IDX_MINMAX: "quest"}
 
@@ -44,6 +46,7 @@ class StepConfig:
     budget: int = 56          # bits per token per KV head (water-filling) or r (fixed)
     fused: bool = False       # bit planes: scan and top-k in one call (sd_score_topk)
     plan_in_scan: bool = True  # bit planes: the plan computed by the scan (sd_plan_score)
+    wmax: bool = True         # bit planes with plan_in_scan: word maxima -> sd_topk_wmax
 
     @property
     def block(self) -> int:
@@ -106,6 +109,9 @@ class DecodeStep:
         tws = sd_topk_workspace_size(self.rows, c.n_units, self.sel)
         self.topk_ws = torch.empty(tws, dtype=torch.uint8, device=dev) if tws else None
         self.fused = c.fused and c.kind == SD_IDX_PLANES
+        self.use_wmax = (c.kind == SD_IDX_PLANES and c.plan_in_scan and c.wmax and not self.fused)
+        self.wmax = (torch.empty((self.rows, c.n // 32), dtype=torch.float32, device=dev)
+                     if self.use_wmax else None)
         if self.fused:
             fws = sd_score_topk_workspace_size(self.shape, self.sel)
             self.fused_ws = torch.empty(max(fws, 256), dtype=torch.uint8, device=dev)
@@ -134,6 +140,10 @@ class DecodeStep:
 
     def stage_topk(self, stream=None):
         c = self.cfg
+        if self.use_wmax:
+            sd_topk_wmax(self.scores, self.wmax, self.rows, c.n, self.sel, self.idx, c.max_count,
+                         self.count, self.topk_ws, stream)
+            return
         st = SD_SCORE_I32 if c.kind == SD_IDX_SIG else SD_SCORE_F32
         sd_topk(st, self.scores, self.rows, c.n_units, c.n, self.sel, self.idx, c.max_count,
                 self.count, self.topk_ws, stream)
@@ -143,7 +153,7 @@ class DecodeStep:
         as stage_prep followed by stage_score)."""
         c, ix = self.cfg, self.index
         sd_plan_score(self.shape, ix["planes"], ix["scales"], q, self.sigma2, c.plan_mode,
-                      c.budget, self.plan, self.scores, stream)
+                      c.budget, self.plan, self.scores, self.wmax, stream)
 
     def stage_score_topk(self, q, stream=None):
         """Bit planes: the scan and the top-k in one call (same results as
