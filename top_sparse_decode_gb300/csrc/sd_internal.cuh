@@ -76,6 +76,10 @@ int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* s
                         const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st,
                         const PsCand* cand = nullptr, const PsPlanIn* plan_in = nullptr,
                         float* wmax = nullptr);
+int launch_score_planes_tma(const Dims& s, const uint32_t* planes, const uint16_t* scales,
+                            const uint8_t* plan, const uint16_t* q, float* scores,
+                            const PsCand* cand, const PsPlanIn* plan_in, float* wmax, int sms,
+                            cudaStream_t st);
 int launch_score_quest(const Dims& s, const uint16_t* summ, const uint16_t* q, float* scores,
                        cudaStream_t st);
 size_t topk_workspace_bytes(int64_t rows, int64_t n_units, const sd_select& sel);

@@ -28,54 +28,50 @@ struct PsRow {
   int nact, nch;
 };
 
-// The read plan of one row computed by a group of kD threads (thread t: channel
-// j = t and its pairs (j, 0..3)), with the same arithmetic and tie order as
-// plan_kernel (sd_plan.cu): the budget largest pairs w_j * 4^-b, ties to the
-// lower 4j + b (water-filling), the budget channels of largest sigma2 (fixed), or
-// 4 bits everywhere (full).  Returns channel t's bits.  sums: 2 * (kD / 32) words
-// of shared memory; bar() synchronises the group (threads t >= kD hold no keys).
-template <int G, class Bar>
-__device__ __forceinline__ int ps_plan_row(int t, const uint16_t* __restrict__ q,
-                                           const float* __restrict__ sigma2, int b, int h,
-                                           int Hq, int mode, int budget, int* sums, Bar bar) {
-  constexpr int NW = kD / 32;
-  const int lane = t & 31, warp = t >> 5;
-  if (mode == SD_PLAN_FULL) return 4;
-  const int nkeys = (mode == SD_PLAN_FIXED ? 1 : 4) * kD;
-  if (budget >= nkeys) return 4;
-  if (budget <= 0) return 0;
-  const int npairs = t >= kD ? 0 : (mode == SD_PLAN_FIXED ? 1 : 4);  // keys of this thread
-  if (t >= kD) t = 0;  // (loads in bounds; its keys are not counted)
-  uint32_t key[4] = {0u, 0u, 0u, 0u};
-  if (mode == SD_PLAN_FIXED) {
-    key[0] = key_of_f32(sigma2[(int64_t)h * kD + t]);
-  } else {
-    float acc = 0.0f;  // gains in fp32, group sum in ascending g, no fused multiply-add
+// The read plan of one row, computed by one warp with the same arithmetic and tie
+// order as plan_kernel (sd_plan.cu): the budget largest pairs w_j * 4^-b, ties to
+// the lower 4j + b (water-filling), the budget channels of largest sigma2 (fixed),
+// or 4 bits everywhere (full).  Lane l holds channels 4 l .. 4 l + 3 and their pairs
+// (j, 0..3) -- pairs 16 l .. 16 l + 15 in pair order -- so every count is a warp
+// reduction.  Writes tb[j] (shared memory) for every channel.
+template <int G>
+__device__ __forceinline__ void ps_plan_row_warp(int lane, const uint16_t* __restrict__ q,
+                                                 const float* __restrict__ sigma2, int b, int h,
+                                                 int Hq, int mode, int budget, int* tb) {
+  const bool fixed = mode == SD_PLAN_FIXED;
+  const int nkeys = (fixed ? 1 : 4) * kD;
+  if (mode == SD_PLAN_FULL || budget >= nkeys || budget <= 0) {
+    const int v = (mode == SD_PLAN_FULL || budget >= nkeys) ? 4 : 0;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float x = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + t]);
-      acc = __fadd_rn(acc, __fmul_rn(x, x));
-    }
-    const float w = __fmul_rn(acc, sigma2[(int64_t)h * kD + t]);
-    const float scale4[4] = {1.0f, 0.25f, 0.0625f, 0.015625f};
-#pragma unroll
-    for (int p = 0; p < 4; ++p) key[p] = key_of_f32(__fmul_rn(w, scale4[p]));
+    for (int c = 0; c < 4; ++c) tb[lane * 4 + c] = v;
+    return;
   }
-  // group-wide count of keys satisfying pred, through two alternating tables
-  int parity = 0;
+  uint32_t key[16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int j = lane * 4 + c;
+    if (fixed) {
+      key[4 * c] = key_of_f32(sigma2[(int64_t)h * kD + j]);
+      key[4 * c + 1] = key[4 * c + 2] = key[4 * c + 3] = 0u;  // not counted
+    } else {
+      float acc = 0.0f;  // gains in fp32, group sum in ascending g, no fused multiply-add
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float x = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]);
+        acc = __fadd_rn(acc, __fmul_rn(x, x));
+      }
+      const float w = __fmul_rn(acc, sigma2[(int64_t)h * kD + j]);
+      const float scale4[4] = {1.0f, 0.25f, 0.0625f, 0.015625f};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) key[4 * c + p] = key_of_f32(__fmul_rn(w, scale4[p]));
+    }
+  }
+  const int per = fixed ? 1 : 4;  // keys per channel that count
   auto count = [&](auto pred) {
-    int c = 0;
+    int n = 0;
 #pragma unroll
-    for (int p = 0; p < 4; ++p) c += p < npairs && pred(key[p]);
-    c = __reduce_add_sync(0xFFFFFFFFu, c);
-    int* tab = sums + parity * NW;
-    parity ^= 1;
-    if (lane == 0 && warp < NW) tab[warp] = c;
-    bar();
-    int tot = 0;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) tot += tab[w];
-    return tot;
+    for (int i = 0; i < 16; ++i) n += ((i & 3) < per) && pred(key[i]);
+    return __reduce_add_sync(0xFFFFFFFFu, n);
   };
   // T: the largest key value with at least `budget` keys >= it
   uint32_t T = 0;
@@ -84,36 +80,36 @@ __device__ __forceinline__ int ps_plan_row(int t, const uint16_t* __restrict__ q
     if (count([&](uint32_t k) { return k >= cand; }) >= budget) T = cand;
   }
   const int above = count([&](uint32_t k) { return k > T; });
-  // rank of each key equal to T among the equal keys, in pair order 4j + p
+  // keys equal to T are taken in pair order until the budget is met
   int eq = 0;
 #pragma unroll
-  for (int p = 0; p < 4; ++p) eq += p < npairs && key[p] == T;
+  for (int i = 0; i < 16; ++i) eq += ((i & 3) < per) && key[i] == T;
   int incl = eq;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += y;
   }
-  int* tab = sums + parity * NW;
-  if (lane == 31 && warp < NW) tab[warp] = incl;
-  bar();
   int before = incl - eq;
-  for (int w = 0; w < warp && w < NW; ++w) before += tab[w];
-  int taken = 0;
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    if (p >= npairs) break;
-    const bool e = key[p] == T;
-    if (key[p] > T || (e && before < budget - above)) ++taken;
-    before += e;
+  for (int c = 0; c < 4; ++c) {
+    int taken = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      if (p >= per) break;
+      const uint32_t k = key[4 * c + p];
+      const bool e = k == T;
+      if (k > T || (e && before < budget - above)) ++taken;
+      before += e;
+    }
+    tb[lane * 4 + c] = fixed ? (taken ? 4 : 0) : taken;
   }
-  return mode == SD_PLAN_FIXED ? (taken ? 4 : 0) : taken;
 }
 
 // Builds R for row bh = b * Hkv + h.  Every thread of the calling group runs it
 // and `bar()` synchronises exactly that group; threads t < kD (t = the thread's
 // index within the group) do the per-channel work, warp t / 32 == 0 the scan.
-// With pl.sigma2 set, the row's plan is computed here (ps_plan_row) instead of
+// With pl.sigma2 set, the row's plan is computed here (ps_plan_row_warp) instead of
 // read from `plan`, and written to pl.out when pl.write.
 struct PsPlanIn {
   const float* sigma2;
@@ -128,10 +124,11 @@ __device__ __noinline__ void ps_build_row(PsRow& R, int t, const uint16_t* __res
                                           bool write_plan = false) {
   const int lane = t & 31;
   int tb = 0;
-  if (pl.sigma2) {  // every thread of the group takes part in the plan's counts
-    tb = ps_plan_row<G>(t, q, pl.sigma2, b, h, Hq, pl.mode, pl.budget,
-                        reinterpret_cast<int*>(R.slot_of), bar);
-    bar();  // slot_of served as the plan's scratch
+  if (pl.sigma2) {  // the plan, by the group's first warp, through slot_of
+    if ((t >> 5) == 0)
+      ps_plan_row_warp<G>(lane, q, pl.sigma2, b, h, Hq, pl.mode, pl.budget, R.slot_of);
+    bar();
+    if (t < kD) tb = R.slot_of[t];
     if (write_plan && t < kD && pl.out) pl.out[bh * kD + t] = (uint8_t)tb;
   }
   if (t < kD) {
@@ -207,5 +204,36 @@ struct PsCand {
   int64_t n32;     // words per row (n / 32)
   int64_t lead, tail;
 };
+
+// Marks this lane's competing scores that reach the row's threshold in the hit
+// masks (warp-collective: every lane of the warp calls it).
+__device__ __forceinline__ void ps_mark(const PsCand& cd, int row, uint32_t T, int64_t tok,
+                                        bool valid, const float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+  const bool all = T == 0;  // key 0 lies below every score's key
+  const float Tf = __uint_as_float((T & 0x80000000u) ? (T & 0x7FFFFFFFu) : ~T);
+  float t[16];  // the maximum of the 32 scores as a tree (depth 5)
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = fmax_nan(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmax_nan(t[i], t[i + w]);
+  const float mx = t[0];
+  // almost every lane lies below the threshold: one compare screens its 32 scores
+  const bool maybe = valid && (all || !(mx < Tf));  // reaches it, or holds a NaN
+  uint32_t hit = 0;
+  bool nan = false;
+  if (maybe) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const bool in = tok + i >= cd.lead && tok + i < cd.tail;
+      nan |= in && v[i] != v[i];
+      if (in && (all || v[i] >= Tf)) hit |= 1u << i;
+    }
+  }
+  if (valid) cd.hits[(int64_t)row * cd.n32 + tok / 32] = hit;  // every word, every call
+  if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) atomicOr(cd.nan + row, 1u);
+}
 
 }  // namespace sd

@@ -165,37 +165,6 @@ __device__ __forceinline__ void nb_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
-// Marks this lane's competing scores that reach the row's threshold in the hit
-// masks (warp-collective: every lane of the warp calls it).
-__device__ __forceinline__ void ps_mark(const PsCand& cd, int row, uint32_t T, int64_t tok,
-                                        bool valid, const float (&v)[32]) {
-  const int lane = threadIdx.x & 31;
-  const bool all = T == 0;  // key 0 lies below every score's key
-  const float Tf = __uint_as_float((T & 0x80000000u) ? (T & 0x7FFFFFFFu) : ~T);
-  float t[16];  // the maximum of the 32 scores as a tree (depth 5)
-#pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = fmax_nan(v[2 * i], v[2 * i + 1]);
-#pragma unroll
-  for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) t[i] = fmax_nan(t[i], t[i + w]);
-  const float mx = t[0];
-  // almost every lane lies below the threshold: one compare screens its 32 scores
-  const bool maybe = valid && (all || !(mx < Tf));  // reaches it, or holds a NaN
-  uint32_t hit = 0;
-  bool nan = false;
-  if (maybe) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const bool in = tok + i >= cd.lead && tok + i < cd.tail;
-      nan |= in && v[i] != v[i];
-      if (in && (all || v[i] >= Tf)) hit |= 1u << i;
-    }
-  }
-  if (valid) cd.hits[(int64_t)row * cd.n32 + tok / 32] = hit;  // every word, every call
-  if (__any_sync(0xFFFFFFFFu, nan) && lane == 0) atomicOr(cd.nan + row, 1u);
-}
-
 // Compute warps: consume slots until the end marker; with CAND, also mark the
 // row's candidates (see PsCand); with wmax, also write each 32-token word's
 // maximum score (NaN if one of them is NaN) to wmax[row][word].
@@ -532,6 +501,11 @@ int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* s
                         const PsCand* cand, const PsPlanIn* plan_in, float* wmax) {
   const bool a16 = planes_aligned(s, planes, scales);
   const PsPlanIn pl = plan_in ? *plan_in : PsPlanIn{};
+  if (a16) {  // the bulk-copy kernel, when every CTA's range meets at most two rows
+    const int rc = launch_score_planes_tma(s, planes, scales, plan, q, scores, cand, plan_in,
+                                           wmax, sm_count(), st);
+    if (rc != 1) return rc;
+  }
   if (cand) {  // the fused scan + top-k path (16-byte aligned layouts only)
     if (!a16) return fail(SD_ERR_INVALID_ARG, "score_planes: candidates need n_cap %% 512 == 0 "
                                               "and 16-byte aligned planes and scales");
