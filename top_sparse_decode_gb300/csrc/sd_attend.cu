@@ -6,9 +6,9 @@
 // Split-n: a CTA handles chunks of kAtChunk selected tokens of one (sequence, KV
 // head) for all G query heads of the group, so every K/V row is read once per
 // group.  Each row is one thread-block cluster of kAtCS CTAs: CTA r takes chunks
-// r, r + kAtCS, ... and keeps a running (m, l, o~) over them; CTA 0 then merges the
-// CTAs' states in rank order over distributed shared memory with the usual
-// rescaling e^{m_r - m}.  (Where that cluster cannot run, CTAs write (m, l, o~)
+// r, r + kAtCS, ... and keeps a running (m, l, o~) over them; then every CTA merges
+// its sixteenth of the outputs over all CTAs' states, in rank order, through
+// distributed shared memory with the usual rescaling e^{m_r - m}.  (Where that cluster cannot run, CTAs write (m, l, o~)
 // partials per chunk and the last CTA of the row, by a ticket, merges them.)
 #include <cooperative_groups.h>
 
@@ -265,7 +265,7 @@ struct AtChunk {
   uint16_t Ks[kAtChunk][kAtPitch];
   uint16_t Vs[kAtChunk][kAtPitch];
   float qs[G][4][kQPitch];
-  float zs[G][kAtChunk];
+  __align__(16) float zt[kAtChunk][G];  // token-major: one row holds every head's value
   float2 ml[G];
   int valid[kAtChunk];
 };
@@ -281,6 +281,8 @@ __device__ __forceinline__ void at_chunk(AtChunk<G>& A, const uint16_t* __restri
       const int64_t tok = ok - 1;
       cp_async16(&A.Ks[r][seg * 8], Kr + tok * kD + seg * 8);
       cp_async16(&A.Vs[r][seg * 8], Vr + tok * kD + seg * 8);
+    } else {  // a skipped row's V is zero, so the P V fold needs no test (its p is 0)
+      *reinterpret_cast<uint4*>(&A.Vs[r][seg * 8]) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   cp_async_wait_all();
@@ -319,19 +321,19 @@ __device__ __forceinline__ void at_chunk(AtChunk<G>& A, const uint16_t* __restri
     }
     if (qq == 0) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) A.zs[g][tt] = ok ? dot[g] * scale : -INFINITY;
+      for (int g = 0; g < G; ++g) A.zt[tt][g] = ok ? dot[g] * scale : -INFINITY;
     }
   }
   __syncthreads();
   {  // per-head chunk max and exponentials: warp w handles heads w, w + 4
     const int warp = t >> 5, lane = t & 31;
     for (int g = warp; g < G; g += 4) {
-      const float z = A.zs[g][lane];
+      const float z = A.zt[lane][g];
       float m = z;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
       const float p = z == -INFINITY ? 0.0f : expf(z - m);
-      A.zs[g][lane] = p;
+      A.zt[lane][g] = p;
       float l = p;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
@@ -394,11 +396,21 @@ attend_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
 #pragma unroll
     for (int g = 0; g < G; ++g) pv[g] = 0.0f;
 #pragma unroll 8
-    for (int r = 0; r < nt; ++r) {
-      if (!A.valid[r]) continue;  // skipped rows were not staged
+    for (int r = 0; r < nt; ++r) {  // skipped rows hold p = 0 and V = 0
       const float v = bf16_to_f32(A.Vs[r][t]);
+      if constexpr (G % 4 == 0) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) pv[g] = fmaf(A.zs[g][r], v, pv[g]);
+        for (int g4 = 0; g4 < G; g4 += 4) {
+          const float4 z4 = *reinterpret_cast<const float4*>(&A.zt[r][g4]);
+          pv[g4] = fmaf(z4.x, v, pv[g4]);
+          pv[g4 + 1] = fmaf(z4.y, v, pv[g4 + 1]);
+          pv[g4 + 2] = fmaf(z4.z, v, pv[g4 + 2]);
+          pv[g4 + 3] = fmaf(z4.w, v, pv[g4 + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; ++g) pv[g] = fmaf(A.zt[r][g], v, pv[g]);
+      }
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -419,33 +431,33 @@ attend_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
     for (int g = 0; g < G; ++g) St.ml[g] = make_float2(mrun[g], lrun[g]);
   }
   cl.sync();
-  if (rank == 0) {  // merge the CTAs' states in rank order
+  // merge: CTA r combines outputs r * 8G .. r * 8G + 8G - 1 (head e / 128, column
+  // e % 128) over every CTA's state, ranks ascending; all loads in flight together
+  if (t < 8 * G) {
+    const int e = rank * 8 * G + t, g = e / kD, col = e % kD;
+    float2 mlr[kAtCS];
+    float orr[kAtCS];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float2 mlr[kAtCS];
-      float orr[kAtCS];
-#pragma unroll
-      for (int r = 0; r < kAtCS; ++r) {  // every rank's loads in flight together
-        const AtState<G>* R = cl.map_shared_rank(&St, r);
-        mlr[r] = R->ml[g];
-        orr[r] = R->o[g][t];
-      }
-      float m = -INFINITY;
-#pragma unroll
-      for (int r = 0; r < kAtCS; ++r) m = fmaxf(m, mlr[r].x);
-      float l = 0.0f, o = 0.0f;
-#pragma unroll
-      for (int r = 0; r < kAtCS; ++r) {
-        const float w = mlr[r].x == -INFINITY ? 0.0f : expf(mlr[r].x - m);
-        l = fmaf(mlr[r].y, w, l);
-        o = fmaf(orr[r], w, o);
-      }
-      const int64_t bq = (int64_t)b * Hq + h * G + g;
-      out[bq * kD + t] = l > 0.0f ? o / l : 0.0f;  // an empty set gives o = 0
-      if (lse && t == 0) lse[bq] = l > 0.0f ? m + logf(l) : -INFINITY;
+    for (int r = 0; r < kAtCS; ++r) {
+      const AtState<G>* R = cl.map_shared_rank(&St, r);
+      mlr[r] = R->ml[g];
+      orr[r] = R->o[g][col];
     }
+    float m = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kAtCS; ++r) m = fmaxf(m, mlr[r].x);
+    float l = 0.0f, o = 0.0f;
+#pragma unroll
+    for (int r = 0; r < kAtCS; ++r) {
+      const float w = mlr[r].x == -INFINITY ? 0.0f : expf(mlr[r].x - m);
+      l = fmaf(mlr[r].y, w, l);
+      o = fmaf(orr[r], w, o);
+    }
+    const int64_t bq = (int64_t)b * Hq + h * G + g;
+    out[bq * kD + col] = l > 0.0f ? o / l : 0.0f;  // an empty set gives o = 0
+    if (lse && col == 0) lse[bq] = l > 0.0f ? m + logf(l) : -INFINITY;
   }
-  cl.sync();  // every CTA's state stays alive until CTA 0 has read it
+  cl.sync();  // every CTA's state stays alive until the others have read it
 }
 
 // Whether the cluster kernel can run on this device (cached per device).
