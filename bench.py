@@ -197,13 +197,13 @@ def scan_traffic(workload: str):
     """DRAM bytes per launch of the scan kernel from the committed ncu summary,
     or None when the kernel source changed since that capture."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "score_planes_longctx-262k.md")
-    src = os.path.join(ROOT, "top_sparse_decode_gb300", "csrc", "sd_score.cu")
+    prof = os.path.join(ROOT, "profiles", "score_planes_tma_longctx-262k.md")
+    src = os.path.join(ROOT, "top_sparse_decode_gb300", "csrc", "sd_scan_tma.cu")
     if not (os.path.exists(prof) and os.path.exists(src)):
         return None
     text = open(prof).read()
     code = open(src).read()
-    i, j = code.find("// Bit-plane prefix scan."), code.find("static int sm_count()")
+    i, j = code.find("namespace sd {"), code.find("int launch_score_planes_tma(")
     if i < 0 or j < i:
         return None
     sha = hashlib.sha256(code[i:j].encode()).hexdigest()  # the scan's device code
@@ -491,14 +491,14 @@ def main():
         "stages_in_step_us": marginal,
         # the scan is bound by one bit test and one predicated FP32 add per planned
         # token-plane: the peak is the FP32 pipe (128 lanes per SM per clock)
-        "roofline": {"bound": "alu", "kernel": "score_planes_kernel",
+        "roofline": {"bound": "alu", "kernel": "score_planes_tma_kernel",
                      "achieved": alu_ops / (st_score * 1e-3) / 1e12,
                      "peak": alu_peak / 1e12, "unit": "T token-planes/s",
                      "frac": alu_ops / (st_score * 1e-3) / alu_peak,
                      "traffic": scan_traffic("longctx-1m") if n == 1048576 else None,
                      "ops_per_launch": alu_ops, "alg_bytes_per_launch": scan_bytes,
                      "peak_kind": "derived: 152 SMs x 128 FP32 lanes x median SM clock"},
-        "roofline_hbm": {"bound": "hbm", "kernel": "score_planes_kernel",
+        "roofline_hbm": {"bound": "hbm", "kernel": "score_planes_tma_kernel",
                          "achieved": scan_gbs, "peak": peak_gbs, "unit": "GB/s",
                          "frac": scan_gbs / peak_gbs, "peak_kind": peak_kind,
                          "alg_bytes_per_launch": scan_bytes},
