@@ -366,6 +366,8 @@ def main():
     st_score = statistics.mean(timed_steps(torch, lambda: step.stage_score(q), K_st, 3, flush))
     st_topk = statistics.mean(timed_steps(torch, lambda: step.stage_topk(), K_st, 3, flush))
     st_att = statistics.mean(timed_steps(torch, lambda: step.stage_attend(q), K_st, 3, flush))
+    st_sa = (statistics.mean(timed_steps(torch, lambda: step.stage_select_attend(q), K_st, 3, flush))
+             if step.use_sa else None)
     st_fused = (statistics.mean(timed_steps(torch, lambda: step.stage_score_topk(q), K_st, 3,
                                             flush)) if step.fused else None)
     st_plan_scan = statistics.mean(timed_steps(torch, lambda: step.stage_plan_score(q), K_st, 3,
@@ -487,7 +489,9 @@ def main():
         "stages_us": {"plan": st_prep * 1e3, "scan": st_score * 1e3, "topk": st_topk * 1e3,
                       "scan_topk": None if st_fused is None else st_fused * 1e3,
                       "plan_scan": st_plan_scan * 1e3,
-                      "gather_attend": st_att * 1e3, "step_eager": eager * 1e3},
+                      "gather_attend": st_att * 1e3,
+                      "select_attend": None if st_sa is None else st_sa * 1e3,
+                      "step_eager": eager * 1e3},
         "stages_in_step_us": marginal,
         # the scan is bound by one bit test and one predicated FP32 add per planned
         # token-plane: the peak is the FP32 pipe (128 lanes per SM per clock)

@@ -200,6 +200,30 @@ int sd_topk_wmax(const float* scores, const float* wmax, int64_t rows, int64_t n
                  void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * sd_select_attend -- sd_topk_wmax then sd_gather_attend on its result (HashAttention
+ * 2.1: TOPK then GATHER-ATT; 2.5: page size 1), in one launch where one 16-CTA
+ * thread-block cluster per row can run both: the same idx, count, out and lse as
+ * the two calls (the selection and the attention run the same device code, with a
+ * cluster barrier between them in place of a kernel boundary).
+ *   scores, wmax, sel: as sd_topk_wmax with rows = B * Hkv and n = shape->n;
+ *   q, K, V, scale, out, lse: as sd_gather_attend; idx [rows][idx_stride] and
+ *   count [rows] receive the selection, as from sd_topk_wmax;
+ *   max_count: as sd_gather_attend, with min(n, sink + local + k) <= max_count <=
+ *   idx_stride.
+ *   workspace: device, at least sd_select_attend_workspace_size(shape, sel,
+ *   max_count) bytes (the two calls' workspaces, used where the fused launch does
+ *   not apply).
+ * Errors: those of the two calls.
+ */
+size_t sd_select_attend_workspace_size(const sd_shape* shape, const sd_select* sel,
+                                       int64_t max_count);
+int sd_select_attend(const sd_shape* shape, const float* scores, const float* wmax,
+                     const sd_select* sel, const void* q, const void* K, const void* V,
+                     float scale, int32_t* idx, int64_t idx_stride, int32_t* count,
+                     int64_t max_count, float* out, float* lse, void* workspace,
+                     size_t ws_bytes, void* stream);
+
+/*
  * sd_score_topk -- sd_score(SD_IDX_PLANES) then sd_topk(SD_SCORE_F32) on those
  * scores, in one call (Fathom's bit-plane scan feeding HashAttention 2.1's TOPK):
  * writes exactly the scores, idx and count the two calls would.

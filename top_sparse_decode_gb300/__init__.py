@@ -29,6 +29,7 @@ __all__ = [
     "sd_gather_attend_noalloc", "sd_offload_gather",
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
     "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax",
+    "sd_select_attend_workspace_size", "sd_select_attend",
 ]
 
 
@@ -150,6 +151,22 @@ def sd_topk_wmax(scores, wmax, rows: int, n: int, sel: SdSelect, idx, idx_stride
     _check(lib().sd_topk_wmax(_ptr(scores), _ptr(wmax), rows, n, ctypes.byref(sel), _ptr(idx),
                               idx_stride, _ptr(count), _ptr(workspace), ws_bytes,
                               _stream(stream)), "sd_topk_wmax")
+
+
+def sd_select_attend_workspace_size(shape: SdShape, sel: SdSelect, max_count: int) -> int:
+    return int(lib().sd_select_attend_workspace_size(ctypes.byref(shape), ctypes.byref(sel),
+                                                     max_count))
+
+
+def sd_select_attend(shape: SdShape, scores, wmax, sel: SdSelect, q, K, V, scale: float, idx,
+                     idx_stride: int, count, max_count: int, out, lse=None, workspace=None,
+                     stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().sd_select_attend(ctypes.byref(shape), _ptr(scores), _ptr(wmax),
+                                  ctypes.byref(sel), _ptr(q), _ptr(K), _ptr(V), float(scale),
+                                  _ptr(idx), idx_stride, _ptr(count), max_count, _ptr(out),
+                                  _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)),
+           "sd_select_attend")
 
 
 def sd_score_topk_workspace_size(shape: SdShape, sel: SdSelect) -> int:

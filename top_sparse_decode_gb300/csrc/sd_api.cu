@@ -336,6 +336,55 @@ int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const 
                               (cudaStream_t)stream);
 }
 
+size_t sd_select_attend_workspace_size(const sd_shape* shape, const sd_select* sel,
+                                       int64_t max_count) {
+  Dims s;
+  if (check_shape(shape, &s) || !sel || max_count < 0) return 0;
+  return select_attend_workspace_bytes(s, *sel, max_count);
+}
+
+int sd_select_attend(const sd_shape* shape, const float* scores, const float* wmax,
+                     const sd_select* sel, const void* q, const void* K, const void* V,
+                     float scale, int32_t* idx, int64_t idx_stride, int32_t* count,
+                     int64_t max_count, float* out, float* lse, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s);
+  if (rc) return rc;
+  if (!scores || !wmax || !q || !K || !V || !idx || !count || !out)
+    return fail(SD_ERR_INVALID_ARG, "sd_select_attend: NULL input");
+  if (!sel || sel->block != 1)
+    return fail(SD_ERR_INVALID_ARG, "sd_select_attend: sel is NULL or sel.block != 1");
+  const int64_t n = s.n, rows = (int64_t)s.B * s.Hkv;
+  if (n < 32 || n % 32)
+    return fail(SD_ERR_INVALID_ARG, "sd_select_attend: n = %lld is not a positive multiple of 32",
+                (long long)n);
+  if (!aligned16(scores) || (uintptr_t)wmax % 4)
+    return fail(SD_ERR_INVALID_ARG,
+                "sd_select_attend: scores must be 16-byte, wmax 4-byte aligned");
+  if (!aligned16(K) || !aligned16(V))
+    return fail(SD_ERR_INVALID_ARG, "sd_select_attend: K and V must be 16-byte aligned");
+  if (sel->k < 1 || sel->k > kMaxTopK)
+    return fail(SD_ERR_UNSUPPORTED, "sd_select_attend: k = %d outside [1, %d]", sel->k, kMaxTopK);
+  if (sel->sink < 0 || sel->local < 0)
+    return fail(SD_ERR_INVALID_ARG, "sd_select_attend: negative window");
+  const int64_t max_units = n < (int64_t)sel->sink + sel->local + sel->k
+                                ? n : (int64_t)sel->sink + sel->local + sel->k;
+  if (idx_stride < max_units || max_count < max_units || idx_stride < max_count)
+    return fail(SD_ERR_INVALID_ARG,
+                "sd_select_attend: need idx_stride >= max_count >= %lld (got %lld, %lld)",
+                (long long)max_units, (long long)idx_stride, (long long)max_count);
+  if (n > kSmallRow && rows > 65535)
+    return fail(SD_ERR_UNSUPPORTED, "sd_select_attend: more than 65535 rows of over %d units",
+                kSmallRow);
+  const size_t need = select_attend_workspace_bytes(s, *sel, max_count);
+  if (need && (!workspace || ws_bytes < need))
+    return fail(SD_ERR_WORKSPACE, "sd_select_attend: workspace %zu < %zu bytes", ws_bytes, need);
+  return launch_select_attend(s, scores, wmax, *sel, (const uint16_t*)q, (const uint16_t*)K,
+                              (const uint16_t*)V, scale, idx, idx_stride, count, max_count, out,
+                              lse, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
 int sd_offload_gather(const sd_shape* shape, const uint32_t* host_planes,
                       const uint16_t* host_scales, const uint8_t* plan, uint32_t* dev_planes,
                       uint16_t* dev_scales, void* stream) {

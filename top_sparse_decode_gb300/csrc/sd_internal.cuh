@@ -100,6 +100,12 @@ int launch_gather_attend(const Dims& s, const uint16_t* q, const uint16_t* K, co
                          const int32_t* idx, int64_t idx_stride, const int32_t* count,
                          int64_t max_count, float scale, float* out, float* lse, void* ws,
                          size_t ws_bytes, cudaStream_t st);
+size_t select_attend_workspace_bytes(const Dims& s, const sd_select& sel, int64_t max_count);
+int launch_select_attend(const Dims& s, const float* scores, const float* wmax,
+                         const sd_select& sel, const uint16_t* q, const uint16_t* K,
+                         const uint16_t* V, float scale, int32_t* idx, int64_t idx_stride,
+                         int32_t* count, int64_t max_count, float* out, float* lse, void* ws,
+                         size_t ws_bytes, cudaStream_t st);
 int launch_offload_gather(const Dims& s, const uint32_t* host_planes, const uint16_t* host_scales,
                           const uint8_t* plan, uint32_t* dev_planes, uint16_t* dev_scales,
                           cudaStream_t st);

@@ -27,7 +27,7 @@
 
 #include <cmath>
 
-#include "sd_internal.cuh"
+#include "sd_attend.cuh"
 #include "sd_planes.cuh"
 
 namespace sd {
@@ -1682,14 +1682,15 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// The selection of one row by its cluster (every thread of every CTA runs it; CTAs
+// leave it at different points: mode 0 after writing their share, mode 2 at once,
+// mode 1 all but CTA 0 at once and CTA 0 after the exact path).
 template <int CS>
-__global__ void __launch_bounds__(kWcThreads, 2)
-topk_wmax_cluster_kernel(const float* __restrict__ scores, const float* __restrict__ wmax, Geo g,
-                         int32_t* __restrict__ idx, int64_t idx_stride,
-                         int32_t* __restrict__ count) {
+__device__ __forceinline__ void wc_select(WcSmem& S, const float* __restrict__ scores,
+                                          const float* __restrict__ wmax, const Geo& g,
+                                          int32_t* __restrict__ idx, int64_t idx_stride,
+                                          int32_t* __restrict__ count) {
   constexpr int NT = kWcThreads;
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  WcSmem& S = *reinterpret_cast<WcSmem*>(smem_raw);
   cg::cluster_group cl = cg::this_cluster();
   const int rank = (int)cl.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1972,6 +1973,45 @@ topk_wmax_cluster_kernel(const float* __restrict__ scores, const float* __restri
   write_units<NT>(g, sel, nsel, idx_row, count + row);
 }
 
+
+template <int CS>
+__global__ void __launch_bounds__(kWcThreads, 2)
+topk_wmax_cluster_kernel(const float* __restrict__ scores, const float* __restrict__ wmax, Geo g,
+                         int32_t* __restrict__ idx, int64_t idx_stride,
+                         int32_t* __restrict__ count) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  wc_select<CS>(*reinterpret_cast<WcSmem*>(smem_raw), scores, wmax, g, idx, idx_stride, count);
+}
+
+// sd_select_attend: the selection above, then gather-attend over the selected rows
+// in the same 16-CTA cluster (at_cluster_row, as attend_cluster_kernel runs it, on
+// threads 0..127 of each CTA), with one cluster barrier between them instead of a
+// kernel boundary.  The attention's staging reuses the selection's buffers.
+template <int G>
+__global__ void __launch_bounds__(kWcThreads, 2)
+select_attend_kernel(const float* __restrict__ scores, const float* __restrict__ wmax, Geo g,
+                     int32_t* __restrict__ idx, int64_t idx_stride, int32_t* __restrict__ count,
+                     const uint16_t* __restrict__ q, const uint16_t* __restrict__ K,
+                     const uint16_t* __restrict__ V, int Hq, int Hkv, int64_t n_tok,
+                     int64_t ncap, int max_count, float scale, float* __restrict__ out,
+                     float* __restrict__ lse) {
+  static_assert(sizeof(AtChunk<G>) <= sizeof(WcSmem::gb) && sizeof(AtState<G>) <= sizeof(WcSmem::lc),
+                "attention buffers must fit in the selection's");
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  WcSmem& S = *reinterpret_cast<WcSmem*>(smem_raw);
+  wc_select<kAtCS>(S, scores, wmax, g, idx, idx_stride, count);
+  cg::cluster_group cl = cg::this_cluster();
+  cl.sync();  // every CTA's idx and count writes are visible cluster-wide
+  if (threadIdx.x < 128) {
+    at_cluster_row<G>(*reinterpret_cast<AtChunk<G>*>(&S.gb[0]),
+                      *reinterpret_cast<AtState<G>*>(&S.lc[0]), blockIdx.y, q, K, V, idx,
+                      idx_stride, count, Hq, Hkv, n_tok, ncap, max_count, scale, out, lse,
+                      [] { asm volatile("bar.sync 5, 128;\n" ::: "memory"); });
+  } else {  // the body's two cluster barriers
+    cl.sync();
+    cl.sync();
+  }
+}
 
 // Resident clusters of CS CTAs of topk_wmax_cluster_kernel (0: cannot run), per device.
 template <int CS>
@@ -2295,6 +2335,109 @@ int launch_score_topk(const Dims& s, const uint32_t* planes, const uint16_t* sca
                                                                 idx, idx_stride, count);
   note_launches(1);
   return check_launch("topk marked");
+}
+
+}  // namespace sd
+
+namespace sd {
+
+// Resident 16-CTA clusters of select_attend_kernel<G> (0: cannot run), per device.
+template <int G>
+static int select_attend_capacity() {
+  static int cap[64];
+  static bool known[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!known[dev]) {
+    auto kern = select_attend_kernel<G>;
+    int nc = 0;
+    bool yes = set_smem_limit((const void*)kern, sizeof(WcSmem), "select_attend") == SD_OK &&
+               cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                   cudaSuccess;
+    if (yes) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kAtCS, 1, 1);
+      cfg.blockDim = dim3(kWcThreads, 1, 1);
+      cfg.dynamicSmemBytes = sizeof(WcSmem);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kAtCS;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
+    }
+    cudaGetLastError();
+    cap[dev] = nc;
+    known[dev] = true;
+  }
+  return cap[dev];
+}
+
+template <int G>
+static int launch_select_attend_g(const Dims& s, const float* scores, const float* wmax, Geo g,
+                                  const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                                  float scale, int32_t* idx, int64_t idx_stride, int32_t* count,
+                                  int64_t max_count, float* out, float* lse, int64_t rows,
+                                  bool* launched, cudaStream_t st) {
+  *launched = false;
+  if (rows > select_attend_capacity<G>()) return SD_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kAtCS, (unsigned)rows, 1);
+  cfg.blockDim = dim3(kWcThreads, 1, 1);
+  cfg.dynamicSmemBytes = sizeof(WcSmem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kAtCS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  *launched = true;
+  if (cudaLaunchKernelEx(&cfg, select_attend_kernel<G>, scores, wmax, g, idx, idx_stride, count,
+                         q, K, V, s.Hq, s.Hkv, s.n, s.ncap, (int)max_count, scale, out,
+                         lse) != cudaSuccess)
+    return check_launch("select_attend");
+  note_launches(1);
+  return check_launch("select_attend");
+}
+
+size_t select_attend_workspace_bytes(const Dims& s, const sd_select& sel, int64_t max_count) {
+  const size_t t = topk_workspace_bytes((int64_t)s.B * s.Hkv, s.n, sel);
+  return ((t + 255) & ~(size_t)255) + attend_workspace_bytes(s, max_count);
+}
+
+int launch_select_attend(const Dims& s, const float* scores, const float* wmax,
+                         const sd_select& sel, const uint16_t* q, const uint16_t* K,
+                         const uint16_t* V, float scale, int32_t* idx, int64_t idx_stride,
+                         int32_t* count, int64_t max_count, float* out, float* lse, void* ws,
+                         size_t ws_bytes, cudaStream_t st) {
+  const int64_t rows = (int64_t)s.B * s.Hkv, n = s.n;
+  Geo g = make_geo(n, n, sel);
+  const int64_t W = g.M > 0 ? ((g.tail - 1) >> 5) - (g.lead >> 5) + 1 : 0;
+  if (n > kSmallRow && g.M > g.k && g.k <= kWmMaxK && W <= kWmWords && W > g.k &&
+      W >= 64 * 16 && n <= (1 << 21) && rows <= 65535 && max_count <= (1 << 30) &&
+      (uintptr_t)scores % 16 == 0) {
+    g.r_sample = sample_rank(g.k, imin64(W, kWmSample), W);
+    bool launched = false;
+    int rc = SD_OK;
+    switch (s.G) {
+      case 1: rc = launch_select_attend_g<1>(s, scores, wmax, g, q, K, V, scale, idx, idx_stride, count, max_count, out, lse, rows, &launched, st); break;
+      case 2: rc = launch_select_attend_g<2>(s, scores, wmax, g, q, K, V, scale, idx, idx_stride, count, max_count, out, lse, rows, &launched, st); break;
+      case 4: rc = launch_select_attend_g<4>(s, scores, wmax, g, q, K, V, scale, idx, idx_stride, count, max_count, out, lse, rows, &launched, st); break;
+      default: rc = launch_select_attend_g<8>(s, scores, wmax, g, q, K, V, scale, idx, idx_stride, count, max_count, out, lse, rows, &launched, st); break;
+    }
+    if (launched || rc != SD_OK) return rc;
+  }
+  // the two calls
+  const size_t t = topk_workspace_bytes(rows, n, sel), ta = (t + 255) & ~(size_t)255;
+  if (int rc = launch_topk_wmax(scores, wmax, rows, n, sel, idx, idx_stride, count, ws, t, st))
+    return rc;
+  return launch_gather_attend(s, q, K, V, idx, idx_stride, count, max_count, scale, out, lse,
+                              ws ? (uint8_t*)ws + ta : nullptr, ws_bytes > ta ? ws_bytes - ta : 0,
+                              st);
 }
 
 }  // namespace sd

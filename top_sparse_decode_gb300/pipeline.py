@@ -11,8 +11,10 @@ HashAttention: Semantic Sparsity for Faster Inference, 2.5.  For bit planes the
 read plan is computed inside the scan (sd_plan_score, same results) unless
 StepConfig.plan_in_scan is False, and the scan also writes each 32-token word's
 maximum score, from which sd_topk_wmax draws the same top-k as sd_topk unless
-StepConfig.wmax is False; with StepConfig.fused the scan and the top-k run as one
-call instead (sd_score_topk, same results).
+StepConfig.wmax is False (with StepConfig.select_attend the top-k and the
+gather-attend then run as one call, sd_select_attend, same results); with
+StepConfig.fused the scan and the top-k run as one call instead (sd_score_topk,
+same results).
 """
 from __future__ import annotations
 
@@ -26,7 +28,8 @@ from . import (SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_S
                SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
                sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_plan_score,
                sd_score, sd_score_topk, sd_score_topk_workspace_size, sd_topk,
-               sd_topk_wmax, sd_topk_workspace_size)
+               sd_select_attend, sd_select_attend_workspace_size, sd_topk_wmax,
+               sd_topk_workspace_size)
 
 KIND_NAMES = {SD_IDX_SIG: "hamming", SD_IDX_PLANES: "planes", SD_IDX_MINMAX: "quest"}
 
@@ -47,6 +50,7 @@ class StepConfig:
     fused: bool = False       # bit planes: scan and top-k in one call (sd_score_topk)
     plan_in_scan: bool = True  # bit planes: the plan computed by the scan (sd_plan_score)
     wmax: bool = True         # bit planes with plan_in_scan: word maxima -> sd_topk_wmax
+    select_attend: bool = False  # with wmax: top-k and gather-attend in one call
 
     @property
     def block(self) -> int:
@@ -117,6 +121,10 @@ class DecodeStep:
             self.fused_ws = torch.empty(max(fws, 256), dtype=torch.uint8, device=dev)
         aws = sd_gather_attend_workspace_size(self.shape, c.max_count)
         self.att_ws = torch.empty(max(aws, 256), dtype=torch.uint8, device=dev)
+        self.use_sa = self.use_wmax and c.select_attend
+        if self.use_sa:
+            sws = sd_select_attend_workspace_size(self.shape, self.sel, c.max_count)
+            self.sa_ws = torch.empty(max(sws, 256), dtype=torch.uint8, device=dev)
         self.out = torch.empty((c.B, c.Hq, c.d), dtype=torch.float32, device=dev)
         self.lse = torch.empty((c.B, c.Hq), dtype=torch.float32, device=dev)
 
@@ -168,12 +176,23 @@ class DecodeStep:
         sd_gather_attend(self.shape, q, self.K, self.V, self.idx, c.max_count, self.count,
                          c.max_count, self.scale, self.out, self.lse, self.att_ws, stream)
 
+    def stage_select_attend(self, q, stream=None):
+        """Bit planes with word maxima: the top-k and gather-attend in one call (same
+        idx, count, out and lse as stage_topk followed by stage_attend)."""
+        c = self.cfg
+        sd_select_attend(self.shape, self.scores, self.wmax, self.sel, q, self.K, self.V,
+                         self.scale, self.idx, c.max_count, self.count, c.max_count, self.out,
+                         self.lse, self.sa_ws, stream)
+
     def stages(self):
         """(name, fn(q, stream)) of the step's stages in call order."""
         topk = ("topk", lambda q, stream=None: self.stage_topk(stream))
         if self.fused:
             return [("plan", self.stage_prep), ("scan_topk", self.stage_score_topk),
                     ("gather_attend", self.stage_attend)]
+        if self.use_sa:
+            return [("plan_scan", self.stage_plan_score),
+                    ("select_attend", self.stage_select_attend)]
         if self.cfg.kind == SD_IDX_PLANES and self.cfg.plan_in_scan:
             return [("plan_scan", self.stage_plan_score), topk,
                     ("gather_attend", self.stage_attend)]
