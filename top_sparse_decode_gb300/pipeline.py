@@ -116,6 +116,7 @@ class DecodeStep:
         self.use_wmax = (c.kind == SD_IDX_PLANES and c.plan_in_scan and c.wmax and not self.fused)
         self.wmax = (torch.empty((self.rows, c.n // 32), dtype=torch.float32, device=dev)
                      if self.use_wmax else None)
+        self.wmax_fresh = False  # the last scan wrote the word maxima of self.scores
         if self.fused:
             fws = sd_score_topk_workspace_size(self.shape, self.sel)
             self.fused_ws = torch.empty(max(fws, 256), dtype=torch.uint8, device=dev)
@@ -138,6 +139,7 @@ class DecodeStep:
 
     def stage_score(self, q, stream=None):
         c, ix = self.cfg, self.index
+        self.wmax_fresh = False  # sd_score writes no word maxima
         if c.kind == SD_IDX_SIG:
             sd_score(SD_IDX_SIG, self.shape, ix["sig"], None, self.qsig, None, self.scores, stream)
         elif c.kind == SD_IDX_PLANES:
@@ -148,7 +150,7 @@ class DecodeStep:
 
     def stage_topk(self, stream=None):
         c = self.cfg
-        if self.use_wmax:
+        if self.use_wmax and self.wmax_fresh:
             sd_topk_wmax(self.scores, self.wmax, self.rows, c.n, self.sel, self.idx, c.max_count,
                          self.count, self.topk_ws, stream)
             return
@@ -162,11 +164,13 @@ class DecodeStep:
         c, ix = self.cfg, self.index
         sd_plan_score(self.shape, ix["planes"], ix["scales"], q, self.sigma2, c.plan_mode,
                       c.budget, self.plan, self.scores, self.wmax, stream)
+        self.wmax_fresh = self.wmax is not None
 
     def stage_score_topk(self, q, stream=None):
         """Bit planes: the scan and the top-k in one call (same results as
         stage_score followed by stage_topk)."""
         ix = self.index
+        self.wmax_fresh = False
         sd_score_topk(self.shape, ix["planes"], ix["scales"], q, self.plan, self.sel,
                       self.scores, self.idx, self.cfg.max_count, self.count, self.fused_ws,
                       stream)
@@ -180,6 +184,10 @@ class DecodeStep:
         """Bit planes with word maxima: the top-k and gather-attend in one call (same
         idx, count, out and lse as stage_topk followed by stage_attend)."""
         c = self.cfg
+        if not self.wmax_fresh:
+            self.stage_topk(stream)
+            self.stage_attend(q, stream)
+            return
         sd_select_attend(self.shape, self.scores, self.wmax, self.sel, q, self.K, self.V,
                          self.scale, self.idx, c.max_count, self.count, c.max_count, self.out,
                          self.lse, self.sa_ws, stream)
