@@ -16,10 +16,29 @@
 namespace sd {
 
 // =====================================================================================
-// Hamming scan: 4 B per token per KV head, four tokens per thread (128-bit loads).
+// Hamming scan: 4 B per token per KV head.  A thread takes 16 tokens as four 128-bit
+// loads 1024 tokens apart, all issued before any is used, so every SM keeps enough
+// bytes in flight to cover HBM latency; stores are 128-bit and coalesced alike.
 // =====================================================================================
+constexpr int kHmThreads = 256, kHmPer = 4;  // 128-bit loads per thread
+constexpr int kHmTile = kHmThreads * 4 * kHmPer;  // tokens per CTA (4096)
+
 template <int G>
-__global__ void __launch_bounds__(256)
+__device__ __forceinline__ int4 hm_score4(uint4 s4, const uint32_t (&qs)[G]) {
+  const uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
+  int r[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    int acc = 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g) acc += __popc(sv[k] ^ qs[g]);
+    r[k] = -acc;
+  }
+  return make_int4(r[0], r[1], r[2], r[3]);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kHmThreads)
 score_hamming_kernel(const uint32_t* __restrict__ sig, const uint32_t* __restrict__ qsig,
                      int Hq, int Hkv, int64_t n, int64_t ncap, bool vec,
                      int32_t* __restrict__ scores) {
@@ -30,27 +49,31 @@ score_hamming_kernel(const uint32_t* __restrict__ sig, const uint32_t* __restric
   for (int g = 0; g < G; ++g) qs[g] = __ldg(qsig + (int64_t)b * Hq + h * G + g);
   const uint32_t* srow = sig + bh * ncap;
   int32_t* orow = scores + bh * n;
-  const int64_t i0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  if (i0 >= n) return;
-  if (vec && i0 + 4 <= n) {
-    uint4 s4 = __ldg(reinterpret_cast<const uint4*>(srow + i0));
-    uint32_t sv[4] = {s4.x, s4.y, s4.z, s4.w};
-    int r[4];
+  const int64_t base = (int64_t)blockIdx.x * kHmTile + threadIdx.x * 4;
+  if (vec && (int64_t)blockIdx.x * kHmTile + kHmTile <= n) {  // a whole tile
+    uint4 s4[kHmPer];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      int acc = 0;
+    for (int j = 0; j < kHmPer; ++j)
+      s4[j] = __ldg(reinterpret_cast<const uint4*>(srow + base + j * kHmThreads * 4));
 #pragma unroll
-      for (int g = 0; g < G; ++g) acc += __popc(sv[k] ^ qs[g]);
-      r[k] = -acc;
-    }
-    *reinterpret_cast<int4*>(orow + i0) = make_int4(r[0], r[1], r[2], r[3]);
-  } else {
-    for (int64_t i = i0; i < imin64(i0 + 4, n); ++i) {
-      uint32_t sv = __ldg(srow + i);
-      int acc = 0;
+    for (int j = 0; j < kHmPer; ++j)
+      *reinterpret_cast<int4*>(orow + base + j * kHmThreads * 4) = hm_score4<G>(s4[j], qs);
+    return;
+  }
+  for (int j = 0; j < kHmPer; ++j) {  // the row's last, partial tile
+    const int64_t i0 = base + j * kHmThreads * 4;
+    if (i0 >= n) break;
+    if (vec && i0 + 4 <= n) {
+      *reinterpret_cast<int4*>(orow + i0) =
+          hm_score4<G>(__ldg(reinterpret_cast<const uint4*>(srow + i0)), qs);
+    } else {
+      for (int64_t i = i0; i < imin64(i0 + 4, n); ++i) {
+        const uint32_t sv = __ldg(srow + i);
+        int acc = 0;
 #pragma unroll
-      for (int g = 0; g < G; ++g) acc += __popc(sv ^ qs[g]);
-      orow[i] = -acc;
+        for (int g = 0; g < G; ++g) acc += __popc(sv ^ qs[g]);
+        orow[i] = -acc;
+      }
     }
   }
 }
@@ -59,8 +82,9 @@ template <int G>
 static void hamming_t(const Dims& s, const uint32_t* sig, const uint32_t* qsig, int32_t* out,
                       cudaStream_t st) {
   bool vec = (s.n % 4 == 0) && (s.ncap % 4 == 0);
-  dim3 grid((unsigned)((s.n + 1023) / 1024), (unsigned)(s.B * s.Hkv));
-  score_hamming_kernel<G><<<grid, 256, 0, st>>>(sig, qsig, s.Hq, s.Hkv, s.n, s.ncap, vec, out);
+  dim3 grid((unsigned)((s.n + kHmTile - 1) / kHmTile), (unsigned)(s.B * s.Hkv));
+  score_hamming_kernel<G><<<grid, kHmThreads, 0, st>>>(sig, qsig, s.Hq, s.Hkv, s.n, s.ncap, vec,
+                                                        out);
   note_launches(1);
 }
 
