@@ -200,6 +200,25 @@ int sd_topk_wmax(const float* scores, const float* wmax, int64_t rows, int64_t n
                  void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * sd_hamming_topk -- sd_score(SD_IDX_SIG) then sd_topk(SD_SCORE_I32, sel.block == 1)
+ * without materialising the scores (HashAttention 2.1 SCORE -> TOPK; 2.2 SCORE =
+ * -Hamming over the group's query signatures; 3.1 windows kept, budget apart): the
+ * same idx and count.  Two passes over the signatures: per 8192-token range a
+ * histogram of the 32G + 1 score values, then the exact k-th best value and its
+ * ties (lowest index first) taken range by range in token order.
+ *   sig uint32 [B][Hkv][n_cap], qsig uint32 [B][Hq] (sd_encode_query); sel with
+ *   block == 1; idx int32 [B*Hkv][idx_stride], count int32 [B*Hkv], as sd_topk.
+ *   workspace: device, at least sd_hamming_topk_workspace_size(shape, sel) bytes;
+ *   the call resets the part it needs on the stream.
+ * Errors: SD_ERR_INVALID_ARG, SD_ERR_UNSUPPORTED (k > 4096, more than 2,097,152
+ * competing tokens, more than 65535 rows), SD_ERR_WORKSPACE, SD_ERR_CUDA.
+ */
+size_t sd_hamming_topk_workspace_size(const sd_shape* shape, const sd_select* sel);
+int sd_hamming_topk(const sd_shape* shape, const uint32_t* sig, const uint32_t* qsig,
+                    const sd_select* sel, int32_t* idx, int64_t idx_stride, int32_t* count,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * sd_select_attend -- sd_topk_wmax then sd_gather_attend on its result (HashAttention
  * 2.1: TOPK then GATHER-ATT; 2.5: page size 1), in one launch where one 16-CTA
  * thread-block cluster per row can run both: the same idx, count, out and lse as

@@ -47,6 +47,8 @@ def run_gpu(sd, cfg, inp, kind, plan_mode=0, budget=56, dev_in=None):
     index = build_index(sc, K, enc)
     step = DecodeStep(sc, K, V, index, enc=enc, sigma2=dev(inp.sigma2))
     step.run(q)
+    if step.use_ht:  # the fused Hamming path keeps no scores: score once more to check them
+        step.stage_score(q)
     torch.cuda.synchronize()
     return (sc, host(step.idx, np.int32), host(step.count, np.int32),
             host(step.out, np.float32), host(step.lse, np.float32), step, (q, K, V))

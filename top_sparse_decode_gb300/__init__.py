@@ -29,7 +29,8 @@ __all__ = [
     "sd_gather_attend_noalloc", "sd_offload_gather",
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
     "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax",
-    "sd_select_attend_workspace_size", "sd_select_attend",
+    "sd_select_attend_workspace_size", "sd_select_attend", "sd_hamming_topk_workspace_size",
+    "sd_hamming_topk",
 ]
 
 
@@ -151,6 +152,18 @@ def sd_topk_wmax(scores, wmax, rows: int, n: int, sel: SdSelect, idx, idx_stride
     _check(lib().sd_topk_wmax(_ptr(scores), _ptr(wmax), rows, n, ctypes.byref(sel), _ptr(idx),
                               idx_stride, _ptr(count), _ptr(workspace), ws_bytes,
                               _stream(stream)), "sd_topk_wmax")
+
+
+def sd_hamming_topk_workspace_size(shape: SdShape, sel: SdSelect) -> int:
+    return int(lib().sd_hamming_topk_workspace_size(ctypes.byref(shape), ctypes.byref(sel)))
+
+
+def sd_hamming_topk(shape: SdShape, sig, qsig, sel: SdSelect, idx, idx_stride: int, count,
+                    workspace=None, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().sd_hamming_topk(ctypes.byref(shape), _ptr(sig), _ptr(qsig), ctypes.byref(sel),
+                                 _ptr(idx), idx_stride, _ptr(count), _ptr(workspace), ws_bytes,
+                                 _stream(stream)), "sd_hamming_topk")
 
 
 def sd_select_attend_workspace_size(shape: SdShape, sel: SdSelect, max_count: int) -> int:

@@ -46,6 +46,8 @@ SIGNATURES = {
     "sd_topk": (_i, [_i, _p, _i64, _i64, _i64, _PL, _p, _i64, _p, _p, _sz, _p]),
     "sd_plan_score": (_i, [_PS, _p, _p, _p, _p, _i, _i, _p, _p, _p, _p]),
     "sd_topk_wmax": (_i, [_p, _p, _i64, _i64, _PL, _p, _i64, _p, _p, _sz, _p]),
+    "sd_hamming_topk_workspace_size": (_sz, [_PS, _PL]),
+    "sd_hamming_topk": (_i, [_PS, _p, _p, _PL, _p, _i64, _p, _p, _sz, _p]),
     "sd_select_attend_workspace_size": (_sz, [_PS, _PL, _i64]),
     "sd_select_attend": (_i, [_PS, _p, _p, _PL, _p, _p, _p, ctypes.c_float, _p, _i64, _p, _i64,
                               _p, _p, _p, _sz, _p]),

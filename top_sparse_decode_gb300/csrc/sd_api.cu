@@ -336,6 +336,41 @@ int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const 
                               (cudaStream_t)stream);
 }
 
+size_t sd_hamming_topk_workspace_size(const sd_shape* shape, const sd_select* sel) {
+  Dims s;
+  if (check_shape(shape, &s) || !sel) return 0;
+  return hamming_topk_workspace_bytes(s, *sel);
+}
+
+int sd_hamming_topk(const sd_shape* shape, const uint32_t* sig, const uint32_t* qsig,
+                    const sd_select* sel, int32_t* idx, int64_t idx_stride, int32_t* count,
+                    void* workspace, size_t ws_bytes, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s);
+  if (rc) return rc;
+  if (!sig || !qsig || !sel || !idx || !count)
+    return fail(SD_ERR_INVALID_ARG, "sd_hamming_topk: NULL input");
+  if (sel->block != 1)
+    return fail(SD_ERR_INVALID_ARG, "sd_hamming_topk: sel.block must be 1 (token mode)");
+  if (sel->k < 1 || sel->k > kMaxTopK)
+    return fail(SD_ERR_UNSUPPORTED, "sd_hamming_topk: k = %d outside [1, %d]", sel->k, kMaxTopK);
+  if (sel->sink < 0 || sel->local < 0)
+    return fail(SD_ERR_INVALID_ARG, "sd_hamming_topk: negative window");
+  const int64_t max_units = s.n < (int64_t)sel->sink + sel->local + sel->k
+                                ? s.n : (int64_t)sel->sink + sel->local + sel->k;
+  if (idx_stride < max_units)
+    return fail(SD_ERR_INVALID_ARG, "sd_hamming_topk: idx_stride %lld < %lld",
+                (long long)idx_stride, (long long)max_units);
+  if (!hamming_topk_supported(s, *sel))
+    return fail(SD_ERR_UNSUPPORTED,
+                "sd_hamming_topk: more than 2,097,152 competing tokens or 65535 rows");
+  const size_t need = hamming_topk_workspace_bytes(s, *sel);
+  if (!workspace || ws_bytes < need)
+    return fail(SD_ERR_WORKSPACE, "sd_hamming_topk: workspace %zu < %zu bytes", ws_bytes, need);
+  return launch_hamming_topk(s, sig, qsig, *sel, idx, idx_stride, count, workspace,
+                             (cudaStream_t)stream);
+}
+
 size_t sd_select_attend_workspace_size(const sd_shape* shape, const sd_select* sel,
                                        int64_t max_count) {
   Dims s;

@@ -100,6 +100,11 @@ int launch_gather_attend(const Dims& s, const uint16_t* q, const uint16_t* K, co
                          const int32_t* idx, int64_t idx_stride, const int32_t* count,
                          int64_t max_count, float scale, float* out, float* lse, void* ws,
                          size_t ws_bytes, cudaStream_t st);
+size_t hamming_topk_workspace_bytes(const Dims& s, const sd_select& sel);
+bool hamming_topk_supported(const Dims& s, const sd_select& sel);
+int launch_hamming_topk(const Dims& s, const uint32_t* sig, const uint32_t* qsig,
+                        const sd_select& sel, int32_t* idx, int64_t idx_stride, int32_t* count,
+                        void* ws, cudaStream_t st);
 size_t select_attend_workspace_bytes(const Dims& s, const sd_select& sel, int64_t max_count);
 int launch_select_attend(const Dims& s, const float* scores, const float* wmax,
                          const sd_select& sel, const uint16_t* q, const uint16_t* K,

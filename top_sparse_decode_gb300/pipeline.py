@@ -14,7 +14,9 @@ maximum score, from which sd_topk_wmax draws the same top-k as sd_topk unless
 StepConfig.wmax is False (with StepConfig.select_attend the top-k and the
 gather-attend then run as one call, sd_select_attend, same results); with
 StepConfig.fused the scan and the top-k run as one call instead (sd_score_topk,
-same results).
+same results).  For signatures the scan
+and the top-k run as one call (sd_hamming_topk, same idx and count, no scores)
+unless StepConfig.hamming_fused is False.
 """
 from __future__ import annotations
 
@@ -28,7 +30,8 @@ from . import (SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_S
                SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
                sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_plan_score,
                sd_score, sd_score_topk, sd_score_topk_workspace_size, sd_topk,
-               sd_select_attend, sd_select_attend_workspace_size, sd_topk_wmax,
+               sd_hamming_topk, sd_hamming_topk_workspace_size, sd_select_attend,
+               sd_select_attend_workspace_size, sd_topk_wmax,
                sd_topk_workspace_size)
 
 KIND_NAMES = {SD_IDX_SIG: "hamming", SD_IDX_PLANES: "planes", SD_IDX_MINMAX: "quest"}
@@ -51,6 +54,7 @@ class StepConfig:
     plan_in_scan: bool = True  # bit planes: the plan computed by the scan (sd_plan_score)
     wmax: bool = True         # bit planes with plan_in_scan: word maxima -> sd_topk_wmax
     select_attend: bool = False  # with wmax: top-k and gather-attend in one call
+    hamming_fused: bool = True  # signatures: scan and top-k in one call (sd_hamming_topk)
 
     @property
     def block(self) -> int:
@@ -123,6 +127,10 @@ class DecodeStep:
         aws = sd_gather_attend_workspace_size(self.shape, c.max_count)
         self.att_ws = torch.empty(max(aws, 256), dtype=torch.uint8, device=dev)
         self.use_sa = self.use_wmax and c.select_attend
+        self.use_ht = c.kind == SD_IDX_SIG and c.hamming_fused and c.block == 1
+        if self.use_ht:
+            hws = sd_hamming_topk_workspace_size(self.shape, self.sel)
+            self.ht_ws = torch.empty(max(hws, 256), dtype=torch.uint8, device=dev)
         if self.use_sa:
             sws = sd_select_attend_workspace_size(self.shape, self.sel, c.max_count)
             self.sa_ws = torch.empty(max(sws, 256), dtype=torch.uint8, device=dev)
@@ -180,6 +188,13 @@ class DecodeStep:
         sd_gather_attend(self.shape, q, self.K, self.V, self.idx, c.max_count, self.count,
                          c.max_count, self.scale, self.out, self.lse, self.att_ws, stream)
 
+    def stage_hamming_topk(self, q, stream=None):
+        """Signatures: the scan and the top-k in one call, without scores (same idx
+        and count as stage_score followed by stage_topk)."""
+        c = self.cfg
+        sd_hamming_topk(self.shape, self.index["sig"], self.qsig, self.sel, self.idx,
+                        c.max_count, self.count, self.ht_ws, stream)
+
     def stage_select_attend(self, q, stream=None):
         """Bit planes with word maxima: the top-k and gather-attend in one call (same
         idx, count, out and lse as stage_topk followed by stage_attend)."""
@@ -197,6 +212,9 @@ class DecodeStep:
         topk = ("topk", lambda q, stream=None: self.stage_topk(stream))
         if self.fused:
             return [("plan", self.stage_prep), ("scan_topk", self.stage_score_topk),
+                    ("gather_attend", self.stage_attend)]
+        if self.use_ht:
+            return [("prep", self.stage_prep), ("scan_topk", self.stage_hamming_topk),
                     ("gather_attend", self.stage_attend)]
         if self.use_sa:
             return [("plan_scan", self.stage_plan_score),
