@@ -125,9 +125,7 @@ hamming_hist_kernel(const uint32_t* __restrict__ sig, const uint32_t* __restrict
   for (int j = 0; j < kHtPer; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t bin = min(u[j][e], (uint32_t)kHtBins);  // outside tokens: the spare bin
-      const uint32_t peers = __match_any_sync(0xFFFFFFFFu, bin);
-      if ((tid & 31) == __ffs((int)peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+      atomicAdd(&h[min(u[j][e], (uint32_t)kHtBins)], 1u);  // outside tokens: the spare bin
     }
   __syncthreads();
   uint32_t* hrow = w.hist + (row * g.P + p) * kHtBins;
@@ -170,12 +168,23 @@ hamming_hist_kernel(const uint32_t* __restrict__ sig, const uint32_t* __restrict
   }
   __syncthreads();
   const int us = ustar, nd = need;
-  // per range: ties (u = u*) and sure tokens (u < u*); ranges ascending
+  // per range: ties (u = u*) and sure tokens (u < u*); ranges ascending.  The P x u*
+  // counts below u* are summed by all threads at once (independent loads, shared
+  // atomics per range); h serves as the per-range sums.
+  const int nbu = min(us, nb);
+  for (int i = tid; i < g.P; i += kHtThreads) h[i] = 0;
+  __syncthreads();
+  const uint32_t* hrow0 = w.hist + row * g.P * kHtBins;
+  for (int e = tid; e < g.P * nbu; e += kHtThreads) {
+    const int pp = e / nbu, i = e - pp * nbu;
+    const uint32_t v = __ldcg(hrow0 + pp * kHtBins + i);
+    if (v) atomicAdd(&h[pp], v);
+  }
+  __syncthreads();
   uint32_t ties = 0, sure = 0;
   if (tid < g.P) {
-    const uint32_t* hp = w.hist + (row * g.P + tid) * kHtBins;
-    for (int i = 0; i < us && i < nb; ++i) sure += __ldcg(hp + i);
-    ties = us < nb ? __ldcg(hp + us) : 0u;
+    sure = h[tid];
+    ties = us < nb ? __ldcg(hrow0 + tid * kHtBins + us) : 0u;
   }
   // exclusive prefixes over the ranges (P <= kHtThreads), taking ties in order
   auto scan = [&](uint32_t v) {
