@@ -298,6 +298,95 @@ def run_reference(args, ws, rank):
 
 
 # ------------------------------------------------------------------------------------
+def other_configs(torch, sd, rl, synth, flush, K_st, peak_gbs):
+    """The other 128k-1M-class workloads, each as one decode step (CUDA-graph replay,
+    L2 flushed before every step): the batched 128k-token bit-plane step at budgets
+    47, 56 and 92 bits and reading all planes, the batch-64 Quest block step, and the
+    HashAttention 32k-token step with 2-layer-MLP signatures."""
+    from top_sparse_decode_gb300.pipeline import DecodeStep, StepConfig, build_index
+    out = {}
+
+    def graph_us(fn):
+        g = capture_graph(torch, fn)
+        return statistics.mean(timed_steps(torch, g.replay, K_st, 3, flush)) * 1e3
+
+    # Fathom, batch 4 x 131072 tokens
+    c2 = synth.config(2)
+    inp = synth.make_inputs(c2)
+    q, K, V = dev_tensor(inp.q, torch), dev_tensor(inp.K, torch), dev_tensor(inp.V, torch)
+    s2 = dev_tensor(inp.sigma2, torch)
+    keys = c2.B * c2.Hkv * c2.n
+    res = {}
+    index = None
+    for name, mode, budget in [("47", sd.SD_PLAN_WATERFILL, 47), ("56", sd.SD_PLAN_WATERFILL, 56),
+                               ("92", sd.SD_PLAN_WATERFILL, 92), ("full", sd.SD_PLAN_FULL, 0)]:
+        sc = StepConfig(sd.SD_IDX_PLANES, c2.B, c2.Hq, c2.Hkv, c2.n, k=c2.k, plan_mode=mode,
+                        budget=budget)
+        if index is None:
+            index = build_index(sc, K)
+        st = DecodeStep(sc, K, V, index, sigma2=s2)
+        st.run(q)
+        torch.cuda.synchronize()
+        t_step = graph_us(lambda: st.run(q))
+        t_scan = graph_us(lambda: st.stage_plan_score(q))
+        plan_np = st.plan.cpu().numpy()
+        sb = rl.plane_scan_bytes(plan_np, c2.n)
+        res[name] = {"us_per_step": t_step, "keys_per_s": keys / (t_step * 1e-6),
+                     "plan_scan_us": t_scan, "bits_per_token": rl.plane_scan_bits_per_token(plan_np),
+                     "scan_bytes": sb, "scan_GBps": sb / (t_scan * 1e-6) / 1e9,
+                     "scan_frac_hbm": sb / (t_scan * 1e-6) / 1e9 / peak_gbs,
+                     "token_planes_per_s": rl.plane_scan_alu_ops(plan_np, c2.n) / (t_scan * 1e-6)}
+        del st
+    out["fathom-128k (B=4, n=131072, k=512)"] = res
+    del q, K, V, s2, index, inp
+
+    # Quest, batch 64 x 16384 tokens, top-128 blocks + 1 local block
+    c3 = synth.config(3)
+    inp = synth.make_inputs(c3)
+    q, K, V = dev_tensor(inp.q, torch), dev_tensor(inp.K, torch), dev_tensor(inp.V, torch)
+    sc = StepConfig(sd.SD_IDX_MINMAX, c3.B, c3.Hq, c3.Hkv, c3.n, k=c3.blk_k, local=c3.blk_local)
+    index = build_index(sc, K)
+    st = DecodeStep(sc, K, V, index)
+    st.run(q)
+    torch.cuda.synchronize()
+    t_step = graph_us(lambda: st.run(q))
+    t_scan = graph_us(lambda: st.stage_score(q))
+    t_topk = graph_us(lambda: st.stage_topk())
+    t_att = graph_us(lambda: st.stage_attend(q))
+    sb = rl.quest_scan_bytes(c3.B, c3.Hkv, c3.n)
+    gb = rl.gather_bytes(st.count.cpu().numpy())
+    keys = c3.B * c3.Hkv * c3.n
+    out["quest-b64-16k (B=64, n=16384, 128+1 blocks)"] = {
+        "us_per_step": t_step, "keys_per_s": keys / (t_step * 1e-6),
+        "scan_us": t_scan, "scan_bytes": sb, "scan_GBps": sb / (t_scan * 1e-6) / 1e9,
+        "scan_frac_hbm": sb / (t_scan * 1e-6) / 1e9 / peak_gbs,
+        "topk_us": t_topk, "attend_us": t_att, "gather_bytes": gb,
+        "attend_GBps": gb / (t_att * 1e-6) / 1e9,
+        "attend_frac_hbm": gb / (t_att * 1e-6) / 1e9 / peak_gbs}
+    del st, index, q, K, V, inp
+
+    # HashAttention, 32768 tokens, 2-layer-MLP signatures, 128 + 512 window tokens
+    c1 = synth.config(1)
+    inp = synth.make_inputs(c1)
+    q, K, V = dev_tensor(inp.q, torch), dev_tensor(inp.K, torch), dev_tensor(inp.V, torch)
+    enc = sd.make_encoder(dev_tensor(inp.W1, torch), dev_tensor(inp.b1, torch),
+                          dev_tensor(inp.W2, torch), dev_tensor(inp.b2, torch))
+    sc = StepConfig(sd.SD_IDX_SIG, c1.B, c1.Hq, c1.Hkv, c1.n, k=c1.k, sink=c1.sink,
+                    local=c1.local)
+    index = build_index(sc, K, enc)
+    st = DecodeStep(sc, K, V, index, enc=enc)
+    st.run(q)
+    torch.cuda.synchronize()
+    t_step = graph_us(lambda: st.run(q))
+    keys = c1.B * c1.Hkv * c1.n
+    out["hash-32k (B=1, n=32768, MLP signatures)"] = {
+        "us_per_step": t_step, "keys_per_s": keys / (t_step * 1e-6),
+        "gather_bytes": rl.gather_bytes(st.count.cpu().numpy())}
+    del st, index, q, K, V, inp
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     ws, rank, local = dist_init()
@@ -470,6 +559,10 @@ def main():
                                  "us_per_step": tos * 1e3, "keys_per_s": keys / (tos * 1e-3)}
         del hp, hs, dpl, dsc, sto
 
+    configs = {}
+    if not args.no_variants:
+        configs = other_configs(torch, sd, rl, synth, flush, K_st, peak_gbs)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, cfg)
@@ -517,6 +610,7 @@ def main():
         "gpu_launches": launches_per_step(step, q) * args.steps,
         "clocks": ck,
         "variants": variants,
+        "other_configs": configs,
         "cpu_baseline": cpu,
     }
     if rank == 0:
