@@ -52,7 +52,6 @@ constexpr int kPtCtasPerSm = 2;
 constexpr int kPtRows = 2;               // rows one CTA's range may meet
 constexpr uint32_t kPtSpin = 1u << 22;   // try_wait rounds before a wait gives up
 constexpr int kInfoFirst = 1, kInfoLast = 2, kInfoEnd = 4;
-constexpr int kBarBuild = 1;             // named barriers 1, 2: the builder groups
 
 struct PtRow {                       // one row's tables
   float qp[4 * kD];                  // per planned entry e: q~_j * 2^(3-p)
@@ -79,11 +78,9 @@ struct PtSlot {
 };
 
 struct PtSmem {
-  union {
-    PtSlot slot[kPtSlots];  // 80 KB
-    PsRow build[2];         // the builder groups' scratch, before the pipeline starts
-  };
+  PtSlot slot[kPtSlots];  // 80 KB
   PtRow rows[kPtRows];
+  int tbs[kD];            // the producer's plan scratch
   PtInfo info[kPtSlots];
   unsigned long long full[kPtSlots], empty[kPtSlots];
   int abort;
@@ -146,32 +143,65 @@ __device__ __forceinline__ PtRange pt_range(int upr, int64_t total_units) {
   return r;
 }
 
-// Builder group g (threads 128 g .. 128 g + 127) builds the tables of the range's
-// row bh0 + g into rows[g]; the plan is written by the CTA whose range holds the
-// row's first unit.
+// The producer warp builds row bh's tables into D (lane l: channels 4 l .. 4 l + 3):
+// the plan (computed here, ps_plan_row_warp, or read), the group-summed query q~_j
+// (g ascending), the planned entries (j ascending, then p) with qp_e = q~_j 2^(3-p)
+// and, at p = 0, qo = q~_j (h(t_j) - 8), and each chunk's distinct channels -- the
+// arithmetic of ps_build_row.  The plan is written when write_plan.  Later posts
+// of the row's chunks publish the tables to the compute warps (the slots' barriers
+// order the writes before them).
 template <int G>
-__device__ __forceinline__ void pt_build(PtSmem& S, int g, const uint16_t* __restrict__ q,
-                                         const uint8_t* __restrict__ plan, int Hq, int Hkv,
-                                         const PsPlanIn& pl, const PtRange& rg, int upr) {
-  const int t = threadIdx.x - 128 * g;
-  const int bh = rg.bh0 + g;
-  const bool write_plan = (int64_t)bh * upr >= rg.u_begin;  // the row starts inside the range
-  PsRow& R = S.build[g];
-  auto bar = [g] { asm volatile("bar.sync %0, 128;\n" ::"r"(kBarBuild + g) : "memory"); };
-  ps_build_row<G>(R, t, q, plan, bh / Hkv, bh % Hkv, Hq, (int64_t)bh, bar, pl, write_plan);
-  PtRow& D = S.rows[g];
-  const int nact = R.nact;
-  for (int e = t; e < nact; e += 128) {
-    const int ent = R.act[e];
-    D.qp[e] = R.qp[e];
-    D.qo[e] = (ent & 3) == 0 ? R.qo[R.eslot[e]] : 0.0f;
-    D.act[e] = (uint16_t)ent;
+__device__ __forceinline__ void pt_build_warp(PtRow& D, int* tbs, int bh,
+                                              const uint16_t* __restrict__ q,
+                                              const uint8_t* __restrict__ plan, int Hq, int Hkv,
+                                              const PsPlanIn& pl, bool write_plan) {
+  const int lane = threadIdx.x & 31;
+  const int b = bh / Hkv, h = bh % Hkv;
+  if (pl.sigma2) {
+    ps_plan_row_warp<G>(lane, q, pl.sigma2, b, h, Hq, pl.mode, pl.budget, tbs);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tbs[lane * 4 + c] = min((int)plan[(int64_t)bh * kD + lane * 4 + c], 4);
   }
+  __syncwarp();
+  int tb[4], tot = 0;
+  float qt[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int j = lane * 4 + c;
+    tb[c] = tbs[j];
+    tot += tb[c];
+    float a = 0.0f;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      a = __fadd_rn(a, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]));
+    qt[c] = a;
+    if (write_plan && pl.out) pl.out[(int64_t)bh * kD + j] = (uint8_t)tb[c];
+  }
+  int incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int pos = incl - tot;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int j = lane * 4 + c;
+    const float qo = __fmul_rn(qt[c], tb[c] < 4 ? (float)((1 << (3 - tb[c])) - 8) : -8.0f);
+    for (int p = 0; p < tb[c]; ++p, ++pos) {
+      D.act[pos] = (uint16_t)(j * 4 + p);
+      D.qp[pos] = ldexpf(qt[c], 3 - p);
+      D.qo[pos] = p == 0 ? qo : 0.0f;
+    }
+  }
+  const int nact = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  __syncwarp();
   // each chunk's distinct channels (entries of one channel are consecutive)
-  for (int k = t; k * kPtChunk < nact; k += 128) {
+  for (int k = lane; k * kPtChunk < nact; k += 32) {
     int nc = 0, prev = -1;
     for (int e = k * kPtChunk; e < min(nact, (k + 1) * kPtChunk); ++e) {
-      const int j = R.act[e] >> 2;
+      const int j = D.act[e] >> 2;
       if (j != prev) {
         D.chl[k][nc++] = (uint8_t)j;
         prev = j;
@@ -180,15 +210,20 @@ __device__ __forceinline__ void pt_build(PtSmem& S, int g, const uint16_t* __res
     }
     D.nchl[k] = (uint8_t)nc;
   }
-  if (t == 0) D.nact = nact;
+  if (lane == 0) D.nact = nact;
+  __syncwarp();
 }
 
 // The producer warp: posts every chunk of the CTA's range, then the end marker.
 // Lane 0 waits for a free slot and posts its byte count and metadata; then lanes
 // 0-15 copy the chunk's planes and lanes 16-31 its channels' scales, side by side.
+template <int G>
 __device__ __forceinline__ void pt_produce(PtSmem& S, const uint32_t* __restrict__ planes,
                                            const uint16_t* __restrict__ scales, int64_t n,
-                                           int64_t ncap, int upr, const PtRange& rg) {
+                                           int64_t ncap, int upr, const PtRange& rg,
+                                           const uint16_t* __restrict__ q,
+                                           const uint8_t* __restrict__ plan, int Hq, int Hkv,
+                                           const PsPlanIn& pl) {
   const int lane = threadIdx.x & 31;
   const uint32_t wstride = (uint32_t)(ncap / 32), sstride = (uint32_t)(ncap / 64);
   const int n32 = (int)(n / 32);
@@ -196,6 +231,7 @@ __device__ __forceinline__ void pt_produce(PtSmem& S, const uint32_t* __restrict
   int bh = rg.bh0;
   int ur = (int)(rg.u_begin - (int64_t)bh * upr);
   int c = 0;  // chunks posted
+  int built = rg.bh0 - 1;  // the last row whose tables are built
   bool ok = true;
   auto wait0 = [&](unsigned long long* b, uint32_t parity) {  // lane 0 waits, the warp learns
     int r = 1;
@@ -208,6 +244,10 @@ __device__ __forceinline__ void pt_produce(PtSmem& S, const uint32_t* __restrict
     const int nwv = min(nu * (kPtUnit / 32), n32 - ur * (kPtUnit / 32));  // valid words (even)
     const uint32_t wbytes = (uint32_t)((nwv + 3) & ~3) * 4;           // 16-byte multiples
     const uint32_t sbytes = (uint32_t)(((nwv / 2) + 7) & ~7) * 2;
+    if (bh != built) {  // a new row: its tables first (the row starts inside the range
+      built = bh;       // when its first unit is the tile's)
+      pt_build_warp<G>(S.rows[bh - rg.bh0], S.tbs, bh, q, plan, Hq, Hkv, pl, ur == 0);
+    }
     const PtRow& R = S.rows[bh - rg.bh0];
     const int nact = R.nact;
     const uint32_t* pl_row = planes + (int64_t)bh * kD * 4 * wstride + tok0 / 32;
@@ -330,8 +370,7 @@ score_planes_tma_kernel(const uint32_t* __restrict__ planes, const uint16_t* __r
                         float* __restrict__ wmax) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   PtSmem& S = *reinterpret_cast<PtSmem*>(smem_raw);
-  const PtRange rg = pt_range(upr, total_units);
-  const int nrows = (int)((rg.u_end - 1) / upr) - rg.bh0 + 1;  // <= kPtRows (host-checked)
+  const PtRange rg = pt_range(upr, total_units);  // meets <= kPtRows rows (host-checked)
   if (threadIdx.x == kPtCompute) {
     for (int s = 0; s < kPtSlots; ++s) {
       mb_init(&S.full[s], 1);
@@ -340,11 +379,9 @@ score_planes_tma_kernel(const uint32_t* __restrict__ planes, const uint16_t* __r
     S.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  const int g = threadIdx.x >> 7;  // builder group (2: the producer warp)
-  if (g < nrows) pt_build<G>(S, g, q, plan, Hq, Hkv, pl, rg, upr);
-  __syncthreads();
+  __syncthreads();  // the barriers are initialised
   if (threadIdx.x >= kPtCompute) {
-    pt_produce(S, planes, scales, n, ncap, upr, rg);
+    pt_produce<G>(S, planes, scales, n, ncap, upr, rg, q, plan, Hq, Hkv, pl);
     return;
   }
   pt_compute<CAND>(S, scores, n, cd, wmax, rg.bh0);
