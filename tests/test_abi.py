@@ -106,6 +106,51 @@ def test_argument_checks(sd):
     assert lib.sd_event_wait(None, 10) == sd.SD_ERR_INVALID_ARG
 
 
+def test_fused_entry_argument_checks(sd):
+    """sd_topk_wmax, sd_hamming_topk and sd_select_attend reject bad arguments on the
+    host, before any device work."""
+    lib = sd.lib()
+    P = 1 << 20  # a fake, aligned address; never dereferenced
+    shp = sd.make_shape(1, 32, 8, 1 << 20)
+    sel = sd.make_select(512)
+    # word maxima: n must be a multiple of 32, scores 16-byte aligned, block 1
+    assert lib.sd_topk_wmax(P, P, 8, 1000, ctypes.byref(sel), P, 512, P, None, 0, None) == \
+        sd.SD_ERR_INVALID_ARG
+    assert lib.sd_topk_wmax(P + 4, P, 8, 1 << 20, ctypes.byref(sel), P, 512, P, None, 0,
+                            None) == sd.SD_ERR_INVALID_ARG
+    selb = sd.make_select(4, 0, 1, 16)
+    assert lib.sd_topk_wmax(P, P, 8, 1 << 20, ctypes.byref(selb), P, 80, P, None, 0, None) == \
+        sd.SD_ERR_INVALID_ARG
+    need = sd.sd_topk_workspace_size(8, 1 << 20, sel)
+    assert lib.sd_topk_wmax(P, P, 8, 1 << 20, ctypes.byref(sel), P, 512, P, P, need - 1,
+                            None) == sd.SD_ERR_WORKSPACE
+    # Hamming scan + top-k: token mode only, k limit, stride, workspace, size limit
+    assert lib.sd_hamming_topk(ctypes.byref(shp), P, P, ctypes.byref(selb), P, 80, P, P, 1 << 30,
+                               None) == sd.SD_ERR_INVALID_ARG
+    big = sd.make_select(5000)
+    assert lib.sd_hamming_topk(ctypes.byref(shp), P, P, ctypes.byref(big), P, 5000, P, P,
+                               1 << 30, None) == sd.SD_ERR_UNSUPPORTED
+    assert lib.sd_hamming_topk(ctypes.byref(shp), P, P, ctypes.byref(sel), P, 511, P, P, 1 << 30,
+                               None) == sd.SD_ERR_INVALID_ARG
+    hw = sd.sd_hamming_topk_workspace_size(shp, sel)
+    assert hw > 0
+    assert lib.sd_hamming_topk(ctypes.byref(shp), P, P, ctypes.byref(sel), P, 512, P, P, hw - 1,
+                               None) == sd.SD_ERR_WORKSPACE
+    huge = sd.make_shape(1, 32, 8, 3 << 20)
+    assert lib.sd_hamming_topk(ctypes.byref(huge), P, P, ctypes.byref(sel), P, 512, P, P, 1 << 40,
+                               None) == sd.SD_ERR_UNSUPPORTED
+    # selection + attention: NULL inputs, strides, workspace
+    assert lib.sd_select_attend(ctypes.byref(shp), P, P, ctypes.byref(sel), P, None, P, 0.1, P,
+                                512, P, 512, P, None, P, 1 << 30, None) == sd.SD_ERR_INVALID_ARG
+    assert lib.sd_select_attend(ctypes.byref(shp), P, P, ctypes.byref(sel), P, P, P, 0.1, P,
+                                512, P, 511, P, None, P, 1 << 30, None) == sd.SD_ERR_INVALID_ARG
+    sw = sd.sd_select_attend_workspace_size(shp, sel, 512)
+    assert sw > 0
+    assert lib.sd_select_attend(ctypes.byref(shp), P, P, ctypes.byref(sel), P, P, P, 0.1, P,
+                                512, P, 512, P, None, P, sw - 1, None) == sd.SD_ERR_WORKSPACE
+    assert sd.sd_last_error()
+
+
 def test_python_binding_raises_with_message(sd):
     shp = sd.make_shape(1, 4, 1, 4096, d=64)
     with pytest.raises(sd.SdError) as ei:
