@@ -1849,7 +1849,8 @@ __device__ __forceinline__ void wc_select(WcSmem& S, const float* __restrict__ s
       __syncthreads();
       const int nb = bits_of(S.kmax - T) + 21;
       if (ngb > (uint32_t)k)
-        tc = radix_select_pw<NT, uint64_t>(S.gb, (int)ngb, (uint32_t)k, nb, 64, S.pwh, S.out);
+        tc = radix_threshold<NT, uint64_t>(S.gb, (int)ngb, (uint32_t)k, 0, nb, S.pwh,
+                                           S.pwh + kBins, S.out);  // 11-bit digits
       // selected units per sending CTA (warp r counts CTA r's candidates)
       if (warp < CS) {
         const uint32_t b0 = S.cbase[warp], len = S.clen[warp];
