@@ -327,7 +327,7 @@ __device__ __forceinline__ void pt_compute(PtSmem& S, float* __restrict__ scores
       const PtRow& R = S.rows[I.row - bh0];
       const PtSlot& sl = S.slot[s];
       const int e0 = I.k * kPtChunk;
-#pragma unroll 2
+#pragma unroll 4  // 45.7 us at 1M tokens, against 49.8 (2) and 51.9 (1); 8, 16: 45.7
       for (int e = 0; e < I.ne; ++e) {
         const int ee = e0 + e;
         const float sf = __half2float(reinterpret_cast<const __half*>(&sl.sc[R.cs[ee]][0])[blk]);
