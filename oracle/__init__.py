@@ -27,6 +27,7 @@ _lock = threading.Lock()
 _lib = None
 
 PLAN_WATERFILL, PLAN_FIXED, PLAN_FULL = 0, 1, 2
+PLAN_TOPQ = 3  # SparQ-style: the r channels of largest sum_g q_gj^2, 4 bits each
 
 
 def build(force: bool = False) -> str:

@@ -243,14 +243,38 @@ double orc_reconstruct(int prefix, int t, double s) {
 int orc_plan(const uint16_t* q, const float* sigma2, int64_t B, int Hq, int Hkv, int d,
              int mode, int budget, uint8_t* plan) {
   int G = Hq / Hkv;
-  if (budget < 0 || mode < 0 || mode > 2 || d < 1 || d > 512) return -1;
-  if (mode == 1 && budget > d) return -1;
+  if (budget < 0 || mode < 0 || mode > 3 || d < 1 || d > 512) return -1;
+  if ((mode == 1 || mode == 3) && budget > d) return -1;
   for (int64_t b = 0; b < B; ++b)
     for (int h = 0; h < Hkv; ++h) {
       uint8_t* pb = plan + (b * Hkv + h) * d;
       const float* s2 = sigma2 + (int64_t)h * d;
       if (mode == 2) { memset(pb, 4, d); continue; }
       memset(pb, 0, d);
+      if (mode == 3) {
+        /* SparQ-style [FA "comparison points": top-r |q| channels at full depth]:
+         * the r channels of largest group query mass u_j = sum_g q_gj^2 (fp32, g
+         * ascending, no contraction), 4 bits each, ties to the lower channel.
+         * READING: a group of G query heads ranks channels by the summed squares,
+         * the same query mass the water-filling gain uses, without sigma2. */
+        float u[512];
+        for (int j = 0; j < d; ++j) {
+          float acc = 0.0f;
+          for (int g = 0; g < G; ++g) {
+            float x = bf16_to_f32(q[(b * Hq + h * G + g) * d + j]);
+            float sq = x * x;
+            acc = acc + sq;
+          }
+          u[j] = acc;
+        }
+        for (int r = 0; r < budget; ++r) {
+          int best = -1;
+          for (int j = 0; j < d; ++j)
+            if (pb[j] == 0 && (best < 0 || u[j] > u[best])) best = j;
+          pb[best] = 4;
+        }
+        continue;
+      }
       if (mode == 1) {
         for (int r = 0; r < budget; ++r) {
           int best = -1;

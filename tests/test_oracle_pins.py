@@ -268,6 +268,35 @@ def test_fixed_and_full_plans():
     assert np.all(f == 4)
 
 
+def test_topq_plan_is_sparq_rule():
+    """SparQ-style plan: with one query head per group it is exactly the top-r |q_j|
+    rule (q^2 of a bf16 value is exact in fp32, so the ranking is |q|'s), ties to
+    the lower channel; with a group, every planned channel's query mass is at least
+    every unplanned one's, r channels get 4 bits, the rest 0."""
+    cfg = synth.config(4, n=64, B=2, Hq=8, Hkv=8)  # G = 1
+    inp = synth.make_inputs(cfg, with_v=False)
+    p = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, oracle.PLAN_TOPQ, 17)
+    qf = synth.bf16_to_f64(inp.q)
+    for b in range(cfg.B):
+        for h in range(cfg.Hkv):
+            top = np.argsort(-np.abs(qf[b, h]), kind="stable")[:17]
+            ref = np.zeros(cfg.d, np.uint8)
+            ref[top] = 4
+            assert np.array_equal(p[b, h], ref), (b, h)
+    cfg = synth.config(4, n=64, B=1)  # G = 4
+    inp = synth.make_inputs(cfg, with_v=False)
+    p = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, oracle.PLAN_TOPQ, 17)
+    qf = synth.bf16_to_f64(inp.q).reshape(cfg.B, cfg.Hkv, cfg.G, cfg.d)
+    u = (qf ** 2).sum(axis=2)  # exact in double
+    for h in range(cfg.Hkv):
+        sel = p[0, h] == 4
+        assert sel.sum() == 17 and set(np.unique(p[0, h])) <= {0, 4}
+        assert u[0, h][sel].min() >= u[0, h][~sel].max()
+    # budgets 0 and d
+    assert np.all(oracle.plan(inp.q, inp.sigma2, cfg.Hkv, oracle.PLAN_TOPQ, 0) == 0)
+    assert np.all(oracle.plan(inp.q, inp.sigma2, cfg.Hkv, oracle.PLAN_TOPQ, cfg.d) == 4)
+
+
 # ---------------------------------------------------------------------------------
 # Bit-plane score
 # ---------------------------------------------------------------------------------
