@@ -198,15 +198,17 @@ def scan_traffic(workload: str):
     or None when the kernel source changed since that capture."""
     import hashlib
     prof = os.path.join(ROOT, "profiles", "score_planes_tma_longctx-262k.md")
-    src = os.path.join(ROOT, "top_sparse_decode_gb300", "csrc", "sd_scan_tma.cu")
-    if not (os.path.exists(prof) and os.path.exists(src)):
+    csrc = os.path.join(ROOT, "top_sparse_decode_gb300", "csrc")
+    src, hdr = os.path.join(csrc, "sd_scan_tma.cu"), os.path.join(csrc, "sd_planes.cuh")
+    if not all(os.path.exists(p) for p in (prof, src, hdr)):
         return None
     text = open(prof).read()
     code = open(src).read()
     i, j = code.find("namespace sd {"), code.find("int launch_score_planes_tma(")
     if i < 0 or j < i:
         return None
-    sha = hashlib.sha256(code[i:j].encode()).hexdigest()  # the scan's device code
+    # the scan's device code: its own source and the plan and table helpers it includes
+    sha = hashlib.sha256((code[i:j] + open(hdr).read()).encode()).hexdigest()
     if sha not in text:
         return None
     for line in text.splitlines():
@@ -500,21 +502,26 @@ def main():
 
     variants = {}
     if not args.no_variants:
-        # fixed 32-channel full-depth scan (the "136-bit" class) on the same planes
-        scf = StepConfig(sd.SD_IDX_PLANES, B, Hq, Hkv, n, k=cfg.k, plan_mode=sd.SD_PLAN_FIXED,
-                         budget=32)
-        stf = DecodeStep(scf, K, V, index, sigma2=sigma2)
-        stf.run(q)
-        torch.cuda.synchronize()
-        pf = stf.plan.cpu().numpy()
-        tf = statistics.mean(timed_steps(torch, lambda: stf.run(q), K_st, 3, flush))
-        tfs = statistics.mean(timed_steps(torch, lambda: stf.stage_score(q), K_st, 3, flush))
-        bf = rl.plane_scan_bytes(pf, n)
-        variants["fixed32x4"] = {"us_per_step": tf * 1e3, "keys_per_s": keys / (tf * 1e-3),
-                                 "scan_us": tfs * 1e3, "scan_bytes": bf,
-                                 "scan_GBps": bf / (tfs * 1e-3) / 1e9,
-                                 "scan_frac_hbm": bf / (tfs * 1e-3) / 1e9 / peak_gbs}
-        del stf
+        # full-depth channel subsets on the same planes: the 32 channels of largest
+        # variance (the 136-bit class) and the 16 of largest query mass (SparQ r = 16,
+        # 68 bits: 4 plane bits and a quarter bit of fp16 scale per channel and token)
+        for vname, vmode, vbudget in [("fixed32x4", sd.SD_PLAN_FIXED, 32),
+                                      ("topq16x4", sd.SD_PLAN_TOPQ, 16)]:
+            scf = StepConfig(sd.SD_IDX_PLANES, B, Hq, Hkv, n, k=cfg.k, plan_mode=vmode,
+                             budget=vbudget)
+            stf = DecodeStep(scf, K, V, index, sigma2=sigma2)
+            stf.run(q)
+            torch.cuda.synchronize()
+            pf = stf.plan.cpu().numpy()
+            tf = statistics.mean(timed_steps(torch, lambda: stf.run(q), K_st, 3, flush))
+            tfs = statistics.mean(timed_steps(torch, lambda: stf.stage_plan_score(q), K_st, 3,
+                                              flush))
+            bf = rl.plane_scan_bytes(pf, n)
+            variants[vname] = {"us_per_step": tf * 1e3, "keys_per_s": keys / (tf * 1e-3),
+                               "plan_scan_us": tfs * 1e3, "scan_bytes": bf,
+                               "scan_GBps": bf / (tfs * 1e-3) / 1e9,
+                               "scan_frac_hbm": bf / (tfs * 1e-3) / 1e9 / peak_gbs}
+            del stf
         # 32-bit Hamming (random projection), query map included
         sch = StepConfig(sd.SD_IDX_SIG, B, Hq, Hkv, n, k=cfg.k)
         enc = sd.make_encoder(dev_tensor(inp.W1, torch), dev_tensor(inp.b1, torch))

@@ -79,7 +79,12 @@ typedef struct sd_encoder {
 } sd_encoder;
 
 typedef enum { SD_IDX_SIG = 0, SD_IDX_PLANES = 1, SD_IDX_MINMAX = 2 } sd_index_kind;
-typedef enum { SD_PLAN_WATERFILL = 0, SD_PLAN_FIXED = 1, SD_PLAN_FULL = 2 } sd_plan_mode;
+typedef enum {
+  SD_PLAN_WATERFILL = 0,
+  SD_PLAN_FIXED = 1,
+  SD_PLAN_FULL = 2,
+  SD_PLAN_TOPQ = 3
+} sd_plan_mode;
 typedef enum { SD_SCORE_I32 = 0, SD_SCORE_F32 = 1 } sd_score_type;
 
 /*
@@ -121,6 +126,15 @@ int sd_encode_query(const sd_shape* shape, const void* q, const sd_encoder* enc,
  *   SD_PLAN_FIXED, budget r in [0, d]: the r channels with the largest sigma2_j
  *     (lowest j on ties) get 4 bits, the others 0.
  *   SD_PLAN_FULL: every channel gets 4 bits (budget ignored).
+ *   SD_PLAN_TOPQ, budget r in [0, d]: the r channels with the largest query mass
+ *     u_j = sum_g q_gj^2 (fp32, g ascending, no fused multiply-add; lowest j on
+ *     ties) get 4 bits, the others 0: the SparQ comparison point on the Fathom
+ *     page (top-r |q| channels read at full depth, r = 16 being its 68-bit
+ *     setting; for G = 1 exactly the r largest |q_j|).  sigma2 is not read and may
+ *     be NULL.
+ * q is required by SD_PLAN_WATERFILL and SD_PLAN_TOPQ, sigma2 by SD_PLAN_WATERFILL
+ * and SD_PLAN_FIXED.  Returns SD_ERR_INVALID_ARG for a NULL required pointer, an
+ * unknown mode or a budget out of range.
  */
 int sd_plan(const sd_shape* shape, const void* q, const float* sigma2, int mode, int budget,
             uint8_t* plan, void* stream);

@@ -78,6 +78,15 @@ def test_argument_checks(sd):
     assert lib.sd_plan(ctypes.byref(shp), P, P, 0, 513, P, None) == sd.SD_ERR_INVALID_ARG
     assert lib.sd_plan(ctypes.byref(shp), P, P, 1, 129, P, None) == sd.SD_ERR_INVALID_ARG
     assert lib.sd_plan(ctypes.byref(shp), P, P, 5, 1, P, None) == sd.SD_ERR_INVALID_ARG
+    # top-q: at most d channels, q required, sigma2 not
+    assert lib.sd_plan(ctypes.byref(shp), P, None, 3, 129, P, None) == sd.SD_ERR_INVALID_ARG
+    assert lib.sd_plan(ctypes.byref(shp), P, None, 3, -1, P, None) == sd.SD_ERR_INVALID_ARG
+    assert lib.sd_plan(ctypes.byref(shp), None, None, 3, 17, P, None) == sd.SD_ERR_INVALID_ARG
+    assert lib.sd_plan(ctypes.byref(shp), P, None, 1, 17, P, None) == sd.SD_ERR_INVALID_ARG
+    assert lib.sd_plan_score(ctypes.byref(shp), P, P, P, None, 3, 129, None, P, None, None) == \
+        sd.SD_ERR_INVALID_ARG
+    assert lib.sd_plan_score(ctypes.byref(shp), P, P, P, None, 0, 56, None, P, None, None) == \
+        sd.SD_ERR_INVALID_ARG
     # top-k limits and strides
     sel = sd.make_select(5000)
     assert lib.sd_topk(1, P, 1, 100, 100, ctypes.byref(sel), P, 5000, P, None, 0, None) == \

@@ -27,6 +27,8 @@ CASES = [  # (G, Hkv, B, n, ncap, mode, budget)
     (4, 4, 1, 65536, 0, 0, 47), (8, 2, 2, 8192 + 192, 8704, 0, 92), (1, 8, 1, 4096, 0, 0, 300),
     (4, 4, 1, 65536, 0, 1, 32), (4, 4, 1, 65536, 0, 1, 0), (4, 4, 1, 65536, 0, 1, 128),
     (2, 4, 2, 16384, 0, 2, 0), (4, 8, 1, 262144, 0, 0, 56),
+    (4, 4, 1, 65536, 0, 3, 17), (1, 8, 1, 4096, 0, 3, 128), (8, 2, 2, 8192 + 192, 8704, 3, 5),
+    (4, 8, 1, 262144, 0, 3, 0),
 ]
 
 
@@ -41,7 +43,8 @@ def test_plan_score_equals_plan_then_score(sd, G, Hkv, B, n, ncap, mode, budget)
     planes = empty((B, Hkv, 128, 4, ncap // 32), np.uint32)
     scales = empty((B, Hkv, 128, ncap // 64), np.uint16)
     sd.sd_build_index(sd.SD_IDX_PLANES, shp, dev(Kp), None, planes, scales)
-    q, s2 = dev(inp.q), dev(inp.sigma2)
+    q = dev(inp.q)
+    s2 = None if mode == sd.SD_PLAN_TOPQ else dev(inp.sigma2)  # top-q reads no variances
     plan1 = empty((B, Hkv, 128), np.uint8)
     sd.sd_plan(shp, q, s2, mode, budget, plan1)
     s1 = empty((B * Hkv, n), np.float32)

@@ -129,14 +129,16 @@ def test_plan_bit_exact(sd, G):
     cfg = synth.config(2, B=3, Hq=2 * G, Hkv=2, n=64)
     inp = synth.make_inputs(cfg, with_v=False)
     inp.q[1, :, 5:9] = 0  # zero-gain channels
+    inp.q[0, :, 20:24] = inp.q[0, :, 20:21]  # equal query mass: ties to the lower channel
     shp = shape_of(sd, cfg)
     plan = empty((cfg.B, cfg.Hkv, cfg.d), np.uint8)
     q = dev(inp.q)
     s2 = dev(inp.sigma2)
     for mode, budgets in [(sd.SD_PLAN_WATERFILL, [0, 1, 47, 56, 92, 200, 511, 512]),
-                          (sd.SD_PLAN_FIXED, [0, 1, 32, 128]), (sd.SD_PLAN_FULL, [0])]:
+                          (sd.SD_PLAN_FIXED, [0, 1, 32, 128]), (sd.SD_PLAN_FULL, [0]),
+                          (sd.SD_PLAN_TOPQ, [0, 1, 17, 21, 22, 32, 124, 127, 128])]:
         for B in budgets:
-            sd.sd_plan(shp, q, s2, mode, B, plan)
+            sd.sd_plan(shp, q, None if mode == sd.SD_PLAN_TOPQ else s2, mode, B, plan)
             torch.cuda.synchronize()
             ref = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, mode, B)
             assert np.array_equal(host(plan, np.uint8), ref), (mode, B)
@@ -147,7 +149,7 @@ def test_plan_bit_exact(sd, G):
 # --------------------------------------------------------------------------------------
 @pytest.mark.parametrize("budget,mode,ncap", [(56, 0, 0), (47, 0, 0), (92, 0, 0), (0, 0, 0),
                                                (32, 1, 0), (0, 2, 0), (56, 0, 4608),
-                                               (0, 2, 4608)])
+                                               (0, 2, 4608), (17, 3, 0), (17, 3, 4608)])
 def test_plane_scores(sd, budget, mode, ncap):
     # n = 4288: one full 4096-token tile and a last tile of 6 words / 3 scale
     # blocks; ncap = 4608 (a multiple of 512) takes the 16-byte staging path

@@ -138,18 +138,28 @@ int sd_encode_query(const sd_shape* shape, const void* q, const sd_encoder* enc,
   return launch_encode_query(s, (const uint16_t*)q, *enc, qsig, (cudaStream_t)stream);
 }
 
+// Pointers and budget range of a read plan (modes as sd_plan_mode).
+static int check_plan_args(const char* fn, const void* q, const float* sigma2, int mode,
+                           int budget) {
+  if ((mode == SD_PLAN_WATERFILL || mode == SD_PLAN_TOPQ) && !q)
+    return fail(SD_ERR_INVALID_ARG, "%s: q is NULL", fn);
+  if ((mode == SD_PLAN_WATERFILL || mode == SD_PLAN_FIXED) && !sigma2)
+    return fail(SD_ERR_INVALID_ARG, "%s: sigma2 is NULL", fn);
+  if (mode == SD_PLAN_WATERFILL && (budget < 0 || budget > 4 * kD))
+    return fail(SD_ERR_INVALID_ARG, "%s: budget %d outside [0, %d]", fn, budget, 4 * kD);
+  if ((mode == SD_PLAN_FIXED || mode == SD_PLAN_TOPQ) && (budget < 0 || budget > kD))
+    return fail(SD_ERR_INVALID_ARG, "%s: channel count %d outside [0, %d]", fn, budget, kD);
+  return SD_OK;
+}
+
 int sd_plan(const sd_shape* shape, const void* q, const float* sigma2, int mode, int budget,
             uint8_t* plan, void* stream) {
   Dims s;
   int rc = check_shape(shape, &s);
   if (rc) return rc;
-  if (!plan || (mode != SD_PLAN_FULL && !sigma2) || (mode == SD_PLAN_WATERFILL && !q))
-    return fail(SD_ERR_INVALID_ARG, "sd_plan: NULL input");
-  if (mode < 0 || mode > 2) return fail(SD_ERR_INVALID_ARG, "sd_plan: unknown mode %d", mode);
-  if (mode == SD_PLAN_WATERFILL && (budget < 0 || budget > 4 * kD))
-    return fail(SD_ERR_INVALID_ARG, "sd_plan: budget %d outside [0, %d]", budget, 4 * kD);
-  if (mode == SD_PLAN_FIXED && (budget < 0 || budget > kD))
-    return fail(SD_ERR_INVALID_ARG, "sd_plan: fixed width %d outside [0, %d]", budget, kD);
+  if (mode < 0 || mode > 3) return fail(SD_ERR_INVALID_ARG, "sd_plan: unknown mode %d", mode);
+  if ((rc = check_plan_args("sd_plan", q, sigma2, mode, budget))) return rc;
+  if (!plan) return fail(SD_ERR_INVALID_ARG, "sd_plan: plan is NULL");
   return launch_plan(s, (const uint16_t*)q, sigma2, mode, budget, plan, (cudaStream_t)stream);
 }
 
@@ -218,19 +228,16 @@ int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales,
   Dims s;
   int rc = check_shape(shape, &s, true);
   if (rc) return rc;
-  if (!planes || !scales || !q || !sigma2 || !scores)
+  if (!planes || !scales || !q || !scores)
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: NULL input");
   if (!aligned16(planes) || !aligned16(scores))
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: planes and scores must be 16-byte aligned");
   if ((uintptr_t)wmax % 4)
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: wmax must be 4-byte aligned");
-  if (mode != SD_PLAN_WATERFILL && mode != SD_PLAN_FIXED && mode != SD_PLAN_FULL)
+  if (mode < 0 || mode > 3)
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: unknown plan mode %d", mode);
-  if (mode == SD_PLAN_WATERFILL && (budget < 0 || budget > 4 * kD))
-    return fail(SD_ERR_INVALID_ARG, "sd_plan_score: budget %d outside [0, %d]", budget, 4 * kD);
-  if (mode == SD_PLAN_FIXED && (budget < 0 || budget > kD))
-    return fail(SD_ERR_INVALID_ARG, "sd_plan_score: fixed width %d outside [0, %d]", budget, kD);
-  const PsPlanIn pl{sigma2, mode, budget, plan};
+  if ((rc = check_plan_args("sd_plan_score", q, sigma2, mode, budget))) return rc;
+  const PsPlanIn pl{true, sigma2, mode, budget, plan};
   return launch_score_planes(s, (const uint32_t*)planes, (const uint16_t*)scales, nullptr,
                              (const uint16_t*)q, scores, (cudaStream_t)stream, nullptr, &pl, wmax);
 }

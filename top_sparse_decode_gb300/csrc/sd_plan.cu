@@ -47,10 +47,22 @@ plan_kernel(const uint16_t* __restrict__ q, const float* __restrict__ sigma2, in
     if (t < kD) out[t] = 4;
     return;
   }
-  if (mode == SD_PLAN_FIXED) {
-    // the `budget` channels of largest sigma2 (lowest j on ties), 4 bits each
-    const uint32_t key = t < kD ? key_of_f32(sigma2[(int64_t)h * kD + t]) : 0u;
+  if (mode == SD_PLAN_FIXED || mode == SD_PLAN_TOPQ) {
+    // the `budget` channels of largest sigma2 (FIXED) or largest query mass
+    // u_j = sum_g q_gj^2 (TOPQ, fp32, g ascending, no fused multiply-add), lowest j
+    // on ties, 4 bits each
     const bool live = t < kD;
+    uint32_t key = 0u;
+    if (live && mode == SD_PLAN_FIXED) {
+      key = key_of_f32(sigma2[(int64_t)h * kD + t]);
+    } else if (live) {
+      float u = 0.0f;
+      for (int g = 0; g < G; ++g) {
+        const float x = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + t]);
+        u = __fadd_rn(u, __fmul_rn(x, x));
+      }
+      key = key_of_f32(u);
+    }
     if (budget >= kD) {
       if (live) out[t] = 4;
       return;

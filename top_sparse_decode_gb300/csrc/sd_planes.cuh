@@ -30,15 +30,15 @@ struct PsRow {
 
 // The read plan of one row, computed by one warp with the same arithmetic and tie
 // order as plan_kernel (sd_plan.cu): the budget largest pairs w_j * 4^-b, ties to
-// the lower 4j + b (water-filling), the budget channels of largest sigma2 (fixed),
-// or 4 bits everywhere (full).  Lane l holds channels 4 l .. 4 l + 3 and their pairs
+// the lower 4j + b (water-filling), the budget channels of largest sigma2 (fixed)
+// or of largest query mass sum_g q_gj^2 (top-q), or 4 bits everywhere (full).  Lane l holds channels 4 l .. 4 l + 3 and their pairs
 // (j, 0..3) -- pairs 16 l .. 16 l + 15 in pair order -- so every count is a warp
 // reduction.  Writes tb[j] (shared memory) for every channel.
 template <int G>
 __device__ __forceinline__ void ps_plan_row_warp(int lane, const uint16_t* __restrict__ q,
                                                  const float* __restrict__ sigma2, int b, int h,
                                                  int Hq, int mode, int budget, int* tb) {
-  const bool fixed = mode == SD_PLAN_FIXED;
+  const bool fixed = mode == SD_PLAN_FIXED || mode == SD_PLAN_TOPQ;  // one key per channel
   const int nkeys = (fixed ? 1 : 4) * kD;
   if (mode == SD_PLAN_FULL || budget >= nkeys || budget <= 0) {
     const int v = (mode == SD_PLAN_FULL || budget >= nkeys) ? 4 : 0;
@@ -50,16 +50,18 @@ __device__ __forceinline__ void ps_plan_row_warp(int lane, const uint16_t* __res
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int j = lane * 4 + c;
-    if (fixed) {
-      key[4 * c] = key_of_f32(sigma2[(int64_t)h * kD + j]);
-      key[4 * c + 1] = key[4 * c + 2] = key[4 * c + 3] = 0u;  // not counted
-    } else {
-      float acc = 0.0f;  // gains in fp32, group sum in ascending g, no fused multiply-add
+    float acc = 0.0f;  // query mass in fp32, group sum in ascending g, no fused multiply-add
+    if (mode != SD_PLAN_FIXED) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float x = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]);
         acc = __fadd_rn(acc, __fmul_rn(x, x));
       }
+    }
+    if (fixed) {  // one key per channel: its variance (fixed) or its query mass (top-q)
+      key[4 * c] = key_of_f32(mode == SD_PLAN_FIXED ? sigma2[(int64_t)h * kD + j] : acc);
+      key[4 * c + 1] = key[4 * c + 2] = key[4 * c + 3] = 0u;  // not counted
+    } else {
       const float w = __fmul_rn(acc, sigma2[(int64_t)h * kD + j]);
       const float scale4[4] = {1.0f, 0.25f, 0.0625f, 0.015625f};
 #pragma unroll
@@ -109,10 +111,11 @@ __device__ __forceinline__ void ps_plan_row_warp(int lane, const uint16_t* __res
 // Builds R for row bh = b * Hkv + h.  Every thread of the calling group runs it
 // and `bar()` synchronises exactly that group; threads t < kD (t = the thread's
 // index within the group) do the per-channel work, warp t / 32 == 0 the scan.
-// With pl.sigma2 set, the row's plan is computed here (ps_plan_row_warp) instead of
-// read from `plan`, and written to pl.out when pl.write.
+// With pl.on set, the row's plan is computed here (ps_plan_row_warp) instead of
+// read from `plan`, and written to pl.out when write_plan.
 struct PsPlanIn {
-  const float* sigma2;
+  bool on;
+  const float* sigma2;  // unused by the full and top-q modes
   int mode, budget;
   uint8_t* out;
 };
@@ -124,7 +127,7 @@ __device__ __noinline__ void ps_build_row(PsRow& R, int t, const uint16_t* __res
                                           bool write_plan = false) {
   const int lane = t & 31;
   int tb = 0;
-  if (pl.sigma2) {  // the plan, by the group's first warp, through slot_of
+  if (pl.on) {  // the plan, by the group's first warp, through slot_of
     if ((t >> 5) == 0)
       ps_plan_row_warp<G>(lane, q, pl.sigma2, b, h, Hq, pl.mode, pl.budget, R.slot_of);
     bar();
@@ -138,7 +141,7 @@ __device__ __noinline__ void ps_build_row(PsRow& R, int t, const uint16_t* __res
     for (int g = 0; g < G; ++g)
       a = __fadd_rn(a, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]));
     R.qt[j] = a;
-    R.tb[j] = pl.sigma2 ? tb : min((int)plan[bh * kD + j], 4);  // 0..4 bits per channel
+    R.tb[j] = pl.on ? tb : min((int)plan[bh * kD + j], 4);  // 0..4 bits per channel
   }
   bar();
   if ((t >> 5) == 0) {  // active entries and channel slots, j ascending

@@ -157,7 +157,7 @@ __device__ __forceinline__ void pt_build_warp(PtRow& D, int* tbs, int bh,
                                               const PsPlanIn& pl, bool write_plan) {
   const int lane = threadIdx.x & 31;
   const int b = bh / Hkv, h = bh % Hkv;
-  if (pl.sigma2) {
+  if (pl.on) {
     ps_plan_row_warp<G>(lane, q, pl.sigma2, b, h, Hq, pl.mode, pl.budget, tbs);
   } else {
 #pragma unroll
