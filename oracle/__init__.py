@@ -137,14 +137,16 @@ def hamming_score(sig: np.ndarray, qsig: np.ndarray) -> np.ndarray:
 
 
 def plane_build(K: np.ndarray):
-    """K bf16 [B][Hkv][n][d] -> planes uint32 [B][Hkv][d][4][n/32], scales f16 bits
-    uint16 [B][Hkv][d][n/64]."""
+    """K bf16 [B][Hkv][n][d] -> planes uint32 [B][Hkv][d][4][2 nb], scales f16 bits
+    uint16 [B][Hkv][d][nb], nb = ceil(n / 64) (a partial last block: scale over the
+    tokens it holds, bits past n zero)."""
     K, pk = _c(K, np.uint16)
     B, Hkv, n, d = K.shape
-    planes = np.empty((B, Hkv, d, 4, n // 32), np.uint32)
-    scales = np.empty((B, Hkv, d, n // 64), np.uint16)
+    nb = (n + 63) // 64
+    planes = np.empty((B, Hkv, d, 4, 2 * nb), np.uint32)
+    scales = np.empty((B, Hkv, d, nb), np.uint16)
     if _l().orc_plane_build(pk, B, Hkv, n, d, planes.ctypes.data, scales.ctypes.data):
-        raise ValueError("plane_build needs n % 64 == 0")
+        raise ValueError("plane_build needs n >= 1")
     return planes, scales
 
 

@@ -178,15 +178,20 @@ void orc_hamming_score(const uint32_t* sig, int64_t B, int Hq, int Hkv, int64_t 
  *   s = f16_rn(absmax / 7) in fp32 arithmetic, replaced by 1 when it is 0;
  *   code_i = clamp(rint(k_ij / s) + 8, 0, 15)  (fp32 IEEE divide, ties-to-even);
  *   plane p (0 = MSB) holds bit (3 - p) of the code.
- * Layout: planes uint32 [B][Hkv][d][4][n/32] (token i is bit i%32 of word i/32),
- *         scales f16   [B][Hkv][d][n/64].
+ * Layout: planes uint32 [B][Hkv][d][4][nw] (token i is bit i%32 of word i/32),
+ *         scales f16   [B][Hkv][d][nb], nb = ceil(n/64) blocks, nw = 2 nb words.
  * READING: the pages fix a 4-bit uniform code with an fp16 scale per channel per
  * 64-token block; absmax/7 with offset 8 is the symmetric [-8, 7] reading.
+ * READING (partial block): the pages write keys into the index as they arrive
+ * ["compressed-key update" on the KV-write path], so a last block may hold fewer
+ * than 64 tokens: its scale is taken over the tokens it holds and the bits of the
+ * positions past n are 0 (storage padding, not keys).  A full rebuild of that block
+ * on each arrival is what keeps the index equal to this definition.
  */
 int orc_plane_build(const uint16_t* K, int64_t B, int Hkv, int64_t n, int d,
                     uint32_t* planes, uint16_t* scales) {
-  if (n % 64) return -1;
-  int64_t nw = n / 32, nb = n / 64;
+  if (n < 1) return -1;
+  int64_t nb = (n + 63) / 64, nw = 2 * nb;
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t b = 0; b < B; ++b)
     for (int h = 0; h < Hkv; ++h) {
@@ -195,17 +200,17 @@ int orc_plane_build(const uint16_t* K, int64_t B, int Hkv, int64_t n, int d,
         uint32_t* pl = planes + (((b * Hkv + h) * d + j) * 4) * nw;
         memset(pl, 0, sizeof(uint32_t) * 4 * nw);
         for (int64_t c = 0; c < nb; ++c) {
+          const int64_t t1 = (c + 1) * 64 < n ? (c + 1) * 64 : n; /* tokens held */
           float amax = 0.0f;
-          for (int t = 0; t < 64; ++t) {
-            float v = fabsf(bf16_to_f32(Kh[(c * 64 + t) * d + j]));
+          for (int64_t i = c * 64; i < t1; ++i) {
+            float v = fabsf(bf16_to_f32(Kh[i * d + j]));
             if (v > amax) amax = v;
           }
           uint16_t s16 = orc_f32_to_f16(amax / 7.0f);
           if ((s16 & 0x7FFFu) == 0) s16 = 0x3C00u; /* scale 0 -> 1 */
           scales[((b * Hkv + h) * d + j) * nb + c] = s16;
           float s = orc_f16_to_f32(s16);
-          for (int t = 0; t < 64; ++t) {
-            int64_t i = c * 64 + t;
+          for (int64_t i = c * 64; i < t1; ++i) {
             float r = rintf(bf16_to_f32(Kh[i * d + j]) / s);
             int code = r <= -8.0f ? 0 : (r >= 7.0f ? 15 : (int)r + 8);
             for (int p = 0; p < 4; ++p)

@@ -189,6 +189,35 @@ def test_plane_scale_rule_and_prefix_invariant():
                 assert abs(khat - khat4) <= sv * 2 ** (3 - t)
 
 
+@pytest.mark.parametrize("n", [5, 64 * 2 + 37, 64 * 3 + 63])
+def test_plane_partial_block_rule(n):
+    """A last block holding r < 64 tokens: its scale is f16_rn(absmax/7) over those r
+    tokens (numpy's float16 rounding), their codes are within half a step, the bits
+    of the positions past n are zero, and the full blocks before it do not depend on
+    the tokens after them (appending keys never changes a closed block)."""
+    cfg = synth.config(0, n=256)
+    inp = synth.make_inputs(cfg, with_v=False)
+    Kn = np.ascontiguousarray(inp.K[:, :, :n])
+    planes, scales = oracle.plane_build(Kn)
+    nb = (n + 63) // 64
+    assert planes.shape[-1] == 2 * nb and scales.shape[-1] == nb
+    K = synth.bf16_to_f64(Kn)[0, 0]  # [n][d]
+    d = K.shape[1]
+    c0 = (nb - 1) * 64
+    amax = np.abs(K[c0:]).max(axis=0).astype(np.float32)
+    s_ref = (amax / np.float32(7)).astype(np.float16)
+    s_ref[s_ref == 0] = 1
+    assert np.array_equal(scales[0, 0, :, nb - 1], s_ref.view(np.uint16))
+    codes = _decode_codes(planes)[0, 0].reshape(d, -1)  # [d][64 nb]
+    s = s_ref.astype(np.float64)[:, None]
+    assert np.all(np.abs(K[c0:].T - s * (codes[:, c0:n] - 8.0)) <= s / 2 * (1 + 1e-12))
+    assert not codes[:, n:].any()  # padding: every plane bit past n is 0
+    if nb > 1:
+        pf, sf = oracle.plane_build(np.ascontiguousarray(inp.K[:, :, :c0]))
+        assert np.array_equal(planes[..., :2 * (nb - 1)], pf)
+        assert np.array_equal(scales[..., :nb - 1], sf)
+
+
 def test_plane_zero_block_scale_is_one():
     K = np.zeros((1, 1, 64, 128), np.uint16)
     planes, scales = oracle.plane_build(K)
