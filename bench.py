@@ -536,7 +536,24 @@ def main():
                                  "scan_us": ths * 1e3, "scan_bytes": bh,
                                  "scan_GBps": bh / (ths * 1e-3) / 1e9,
                                  "scan_frac_hbm": bh / (ths * 1e-3) / 1e9 / peak_gbs}
-        del sth, ih
+
+        # the KV-write path's index update for one new token (n_old = n - 1): its
+        # signature, the 64-token bit-plane block it fills (re-quantised), its 16-token
+        # min/max block; eager calls, one launch each (K is unchanged, so every index
+        # keeps its content)
+        shp_a = sd.make_shape(B, Hq, Hkv, n)
+        summ = torch.empty((B, Hkv, (n + 15) // 16, 2, 128), dtype=torch.int16, device="cuda")
+        sd.sd_build_index(sd.SD_IDX_MINMAX, shp_a, K, None, summ)
+        appends = [
+            ("sig", lambda: sd.sd_append_index(sd.SD_IDX_SIG, shp_a, n - 1, K, enc, ih["sig"])),
+            ("planes", lambda: sd.sd_append_index(sd.SD_IDX_PLANES, shp_a, n - 1, K, None,
+                                                  index["planes"], index["scales"])),
+            ("minmax", lambda: sd.sd_append_index(sd.SD_IDX_MINMAX, shp_a, n - 1, K, None,
+                                                  summ))]
+        variants["append_1token"] = {
+            f"{name}_us": statistics.mean(timed_steps(torch, fn, K_st, 3, flush)) * 1e3
+            for name, fn in appends}
+        del sth, ih, summ
 
         # index in pinned host memory: gather the planned prefixes over the host link
         # (NVLink-C2C on a Grace host), then scan, select and attend

@@ -94,10 +94,14 @@ typedef enum { SD_SCORE_I32 = 0, SD_SCORE_F32 = 1 } sd_score_type;
  *     signatures; bit o = 1 iff F_o(k) > 0.  Every dot product is the fp32 chain
  *     acc = fma(w_j, x_j, acc), j ascending from +0, then acc + bias, so the
  *     bits are reproducible on any IEEE machine.  enc is required; out1 unused.
- *   SD_IDX_PLANES (Fathom, bit planes): requires n % 64 == 0 and n_cap % 64 == 0.
+ *   SD_IDX_PLANES (Fathom, bit planes): requires n_cap % 64 == 0.
  *     out0 = uint32 planes [B][hkv][d][4][n_cap/32] (token i = bit i%32 of word
  *     i/32; plane 0 = MSB), out1 = fp16 scales [B][hkv][d][n_cap/64] with
  *     s = f16_rn(absmax/7) (1 if that is 0) and code = clamp(rint(k/s)+8, 0, 15).
+ *     A last block holding fewer than 64 tokens (n % 64 != 0) takes its scale over
+ *     the tokens it holds; its bits past n are 0.  (The plane scans, sd_score and
+ *     sd_plan_score, still need n % 64 == 0.)  Words and scales of blocks past
+ *     ceil(n/64) are not written.
  *   SD_IDX_MINMAX (OasisKV, Quest-style summaries): out0 = bf16 summaries
  *     [B][hkv][ceil(n_cap/16)][2][d]: per 16-token block the channel min row then
  *     the max row (exact keys; -0.0 orders below +0.0; the last block may be
@@ -105,6 +109,22 @@ typedef enum { SD_SCORE_I32 = 0, SD_SCORE_F32 = 1 } sd_score_type;
  */
 int sd_build_index(int kind, const sd_shape* shape, const void* K, const sd_encoder* enc,
                    void* out0, void* out1, void* stream);
+
+/*
+ * sd_append_index -- incremental index update on the KV-write path (HashAttention
+ * 2.2: signatures computed as keys are written and cached; OasisKV system design:
+ * the compressed-key update).  The index in out0/out1 holds sd_build_index's result
+ * for the first n_old tokens; K now holds tokens [0, n) (n = shape->n, 0 <= n_old
+ * <= n, any n, typically n_old + 1 per decode step).  On return the index equals
+ * sd_build_index's result for n tokens, bit for bit.  Rewritten: SD_IDX_SIG the
+ * signatures of tokens [n_old, n); SD_IDX_MINMAX the 16-token blocks from
+ * floor(n_old/16) on; SD_IDX_PLANES the 64-token blocks from floor(n_old/64) on (the
+ * block being filled is re-quantised, since a new key can raise its scale).  Work
+ * and traffic are proportional to n - n_old plus one block.  n_old == n does
+ * nothing.  Arguments, layouts and errors otherwise as sd_build_index.
+ */
+int sd_append_index(int kind, const sd_shape* shape, int64_t n_old, const void* K,
+                    const sd_encoder* enc, void* out0, void* out1, void* stream);
 
 /*
  * sd_encode_query -- query signatures phi_q(q) (HashAttention 2.2), the

@@ -27,7 +27,7 @@ def header_functions():
 
 def test_header_declares_the_path():
     names = header_functions()
-    for must in ["sd_build_index", "sd_encode_query", "sd_plan", "sd_score", "sd_topk",
+    for must in ["sd_build_index", "sd_append_index", "sd_encode_query", "sd_plan", "sd_score", "sd_topk",
                  "sd_gather_attend", "sd_offload_gather", "sd_last_error"]:
         assert must in names
 
@@ -74,6 +74,25 @@ def test_argument_checks(sd):
     enc = sd._abi.SdEncoder(P, None, 100, P, None)
     assert lib.sd_build_index(0, ctypes.byref(shp), P, ctypes.byref(enc), P, None, None) == \
         sd.SD_ERR_UNSUPPORTED
+    # appends: n_old in [0, n], planes need n_cap % 64 == 0 (any n), scales required
+    shp_a = sd.make_shape(1, 4, 1, 4001, 128, 4032)
+    assert lib.sd_append_index(2, ctypes.byref(shp_a), 4002, P, None, P, None, None) == \
+        sd.SD_ERR_INVALID_ARG
+    assert lib.sd_append_index(2, ctypes.byref(shp_a), -1, P, None, P, None, None) == \
+        sd.SD_ERR_INVALID_ARG
+    assert lib.sd_append_index(1, ctypes.byref(shp_a), 4000, P, None, P, None, None) == \
+        sd.SD_ERR_INVALID_ARG
+    shp_b = sd.make_shape(1, 4, 1, 4001, 128, 4040)
+    assert lib.sd_append_index(1, ctypes.byref(shp_b), 4000, P, None, P, P, None) == \
+        sd.SD_ERR_UNSUPPORTED
+    assert lib.sd_append_index(0, ctypes.byref(shp_a), 4000, P, None, P, None, None) == \
+        sd.SD_ERR_INVALID_ARG
+    assert lib.sd_append_index(7, ctypes.byref(shp_a), 4000, P, None, P, None, None) == \
+        sd.SD_ERR_INVALID_ARG
+    assert lib.sd_append_index(2, ctypes.byref(shp_a), 4000, P + 8, None, P, None, None) == \
+        sd.SD_ERR_INVALID_ARG
+    # n_old == n appends nothing and launches nothing
+    assert lib.sd_append_index(2, ctypes.byref(shp_a), 4001, P, None, P, None, None) == sd.SD_OK
     # plan budgets
     assert lib.sd_plan(ctypes.byref(shp), P, P, 0, 513, P, None) == sd.SD_ERR_INVALID_ARG
     assert lib.sd_plan(ctypes.byref(shp), P, P, 1, 129, P, None) == sd.SD_ERR_INVALID_ARG

@@ -24,8 +24,8 @@ from ._abi import (SD_ERR_CUDA, SD_ERR_INVALID_ARG, SD_ERR_TIMEOUT, SD_ERR_UNSUP
 
 __all__ = [
     "SdError", "make_shape", "make_encoder", "make_select", "lib",
-    "sd_build_index", "sd_encode_query", "sd_plan", "sd_score", "sd_topk_workspace_size",
-    "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
+    "sd_build_index", "sd_append_index", "sd_encode_query", "sd_plan", "sd_score",
+    "sd_topk_workspace_size", "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
     "sd_gather_attend_noalloc", "sd_offload_gather",
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
     "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax",
@@ -108,6 +108,13 @@ def sd_build_index(kind: int, shape: SdShape, K, enc: Optional[_Encoder], out0, 
     e = ctypes.byref(enc.c) if enc is not None else None
     _check(lib().sd_build_index(kind, ctypes.byref(shape), _ptr(K), e, _ptr(out0), _ptr(out1),
                                 _stream(stream)), "sd_build_index")
+
+
+def sd_append_index(kind: int, shape: SdShape, n_old: int, K, enc: Optional[_Encoder], out0,
+                    out1=None, stream=None) -> None:
+    e = ctypes.byref(enc.c) if enc is not None else None
+    _check(lib().sd_append_index(kind, ctypes.byref(shape), n_old, _ptr(K), e, _ptr(out0),
+                                 _ptr(out1), _stream(stream)), "sd_append_index")
 
 
 def sd_encode_query(shape: SdShape, q, enc: _Encoder, qsig, stream=None) -> None:

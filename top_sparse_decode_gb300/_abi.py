@@ -39,6 +39,7 @@ _p, _i, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size
 _PS, _PE, _PL = ctypes.POINTER(SdShape), ctypes.POINTER(SdEncoder), ctypes.POINTER(SdSelect)
 SIGNATURES = {
     "sd_build_index": (_i, [_i, _PS, _p, _PE, _p, _p, _p]),
+    "sd_append_index": (_i, [_i, _PS, _i64, _p, _PE, _p, _p, _p]),
     "sd_encode_query": (_i, [_PS, _p, _PE, _p, _p]),
     "sd_plan": (_i, [_PS, _p, _p, _i, _i, _p, _p]),
     "sd_score": (_i, [_i, _PS, _p, _p, _p, _p, _p, _p]),

@@ -105,27 +105,46 @@ int64_t sd_launch_count(void) { return (int64_t)launch_total(); }
 
 const char* sd_last_error(void) { return g_err; }
 
-int sd_build_index(int kind, const sd_shape* shape, const void* K, const sd_encoder* enc,
-                   void* out0, void* out1, void* stream) {
+// sd_build_index and sd_append_index: tokens [t0, n) of K are (re)indexed.
+static int index_tokens(const char* fn, int kind, const sd_shape* shape, int64_t t0,
+                        const void* K, const sd_encoder* enc, void* out0, void* out1,
+                        void* stream) {
   Dims s;
-  int rc = check_shape(shape, &s, kind == SD_IDX_PLANES);
+  int rc = check_shape(shape, &s);
   if (rc) return rc;
-  if (!K || !out0) return fail(SD_ERR_INVALID_ARG, "sd_build_index: K or out0 is NULL");
+  if (t0 < 0 || t0 > s.n)
+    return fail(SD_ERR_INVALID_ARG, "%s: n_old = %lld outside [0, n = %lld]", fn, (long long)t0,
+                (long long)s.n);
+  if (!K || !out0) return fail(SD_ERR_INVALID_ARG, "%s: K or out0 is NULL", fn);
   if (!aligned16(K) || !aligned16(out0))
-    return fail(SD_ERR_INVALID_ARG, "sd_build_index: K and out0 must be 16-byte aligned");
+    return fail(SD_ERR_INVALID_ARG, "%s: K and out0 must be 16-byte aligned", fn);
+  if (kind == SD_IDX_SIG && (rc = check_encoder(enc))) return rc;
+  if (kind == SD_IDX_PLANES && s.ncap % 64)
+    return fail(SD_ERR_UNSUPPORTED, "%s: bit planes need n_cap to be a multiple of 64", fn);
+  if (kind == SD_IDX_PLANES && !out1)
+    return fail(SD_ERR_INVALID_ARG, "%s: scales (out1) is NULL", fn);
+  if (kind != SD_IDX_SIG && kind != SD_IDX_PLANES && kind != SD_IDX_MINMAX)
+    return fail(SD_ERR_INVALID_ARG, "%s: unknown kind %d", fn, kind);
+  if (t0 == s.n) return SD_OK;  // nothing appended
   cudaStream_t st = (cudaStream_t)stream;
   switch (kind) {
     case SD_IDX_SIG:
-      if ((rc = check_encoder(enc))) return rc;
-      return launch_sig_build(s, (const uint16_t*)K, *enc, (uint32_t*)out0, st);
+      return launch_sig_build(s, (const uint16_t*)K, *enc, (uint32_t*)out0, st, t0);
     case SD_IDX_PLANES:
-      if (!out1) return fail(SD_ERR_INVALID_ARG, "sd_build_index: scales (out1) is NULL");
-      return launch_plane_build(s, (const uint16_t*)K, (uint32_t*)out0, (uint16_t*)out1, st);
-    case SD_IDX_MINMAX:
-      return launch_minmax_build(s, (const uint16_t*)K, (uint16_t*)out0, st);
+      return launch_plane_build(s, (const uint16_t*)K, (uint32_t*)out0, (uint16_t*)out1, st, t0);
     default:
-      return fail(SD_ERR_INVALID_ARG, "sd_build_index: unknown kind %d", kind);
+      return launch_minmax_build(s, (const uint16_t*)K, (uint16_t*)out0, st, t0);
   }
+}
+
+int sd_build_index(int kind, const sd_shape* shape, const void* K, const sd_encoder* enc,
+                   void* out0, void* out1, void* stream) {
+  return index_tokens("sd_build_index", kind, shape, 0, K, enc, out0, out1, stream);
+}
+
+int sd_append_index(int kind, const sd_shape* shape, int64_t n_old, const void* K,
+                    const sd_encoder* enc, void* out0, void* out1, void* stream) {
+  return index_tokens("sd_append_index", kind, shape, n_old, K, enc, out0, out1, stream);
 }
 
 int sd_encode_query(const sd_shape* shape, const void* q, const sd_encoder* enc, uint32_t* qsig,

@@ -24,8 +24,8 @@ namespace sd {
 // read as warp-wide broadcasts.
 template <int HID>
 __global__ void __launch_bounds__(128)
-sig_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap, int64_t rows,
-                 const float* __restrict__ W1, const float* __restrict__ b1,
+sig_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap, int64_t t0,
+                 int64_t rows, const float* __restrict__ W1, const float* __restrict__ b1,
                  const float* __restrict__ W2, const float* __restrict__ b2,
                  uint32_t* __restrict__ sig) {
   constexpr int H1 = HID ? HID : 32;  // width of the first layer
@@ -49,7 +49,8 @@ sig_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap, int64_
   __syncthreads();
   int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= rows) return;
-  int64_t bh = r / n, i = r - bh * n;
+  const int64_t cnt = n - t0;  // tokens [t0, n) of every row
+  const int64_t bh = r / cnt, i = t0 + (r - bh * cnt);
   const uint4* xrow = reinterpret_cast<const uint4*>(K + (bh * ncap + i) * kD);
 
   float out[32];
@@ -184,14 +185,14 @@ encode_query_kernel(const uint16_t* __restrict__ q, int rows, const float* __res
 
 template <int HID>
 static int sig_build_t(const Dims& s, const uint16_t* K, const sd_encoder& e, uint32_t* sig,
-                       cudaStream_t st) {
+                       int64_t t0, cudaStream_t st) {
   constexpr int H1 = HID ? HID : 32;
   size_t smem = sizeof(float) * (kD * H1 + H1 + HID * 32 + 32);
   auto kern = sig_build_kernel<HID>;
   if (int rc_ = set_smem_limit((const void*)kern, smem, "sig_build: smem attribute")) return rc_;
-  int64_t rows = (int64_t)s.B * s.Hkv * s.n;
+  int64_t rows = (int64_t)s.B * s.Hkv * (s.n - t0);
   unsigned grid = (unsigned)((rows + 127) / 128);
-  kern<<<grid, 128, smem, st>>>(K, s.n, s.ncap, rows, e.W1, e.b1, e.W2, e.b2, sig);
+  kern<<<grid, 128, smem, st>>>(K, s.n, s.ncap, t0, rows, e.W1, e.b1, e.W2, e.b2, sig);
   note_launches(1);
   return check_launch("sig_build");
 }
@@ -211,12 +212,12 @@ static int encode_query_t(const Dims& s, const uint16_t* q, const sd_encoder& e,
 }
 
 int launch_sig_build(const Dims& s, const uint16_t* K, const sd_encoder& e, uint32_t* sig,
-                     cudaStream_t st) {
+                     cudaStream_t st, int64_t t0) {
   switch (e.hidden) {
-    case 0: return sig_build_t<0>(s, K, e, sig, st);
-    case 32: return sig_build_t<32>(s, K, e, sig, st);
-    case 64: return sig_build_t<64>(s, K, e, sig, st);
-    default: return sig_build_t<128>(s, K, e, sig, st);
+    case 0: return sig_build_t<0>(s, K, e, sig, t0, st);
+    case 32: return sig_build_t<32>(s, K, e, sig, t0, st);
+    case 64: return sig_build_t<64>(s, K, e, sig, t0, st);
+    default: return sig_build_t<128>(s, K, e, sig, t0, st);
   }
 }
 
@@ -234,21 +235,25 @@ int launch_encode_query(const Dims& s, const uint16_t* q, const sd_encoder& e, u
 // Bit planes.  Per (channel, 64-token block): s = f16_rn(absmax / 7) (1 if 0),
 // code = clamp(rint(k / s) + 8, 0, 15) with an IEEE fp32 divide; plane p holds bit
 // (3 - p).  A CTA covers 1024 tokens (16 blocks) of one (sequence, KV head) so
-// that each (channel, plane) row it writes is 128 contiguous bytes.
+// that each (channel, plane) row it writes is 128 contiguous bytes.  A last block
+// holding fewer than 64 tokens takes its scale over them (rows past n are staged
+// as zeros, which leave absmax unchanged) and gets zero bits past n.  The blocks
+// from tok_begin (a multiple of 64) on are written, so an append rebuilds only
+// the block it extends and the ones after it.
 // =====================================================================================
 constexpr int kPbTile = 1024;
 constexpr int kPbPitch = kD + 8;  // bf16 row pitch of the staged block
 
 __global__ void __launch_bounds__(256)
-plane_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap,
+plane_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap, int64_t tok_begin,
                    uint32_t* __restrict__ planes, uint16_t* __restrict__ scales) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem_raw);                   // [64][kPbPitch]
   uint32_t* ws = reinterpret_cast<uint32_t*>(xs + 64 * kPbPitch);         // [kD][4][32]
   uint16_t* ss = reinterpret_cast<uint16_t*>(ws + kD * 4 * 32);           // [kD][16]
   const int64_t bh = blockIdx.y;
-  const int64_t tok0 = (int64_t)blockIdx.x * kPbTile;
-  const int nblk = (int)imin64(kPbTile / 64, (n - tok0) / 64);
+  const int64_t tok0 = tok_begin + (int64_t)blockIdx.x * kPbTile;
+  const int nblk = (int)imin64(kPbTile / 64, (n - tok0 + 63) / 64);
   const uint16_t* Kb = K + (bh * ncap + tok0) * kD;
   const int j = threadIdx.x & (kD - 1), half = threadIdx.x >> 7;
 
@@ -256,7 +261,9 @@ plane_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap,
     // stage 64 rows x 256 B
     for (int e = threadIdx.x; e < 64 * 16; e += 256) {
       int row = e >> 4, seg = e & 15;
-      uint4 v = __ldg(reinterpret_cast<const uint4*>(Kb + ((int64_t)blk * 64 + row) * kD) + seg);
+      const int64_t t = (int64_t)blk * 64 + row;  // token tok0 + t
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (tok0 + t < n) v = __ldg(reinterpret_cast<const uint4*>(Kb + t * kD) + seg);
       *reinterpret_cast<uint4*>(xs + row * kPbPitch + seg * 8) = v;
     }
     __syncthreads();
@@ -278,6 +285,13 @@ plane_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap,
       w2 |= (uint32_t)((code >> 1) & 1) << r;
       w3 |= (uint32_t)(code & 1) << r;
     }
+    // positions past n hold no key: their bits are 0
+    const int64_t held = n - (tok0 + (int64_t)blk * 64 + half * 32);
+    const uint32_t keep = held >= 32 ? 0xFFFFFFFFu : (held <= 0 ? 0u : (1u << held) - 1u);
+    w0 &= keep;
+    w1 &= keep;
+    w2 &= keep;
+    w3 &= keep;
     uint32_t* wj = ws + j * 128 + blk * 2 + half;
     wj[0] = w0;
     wj[32] = w1;
@@ -301,11 +315,12 @@ plane_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap,
 }
 
 int launch_plane_build(const Dims& s, const uint16_t* K, uint32_t* planes, uint16_t* scales,
-                       cudaStream_t st) {
+                       cudaStream_t st, int64_t t0) {
   size_t smem = 64 * kPbPitch * 2 + kD * 4 * 32 * 4 + kD * 16 * 2;
   if (int rc_ = set_smem_limit((const void*)plane_build_kernel, smem, "plane_build: smem attribute")) return rc_;
-  dim3 grid((unsigned)((s.n + kPbTile - 1) / kPbTile), (unsigned)(s.B * s.Hkv));
-  plane_build_kernel<<<grid, 256, smem, st>>>(K, s.n, s.ncap, planes, scales);
+  const int64_t tb = t0 / 64 * 64;  // the block holding token t0 starts the rebuild
+  dim3 grid((unsigned)((s.n - tb + kPbTile - 1) / kPbTile), (unsigned)(s.B * s.Hkv));
+  plane_build_kernel<<<grid, 256, smem, st>>>(K, s.n, s.ncap, tb, planes, scales);
   note_launches(1);
   return check_launch("plane_build");
 }
@@ -322,10 +337,10 @@ __device__ __forceinline__ uint32_t unord16(uint32_t k) {
 }
 
 __global__ void __launch_bounds__(256)
-minmax_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap,
+minmax_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap, int64_t c0,
                     uint16_t* __restrict__ summ) {
   const int64_t bh = blockIdx.y;
-  const int64_t c = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t c = c0 + (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int64_t nblk_valid = (n + 15) / 16, nblk_cap = (ncap + 15) / 16;
   if (c >= nblk_valid) return;
@@ -358,10 +373,11 @@ minmax_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap,
   *reinterpret_cast<uint2*>(out + kD) = hi;
 }
 
-int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaStream_t st) {
-  int64_t nblk = (s.n + 15) / 16;
-  dim3 grid((unsigned)((nblk + 7) / 8), (unsigned)(s.B * s.Hkv));
-  minmax_build_kernel<<<grid, 256, 0, st>>>(K, s.n, s.ncap, summ);
+int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaStream_t st,
+                        int64_t t0) {
+  const int64_t nblk = (s.n + 15) / 16, c0 = t0 / 16;  // blocks [c0, nblk) are rebuilt
+  dim3 grid((unsigned)((nblk - c0 + 7) / 8), (unsigned)(s.B * s.Hkv));
+  minmax_build_kernel<<<grid, 256, 0, st>>>(K, s.n, s.ncap, c0, summ);
   note_launches(1);
   return check_launch("minmax_build");
 }

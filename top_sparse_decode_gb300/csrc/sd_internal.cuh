@@ -58,13 +58,16 @@ struct Dims {
   int64_t n, ncap;
 };
 
+// Index builds over tokens [0, s.n); with t0 > 0 only what tokens [t0, s.n) touch is
+// rewritten (their signatures, the 16- or 64-token blocks from the one holding t0).
 int launch_sig_build(const Dims& s, const uint16_t* K, const sd_encoder& enc, uint32_t* sig,
-                     cudaStream_t st);
+                     cudaStream_t st, int64_t t0 = 0);
 int launch_encode_query(const Dims& s, const uint16_t* q, const sd_encoder& enc, uint32_t* qsig,
                         cudaStream_t st);
 int launch_plane_build(const Dims& s, const uint16_t* K, uint32_t* planes, uint16_t* scales,
-                       cudaStream_t st);
-int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaStream_t st);
+                       cudaStream_t st, int64_t t0 = 0);
+int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaStream_t st,
+                        int64_t t0 = 0);
 int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode, int budget,
                 uint8_t* plan, cudaStream_t st);
 int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsig,
