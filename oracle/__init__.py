@@ -80,6 +80,9 @@ def _l():
             lib.orc_gather_attend.restype = None
             lib.orc_prefix_copy.argtypes = [p, p, p, i64, i32, i64, i32, p, p]
             lib.orc_prefix_copy.restype = None
+            lib.orc_delta_select.argtypes = [i64, i64, i64, i32, i32, i32, p, p, i64, p, i32,
+                                             i64, i32, p, p, p, p, p, p, p, p, i64, p]
+            lib.orc_delta_select.restype = i32
             _lib = lib
     return _lib
 
@@ -246,3 +249,49 @@ def prefix_copy(src_planes, src_scales, plan_, dst_planes, dst_scales):
     B, Hkv, d, _, nw = src_planes.shape
     _l().orc_prefix_copy(pp, ps, ppl, B, Hkv, nw * 32, d, dst_planes.ctypes.data,
                          dst_scales.ctypes.data)
+
+
+class Resident:
+    """Resident-set state of the delta selection, per row (sequence, KV head):
+    slot_unit [rows][R], slot_last [rows][R] (int64), unit_slot [rows][n_units];
+    all -1 when empty."""
+
+    def __init__(self, rows: int, R: int, n_units: int):
+        self.slot_unit = np.full((rows, R), -1, np.int32)
+        self.slot_last = np.full((rows, R), -1, np.int64)
+        self.unit_slot = np.full((rows, n_units), -1, np.int32)
+
+    def copy(self):
+        r = Resident.__new__(Resident)
+        r.slot_unit, r.slot_last, r.unit_slot = (self.slot_unit.copy(), self.slot_last.copy(),
+                                                 self.unit_slot.copy())
+        return r
+
+
+def delta_select(state: Resident, scores, idx, count, block: int, n_tokens: int, sink: int,
+                 local: int, C: int, step: int, pool_stride: int):
+    """One step of the delta selection; updates `state` in place.  scores float32
+    [rows][n_units], idx/count the top-k output (tokens).  Returns (plan_slot,
+    plan_unit, plan_evict [rows][C], plan_count [rows], pool_idx [rows][pool_stride]
+    (-1 past pool_count), pool_count [rows])."""
+    scores, psc = _c(scores, np.float32)
+    idx, pi = _c(idx, np.int32)
+    count, pc = _c(count, np.int32)
+    rows, nu = scores.shape
+    R = state.slot_unit.shape[1]
+    ps = np.full((rows, max(C, 1)), -1, np.int32)
+    pu, pe = ps.copy(), ps.copy()
+    pcount = np.zeros(rows, np.int32)
+    pool = np.full((rows, pool_stride), -1, np.int32)
+    pool_count = np.zeros(rows, np.int32)
+    for a in (state.slot_unit, state.slot_last, state.unit_slot):
+        assert a.flags["C_CONTIGUOUS"]
+    rc = _l().orc_delta_select(rows, nu, n_tokens, block, sink, local, psc, pi, idx.shape[-1], pc,
+                               C, step, R, state.slot_unit.ctypes.data,
+                               state.slot_last.ctypes.data, state.unit_slot.ctypes.data,
+                               ps.ctypes.data, pu.ctypes.data, pe.ctypes.data,
+                               pcount.ctypes.data, pool.ctypes.data, pool_stride,
+                               pool_count.ctypes.data)
+    if rc:
+        raise ValueError("delta_select: bad block, R, C or step")
+    return ps[:, :C], pu[:, :C], pe[:, :C], pcount, pool, pool_count

@@ -585,3 +585,128 @@ void orc_prefix_copy(const uint32_t* src_planes, const uint16_t* src_scales,
         memcpy(dst_scales + base * nb, src_scales + base * nb, sizeof(uint16_t) * (size_t)nb);
       }
 }
+
+/* ------------------------------------------------------------------------------ */
+/* F3  delta selection against a resident set  [OA "method details": intersect the  */
+/*     predicted top-K with the resident set, admit at most C non-resident blocks   */
+/*     per head, each paired with the least-recently-selected resident block]       */
+/* ------------------------------------------------------------------------------ */
+/*
+ * One decode step of the selection worker, per row r = (sequence, KV head).
+ * State (kept by the caller between steps; all -1 initially):
+ *   slot_unit [rows][R]   unit held by each of the R resident slots, -1 empty;
+ *   slot_last [rows][R]   step at which that unit was last selected, -1 empty;
+ *   unit_slot [rows][nu]  slot holding each unit, -1 if it is not resident.
+ * Input: the top-k output (idx, count) in units of `block` tokens (tokens of each
+ * selected unit expanded, ascending, as the top-k writes them): the predicted set P
+ * is every unit u with token u*block listed.  A row with count < 0 (a NaN score)
+ * is left alone: plan_count = pool_count = -1.
+ * 1. Hits: units of P already resident; their slot_last becomes `step`.
+ * 2. Misses, in admission order: forced units first (sink [0, sink), local
+ *    [nu - local, nu)), unit ascending; then the others by score descending, unit
+ *    ascending (-0.0 equal to +0.0).
+ * 3. Eviction targets: the slots not holding a unit of P, by slot_last ascending
+ *    (empty slots, -1, first), slot ascending.
+ * 4. a = min(C, misses, targets): miss i goes to target i; the target's old unit
+ *    (if any) stops being resident; slot_last of the slot becomes `step`.  The plan
+ *    lists (slot, unit, evicted unit or -1) for i < a; plan_count = a.
+ * 5. pool_idx: for the units of P resident after the step, in unit order, the pool
+ *    rows slot*block + t for the unit's tokens t < min(block, n_tokens - u*block);
+ *    pool_count = their number.
+ * READING: the pages fix the intersection, the cap C, the pairing with a
+ * least-recently-selected target and that hits move nothing; which misses go first
+ * when more than C are missing, and the order of equally old targets, are not
+ * stated: forced units (the local block being written) first, then by score, and
+ * the lower slot first are the readings taken.
+ */
+int orc_delta_select(int64_t rows, int64_t nu, int64_t n_tokens, int block, int sink,
+                     int local, const float* scores, const int32_t* idx, int64_t idx_stride,
+                     const int32_t* count, int C, int64_t step, int R, int32_t* slot_unit,
+                     int64_t* slot_last, int32_t* unit_slot, int32_t* plan_slot,
+                     int32_t* plan_unit, int32_t* plan_evict, int32_t* plan_count,
+                     int32_t* pool_idx, int64_t pool_stride, int32_t* pool_count) {
+  if (block < 1 || R < 1 || C < 0 || step < 0) return -1;
+  int32_t* P = malloc(sizeof(int32_t) * (size_t)(nu > 0 ? nu : 1));
+  char* inP = malloc((size_t)(R > 0 ? R : 1));
+  char* taken = malloc((size_t)(nu > 0 ? nu : 1));
+  for (int64_t r = 0; r < rows; ++r) {
+    int32_t* su = slot_unit + r * R;
+    int64_t* sl = slot_last + r * R;
+    int32_t* us = unit_slot + r * nu;
+    const float* sc = scores + r * nu;
+    const int64_t c = count[r];
+    if (c < 0) {
+      plan_count[r] = -1;
+      pool_count[r] = -1;
+      continue;
+    }
+    /* the predicted units, ascending */
+    int64_t np = 0;
+    for (int64_t i = 0; i < c; ++i) {
+      int32_t t = idx[r * idx_stride + i];
+      if (t >= 0 && t < n_tokens && t % block == 0 && t / block < nu) P[np++] = t / block;
+    }
+    /* 1. hits */
+    memset(inP, 0, (size_t)R);
+    for (int64_t i = 0; i < np; ++i) {
+      int32_t s = us[P[i]];
+      if (s >= 0) {
+        inP[s] = 1;
+        sl[s] = step;
+      }
+    }
+    /* 2-4. admit misses one at a time: the best remaining miss to the oldest target */
+    int a = 0;
+    for (int64_t i = 0; i < np; ++i) taken[P[i]] = 0;
+    while (a < C) {
+      int64_t best = -1; /* index into P */
+      for (int64_t i = 0; i < np; ++i) {
+        int32_t u = P[i];
+        if (us[u] >= 0 || taken[u]) continue;
+        if (best < 0) { best = i; continue; }
+        int32_t v = P[best];
+        int fu = u < sink || u >= nu - local, fv = v < sink || v >= nu - local;
+        float xu = sc[u], xv = sc[v];
+        int better;
+        if (fu != fv) better = fu;
+        else if (fu) better = u < v;
+        else if (xu != xv) better = xu > xv;
+        else better = u < v;
+        if (better) best = i;
+      }
+      if (best < 0) break; /* no miss left */
+      int s_t = -1;
+      for (int s = 0; s < R; ++s) {
+        if (inP[s]) continue;
+        if (s_t < 0 || sl[s] < sl[s_t]) s_t = s; /* strict: the lower slot on ties */
+      }
+      if (s_t < 0) break; /* no target left */
+      int32_t u = P[best], old = su[s_t];
+      if (old >= 0) us[old] = -1;
+      su[s_t] = u;
+      sl[s_t] = step;
+      us[u] = s_t;
+      inP[s_t] = 1;
+      taken[u] = 1;
+      plan_slot[r * (int64_t)C + a] = s_t;
+      plan_unit[r * (int64_t)C + a] = u;
+      plan_evict[r * (int64_t)C + a] = old;
+      ++a;
+    }
+    plan_count[r] = a;
+    /* 5. pool rows of the resident predicted units */
+    int64_t pc = 0;
+    for (int64_t i = 0; i < np; ++i) {
+      int32_t u = P[i], s = us[u];
+      if (s < 0) continue;
+      int64_t len = n_tokens - (int64_t)u * block;
+      if (len > block) len = block;
+      for (int64_t t = 0; t < len; ++t) pool_idx[r * pool_stride + pc++] = (int32_t)(s * block + t);
+    }
+    pool_count[r] = (int32_t)pc;
+  }
+  free(P);
+  free(inP);
+  free(taken);
+  return 0;
+}

@@ -519,3 +519,93 @@ def test_prefix_copy_copies_exactly_the_planned_prefix():
         assert np.array_equal(dp[0, 0, j, :t], planes[0, 0, j, :t])
         assert np.all(dp[0, 0, j, t:] == 0)
         assert np.array_equal(ds[0, 0, j], scales[0, 0, j] if t else np.zeros_like(ds[0, 0, j]))
+
+
+# ---------------------------------------------------------------------------------
+# F3 delta selection against a resident set (OasisKV, method details)
+# ---------------------------------------------------------------------------------
+def _expand(units, block, n_tokens):
+    return [t for u in sorted(units) for t in range(u * block, min((u + 1) * block, n_tokens))]
+
+
+def test_delta_select_worked_example():
+    """The hand-worked six-step sequence of tests/golden (one KV head, 3 slots,
+    16-token units, a forced local unit, ties, -0.0, C = 0 and a NaN row)."""
+    g = json.load(open(os.path.join(GOLD, "delta_select_worked_example.json")))
+    R, block, n_tok, nu = g["R"], g["block"], g["n_tokens"], g["n_units"]
+    st = oracle.Resident(1, R, nu)
+    for step, s in enumerate(g["steps"]):
+        sc = np.array([[float(x) for x in s["scores"]]], np.float32)
+        if s["P"] is None:
+            idx, cnt = np.zeros((1, 8), np.int32), np.array([-1], np.int32)
+        else:
+            toks = _expand(s["P"], block, n_tok)
+            idx, cnt = np.array([toks], np.int32), np.array([len(toks)], np.int32)
+        ps, pu, pe, pc, pool, pcount = oracle.delta_select(st, sc, idx, cnt, block, n_tok,
+                                                          g["sink"], g["local"], s["C"], step,
+                                                          64)
+        if s["plan"] is None:
+            assert pc[0] == -1 and pcount[0] == -1
+        else:
+            assert pc[0] == len(s["plan"])
+            got = [[int(ps[0, i]), int(pu[0, i]), int(pe[0, i])] for i in range(pc[0])]
+            assert got == s["plan"], (step, got)
+            rows = [r for a, b in s["pool"] for r in range(a, b)]
+            assert pcount[0] == len(rows) and list(pool[0, :pcount[0]]) == rows, step
+        assert list(st.slot_unit[0]) == s["slot_unit"], step
+        assert list(st.slot_last[0]) == s["slot_last"], step
+        us = np.full(nu, -1)
+        for slot, u in enumerate(s["slot_unit"]):
+            if u >= 0:
+                us[u] = slot
+        assert np.array_equal(st.unit_slot[0], us), step
+
+
+def test_delta_select_invariants_random():
+    """Random drifting predictions over many steps: at most C admissions per row and
+    step, hits keep their slot, the map stays a bijection, every admitted miss ranks
+    ahead of every miss left out, every evicted target is no more recently selected
+    than any slot kept outside the prediction, and the pool rows are exactly the
+    resident predicted units' tokens."""
+    rng = np.random.default_rng(7)
+    rows, nu, block, R, k, sink, local = 6, 96, 16, 20, 12, 1, 2
+    n_tok = nu * block - 5
+    st = oracle.Resident(rows, R, nu)
+    for step in range(40):
+        C = int(rng.integers(0, 6))
+        sc = rng.normal(size=(rows, nu)).astype(np.float32)
+        sc[:, ::7] = 0.5  # ties
+        ri, rc = oracle.topk(sc, k, sink, local, block, n_tok)
+        before = st.copy()
+        ps, pu, pe, pc, pool, pcount = oracle.delta_select(st, sc, ri, rc, block, n_tok, sink,
+                                                          local, C, step, ri.shape[1])
+        for r in range(rows):
+            P = sorted({int(t) // block for t in ri[r, :rc[r]] if t % block == 0})
+            hits = [u for u in P if before.unit_slot[r, u] >= 0]
+            miss = [u for u in P if before.unit_slot[r, u] < 0]
+            a = int(pc[r])
+            free = [s for s in range(R) if before.slot_unit[r, s] not in P]
+            assert a == min(C, len(miss), len(free))
+            for u in hits:
+                assert st.unit_slot[r, u] == before.unit_slot[r, u]
+                assert st.slot_last[r, st.unit_slot[r, u]] == step
+            res = st.unit_slot[r] >= 0
+            assert res.sum() == (st.slot_unit[r] >= 0).sum()
+            for s in range(R):
+                if st.slot_unit[r, s] >= 0:
+                    assert st.unit_slot[r, st.slot_unit[r, s]] == s
+
+            def key(u):  # admission order: forced first, then score desc, unit asc
+                forced = u < sink or u >= nu - local
+                return (0, u) if forced else (1, -float(sc[r, u]), u)
+            admitted = [int(x) for x in pu[r, :a]]
+            assert admitted == sorted(miss, key=key)[:a]
+            evicted = [int(x) for x in ps[r, :a]]
+            kept = [s for s in free if s not in evicted]
+            for s in evicted:
+                assert pe[r, evicted.index(s)] == before.slot_unit[r, s]
+                for s2 in kept:
+                    assert (before.slot_last[r, s], s) < (before.slot_last[r, s2], s2)
+            rows_exp = [int(st.unit_slot[r, u]) * block + t for u in P if st.unit_slot[r, u] >= 0
+                        for t in range(min(block, n_tok - u * block))]
+            assert list(pool[r, :pcount[r]]) == rows_exp
