@@ -365,6 +365,54 @@ def other_configs(torch, sd, rl, synth, flush, K_st, peak_gbs):
         "topk_us": t_topk, "attend_us": t_att, "gather_bytes": gb,
         "attend_GBps": gb / (t_att * 1e-6) / 1e9,
         "attend_frac_hbm": gb / (t_att * 1e-6) / 1e9 / peak_gbs}
+
+    # OasisKV's resident set on the same step: 129 slots of 16 tokens per KV head, at
+    # most C = 7 admissions per head and step (fetch ratio 0.05 of K = 128), full K/V
+    # in pinned host memory; two queries alternate so that every step has misses
+    R, C, rows3 = 129, 7, c3.B * c3.Hkv
+    preds = []
+    for qq in (q, torch.roll(q, 1, dims=2)):
+        st.stage_score(qq)
+        st.stage_topk()
+        preds.append((st.scores.clone(), st.idx.clone(), st.count.clone()))
+    Kh, Vh = K.cpu().pin_memory(), V.cpu().pin_memory()
+    res = sd.Resident(rows3, R, sc.n_units)
+    Kp = torch.zeros((c3.B, c3.Hkv, R * 16, 128), dtype=torch.bfloat16, device="cuda")
+    Vp = torch.zeros_like(Kp)
+    plan = [torch.empty((rows3, C), dtype=torch.int32, device="cuda") for _ in range(3)]
+    pcnt = torch.empty(rows3, dtype=torch.int32, device="cuda")
+    pool = torch.empty((rows3, sc.max_count), dtype=torch.int32, device="cuda")
+    pool_cnt = torch.empty(rows3, dtype=torch.int32, device="cuda")
+    shp3 = sd.make_shape(c3.B, c3.Hq, c3.Hkv, c3.n)
+    counter = [0]
+
+    def select():
+        s3, i3, n3 = preds[counter[0] % 2]
+        sd.sd_delta_select(shp3, st.sel, s3, i3, sc.max_count, n3, C, counter[0], res, *plan,
+                           pcnt, pool, sc.max_count, pool_cnt)
+        counter[0] += 1
+
+    def transfer():
+        sd.sd_resident_gather(shp3, 16, Kh, Vh, plan[0], plan[1], pcnt, C, R, Kp, Vp)
+
+    for _ in range(4):  # fill the set
+        select()
+        transfer()
+    t_sel = statistics.mean(timed_steps(torch, select, K_st, 3, flush)) * 1e3
+
+    def both():
+        select()
+        transfer()
+    t_both = statistics.mean(timed_steps(torch, both, K_st, 3, flush)) * 1e3
+    select()
+    torch.cuda.synchronize()
+    admitted = int(pcnt.clamp(min=0).sum().item())
+    xfer = admitted * 16 * 128 * 2 * 2  # K and V rows of the admitted blocks
+    out["quest-b64-16k (B=64, n=16384, 128+1 blocks)"]["resident_129x16_C7"] = {
+        "delta_select_us": t_sel, "select_and_transfer_us": t_both,
+        "admitted_blocks_per_step": admitted, "transfer_bytes_per_step": xfer,
+        "host_link_GBps": xfer / ((t_both - t_sel) * 1e-6) / 1e9 if t_both > t_sel else None}
+    del Kh, Vh, Kp, Vp, preds, res
     del st, index, q, K, V, inp
 
     # HashAttention, 32768 tokens, 2-layer-MLP signatures, 128 + 512 window tokens

@@ -358,6 +358,73 @@ int sd_offload_gather(const sd_shape* shape, const uint32_t* host_planes,
                       uint16_t* dev_scales, void* stream);
 
 /*
+ * Resident set of the delta selection (OasisKV method details: the GPU keeps a
+ * fixed pool of blocks per KV head -- 129 blocks of 16 tokens there -- and a head-
+ * level map from logical blocks to pool pages).  Device arrays owned by the
+ * caller, rows = B * hkv; every entry -1 for an empty set (fill the bytes with 0xFF):
+ *   slot_unit int32 [rows][n_slots]  unit held by each slot, -1 empty;
+ *   slot_last int32 [rows][n_slots]  step at which that unit was last selected;
+ *   unit_slot int32 [rows][n_units]  slot holding each unit, -1 not resident.
+ */
+typedef struct sd_resident {
+  int32_t n_slots;
+  int32_t* slot_unit;
+  int32_t* slot_last;
+  int32_t* unit_slot;
+} sd_resident;
+
+/*
+ * sd_delta_select -- the KV-selection step (OasisKV method details): intersect the
+ * predicted units with the resident set and plan at most admit_cap admissions per
+ * (sequence, KV head), each evicting the least-recently-selected slot outside the
+ * prediction.
+ *   shape: n tokens; units are blocks of sel->block tokens, n_units =
+ *   ceil(n / block).  scores: fp32 [rows][n_units] and idx/count: the sd_topk
+ *   output over those scores (tokens of each unit expanded, ascending; a unit is
+ *   predicted when its first token is listed).  A row with count < 0 is left
+ *   alone (plan_count = pool_count = -1).
+ *   Hits (predicted and resident) stay where they are; their slot_last becomes
+ *   step.  Misses are admitted in order: forced units (sel's sink and local
+ *   windows) unit ascending, then score descending, unit ascending (-0.0 equals
+ *   +0.0).  Targets: the slots not holding a predicted unit, by slot_last
+ *   ascending (empty slots first), slot ascending.  a = min(admit_cap, misses,
+ *   targets) pairs are made; slot_last of each taken slot becomes step.
+ *   Outputs: plan_slot / plan_unit / plan_evict int32 [rows][admit_cap] (entries
+ *   past plan_count not written; plan_evict = the unit evicted or -1) and
+ *   plan_count [rows]; pool_idx int32 [rows][pool_stride]: the pool rows
+ *   slot*block + t of every predicted unit resident after the step, in unit order
+ *   (t < the unit's token count), pool_count [rows] (the input of sd_gather_attend
+ *   over the pool).
+ *   Limits: 1 <= block <= 4096; min(n_units, sink + local + k) <= 8192 units;
+ *   1 <= n_slots <= 4096; 0 <= admit_cap <= 8192; 0 <= step < 2^31 - 1;
+ *   idx_stride and pool_stride at least min(n_units, sink + local + k) * block.
+ *   Steps of one resident set must not overlap.  The state is read as it stands:
+ *   a map entry that disagrees with its slot counts as not resident, so no state
+ *   content can make the kernel access memory outside the arrays.
+ */
+int sd_delta_select(const sd_shape* shape, const sd_select* sel, const float* scores,
+                    const int32_t* idx, int64_t idx_stride, const int32_t* count,
+                    int32_t admit_cap, int32_t step, const sd_resident* res,
+                    int32_t* plan_slot, int32_t* plan_unit, int32_t* plan_evict,
+                    int32_t* plan_count, int32_t* pool_idx, int64_t pool_stride,
+                    int32_t* pool_count, void* stream);
+
+/*
+ * sd_resident_gather -- the KV-transfer step (OasisKV: a UVA gather kernel writes
+ * the planned blocks from pinned CPU memory into the GPU's resident pages): for
+ * each plan entry i < plan_count of each row, the unit's tokens [u*block,
+ * min((u+1)*block, n)) of K and V are copied to pool rows slot*block..; rows of a
+ * short last unit past n are written as zeros.
+ *   K, V: bf16 [B][hkv][n_cap][d], device memory or pinned host memory (cudaHostAlloc
+ *   or registered); K_pool, V_pool: device bf16 [B][hkv][n_slots * block][d].  All
+ *   16-byte aligned.  Entries with a slot or unit out of range are skipped.
+ */
+int sd_resident_gather(const sd_shape* shape, int32_t block, const void* K, const void* V,
+                       const int32_t* plan_slot, const int32_t* plan_unit,
+                       const int32_t* plan_count, int32_t admit_cap, int32_t n_slots,
+                       void* K_pool, void* V_pool, void* stream);
+
+/*
  * sd_event_wait -- host-side bounded wait on a cudaEvent_t (passed as void*):
  * polls until the event completes or timeout_us microseconds pass
  * (SD_ERR_TIMEOUT).  Lets a caller bound its wait for an offload copy.

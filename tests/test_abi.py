@@ -93,6 +93,34 @@ def test_argument_checks(sd):
         sd.SD_ERR_INVALID_ARG
     # n_old == n appends nothing and launches nothing
     assert lib.sd_append_index(2, ctypes.byref(shp_a), 4001, P, None, P, None, None) == sd.SD_OK
+    # delta selection: block, slots, cap, step, strides; gather: block and slots
+    res = sd._abi.SdResident(16, P, P, P)
+    selb16 = sd.make_select(8, 0, 1, 16)
+    shp_d = sd.make_shape(2, 8, 2, 1600)
+
+    def ds(sel=selb16, cap=4, step=0, r=res, istride=9 * 16, pstride=9 * 16):
+        return lib.sd_delta_select(ctypes.byref(shp_d), ctypes.byref(sel), P, P, istride, P, cap,
+                                   step, ctypes.byref(r), P, P, P, P, P, pstride, P, None)
+    assert ds(sel=sd.make_select(8, 0, 1, 0)) == sd.SD_ERR_INVALID_ARG
+    assert ds(cap=-1) == sd.SD_ERR_INVALID_ARG
+    assert ds(step=-1) == sd.SD_ERR_INVALID_ARG
+    assert ds(step=0x7FFFFFFF) == sd.SD_ERR_INVALID_ARG
+    assert ds(istride=9 * 16 - 1) == sd.SD_ERR_INVALID_ARG
+    assert ds(pstride=9 * 16 - 1) == sd.SD_ERR_INVALID_ARG
+    assert ds(r=sd._abi.SdResident(0, P, P, P)) == sd.SD_ERR_UNSUPPORTED
+    assert ds(r=sd._abi.SdResident(5000, P, P, P)) == sd.SD_ERR_UNSUPPORTED
+    assert ds(r=sd._abi.SdResident(16, P, None, P)) == sd.SD_ERR_INVALID_ARG
+    shp_big = sd.make_shape(1, 1, 1, 1 << 16)
+    sel_big = sd.make_select(4096, 4096, 4096, 1)  # 12,288 predicted units
+    assert lib.sd_delta_select(ctypes.byref(shp_big), ctypes.byref(sel_big), P, P, 1 << 20, P, 4,
+                               0, ctypes.byref(res), P, P, P, P, P, 1 << 20, P, None) == \
+        sd.SD_ERR_UNSUPPORTED
+    assert lib.sd_resident_gather(ctypes.byref(shp_d), 0, P, P, P, P, P, 4, 16, P, P, None) == \
+        sd.SD_ERR_INVALID_ARG
+    assert lib.sd_resident_gather(ctypes.byref(shp_d), 16, P, P, P, P, P, 4, 0, P, P, None) == \
+        sd.SD_ERR_UNSUPPORTED
+    assert lib.sd_resident_gather(ctypes.byref(shp_d), 16, P + 8, P, P, P, P, 4, 16, P, P,
+                                  None) == sd.SD_ERR_INVALID_ARG
     # plan budgets
     assert lib.sd_plan(ctypes.byref(shp), P, P, 0, 513, P, None) == sd.SD_ERR_INVALID_ARG
     assert lib.sd_plan(ctypes.byref(shp), P, P, 1, 129, P, None) == sd.SD_ERR_INVALID_ARG

@@ -26,7 +26,8 @@ __all__ = [
     "SdError", "make_shape", "make_encoder", "make_select", "lib",
     "sd_build_index", "sd_append_index", "sd_encode_query", "sd_plan", "sd_score",
     "sd_topk_workspace_size", "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
-    "sd_gather_attend_noalloc", "sd_offload_gather",
+    "sd_gather_attend_noalloc", "sd_offload_gather", "Resident", "sd_delta_select",
+    "sd_resident_gather",
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
     "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax",
     "sd_select_attend_workspace_size", "sd_select_attend", "sd_hamming_topk_workspace_size",
@@ -230,6 +231,37 @@ def sd_offload_gather(shape: SdShape, host_planes, host_scales, plan, dev_planes
     _check(lib().sd_offload_gather(ctypes.byref(shape), _ptr(host_planes), _ptr(host_scales),
                                    _ptr(plan), _ptr(dev_planes), _ptr(dev_scales),
                                    _stream(stream)), "sd_offload_gather")
+
+
+class Resident:
+    """A resident set on the device (sd_resident): slot_unit and slot_last int32
+    [rows][n_slots], unit_slot int32 [rows][n_units], all -1 when empty."""
+
+    def __init__(self, rows: int, n_slots: int, n_units: int, device="cuda"):
+        self.n_slots = n_slots
+        self.slot_unit = torch.full((rows, n_slots), -1, dtype=torch.int32, device=device)
+        self.slot_last = torch.full((rows, n_slots), -1, dtype=torch.int32, device=device)
+        self.unit_slot = torch.full((rows, n_units), -1, dtype=torch.int32, device=device)
+        self.c = _abi.SdResident(n_slots, _ptr(self.slot_unit), _ptr(self.slot_last),
+                                 _ptr(self.unit_slot))
+
+
+def sd_delta_select(shape: SdShape, sel: SdSelect, scores, idx, idx_stride: int, count,
+                    admit_cap: int, step: int, res: Resident, plan_slot, plan_unit, plan_evict,
+                    plan_count, pool_idx, pool_stride: int, pool_count, stream=None) -> None:
+    _check(lib().sd_delta_select(ctypes.byref(shape), ctypes.byref(sel), _ptr(scores), _ptr(idx),
+                                 idx_stride, _ptr(count), admit_cap, step, ctypes.byref(res.c),
+                                 _ptr(plan_slot), _ptr(plan_unit), _ptr(plan_evict),
+                                 _ptr(plan_count), _ptr(pool_idx), pool_stride, _ptr(pool_count),
+                                 _stream(stream)), "sd_delta_select")
+
+
+def sd_resident_gather(shape: SdShape, block: int, K, V, plan_slot, plan_unit, plan_count,
+                       admit_cap: int, n_slots: int, K_pool, V_pool, stream=None) -> None:
+    _check(lib().sd_resident_gather(ctypes.byref(shape), block, _ptr(K), _ptr(V), _ptr(plan_slot),
+                                    _ptr(plan_unit), _ptr(plan_count), admit_cap, n_slots,
+                                    _ptr(K_pool), _ptr(V_pool), _stream(stream)),
+           "sd_resident_gather")
 
 
 def sd_event_wait(event, timeout_us: int) -> None:

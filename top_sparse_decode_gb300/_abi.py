@@ -29,6 +29,11 @@ class SdEncoder(ctypes.Structure):
                 ("W2", ctypes.c_void_p), ("b2", ctypes.c_void_p)]
 
 
+class SdResident(ctypes.Structure):
+    _fields_ = [("n_slots", ctypes.c_int32), ("slot_unit", ctypes.c_void_p),
+                ("slot_last", ctypes.c_void_p), ("unit_slot", ctypes.c_void_p)]
+
+
 class SdSelect(ctypes.Structure):
     _fields_ = [("k", ctypes.c_int32), ("sink", ctypes.c_int32), ("local", ctypes.c_int32),
                 ("block", ctypes.c_int32)]
@@ -37,6 +42,7 @@ class SdSelect(ctypes.Structure):
 # name -> (restype, argtypes); the same list as include/sd.h
 _p, _i, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
 _PS, _PE, _PL = ctypes.POINTER(SdShape), ctypes.POINTER(SdEncoder), ctypes.POINTER(SdSelect)
+_PR = ctypes.POINTER(SdResident)
 SIGNATURES = {
     "sd_build_index": (_i, [_i, _PS, _p, _PE, _p, _p, _p]),
     "sd_append_index": (_i, [_i, _PS, _i64, _p, _PE, _p, _p, _p]),
@@ -60,6 +66,10 @@ SIGNATURES = {
     "sd_gather_attend_noalloc": (_i, [_PS, _p, _p, _p, _p, _i64, _p, _i64, ctypes.c_float, _p,
                                       _p, _p]),
     "sd_offload_gather": (_i, [_PS, _p, _p, _p, _p, _p, _p]),
+    "sd_delta_select": (_i, [_PS, _PL, _p, _p, _i64, _p, ctypes.c_int32, ctypes.c_int32, _PR,
+                             _p, _p, _p, _p, _p, _i64, _p, _p]),
+    "sd_resident_gather": (_i, [_PS, ctypes.c_int32, _p, _p, _p, _p, _p, ctypes.c_int32,
+                                ctypes.c_int32, _p, _p, _p]),
     "sd_event_wait": (_i, [_p, _i64]),
     "sd_last_error": (ctypes.c_char_p, []),
     "sd_version": (_i, []),

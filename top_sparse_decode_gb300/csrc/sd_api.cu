@@ -476,6 +476,97 @@ int sd_offload_gather(const sd_shape* shape, const uint32_t* host_planes,
                                dev_planes, dev_scales, (cudaStream_t)stream);
 }
 
+int sd_delta_select(const sd_shape* shape, const sd_select* sel, const float* scores,
+                    const int32_t* idx, int64_t idx_stride, const int32_t* count,
+                    int32_t admit_cap, int32_t step, const sd_resident* res,
+                    int32_t* plan_slot, int32_t* plan_unit, int32_t* plan_evict,
+                    int32_t* plan_count, int32_t* pool_idx, int64_t pool_stride,
+                    int32_t* pool_count, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s);
+  if (rc) return rc;
+  if (!sel || sel->block < 1 || sel->block > 4096)
+    return fail(SD_ERR_INVALID_ARG, "sd_delta_select: sel is NULL or sel.block outside [1, 4096]");
+  if (sel->k < 1 || sel->sink < 0 || sel->local < 0)
+    return fail(SD_ERR_INVALID_ARG, "sd_delta_select: bad k, sink or local");
+  if (!scores || !idx || !count || !res || !plan_count || !pool_idx || !pool_count)
+    return fail(SD_ERR_INVALID_ARG, "sd_delta_select: NULL input");
+  if (!res->slot_unit || !res->slot_last || !res->unit_slot)
+    return fail(SD_ERR_INVALID_ARG, "sd_delta_select: NULL resident-set array");
+  if (res->n_slots < 1 || res->n_slots > kDsMaxSlots)
+    return fail(SD_ERR_UNSUPPORTED, "sd_delta_select: n_slots = %d outside [1, %d]",
+                res->n_slots, kDsMaxSlots);
+  if (admit_cap < 0 || admit_cap > kDsMaxUnits)
+    return fail(SD_ERR_INVALID_ARG, "sd_delta_select: admit_cap = %d outside [0, %d]", admit_cap,
+                kDsMaxUnits);
+  if (admit_cap > 0 && (!plan_slot || !plan_unit || !plan_evict))
+    return fail(SD_ERR_INVALID_ARG, "sd_delta_select: NULL plan array");
+  if (step < 0 || step >= 0x7FFFFFFF)
+    return fail(SD_ERR_INVALID_ARG, "sd_delta_select: step = %d outside [0, 2^31 - 2]", step);
+  const int64_t nu = (s.n + sel->block - 1) / sel->block;
+  const int64_t units = imin64(nu, (int64_t)sel->sink + sel->local + sel->k);
+  if (units > kDsMaxUnits)
+    return fail(SD_ERR_UNSUPPORTED, "sd_delta_select: up to %lld predicted units (limit %d)",
+                (long long)units, kDsMaxUnits);
+  if (idx_stride < units * sel->block || pool_stride < units * sel->block)
+    return fail(SD_ERR_INVALID_ARG, "sd_delta_select: idx_stride and pool_stride must be at "
+                "least %lld", (long long)(units * sel->block));
+  return launch_delta_select((int64_t)s.B * s.Hkv, nu, s.n, sel->block, sel->sink, sel->local,
+                             scores, idx, idx_stride, count, admit_cap, step, res->n_slots,
+                             res->slot_unit, res->slot_last, res->unit_slot, plan_slot,
+                             plan_unit, plan_evict, plan_count, pool_idx, pool_stride,
+                             pool_count, (cudaStream_t)stream);
+}
+
+// A device address for p: device memory as it is, pinned host memory through its
+// mapping; anything else is refused.
+static int device_view(const char* fn, const void* p, const void** out) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SD_ERR_INVALID_ARG, "%s: cannot query pointer: %s", fn, cudaGetErrorString(e));
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return SD_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *out = a.devicePointer;
+    return SD_OK;
+  }
+  return fail(SD_ERR_INVALID_ARG, "%s: K and V must be device or pinned host memory", fn);
+}
+
+int sd_resident_gather(const sd_shape* shape, int32_t block, const void* K, const void* V,
+                       const int32_t* plan_slot, const int32_t* plan_unit,
+                       const int32_t* plan_count, int32_t admit_cap, int32_t n_slots,
+                       void* K_pool, void* V_pool, void* stream) {
+  Dims s;
+  int rc = check_shape(shape, &s);
+  if (rc) return rc;
+  if (block < 1 || block > 4096)
+    return fail(SD_ERR_INVALID_ARG, "sd_resident_gather: block = %d outside [1, 4096]", block);
+  if (n_slots < 1 || n_slots > kDsMaxSlots)
+    return fail(SD_ERR_UNSUPPORTED, "sd_resident_gather: n_slots = %d outside [1, %d]", n_slots,
+                kDsMaxSlots);
+  if (admit_cap < 0 || admit_cap > kDsMaxUnits)
+    return fail(SD_ERR_INVALID_ARG, "sd_resident_gather: admit_cap = %d outside [0, %d]",
+                admit_cap, kDsMaxUnits);
+  if (!K || !V || !plan_count || !K_pool || !V_pool ||
+      (admit_cap > 0 && (!plan_slot || !plan_unit)))
+    return fail(SD_ERR_INVALID_ARG, "sd_resident_gather: NULL input");
+  if (!aligned16(K) || !aligned16(V) || !aligned16(K_pool) || !aligned16(V_pool))
+    return fail(SD_ERR_INVALID_ARG, "sd_resident_gather: K, V and the pools must be 16-byte "
+                "aligned");
+  const void *dk = nullptr, *dv = nullptr;
+  if ((rc = device_view("sd_resident_gather", K, &dk))) return rc;
+  if ((rc = device_view("sd_resident_gather", V, &dv))) return rc;
+  return launch_resident_gather(s, block, (const uint16_t*)dk, (const uint16_t*)dv, plan_slot,
+                                plan_unit, plan_count, admit_cap, n_slots, (uint16_t*)K_pool,
+                                (uint16_t*)V_pool, (cudaStream_t)stream);
+}
+
 int sd_event_wait(void* event, int64_t timeout_us) {
   if (!event || timeout_us < 0) return fail(SD_ERR_INVALID_ARG, "sd_event_wait: bad argument");
   auto t0 = std::chrono::steady_clock::now();

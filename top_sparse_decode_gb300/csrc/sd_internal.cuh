@@ -70,6 +70,22 @@ int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaSt
                         int64_t t0 = 0);
 int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode, int budget,
                 uint8_t* plan, cudaStream_t st);
+
+// Delta selection against a resident set and the gather of admitted units
+// (sd_resident.cu).
+constexpr int kDsMaxUnits = 8192;  // predicted units per row
+constexpr int kDsMaxSlots = 4096;  // resident slots per row
+int launch_delta_select(int64_t rows, int64_t nu, int64_t n_tokens, int block, int sink,
+                        int local, const float* scores, const int32_t* idx, int64_t idx_stride,
+                        const int32_t* count, int C, int step, int R, int32_t* slot_unit,
+                        int32_t* slot_last, int32_t* unit_slot, int32_t* plan_slot,
+                        int32_t* plan_unit, int32_t* plan_evict, int32_t* plan_count,
+                        int32_t* pool_idx, int64_t pool_stride, int32_t* pool_count,
+                        cudaStream_t st);
+int launch_resident_gather(const Dims& s, int block, const uint16_t* K, const uint16_t* V,
+                           const int32_t* plan_slot, const int32_t* plan_unit,
+                           const int32_t* plan_count, int C, int R, uint16_t* Kp, uint16_t* Vp,
+                           cudaStream_t st);
 int launch_score_hamming(const Dims& s, const uint32_t* sig, const uint32_t* qsig,
                          int32_t* scores, cudaStream_t st);
 // (cand: the fused scan + top-k's candidate marks, or null; plan_in: compute the
