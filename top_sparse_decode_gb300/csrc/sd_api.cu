@@ -512,7 +512,7 @@ int sd_delta_select(const sd_shape* shape, const sd_select* sel, const float* sc
     return fail(SD_ERR_INVALID_ARG, "sd_delta_select: idx_stride and pool_stride must be at "
                 "least %lld", (long long)(units * sel->block));
   return launch_delta_select((int64_t)s.B * s.Hkv, nu, s.n, sel->block, sel->sink, sel->local,
-                             scores, idx, idx_stride, count, admit_cap, step, res->n_slots,
+                             sel->k, scores, idx, idx_stride, count, admit_cap, step, res->n_slots,
                              res->slot_unit, res->slot_last, res->unit_slot, plan_slot,
                              plan_unit, plan_evict, plan_count, pool_idx, pool_stride,
                              pool_count, (cudaStream_t)stream);

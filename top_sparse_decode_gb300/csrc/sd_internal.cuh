@@ -76,7 +76,7 @@ int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode,
 constexpr int kDsMaxUnits = 8192;  // predicted units per row
 constexpr int kDsMaxSlots = 4096;  // resident slots per row
 int launch_delta_select(int64_t rows, int64_t nu, int64_t n_tokens, int block, int sink,
-                        int local, const float* scores, const int32_t* idx, int64_t idx_stride,
+                        int local, int sel_k, const float* scores, const int32_t* idx, int64_t idx_stride,
                         const int32_t* count, int C, int step, int R, int32_t* slot_unit,
                         int32_t* slot_last, int32_t* unit_slot, int32_t* plan_slot,
                         int32_t* plan_unit, int32_t* plan_evict, int32_t* plan_count,

@@ -9,8 +9,9 @@
 // top-k output into shared memory; hits are found through the unit -> slot map;
 // the a = min(C, misses, targets) admissions are made one round at a time, each a
 // block-wide arg-max over the misses' admission keys and arg-min over the free
-// slots' (last selected, slot) keys.  C is small in practice (a fetch ratio of a
-// few percent of K), so a round per admission costs less than sorting either list.
+// slots' (last selected, slot) keys, both cached in shared memory.  C is small in
+// practice (a fetch ratio of a few percent of K), so a round per admission costs
+// less than sorting either list.
 #include "sd_internal.cuh"
 
 namespace sd {
@@ -18,31 +19,20 @@ namespace sd {
 constexpr int kDsThreads = 256;
 constexpr int kDsWarps = kDsThreads / 32;
 
-struct DsSmem {
-  int32_t P[kDsMaxUnits];      // predicted units, ascending
-  int32_t pslot[kDsMaxUnits];  // slot after the step; -1 a miss not admitted (yet)
-  uint8_t busy[kDsMaxSlots];   // holds a predicted unit, or taken as a target
+// Shared memory: the reduction scratch, then per predicted unit its admission key
+// mkey (0 once resident or admitted), the unit P (ascending) and its slot after the
+// step pslot (-1 while not resident), then per slot the unit it holds and its target
+// key (last selected + 1, slot), ~0 once it holds a predicted unit.  Sized by the
+// launch's bounds (maxP = min(n_units, sink + local + k)): at OasisKV's 129 units
+// and 129 slots a CTA needs under 4 KB, so every row of a large batch runs at once,
+// and the admission rounds touch shared memory only.
+struct DsHead {
   unsigned long long red[2][kDsWarps];
   int wtot[kDsWarps];
-  int np;
 };
 
-// Exclusive position of this thread's flag among the CTA's flags, in thread order,
-// and the CTA's total (two barriers).
-__device__ __forceinline__ int ds_rank(bool flag, int* wtot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t m = __ballot_sync(0xFFFFFFFFu, flag);
-  if (lane == 0) wtot[warp] = __popc(m);
-  __syncthreads();
-  int before = 0, all = 0;
-#pragma unroll
-  for (int w = 0; w < kDsWarps; ++w) {
-    before += w < warp ? wtot[w] : 0;
-    all += wtot[w];
-  }
-  __syncthreads();  // wtot is reused by the next call
-  *total = all;
-  return before + __popc(m & ((1u << lane) - 1u));
+__host__ __device__ __forceinline__ size_t ds_smem_bytes(int maxP, int R) {
+  return sizeof(DsHead) + 16 * (size_t)maxP + 12 * (size_t)R;
 }
 
 // Exclusive prefix of v over the CTA in thread order, and the total.
@@ -68,7 +58,7 @@ __device__ __forceinline__ int ds_scan(int v, int* wtot, int* total) {
 }
 
 __global__ void __launch_bounds__(kDsThreads)
-delta_select_kernel(int64_t nu, int64_t n_tokens, int block, int sink, int local,
+delta_select_kernel(int maxP, int64_t nu, int64_t n_tokens, int block, int sink, int local,
                     const float* __restrict__ scores, const int32_t* __restrict__ idx,
                     int64_t idx_stride, const int32_t* __restrict__ count, int C, int step,
                     int R, int32_t* __restrict__ slot_unit, int32_t* __restrict__ slot_last,
@@ -77,13 +67,19 @@ delta_select_kernel(int64_t nu, int64_t n_tokens, int block, int sink, int local
                     int32_t* __restrict__ plan_count, int32_t* __restrict__ pool_idx,
                     int64_t pool_stride, int32_t* __restrict__ pool_count) {
   extern __shared__ __align__(16) uint8_t ds_raw[];
-  DsSmem& S = *reinterpret_cast<DsSmem*>(ds_raw);
+  DsHead& S = *reinterpret_cast<DsHead*>(ds_raw);
+  unsigned long long* mkey = reinterpret_cast<unsigned long long*>(ds_raw + sizeof(DsHead));
+  unsigned long long* skey = mkey + maxP;
+  int32_t* P = reinterpret_cast<int32_t*>(skey + R);
+  int32_t* pslot = P + maxP;
+  int32_t* sunit = pslot + maxP;
   const int64_t row = blockIdx.x;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   int32_t* su = slot_unit + row * R;
   int32_t* sl = slot_last + row * R;
   int32_t* us = unit_slot + row * nu;
   const float* sc = scores + row * nu;
+  const int32_t* ir = idx + row * idx_stride;
   const int c = (int)min((int64_t)count[row], idx_stride);
   if (c < 0) {  // a NaN score in the row: nothing changes
     if (t == 0) {
@@ -92,36 +88,54 @@ delta_select_kernel(int64_t nu, int64_t n_tokens, int block, int sink, int local
     }
     return;
   }
-  // the predicted units: the tokens that start a unit, in the top-k's (ascending) order
-  int np = 0;
-  for (int base = 0; base < c; base += kDsThreads) {
-    int u = -1;
-    if (base + t < c) {
-      const int32_t tok = idx[row * idx_stride + base + t];
-      if (tok >= 0 && tok < n_tokens && tok % block == 0 && tok / block < nu) u = tok / block;
-    }
-    int tot;
-    const int pos = np + ds_rank(u >= 0, S.wtot, &tot);
-    if (u >= 0 && pos < kDsMaxUnits) S.P[pos] = u;
-    np = min(np + tot, kDsMaxUnits);
+  // the slots' state, once
+  for (int s = t; s < R; s += kDsThreads) {
+    sunit[s] = su[s];
+    skey[s] = ((unsigned long long)(uint32_t)(sl[s] + 1) << 32) | (uint32_t)s;
   }
-  for (int s = t; s < R; s += kDsThreads) S.busy[s] = 0;
+  // the predicted units: the tokens that start a unit, in the top-k's (ascending)
+  // order; thread t takes the contiguous segment [t * per, (t + 1) * per) of the list
+  const int per = (c + kDsThreads - 1) / kDsThreads;
+  const int i0 = min(t * per, c), i1 = min(i0 + per, c);
+  auto unit_of = [&](int32_t tok) -> int {
+    return (tok >= 0 && tok < n_tokens && tok % block == 0 && tok / block < nu) ? tok / block
+                                                                                 : -1;
+  };
+  int mine_n = 0;
+  for (int i = i0; i < i1; ++i) mine_n += unit_of(ir[i]) >= 0;
+  int np;
+  int pos = ds_scan(mine_n, S.wtot, &np);
+  for (int i = i0; i < i1; ++i) {
+    const int u = unit_of(ir[i]);
+    if (u >= 0) {
+      if (pos < maxP) P[pos] = u;
+      ++pos;
+    }
+  }
+  np = min(np, maxP);
   __syncthreads();
   // hits: resident predicted units (a map entry that disagrees with its slot counts
-  // as not resident); they refresh their slot's last-selected step
+  // as not resident) refresh their slot's last-selected step; misses get their
+  // admission key: forced units first, then score descending, unit ascending (the
+  // unit sits in the low bits, so keys are unique and never 0)
   int my_hits = 0, my_miss = 0;
   for (int i = t; i < np; i += kDsThreads) {
-    const int u = S.P[i];
+    const int u = P[i];
     const int s = us[u];
-    const bool hit = s >= 0 && s < R && su[s] == u;
+    const bool hit = s >= 0 && s < R && sunit[s] == u;
+    unsigned long long key = 0ull;
     if (hit) {
-      S.busy[s] = 1;
+      skey[s] = ~0ull;
       sl[s] = step;
       ++my_hits;
     } else {
+      const bool forced = u < sink || (int64_t)u >= nu - local;
+      key = forced ? (1ull << 63) | (0x7FFFFFFFull - (unsigned)u)
+                   : ((unsigned long long)key_of_f32(sc[u]) << 31) | (0x7FFFFFFFull - (unsigned)u);
       ++my_miss;
     }
-    S.pslot[i] = hit ? s : -1;
+    mkey[i] = key;
+    pslot[i] = hit ? s : -1;
   }
   int hits, misses;
   ds_scan(my_hits, S.wtot, &hits);
@@ -129,29 +143,18 @@ delta_select_kernel(int64_t nu, int64_t n_tokens, int block, int sink, int local
   const int a = min(C, min(misses, R - hits));
   int made = 0;
   for (int i = 0; i < a; ++i) {
-    // the best remaining miss: forced units first, then score descending, unit
-    // ascending (keys are unique: the unit is in the low bits; 0 means none)
-    unsigned long long bm = 0ull;
+    // the best remaining miss and the oldest free slot (empty slots hold key 0 in
+    // their high half, so they come first)
+    unsigned long long bm = 0ull, bt = ~0ull;
     int bj = -1;
     for (int j = t; j < np; j += kDsThreads) {
-      if (S.pslot[j] != -1) continue;
-      const int u = S.P[j];
-      const bool forced = u < sink || (int64_t)u >= nu - local;
-      const unsigned long long key =
-          forced ? (1ull << 63) | (0x7FFFFFFFull - (unsigned)u)
-                 : ((unsigned long long)key_of_f32(sc[u]) << 31) | (0x7FFFFFFFull - (unsigned)u);
-      if (key > bm) {
-        bm = key;
+      const unsigned long long k = mkey[j];
+      if (k > bm) {
+        bm = k;
         bj = j;
       }
     }
-    // the oldest free slot: (last selected + 1, slot) ascending (empty slots hold -1)
-    unsigned long long bt = ~0ull;
-    for (int s = t; s < R; s += kDsThreads) {
-      if (S.busy[s]) continue;
-      const unsigned long long key = ((unsigned long long)(uint32_t)(sl[s] + 1) << 32) | (uint32_t)s;
-      bt = min(bt, key);
-    }
+    for (int s = t; s < R; s += kDsThreads) bt = min(bt, skey[s]);
     const unsigned long long mine = bm;  // this thread's own best miss
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -171,16 +174,20 @@ delta_select_kernel(int64_t nu, int64_t n_tokens, int block, int sink, int local
     }
     if (wm == 0ull || wt == ~0ull) break;  // no miss or no free slot left (uniform)
     const int s = (int)(uint32_t)wt;
-    if (bj >= 0 && mine == wm) S.pslot[bj] = s;  // the winning miss's owner
+    if (bj >= 0 && mine == wm) {  // the winning miss's owner
+      mkey[bj] = 0ull;
+      pslot[bj] = s;
+    }
     if (t == 0) {
       const int u = (int)(0x7FFFFFFFull - (wm & 0x7FFFFFFFull));
-      const int old = su[s];
+      const int old = sunit[s];
       const bool had = old >= 0 && old < nu;
-      if (had && us[old] == s) us[old] = -1;  // evicted: no longer resident
+      if (had) us[old] = -1;  // evicted: no longer resident
       su[s] = u;
       sl[s] = step;
       us[u] = s;
-      S.busy[s] = 1;
+      sunit[s] = u;
+      skey[s] = ~0ull;
       plan_slot[row * C + i] = s;
       plan_unit[row * C + i] = u;
       plan_evict[row * C + i] = had ? old : -1;
@@ -194,9 +201,9 @@ delta_select_kernel(int64_t nu, int64_t n_tokens, int block, int sink, int local
   for (int base = 0; base < np; base += kDsThreads) {
     const int i = base + t;
     int len = 0, s = -1, u = 0;
-    if (i < np && S.pslot[i] >= 0) {
-      s = S.pslot[i];
-      u = S.P[i];
+    if (i < np && pslot[i] >= 0) {
+      s = pslot[i];
+      u = P[i];
       len = (int)min((int64_t)block, n_tokens - (int64_t)u * block);
     }
     int tot;
@@ -208,20 +215,19 @@ delta_select_kernel(int64_t nu, int64_t n_tokens, int block, int sink, int local
   if (t == 0) pool_count[row] = (int32_t)min(base_rows, pool_stride);
 }
 
-size_t delta_select_smem() { return sizeof(DsSmem); }
-
 int launch_delta_select(int64_t rows, int64_t nu, int64_t n_tokens, int block, int sink,
-                        int local, const float* scores, const int32_t* idx, int64_t idx_stride,
+                        int local, int sel_k, const float* scores, const int32_t* idx, int64_t idx_stride,
                         const int32_t* count, int C, int step, int R, int32_t* slot_unit,
                         int32_t* slot_last, int32_t* unit_slot, int32_t* plan_slot,
                         int32_t* plan_unit, int32_t* plan_evict, int32_t* plan_count,
                         int32_t* pool_idx, int64_t pool_stride, int32_t* pool_count,
                         cudaStream_t st) {
-  if (int rc = set_smem_limit((const void*)delta_select_kernel, sizeof(DsSmem),
-                              "delta_select: smem attribute"))
+  const int maxP = (int)imin64(nu, (int64_t)sink + local + sel_k);
+  const size_t smem = ds_smem_bytes(maxP, R);
+  if (int rc = set_smem_limit((const void*)delta_select_kernel, smem, "delta_select: smem attribute"))
     return rc;
-  delta_select_kernel<<<(unsigned)rows, kDsThreads, sizeof(DsSmem), st>>>(
-      nu, n_tokens, block, sink, local, scores, idx, idx_stride, count, C, step, R, slot_unit,
+  delta_select_kernel<<<(unsigned)rows, kDsThreads, smem, st>>>(
+      maxP, nu, n_tokens, block, sink, local, scores, idx, idx_stride, count, C, step, R, slot_unit,
       slot_last, unit_slot, plan_slot, plan_unit, plan_evict, plan_count, pool_idx, pool_stride,
       pool_count);
   note_launches(1);
