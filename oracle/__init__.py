@@ -83,6 +83,10 @@ def _l():
             lib.orc_delta_select.argtypes = [i64, i64, i64, i32, i32, i32, p, p, i64, p, i32,
                                              i64, i32, p, p, p, p, p, p, p, p, i64, p]
             lib.orc_delta_select.restype = i32
+            lib.orc_landmark_build.argtypes = [p, i64, i32, i64, i32, i32, p]
+            lib.orc_landmark_build.restype = None
+            lib.orc_landmark_score.argtypes = [p, p, i64, i32, i32, i64, i32, p, p]
+            lib.orc_landmark_score.restype = None
             _lib = lib
     return _lib
 
@@ -199,6 +203,30 @@ def quest_score(summ, q, with_l1: bool = False):
     U = np.empty((B, Hkv, nblk), np.float64)
     l1 = np.empty((B, Hkv, nblk), np.float64)
     _l().orc_quest_score(ps, pq, B, Hq, Hkv, nblk, d, U.ctypes.data, l1.ctypes.data)
+    return (U, l1) if with_l1 else U
+
+
+LANDMARK_BLOCK = 8
+
+
+def landmark_build(K: np.ndarray, blk: int = LANDMARK_BLOCK) -> np.ndarray:
+    """K bf16 [B][Hkv][n][d] -> landmarks bf16 [B][Hkv][ceil(n/blk)][d] (block means)."""
+    K, pk = _c(K, np.uint16)
+    B, Hkv, n, d = K.shape
+    out = np.empty((B, Hkv, (n + blk - 1) // blk, d), np.uint16)
+    _l().orc_landmark_build(pk, B, Hkv, n, d, blk, out.ctypes.data)
+    return out
+
+
+def landmark_score(L, q, with_l1: bool = False):
+    """L bf16 [B][Hkv][nblk][d], q bf16 [B][Hq][d] -> U float64 [B][Hkv][nblk]."""
+    L, pl = _c(L, np.uint16)
+    q, pq = _c(q, np.uint16)
+    B, Hkv, nblk, d = L.shape
+    Hq = q.shape[1]
+    U = np.empty((B, Hkv, nblk), np.float64)
+    l1 = np.empty((B, Hkv, nblk), np.float64)
+    _l().orc_landmark_score(pl, pq, B, Hq, Hkv, nblk, d, U.ctypes.data, l1.ctypes.data)
     return (U, l1) if with_l1 else U
 
 

@@ -710,3 +710,62 @@ int orc_delta_select(int64_t rows, int64_t nu, int64_t n_tokens, int block, int 
   free(taken);
   return 0;
 }
+
+/* ------------------------------------------------------------------------------ */
+/* F2  block landmarks  [FA results: the "8-token block landmark" scan, a          */
+/*     comparison point the 56-bit read is timed against]                          */
+/* ------------------------------------------------------------------------------ */
+/*
+ * READING: the page names the scan and its 8-token blocks only.  The landmark of a
+ * block is taken as the mean of its keys: per channel the fp32 sum of the block's
+ * held tokens in token order, divided (fp32, IEEE) by their count and rounded to
+ * bf16 (nearest, ties to even); a short last block averages the tokens it holds.
+ * The block's score is the summed group query's dot product with its landmark,
+ * sum_g sum_j q_gj L_j (here in double), like every other scorer's group sum.
+ */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+void orc_landmark_build(const uint16_t* K, int64_t B, int Hkv, int64_t n, int d, int blk,
+                        uint16_t* L) {
+  int64_t nblk = (n + blk - 1) / blk;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      const uint16_t* Kh = K + (b * Hkv + h) * n * d;
+      for (int64_t c = 0; c < nblk; ++c) {
+        int64_t t1 = (c + 1) * blk < n ? (c + 1) * blk : n;
+        float cnt = (float)(t1 - c * blk);
+        for (int j = 0; j < d; ++j) {
+          float s = 0.0f;
+          for (int64_t t = c * blk; t < t1; ++t) s += bf16_to_f32(Kh[t * d + j]);
+          L[((b * Hkv + h) * nblk + c) * d + j] = f32_to_bf16_rne(s / cnt);
+        }
+      }
+    }
+}
+
+void orc_landmark_score(const uint16_t* L, const uint16_t* q, int64_t B, int Hq, int Hkv,
+                        int64_t nblk, int d, double* U, double* l1) {
+  int G = Hq / Hkv;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h)
+      for (int64_t c = 0; c < nblk; ++c) {
+        const uint16_t* lm = L + ((b * Hkv + h) * nblk + c) * d;
+        double acc = 0.0, mass = 0.0;
+        for (int g = 0; g < G; ++g)
+          for (int j = 0; j < d; ++j) {
+            double v = (double)bf16_to_f32(q[(b * Hq + h * G + g) * d + j]) * bf16_to_f32(lm[j]);
+            acc += v;
+            mass += fabs(v);
+          }
+        U[(b * Hkv + h) * nblk + c] = acc;
+        if (l1) l1[(b * Hkv + h) * nblk + c] = mass;
+      }
+}

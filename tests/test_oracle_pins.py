@@ -609,3 +609,47 @@ def test_delta_select_invariants_random():
             rows_exp = [int(st.unit_slot[r, u]) * block + t for u in P if st.unit_slot[r, u] >= 0
                         for t in range(min(block, n_tok - u * block))]
             assert list(pool[r, :pcount[r]]) == rows_exp
+
+
+# ---------------------------------------------------------------------------------
+# F2 8-token block landmarks (Fathom, results: the block-landmark comparison scan)
+# ---------------------------------------------------------------------------------
+def test_landmark_is_block_mean():
+    """Keys on a coarse grid (every fp32 sum exact) and block counts that are powers
+    of two (every quotient exact): the landmark equals the numpy mean of the held
+    tokens rounded once to bf16, for full blocks and a short last block of 4."""
+    rng = np.random.default_rng(21)
+    n, d = 8 * 5 + 4, 16
+    vals = rng.integers(-64, 65, size=(1, 2, n, d)).astype(np.float64) / 8.0
+    K = synth.to_bf16(vals)
+    L = synth.bf16_to_f64(oracle.landmark_build(K))
+    k = synth.bf16_to_f64(K)
+    for c in range(6):
+        blkv = k[:, :, 8 * c:min(8 * c + 8, n)]
+        ref = synth.bf16_to_f64(synth.to_bf16(blkv.mean(axis=2)))
+        assert np.array_equal(L[:, :, c], ref), c
+
+
+def test_landmark_of_identical_keys_is_the_key():
+    rng = np.random.default_rng(22)
+    row = synth.to_bf16(rng.normal(size=128) * 3)
+    K = np.broadcast_to(row, (1, 1, 24, 128)).copy()
+    L = oracle.landmark_build(K)
+    assert np.array_equal(L[0, 0], np.broadcast_to(row, (3, 128)))
+
+
+def test_landmark_score_is_group_dot_product():
+    """U = sum_g <q_g, L> against numpy's matmul; a one-hot query reads one channel."""
+    cfg = synth.config(0, n=8 * 40, Hq=8, Hkv=2, B=2)
+    inp = synth.make_inputs(cfg, with_v=False)
+    L = oracle.landmark_build(inp.K)
+    U, l1 = oracle.landmark_score(L, inp.q, with_l1=True)
+    q = synth.bf16_to_f64(inp.q).reshape(2, 2, 4, 128)
+    Lf = synth.bf16_to_f64(L)
+    ref = np.einsum("bhgj,bhcj->bhc", q, Lf)
+    assert np.allclose(U, ref, rtol=0, atol=1e-9 * np.abs(ref).max())
+    assert np.allclose(l1, np.einsum("bhgj,bhcj->bhc", np.abs(q), np.abs(Lf)), rtol=1e-12)
+    onehot = np.zeros((1, 1, 128), np.float64)
+    onehot[0, 0, 37] = 1.0
+    U1 = oracle.landmark_score(L[:1, :1], synth.to_bf16(onehot))
+    assert np.array_equal(U1[0, 0], Lf[0, 0, :, 37])
