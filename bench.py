@@ -570,6 +570,21 @@ def main():
                                "scan_GBps": bf / (tfs * 1e-3) / 1e9,
                                "scan_frac_hbm": bf / (tfs * 1e-3) / 1e9 / peak_gbs}
             del stf
+        # the 8-token block landmark scan (256 B of landmark per 8 tokens per KV head),
+        # top-64 blocks (512 tokens), gather-attend
+        scl = StepConfig(sd.SD_IDX_LANDMARK, B, Hq, Hkv, n, k=cfg.k // 8)
+        il = build_index(scl, K)
+        stl = DecodeStep(scl, K, V, il)
+        stl.run(q)
+        torch.cuda.synchronize()
+        tl = statistics.mean(timed_steps(torch, lambda: stl.run(q), K_st, 3, flush))
+        tls = statistics.mean(timed_steps(torch, lambda: stl.stage_score(q), K_st, 3, flush))
+        bl = B * Hkv * ((n + 7) // 8) * 128 * 2
+        variants["landmark8"] = {"us_per_step": tl * 1e3, "keys_per_s": keys / (tl * 1e-3),
+                                 "scan_us": tls * 1e3, "scan_bytes": bl,
+                                 "scan_GBps": bl / (tls * 1e-3) / 1e9,
+                                 "scan_frac_hbm": bl / (tls * 1e-3) / 1e9 / peak_gbs}
+        del stl, il
         # 32-bit Hamming (random projection), query map included
         sch = StepConfig(sd.SD_IDX_SIG, B, Hq, Hkv, n, k=cfg.k)
         enc = sd.make_encoder(dev_tensor(inp.W1, torch), dev_tensor(inp.b1, torch))

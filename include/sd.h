@@ -78,7 +78,12 @@ typedef struct sd_encoder {
   const float* b2;
 } sd_encoder;
 
-typedef enum { SD_IDX_SIG = 0, SD_IDX_PLANES = 1, SD_IDX_MINMAX = 2 } sd_index_kind;
+typedef enum {
+  SD_IDX_SIG = 0,
+  SD_IDX_PLANES = 1,
+  SD_IDX_MINMAX = 2,
+  SD_IDX_LANDMARK = 3
+} sd_index_kind;
 typedef enum {
   SD_PLAN_WATERFILL = 0,
   SD_PLAN_FIXED = 1,
@@ -106,6 +111,10 @@ typedef enum { SD_SCORE_I32 = 0, SD_SCORE_F32 = 1 } sd_score_type;
  *     [B][hkv][ceil(n_cap/16)][2][d]: per 16-token block the channel min row then
  *     the max row (exact keys; -0.0 orders below +0.0; the last block may be
  *     short).  out1 unused.
+ *   SD_IDX_LANDMARK (the Fathom page's 8-token block landmark scan, a comparison
+ *     point): out0 = bf16 landmarks [B][hkv][ceil(n_cap/8)][d]: per 8-token block
+ *     the fp32 sum of its held keys in token order, divided by their count (fp32)
+ *     and rounded to bf16 (nearest, ties to even).  out1 unused.
  */
 int sd_build_index(int kind, const sd_shape* shape, const void* K, const sd_encoder* enc,
                    void* out0, void* out1, void* stream);
@@ -171,6 +180,9 @@ int sd_plan(const sd_shape* shape, const void* q, const float* sigma2, int mode,
  *     bits cleared.  Only the first plan_j planes of channel j are read.
  *   SD_IDX_MINMAX (OasisKV/Quest bound): index0 = summaries, q_or_qsig = bf16
  *     q; scores fp32 [B*hkv][ceil(n/16)] = sum_g sum_j max(q_gj min_j, q_gj max_j).
+ *   SD_IDX_LANDMARK: index0 = landmarks, q_or_qsig = bf16 q; scores fp32
+ *     [B*hkv][ceil(n/8)] = sum_g sum_j q_gj L_j (computed as sum_j q~_j L_j with the
+ *     group sum q~ in fp32).
  */
 int sd_score(int kind, const sd_shape* shape, const void* index0, const void* index1,
              const void* q_or_qsig, const uint8_t* plan, void* scores, void* stream);

@@ -25,7 +25,7 @@ def sd():
     return m
 
 
-KINDS = ["sig", "sig_mlp", "planes", "minmax"]
+KINDS = ["sig", "sig_mlp", "planes", "minmax", "landmark"]
 
 
 def buffers(sd, kind, B, Hkv, ncap, fill):
@@ -40,6 +40,8 @@ def buffers(sd, kind, B, Hkv, ncap, fill):
     if kind == "planes":
         return full((B, Hkv, 128, 4, ncap // 32), np.uint32), full((B, Hkv, 128, ncap // 64),
                                                                  np.uint16)
+    if kind == "landmark":
+        return full((B, Hkv, (ncap + 7) // 8, 128), np.uint16), None
     return full((B, Hkv, (ncap + 15) // 16, 2, 128), np.uint16), None
 
 
@@ -52,6 +54,10 @@ def valid(kind, B, Hkv, ncap, n, o0, o1):
         p = host(o0, np.uint8).view(np.uint32).reshape(B, Hkv, 128, 4, ncap // 32)
         s = host(o1, np.uint8).view(np.uint16).reshape(B, Hkv, 128, ncap // 64)
         return [p[..., :2 * nb], s[..., :nb]]
+    if kind == "landmark":
+        nb = (n + 7) // 8
+        lm = host(o0, np.uint8).view(np.uint16).reshape(B, Hkv, (ncap + 7) // 8, 128)
+        return [lm[:, :, :nb]]
     nb = (n + 15) // 16
     m = host(o0, np.uint8).view(np.uint16).reshape(B, Hkv, (ncap + 15) // 16, 2, 128)
     return [m[:, :, :nb]]
@@ -59,7 +65,7 @@ def valid(kind, B, Hkv, ncap, n, o0, o1):
 
 def kind_id(sd, kind):
     return {"sig": sd.SD_IDX_SIG, "sig_mlp": sd.SD_IDX_SIG, "planes": sd.SD_IDX_PLANES,
-            "minmax": sd.SD_IDX_MINMAX}[kind]
+            "minmax": sd.SD_IDX_MINMAX, "landmark": sd.SD_IDX_LANDMARK}[kind]
 
 
 def setup(sd, kind, B, Hkv, ncap):
@@ -79,6 +85,8 @@ def oracle_index(kind, inp, n):
         return [oracle.sig_encode(K, inp.W1, inp.b1, inp.W2, inp.b2)]
     if kind == "planes":
         return list(oracle.plane_build(K))
+    if kind == "landmark":
+        return [oracle.landmark_build(K)]
     return [oracle.minmax_build(K)]
 
 

@@ -31,6 +31,9 @@ def step_config(sd, cfg, kind, plan_mode=0, budget=56):
     if kind == sd.SD_IDX_MINMAX:
         return StepConfig(kind, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.d, k=cfg.blk_k, sink=0,
                           local=cfg.blk_local)
+    if kind == sd.SD_IDX_LANDMARK:  # the token budget and windows in 8-token blocks
+        return StepConfig(kind, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.d, k=max(1, cfg.k // 8),
+                          sink=(cfg.sink + 7) // 8, local=(cfg.local + 7) // 8)
     return StepConfig(kind, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.d, k=cfg.k, sink=cfg.sink,
                       local=cfg.local, plan_mode=plan_mode, budget=budget)
 
@@ -65,6 +68,9 @@ def oracle_scores(cfg, inp, kind, plan_mode=0, budget=56):
         pl = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, plan_mode, budget)
         s, l1 = oracle.plane_score(p, sc, pl, inp.q, with_l1=True)
         return s.reshape(cfg.B * cfg.Hkv, -1), l1.reshape(cfg.B * cfg.Hkv, -1)
+    if kind == 3:
+        s, l1 = oracle.landmark_score(oracle.landmark_build(inp.K), inp.q, with_l1=True)
+        return s.reshape(cfg.B * cfg.Hkv, -1), l1.reshape(cfg.B * cfg.Hkv, -1)
     summ = oracle.minmax_build(inp.K)
     s, l1 = oracle.quest_score(summ, inp.q, with_l1=True)
     return s.reshape(cfg.B * cfg.Hkv, -1), l1.reshape(cfg.B * cfg.Hkv, -1)
@@ -97,9 +103,10 @@ def check_step(sd, cfg, inp, kind, plan_mode=0, budget=56, dev_in=None):
     # side metric: recall of the planted keys / blocks
     planted = inp.planted.reshape(rows, -1)
     hit = 0
+    per = sc.block if not cfg.block_mode else 1  # planted tokens -> units
     for r in range(rows):
         units = set((gi[r, :gc[r]] // sc.block).tolist())
-        hit += sum(int(p) in units for p in planted[r])
+        hit += sum(int(p) // per in units for p in planted[r])
     return hit / planted.size, err, dev_t
 
 
@@ -107,7 +114,7 @@ def test_cfg0_tiny_all_scorers(sd):
     cfg = synth.config(0)
     inp = synth.make_inputs(cfg)
     dev_in = (dev(inp.q), dev(inp.K), dev(inp.V))
-    for kind in (sd.SD_IDX_SIG, sd.SD_IDX_PLANES, sd.SD_IDX_MINMAX):
+    for kind in (sd.SD_IDX_SIG, sd.SD_IDX_PLANES, sd.SD_IDX_MINMAX, sd.SD_IDX_LANDMARK):
         check_step(sd, cfg, inp, kind, dev_in=dev_in)
 
 
@@ -116,7 +123,8 @@ def test_cfg0_ragged_sizes(sd):
     for n in (64 * 37, 16 * 53 + 7):
         cfg = synth.config(0, n=n, k=40, sink=3, local=17, blk_k=5)
         inp = synth.make_inputs(cfg)
-        kinds = [sd.SD_IDX_SIG, sd.SD_IDX_MINMAX] + ([sd.SD_IDX_PLANES] if n % 64 == 0 else [])
+        kinds = [sd.SD_IDX_SIG, sd.SD_IDX_MINMAX, sd.SD_IDX_LANDMARK] + \
+            ([sd.SD_IDX_PLANES] if n % 64 == 0 else [])
         for kind in kinds:
             check_step(sd, cfg, inp, kind)
 

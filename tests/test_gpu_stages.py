@@ -212,6 +212,44 @@ def test_quest_scores(sd, G, n):
 
 
 # --------------------------------------------------------------------------------------
+# 8-token block landmarks (Fathom's landmark comparison scan): build bit-exact,
+# scores within 1e-5 of the L1 mass
+# --------------------------------------------------------------------------------------
+@pytest.mark.parametrize("n,ncap", [(8 * 1000, 0), (8 * 777 + 5, 0), (1, 0), (4101, 4160)])
+def test_landmark_build_bit_exact(sd, n, ncap):
+    cfg = synth.config(3, B=2, Hq=8, Hkv=2, n=n, planted=0)
+    inp = synth.make_inputs(cfg, with_v=False)
+    ncap = ncap or n
+    Kp = np.zeros((cfg.B, cfg.Hkv, ncap, cfg.d), np.uint16)
+    Kp[:, :, :n] = inp.K
+    shp = shape_of(sd, cfg, n_cap=ncap)
+    L = torch.full((cfg.B, cfg.Hkv, (ncap + 7) // 8, cfg.d), 0x1234, dtype=torch.int16,
+                   device="cuda")
+    sd.sd_build_index(sd.SD_IDX_LANDMARK, shp, dev(Kp), None, L)
+    torch.cuda.synchronize()
+    nb = (n + 7) // 8
+    got = host(L, np.uint16)
+    assert np.array_equal(got[:, :, :nb], oracle.landmark_build(inp.K))
+    assert (got[:, :, nb:] == 0x1234).all()  # blocks past n are not written
+
+
+@pytest.mark.parametrize("G,n", [(4, 8 * 4096), (8, 8 * 100 + 3), (1, 8 * 33), (2, 8 * 5000)])
+def test_landmark_scores(sd, G, n):
+    cfg = synth.config(3, B=3, Hq=2 * G, Hkv=2, n=n, planted=0)
+    inp = synth.make_inputs(cfg, with_v=False)
+    shp = shape_of(sd, cfg)
+    ref_L = oracle.landmark_build(inp.K)
+    ref, l1 = oracle.landmark_score(ref_L, inp.q, with_l1=True)
+    L = empty(ref_L.shape, np.uint16)
+    sd.sd_build_index(sd.SD_IDX_LANDMARK, shp, dev(inp.K), None, L)
+    scores = empty(ref.shape, np.float32)
+    sd.sd_score(sd.SD_IDX_LANDMARK, shp, L, None, dev(inp.q), None, scores)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(L, np.uint16), ref_L)
+    check_scores(host(scores, np.float32), ref, l1, "landmark scores")
+
+
+# --------------------------------------------------------------------------------------
 # S6 top-k on identical generated scores: bit-exact against the oracle
 # --------------------------------------------------------------------------------------
 def run_topk(sd, scores_np, k, sink, local, block=1, n_tokens=None):

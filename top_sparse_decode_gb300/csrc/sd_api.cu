@@ -123,7 +123,8 @@ static int index_tokens(const char* fn, int kind, const sd_shape* shape, int64_t
     return fail(SD_ERR_UNSUPPORTED, "%s: bit planes need n_cap to be a multiple of 64", fn);
   if (kind == SD_IDX_PLANES && !out1)
     return fail(SD_ERR_INVALID_ARG, "%s: scales (out1) is NULL", fn);
-  if (kind != SD_IDX_SIG && kind != SD_IDX_PLANES && kind != SD_IDX_MINMAX)
+  if (kind != SD_IDX_SIG && kind != SD_IDX_PLANES && kind != SD_IDX_MINMAX &&
+      kind != SD_IDX_LANDMARK)
     return fail(SD_ERR_INVALID_ARG, "%s: unknown kind %d", fn, kind);
   if (t0 == s.n) return SD_OK;  // nothing appended
   cudaStream_t st = (cudaStream_t)stream;
@@ -132,6 +133,8 @@ static int index_tokens(const char* fn, int kind, const sd_shape* shape, int64_t
       return launch_sig_build(s, (const uint16_t*)K, *enc, (uint32_t*)out0, st, t0);
     case SD_IDX_PLANES:
       return launch_plane_build(s, (const uint16_t*)K, (uint32_t*)out0, (uint16_t*)out1, st, t0);
+    case SD_IDX_LANDMARK:
+      return launch_landmark_build(s, (const uint16_t*)K, (uint16_t*)out0, st, t0);
     default:
       return launch_minmax_build(s, (const uint16_t*)K, (uint16_t*)out0, st, t0);
   }
@@ -202,6 +205,9 @@ int sd_score(int kind, const sd_shape* shape, const void* index0, const void* in
     case SD_IDX_MINMAX:
       return launch_score_quest(s, (const uint16_t*)index0, (const uint16_t*)q_or_qsig,
                                 (float*)scores, st);
+    case SD_IDX_LANDMARK:
+      return launch_score_landmark(s, (const uint16_t*)index0, (const uint16_t*)q_or_qsig,
+                                   (float*)scores, st);
     default:
       return fail(SD_ERR_INVALID_ARG, "sd_score: unknown kind %d", kind);
   }

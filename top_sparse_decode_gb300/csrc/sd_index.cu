@@ -8,6 +8,8 @@
 //                   prerequisites, Quest-style per-block per-channel summaries
 #include <cuda_fp16.h>
 
+#include <cuda_bf16.h>
+
 #include "sd_internal.cuh"
 
 namespace sd {
@@ -380,6 +382,50 @@ int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaSt
   minmax_build_kernel<<<grid, 256, 0, st>>>(K, s.n, s.ncap, c0, summ);
   note_launches(1);
   return check_launch("minmax_build");
+}
+
+// =====================================================================================
+// Block landmarks (the Fathom page's 8-token block landmark scan): per block of 8
+// tokens the bf16 rounding (nearest even) of the fp32 mean of its held keys, summed
+// in token order.  One warp per block, lane l owns channels 4l..4l+3.
+// =====================================================================================
+__global__ void __launch_bounds__(256)
+landmark_build_kernel(const uint16_t* __restrict__ K, int64_t n, int64_t ncap, int64_t c0,
+                      uint16_t* __restrict__ L) {
+  const int64_t bh = blockIdx.y;
+  const int64_t c = c0 + (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t nblk_valid = (n + kLmBlock - 1) / kLmBlock;
+  const int64_t nblk_cap = (ncap + kLmBlock - 1) / kLmBlock;
+  if (c >= nblk_valid) return;
+  const int64_t t0 = c * kLmBlock, t1 = imin64(t0 + kLmBlock, n);
+  const uint16_t* Kb = K + bh * ncap * kD + lane * 4;
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int64_t t = t0; t < t1; ++t) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(Kb + t * kD));
+    s[0] = __fadd_rn(s[0], bf16_lo(v.x));
+    s[1] = __fadd_rn(s[1], bf16_hi(v.x));
+    s[2] = __fadd_rn(s[2], bf16_lo(v.y));
+    s[3] = __fadd_rn(s[3], bf16_hi(v.y));
+  }
+  const float cnt = (float)(t1 - t0);
+  uint32_t h[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    h[k] = __bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(s[k], cnt)));
+  uint2 out;
+  out.x = h[0] | (h[1] << 16);
+  out.y = h[2] | (h[3] << 16);
+  *reinterpret_cast<uint2*>(L + (bh * nblk_cap + c) * kD + lane * 4) = out;
+}
+
+int launch_landmark_build(const Dims& s, const uint16_t* K, uint16_t* L, cudaStream_t st,
+                          int64_t t0) {
+  const int64_t nblk = (s.n + kLmBlock - 1) / kLmBlock, c0 = t0 / kLmBlock;
+  dim3 grid((unsigned)((nblk - c0 + 7) / 8), (unsigned)(s.B * s.Hkv));
+  landmark_build_kernel<<<grid, 256, 0, st>>>(K, s.n, s.ncap, c0, L);
+  note_launches(1);
+  return check_launch("landmark_build");
 }
 
 }  // namespace sd

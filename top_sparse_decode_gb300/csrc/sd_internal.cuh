@@ -68,6 +68,11 @@ int launch_plane_build(const Dims& s, const uint16_t* K, uint32_t* planes, uint1
                        cudaStream_t st, int64_t t0 = 0);
 int launch_minmax_build(const Dims& s, const uint16_t* K, uint16_t* summ, cudaStream_t st,
                         int64_t t0 = 0);
+constexpr int kLmBlock = 8;  // tokens per landmark block
+int launch_landmark_build(const Dims& s, const uint16_t* K, uint16_t* L, cudaStream_t st,
+                          int64_t t0 = 0);
+int launch_score_landmark(const Dims& s, const uint16_t* L, const uint16_t* q, float* scores,
+                          cudaStream_t st);
 int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode, int budget,
                 uint8_t* plan, cudaStream_t st);
 

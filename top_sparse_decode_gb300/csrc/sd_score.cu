@@ -626,4 +626,69 @@ int launch_score_quest(const Dims& s, const uint16_t* summ, const uint16_t* q, f
   return check_launch("score_quest");
 }
 
+// =====================================================================================
+// Block landmark scan: U = sum_j q~_j L_j, q~ the group-summed query (fp32, g
+// ascending).  A warp scores 4 blocks (256 B each), lane l owning channels 4l..4l+3;
+// a CTA scores 32 blocks.
+// =====================================================================================
+template <int G>
+__global__ void __launch_bounds__(256)
+score_landmark_kernel(const uint16_t* __restrict__ L, const uint16_t* __restrict__ q, int Hq,
+                      int Hkv, int64_t n, int64_t ncap, float* __restrict__ scores) {
+  __shared__ float Qs[kD];
+  const int64_t bh = blockIdx.y;
+  const int b = (int)(bh / Hkv), h = (int)(bh % Hkv);
+  if (threadIdx.x < kD) {
+    float a = 0.0f;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      a = __fadd_rn(a, bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + threadIdx.x]));
+    Qs[threadIdx.x] = a;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nblk = (n + kLmBlock - 1) / kLmBlock, nblk_cap = (ncap + kLmBlock - 1) / kLmBlock;
+  float Q[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) Q[k] = Qs[lane * 4 + k];
+  const int64_t c0 = (int64_t)blockIdx.x * 32 + warp * 4;
+  float acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    acc[k] = 0.0f;
+    const int64_t c = c0 + k;
+    if (c < nblk) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(L + (bh * nblk_cap + c) * kD + lane * 4));
+      float a = 0.0f;
+      a = __fmaf_rn(Q[0], bf16_lo(v.x), a);
+      a = __fmaf_rn(Q[1], bf16_hi(v.x), a);
+      a = __fmaf_rn(Q[2], bf16_lo(v.y), a);
+      a = __fmaf_rn(Q[3], bf16_hi(v.y), a);
+      acc[k] = a;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] += __shfl_xor_sync(0xFFFFFFFFu, acc[k], o);
+  if (lane < 4 && c0 + lane < nblk) {
+    float r = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
+    scores[bh * nblk + c0 + lane] = r;
+  }
+}
+
+int launch_score_landmark(const Dims& s, const uint16_t* L, const uint16_t* q, float* scores,
+                          cudaStream_t st) {
+  const int64_t nblk = (s.n + kLmBlock - 1) / kLmBlock;
+  dim3 grid((unsigned)((nblk + 31) / 32), (unsigned)(s.B * s.Hkv));
+  switch (s.G) {
+    case 1: score_landmark_kernel<1><<<grid, 256, 0, st>>>(L, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
+    case 2: score_landmark_kernel<2><<<grid, 256, 0, st>>>(L, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
+    case 4: score_landmark_kernel<4><<<grid, 256, 0, st>>>(L, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
+    default: score_landmark_kernel<8><<<grid, 256, 0, st>>>(L, q, s.Hq, s.Hkv, s.n, s.ncap, scores); break;
+  }
+  note_launches(1);
+  return check_launch("score_landmark");
+}
+
 }  // namespace sd

@@ -26,7 +26,7 @@ from typing import Optional
 
 import torch
 
-from . import (SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_SCORE_F32,
+from . import (SD_IDX_LANDMARK, SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_SCORE_F32,
                SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
                sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_plan_score,
                sd_score, sd_score_topk, sd_score_topk_workspace_size, sd_topk,
@@ -34,18 +34,20 @@ from . import (SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_S
                sd_select_attend_workspace_size, sd_topk_wmax,
                sd_topk_workspace_size)
 
-KIND_NAMES = {SD_IDX_SIG: "hamming", SD_IDX_PLANES: "planes", SD_IDX_MINMAX: "quest"}
+KIND_NAMES = {SD_IDX_SIG: "hamming", SD_IDX_PLANES: "planes", SD_IDX_MINMAX: "quest",
+              SD_IDX_LANDMARK: "landmark"}
+BLOCK_OF = {SD_IDX_MINMAX: 16, SD_IDX_LANDMARK: 8}  # tokens per scored unit (else 1)
 
 
 @dataclasses.dataclass
 class StepConfig:
-    kind: int                 # SD_IDX_SIG, SD_IDX_PLANES or SD_IDX_MINMAX
+    kind: int                 # SD_IDX_SIG, SD_IDX_PLANES, SD_IDX_MINMAX or SD_IDX_LANDMARK
     B: int
     Hq: int
     Hkv: int
     n: int
     d: int = 128
-    k: int = 512              # tokens (token mode) or blocks (block mode, kind MINMAX)
+    k: int = 512              # tokens (token mode) or blocks (MINMAX, LANDMARK)
     sink: int = 0             # forced leading units
     local: int = 0            # forced trailing units
     plan_mode: int = SD_PLAN_WATERFILL
@@ -58,11 +60,11 @@ class StepConfig:
 
     @property
     def block(self) -> int:
-        return 16 if self.kind == SD_IDX_MINMAX else 1
+        return BLOCK_OF.get(self.kind, 1)
 
     @property
     def n_units(self) -> int:
-        return (self.n + 15) // 16 if self.kind == SD_IDX_MINMAX else self.n
+        return (self.n + self.block - 1) // self.block
 
     @property
     def max_count(self) -> int:
@@ -77,6 +79,9 @@ def index_buffers(cfg: StepConfig, device="cuda") -> dict:
     if cfg.kind == SD_IDX_PLANES:
         return {"planes": torch.empty((B, H, d, 4, n // 32), dtype=torch.int32, device=device),
                 "scales": torch.empty((B, H, d, n // 64), dtype=torch.int16, device=device)}
+    if cfg.kind == SD_IDX_LANDMARK:
+        return {"landmarks": torch.empty((B, H, cfg.n_units, d), dtype=torch.int16,
+                                         device=device)}
     nblk = (n + 15) // 16
     return {"summ": torch.empty((B, H, nblk, 2, d), dtype=torch.int16, device=device)}
 
@@ -89,6 +94,8 @@ def build_index(cfg: StepConfig, K: torch.Tensor, enc=None, stream=None) -> dict
         sd_build_index(SD_IDX_SIG, shp, K, enc, idx["sig"], None, stream)
     elif cfg.kind == SD_IDX_PLANES:
         sd_build_index(SD_IDX_PLANES, shp, K, None, idx["planes"], idx["scales"], stream)
+    elif cfg.kind == SD_IDX_LANDMARK:
+        sd_build_index(SD_IDX_LANDMARK, shp, K, None, idx["landmarks"], None, stream)
     else:
         sd_build_index(SD_IDX_MINMAX, shp, K, None, idx["summ"], None, stream)
     return idx
@@ -153,6 +160,9 @@ class DecodeStep:
         elif c.kind == SD_IDX_PLANES:
             sd_score(SD_IDX_PLANES, self.shape, ix["planes"], ix["scales"], q, self.plan,
                      self.scores, stream)
+        elif c.kind == SD_IDX_LANDMARK:
+            sd_score(SD_IDX_LANDMARK, self.shape, ix["landmarks"], None, q, None, self.scores,
+                     stream)
         else:
             sd_score(SD_IDX_MINMAX, self.shape, ix["summ"], None, q, None, self.scores, stream)
 
