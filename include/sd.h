@@ -127,8 +127,9 @@ int sd_build_index(int kind, const sd_shape* shape, const void* K, const sd_enco
  * <= n, any n, typically n_old + 1 per decode step).  On return the index equals
  * sd_build_index's result for n tokens, bit for bit.  Rewritten: SD_IDX_SIG the
  * signatures of tokens [n_old, n); SD_IDX_MINMAX the 16-token blocks from
- * floor(n_old/16) on; SD_IDX_PLANES the 64-token blocks from floor(n_old/64) on (the
- * block being filled is re-quantised, since a new key can raise its scale).  Work
+ * floor(n_old/16) on; SD_IDX_LANDMARK the 8-token blocks from floor(n_old/8) on;
+ * SD_IDX_PLANES the 64-token blocks from floor(n_old/64) on (the block being filled
+ * is re-quantised, since a new key can raise its scale).  Work
  * and traffic are proportional to n - n_old plus one block.  n_old == n does
  * nothing.  Arguments, layouts and errors otherwise as sd_build_index.
  */
