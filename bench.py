@@ -407,7 +407,7 @@ def other_configs(torch, sd, rl, synth, flush, K_st, peak_gbs):
     select()
     torch.cuda.synchronize()
     admitted = int(pcnt.clamp(min=0).sum().item())
-    xfer = admitted * 16 * 128 * 2 * 2  # K and V rows of the admitted blocks
+    xfer = rl.resident_transfer_bytes(admitted)  # K and V rows of the admitted blocks
     out["quest-b64-16k (B=64, n=16384, 128+1 blocks)"]["resident_129x16_C7"] = {
         "delta_select_us": t_sel, "select_and_transfer_us": t_both,
         "admitted_blocks_per_step": admitted, "transfer_bytes_per_step": xfer,
@@ -579,7 +579,7 @@ def main():
         torch.cuda.synchronize()
         tl = statistics.mean(timed_steps(torch, lambda: stl.run(q), K_st, 3, flush))
         tls = statistics.mean(timed_steps(torch, lambda: stl.stage_score(q), K_st, 3, flush))
-        bl = B * Hkv * ((n + 7) // 8) * 128 * 2
+        bl = rl.landmark_scan_bytes(B, Hkv, n)
         variants["landmark8"] = {"us_per_step": tl * 1e3, "keys_per_s": keys / (tl * 1e-3),
                                  "scan_us": tls * 1e3, "scan_bytes": bl,
                                  "scan_GBps": bl / (tls * 1e-3) / 1e9,

@@ -36,3 +36,19 @@ def test_summary_fraction_and_block_budget():
     assert frac == g["summary_fraction"]
     assert g["blocks"] * g["block_tokens"] == g["tokens_per_head"]
     assert rl.gather_bytes([g["tokens_per_head"]]) == g["tokens_per_head"] * 512
+
+
+def test_sparq_bit_counts_match_the_results_table():
+    """SparQ r channels at full depth cost r x (4 plane bits + a quarter bit of fp16
+    scale per 64 tokens): 68 bits at r = 16 and 136 at r = 32, as the table prints."""
+    g = json.load(open(GOLD))
+    assert rl.fixed_scan_bytes_per_token(16) * 8 == g["sparq_r16_bits"]
+    assert rl.fixed_scan_bytes_per_token(32) * 8 == g["sparq_r32_bits"]
+
+
+def test_landmark_and_resident_bytes():
+    # 8-token landmarks: 32 B (256 bits) per token per KV head
+    assert rl.landmark_scan_bytes(1, 8, 1 << 20) == 8 * (1 << 20) * 32
+    assert rl.landmark_scan_bytes(1, 1, 9) == 2 * 256  # a short last block is a full row
+    # an admitted 16-token block moves 16 K rows and 16 V rows of 256 B
+    assert rl.resident_transfer_bytes(3584) == 3584 * 16 * 512

@@ -48,6 +48,16 @@ def quest_scan_bytes(B: int, Hkv: int, n: int) -> int:
     return B * Hkv * ((n + 15) // 16) * 2 * ROW_BYTES
 
 
+def landmark_scan_bytes(B: int, Hkv: int, n: int, block: int = 8) -> int:
+    """One bf16 landmark row (256 B) per `block` tokens per KV head."""
+    return B * Hkv * ((n + block - 1) // block) * ROW_BYTES
+
+
+def resident_transfer_bytes(admitted_units: int, block: int = 16) -> int:
+    """K and V rows of the units admitted into a resident set (512 B per token)."""
+    return int(admitted_units) * block * KV_ROW_BYTES
+
+
 def gather_bytes(counts: np.ndarray) -> int:
     return int(np.asarray(counts, np.int64).clip(min=0).sum() * KV_ROW_BYTES)
 
