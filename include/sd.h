@@ -414,6 +414,11 @@ typedef struct sd_resident {
  *   Steps of one resident set must not overlap.  The state is read as it stands:
  *   a map entry that disagrees with its slot counts as not resident, so no state
  *   content can make the kernel access memory outside the arrays.
+ *   Errors (nothing is launched): SD_ERR_INVALID_ARG for a NULL required pointer
+ *   (plan arrays are required when admit_cap > 0), a bad sel, admit_cap, step or
+ *   stride; SD_ERR_UNSUPPORTED for n_slots or the predicted-unit bound outside
+ *   the limits; SD_ERR_CUDA if the launch fails.  All arrays are device memory
+ *   owned by the caller.
  */
 int sd_delta_select(const sd_shape* shape, const sd_select* sel, const float* scores,
                     const int32_t* idx, int64_t idx_stride, const int32_t* count,
@@ -431,6 +436,9 @@ int sd_delta_select(const sd_shape* shape, const sd_select* sel, const float* sc
  *   K, V: bf16 [B][hkv][n_cap][d], device memory or pinned host memory (cudaHostAlloc
  *   or registered); K_pool, V_pool: device bf16 [B][hkv][n_slots * block][d].  All
  *   16-byte aligned.  Entries with a slot or unit out of range are skipped.
+ *   Errors: SD_ERR_INVALID_ARG for a NULL or misaligned pointer, a block outside
+ *   [1, 4096], admit_cap outside [0, 8192] or K/V that are neither device nor
+ *   pinned host memory; SD_ERR_UNSUPPORTED for n_slots outside [1, 4096].
  */
 int sd_resident_gather(const sd_shape* shape, int32_t block, const void* K, const void* V,
                        const int32_t* plan_slot, const int32_t* plan_unit,
