@@ -455,7 +455,8 @@ int sd_event_wait(void* event, int64_t timeout_us);
 /* Thread-local message of the last failing call on this thread ("" if none). */
 const char* sd_last_error(void);
 
-/* ABI version (major * 100 + minor). */
+/* ABI version (major * 100 + minor): 101 adds sd_append_index, SD_PLAN_TOPQ,
+ * SD_IDX_LANDMARK, sd_delta_select and sd_resident_gather to 100. */
 int sd_version(void);
 
 /*

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(sd):
     assert sorted(_abi.SIGNATURES) == header_functions()
     for name in header_functions():
         assert callable(getattr(sd, name)), name
-    assert sd.sd_version() == 100
+    assert sd.sd_version() == 101  # 1.01: append, top-q plan, landmarks, resident set
 
 
 def test_shape_checks(sd):

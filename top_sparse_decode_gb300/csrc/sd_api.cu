@@ -99,7 +99,7 @@ using namespace sd;
 
 extern "C" {
 
-int sd_version(void) { return 100; }
+int sd_version(void) { return 101; }
 
 int64_t sd_launch_count(void) { return (int64_t)launch_total(); }
 
