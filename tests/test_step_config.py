@@ -22,3 +22,26 @@ def test_units_and_stride(kind, block, n):
 def test_degenerate_budget_takes_every_unit():
     c = StepConfig(sd.SD_IDX_LANDMARK, 1, 4, 1, 100, k=50, sink=3, local=3)
     assert c.n_units == 13 and c.max_count == 13 * 8
+
+
+def test_stage_tracing_wraps_each_stage_in_order():
+    """run_stages with trace: every stage runs inside a range of its own name, in
+    order, and a range is closed even when its stage raises."""
+    from top_sparse_decode_gb300.pipeline import run_stages
+    log = []
+    stages = [(n, lambda q, s, n=n: log.append(("run", n, q, s))) for n in ("plan_scan", "topk")]
+    run_stages(stages, "q", "st", True, push=lambda n: log.append(("push", n)),
+               pop=lambda: log.append(("pop",)))
+    assert log == [("push", "sd.plan_scan"), ("run", "plan_scan", "q", "st"), ("pop",),
+                   ("push", "sd.topk"), ("run", "topk", "q", "st"), ("pop",)]
+    log.clear()
+    run_stages(stages, "q", None)  # untraced: the calls alone
+    assert [e[0] for e in log] == ["run", "run"]
+
+    def boom(q, s):
+        raise RuntimeError("stage failed")
+    log.clear()
+    with pytest.raises(RuntimeError):
+        run_stages([("bad", boom)], "q", None, True, push=lambda n: log.append(("push", n)),
+                   pop=lambda: log.append(("pop",)))
+    assert log == [("push", "sd.bad"), ("pop",)]

@@ -26,8 +26,8 @@ from typing import Optional
 
 import torch
 
-from . import (SD_IDX_LANDMARK, SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL, SD_SCORE_F32,
-               SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
+from . import (SD_IDX_LANDMARK, SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG, SD_PLAN_WATERFILL,
+               SD_SCORE_F32, SD_SCORE_I32, make_select, make_shape, sd_build_index, sd_encode_query,
                sd_gather_attend, sd_gather_attend_workspace_size, sd_plan, sd_plan_score,
                sd_score, sd_score_topk, sd_score_topk_workspace_size, sd_topk,
                sd_hamming_topk, sd_hamming_topk_workspace_size, sd_select_attend,
@@ -236,7 +236,24 @@ class DecodeStep:
         return [(first, self.stage_prep), ("scan", self.stage_score), topk,
                 ("gather_attend", self.stage_attend)]
 
-    def run(self, q, stream=None):
-        for _, fn in self.stages():
-            fn(q, stream)
+    def run(self, q, stream=None, trace: bool = False):
+        """One step.  With trace, each stage is an NVTX range named after it (for a
+        profiler's timeline; the ranges cost nothing when no tool is attached)."""
+        run_stages(self.stages(), q, stream, trace)
         return self.out
+
+
+def run_stages(stages, q, stream=None, trace: bool = False, push=None, pop=None):
+    """Calls each (name, fn) of `stages` as fn(q, stream), in order; with trace,
+    inside an NVTX range of that name (push/pop default to torch.cuda.nvtx)."""
+    if trace:
+        push = push or torch.cuda.nvtx.range_push
+        pop = pop or torch.cuda.nvtx.range_pop
+    for name, fn in stages:
+        if trace:
+            push(f"sd.{name}")
+        try:
+            fn(q, stream)
+        finally:
+            if trace:
+                pop()
