@@ -168,13 +168,18 @@ def plan(q: np.ndarray, sigma2: np.ndarray, Hkv: int, mode: int, budget: int) ->
     return out
 
 
-def plane_score(planes, scales, plan_, q, with_l1: bool = False):
+def plane_score(planes, scales, plan_, q, with_l1: bool = False, n: int = None):
+    """Scores of the n tokens (default: every position the planes hold) from the
+    planes [B][Hkv][d][4][2 nb] and scales [B][Hkv][d][nb], nb = ceil(n / 64)."""
     planes, pp = _c(planes, np.uint32)
     scales, psc = _c(scales, np.uint16)
     plan_, ppl = _c(plan_, np.uint8)
     q, pq = _c(q, np.uint16)
     B, Hkv, d, _, nw = planes.shape
-    n = nw * 32
+    if n is None:
+        n = nw * 32
+    if nw != 2 * ((n + 63) // 64) or scales.shape[-1] != nw // 2:
+        raise ValueError("plane_score: planes / scales do not hold ceil(n / 64) blocks")
     Hq = q.shape[1]
     out = np.empty((B, Hkv, n), np.float64)
     _l().orc_plane_score(pp, psc, ppl, pq, B, Hq, Hkv, n, d, out.ctypes.data)

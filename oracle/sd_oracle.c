@@ -319,13 +319,16 @@ int orc_plan(const uint16_t* q, const float* sigma2, int64_t B, int Hq, int Hkv,
 /* ------------------------------------------------------------------------------ */
 /*
  * score[b][h][i] = sum_g sum_j q_gj * khat_ij(t = plan_j), khat from the first
- * plan_j planes of channel j and the block's scale (orc_reconstruct), in double.
+ * plan_j planes of channel j and the block's scale (orc_reconstruct), in double,
+ * for the n tokens i < n.  The planes hold nb = ceil(n / 64) blocks (2 nb words per
+ * plane), as orc_plane_build writes them: a partial last block is scored with its
+ * own scale (READING: keys enter the index as they are written).
  */
 void orc_plane_score(const uint32_t* planes, const uint16_t* scales, const uint8_t* plan,
                      const uint16_t* q, int64_t B, int Hq, int Hkv, int64_t n, int d,
                      double* score) {
   int G = Hq / Hkv;
-  int64_t nw = n / 32, nb = n / 64;
+  int64_t nb = (n + 63) / 64, nw = 2 * nb;
 #pragma omp parallel for collapse(3) schedule(static)
   for (int64_t b = 0; b < B; ++b)
     for (int h = 0; h < Hkv; ++h)
@@ -353,7 +356,7 @@ void orc_plane_score_l1(const uint32_t* planes, const uint16_t* scales, const ui
                         const uint16_t* q, int64_t B, int Hq, int Hkv, int64_t n, int d,
                         double* l1) {
   int G = Hq / Hkv;
-  int64_t nw = n / 32, nb = n / 64;
+  int64_t nb = (n + 63) / 64, nw = 2 * nb;
 #pragma omp parallel for collapse(3) schedule(static)
   for (int64_t b = 0; b < B; ++b)
     for (int h = 0; h < Hkv; ++h)

@@ -87,6 +87,43 @@ def test_signature_bits_match_exact_sign(hidden):
     assert np.array_equal(bits[sure], (pre > 0)[sure])
 
 
+def test_signature_chain_is_ascending_fmaf_then_bias():
+    """Hand-built rows on which the canonical chain -- acc = fma(w_j, x_j, acc), j
+    ascending, then + bias -- and its plausible variants give opposite bits.
+    (1 + 2^-7)(1 + 2^-23) = 1 + 2^-7 + 2^-23 + 2^-30 rounds to fp32 by dropping 2^-30.
+    Against w_0 x_0 = -(1 + 2^-7 + 2^-23) the fused chain keeps +2^-30 (bit 1); a
+    separate multiply and add, or the chain taken in descending j, cancels to 0
+    (bit 0).  A bias of -1.5 * 2^-30 added after the chain gives -2^-31 (bit 0);
+    added first it would vanish below half an ulp of the first product (bit 1)."""
+    d = 128
+    c = np.float32(1 + 2**-7 + 2**-23)
+    w1 = np.float32(1 + 2**-23)
+    assert float(c) == 1 + 2**-7 + 2**-23 and float(w1) == 1 + 2**-23
+    x = np.zeros((1, d), np.uint16)
+    x[0, 0], x[0, 1] = 0x3F80, 0x3F81  # bf16 1.0 and 1 + 2^-7
+    W1 = np.zeros((32, d), np.float32)
+    b1 = np.zeros(32, np.float32)
+    W1[0, :2] = (-c, w1)   # fused ascending chain: +2^-30
+    W1[1, :2] = (c, -w1)   # -2^-30
+    W1[2, :2] = (-c, w1)
+    b1[2] = np.float32(-1.5 * 2**-30)
+    W1[3, 1] = w1          # a plain positive product
+    sig = int(oracle.sig_encode(x, W1, b1)[0])
+    assert [(sig >> o) & 1 for o in range(4)] == [1, 0, 0, 1]
+    assert sig >> 4 == 0   # all-zero rows give +0 -> bit 0
+    # the same residue through an MLP's hidden unit: ReLU(2^-30) = 2^-30 feeds
+    # output 0 with weight 1; a mul+add hidden chain would feed 0
+    hidden = 16
+    H1 = np.zeros((hidden, d), np.float32)
+    H1[0, :2] = (-c, w1)
+    H2 = np.zeros((32, hidden), np.float32)
+    H2[0, 0] = 1.0
+    H2[1, 0] = -1.0
+    sig2 = int(oracle.sig_encode(x, H1, np.zeros(hidden, np.float32), H2,
+                                 np.zeros(32, np.float32))[0])
+    assert sig2 == 1
+
+
 def test_signature_zero_gives_zero_bit():
     d = 128
     x = np.zeros((2, d), np.uint16)
@@ -405,6 +442,74 @@ def test_quest_bound_dominates_every_in_block_dot():
     K1 = np.repeat(inp.K[:1, :1, :1], 16, axis=2)
     U1 = oracle.quest_score(oracle.minmax_build(K1), inp.q[:1, :G])
     assert U1[0, 0, 0] == pytest.approx(float(Kf[0, 0, 0] @ qf[0, :G].sum(axis=0)), rel=1e-12)
+
+
+def _khat_by_bins(planes, scales, plan_, n):
+    """khat_ij(t_j) [B][Hkv][d][n] decoded by numpy from the planes: the first t_j
+    planes give the bin (code >> (4 - t)) of [-8 s, 8 s) cut into 2^t bins; the
+    reconstruction is its midpoint for t < 4 and the 4-bit grid value s (code - 8)
+    for t = 4 (an unread channel, t = 0, is the midpoint of [-8 s, 8 s), 0)."""
+    codes = _decode_codes(planes)
+    B, Hkv, d = planes.shape[:3]
+    codes = codes.reshape(B, Hkv, d, -1)[..., :n].astype(np.int64)
+    s = np.repeat(scales.view(np.float16).astype(np.float64), 64, axis=-1)[..., :n]
+    t = plan_.astype(np.int64)[..., None]
+    width = s * 2.0 ** (4 - t)
+    mid = -8 * s + (codes >> (4 - t)) * width + width / 2
+    return np.where(t == 4, s * (codes - 8.0), mid)
+
+
+@pytest.mark.parametrize("n,mode,budget", [(64 * 5, oracle.PLAN_WATERFILL, 56),
+                                           (64 * 5 + 23, oracle.PLAN_WATERFILL, 92),
+                                           (64 * 3 + 1, oracle.PLAN_WATERFILL, 7),
+                                           (64 * 4 + 40, "random", 0)])
+def test_plane_score_and_l1_mass_by_numpy_decoding(n, mode, budget):
+    """The bit-plane score sum_g sum_j q_gj khat_ij(t_j) and its tolerance mass
+    sum_g sum_j |q_gj khat_ij(t_j)| against numpy over independently decoded
+    codes, for water-filled and arbitrary plans, with a partial last block.  A
+    mass formed from |q~_j| (group-summed first), or from |q| |s| 8, or with a term
+    dropped, fails here."""
+    cfg = synth.config(0, n=n, B=2, Hq=8, Hkv=2)
+    inp = synth.make_inputs(cfg, with_v=False)
+    planes, scales = oracle.plane_build(inp.K)
+    if mode == "random":
+        u = synth.uniform(77, 1, cfg.B * cfg.Hkv * cfg.d)
+        plan_ = np.floor(u * 5).astype(np.uint8).reshape(cfg.B, cfg.Hkv, cfg.d)
+    else:
+        plan_ = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, mode, budget)
+    sc, l1 = oracle.plane_score(planes, scales, plan_, inp.q, with_l1=True, n=n)
+    kh = _khat_by_bins(planes, scales, plan_, n)                    # [B][H][d][n]
+    q = synth.bf16_to_f64(inp.q).reshape(cfg.B, cfg.Hkv, cfg.G, cfg.d)
+    ref = np.einsum("bhgj,bhjn->bhn", q, kh)
+    mass = np.einsum("bhgj,bhjn->bhn", np.abs(q), np.abs(kh))
+    assert np.allclose(sc, ref, rtol=0, atol=1e-12 * mass.max())
+    assert np.allclose(l1, mass, rtol=1e-12, atol=0)
+    # the mass is not the looser |q~| form unless every group's signs agree
+    qt = np.abs(q.sum(axis=2))
+    loose = np.einsum("bhj,bhjn->bhn", qt, np.abs(kh))
+    assert np.all(l1 >= loose * (1 - 1e-12)) and np.any(l1 > loose * (1 + 1e-6))
+
+
+def test_quest_l1_mass_is_sum_of_abs_bound_terms():
+    """The Quest tolerance mass sum_g sum_j |max(q_gj min_j, q_gj max_j)| against
+    numpy over the summaries; it bounds |U| and equals U on a block whose every
+    term is non-negative (q and the keys of one sign)."""
+    cfg = synth.config(3, B=2, Hkv=2, Hq=8, n=16 * 9 + 3, planted=2)
+    inp = synth.make_inputs(cfg, with_v=False)
+    summ = oracle.minmax_build(inp.K)
+    U, l1 = oracle.quest_score(summ, inp.q, with_l1=True)
+    q = synth.bf16_to_f64(inp.q).reshape(cfg.B, cfg.Hkv, cfg.G, 1, cfg.d)
+    mn = synth.bf16_to_f64(summ[:, :, :, 0])[:, :, None]   # [B][H][1][c][d]
+    mx = synth.bf16_to_f64(summ[:, :, :, 1])[:, :, None]
+    terms = np.maximum(q * mn, q * mx)                      # [B][H][G][c][d]
+    assert np.allclose(U, terms.sum(axis=(2, 4)), rtol=0, atol=1e-12 * np.abs(terms).sum())
+    assert np.allclose(l1, np.abs(terms).sum(axis=(2, 4)), rtol=1e-12, atol=0)
+    assert np.all(np.abs(U) <= l1 * (1 + 1e-12))
+    Kp = np.abs(synth.bf16_to_f64(inp.K[:1, :1, :16]))
+    qp = np.abs(synth.bf16_to_f64(inp.q[:1, :cfg.G]))
+    Up, lp = oracle.quest_score(oracle.minmax_build(synth.to_bf16(Kp)), synth.to_bf16(qp),
+                                with_l1=True)
+    assert Up[0, 0, 0] == pytest.approx(lp[0, 0, 0], rel=1e-12)
 
 
 # ---------------------------------------------------------------------------------
