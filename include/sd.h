@@ -334,20 +334,28 @@ int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const 
 
 /*
  * sd_gather_attend_noalloc -- sd_gather_attend for callers that cannot allocate
- * device memory: code running while its stream is captured into a CUDA graph,
- * engines whose host framework owns every device allocation, real-time loops
- * that must not take allocator locks.  (The pages have no counterpart: this is
- * a property of the library, not of the method.)
+ * device memory or hand the library a workspace: engines whose host framework
+ * owns every device allocation (a pool or custom allocator the library must not
+ * bypass), real-time loops that must not take allocator locks or let cudaMalloc
+ * synchronise the device, and code that runs where cudaMalloc may not be called.
+ * (The pages have no counterpart: this is a property of the library, not of the
+ * method.)
  *   Same arguments, layouts and results as sd_gather_attend, without the
- *   workspace: the split-n partials live in a 4 MiB file-scope device array
- *   that every GPU loading libsd holds until the process exits.  Requests whose
- *   partials need more (sd_gather_attend_workspace_size() > 4 MiB) are rejected
- *   with SD_ERR_UNSUPPORTED before anything is enqueued.  Allocates nothing.
+ *   workspace: when the split-n kernel runs, its partials live in a 4 MiB
+ *   file-scope device array that every GPU loading libsd holds until the process
+ *   exits.  The limit is applied to every call, whichever kernel then runs:
+ *   requests whose partials would need more (sd_gather_attend_workspace_size()
+ *   > 4 MiB) are rejected with SD_ERR_UNSUPPORTED before anything is enqueued,
+ *   so a call that succeeds on one GPU succeeds on every GPU.  Allocates nothing.
  *   The first call on each device looks up that device's copy of the array
- *   (cudaGetSymbolAddress, with the device current); make that first call before
- *   any stream capture.  All calls on a device share the array and it keeps the
- *   last call's contents: each call first clears the per-row counters that
- *   must start at zero (partials are written before they are read); calls that
+ *   (cudaGetSymbolAddress, with the device current) and keeps the address for
+ *   the process; make that first call before any stream capture.  A device
+ *   reset (cudaDeviceReset) invalidates the kept address: do not call this entry
+ *   point on a device after resetting it.  On GPUs where the 16-CTA cluster
+ *   kernel runs, the array is not used.  When the split-n kernel runs, all calls
+ *   on a device share the array and it keeps the last call's contents: each such
+ *   call first clears the per-row counters that must start at zero (on the
+ *   caller's stream; partials are written before they are read), and calls that
  *   overlap on the GPU race on it.
  */
 int sd_gather_attend_noalloc(const sd_shape* shape, const void* q, const void* K, const void* V,
@@ -446,6 +454,38 @@ int sd_resident_gather(const sd_shape* shape, int32_t block, const void* K, cons
                        void* K_pool, void* V_pool, void* stream);
 
 /*
+ * sd_device_status -- device-side errors of the work already enqueued on
+ * `stream`: waits for the stream, then reads and clears this GPU's libsd error
+ * word.  Every wait inside libsd's kernels is bounded; one that runs out (a
+ * bulk copy that never lands) makes the kernel stop its work early and set the
+ * word instead of hanging.  Returns SD_OK, SD_ERR_TIMEOUT when a kernel gave up
+ * since the last check (its outputs are incomplete; message in sd_last_error()),
+ * or SD_ERR_CUDA when the stream reports an error.  Synchronises `stream`: call
+ * it between steps, not inside a captured graph.
+ */
+int sd_device_status(void* stream);
+
+/*
+ * sd_set_fallback_paths -- testing switch (process-wide, off by default): while
+ * on, sd_gather_attend (and its no-allocation variant), the top-k entry points
+ * and the bit-plane scans take the kernels they use on GPUs where their
+ * thread-block clusters cannot be co-resident or bulk copies do not apply: the
+ * split-n gather-attend with workspace partials, the sampled-threshold
+ * sample/filter/finish top-k, the one-CTA word-maxima top-k, sd_select_attend
+ * as its two calls, and the cp.async bit-plane scan.  Results are the same.
+ * Returns the previous setting.
+ */
+int sd_set_fallback_paths(int on);
+
+/*
+ * sd_debug_set_device_error -- testing: sets this GPU's libsd error word as a
+ * kernel whose bounded wait ran out would (ordered on `stream`, then waits for
+ * it), so that sd_device_status's report can be tested without making a wait
+ * run out.
+ */
+int sd_debug_set_device_error(void* stream);
+
+/*
  * sd_event_wait -- host-side bounded wait on a cudaEvent_t (passed as void*):
  * polls until the event completes or timeout_us microseconds pass
  * (SD_ERR_TIMEOUT).  Lets a caller bound its wait for an offload copy.
@@ -456,7 +496,8 @@ int sd_event_wait(void* event, int64_t timeout_us);
 const char* sd_last_error(void);
 
 /* ABI version (major * 100 + minor): 101 adds sd_append_index, SD_PLAN_TOPQ,
- * SD_IDX_LANDMARK, sd_delta_select and sd_resident_gather to 100. */
+ * SD_IDX_LANDMARK, sd_delta_select and sd_resident_gather to 100; 102 adds
+ * sd_device_status, sd_set_fallback_paths and sd_debug_set_device_error. */
 int sd_version(void);
 
 /*

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(sd):
     assert sorted(_abi.SIGNATURES) == header_functions()
     for name in header_functions():
         assert callable(getattr(sd, name)), name
-    assert sd.sd_version() == 101  # 1.01: append, top-q plan, landmarks, resident set
+    assert sd.sd_version() == 102  # 1.02: device status, fallback switch
 
 
 def test_shape_checks(sd):
@@ -212,3 +212,9 @@ def test_python_binding_raises_with_message(sd):
     with pytest.raises(sd.SdError) as ei:
         sd.sd_plan(shp, 16, 16, 0, 56, 16, stream=0)
     assert ei.value.code == sd.SD_ERR_UNSUPPORTED and "d = 64" in str(ei.value)
+
+
+def test_fallback_switch_is_off_by_default_and_returns_previous(sd):
+    assert sd.sd_set_fallback_paths(True) is False
+    assert sd.sd_set_fallback_paths(False) is True
+    assert sd.sd_set_fallback_paths(False) is False

@@ -1,13 +1,17 @@
 """sd_gather_attend_noalloc: gather-attend for callers that cannot allocate device
-memory (code running under CUDA-graph stream capture, engines whose framework owns
-every allocation, real-time loops that must not take allocator locks).  Its
-partials live in libsd's static per-GPU array instead of a caller workspace.
+memory or hand over a workspace (engines whose framework owns every device
+allocation, real-time loops that must not take allocator locks or let cudaMalloc
+synchronise the device).  When the split-n kernel runs, its partials live in
+libsd's static per-GPU array instead of a caller workspace.
 
 The GPU test calls it through the C ABI twice in a row, on different problems,
 and checks each result against sd_gather_attend with a caller workspace, within
-the attention tolerance of the other parity tests.  This file is collected last
-so that a run stopping at the first failure has already run everything else;
-it also passes on its own in a fresh process."""
+the attention tolerance of the other parity tests: once as the GB300 runs it (the
+16-CTA cluster kernel, which needs no scratch) and once with the split-n kernel
+forced (sd_set_fallback_paths), so that both calls really write, and the second
+reuses, the shared array.  This file is collected last so that a run stopping at
+the first failure has already run everything else; it also passes on its own in
+a fresh process."""
 import ctypes
 import math
 
@@ -42,10 +46,18 @@ def test_noalloc_rejects_oversized_requests_before_any_cuda_call(sd):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_twice(sd):
+@pytest.mark.parametrize("split_n", [False, True])
+def test_noalloc_matches_workspace_entry_point_twice(sd, split_n):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    results = []
+    prev = sd.sd_set_fallback_paths(split_n)
+    try:
+        _two_calls(sd)
+    finally:
+        sd.sd_set_fallback_paths(prev)
+
+
+def _two_calls(sd):
     for trial, (G, Hkv, n, max_count) in enumerate([(4, 8, 6000, 1152), (8, 3, 3000, 700)]):
         cfg = synth.config(1, B=2, Hq=G * Hkv, Hkv=Hkv, n=n)
         inp = synth.make_inputs(cfg)
@@ -74,5 +86,3 @@ def test_noalloc_matches_workspace_entry_point_twice(sd):
         assert np.abs(o - r).max() <= ATT_ATOL
         lg, lr = host(lse, np.float32), host(lse_ref, np.float32)
         assert np.abs(lg - lr).max() <= 1e-4 * max(1.0, np.abs(lr).max())
-        results.append(o)
-    assert results[0].shape != results[1].shape

@@ -28,7 +28,8 @@ __all__ = [
     "sd_topk_workspace_size", "sd_topk", "sd_gather_attend_workspace_size", "sd_gather_attend",
     "sd_gather_attend_noalloc", "sd_offload_gather", "Resident", "sd_delta_select",
     "sd_resident_gather",
-    "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count",
+    "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count", "sd_device_status",
+    "sd_set_fallback_paths", "sd_debug_set_device_error",
     "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax",
     "sd_select_attend_workspace_size", "sd_select_attend", "sd_hamming_topk_workspace_size",
     "sd_hamming_topk",
@@ -262,6 +263,25 @@ def sd_resident_gather(shape: SdShape, block: int, K, V, plan_slot, plan_unit, p
                                     _ptr(plan_unit), _ptr(plan_count), admit_cap, n_slots,
                                     _ptr(K_pool), _ptr(V_pool), _stream(stream)),
            "sd_resident_gather")
+
+
+def sd_device_status(stream=None) -> None:
+    """Raises SdError(SD_ERR_TIMEOUT) when a kernel enqueued on `stream` (or earlier)
+    stopped early because a bounded wait ran out; clears the report.  Waits for
+    the stream."""
+    _check(lib().sd_device_status(_stream(stream)), "sd_device_status")
+
+
+def sd_set_fallback_paths(on: bool) -> bool:
+    """Testing switch: route attention, top-k and the bit-plane scan to the kernels
+    used where clusters cannot be co-resident (same results).  Returns the
+    previous setting."""
+    return bool(lib().sd_set_fallback_paths(1 if on else 0))
+
+
+def sd_debug_set_device_error(stream=None) -> None:
+    """Testing: raise the device error word that sd_device_status reports."""
+    _check(lib().sd_debug_set_device_error(_stream(stream)), "sd_debug_set_device_error")
 
 
 def sd_event_wait(event, timeout_us: int) -> None:

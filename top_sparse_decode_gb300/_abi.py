@@ -70,6 +70,9 @@ SIGNATURES = {
                              _p, _p, _p, _p, _p, _i64, _p, _p]),
     "sd_resident_gather": (_i, [_PS, ctypes.c_int32, _p, _p, _p, _p, _p, ctypes.c_int32,
                                 ctypes.c_int32, _p, _p, _p]),
+    "sd_device_status": (_i, [_p]),
+    "sd_set_fallback_paths": (_i, [_i]),
+    "sd_debug_set_device_error": (_i, [_p]),
     "sd_event_wait": (_i, [_p, _i64]),
     "sd_last_error": (ctypes.c_char_p, []),
     "sd_version": (_i, []),

@@ -32,6 +32,9 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+static std::atomic<int> g_fallback{0};
+bool fallback_forced() { return g_fallback.load(std::memory_order_relaxed) != 0; }
+
 static std::atomic<long long> g_launches{0};
 void note_launches(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
 static long long launch_total() { return g_launches.load(std::memory_order_relaxed); }
@@ -99,7 +102,7 @@ using namespace sd;
 
 extern "C" {
 
-int sd_version(void) { return 101; }
+int sd_version(void) { return 102; }
 
 int64_t sd_launch_count(void) { return (int64_t)launch_total(); }
 
@@ -571,6 +574,24 @@ int sd_resident_gather(const sd_shape* shape, int32_t block, const void* K, cons
   return launch_resident_gather(s, block, (const uint16_t*)dk, (const uint16_t*)dv, plan_slot,
                                 plan_unit, plan_count, admit_cap, n_slots, (uint16_t*)K_pool,
                                 (uint16_t*)V_pool, (cudaStream_t)stream);
+}
+
+int sd_set_fallback_paths(int on) {
+  return g_fallback.exchange(on ? 1 : 0, std::memory_order_relaxed);
+}
+
+int sd_device_status(void* stream) {
+  unsigned word = 0;
+  if (int rc = scan_error_take((cudaStream_t)stream, &word)) return rc;
+  if (word)
+    return fail(SD_ERR_TIMEOUT,
+                "sd_device_status: a bounded wait inside a bit-plane scan ran out since the last "
+                "check; that scan stopped early and its scores are incomplete");
+  return SD_OK;
+}
+
+int sd_debug_set_device_error(void* stream) {
+  return scan_error_set(1u, (cudaStream_t)stream);
 }
 
 int sd_event_wait(void* event, int64_t timeout_us) {

@@ -259,11 +259,9 @@ attend_cluster_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict
 // Whether the cluster kernel can run on this device (cached per device).
 template <int G>
 static bool attend_cluster_ok() {
-  static int ok[64];
-  static bool known[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (!known[dev]) {
+  if (fallback_forced()) return false;
+  static std::atomic<int> ok[kMaxDev];
+  return per_device_cached(ok, [] {
     auto kern = attend_cluster_kernel<G>;
     int nc = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
@@ -281,10 +279,8 @@ static bool attend_cluster_ok() {
       if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
     }
     cudaGetLastError();
-    ok[dev] = nc > 0;
-    known[dev] = true;
-  }
-  return ok[dev] != 0;
+    return nc > 0 ? 1 : 0;
+  }) != 0;
 }
 
 template <int G>

@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "sd.h"
 
 namespace sd {
@@ -26,6 +28,38 @@ void note_launches(int k);
 // kernel): later calls, including those made while a stream is being captured
 // into a CUDA graph, issue no CUDA call.
 int set_smem_limit(const void* kernel, size_t bytes, const char* what);
+
+// True while sd_set_fallback_paths(1) is in force: the gather-attend, the top-k
+// kernels and the bit-plane scan take the kernels they use on GPUs where their
+// thread-block clusters cannot be co-resident or bulk copies do not apply (the
+// split-n attention with its workspace partials, the sample/filter/finish top-k,
+// the one-CTA word-maxima top-k, the cp.async scan).  Off by default.
+bool fallback_forced();
+
+// A per-device value computed once by `compute` (for example an occupancy query)
+// and cached; concurrent first calls may both compute it, and every reader sees
+// either "unknown" or the whole value.  Returns 0 when the current device cannot
+// be read.
+constexpr int kMaxDev = 64;
+template <class F>
+inline int per_device_cached(std::atomic<int> (&tab)[kMaxDev], F compute) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return 0;
+  }
+  int v = tab[dev].load(std::memory_order_acquire);  // value + 1; 0 = not yet known
+  if (v == 0) {
+    v = compute() + 1;
+    tab[dev].store(v, std::memory_order_release);
+  }
+  return v - 1;
+}
+
+// The scan's device error word (sd_scan_tma.cu): read-and-clear, and a host-side
+// setter for testing the report without making a wait run out.
+int scan_error_take(cudaStream_t st, unsigned* word);
+int scan_error_set(unsigned word, cudaStream_t st);
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }

@@ -1,18 +1,25 @@
 // sd_gather_attend_noalloc: gather-attend for callers that cannot allocate device
-// memory.  Some callers cannot call cudaMalloc or hand over a workspace: code that
-// runs while a stream is being captured into a CUDA graph (cudaMalloc is not a
-// stream operation and may synchronise the device), attention back-ends whose
-// host framework owns every device allocation, and real-time loops that must not
-// take allocator locks.  This entry point runs the same split-n kernels as
-// sd_gather_attend, with their partial (m, l, o) results kept in one file-scope
-// device array instead of a caller workspace.
+// memory or hand the library a workspace: attention back-ends whose host framework
+// owns every device allocation (a pool or custom allocator the library must not
+// bypass), real-time loops that must not take allocator locks or let cudaMalloc
+// synchronise the device, and code that runs where cudaMalloc may not be called.
+// This entry point runs the same kernels as sd_gather_attend; when the split-n
+// kernel runs (GPUs where the 16-CTA cluster kernel cannot be co-resident), its
+// partial (m, l, o) results are kept in one file-scope device array instead of a
+// caller workspace.  The cluster kernel needs no scratch and leaves the array
+// alone.
 //
 // The array is a module global: every GPU that loads libsd holds its
 // kNoallocScratchBytes until the process exits, and every call on a GPU shares
-// that GPU's copy.  The array keeps the previous call's contents; every call
-// first clears the per-row counters that must start at zero (with a memset on the
-// caller's stream), and the kernels write every partial before they read it.  Calls whose work overlaps on the GPU (different streams without
-// ordering, or host threads) race on the array.
+// that GPU's copy.  The size limit applies to every call, whichever kernel runs,
+// so that a call accepted on one GPU is accepted on all.  The array keeps the
+// previous call's contents: a call that runs the split-n kernel first clears the
+// per-row counters that must start at zero (with a memset on the caller's
+// stream), and the kernel writes every partial before it reads it.  Such calls
+// whose work overlaps on the GPU (different streams without ordering, or host
+// threads) race on the array.  The array's device address is looked up once per
+// device and kept for the process: after a device reset (cudaDeviceReset) it is
+// stale, so the entry point must not be used on a device that has been reset.
 #include <mutex>
 
 #include "sd_internal.cuh"

@@ -402,6 +402,32 @@ int pt_launch(const Dims& s, const uint32_t* planes, const uint16_t* scales, con
 
 }  // namespace
 
+// Reads this GPU's scan error word after the work on `st`, then clears it (both
+// ordered on `st`; the host waits for the stream).
+int scan_error_take(cudaStream_t st, unsigned* word) {
+  *word = 0;
+  unsigned zero = 0;
+  if (cudaMemcpyFromSymbolAsync(word, g_scan_timeout, sizeof(unsigned), 0,
+                                cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return check_launch("device status: read");
+  if (*word &&
+      (cudaMemcpyToSymbolAsync(g_scan_timeout, &zero, sizeof(unsigned), 0,
+                               cudaMemcpyHostToDevice, st) != cudaSuccess ||
+       cudaStreamSynchronize(st) != cudaSuccess))
+    return check_launch("device status: clear");
+  return SD_OK;
+}
+
+// Sets the word as a scan whose bounded wait ran out would (for testing the report).
+int scan_error_set(unsigned word, cudaStream_t st) {
+  if (cudaMemcpyToSymbolAsync(g_scan_timeout, &word, sizeof(unsigned), 0, cudaMemcpyHostToDevice,
+                              st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return check_launch("device status: set");
+  return SD_OK;
+}
+
 // The bulk-copy scan applies when every CTA's range meets at most two rows; returns
 // 1 (not launched) otherwise.  Layouts must be 16-byte aligned (planes_aligned).
 int launch_score_planes_tma(const Dims& s, const uint32_t* planes, const uint16_t* scales,

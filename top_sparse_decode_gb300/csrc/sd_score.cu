@@ -523,7 +523,7 @@ bool planes_aligned(const Dims& s, const void* planes, const void* scales) {
 int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* scales,
                         const uint8_t* plan, const uint16_t* q, float* scores, cudaStream_t st,
                         const PsCand* cand, const PsPlanIn* plan_in, float* wmax) {
-  const bool a16 = planes_aligned(s, planes, scales);
+  const bool a16 = planes_aligned(s, planes, scales) && !fallback_forced();
   const PsPlanIn pl = plan_in ? *plan_in : PsPlanIn{};
   if (a16) {  // the bulk-copy kernel, when every CTA's range meets at most two rows
     const int rc = launch_score_planes_tma(s, planes, scales, plan, q, scores, cand, plan_in,

@@ -1190,11 +1190,9 @@ topk_cluster_kernel(const void* __restrict__ scores, Geo g, int32_t* __restrict_
 // all fit in one wave.
 template <bool F32, int CS>
 static int cluster_capacity() {
-  static int cap[64];
-  static bool known[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!known[dev]) {
+  if (fallback_forced()) return 0;
+  static std::atomic<int> cap[kMaxDev];
+  return per_device_cached(cap, [] {
     auto kern = topk_cluster_kernel<F32, CS>;
     int n = 0;
     bool yes = set_smem_limit((const void*)kern, sizeof(ClSmem), "topk cluster") == SD_OK;
@@ -1216,10 +1214,8 @@ static int cluster_capacity() {
       if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
-    cap[dev] = n;
-    known[dev] = true;
-  }
-  return cap[dev];
+    return n;
+  });
 }
 
 template <bool F32, int CS>
@@ -2017,11 +2013,9 @@ select_attend_kernel(const float* __restrict__ scores, const float* __restrict__
 // Resident clusters of CS CTAs of topk_wmax_cluster_kernel (0: cannot run), per device.
 template <int CS>
 static int wmax_cluster_capacity() {
-  static int cap[64];
-  static bool known[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!known[dev]) {
+  if (fallback_forced()) return 0;
+  static std::atomic<int> cap[kMaxDev];
+  return per_device_cached(cap, [] {
     auto kern = topk_wmax_cluster_kernel<CS>;
     int nc = 0;
     bool yes = set_smem_limit((const void*)kern, sizeof(WcSmem), "topk_wmax cluster") == SD_OK;
@@ -2043,10 +2037,8 @@ static int wmax_cluster_capacity() {
       if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
     }
     cudaGetLastError();
-    cap[dev] = nc;
-    known[dev] = true;
-  }
-  return cap[dev];
+    return nc;
+  });
 }
 
 template <int CS>
@@ -2345,11 +2337,9 @@ namespace sd {
 // Resident 16-CTA clusters of select_attend_kernel<G> (0: cannot run), per device.
 template <int G>
 static int select_attend_capacity() {
-  static int cap[64];
-  static bool known[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!known[dev]) {
+  if (fallback_forced()) return 0;
+  static std::atomic<int> cap[kMaxDev];
+  return per_device_cached(cap, [] {
     auto kern = select_attend_kernel<G>;
     int nc = 0;
     bool yes = set_smem_limit((const void*)kern, sizeof(WcSmem), "select_attend") == SD_OK &&
@@ -2370,10 +2360,8 @@ static int select_attend_capacity() {
       if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
     }
     cudaGetLastError();
-    cap[dev] = nc;
-    known[dev] = true;
-  }
-  return cap[dev];
+    return nc;
+  });
 }
 
 template <int G>
