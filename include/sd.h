@@ -104,8 +104,8 @@ typedef enum { SD_SCORE_I32 = 0, SD_SCORE_F32 = 1 } sd_score_type;
  *     i/32; plane 0 = MSB), out1 = fp16 scales [B][hkv][d][n_cap/64] with
  *     s = f16_rn(absmax/7) (1 if that is 0) and code = clamp(rint(k/s)+8, 0, 15).
  *     A last block holding fewer than 64 tokens (n % 64 != 0) takes its scale over
- *     the tokens it holds; its bits past n are 0.  (The plane scans, sd_score and
- *     sd_plan_score, still need n % 64 == 0.)  Words and scales of blocks past
+ *     the tokens it holds; its bits past n are 0.  The plane scans (sd_score,
+ *     sd_plan_score) read such an index at any n.  Words and scales of blocks past
  *     ceil(n/64) are not written.
  *   SD_IDX_MINMAX (OasisKV, Quest-style summaries): out0 = bf16 summaries
  *     [B][hkv][ceil(n_cap/16)][2][d]: per 16-token block the channel min row then
@@ -222,8 +222,10 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
  * and sigma2 itself, with sd_plan's arithmetic, and writes exactly the scores the
  * two calls would.  Arguments as sd_plan (q, sigma2, mode, budget; plan may be
  * NULL, else it receives the plan) and sd_score (planes, scales, scores).
- *   wmax: NULL, or fp32 [B*hkv][n / 32], 4-byte aligned, receiving each 32-token
- *   word's largest score (NaN if one of the 32 is NaN): the input of sd_topk_wmax.
+ *   Any n >= 1 (n_cap a multiple of 64).
+ *   wmax: NULL, or fp32 [B*hkv][ceil(n / 32)], 4-byte aligned, receiving each
+ *   32-token word's largest score over its tokens < n (NaN if one of them is NaN):
+ *   the input of sd_topk_wmax.
  */
 int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales, const void* q,
                   const float* sigma2, int mode, int budget, uint8_t* plan, float* scores,
@@ -234,9 +236,9 @@ int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales,
  * 32-unit maxima are known (HashAttention 2.1 TOPK over the scores of the Fathom
  * bit-plane scan): the same idx and count, drawn from the words whose maximum
  * reaches a sampled threshold instead of from every score of the row.
- *   scores fp32 [rows][n], 16-byte aligned; wmax fp32 [rows][n / 32] with
- *   wmax[r][w] the largest of scores[r][32w .. 32w + 31], NaN if one of them is
- *   NaN (as sd_plan_score writes it); n a multiple of 32.  Other arguments and
+ *   scores fp32 [rows][n], 16-byte aligned; wmax fp32 [rows][ceil(n / 32)] with
+ *   wmax[r][w] the largest of scores[r][32w .. min(32w + 31, n - 1)], NaN if one
+ *   of them is NaN (as sd_plan_score writes it); any n >= 1.  Other arguments and
  *   limits as sd_topk with n_units = n_tokens = n.  Calls outside the one-CTA
  *   path (k > 1024, more than 36,864 words meeting [sink, n - local), rows of at
  *   most 8192 units, or n - sink - local <= k) run sd_topk's kernels, so the

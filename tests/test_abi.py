@@ -169,8 +169,8 @@ def test_fused_entry_argument_checks(sd):
     P = 1 << 20  # a fake, aligned address; never dereferenced
     shp = sd.make_shape(1, 32, 8, 1 << 20)
     sel = sd.make_select(512)
-    # word maxima: n must be a multiple of 32, scores 16-byte aligned, block 1
-    assert lib.sd_topk_wmax(P, P, 8, 1000, ctypes.byref(sel), P, 512, P, None, 0, None) == \
+    # word maxima: n >= 1, scores 16-byte aligned, block 1
+    assert lib.sd_topk_wmax(P, P, 8, 0, ctypes.byref(sel), P, 512, P, None, 0, None) == \
         sd.SD_ERR_INVALID_ARG
     assert lib.sd_topk_wmax(P + 4, P, 8, 1 << 20, ctypes.byref(sel), P, 512, P, None, 0,
                             None) == sd.SD_ERR_INVALID_ARG

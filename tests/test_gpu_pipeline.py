@@ -34,13 +34,24 @@ def step_config(sd, cfg, kind, plan_mode=0, budget=56):
     if kind == sd.SD_IDX_LANDMARK:  # the token budget and windows in 8-token blocks
         return StepConfig(kind, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.d, k=max(1, cfg.k // 8),
                           sink=(cfg.sink + 7) // 8, local=(cfg.local + 7) // 8)
+    # bit planes need a capacity that is a multiple of 64: a ragged n gets a padded one
+    ncap = 0 if kind != sd.SD_IDX_PLANES or cfg.n % 64 == 0 else -(-cfg.n // 512) * 512
     return StepConfig(kind, cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.d, k=cfg.k, sink=cfg.sink,
-                      local=cfg.local, plan_mode=plan_mode, budget=budget)
+                      local=cfg.local, plan_mode=plan_mode, budget=budget, n_cap=ncap)
+
+
+def padded(x, ncap):
+    """K-like [B][H][n][d] -> [B][H][ncap][d], zeros past n (capacity, not keys)."""
+    out = np.zeros(x.shape[:2] + (ncap,) + x.shape[3:], x.dtype)
+    out[:, :, :x.shape[2]] = x
+    return out
 
 
 def run_gpu(sd, cfg, inp, kind, plan_mode=0, budget=56, dev_in=None):
     from top_sparse_decode_gb300.pipeline import DecodeStep, build_index
     sc = step_config(sd, cfg, kind, plan_mode, budget)
+    if sc.n_cap:
+        dev_in = (dev(inp.q), dev(padded(inp.K, sc.n_cap)), dev(padded(inp.V, sc.n_cap)))
     q, K, V = dev_in if dev_in else (dev(inp.q), dev(inp.K), dev(inp.V))
     enc = None
     if kind == sd.SD_IDX_SIG:
@@ -66,7 +77,7 @@ def oracle_scores(cfg, inp, kind, plan_mode=0, budget=56):
     if kind == 1:
         p, sc = oracle.plane_build(inp.K)
         pl = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, plan_mode, budget)
-        s, l1 = oracle.plane_score(p, sc, pl, inp.q, with_l1=True)
+        s, l1 = oracle.plane_score(p, sc, pl, inp.q, with_l1=True, n=cfg.n)
         return s.reshape(cfg.B * cfg.Hkv, -1), l1.reshape(cfg.B * cfg.Hkv, -1)
     if kind == 3:
         s, l1 = oracle.landmark_score(oracle.landmark_build(inp.K), inp.q, with_l1=True)
@@ -134,8 +145,7 @@ def test_cfg0_ragged_sizes(sd):
     for n in (64 * 37, 16 * 53 + 7):
         cfg = synth.config(0, n=n, k=40, sink=3, local=17, blk_k=5)
         inp = synth.make_inputs(cfg)
-        kinds = [sd.SD_IDX_SIG, sd.SD_IDX_MINMAX, sd.SD_IDX_LANDMARK] + \
-            ([sd.SD_IDX_PLANES] if n % 64 == 0 else [])
+        kinds = [sd.SD_IDX_SIG, sd.SD_IDX_MINMAX, sd.SD_IDX_LANDMARK, sd.SD_IDX_PLANES]
         for kind in kinds:
             check_step(sd, cfg, inp, kind)
 

@@ -63,8 +63,11 @@ int set_smem_limit(const void* kernel, size_t bytes, const char* what) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Validates a shape and fills Dims.  need_n64: planes layout constraint.
-static int check_shape(const sd_shape* sh, Dims* out, bool need_n64 = false) {
+// Validates a shape and fills Dims.  need_n64: n and n_cap multiples of 64 (the
+// bulk-copy and cp.async bit-plane kernels); need_cap64: n_cap a multiple of 64
+// (the planes layout), any n.
+static int check_shape(const sd_shape* sh, Dims* out, bool need_n64 = false,
+                       bool need_cap64 = false) {
   if (!sh) return fail(SD_ERR_INVALID_ARG, "shape is NULL");
   if (sh->batch < 1 || sh->hq < 1 || sh->hkv < 1 || sh->n < 1)
     return fail(SD_ERR_INVALID_ARG, "shape: batch, hq, hkv and n must be positive");
@@ -83,6 +86,8 @@ static int check_shape(const sd_shape* sh, Dims* out, bool need_n64 = false) {
     return fail(SD_ERR_UNSUPPORTED, "shape: batch * hkv > 65535");
   if (need_n64 && (sh->n % 64 || ncap % 64))
     return fail(SD_ERR_UNSUPPORTED, "bit planes need n and n_cap to be multiples of 64");
+  if (need_cap64 && ncap % 64)
+    return fail(SD_ERR_UNSUPPORTED, "bit planes need n_cap to be a multiple of 64");
   *out = Dims{sh->batch, sh->hq, sh->hkv, G, sh->n, ncap};
   return SD_OK;
 }
@@ -191,7 +196,7 @@ int sd_plan(const sd_shape* shape, const void* q, const float* sigma2, int mode,
 int sd_score(int kind, const sd_shape* shape, const void* index0, const void* index1,
              const void* q_or_qsig, const uint8_t* plan, void* scores, void* stream) {
   Dims s;
-  int rc = check_shape(shape, &s, kind == SD_IDX_PLANES);
+  int rc = check_shape(shape, &s, false, kind == SD_IDX_PLANES);
   if (rc) return rc;
   if (!index0 || !q_or_qsig || !scores) return fail(SD_ERR_INVALID_ARG, "sd_score: NULL input");
   if (!aligned16(index0) || !aligned16(scores))
@@ -254,7 +259,7 @@ int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales,
                   const float* sigma2, int mode, int budget, uint8_t* plan, float* scores,
                   float* wmax, void* stream) {
   Dims s;
-  int rc = check_shape(shape, &s, true);
+  int rc = check_shape(shape, &s, false, true);
   if (rc) return rc;
   if (!planes || !scales || !q || !scores)
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: NULL input");
@@ -277,9 +282,7 @@ int sd_topk_wmax(const float* scores, const float* wmax, int64_t rows, int64_t n
     return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: NULL input");
   if (!sel || sel->block != 1)
     return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: sel is NULL or sel.block != 1");
-  if (n < 32 || n % 32)
-    return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: n = %lld is not a positive multiple of 32",
-                (long long)n);
+  if (n < 1) return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: n = %lld < 1", (long long)n);
   if (!aligned16(scores) || (uintptr_t)wmax % 4)
     return fail(SD_ERR_INVALID_ARG, "sd_topk_wmax: scores must be 16-byte, wmax 4-byte aligned");
   // the remaining checks are sd_topk's
@@ -426,9 +429,7 @@ int sd_select_attend(const sd_shape* shape, const float* scores, const float* wm
   if (!sel || sel->block != 1)
     return fail(SD_ERR_INVALID_ARG, "sd_select_attend: sel is NULL or sel.block != 1");
   const int64_t n = s.n, rows = (int64_t)s.B * s.Hkv;
-  if (n < 32 || n % 32)
-    return fail(SD_ERR_INVALID_ARG, "sd_select_attend: n = %lld is not a positive multiple of 32",
-                (long long)n);
+  if (n < 1) return fail(SD_ERR_INVALID_ARG, "sd_select_attend: n = %lld < 1", (long long)n);
   if (!aligned16(scores) || (uintptr_t)wmax % 4)
     return fail(SD_ERR_INVALID_ARG,
                 "sd_select_attend: scores must be 16-byte, wmax 4-byte aligned");

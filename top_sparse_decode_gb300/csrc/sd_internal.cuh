@@ -138,6 +138,11 @@ int launch_score_planes_tma(const Dims& s, const uint32_t* planes, const uint16_
                             const uint8_t* plan, const uint16_t* q, float* scores,
                             const PsCand* cand, const PsPlanIn* plan_in, float* wmax, int sms,
                             cudaStream_t st);
+// Direct-streaming bit-plane scan (sd_scan_direct.cu): any n, n_cap % 64 == 0;
+// returns 1 (not launched) when plane offsets exceed 32 bits.
+int launch_score_planes_direct(const Dims& s, const uint32_t* planes, const uint16_t* scales,
+                               const uint8_t* plan, const uint16_t* q, float* scores,
+                               const PsPlanIn* plan_in, float* wmax, int sms, cudaStream_t st);
 int launch_score_quest(const Dims& s, const uint16_t* summ, const uint16_t* q, float* scores,
                        cudaStream_t st);
 size_t topk_workspace_bytes(int64_t rows, int64_t n_units, const sd_select& sel);

@@ -31,58 +31,53 @@ struct PsRow {
 // The read plan of one row, computed by one warp with the same arithmetic and tie
 // order as plan_kernel (sd_plan.cu): the budget largest pairs w_j * 4^-b, ties to
 // the lower 4j + b (water-filling), the budget channels of largest sigma2 (fixed)
-// or of largest query mass sum_g q_gj^2 (top-q), or 4 bits everywhere (full).  Lane l holds channels 4 l .. 4 l + 3 and their pairs
-// (j, 0..3) -- pairs 16 l .. 16 l + 15 in pair order -- so every count is a warp
-// reduction.  Writes tb[j] (shared memory) for every channel.
-template <int G>
-__device__ __forceinline__ void ps_plan_row_warp(int lane, const uint16_t* __restrict__ q,
-                                                 const float* __restrict__ sigma2, int b, int h,
-                                                 int Hq, int mode, int budget, int* tb) {
-  const bool fixed = mode == SD_PLAN_FIXED || mode == SD_PLAN_TOPQ;  // one key per channel
-  const int nkeys = (fixed ? 1 : 4) * kD;
+// or of largest query mass sum_g q_gj^2 (top-q), or 4 bits everywhere (full).  Lane
+// l holds channels 4 l .. 4 l + 3 and their pairs (j, 0..3) -- pairs 16 l .. 16 l + 15
+// in pair order -- with mass[c] = sum_g q_gj^2 (fp32, g ascending, no fused
+// multiply-add) and s2[c] = sigma2 of channel 4 l + c.  Writes tb[j] (shared memory)
+// for every channel.
+__device__ __forceinline__ bool ps_plan_fixed(int mode) {
+  return mode == SD_PLAN_FIXED || mode == SD_PLAN_TOPQ;  // one key per channel
+}
+// Whether the plan is all-4 or all-0 without a search; then *v is the bits.
+__device__ __forceinline__ bool ps_plan_trivial(int mode, int budget, int* v) {
+  const int nkeys = (ps_plan_fixed(mode) ? 1 : 4) * kD;
   if (mode == SD_PLAN_FULL || budget >= nkeys || budget <= 0) {
-    const int v = (mode == SD_PLAN_FULL || budget >= nkeys) ? 4 : 0;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tb[lane * 4 + c] = v;
-    return;
+    *v = (mode == SD_PLAN_FULL || budget >= nkeys) ? 4 : 0;
+    return true;
   }
-  uint32_t key[16];
+  return false;
+}
+// The lane's 16 pair keys (slots 4c + p; with one key per channel only p = 0 counts).
+__device__ __forceinline__ void ps_plan_keys(const float (&mass)[4], const float (&s2)[4], int mode,
+                                             uint32_t (&key)[16]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const int j = lane * 4 + c;
-    float acc = 0.0f;  // query mass in fp32, group sum in ascending g, no fused multiply-add
-    if (mode != SD_PLAN_FIXED) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float x = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]);
-        acc = __fadd_rn(acc, __fmul_rn(x, x));
-      }
-    }
-    if (fixed) {  // one key per channel: its variance (fixed) or its query mass (top-q)
-      key[4 * c] = key_of_f32(mode == SD_PLAN_FIXED ? sigma2[(int64_t)h * kD + j] : acc);
+    if (ps_plan_fixed(mode)) {  // its variance (fixed) or its query mass (top-q)
+      key[4 * c] = key_of_f32(mode == SD_PLAN_FIXED ? s2[c] : mass[c]);
       key[4 * c + 1] = key[4 * c + 2] = key[4 * c + 3] = 0u;  // not counted
     } else {
-      const float w = __fmul_rn(acc, sigma2[(int64_t)h * kD + j]);
+      const float w = __fmul_rn(mass[c], s2[c]);
       const float scale4[4] = {1.0f, 0.25f, 0.0625f, 0.015625f};
 #pragma unroll
       for (int p = 0; p < 4; ++p) key[4 * c + p] = key_of_f32(__fmul_rn(w, scale4[p]));
     }
   }
-  const int per = fixed ? 1 : 4;  // keys per channel that count
-  auto count = [&](auto pred) {
-    int n = 0;
+}
+// Keys of the warp satisfying pred (every lane calls it).
+template <class P>
+__device__ __forceinline__ int ps_plan_count(const uint32_t (&key)[16], int per, P pred) {
+  int n = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) n += ((i & 3) < per) && pred(key[i]);
-    return __reduce_add_sync(0xFFFFFFFFu, n);
-  };
-  // T: the largest key value with at least `budget` keys >= it
-  uint32_t T = 0;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    if (count([&](uint32_t k) { return k >= cand; }) >= budget) T = cand;
-  }
-  const int above = count([&](uint32_t k) { return k > T; });
-  // keys equal to T are taken in pair order until the budget is met
+  for (int i = 0; i < 16; ++i) n += ((i & 3) < per) && pred(key[i]);
+  return __reduce_add_sync(0xFFFFFFFFu, n);
+}
+// Given T, the budget-th largest key: every key above T is taken and the keys equal
+// to T in pair order until the budget is met; writes tb[j] for the lane's channels.
+__device__ __forceinline__ void ps_plan_finish(int lane, const uint32_t (&key)[16], int mode,
+                                               int budget, uint32_t T, int* tb) {
+  const int per = ps_plan_fixed(mode) ? 1 : 4;
+  const int above = ps_plan_count(key, per, [&](uint32_t k) { return k > T; });
   int eq = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) eq += ((i & 3) < per) && key[i] == T;
@@ -104,8 +99,69 @@ __device__ __forceinline__ void ps_plan_row_warp(int lane, const uint16_t* __res
       if (k > T || (e && before < budget - above)) ++taken;
       before += e;
     }
-    tb[lane * 4 + c] = fixed ? (taken ? 4 : 0) : taken;
+    tb[lane * 4 + c] = ps_plan_fixed(mode) ? (taken ? 4 : 0) : taken;
   }
+}
+
+__device__ __forceinline__ void ps_plan_lane(int lane, const float (&mass)[4], const float (&s2)[4],
+                                             int mode, int budget, int* tb) {
+  int v;
+  if (ps_plan_trivial(mode, budget, &v)) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tb[lane * 4 + c] = v;
+    return;
+  }
+  uint32_t key[16];
+  ps_plan_keys(mass, s2, mode, key);
+  const int per = ps_plan_fixed(mode) ? 1 : 4;
+  // T: the largest key value with at least `budget` keys >= it
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    if (ps_plan_count(key, per, [&](uint32_t k) { return k >= cand; }) >= budget) T = cand;
+  }
+  ps_plan_finish(lane, key, mode, budget, T, tb);
+}
+
+// Loads lane l's query values for channels 4 l .. 4 l + 3 (g ascending) and returns
+// their group sum q~ (fp32, g ascending) and mass sum_g q^2 (fp32, no fused
+// multiply-add), plus sigma2 of those channels when the mode reads it.  All loads
+// are issued before any arithmetic.
+template <int G>
+__device__ __forceinline__ void ps_load_row(int lane, const uint16_t* __restrict__ q,
+                                            const float* __restrict__ sigma2, int b, int h, int Hq,
+                                            bool need_s2, float (&qt)[4], float (&mass)[4],
+                                            float (&s2)[4]) {
+  float x[4][G];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      x[c][g] = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + lane * 4 + c]);
+    s2[c] = need_s2 ? sigma2[(int64_t)h * kD + lane * 4 + c] : 0.0f;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float a = 0.0f, m = 0.0f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      a = __fadd_rn(a, x[c][g]);
+      m = __fadd_rn(m, __fmul_rn(x[c][g], x[c][g]));
+    }
+    qt[c] = a;
+    mass[c] = m;
+  }
+}
+
+// The plan of row (b, h) by one warp from q and sigma2 (see ps_plan_lane).
+template <int G>
+__device__ __forceinline__ void ps_plan_row_warp(int lane, const uint16_t* __restrict__ q,
+                                                 const float* __restrict__ sigma2, int b, int h,
+                                                 int Hq, int mode, int budget, int* tb) {
+  float qt[4], mass[4], s2[4];
+  ps_load_row<G>(lane, q, sigma2, b, h, Hq, mode == SD_PLAN_WATERFILL || mode == SD_PLAN_FIXED,
+                 qt, mass, s2);
+  ps_plan_lane(lane, mass, s2, mode, budget, tb);
 }
 
 // Builds R for row bh = b * Hkv + h.  Every thread of the calling group runs it

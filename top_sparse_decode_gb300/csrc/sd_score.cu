@@ -525,10 +525,17 @@ int launch_score_planes(const Dims& s, const uint32_t* planes, const uint16_t* s
                         const PsCand* cand, const PsPlanIn* plan_in, float* wmax) {
   const bool a16 = planes_aligned(s, planes, scales) && !fallback_forced();
   const PsPlanIn pl = plan_in ? *plan_in : PsPlanIn{};
-  if (a16) {  // the bulk-copy kernel, when every CTA's range meets at most two rows
+  if (a16) {  // the bulk-copy kernel (any n), when every CTA's range meets at most two rows
     const int rc = launch_score_planes_tma(s, planes, scales, plan, q, scores, cand, plan_in,
                                            wmax, sm_count(), st);
     if (rc != 1) return rc;
+  }
+  if (s.n % 64) {  // a partial last block outside the bulk-copy kernel: the direct kernel
+    if (cand) return fail(SD_ERR_UNSUPPORTED, "score_planes: candidates need n %% 64 == 0");
+    const int rc = launch_score_planes_direct(s, planes, scales, plan, q, scores, plan_in, wmax,
+                                              sm_count(), st);
+    if (rc != 1) return rc;
+    return fail(SD_ERR_UNSUPPORTED, "score_planes: n_cap too large for n %% 64 != 0");
   }
   if (cand) {  // the fused scan + top-k path (16-byte aligned layouts only)
     if (!a16) return fail(SD_ERR_INVALID_ARG, "score_planes: candidates need n_cap %% 512 == 0 "

@@ -1413,7 +1413,7 @@ topk_wmax_kernel(const float* __restrict__ scores, const float* __restrict__ wma
   WmSmem& S = *reinterpret_cast<WmSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.x;
-  const int64_t n = g.n_units, nw = n >> 5;
+  const int64_t n = g.n_units, nw = (n + 31) >> 5;  // word maxima per row (a last word may be partial)
   const float* srow = scores + row * n;
   int32_t* idx_row = idx + row * idx_stride;
   const int lead = g.lead, tail = g.tail, M = g.M, k = g.k;
@@ -1507,7 +1507,7 @@ topk_wmax_kernel(const float* __restrict__ scores, const float* __restrict__ wma
         for (int u = 0; u < 8; ++u) {
           const int c = c0 + u;
           ub[u] = c < (int)ncw ? (w0 + (int)S.cw[c]) * 32 : -64;
-          x[u] = c < (int)ncw ? __ldg(srow + ub[u] + lane) : -INFINITY;
+          x[u] = c < (int)ncw && ub[u] + lane < n ? __ldg(srow + ub[u] + lane) : -INFINITY;
         }
         uint32_t msk[8], tot = 0;
 #pragma unroll
@@ -1691,7 +1691,7 @@ __device__ __forceinline__ void wc_select(WcSmem& S, const float* __restrict__ s
   const int rank = (int)cl.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t row = blockIdx.y;
-  const int64_t n = g.n_units, nw = n >> 5;
+  const int64_t n = g.n_units, nw = (n + 31) >> 5;  // word maxima per row (a last word may be partial)
   const float* srow = scores + row * n;
   int32_t* idx_row = idx + row * idx_stride;
   const int lead = g.lead, tail = g.tail, k = g.k;
@@ -1779,7 +1779,7 @@ __device__ __forceinline__ void wc_select(WcSmem& S, const float* __restrict__ s
       for (int u = 0; u < 8; ++u) {
         const int c = c0 + u;
         ub[u] = c < (int)nl ? (w0 + (int)S.lw[c]) * 32 : -64;
-        x[u] = c < (int)nl ? __ldg(srow + ub[u] + lane) : -INFINITY;
+        x[u] = c < (int)nl && ub[u] + lane < n ? __ldg(srow + ub[u] + lane) : -INFINITY;
       }
       uint32_t msk[8], tot = 0;
 #pragma unroll

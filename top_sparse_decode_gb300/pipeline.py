@@ -57,6 +57,12 @@ class StepConfig:
     wmax: bool = True         # bit planes with plan_in_scan: word maxima -> sd_topk_wmax
     select_attend: bool = False  # with wmax: top-k and gather-attend in one call
     hamming_fused: bool = True  # signatures: scan and top-k in one call (sd_hamming_topk)
+    n_cap: int = 0            # allocated tokens per (sequence, KV head), >= n (0: n); the
+                              # stride of K, V and the index; a multiple of 64 for planes
+
+    @property
+    def cap(self) -> int:
+        return self.n_cap or self.n
 
     @property
     def block(self) -> int:
@@ -73,14 +79,14 @@ class StepConfig:
 
 def index_buffers(cfg: StepConfig, device="cuda") -> dict:
     """Allocates the key-side index of cfg.kind (uninitialised)."""
-    B, H, n, d = cfg.B, cfg.Hkv, cfg.n, cfg.d
+    B, H, n, d = cfg.B, cfg.Hkv, cfg.cap, cfg.d
     if cfg.kind == SD_IDX_SIG:
         return {"sig": torch.empty((B, H, n), dtype=torch.int32, device=device)}
     if cfg.kind == SD_IDX_PLANES:
         return {"planes": torch.empty((B, H, d, 4, n // 32), dtype=torch.int32, device=device),
                 "scales": torch.empty((B, H, d, n // 64), dtype=torch.int16, device=device)}
     if cfg.kind == SD_IDX_LANDMARK:
-        return {"landmarks": torch.empty((B, H, cfg.n_units, d), dtype=torch.int16,
+        return {"landmarks": torch.empty((B, H, (n + 7) // 8, d), dtype=torch.int16,
                                          device=device)}
     nblk = (n + 15) // 16
     return {"summ": torch.empty((B, H, nblk, 2, d), dtype=torch.int16, device=device)}
@@ -88,7 +94,7 @@ def index_buffers(cfg: StepConfig, device="cuda") -> dict:
 
 def build_index(cfg: StepConfig, K: torch.Tensor, enc=None, stream=None) -> dict:
     """Runs sd_build_index for cfg.kind (the KV-write path) and returns the index."""
-    shp = make_shape(cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.d)
+    shp = make_shape(cfg.B, cfg.Hq, cfg.Hkv, cfg.n, cfg.d, cfg.n_cap)
     idx = index_buffers(cfg, K.device)
     if cfg.kind == SD_IDX_SIG:
         sd_build_index(SD_IDX_SIG, shp, K, enc, idx["sig"], None, stream)
@@ -112,7 +118,7 @@ class DecodeStep:
         self.scale = 1.0 / math.sqrt(cfg.d) if scale is None else scale
         dev = K.device
         c = cfg
-        self.shape = make_shape(c.B, c.Hq, c.Hkv, c.n, c.d)
+        self.shape = make_shape(c.B, c.Hq, c.Hkv, c.n, c.d, c.n_cap)
         self.rows = c.B * c.Hkv
         self.sel = make_select(c.k, c.sink, c.local, c.block)
         sdt = torch.int32 if c.kind == SD_IDX_SIG else torch.float32
@@ -125,7 +131,7 @@ class DecodeStep:
         self.topk_ws = torch.empty(tws, dtype=torch.uint8, device=dev) if tws else None
         self.fused = c.fused and c.kind == SD_IDX_PLANES
         self.use_wmax = (c.kind == SD_IDX_PLANES and c.plan_in_scan and c.wmax and not self.fused)
-        self.wmax = (torch.empty((self.rows, c.n // 32), dtype=torch.float32, device=dev)
+        self.wmax = (torch.empty((self.rows, (c.n + 31) // 32), dtype=torch.float32, device=dev)
                      if self.use_wmax else None)
         self.wmax_fresh = False  # the last scan wrote the word maxima of self.scores
         if self.fused:
