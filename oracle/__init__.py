@@ -28,6 +28,7 @@ _lib = None
 
 PLAN_WATERFILL, PLAN_FIXED, PLAN_FULL = 0, 1, 2
 PLAN_TOPQ = 3  # SparQ-style: the r channels of largest sum_g q_gj^2, 4 bits each
+PLAN_SPLIT = 4  # water-filling of a sequence's Hkv * budget bits across its KV heads
 
 
 def build(force: bool = False) -> str:

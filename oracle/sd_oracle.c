@@ -245,11 +245,57 @@ double orc_reconstruct(int prefix, int t, double s) {
  * One plan per (sequence, KV head): the query heads of a group share it.
  * READING: "average budget B" is sum_j b_j = B bits per token per KV head.
  */
+/*
+ * mode 4 SPLIT(budget): the budget split across the KV heads of a sequence.  The
+ *   sequence's total Hkv * budget bits go, one at a time, to the (head h, channel j)
+ *   with the largest w_hj * 4^-b_hj among b_hj < 4, w_hj = fl32(fl32(sum over head
+ *   h's group of q_gj^2) * sigma2_hj); ties to the lower h, then the lower j.  With
+ *   one KV head it is WATERFILL.
+ *   READING: the Fathom page keeps one budget per query and layer by default and
+ *   calibrates per-layer budgets; the natural extension of its marginal-gain rule to
+ *   the heads of a layer is one greedy over all of them under their summed budget.
+ */
+static void plan_split(const uint16_t* q, const float* sigma2, int64_t b, int Hq, int Hkv, int d,
+                       int budget, uint8_t* plan) {
+  int G = Hq / Hkv;
+  float* w = (float*)malloc(sizeof(float) * (size_t)Hkv * d);
+  for (int h = 0; h < Hkv; ++h)
+    for (int j = 0; j < d; ++j) {
+      float acc = 0.0f;
+      for (int g = 0; g < G; ++g) {
+        float x = bf16_to_f32(q[(b * Hq + h * G + g) * d + j]);
+        float sq = x * x;
+        acc = acc + sq;
+      }
+      w[h * d + j] = acc * sigma2[(int64_t)h * d + j];
+    }
+  uint8_t* pb = plan + b * Hkv * d;
+  memset(pb, 0, (size_t)Hkv * d);
+  int64_t total = (int64_t)Hkv * budget, cap = (int64_t)Hkv * 4 * d;
+  if (total > cap) total = cap;
+  for (int64_t st = 0; st < total; ++st) {
+    int best = -1;
+    float bestg = 0.0f;
+    for (int hj = 0; hj < Hkv * d; ++hj) {  /* h ascending, then j ascending */
+      if (pb[hj] >= 4) continue;
+      float gj = ldexpf(w[hj], -2 * pb[hj]);
+      if (best < 0 || gj > bestg) { best = hj; bestg = gj; }
+    }
+    pb[best] += 1;
+  }
+  free(w);
+}
+
 int orc_plan(const uint16_t* q, const float* sigma2, int64_t B, int Hq, int Hkv, int d,
              int mode, int budget, uint8_t* plan) {
   int G = Hq / Hkv;
-  if (budget < 0 || mode < 0 || mode > 3 || d < 1 || d > 512) return -1;
+  if (budget < 0 || mode < 0 || mode > 4 || d < 1 || d > 512) return -1;
   if ((mode == 1 || mode == 3) && budget > d) return -1;
+  if (mode == 4) {
+    if (budget > 4 * d) return -1;
+    for (int64_t b = 0; b < B; ++b) plan_split(q, sigma2, b, Hq, Hkv, d, budget, plan);
+    return 0;
+  }
   for (int64_t b = 0; b < B; ++b)
     for (int h = 0; h < Hkv; ++h) {
       uint8_t* pb = plan + (b * Hkv + h) * d;

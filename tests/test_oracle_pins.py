@@ -301,6 +301,55 @@ def test_waterfill_is_optimal_by_brute_force(d, G):
                 assert val == pytest.approx(_brute_plan_objective(w, B), rel=1e-12, abs=1e-300)
 
 
+@pytest.mark.parametrize("Hkv,d,G", [(2, 2, 1), (2, 3, 2), (3, 2, 2)])
+def test_budget_split_is_optimal_by_brute_force(Hkv, d, G):
+    """The cross-head split (Fathom's marginal-gain rule over every KV head of a
+    sequence under their summed budget) maximises sum over (h, j) of
+    w_hj (1 - 4^-b_hj) among all allocations of Hkv * B bits: brute force over
+    every allocation; nested in B; the bits of every head within [0, 4]."""
+    for trial in range(2):
+        q = synth.normal_bf16(300 + trial, 1, Hkv * G, d).reshape(1, Hkv * G, d)
+        sigma2 = (synth.uniform(300 + trial, 2, Hkv * d) * 4 + 0.01).astype(np.float32)
+        sigma2 = sigma2.reshape(Hkv, d)
+        w = np.concatenate([_gains(q, sigma2, h, G) for h in range(Hkv)])
+        prev = np.zeros(Hkv * d, np.int64)
+        for B in range(0, 4 * d + 1):
+            p = oracle.plan(q, sigma2, Hkv, oracle.PLAN_SPLIT, B)[0].reshape(-1).astype(np.int64)
+            assert p.sum() == Hkv * B and p.max() <= 4
+            assert np.all(p >= prev)
+            prev = p
+            val = float(np.sum(w * (1 - 4.0 ** -p)))
+            assert val == pytest.approx(_brute_plan_objective(w, Hkv * B), rel=1e-12, abs=1e-300)
+
+
+def test_budget_split_one_head_is_waterfill_and_moves_bits_between_heads():
+    cfg = synth.config(2, B=2, Hq=8, Hkv=2, n=64)
+    inp = synth.make_inputs(cfg, with_v=False)
+    q1 = np.ascontiguousarray(inp.q[:, :4])
+    s1 = np.ascontiguousarray(inp.sigma2[:1])
+    for B in (0, 7, 56, 300, 512):
+        assert np.array_equal(oracle.plan(q1, s1, 1, oracle.PLAN_SPLIT, B),
+                              oracle.plan(q1, s1, 1, oracle.PLAN_WATERFILL, B))
+    # a head whose gains are 16x larger takes more of the shared budget
+    s2 = inp.sigma2.copy()
+    s2[1] *= 16.0
+    p = oracle.plan(inp.q, s2, 2, oracle.PLAN_SPLIT, 56).astype(np.int64)
+    per_head = p.sum(axis=-1)
+    assert np.all(per_head.sum(axis=-1) == 2 * 56)
+    assert np.all(per_head[:, 1] > per_head[:, 0])
+
+
+def test_budget_split_ties_go_to_lower_head_then_channel():
+    # every gain equal: the bits go to head 0's channels first (lower j first, each
+    # channel's b = 0 pairs before any b = 1), then head 1's
+    d, G, Hkv = 4, 1, 2
+    q = np.full((1, Hkv * G, d), 0x3F80, np.uint16)  # bf16 1.0
+    sigma2 = np.ones((Hkv, d), np.float32)
+    p = oracle.plan(q, sigma2, Hkv, oracle.PLAN_SPLIT, 3)[0]
+    # 6 bits of equal gain at b = 0: head 0 channels 0..3, then head 1 channels 0..1
+    assert p.tolist() == [[1, 1, 1, 1], [1, 1, 0, 0]]
+
+
 def test_waterfill_ties_go_to_lower_channel():
     d = 4
     q = np.zeros((1, 1, d), np.uint16)
