@@ -88,7 +88,8 @@ typedef enum {
   SD_PLAN_WATERFILL = 0,
   SD_PLAN_FIXED = 1,
   SD_PLAN_FULL = 2,
-  SD_PLAN_TOPQ = 3
+  SD_PLAN_TOPQ = 3,
+  SD_PLAN_SPLIT = 4
 } sd_plan_mode;
 typedef enum { SD_SCORE_I32 = 0, SD_SCORE_F32 = 1 } sd_score_type;
 
@@ -162,9 +163,17 @@ int sd_encode_query(const sd_shape* shape, const void* q, const sd_encoder* enc,
  *     page (top-r |q| channels read at full depth, r = 16 being its 68-bit
  *     setting; for G = 1 exactly the r largest |q_j|).  sigma2 is not read and may
  *     be NULL.
- * q is required by SD_PLAN_WATERFILL and SD_PLAN_TOPQ, sigma2 by SD_PLAN_WATERFILL
- * and SD_PLAN_FIXED.  Returns SD_ERR_INVALID_ARG for a NULL required pointer, an
- * unknown mode or a budget out of range.
+ *   SD_PLAN_SPLIT, budget B in [0, 4d]: the budget split across the KV heads of a
+ *     sequence: its hkv * B bits go one at a time to the (head h, channel j) with
+ *     the largest w_hj * 4^-b_hj among b_hj < 4 (w_hj as SD_PLAN_WATERFILL's for
+ *     head h), lowest h, then lowest j, on ties; each head's sum varies, the
+ *     sequence's is hkv * B.  With hkv = 1 it equals SD_PLAN_WATERFILL.  (The
+ *     Fathom page keeps one budget per query and calibrates per-layer budgets;
+ *     this is its marginal-gain rule over the heads of a layer.)
+ * q is required by SD_PLAN_WATERFILL, SD_PLAN_TOPQ and SD_PLAN_SPLIT, sigma2 by
+ * SD_PLAN_WATERFILL, SD_PLAN_FIXED and SD_PLAN_SPLIT.  Returns SD_ERR_INVALID_ARG
+ * for a NULL required pointer, an unknown mode or a budget out of range, and
+ * SD_ERR_UNSUPPORTED for SD_PLAN_SPLIT with hkv > 64.
  */
 int sd_plan(const sd_shape* shape, const void* q, const float* sigma2, int mode, int budget,
             uint8_t* plan, void* stream);
@@ -222,6 +231,8 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
  * and sigma2 itself, with sd_plan's arithmetic, and writes exactly the scores the
  * two calls would.  Arguments as sd_plan (q, sigma2, mode, budget; plan may be
  * NULL, else it receives the plan) and sd_score (planes, scales, scores).
+ * SD_PLAN_SPLIT couples the heads of a sequence, so it runs as sd_plan's kernel
+ * and then the scan (two launches) and needs the plan buffer.
  *   Any n >= 1 (n_cap a multiple of 64).
  *   wmax: NULL, or fp32 [B*hkv][ceil(n / 32)], 4-byte aligned, receiving each
  *   32-token word's largest score over its tokens < n (NaN if one of them is NaN):

@@ -170,7 +170,7 @@ def test_cfg2_fathom_128k_full(sd):
     cfg = synth.config(2)
     inp = synth.make_inputs(cfg)
     dev_in = (dev(inp.q), dev(inp.K), dev(inp.V))
-    for mode, budget in [(0, 47), (0, 56), (0, 92), (2, 0), (3, 16)]:
+    for mode, budget in [(0, 47), (0, 56), (0, 92), (2, 0), (3, 16), (4, 56)]:
         recall, err, _ = check_step(sd, cfg, inp, sd.SD_IDX_PLANES, mode, budget, dev_in)
         print(f"cfg2 mode {mode} budget {budget}: planted recall {recall:.3f}, err {err:.2e}")
 

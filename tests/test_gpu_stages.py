@@ -144,6 +144,32 @@ def test_plan_bit_exact(sd, G):
             assert np.array_equal(host(plan, np.uint8), ref), (mode, B)
 
 
+@pytest.mark.parametrize("Hkv,G,B", [(1, 4, 2), (2, 4, 3), (8, 4, 2), (3, 2, 1), (16, 1, 1)])
+def test_plan_split_bit_exact(sd, Hkv, G, B):
+    """The budget split across KV heads (one CTA per sequence) equals the oracle's
+    greedy over every (head, channel) of the sequence, ties to the lower head and
+    channel; with one head it is the water-filling plan."""
+    cfg = synth.config(2, B=B, Hq=G * Hkv, Hkv=Hkv, n=64)
+    inp = synth.make_inputs(cfg, with_v=False)
+    inp.q[0, :, 5:9] = 0  # zero-gain channels
+    if Hkv > 1:  # equal gains in two heads: ties to the lower head
+        inp.sigma2[1] = inp.sigma2[0]
+        inp.q[0, G:2 * G] = inp.q[0, :G]
+    shp = shape_of(sd, cfg)
+    plan = empty((cfg.B, cfg.Hkv, cfg.d), np.uint8)
+    q, s2 = dev(inp.q), dev(inp.sigma2)
+    for budget in [0, 1, 47, 56, 92, 200, 511, 512]:
+        sd.sd_plan(shp, q, s2, sd.SD_PLAN_SPLIT, budget, plan)
+        torch.cuda.synchronize()
+        ref = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, oracle.PLAN_SPLIT, budget)
+        got = host(plan, np.uint8)
+        assert np.array_equal(got, ref), budget
+        assert np.all(got.astype(np.int64).sum(axis=(1, 2)) == min(Hkv * budget, Hkv * 512))
+        if Hkv == 1:
+            assert np.array_equal(got, oracle.plan(inp.q, inp.sigma2, 1, oracle.PLAN_WATERFILL,
+                                                   budget))
+
+
 # --------------------------------------------------------------------------------------
 # S5b bit-plane scan and S5c Quest bound: within 1e-5 of the L1 mass
 # --------------------------------------------------------------------------------------

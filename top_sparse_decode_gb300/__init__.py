@@ -19,7 +19,8 @@ import torch
 from . import _abi
 from ._abi import (SD_ERR_CUDA, SD_ERR_INVALID_ARG, SD_ERR_TIMEOUT, SD_ERR_UNSUPPORTED,  # noqa: F401
                    SD_ERR_WORKSPACE, SD_IDX_LANDMARK, SD_IDX_MINMAX, SD_IDX_PLANES, SD_IDX_SIG,
-                   SD_OK, SD_PLAN_FIXED, SD_PLAN_FULL, SD_PLAN_TOPQ, SD_PLAN_WATERFILL,
+                   SD_OK, SD_PLAN_FIXED, SD_PLAN_FULL, SD_PLAN_SPLIT, SD_PLAN_TOPQ,
+                   SD_PLAN_WATERFILL,
                    SD_SCORE_F32, SD_SCORE_I32, SdEncoder, SdSelect, SdShape)
 
 __all__ = [

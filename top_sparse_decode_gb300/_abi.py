@@ -15,7 +15,7 @@ SD_ERR_TIMEOUT = -4
 SD_ERR_WORKSPACE = -5
 
 SD_IDX_SIG, SD_IDX_PLANES, SD_IDX_MINMAX, SD_IDX_LANDMARK = 0, 1, 2, 3
-SD_PLAN_WATERFILL, SD_PLAN_FIXED, SD_PLAN_FULL, SD_PLAN_TOPQ = 0, 1, 2, 3
+SD_PLAN_WATERFILL, SD_PLAN_FIXED, SD_PLAN_FULL, SD_PLAN_TOPQ, SD_PLAN_SPLIT = 0, 1, 2, 3, 4
 SD_SCORE_I32, SD_SCORE_F32 = 0, 1
 
 

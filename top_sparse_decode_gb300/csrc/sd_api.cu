@@ -171,11 +171,12 @@ int sd_encode_query(const sd_shape* shape, const void* q, const sd_encoder* enc,
 // Pointers and budget range of a read plan (modes as sd_plan_mode).
 static int check_plan_args(const char* fn, const void* q, const float* sigma2, int mode,
                            int budget) {
-  if ((mode == SD_PLAN_WATERFILL || mode == SD_PLAN_TOPQ) && !q)
+  const bool split = mode == SD_PLAN_SPLIT;
+  if ((mode == SD_PLAN_WATERFILL || mode == SD_PLAN_TOPQ || split) && !q)
     return fail(SD_ERR_INVALID_ARG, "%s: q is NULL", fn);
-  if ((mode == SD_PLAN_WATERFILL || mode == SD_PLAN_FIXED) && !sigma2)
+  if ((mode == SD_PLAN_WATERFILL || mode == SD_PLAN_FIXED || split) && !sigma2)
     return fail(SD_ERR_INVALID_ARG, "%s: sigma2 is NULL", fn);
-  if (mode == SD_PLAN_WATERFILL && (budget < 0 || budget > 4 * kD))
+  if ((mode == SD_PLAN_WATERFILL || split) && (budget < 0 || budget > 4 * kD))
     return fail(SD_ERR_INVALID_ARG, "%s: budget %d outside [0, %d]", fn, budget, 4 * kD);
   if ((mode == SD_PLAN_FIXED || mode == SD_PLAN_TOPQ) && (budget < 0 || budget > kD))
     return fail(SD_ERR_INVALID_ARG, "%s: channel count %d outside [0, %d]", fn, budget, kD);
@@ -187,7 +188,10 @@ int sd_plan(const sd_shape* shape, const void* q, const float* sigma2, int mode,
   Dims s;
   int rc = check_shape(shape, &s);
   if (rc) return rc;
-  if (mode < 0 || mode > 3) return fail(SD_ERR_INVALID_ARG, "sd_plan: unknown mode %d", mode);
+  if (mode < 0 || mode > 4) return fail(SD_ERR_INVALID_ARG, "sd_plan: unknown mode %d", mode);
+  if (mode == SD_PLAN_SPLIT && s.Hkv > kSplitMaxHeads)
+    return fail(SD_ERR_UNSUPPORTED, "sd_plan: SD_PLAN_SPLIT with hkv = %d > %d", s.Hkv,
+                kSplitMaxHeads);
   if ((rc = check_plan_args("sd_plan", q, sigma2, mode, budget))) return rc;
   if (!plan) return fail(SD_ERR_INVALID_ARG, "sd_plan: plan is NULL");
   return launch_plan(s, (const uint16_t*)q, sigma2, mode, budget, plan, (cudaStream_t)stream);
@@ -267,9 +271,20 @@ int sd_plan_score(const sd_shape* shape, const void* planes, const void* scales,
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: planes and scores must be 16-byte aligned");
   if ((uintptr_t)wmax % 4)
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: wmax must be 4-byte aligned");
-  if (mode < 0 || mode > 3)
+  if (mode < 0 || mode > 4)
     return fail(SD_ERR_INVALID_ARG, "sd_plan_score: unknown plan mode %d", mode);
   if ((rc = check_plan_args("sd_plan_score", q, sigma2, mode, budget))) return rc;
+  if (mode == SD_PLAN_SPLIT) {  // the heads of a sequence are coupled: plan kernel, then scan
+    if (!plan) return fail(SD_ERR_INVALID_ARG, "sd_plan_score: SD_PLAN_SPLIT needs the plan buffer");
+    if (s.Hkv > kSplitMaxHeads)
+      return fail(SD_ERR_UNSUPPORTED, "sd_plan_score: SD_PLAN_SPLIT with hkv = %d > %d", s.Hkv,
+                  kSplitMaxHeads);
+    if ((rc = launch_plan(s, (const uint16_t*)q, sigma2, mode, budget, plan, (cudaStream_t)stream)))
+      return rc;
+    return launch_score_planes(s, (const uint32_t*)planes, (const uint16_t*)scales, plan,
+                               (const uint16_t*)q, scores, (cudaStream_t)stream, nullptr, nullptr,
+                               wmax);
+  }
   const PsPlanIn pl{true, sigma2, mode, budget, plan};
   return launch_score_planes(s, (const uint32_t*)planes, (const uint16_t*)scales, nullptr,
                              (const uint16_t*)q, scores, (cudaStream_t)stream, nullptr, &pl, wmax);

@@ -107,6 +107,7 @@ int launch_landmark_build(const Dims& s, const uint16_t* K, uint16_t* L, cudaStr
                           int64_t t0 = 0);
 int launch_score_landmark(const Dims& s, const uint16_t* L, const uint16_t* q, float* scores,
                           cudaStream_t st);
+constexpr int kSplitMaxHeads = 64;  // KV heads one SD_PLAN_SPLIT plan may couple
 int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode, int budget,
                 uint8_t* plan, cudaStream_t st);
 

@@ -112,8 +112,124 @@ plan_kernel(const uint16_t* __restrict__ q, const float* __restrict__ sigma2, in
   if (bit == 0) out[j] = (uint8_t)cnt;
 }
 
+// SD_PLAN_SPLIT: the budget split across the KV heads of a sequence.  One CTA per
+// sequence; the sequence's channels (h, j) are flattened to hj = h * kD + j and
+// thread t owns channels t C .. t C + C - 1 with all four of their pairs, so the
+// thread's pairs are contiguous in pair order 4 hj + b.  The (Hkv * budget)-th
+// largest pair value T is found with the 32-step bitwise search (one block-wide
+// count per step), every pair above T is taken and the pairs equal to T in pair
+// order until the total is met; a channel's bits are its pairs taken (a prefix
+// b = 0, 1, ... since its gains do not increase with b).  Same keys as plan_kernel's
+// water-filling, so one head gives the same plan.
+constexpr int kSplitThreads = 1024;
+constexpr int kSplitChan = kSplitMaxHeads * kD / kSplitThreads;  // channels per thread, at most
+
+// block-wide sum (every thread calls it; the result reaches every thread)
+__device__ __forceinline__ int split_block_sum(int v, int* wsum, int* tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = __reduce_add_sync(0xFFFFFFFFu, v);
+  if (lane == 0) wsum[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int x = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0;
+    x = __reduce_add_sync(0xFFFFFFFFu, x);
+    if (lane == 0) *tot = x;
+  }
+  __syncthreads();
+  const int r = *tot;
+  __syncthreads();  // wsum and tot are rewritten by the next call
+  return r;
+}
+
+__global__ void __launch_bounds__(kSplitThreads)
+plan_split_kernel(const uint16_t* __restrict__ q, const float* __restrict__ sigma2, int Hq,
+                  int Hkv, int G, int budget, uint8_t* __restrict__ plan) {
+  __shared__ int wsum[32];
+  __shared__ int tot;
+  const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int nch = Hkv * kD;
+  const int C = (nch + kSplitThreads - 1) / kSplitThreads;  // <= kSplitChan
+  const int c0 = t * C;
+  uint8_t* out = plan + (int64_t)b * nch;
+  const int64_t total = imin64((int64_t)Hkv * budget, 4 * (int64_t)nch);
+  if (total == 0 || total == 4 * (int64_t)nch) {
+    for (int c = 0; c < C; ++c)
+      if (c0 + c < nch) out[c0 + c] = total ? 4 : 0;
+    return;
+  }
+  uint32_t key[kSplitChan][4];
+  const float scale4[4] = {1.0f, 0.25f, 0.0625f, 0.015625f};
+#pragma unroll
+  for (int c = 0; c < kSplitChan; ++c) {
+    const int hj = c0 + c;
+    float w = 0.0f;
+    if (c < C && hj < nch) {
+      const int h = hj / kD, j = hj % kD;
+      float acc = 0.0f;  // fp32, group sum in ascending g, no fused multiply-add
+      for (int g = 0; g < G; ++g) {
+        const float x = bf16_to_f32(q[((int64_t)b * Hq + h * G + g) * kD + j]);
+        acc = __fadd_rn(acc, __fmul_rn(x, x));
+      }
+      w = __fmul_rn(acc, sigma2[(int64_t)h * kD + j]);
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+      key[c][p] = (c < C && hj < nch) ? key_of_f32(__fmul_rn(w, scale4[p])) : 0u;
+  }
+  auto live = [&](int c) { return c < C && c0 + c < nch; };
+  auto count = [&](auto pred) {
+    int n = 0;
+#pragma unroll
+    for (int c = 0; c < kSplitChan; ++c)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) n += live(c) && pred(key[c][p]);
+    return split_block_sum(n, wsum, &tot);
+  };
+  // T: the largest value with at least `total` pairs >= it
+  uint32_t T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    if (count([&](uint32_t k) { return k >= cand; }) >= total) T = cand;
+  }
+  const int above = count([&](uint32_t k) { return k > T; });
+  // pairs equal to T before this thread's, in pair order: a block exclusive scan
+  int eq = 0;
+#pragma unroll
+  for (int c = 0; c < kSplitChan; ++c)
+#pragma unroll
+    for (int p = 0; p < 4; ++p) eq += live(c) && key[c][p] == T;
+  int incl = eq;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int before = incl - eq;
+  for (int w2 = 0; w2 < warp; ++w2) before += wsum[w2];
+#pragma unroll
+  for (int c = 0; c < kSplitChan; ++c) {
+    if (!live(c)) continue;
+    int taken = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t k = key[c][p];
+      const bool e = k == T;
+      if (k > T || (e && before < total - above)) ++taken;
+      before += e;
+    }
+    out[c0 + c] = (uint8_t)taken;
+  }
+}
+
 int launch_plan(const Dims& s, const uint16_t* q, const float* sigma2, int mode, int budget,
                 uint8_t* plan, cudaStream_t st) {
+  if (mode == SD_PLAN_SPLIT) {
+    plan_split_kernel<<<s.B, kSplitThreads, 0, st>>>(q, sigma2, s.Hq, s.Hkv, s.G, budget, plan);
+    note_launches(1);
+    return check_launch("plan split");
+  }
   plan_kernel<<<s.B * s.Hkv, 4 * kD, 0, st>>>(q, sigma2, s.Hq, s.Hkv, s.G, mode, budget, plan);
   note_launches(1);
   return check_launch("plan");
