@@ -329,3 +329,121 @@ def delta_select(state: Resident, scores, idx, count, block: int, n_tokens: int,
     if rc:
         raise ValueError("delta_select: bad block, R, C or step")
     return ps[:, :C], pu[:, :C], pe[:, :C], pcount, pool, pool_count
+
+
+# ------------------------------------------------------------------------------------
+# One sequence split by tokens across shards (HashAttention: Semantic Sparsity for
+# Faster Inference, 2.5: contexts beyond one device; a sequence held by several
+# devices needs one exchange of top-k candidates and one of attention partials).
+# READING: shards are contiguous token ranges cut at multiples of 64 tokens (whole
+# bit-plane scale blocks, so each shard's own index gives the unsharded scores);
+# the forced windows stay with the shard holding them; the retrieval budget k is
+# the sequence's, as unsharded.
+# ------------------------------------------------------------------------------------
+def shard_bounds(n: int, shards: int):
+    """Token boundaries a_0 = 0 < ... < a_S = n of S contiguous shards cut at
+    multiples of 64 tokens (64 * floor(nb * s / S), nb = ceil(n / 64))."""
+    nb = (n + 63) // 64
+    return [min(n, 64 * ((nb * s) // shards)) for s in range(shards + 1)]
+
+
+def shard_windows(n: int, a: int, b: int, sink: int, local: int):
+    """The forced windows of shard [a, b) in its own token indices: (sink_s, local_s),
+    the parts of [0, lead) and [tail, n) it holds (lead = min(sink, n),
+    tail = max(n - local, lead), as the unsharded top-k takes them)."""
+    lead = min(sink, n)
+    tail = max(n - local, lead)
+    ns = b - a
+    sink_s = min(max(lead - a, 0), ns)
+    local_s = min(max(b - max(a, tail), 0), ns)
+    return sink_s, local_s
+
+
+def shard_candidates(scores_s, k: int, sink_s: int, local_s: int, a: int):
+    """Shard-local top-k of the competing tokens [sink_s, n_s - local_s) of each row,
+    in the order (score descending, index ascending): (score [rows][k] float64,
+    global index [rows][k] int32 (-1 past the count), count [rows], -1 for a row
+    holding a NaN)."""
+    s = np.asarray(scores_s, np.float64)
+    rows, ns = s.shape
+    lo, hi = sink_s, max(ns - local_s, sink_s)
+    sc = np.full((rows, k), -np.inf)
+    ix = np.full((rows, k), -1, np.int32)
+    cnt = np.zeros(rows, np.int32)
+    for r in range(rows):
+        seg = s[r, lo:hi]
+        if np.isnan(seg).any():
+            cnt[r] = -1
+            continue
+        order = sorted(range(len(seg)), key=lambda i: (-seg[i], i))[:k]
+        cnt[r] = len(order)
+        for t, i in enumerate(order):
+            sc[r, t] = seg[i]
+            ix[r, t] = a + lo + i
+    return sc, ix, cnt
+
+
+def topk_merge(cand_scores, cand_idx, cand_counts, k: int):
+    """The sequence's top-k from every shard's candidates: the first k of their union
+    in the order (score descending, global index ascending), written ascending.
+    Returns (idx [rows][k] int32, -1 past the count; count [rows], -1 if any shard
+    reported a NaN row)."""
+    S = len(cand_scores)
+    rows = cand_scores[0].shape[0]
+    idx = np.full((rows, k), -1, np.int32)
+    cnt = np.zeros(rows, np.int32)
+    for r in range(rows):
+        if any(int(cand_counts[s][r]) < 0 for s in range(S)):
+            cnt[r] = -1
+            continue
+        pool = [(float(cand_scores[s][r, t]), int(cand_idx[s][r, t]))
+                for s in range(S) for t in range(int(cand_counts[s][r]))]
+        best = sorted(pool, key=lambda x: (-x[0], x[1]))[:k]
+        sel = sorted(i for _, i in best)
+        cnt[r] = len(sel)
+        idx[r, :len(sel)] = sel
+    return idx, cnt
+
+
+def shard_select(sel_idx, sel_counts, a: int, b: int, sink_s: int, local_s: int):
+    """Shard [a, b)'s attention set in its own token indices, ascending: its forced
+    windows [0, sink_s) and [n_s - local_s, n_s) and the merged top-k's tokens in
+    [a, b).  Returns (idx [rows][stride] int32, count [rows]); a NaN row (count -1)
+    stays -1."""
+    rows = sel_idx.shape[0]
+    ns = b - a
+    sets = []
+    for r in range(rows):
+        if sel_counts[r] < 0:
+            sets.append(None)
+            continue
+        mine = [int(t) - a for t in sel_idx[r, :sel_counts[r]] if a <= t < b]
+        forced = list(range(sink_s)) + list(range(ns - local_s, ns))
+        sets.append(sorted(set(forced) | set(mine)))
+    stride = max([1] + [len(x) for x in sets if x is not None])
+    idx = np.full((rows, stride), -1, np.int32)
+    cnt = np.zeros(rows, np.int32)
+    for r, x in enumerate(sets):
+        if x is None:
+            cnt[r] = -1
+            continue
+        cnt[r] = len(x)
+        idx[r, :len(x)] = x
+    return idx, cnt
+
+
+def attend_combine(outs, lses):
+    """Split-softmax combine of per-shard attention over disjoint token sets: with
+    L = log sum_s exp(lse_s), o = sum_s exp(lse_s - L) o_s and lse = L; shards with
+    an empty set (lse = -inf) weigh 0; all empty gives o = 0, lse = -inf."""
+    lse = np.stack([np.asarray(x, np.float64) for x in lses])          # [S][B][Hq]
+    o = np.stack([np.asarray(x, np.float64) for x in outs])            # [S][B][Hq][d]
+    m = lse.max(axis=0)
+    fin = np.isfinite(m)
+    w = np.where(fin[None], np.exp(np.where(np.isfinite(lse), lse - np.where(fin, m, 0)[None],
+                                            -np.inf)), 0.0)
+    tot = w.sum(axis=0)
+    out = np.where(fin[..., None], (w[..., None] * o).sum(axis=0) /
+                   np.where(tot > 0, tot, 1.0)[..., None], 0.0)
+    L = np.where(fin, m + np.log(np.where(tot > 0, tot, 1.0)), -np.inf)
+    return out, L

@@ -807,3 +807,69 @@ def test_landmark_score_is_group_dot_product():
     onehot[0, 0, 37] = 1.0
     U1 = oracle.landmark_score(L[:1, :1], synth.to_bf16(onehot))
     assert np.array_equal(U1[0, 0], Lf[0, 0, :, 37])
+
+
+# ---------------------------------------------------------------------------------
+# One sequence split by tokens (HashAttention 2.5, contexts beyond one device): the
+# shards' candidates merged and their attention combined equal the unsharded step
+# ---------------------------------------------------------------------------------
+@pytest.mark.parametrize("S,n,k,sink,local", [(2, 64 * 20 + 17, 40, 3, 17), (3, 64 * 9, 30, 0, 0),
+                                              (4, 64 * 7 + 1, 25, 70, 5), (2, 300, 400, 4, 4)])
+def test_sharded_oracle_step_equals_unsharded(S, n, k, sink, local):
+    cfg = synth.config(0, n=n, B=2, Hq=8, Hkv=2, k=k, sink=sink, local=local)
+    inp = synth.make_inputs(cfg)
+    planes, scales = oracle.plane_build(inp.K)
+    plan = oracle.plan(inp.q, inp.sigma2, cfg.Hkv, oracle.PLAN_WATERFILL, 56)
+    s = oracle.plane_score(planes, scales, plan, inp.q, n=n).reshape(4, n)
+    ri, rc = oracle.topk(s, k, sink, local)
+    ro, rl = oracle.gather_attend(inp.q, inp.K, inp.V, ri.reshape(2, 2, -1), rc.reshape(2, 2),
+                                  1 / math.sqrt(cfg.d))
+    cut = oracle.shard_bounds(n, S)
+    assert cut[0] == 0 and cut[-1] == n and all(c % 64 == 0 for c in cut[:-1])
+    cands, outs, lses = [], [], []
+    for sh in range(S):
+        a, b = cut[sh], cut[sh + 1]
+        Ks = np.ascontiguousarray(inp.K[:, :, a:b])
+        ps, ss = oracle.plane_build(Ks)
+        s_s = oracle.plane_score(ps, ss, plan, inp.q, n=b - a).reshape(4, b - a)
+        assert np.array_equal(s_s, s[:, a:b])  # whole scale blocks: the same scores
+        cands.append(oracle.shard_candidates(s_s, k, *oracle.shard_windows(n, a, b, sink, local), a))
+    mi, mc = oracle.topk_merge([c[0] for c in cands], [c[1] for c in cands],
+                               [c[2] for c in cands], k)
+    union = [[] for _ in range(4)]
+    for sh in range(S):
+        a, b = cut[sh], cut[sh + 1]
+        li, lc = oracle.shard_select(mi, mc, a, b, *oracle.shard_windows(n, a, b, sink, local))
+        for r in range(4):
+            union[r] += [int(t) + a for t in li[r, :lc[r]]]
+        o, l = oracle.gather_attend(inp.q, np.ascontiguousarray(inp.K[:, :, a:b]),
+                                    np.ascontiguousarray(inp.V[:, :, a:b]),
+                                    li.reshape(2, 2, -1), lc.reshape(2, 2), 1 / math.sqrt(cfg.d))
+        outs.append(o)
+        lses.append(l)
+    # the shards' sets, shifted to global indices, partition the unsharded set
+    for r in range(4):
+        assert sorted(union[r]) == ri[r, :rc[r]].tolist()
+    o, l = oracle.attend_combine(outs, lses)
+    assert np.abs(o - ro).max() < 1e-12 and np.abs(l - rl).max() < 1e-12
+
+
+def test_attend_combine_special_cases():
+    o1 = np.ones((1, 1, 4))
+    o2 = np.full((1, 1, 4), 3.0)
+    # equal masses: the mean; one empty shard: the other; all empty: 0 and -inf
+    o, l = oracle.attend_combine([o1, o2], [np.zeros((1, 1)), np.zeros((1, 1))])
+    assert np.allclose(o, 2.0) and np.allclose(l, math.log(2.0))
+    o, l = oracle.attend_combine([o1, o2], [np.full((1, 1), -np.inf), np.full((1, 1), 0.5)])
+    assert np.allclose(o, 3.0) and np.allclose(l, 0.5)
+    o, l = oracle.attend_combine([o1, o2], [np.full((1, 1), -np.inf)] * 2)
+    assert np.all(o == 0.0) and np.all(l == -np.inf)
+
+
+def test_topk_merge_nan_and_short_rows():
+    sc = [np.array([[3.0, 1.0, -np.inf]]), np.array([[2.0, -np.inf, -np.inf]])]
+    ix = [np.array([[10, 4, -1]], np.int32), np.array([[70, -1, -1]], np.int32)]
+    mi, mc = oracle.topk_merge(sc, ix, [np.array([2]), np.array([1])], 3)
+    assert mc.tolist() == [3] and mi[0].tolist() == [4, 10, 70]
+    mi, mc = oracle.topk_merge(sc, ix, [np.array([2]), np.array([-1])], 3)
+    assert mc.tolist() == [-1]
