@@ -467,6 +467,65 @@ int sd_resident_gather(const sd_shape* shape, int32_t block, const void* K, cons
                        void* K_pool, void* V_pool, void* stream);
 
 /*
+ * One sequence split by tokens across devices (HashAttention 2.5: contexts beyond
+ * one device).  Shard s holds tokens [a_s, a_s + n_s) of the sequence with its own
+ * index, K and V (cut at whole 64-token blocks, so its bit-plane scores are the
+ * unsharded ones); the forced windows [0, lead) and [tail, n) stay with the shards
+ * holding them, as (sink_s, local_s) in the shard's own indices.  A step: each shard
+ * runs its plan, scan and sd_topk with (k, sink_s, local_s); sd_shard_candidates;
+ * an all-gather of the candidates; sd_topk_merge (every shard the same result);
+ * sd_shard_select; sd_gather_attend on the shard's set; an all-gather of (out, lse);
+ * sd_attend_combine.  The result equals the unsharded step's selection exactly and
+ * its attention within rounding.
+ *
+ * sd_shard_candidates -- the shard's competing tokens of its own top-k: the entries
+ *   of idx [rows][idx_stride] (ascending, count [rows]) in [sink_s, n_s - local_s),
+ *   in their order, with scores [rows][n_s] (fp32) and global index offset + t:
+ *   cand_score fp32 [rows][k], cand_idx int32 [rows][k], cand_count [rows] (-1 for a
+ *   row whose count is -1).  Entries past cand_count are not written.
+ */
+int sd_shard_candidates(const float* scores, int64_t rows, int64_t n_s, const int32_t* idx,
+                        int64_t idx_stride, const int32_t* count, int32_t sink_s, int32_t local_s,
+                        int64_t offset, int32_t k, float* cand_score, int32_t* cand_idx,
+                        int32_t* cand_count, void* stream);
+
+/*
+ * sd_topk_merge -- the sequence's top-k from every shard's candidates:
+ *   cand_score fp32 [shards][rows][k], cand_idx int32 [shards][rows][k], cand_count
+ *   int32 [shards][rows] (as sd_shard_candidates writes them, gathered).  Of their
+ *   union, the first k in the order (score descending, index ascending; -0.0 equals
+ *   +0.0) are written ascending to idx [rows][idx_stride >= k]; count [rows] = their
+ *   number, -1 if any shard's count is -1.  shards * k <= 8192.
+ */
+int sd_topk_merge(int64_t rows, int32_t shards, int32_t k, const float* cand_score,
+                  const int32_t* cand_idx, const int32_t* cand_count, int32_t* idx,
+                  int64_t idx_stride, int32_t* count, void* stream);
+
+/*
+ * sd_shard_select -- the shard's attention set in its own indices, ascending:
+ *   [0, sink_s), the merged tokens (sel_idx [rows][sel_stride], sel_count [rows],
+ *   global, ascending, at most k) that lie in [offset, offset + n_s) shifted by
+ *   -offset, and [n_s - local_s, n_s); idx [rows][idx_stride >= sink_s + local_s +
+ *   k], count [rows] (-1 where sel_count is -1).  The input of sd_gather_attend over
+ *   the shard's K and V.
+ */
+int sd_shard_select(int64_t rows, const int32_t* sel_idx, int64_t sel_stride,
+                    const int32_t* sel_count, int64_t offset, int64_t n_s, int32_t sink_s,
+                    int32_t local_s, int32_t k, int32_t* idx, int64_t idx_stride, int32_t* count,
+                    void* stream);
+
+/*
+ * sd_attend_combine -- the split-softmax combine of the shards' attention over
+ *   disjoint token sets: outs fp32 [shards][batch][hq][128] and lses fp32
+ *   [shards][batch][hq] as sd_gather_attend writes them; with L = log sum_s
+ *   exp(lse_s), out = sum_s exp(lse_s - L) out_s and lse = L (lse may be NULL).
+ *   Shards with an empty set (lse = -inf) weigh 0; all empty give out = 0, lse =
+ *   -inf.
+ */
+int sd_attend_combine(int32_t shards, int64_t batch, int32_t hq, const float* outs,
+                      const float* lses, float* out, float* lse, void* stream);
+
+/*
  * sd_device_status -- device-side errors of the work already enqueued on
  * `stream`: waits for the stream, then reads and clears this GPU's libsd error
  * word.  Every wait inside libsd's kernels is bounded; one that runs out (a
@@ -510,7 +569,9 @@ const char* sd_last_error(void);
 
 /* ABI version (major * 100 + minor): 101 adds sd_append_index, SD_PLAN_TOPQ,
  * SD_IDX_LANDMARK, sd_delta_select and sd_resident_gather to 100; 102 adds
- * sd_device_status, sd_set_fallback_paths and sd_debug_set_device_error. */
+ * sd_device_status, sd_set_fallback_paths and sd_debug_set_device_error; 103 adds
+ * SD_PLAN_SPLIT, sd_shard_candidates, sd_topk_merge, sd_shard_select and
+ * sd_attend_combine. */
 int sd_version(void);
 
 /*

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(sd):
     assert sorted(_abi.SIGNATURES) == header_functions()
     for name in header_functions():
         assert callable(getattr(sd, name)), name
-    assert sd.sd_version() == 102  # 1.02: device status, fallback switch
+    assert sd.sd_version() == 103  # 1.03: split plan, sequence shards
 
 
 def test_shape_checks(sd):

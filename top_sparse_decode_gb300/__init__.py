@@ -30,7 +30,8 @@ __all__ = [
     "sd_gather_attend_noalloc", "sd_offload_gather", "Resident", "sd_delta_select",
     "sd_resident_gather",
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count", "sd_device_status",
-    "sd_set_fallback_paths", "sd_debug_set_device_error",
+    "sd_set_fallback_paths", "sd_debug_set_device_error", "sd_shard_candidates",
+    "sd_topk_merge", "sd_shard_select", "sd_attend_combine",
     "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax",
     "sd_select_attend_workspace_size", "sd_select_attend", "sd_hamming_topk_workspace_size",
     "sd_hamming_topk",
@@ -264,6 +265,36 @@ def sd_resident_gather(shape: SdShape, block: int, K, V, plan_slot, plan_unit, p
                                     _ptr(plan_unit), _ptr(plan_count), admit_cap, n_slots,
                                     _ptr(K_pool), _ptr(V_pool), _stream(stream)),
            "sd_resident_gather")
+
+
+def sd_shard_candidates(scores, rows: int, n_s: int, idx, idx_stride: int, count, sink_s: int,
+                        local_s: int, offset: int, k: int, cand_score, cand_idx, cand_count,
+                        stream=None) -> None:
+    _check(lib().sd_shard_candidates(_ptr(scores), rows, n_s, _ptr(idx), idx_stride, _ptr(count),
+                                     sink_s, local_s, offset, k, _ptr(cand_score),
+                                     _ptr(cand_idx), _ptr(cand_count), _stream(stream)),
+           "sd_shard_candidates")
+
+
+def sd_topk_merge(rows: int, shards: int, k: int, cand_score, cand_idx, cand_count, idx,
+                  idx_stride: int, count, stream=None) -> None:
+    _check(lib().sd_topk_merge(rows, shards, k, _ptr(cand_score), _ptr(cand_idx),
+                               _ptr(cand_count), _ptr(idx), idx_stride, _ptr(count),
+                               _stream(stream)), "sd_topk_merge")
+
+
+def sd_shard_select(rows: int, sel_idx, sel_stride: int, sel_count, offset: int, n_s: int,
+                    sink_s: int, local_s: int, k: int, idx, idx_stride: int, count,
+                    stream=None) -> None:
+    _check(lib().sd_shard_select(rows, _ptr(sel_idx), sel_stride, _ptr(sel_count), offset, n_s,
+                                 sink_s, local_s, k, _ptr(idx), idx_stride, _ptr(count),
+                                 _stream(stream)), "sd_shard_select")
+
+
+def sd_attend_combine(shards: int, batch: int, hq: int, outs, lses, out, lse=None,
+                      stream=None) -> None:
+    _check(lib().sd_attend_combine(shards, batch, hq, _ptr(outs), _ptr(lses), _ptr(out),
+                                   _ptr(lse), _stream(stream)), "sd_attend_combine")
 
 
 def sd_device_status(stream=None) -> None:

@@ -70,6 +70,12 @@ SIGNATURES = {
                              _p, _p, _p, _p, _p, _i64, _p, _p]),
     "sd_resident_gather": (_i, [_PS, ctypes.c_int32, _p, _p, _p, _p, _p, ctypes.c_int32,
                                 ctypes.c_int32, _p, _p, _p]),
+    "sd_shard_candidates": (_i, [_p, _i64, _i64, _p, _i64, _p, ctypes.c_int32, ctypes.c_int32,
+                                 _i64, ctypes.c_int32, _p, _p, _p, _p]),
+    "sd_topk_merge": (_i, [_i64, ctypes.c_int32, ctypes.c_int32, _p, _p, _p, _p, _i64, _p, _p]),
+    "sd_shard_select": (_i, [_i64, _p, _i64, _p, _i64, _i64, ctypes.c_int32, ctypes.c_int32,
+                             ctypes.c_int32, _p, _i64, _p, _p]),
+    "sd_attend_combine": (_i, [ctypes.c_int32, _i64, ctypes.c_int32, _p, _p, _p, _p, _p]),
     "sd_device_status": (_i, [_p]),
     "sd_set_fallback_paths": (_i, [_i]),
     "sd_debug_set_device_error": (_i, [_p]),

@@ -107,7 +107,7 @@ using namespace sd;
 
 extern "C" {
 
-int sd_version(void) { return 102; }
+int sd_version(void) { return 103; }
 
 int64_t sd_launch_count(void) { return (int64_t)launch_total(); }
 
@@ -590,6 +590,60 @@ int sd_resident_gather(const sd_shape* shape, int32_t block, const void* K, cons
   return launch_resident_gather(s, block, (const uint16_t*)dk, (const uint16_t*)dv, plan_slot,
                                 plan_unit, plan_count, admit_cap, n_slots, (uint16_t*)K_pool,
                                 (uint16_t*)V_pool, (cudaStream_t)stream);
+}
+
+int sd_shard_candidates(const float* scores, int64_t rows, int64_t n_s, const int32_t* idx,
+                        int64_t idx_stride, const int32_t* count, int32_t sink_s, int32_t local_s,
+                        int64_t offset, int32_t k, float* cand_score, int32_t* cand_idx,
+                        int32_t* cand_count, void* stream) {
+  if (!scores || !idx || !count || !cand_score || !cand_idx || !cand_count)
+    return fail(SD_ERR_INVALID_ARG, "sd_shard_candidates: NULL input");
+  if (rows < 1 || rows > 65535 * 8 || n_s < 1 || n_s >= ((int64_t)1 << 31) || offset < 0 ||
+      offset + n_s >= ((int64_t)1 << 31))
+    return fail(SD_ERR_INVALID_ARG, "sd_shard_candidates: bad rows, n_s or offset");
+  if (k < 1 || k > kMaxTopK || sink_s < 0 || local_s < 0 || idx_stride < 1)
+    return fail(SD_ERR_INVALID_ARG, "sd_shard_candidates: bad k, window or stride");
+  return launch_shard_candidates(scores, rows, n_s, idx, idx_stride, count, sink_s, local_s,
+                                 offset, k, cand_score, cand_idx, cand_count,
+                                 (cudaStream_t)stream);
+}
+
+int sd_topk_merge(int64_t rows, int32_t shards, int32_t k, const float* cand_score,
+                  const int32_t* cand_idx, const int32_t* cand_count, int32_t* idx,
+                  int64_t idx_stride, int32_t* count, void* stream) {
+  if (!cand_score || !cand_idx || !cand_count || !idx || !count)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_merge: NULL input");
+  if (rows < 1 || rows > 2147483647 || shards < 1 || k < 1 || k > kMaxTopK || idx_stride < k)
+    return fail(SD_ERR_INVALID_ARG, "sd_topk_merge: bad rows, shards, k or stride");
+  if ((int64_t)shards * k > kMergeMaxCand)
+    return fail(SD_ERR_UNSUPPORTED, "sd_topk_merge: shards * k = %lld > %d",
+                (long long)shards * k, kMergeMaxCand);
+  return launch_topk_merge(rows, shards, k, cand_score, cand_idx, cand_count, idx, idx_stride,
+                           count, (cudaStream_t)stream);
+}
+
+int sd_shard_select(int64_t rows, const int32_t* sel_idx, int64_t sel_stride,
+                    const int32_t* sel_count, int64_t offset, int64_t n_s, int32_t sink_s,
+                    int32_t local_s, int32_t k, int32_t* idx, int64_t idx_stride, int32_t* count,
+                    void* stream) {
+  if (!sel_idx || !sel_count || !idx || !count)
+    return fail(SD_ERR_INVALID_ARG, "sd_shard_select: NULL input");
+  if (rows < 1 || rows > 65535 * 8 || n_s < 1 || n_s >= ((int64_t)1 << 31) || offset < 0 ||
+      sink_s < 0 || local_s < 0 || (int64_t)sink_s + local_s > n_s || k < 0 || sel_stride < k)
+    return fail(SD_ERR_INVALID_ARG, "sd_shard_select: bad rows, n_s, offset, window or stride");
+  if (idx_stride < (int64_t)sink_s + local_s + k)
+    return fail(SD_ERR_INVALID_ARG, "sd_shard_select: idx_stride %lld < %lld",
+                (long long)idx_stride, (long long)sink_s + local_s + k);
+  return launch_shard_select(rows, sel_idx, sel_stride, sel_count, offset, n_s, sink_s, local_s,
+                             idx, idx_stride, count, (cudaStream_t)stream);
+}
+
+int sd_attend_combine(int32_t shards, int64_t batch, int32_t hq, const float* outs,
+                      const float* lses, float* out, float* lse, void* stream) {
+  if (!outs || !lses || !out) return fail(SD_ERR_INVALID_ARG, "sd_attend_combine: NULL input");
+  if (shards < 1 || batch < 1 || hq < 1 || batch * hq * kD >= ((int64_t)1 << 40))
+    return fail(SD_ERR_INVALID_ARG, "sd_attend_combine: bad shards, batch or hq");
+  return launch_attend_combine(shards, batch * hq, outs, lses, out, lse, (cudaStream_t)stream);
 }
 
 int sd_set_fallback_paths(int on) {

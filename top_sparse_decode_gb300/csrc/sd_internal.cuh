@@ -175,6 +175,20 @@ int launch_select_attend(const Dims& s, const float* scores, const float* wmax,
                          const uint16_t* V, float scale, int32_t* idx, int64_t idx_stride,
                          int32_t* count, int64_t max_count, float* out, float* lse, void* ws,
                          size_t ws_bytes, cudaStream_t st);
+// One sequence split by tokens across devices (sd_shard.cu).
+constexpr int kMergeMaxCand = 8192;  // shards * k one merge may hold
+int launch_shard_candidates(const float* scores, int64_t rows, int64_t n_s, const int32_t* idx,
+                            int64_t idx_stride, const int32_t* count, int sink_s, int local_s,
+                            int64_t offset, int k, float* cs, int32_t* ci, int32_t* cc,
+                            cudaStream_t st);
+int launch_topk_merge(int64_t rows, int S, int k, const float* cs, const int32_t* ci,
+                      const int32_t* cc, int32_t* out, int64_t out_stride, int32_t* ocount,
+                      cudaStream_t st);
+int launch_shard_select(int64_t rows, const int32_t* sel, int64_t sel_stride,
+                        const int32_t* scount, int64_t a, int64_t n_s, int sink_s, int local_s,
+                        int32_t* out, int64_t out_stride, int32_t* ocount, cudaStream_t st);
+int launch_attend_combine(int S, int64_t BH, const float* outs, const float* lses, float* out,
+                          float* lse, cudaStream_t st);
 int launch_offload_gather(const Dims& s, const uint32_t* host_planes, const uint16_t* host_scales,
                           const uint8_t* plan, uint32_t* dev_planes, uint16_t* dev_scales,
                           cudaStream_t st);
