@@ -12,7 +12,8 @@ gather-attend (the KV-write-path index build is done once, untimed).
 
 Timing: W untimed warm-up steps, then exactly K steps, each timed with CUDA
 events on the launching stream; L2 (129 MB) is flushed before every timed step
-by writing a 256 MB buffer, outside the events.  `value` = keys scored per
+by writing a 256 MB buffer and then reading another 256 MB buffer (L2 then holds
+clean lines of unrelated data), outside the events.  `value` = keys scored per
 second = (B * Hkv * n) / step time, summed over ranks (independent replicas,
 weak scaling).  One JSON line is printed by rank 0.
 
@@ -146,6 +147,22 @@ def dev_tensor(x, torch):
 
 
 # ------------------------------------------------------------------------------------
+class L2Flush:
+    """Before every timed step: write a 256 MB buffer (larger than the 129 MB L2),
+    then read another 256 MB buffer, so that the step finds L2 holding clean lines
+    of unrelated data (none of its inputs, and no dirty lines of the flush left for
+    the step to write back)."""
+
+    def __init__(self, torch):
+        self.a = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.b = torch.zeros(64 << 20, dtype=torch.int32, device="cuda")
+        self.sink = torch.empty((), dtype=torch.int32, device="cuda")
+
+    def zero_(self):
+        self.a.zero_()
+        self.sink.copy_(self.b.max())
+
+
 def timed_steps(torch, fn, steps, warmup, flush_buf, ws=1):
     """Runs fn() warmup + steps times; returns per-step device ms of the timed ones.
     The L2 flush before each step sits outside the events."""
@@ -226,7 +243,7 @@ def peaks():
 
 
 # ------------------------------------------------------------------------------------
-def oracle_sample(inp, heads, n_tok):
+def oracle_sample(inp, heads, n_tok, build=True):
     """Oracle inputs for a sample of the step: the first `heads` KV heads of
     sequence 0 over the first n_tok tokens, with its planes (KV-write path)."""
     import oracle
@@ -235,34 +252,84 @@ def oracle_sample(inp, heads, n_tok):
     Kh = np.ascontiguousarray(inp.K[:1, :heads, :n_tok])
     Vh = np.ascontiguousarray(inp.V[:1, :heads, :n_tok])
     s2 = np.ascontiguousarray(inp.sigma2[:heads])
-    planes, scales = oracle.plane_build(Kh)
-    return dict(q=qh, K=Kh, V=Vh, s2=s2, planes=planes, scales=scales, heads=heads, n=n_tok)
+    smp = dict(q=qh, K=Kh, V=Vh, s2=s2, heads=heads, n=n_tok)
+    if build:
+        t0 = time.perf_counter()
+        smp["planes"], smp["scales"] = oracle.plane_build(Kh)
+        smp["build_s"] = time.perf_counter() - t0
+    return smp
 
 
-def oracle_step(smp, k, d=128):
+def oracle_step(smp, k, d=128, stages=None):
     """The oracle, as it stands: plan -> bit-plane score -> top-k -> gather-attend.
-    Returns seconds."""
+    Returns seconds; with a dict `stages`, adds each stage's seconds to it."""
     import oracle
     h = smp["heads"]
-    t0 = time.perf_counter()
+    t = [time.perf_counter()]
     plan = oracle.plan(smp["q"], smp["s2"], h, oracle.PLAN_WATERFILL, 56)
+    t.append(time.perf_counter())
     sc = oracle.plane_score(smp["planes"], smp["scales"], plan, smp["q"])
+    t.append(time.perf_counter())
     idx, cnt = oracle.topk(sc.reshape(h, -1), k, 0, 0)
+    t.append(time.perf_counter())
     oracle.gather_attend(smp["q"], smp["K"], smp["V"], idx.reshape(1, h, -1),
                          cnt.reshape(1, h), 1 / math.sqrt(d))
-    return time.perf_counter() - t0
+    t.append(time.perf_counter())
+    if stages is not None:
+        for nm, a, b in zip(("plan", "score", "topk", "gather_attend"), t[:-1], t[1:]):
+            stages[nm] = stages.get(nm, 0.0) + (b - a)
+    return t[-1] - t[0]
+
+
+def cpu_model() -> str:
+    """The host CPU's model string (lscpu, else /proc/cpuinfo, else the machine)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 def cpu_baseline(inp, cfg, heads=None):
-    """CPU baseline leg: the oracle on the same 1M-token step (all KV heads)."""
+    """CPU baseline leg: the oracle, as it stands, on the host cores.
+    Multi-thread: the whole 1M-token step (every KV head), per stage, with the
+    KV-write-path index build timed apart.  Single-thread: one KV head over the
+    first 262,144 tokens, per stage (about 1/32 of the step's work)."""
     import oracle
     heads = heads or cfg.Hkv
+    cores = oracle.threads()
+    st_mt = {}
     smp = oracle_sample(inp, heads, cfg.n)
-    dt = oracle_step(smp, cfg.k, cfg.d)
-    return {"value": heads * cfg.n / dt, "unit": UNIT, "cores": oracle.threads(),
-            "kind": "oracle",
+    dt = oracle_step(smp, cfg.k, cfg.d, st_mt)
+    n1 = min(cfg.n, 1 << 18)
+    prev = oracle.set_threads(1)
+    try:
+        st_1 = {}
+        smp1 = oracle_sample(inp, 1, n1)
+        dt1 = oracle_step(smp1, cfg.k, cfg.d, st_1)
+    finally:
+        oracle.set_threads(prev)
+    return {"value": heads * cfg.n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{heads} of {cfg.Hkv} KV heads x {cfg.n} tokens of the step (plan, "
-                      f"bit-plane score, top-{cfg.k}, gather-attend) in {dt:.2f} s"}
+                      f"bit-plane score, top-{cfg.k}, gather-attend) in {dt:.2f} s on "
+                      f"{cores} threads",
+            "stages_s": {k2: round(v, 4) for k2, v in st_mt.items()},
+            "index_build_s": round(smp["build_s"], 4),
+            "single_thread": {"value": n1 / dt1, "unit": UNIT, "cores": 1,
+                              "sample": f"1 KV head x {n1} tokens of the step in {dt1:.2f} s",
+                              "stages_s": {k2: round(v, 4) for k2, v in st_1.items()},
+                              "index_build_s": round(smp1["build_s"], 4)}}
 
 
 def run_reference(args, ws, rank):
@@ -464,7 +531,7 @@ def main():
     K = dev_tensor(inp.K, torch)
     V = dev_tensor(inp.V, torch)
     sigma2 = dev_tensor(inp.sigma2, torch)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     B, Hq, Hkv, n = cfg.B, cfg.Hq, cfg.Hkv, cfg.n
     keys = B * Hkv * n
 
@@ -495,6 +562,7 @@ def main():
     clocks.start()
     times = timed_steps(torch, run, args.steps, args.warmup, flush, ws)
     ck = clocks.stop()
+    sd.sd_device_status()  # raises if a bounded wait inside a kernel ran out
     t_step = statistics.mean(times)
     t_step_max = max_over_ranks(t_step, ws)
     value = keys * ws / (t_step_max * 1e-3)
@@ -554,7 +622,8 @@ def main():
         # variance (the 136-bit class) and the 16 of largest query mass (SparQ r = 16,
         # 68 bits: 4 plane bits and a quarter bit of fp16 scale per channel and token)
         for vname, vmode, vbudget in [("fixed32x4", sd.SD_PLAN_FIXED, 32),
-                                      ("topq16x4", sd.SD_PLAN_TOPQ, 16)]:
+                                      ("topq16x4", sd.SD_PLAN_TOPQ, 16),
+                                      ("split56", sd.SD_PLAN_SPLIT, 56)]:
             scf = StepConfig(sd.SD_IDX_PLANES, B, Hq, Hkv, n, k=cfg.k, plan_mode=vmode,
                              budget=vbudget)
             stf = DecodeStep(scf, K, V, index, sigma2=sigma2)
@@ -654,9 +723,10 @@ def main():
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, cfg)
 
-    # ALU peak: 152 SMs x 128 lanes x the median SM clock seen under load
+    # ALU peak: the device's SMs x 128 FP32 lanes x the median SM clock seen under load
     sm_mhz = ck.get("sm_mhz") or 1920.0
-    alu_peak = 152 * 128 * sm_mhz * 1e6
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    alu_peak = sms * 128 * sm_mhz * 1e6
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step_max, "higher_is_better": True,
@@ -664,7 +734,9 @@ def main():
         "config": {"workload": f"longctx-1m: B={B}, Hq={Hq}, Hkv={Hkv}, d={cfg.d}, n={n}; "
                                f"56-bit water-filled bit-plane scan, top-{cfg.k}, "
                                f"gather-attend over bf16 K/V in HBM",
-                   "l2": "flushed (256 MB write) before every timed step", "launch": mode,
+                   "l2": "flushed before every timed step: a 256 MB write, then a 256 MB "
+                         "read of another buffer (no dirty lines of the flush left)",
+                   "launch": mode,
                    "parallelism": f"replicas x{ws}"},
         "us_per_step": t_step_max * 1e3,
         "stages_us": {"plan": st_prep * 1e3, "scan": st_score * 1e3, "topk": st_topk * 1e3,
@@ -680,9 +752,14 @@ def main():
                      "achieved": alu_ops / (st_score * 1e-3) / 1e12,
                      "peak": alu_peak / 1e12, "unit": "T token-planes/s",
                      "frac": alu_ops / (st_score * 1e-3) / alu_peak,
+                     # the bit test and the predicated add are two issued instructions:
+                     # the issue-rate bound is half the one-operation peak
+                     "frac_issue_bound": 2 * alu_ops / (st_score * 1e-3) / alu_peak,
                      "traffic": scan_traffic("longctx-1m") if n == 1048576 else None,
                      "ops_per_launch": alu_ops, "alg_bytes_per_launch": scan_bytes,
-                     "peak_kind": "derived: 152 SMs x 128 FP32 lanes x median SM clock"},
+                     "peak_kind": f"derived: {sms} SMs x 128 FP32 lanes x median SM clock "
+                                  f"({sm_mhz:.0f} MHz); frac counts one operation per "
+                                  f"token-plane, frac_issue_bound two instructions"},
         "roofline_hbm": {"bound": "hbm", "kernel": "score_planes_tma_kernel",
                          "achieved": scan_gbs, "peak": peak_gbs, "unit": "GB/s",
                          "frac": scan_gbs / peak_gbs, "peak_kind": peak_kind,

@@ -56,6 +56,8 @@ def _l():
             lib.orc_f16_to_f32.restype = ctypes.c_float
             lib.orc_threads.argtypes = []
             lib.orc_threads.restype = i32
+            lib.orc_set_threads.argtypes = [i32]
+            lib.orc_set_threads.restype = i32
             lib.orc_reconstruct.argtypes = [i32, i32, d]
             lib.orc_reconstruct.restype = d
             lib.orc_sig_encode.argtypes = [p, i64, i32, p, p, i32, p, p, p]
@@ -99,6 +101,11 @@ def _c(a, dtype):
 
 def threads() -> int:
     return int(_l().orc_threads())
+
+
+def set_threads(t: int) -> int:
+    """Threads of the oracle's parallel loops from now on; returns the previous count."""
+    return int(_l().orc_set_threads(int(t)))
 
 
 def f32_to_f16(x: float) -> int:

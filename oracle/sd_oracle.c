@@ -95,6 +95,12 @@ float orc_f16_to_f32(uint16_t h) {
 
 /* threads the oracle's parallel loops use (for reporting a CPU baseline) */
 int orc_threads(void) { return omp_get_max_threads(); }
+/* sets them (the CPU baseline's single-thread leg); returns the previous count */
+int orc_set_threads(int t) {
+  int prev = omp_get_max_threads();
+  if (t >= 1) omp_set_num_threads(t);
+  return prev;
+}
 
 static int popcount32(uint32_t x) {
   int c = 0;
