@@ -65,6 +65,34 @@ def test_plan_score_any_n(sd, n, ncap):
     assert np.array_equal(host(wmax, np.float32), pad.reshape(rows.shape[0], -1, 32).max(axis=2))
 
 
+def test_plan_score_any_n_block_per_lane(sd):
+    # 8 KV heads x 655,377 tokens: every CTA's range exceeds one 16K-token tile, so
+    # the scan's compute lanes own whole 64-token blocks; the last block is partial
+    n = 655360 + 17
+    ncap = 655360 + 512
+    cfg = synth.config(2, B=1, Hq=32, Hkv=8, n=n)
+    inp = synth.make_inputs(cfg, with_v=False)
+    shp = sd.make_shape(1, 32, 8, n, n_cap=ncap)
+    planes = empty((1, 8, 128, 4, ncap // 32), np.uint32)
+    scales = empty((1, 8, 128, ncap // 64), np.uint16)
+    sd.sd_build_index(sd.SD_IDX_PLANES, shp, dev(padded(inp.K, ncap)), None, planes, scales)
+    plan = empty((1, 8, 128), np.uint8)
+    scores = empty((8, n), np.float32)
+    wmax = empty((8, (n + 31) // 32), np.float32)
+    sd.sd_plan_score(shp, planes, scales, dev(inp.q), dev(inp.sigma2), sd.SD_PLAN_WATERFILL, 56,
+                     plan, scores, wmax)
+    torch.cuda.synchronize()
+    rp, rs = oracle.plane_build(inp.K)
+    rplan = oracle.plan(inp.q, inp.sigma2, 8, 0, 56)
+    assert np.array_equal(host(plan, np.uint8), rplan)
+    ref, l1 = oracle.plane_score(rp, rs, rplan, inp.q, with_l1=True, n=n)
+    got = host(scores, np.float32)
+    check_scores(got, ref.reshape(8, n), l1.reshape(8, n), "any-n plane scores (block per lane)")
+    pad = np.full((8, ((n + 31) // 32) * 32), -np.inf, np.float32)
+    pad[:, :n] = got
+    assert np.array_equal(host(wmax, np.float32), pad.reshape(8, -1, 32).max(axis=2))
+
+
 @pytest.mark.parametrize("n,k,sink,local", [(20000 + 7, 512, 0, 0), (65536 + 1, 512, 0, 0),
                                             (40000 + 19, 300, 5, 100)])
 def test_topk_wmax_any_n(sd, n, k, sink, local):

@@ -420,11 +420,10 @@ score_planes_tma_kernel(const uint32_t* __restrict__ planes, const uint16_t* __r
   pt_compute<CAND, WPL>(S, scores, n, cd, wmax, rg.bh0);
 }
 
-template <int G, bool CAND>
+template <int G, bool CAND, int WPL>
 int pt_launch(const Dims& s, const uint32_t* planes, const uint16_t* scales, const uint8_t* plan,
               const uint16_t* q, float* scores, const PsCand& cd, const PsPlanIn& pl, float* wmax,
               int grid, int upr, int64_t total, cudaStream_t st) {
-  constexpr int WPL = CAND ? 1 : 2;
   auto kern = score_planes_tma_kernel<G, CAND, WPL>;
   if (int rc = set_smem_limit((const void*)kern, sizeof(PtSmem<WPL>),
                               "score_planes_tma: smem attribute"))
@@ -480,17 +479,27 @@ int launch_score_planes_tma(const Dims& s, const uint32_t* planes, const uint16_
   const PsCand none{};
   if (cand) {
     switch (s.G) {
-      case 1: return pt_launch<1, true>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, grid, upr, total, st);
-      case 2: return pt_launch<2, true>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, grid, upr, total, st);
-      case 4: return pt_launch<4, true>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, grid, upr, total, st);
-      default: return pt_launch<8, true>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, grid, upr, total, st);
+      case 1: return pt_launch<1, true, 1>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, grid, upr, total, st);
+      case 2: return pt_launch<2, true, 1>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, grid, upr, total, st);
+      case 4: return pt_launch<4, true, 1>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, grid, upr, total, st);
+      default: return pt_launch<8, true, 1>(s, planes, scales, plan, q, scores, *cand, pl, nullptr, grid, upr, total, st);
+    }
+  }
+  // a CTA whose range is under one 16K-token tile keeps every lane busy with one
+  // word per lane (8K-token tiles); longer ranges take a block per lane
+  if (total * kPtUnit / grid < PtGeo<2>::kTile) {
+    switch (s.G) {
+      case 1: return pt_launch<1, false, 1>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
+      case 2: return pt_launch<2, false, 1>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
+      case 4: return pt_launch<4, false, 1>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
+      default: return pt_launch<8, false, 1>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
     }
   }
   switch (s.G) {
-    case 1: return pt_launch<1, false>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
-    case 2: return pt_launch<2, false>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
-    case 4: return pt_launch<4, false>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
-    default: return pt_launch<8, false>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
+    case 1: return pt_launch<1, false, 2>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
+    case 2: return pt_launch<2, false, 2>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
+    case 4: return pt_launch<4, false, 2>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
+    default: return pt_launch<8, false, 2>(s, planes, scales, plan, q, scores, none, pl, wmax, grid, upr, total, st);
   }
 }
 
