@@ -61,6 +61,20 @@ int set_smem_limit(const void* kernel, size_t bytes, const char* what) {
   return SD_OK;
 }
 
+int device_sm_count() {
+  static std::atomic<int> cnt[kMaxDev];
+  const int c = per_device_cached(cnt, [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      return 0;
+    }
+    return v;
+  });
+  return c > 0 ? c : 152;
+}
+
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Validates a shape and fills Dims.  need_n64: n and n_cap multiples of 64 (the

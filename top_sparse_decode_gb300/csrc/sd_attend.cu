@@ -3,7 +3,9 @@
 // with the denominator index fixed as on that page) and 2.5 (page size 1: the
 // selected rows are read in place, by index, 256 contiguous bytes each).
 //
-// Split-n: a CTA handles chunks of kAtChunk selected tokens of one (sequence, KV
+// Many long rows (a batch of sequences) go to the streaming kernel
+// (sd_attend_stream.cu), which keeps every SM's share of the rows in flight from HBM.
+// Otherwise, split-n: a CTA handles chunks of kAtChunk selected tokens of one (sequence, KV
 // head) for all G query heads of the group, so every K/V row is read once per
 // group.  Each row is one thread-block cluster of kAtCS CTAs: CTA r takes chunks
 // r, r + kAtCS, ... and keeps a running (m, l, o~) over them; then every CTA merges
@@ -289,6 +291,13 @@ static int attend_t(const Dims& s, const uint16_t* q, const uint16_t* K, const u
                     int64_t max_count, float scale, float* out, float* lse, void* ws,
                     cudaStream_t st) {
   const int64_t rows = (int64_t)s.B * s.Hkv;
+  const int nch = (int)attend_chunks(max_count);
+  if (!fallback_forced() && nch > 0) {  // many long rows: the streaming kernel
+    AttWs w = carve_att(ws, rows, nch, G);
+    int rc = launch_attend_stream(s, q, K, V, idx, idx_stride, count, max_count, scale, out, lse,
+                                  w.ticket, w.part_o, w.part_ml, nch, st);
+    if (rc != 1) return rc;
+  }
   if (attend_cluster_ok<G>()) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kAtCS, (unsigned)rows, 1);
@@ -308,7 +317,6 @@ static int attend_t(const Dims& s, const uint16_t* q, const uint16_t* K, const u
     note_launches(1);
     return check_launch("attend cluster");
   }
-  const int nch = (int)attend_chunks(max_count);
   AttWs w = carve_att(ws, rows, nch, G);
   if (cudaMemsetAsync(w.ticket, 0, sizeof(uint32_t) * rows, st) != cudaSuccess)
     return check_launch("attend: ticket clear");

@@ -60,6 +60,8 @@ inline int per_device_cached(std::atomic<int> (&tab)[kMaxDev], F compute) {
 // setter for testing the report without making a wait run out.
 int scan_error_take(cudaStream_t st, unsigned* word);
 int scan_error_set(unsigned word, cudaStream_t st);
+// The current device's SM count (cached per device; 152 if it cannot be read).
+int device_sm_count();
 
 __host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
@@ -160,6 +162,13 @@ int launch_topk_wmax(const float* scores, const float* wmax, int64_t rows, int64
                      const sd_select& sel, int32_t* idx, int64_t idx_stride, int32_t* count,
                      void* ws, size_t ws_bytes, cudaStream_t st);
 size_t attend_workspace_bytes(const Dims& s, int64_t max_count);
+// The streaming gather-attend (sd_attend_stream.cu) over the split-n workspace's
+// ticket and partial slots; returns 1 (not launched) where it does not apply.
+int launch_attend_stream(const Dims& s, const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                         const int32_t* idx, int64_t idx_stride, const int32_t* count,
+                         int64_t max_count, float scale, float* out, float* lse,
+                         uint32_t* ticket, float* part_o, float2* part_ml, int slots_avail,
+                         cudaStream_t st);
 int launch_gather_attend(const Dims& s, const uint16_t* q, const uint16_t* K, const uint16_t* V,
                          const int32_t* idx, int64_t idx_stride, const int32_t* count,
                          int64_t max_count, float scale, float* out, float* lse, void* ws,

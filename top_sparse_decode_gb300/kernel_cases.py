@@ -209,16 +209,37 @@ def main():
     p = argparse.ArgumentParser()
     p.add_argument("case")
     p.add_argument("--reps", type=int, default=3)
+    p.add_argument("--time", action="store_true",
+                   help="flush L2 before each run and print the mean CUDA-event time of a run")
     a = p.parse_args()
     from top_sparse_decode_gb300 import build
     build.build()
     fn = make_case(a.case)
     torch.cuda.synchronize()
+    if not a.time:
+        for _ in range(a.reps):
+            fn()
+        torch.cuda.synchronize()
+        sd.sd_device_status()
+        print(f"{a.case}: {a.reps} runs ok")
+        return
+    # L2 flush: write one 256 MB buffer, then read another (no dirty lines left behind)
+    wbuf = torch.empty(64 << 20, dtype=torch.float32, device=DEV)
+    rbuf = torch.ones(64 << 20, dtype=torch.float32, device=DEV)
+    sink = torch.empty((), dtype=torch.float32, device=DEV)
+    total = 0.0
     for _ in range(a.reps):
+        wbuf.zero_()
+        sink.copy_(rbuf.max())
+        torch.cuda._sleep(1 << 21)  # ~1 ms on the device: the run is queued before e0 fires
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
         fn()
-    torch.cuda.synchronize()
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
     sd.sd_device_status()
-    print(f"{a.case}: {a.reps} runs ok")
+    print(f"{a.case}: {1e3 * total / a.reps:.1f} us per run (mean of {a.reps}, L2 flushed)")
 
 
 if __name__ == "__main__":
