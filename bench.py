@@ -214,7 +214,7 @@ def scan_traffic(workload: str):
     """DRAM bytes per launch of the scan kernel from the committed ncu summary,
     or None when the kernel source changed since that capture."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "score_planes_tma_longctx-262k.md")
+    prof = os.path.join(ROOT, "profiles", "score_planes_tma_scan56-1m.md")
     csrc = os.path.join(ROOT, "top_sparse_decode_gb300", "csrc")
     src, hdr = os.path.join(csrc, "sd_scan_tma.cu"), os.path.join(csrc, "sd_planes.cuh")
     if not all(os.path.exists(p) for p in (prof, src, hdr)):

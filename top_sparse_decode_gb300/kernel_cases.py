@@ -229,9 +229,9 @@ def main():
     sink = torch.empty((), dtype=torch.float32, device=DEV)
     total = 0.0
     for _ in range(a.reps):
+        torch.cuda._sleep(1 << 21)  # ~1 ms on the device: the run is queued before e0 fires
         wbuf.zero_()
         sink.copy_(rbuf.max())
-        torch.cuda._sleep(1 << 21)  # ~1 ms on the device: the run is queued before e0 fires
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
