@@ -145,3 +145,20 @@ def test_nan_row(sd):
     r = both(sd, K, q, s2, 1, G * Hkv, Hkv, n, 512)
     assert r[2][2] == -1 and r[5][2] == -1
     assert_same(r)
+
+
+def test_fused_against_oracle_262k(sd):
+    """sd_score_topk against the oracle itself: scores within 1e-5 of their L1 mass,
+    index sets equal up to swaps inside that tolerance, at 8 KV heads x 262,144."""
+    import oracle
+    from _helpers import check_float_topk, check_scores
+    B, Hkv, n, k, sink, local = 1, 8, 262144, 512, 4, 64
+    K, q, s2 = seeded(B, 4 * Hkv, Hkv, n)
+    s1, i1, c1, sf, i2, c2 = both(sd, K, q, s2, B, 4 * Hkv, Hkv, n, k, sink, local)
+    rp, rs = oracle.plane_build(K)
+    rplan = oracle.plan(q, s2, Hkv, 0, 56)
+    ref, l1 = oracle.plane_score(rp, rs, rplan, q, with_l1=True)
+    ref, l1 = ref.reshape(B * Hkv, n), l1.reshape(B * Hkv, n)
+    check_scores(sf.view(np.float32), ref, l1, "sd_score_topk scores vs oracle")
+    ri, rc = oracle.topk(ref, k, sink, local, 1, n)
+    check_float_topk(i2, c2, ri, rc, ref, l1, k, sink, local, 1, n)

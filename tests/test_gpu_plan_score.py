@@ -58,3 +58,28 @@ def test_plan_score_equals_plan_then_score(sd, G, Hkv, B, n, ncap, mode, budget)
     assert np.array_equal(host(plan1, np.uint8), host(plan2, np.uint8))
     assert np.array_equal(host(s1, np.uint32), host(s2o, np.uint32))
     assert np.array_equal(host(s1, np.uint32), host(s3, np.uint32))
+
+
+def test_plan_score_against_oracle_262k(sd):
+    """sd_plan_score against the oracle itself (plan bit-exact, scores within 1e-5 of
+    their L1 mass), 8 KV heads x 262,144 tokens at 56 bits."""
+    import oracle
+    from _helpers import check_scores
+    B, Hkv, G, n = 1, 8, 4, 262144
+    cfg = synth.config(4, B=B, Hq=G * Hkv, Hkv=Hkv, n=n)
+    inp = synth.make_inputs(cfg, with_v=False)
+    shp = sd.make_shape(B, G * Hkv, Hkv, n)
+    planes = empty((B, Hkv, 128, 4, n // 32), np.uint32)
+    scales = empty((B, Hkv, 128, n // 64), np.uint16)
+    sd.sd_build_index(sd.SD_IDX_PLANES, shp, dev(inp.K), None, planes, scales)
+    plan = empty((B, Hkv, 128), np.uint8)
+    scores = empty((B * Hkv, n), np.float32)
+    sd.sd_plan_score(shp, planes, scales, dev(inp.q), dev(inp.sigma2), sd.SD_PLAN_WATERFILL, 56,
+                     plan, scores)
+    torch.cuda.synchronize()
+    rp, rs = oracle.plane_build(inp.K)
+    rplan = oracle.plan(inp.q, inp.sigma2, Hkv, 0, 56)
+    assert np.array_equal(host(plan, np.uint8), rplan)
+    ref, l1 = oracle.plane_score(rp, rs, rplan, inp.q, with_l1=True)
+    check_scores(host(scores, np.float32), ref.reshape(B * Hkv, n), l1.reshape(B * Hkv, n),
+                 "sd_plan_score vs oracle")
