@@ -24,6 +24,10 @@ the cases fix those.  Cases:
   resident_gather  admitted blocks from pinned host K/V into the resident pool
   offload       planned-prefix gather from pinned host planes, 8 x 1M tokens
   merge         sequence-shard top-k merge, 16 shards x 512 candidates, 64 rows
+  topk_wmax     top-512 of 8 rows of 1M random scores through their 32-token word
+                maxima (sd_topk_wmax), as in the long-context step
+  attend_1m     gather-attend of 8 rows x 512 selected tokens (sd_gather_attend), the
+                long-context step's shape; K/V of 131,072 tokens
 """
 from __future__ import annotations
 
@@ -194,6 +198,32 @@ def make_case(name: str):
         hs = idx["scales"].cpu().pin_memory()
         dp, ds = torch.empty_like(idx["planes"]), torch.empty_like(idx["scales"])
         return lambda: sd.sd_offload_gather(shp, hp, hs, plan, dp, ds)
+    if name == "topk_wmax":  # the long-context step's top-512 from scores and word maxima
+        Hkv, n, k = 8, 1 << 20, 512
+        scores = torch.randn((Hkv, n), device=DEV, generator=gen)
+        wmax = scores.view(Hkv, n // 32, 32).amax(dim=2).contiguous()
+        sel = sd.make_select(k)
+        stride = k
+        idx = torch.empty((Hkv, stride), dtype=torch.int32, device=DEV)
+        cnt = torch.empty((Hkv,), dtype=torch.int32, device=DEV)
+        ws = torch.empty(max(sd.sd_topk_workspace_size(Hkv, n, sel), 256), dtype=torch.uint8,
+                         device=DEV)
+        return lambda: sd.sd_topk_wmax(scores, wmax, Hkv, n, sel, idx, stride, cnt, ws)
+    if name == "attend_1m":  # the long-context step's gather-attend: 8 rows of 512 tokens
+        Hkv, G, n, c = 8, 4, 1 << 17, 512
+        K = _bf16((1, Hkv, n, 128), gen)
+        V = _bf16((1, Hkv, n, 128), gen)
+        q = _bf16((1, Hkv * G, 128), gen)
+        idx = torch.sort(torch.rand((Hkv, n), device=DEV, generator=gen).argsort(dim=1)[:, :c],
+                         dim=1).values.to(torch.int32).contiguous()
+        cnt = torch.full((Hkv,), c, dtype=torch.int32, device=DEV)
+        shp = sd.make_shape(1, Hkv * G, Hkv, n)
+        ws = torch.empty(max(sd.sd_gather_attend_workspace_size(shp, c), 256), dtype=torch.uint8,
+                         device=DEV)
+        out = torch.empty((1, Hkv * G, 128), dtype=torch.float32, device=DEV)
+        lse = torch.empty((1, Hkv * G), dtype=torch.float32, device=DEV)
+        return lambda: sd.sd_gather_attend(shp, q, K, V, idx, c, cnt, c, 1 / math.sqrt(128), out,
+                                           lse, ws)
     if name == "merge":
         S, rows, k = 16, 64, 512
         cs = torch.randn((S, rows, k), device=DEV, generator=gen)
@@ -210,7 +240,8 @@ def main():
     p.add_argument("case")
     p.add_argument("--reps", type=int, default=3)
     p.add_argument("--time", action="store_true",
-                   help="flush L2 before each run and print the mean CUDA-event time of a run")
+                   help="replay the run as a CUDA graph after an L2 flush and print the mean "
+                        "CUDA-event time of a replay")
     a = p.parse_args()
     from top_sparse_decode_gb300 import build
     build.build()
@@ -223,18 +254,30 @@ def main():
         sd.sd_device_status()
         print(f"{a.case}: {a.reps} runs ok")
         return
-    # L2 flush: write one 256 MB buffer, then read another (no dirty lines left behind)
+    # the run as a CUDA graph (host launch cost off the device's timeline), each replay
+    # after an L2 flush (write one 256 MB buffer, then read another: no dirty lines)
+    # and a ~50 us device-side spin, so the replay is queued before e0 fires
     wbuf = torch.empty(64 << 20, dtype=torch.float32, device=DEV)
     rbuf = torch.ones(64 << 20, dtype=torch.float32, device=DEV)
     sink = torch.empty((), dtype=torch.float32, device=DEV)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        fn()  # warm: attributes and caches set outside the capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            fn()
+    torch.cuda.current_stream().wait_stream(cap)
+    torch.cuda.synchronize()
     total = 0.0
     for _ in range(a.reps):
-        torch.cuda._sleep(1 << 21)  # ~1 ms on the device: the run is queued before e0 fires
         wbuf.zero_()
         sink.copy_(rbuf.max())
+        torch.cuda._sleep(100000)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        fn()
+        graph.replay()
         e1.record()
         torch.cuda.synchronize()
         total += e0.elapsed_time(e1)
