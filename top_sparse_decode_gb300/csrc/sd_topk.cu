@@ -1678,6 +1678,70 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
+// The exact path of the word-maxima selection (CTA 0 alone, rare: fewer than k
+// candidates, a candidate buffer overflow): kept out of line so that the common
+// path's code stays small.
+__device__ __noinline__ void wc_exact(WcSmem& S, const float* __restrict__ srow,
+                                      const float* __restrict__ wrow, const Geo& g,
+                                      int32_t* __restrict__ idx_row, int32_t* __restrict__ count_row,
+                                      int w0, int W, int64_t n) {
+  constexpr int NT = kWcThreads;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lead = g.lead, tail = g.tail, k = g.k;
+  const bool cut0 = (lead & 31) != 0, cut1 = (tail & 31) != 0;
+  // ---- the exact path (CTA 0 alone): the k largest words, then their units ----
+  // word keys from wmax, the cut words' competing maxima recomputed
+  uint32_t* hist = S.pwh;
+  uint32_t* sel = S.pwh + 2048;
+  uint32_t* scratch = S.pwh + 3072;
+  if (warp < 2) {
+    const int i = warp == 0 ? 0 : W - 1;
+    const int u = (w0 + i) * 32 + lane;
+    float m = u >= lead && u < tail ? __ldg(srow + u) : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) S.out[2 + warp] = key_of_f32(m);
+  }
+  if (tid == 0) { S.nlist = 0; S.nsel = 0; }
+  __syncthreads();
+  const uint32_t kc0 = S.out[2], kc1 = S.out[3];
+  const int M = g.M;
+  const int kw = min(k, W);
+  const int bW = bits_of((uint32_t)(W - 1));
+  const int bI = bits_of((uint32_t)(M - 1));
+  auto wkey = [&](int i) {
+    const uint32_t key = (i == 0 && cut0) ? kc0
+                       : (i == W - 1 && cut1) ? kc1 : key_of_f32(__ldg(wrow + i));
+    return ((uint64_t)key << bW) | (uint64_t)(W - 1 - i);
+  };
+  uint64_t Tw = 0;
+  if (W > k)
+    Tw = radix_select_fn<NT>(W, [&](int i, uint64_t& x) { x = wkey(i); return true; },
+                             (uint32_t)k, 32 + bW, hist, scratch, S.out);
+  for (int i = tid; i < W; i += NT)
+    if (wkey(i) >= Tw) S.lw[atomicAdd(&S.nlist, 1u)] = (uint32_t)i;
+  __syncthreads();
+  auto unit_of = [&](int e) { return (w0 + (int)S.lw[e >> 5]) * 32 + (e & 31); };
+  auto get = [&](int e, uint64_t& x) {
+    const int u = unit_of(e);
+    if (u < lead || u >= tail) return false;
+    x = ((uint64_t)key_of_f32(__ldg(srow + u)) << bI) |
+        (uint64_t)((uint32_t)(M - 1) - (uint32_t)(u - lead));
+    return true;
+  };
+  const uint64_t Tu = radix_select_fn<NT>(kw * 32, get, (uint32_t)k, 32 + bI, hist, scratch,
+                                          S.out);
+  for (int e = tid; e < kw * 32; e += NT) {
+    uint64_t x;
+    if (get(e, x) && x >= Tu) sel[atomicAdd(&S.nsel, 1u)] = (uint32_t)unit_of(e);
+  }
+  __syncthreads();
+  const int nsel = (int)S.nsel;
+  uint32_t* tmp = reinterpret_cast<uint32_t*>(S.gb);
+  sort_units<NT>(sel, nsel, bits_of((uint32_t)(n - 1)), tmp, tmp + 2048);
+  write_units<NT>(g, sel, nsel, idx_row, count_row);
+}
+
 // The selection of one row by its cluster (every thread of every CTA runs it; CTAs
 // leave it at different points: mode 0 after writing their share, mode 2 at once,
 // mode 1 all but CTA 0 at once and CTA 0 after the exact path).
@@ -1917,57 +1981,7 @@ __device__ __forceinline__ void wc_select(WcSmem& S, const float* __restrict__ s
   }
   if (rank != 0) return;
 
-  // ---- the exact path (CTA 0 alone): the k largest words, then their units ----
-  // word keys from wmax, the cut words' competing maxima recomputed
-  uint32_t* hist = S.pwh;
-  uint32_t* sel = S.pwh + 2048;
-  uint32_t* scratch = S.pwh + 3072;
-  if (warp < 2) {
-    const int i = warp == 0 ? 0 : W - 1;
-    const int u = (w0 + i) * 32 + lane;
-    float m = u >= lead && u < tail ? __ldg(srow + u) : -INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) S.out[2 + warp] = key_of_f32(m);
-  }
-  if (tid == 0) { S.nlist = 0; S.nsel = 0; }
-  __syncthreads();
-  const uint32_t kc0 = S.out[2], kc1 = S.out[3];
-  const int M = g.M;
-  const int kw = min(k, W);
-  const int bW = bits_of((uint32_t)(W - 1));
-  const int bI = bits_of((uint32_t)(M - 1));
-  auto wkey = [&](int i) {
-    const uint32_t key = (i == 0 && cut0) ? kc0
-                       : (i == W - 1 && cut1) ? kc1 : key_of_f32(__ldg(wrow + i));
-    return ((uint64_t)key << bW) | (uint64_t)(W - 1 - i);
-  };
-  uint64_t Tw = 0;
-  if (W > k)
-    Tw = radix_select_fn<NT>(W, [&](int i, uint64_t& x) { x = wkey(i); return true; },
-                             (uint32_t)k, 32 + bW, hist, scratch, S.out);
-  for (int i = tid; i < W; i += NT)
-    if (wkey(i) >= Tw) S.lw[atomicAdd(&S.nlist, 1u)] = (uint32_t)i;
-  __syncthreads();
-  auto unit_of = [&](int e) { return (w0 + (int)S.lw[e >> 5]) * 32 + (e & 31); };
-  auto get = [&](int e, uint64_t& x) {
-    const int u = unit_of(e);
-    if (u < lead || u >= tail) return false;
-    x = ((uint64_t)key_of_f32(__ldg(srow + u)) << bI) |
-        (uint64_t)((uint32_t)(M - 1) - (uint32_t)(u - lead));
-    return true;
-  };
-  const uint64_t Tu = radix_select_fn<NT>(kw * 32, get, (uint32_t)k, 32 + bI, hist, scratch,
-                                          S.out);
-  for (int e = tid; e < kw * 32; e += NT) {
-    uint64_t x;
-    if (get(e, x) && x >= Tu) sel[atomicAdd(&S.nsel, 1u)] = (uint32_t)unit_of(e);
-  }
-  __syncthreads();
-  const int nsel = (int)S.nsel;
-  uint32_t* tmp = reinterpret_cast<uint32_t*>(S.gb);
-  sort_units<NT>(sel, nsel, bits_of((uint32_t)(n - 1)), tmp, tmp + 2048);
-  write_units<NT>(g, sel, nsel, idx_row, count + row);
+  wc_exact(S, srow, wrow, g, idx_row, count + row, w0, W, n);
 }
 
 
