@@ -8,8 +8,8 @@ The GPU test calls it through the C ABI twice in a row, on different problems,
 and checks each result against sd_gather_attend with a caller workspace, within
 the attention tolerance of the other parity tests: once as the GB300 runs it (the
 16-CTA cluster kernel, which needs no scratch) and once with the split-n kernel
-forced (sd_set_fallback_paths), so that both calls really write, and the second
-reuses, the shared array.  This file is collected last so that a run stopping at
+forced (sd_set_fallback_paths), and once on 256 rows, which take the streaming
+kernel, so that both calls really write, and the second reuses, the shared array.  This file is collected last so that a run stopping at
 the first failure has already run everything else; it also passes on its own in
 a fresh process."""
 import ctypes
@@ -45,21 +45,29 @@ def test_noalloc_rejects_oversized_requests_before_any_cuda_call(sd):
     assert "more than" in sd.sd_last_error()
 
 
+# (G, Hkv, B, n, max_count) of the two calls: a few long rows (the cluster kernel, or
+# the split-n kernel when forced), or 256 rows of 320 tokens (the streaming kernel,
+# whose ticket and partials then live in the static array)
+FEW_ROWS = [(4, 8, 2, 6000, 1152), (8, 3, 2, 3000, 700)]
+MANY_ROWS = [(1, 8, 32, 4096, 320), (2, 8, 32, 4096, 320)]
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("split_n", [False, True])
-def test_noalloc_matches_workspace_entry_point_twice(sd, split_n):
+@pytest.mark.parametrize("split_n,problems", [(False, FEW_ROWS), (True, FEW_ROWS),
+                                              (False, MANY_ROWS)])
+def test_noalloc_matches_workspace_entry_point_twice(sd, split_n, problems):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     prev = sd.sd_set_fallback_paths(split_n)
     try:
-        _two_calls(sd)
+        _two_calls(sd, problems)
     finally:
         sd.sd_set_fallback_paths(prev)
 
 
-def _two_calls(sd):
-    for trial, (G, Hkv, n, max_count) in enumerate([(4, 8, 6000, 1152), (8, 3, 3000, 700)]):
-        cfg = synth.config(1, B=2, Hq=G * Hkv, Hkv=Hkv, n=n)
+def _two_calls(sd, problems):
+    for trial, (G, Hkv, B, n, max_count) in enumerate(problems):
+        cfg = synth.config(1, B=B, Hq=G * Hkv, Hkv=Hkv, n=n)
         inp = synth.make_inputs(cfg)
         rows = cfg.B * cfg.Hkv
         counts = np.linspace(1, max_count, rows).astype(np.int64)
