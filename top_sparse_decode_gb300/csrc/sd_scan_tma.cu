@@ -470,7 +470,15 @@ int launch_score_planes_tma(const Dims& s, const uint32_t* planes, const uint16_
                             cudaStream_t st) {
   const int upr = (int)((s.n + kPtUnit - 1) / kPtUnit);  // units per row (n < 2^31)
   const int64_t total = (int64_t)upr * s.B * s.Hkv;
-  const int grid = (int)imin64(total, (int64_t)sms * kPtCtasPerSm);
+  int grid = (int)imin64(total, (int64_t)sms * kPtCtasPerSm);
+  // whole CTAs per row where that gives up at most a tenth of the grid: then no range
+  // meets two rows, whose second row's tables a CTA would build in mid-range while
+  // its compute warps wait
+  const int64_t rows = (int64_t)s.B * s.Hkv;
+  if (rows < grid) {
+    const int64_t per = grid / rows;
+    if (per * rows * 10 >= (int64_t)grid * 9 && per <= upr) grid = (int)(per * rows);
+  }
   for (int b = 0; b < grid; ++b) {  // rows met by each CTA's range
     const int64_t u0 = (int64_t)b * total / grid, u1 = (int64_t)(b + 1) * total / grid;
     if (u1 > u0 && (u1 - 1) / upr - u0 / upr + 1 > kPtRows) return 1;
