@@ -336,8 +336,13 @@ int sd_score_topk(const sd_shape* shape, const void* planes, const void* scales,
  *   q bf16 [B][hq][d]; K, V bf16 [B][hkv][n_cap][d]; idx int32 [B*hkv][idx_stride]
  *   (token indices < n, any order); count int32 [B*hkv] (<= max_count);
  *   out fp32 [B][hq][d]; lse fp32 [B][hq] or NULL.  An empty set gives out = 0,
- *   lse = -inf.  The set is split across CTAs and merged by an online-softmax
- *   combine.  Workspace: sd_gather_attend_workspace_size() bytes (device).
+ *   lse = -inf.  The set is split across CTAs (or warps) and merged by an
+ *   online-softmax combine: a few rows go to one thread-block cluster per row;
+ *   many long rows (at least 4 groups of 16 selected tokens per warp of a full
+ *   grid, with q 16-byte aligned) go to a persistent kernel whose warps each take
+ *   an equal range of 16-token groups and run QK^T and PV on the tensor cores,
+ *   their partials combined through the workspace.  Workspace:
+ *   sd_gather_attend_workspace_size() bytes (device).
  */
 size_t sd_gather_attend_workspace_size(const sd_shape* shape, int64_t max_count);
 int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const void* V,
@@ -354,9 +359,9 @@ int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const 
  * (The pages have no counterpart: this is a property of the library, not of the
  * method.)
  *   Same arguments, layouts and results as sd_gather_attend, without the
- *   workspace: when the split-n kernel runs, its partials live in a 4 MiB
- *   file-scope device array that every GPU loading libsd holds until the process
- *   exits.  The limit is applied to every call, whichever kernel then runs:
+ *   workspace: when the split-n or the many-row kernel runs, its ticket and
+ *   partials live in a 4 MiB file-scope device array that every GPU loading libsd
+ *   holds until the process exits.  The limit is applied to every call, whichever kernel then runs:
  *   requests whose partials would need more (sd_gather_attend_workspace_size()
  *   > 4 MiB) are rejected with SD_ERR_UNSUPPORTED before anything is enqueued,
  *   so a call that succeeds on one GPU succeeds on every GPU.  Allocates nothing.
@@ -364,8 +369,8 @@ int sd_gather_attend(const sd_shape* shape, const void* q, const void* K, const 
  *   (cudaGetSymbolAddress, with the device current) and keeps the address for
  *   the process; make that first call before any stream capture.  A device
  *   reset (cudaDeviceReset) invalidates the kept address: do not call this entry
- *   point on a device after resetting it.  On GPUs where the 16-CTA cluster
- *   kernel runs, the array is not used.  When the split-n kernel runs, all calls
+ *   point on a device after resetting it.  When the 16-CTA cluster kernel runs,
+ *   the array is not used.  When another kernel runs, all calls
  *   on a device share the array and it keeps the last call's contents: each such
  *   call first clears the per-row counters that must start at zero (on the
  *   caller's stream; partials are written before they are read), and calls that
