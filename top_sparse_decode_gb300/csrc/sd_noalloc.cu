@@ -4,17 +4,17 @@
 // bypass), real-time loops that must not take allocator locks or let cudaMalloc
 // synchronise the device, and code that runs where cudaMalloc may not be called.
 // This entry point runs the same kernels as sd_gather_attend; when the split-n
-// kernel runs (GPUs where the 16-CTA cluster kernel cannot be co-resident), its
-// partial (m, l, o) results are kept in one file-scope device array instead of a
-// caller workspace.  The cluster kernel needs no scratch and leaves the array
-// alone.
+// kernel (GPUs where the 16-CTA cluster kernel cannot be co-resident) or the
+// many-row streaming kernel runs, its ticket and partial (m, l, o) results are
+// kept in one file-scope device array instead of a caller workspace.  The cluster
+// kernel needs no scratch and leaves the array alone.
 //
 // The array is a module global: every GPU that loads libsd holds its
 // kNoallocScratchBytes until the process exits, and every call on a GPU shares
 // that GPU's copy.  The size limit applies to every call, whichever kernel runs,
 // so that a call accepted on one GPU is accepted on all.  The array keeps the
-// previous call's contents: a call that runs the split-n kernel first clears the
-// per-row counters that must start at zero (with a memset on the caller's
+// previous call's contents: a call that runs either of those kernels first clears
+// the per-row counters that must start at zero (with a memset on the caller's
 // stream), and the kernel writes every partial before it reads it.  Such calls
 // whose work overlaps on the GPU (different streams without ordering, or host
 // threads) race on the array.  The array's device address is looked up once per
