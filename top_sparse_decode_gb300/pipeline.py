@@ -147,8 +147,11 @@ class DecodeStep:
         if self.use_sa:
             sws = sd_select_attend_workspace_size(self.shape, self.sel, c.max_count)
             self.sa_ws = torch.empty(max(sws, 256), dtype=torch.uint8, device=dev)
-        self.out = torch.empty((c.B, c.Hq, c.d), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((c.B, c.Hq), dtype=torch.float32, device=dev)
+        # out and lse in one buffer (out first), so that one copy moves the result
+        nout = c.B * c.Hq * c.d
+        self.result = torch.empty(nout + c.B * c.Hq, dtype=torch.float32, device=dev)
+        self.out = self.result[:nout].view(c.B, c.Hq, c.d)
+        self.lse = self.result[nout:].view(c.B, c.Hq)
 
     # the four stages, separately callable for per-stage timing
     def stage_prep(self, q, stream=None):
