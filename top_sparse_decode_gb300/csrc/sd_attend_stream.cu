@@ -268,9 +268,10 @@ struct AsState {
   float mref, l;  // reference max (log2 units) of the lane's head gid; its partial sum
 };
 
-// One slot of the warp's two-deep pipeline: the K and V fragments of the group at
-// `pos` (mask: its positions holding a token), and the indices of the group two
-// ahead (`npos`, this lane's token `ntok`), whose rows the slot loads next.
+// The warp's groups in flight: the K and V fragments of the group at `pos` (mask:
+// its positions holding a token), and the positions and indices of the three groups
+// after it -- the next one's rows load into these registers as they free up, the
+// one three ahead is prefetched into L2.
 struct AsSlot {
   uint4 k[2][4], v[4][2];
   AsPos pos, npos, ppos, fpos;  // this group and the three after it
