@@ -563,6 +563,18 @@ int sd_set_fallback_paths(int on);
 int sd_debug_set_device_error(void* stream);
 
 /*
+ * sd_copy -- copy `bytes` bytes from src to dst with a kernel on `stream`, where
+ * each pointer is device memory or pinned host memory that the device reaches
+ * at the same address (unified addressing: cudaHostAlloc / pin_memory buffers).
+ * For a decode step's small inputs and results: inside a CUDA graph a copy
+ * kernel over the pinned memory's mapping finishes sooner than a copy-engine
+ * transfer.  Both pointers 16-byte aligned, bytes a multiple of 16
+ * (SD_ERR_INVALID_ARG otherwise); the ranges must not overlap; bytes = 0 does
+ * nothing.
+ */
+int sd_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * sd_event_wait -- host-side bounded wait on a cudaEvent_t (passed as void*):
  * polls until the event completes or timeout_us microseconds pass
  * (SD_ERR_TIMEOUT).  Lets a caller bound its wait for an offload copy.
@@ -576,7 +588,7 @@ const char* sd_last_error(void);
  * SD_IDX_LANDMARK, sd_delta_select and sd_resident_gather to 100; 102 adds
  * sd_device_status, sd_set_fallback_paths and sd_debug_set_device_error; 103 adds
  * SD_PLAN_SPLIT, sd_shard_candidates, sd_topk_merge, sd_shard_select and
- * sd_attend_combine. */
+ * sd_attend_combine; 104 adds sd_copy. */
 int sd_version(void);
 
 /*

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(sd):
     assert sorted(_abi.SIGNATURES) == header_functions()
     for name in header_functions():
         assert callable(getattr(sd, name)), name
-    assert sd.sd_version() == 103  # 1.03: split plan, sequence shards
+    assert sd.sd_version() == 104  # 1.04: sd_copy
 
 
 def test_shape_checks(sd):
@@ -218,3 +218,12 @@ def test_fallback_switch_is_off_by_default_and_returns_previous(sd):
     assert sd.sd_set_fallback_paths(True) is False
     assert sd.sd_set_fallback_paths(False) is True
     assert sd.sd_set_fallback_paths(False) is False
+
+
+def test_copy_argument_checks(sd):
+    lib = sd.lib()
+    A = 1 << 20  # aligned placeholder addresses; never dereferenced
+    assert lib.sd_copy(A, A + 64, 0, None) == sd.SD_OK  # nothing to do
+    for dst, src, n in [(None, A, 16), (A, None, 16), (A + 8, A, 16), (A, A + 4, 16), (A, A, 24)]:
+        assert lib.sd_copy(dst, src, n, None) == sd.SD_ERR_INVALID_ARG
+        assert "sd_copy" in sd.sd_last_error()

@@ -32,7 +32,7 @@ __all__ = [
     "sd_event_wait", "sd_last_error", "sd_version", "sd_launch_count", "sd_device_status",
     "sd_set_fallback_paths", "sd_debug_set_device_error", "sd_shard_candidates",
     "sd_topk_merge", "sd_shard_select", "sd_attend_combine",
-    "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax",
+    "sd_score_topk_workspace_size", "sd_score_topk", "sd_plan_score", "sd_topk_wmax", "sd_copy",
     "sd_select_attend_workspace_size", "sd_select_attend", "sd_hamming_topk_workspace_size",
     "sd_hamming_topk",
 ]
@@ -314,6 +314,14 @@ def sd_set_fallback_paths(on: bool) -> bool:
 def sd_debug_set_device_error(stream=None) -> None:
     """Testing: raise the device error word that sd_device_status reports."""
     _check(lib().sd_debug_set_device_error(_stream(stream)), "sd_debug_set_device_error")
+
+
+def sd_copy(dst, src, nbytes: Optional[int] = None, stream=None) -> None:
+    """Kernel copy of nbytes (default: all of src) between device memory and pinned
+    host memory (tensors or raw addresses)."""
+    if nbytes is None:
+        nbytes = src.numel() * src.element_size()
+    _check(lib().sd_copy(_ptr(dst), _ptr(src), int(nbytes), _stream(stream)), "sd_copy")
 
 
 def sd_event_wait(event, timeout_us: int) -> None:

@@ -80,6 +80,7 @@ SIGNATURES = {
     "sd_set_fallback_paths": (_i, [_i]),
     "sd_debug_set_device_error": (_i, [_p]),
     "sd_event_wait": (_i, [_p, _i64]),
+    "sd_copy": (_i, [_p, _p, _sz, _p]),
     "sd_last_error": (ctypes.c_char_p, []),
     "sd_version": (_i, []),
     "sd_launch_count": (_i64, []),

@@ -121,7 +121,7 @@ using namespace sd;
 
 extern "C" {
 
-int sd_version(void) { return 103; }
+int sd_version(void) { return 104; }
 
 int64_t sd_launch_count(void) { return (int64_t)launch_total(); }
 
@@ -676,6 +676,37 @@ int sd_device_status(void* stream) {
 
 int sd_debug_set_device_error(void* stream) {
   return scan_error_set(1u, (cudaStream_t)stream);
+}
+
+namespace {
+// 16-byte words, grid-strided; several loads in flight per thread.
+__global__ void __launch_bounds__(256) copy16_kernel(uint4* __restrict__ dst,
+                                                     const uint4* __restrict__ src, int64_t n16) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+    dst[i] = a;
+    dst[i + stride] = b;
+    dst[i + 2 * stride] = c;
+    dst[i + 3 * stride] = d;
+  }
+  for (; i < n16; i += stride) dst[i] = src[i];
+}
+}  // namespace
+
+int sd_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return SD_OK;
+  if (!dst || !src) return fail(SD_ERR_INVALID_ARG, "sd_copy: NULL pointer");
+  if (!aligned16(dst) || !aligned16(src) || bytes % 16)
+    return fail(SD_ERR_INVALID_ARG, "sd_copy: pointers must be 16-byte aligned and bytes a "
+                                    "multiple of 16");
+  const int64_t n16 = (int64_t)(bytes / 16);
+  const int64_t blocks = imin64((n16 + 255) / 256, (int64_t)device_sm_count() * 4);
+  copy16_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
+      static_cast<uint4*>(dst), static_cast<const uint4*>(src), n16);
+  note_launches(1);
+  return check_launch("sd_copy");
 }
 
 int sd_event_wait(void* event, int64_t timeout_us) {
