@@ -365,6 +365,65 @@ def test_topk_block_mode_bit_exact(sd):
         assert np.array_equal(gi[r, :gc[r]], ri[r, :rc[r]])
 
 
+# Rows of at most 2048 competing units take the register kernel (one CTA of 4 warps
+# per row, keys in registers, a bitwise search for the k-th largest key, ties that
+# span warps); 2049 takes the shared-memory CTA kernel.
+REG_TOPK_CASES = [
+    # (rows, n_units, kind, levels, k, sink, local)
+    (701, 1024, "f32", 0, 128, 0, 1),   # many rows
+    (5, 2056, "f32ties", 3, 200, 4, 4),  # M = 2048, the largest warp row
+    (3, 2049, "f32", 0, 100, 0, 0),     # M = 2049: the CTA kernel
+    (6, 33, "int", 4, 5, 0, 0),
+    (7, 129, "f32ties", 2, 64, 0, 0),
+    (3, 300, "const", 0, 17, 0, 0),     # every key tied: the lowest units
+    (2, 200, "f32", 0, 1, 3, 3),        # k = 1 beside the windows
+    (2, 150, "f32", 0, 200, 2, 2),      # k >= M: every unit
+    (2, 1, "f32", 0, 1, 0, 0),
+    (9, 600, "int", 1, 250, 1, 1),
+]
+
+
+@pytest.mark.parametrize("rows,n,kind,levels,k,sink,local", REG_TOPK_CASES)
+def test_topk_reg_rows_bit_exact(sd, rows, n, kind, levels, k, sink, local):
+    s = synth.make_scores(2000 + n + k, rows, n, kind, levels)
+    gi, gc = run_topk(sd, s, k, sink, local)
+    ri, rc = oracle.topk(s, k, sink, local)
+    for r in range(rows):
+        assert gc[r] == rc[r], (r, gc[r], rc[r])
+        assert np.array_equal(gi[r, :gc[r]], ri[r, :rc[r]]), r
+
+
+def test_topk_reg_rows_block_mode_last_unit(sd):
+    # no trailing window: the cut last block competes, and is taken in rows 0, 2, 4
+    nblk = 1024
+    s = synth.make_scores(78, 5, nblk, "f32")
+    s[::2, nblk - 1] = 100.0
+    n_tokens = nblk * 16 - 5
+    gi, gc = run_topk(sd, s, 128, 0, 0, block=16, n_tokens=n_tokens)
+    ri, rc = oracle.topk(s, 128, 0, 0, block=16, n_tokens=n_tokens)
+    assert np.array_equal(gc, rc) and gc[0] == 128 * 16 - 5 and gc[1] == 128 * 16
+    for r in range(5):
+        assert np.array_equal(gi[r, :gc[r]], ri[r, :rc[r]]), r
+
+
+def test_topk_reg_rows_signed_zeros_infinities_nan(sd):
+    rng = np.random.default_rng(11)
+    s = rng.standard_normal((8, 1000)).astype(np.float32)
+    s[0] = np.where(rng.random(1000) < 0.5, np.float32(-0.0), np.float32(0.0))
+    s[1, rng.choice(1000, 30, replace=False)] = np.inf
+    s[1, rng.choice(1000, 30, replace=False)] = -np.inf
+    s[2] = -np.inf
+    s[3, 500] = np.nan   # a competing NaN: the row reports -1
+    s[4, 1] = np.nan     # inside the leading window: ignored
+    s[5, 998] = np.nan   # inside the trailing window: ignored
+    gi, gc = run_topk(sd, s, 40, 2, 3)
+    ri, rc = oracle.topk(np.where(np.isnan(s), np.float32(0), s), 40, 2, 3)
+    assert gc[3] == -1
+    for r in (0, 1, 2, 4, 5, 6, 7):
+        assert gc[r] == rc[r], (r, gc[r], rc[r])
+        assert np.array_equal(gi[r, :gc[r]], ri[r, :rc[r]]), r
+
+
 def test_topk_nan_row(sd):
     s = synth.make_scores(5, 3, 9000, "f32")
     s[1, 4444] = np.nan

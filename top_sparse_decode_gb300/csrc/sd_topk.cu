@@ -9,7 +9,8 @@
 // (key = order-preserving 32-bit image of the score, kmin the candidates' minimum,
 // M = tail - lead candidates, bI = bits of M - 1), so "top-k by C" is exactly the
 // required order with no ties left, and a radix select over C needs no tie pass.
-// Rows of up to kSmallRow units are selected by one CTA in shared memory.
+// Rows of up to kSmallRow units are selected by one CTA in shared memory, or in
+// registers when at most kRegRow of their units compete.
 // Longer rows take three kernels:
 //   1. sample: one CTA per row reads an evenly spaced sample of up to 16K keys
 //      and takes T_est = its r-th largest key, r = mu + 5 sqrt(mu) + 2 with
@@ -276,30 +277,37 @@ __device__ uint64_t radix_threshold(const KT* C, int c, uint32_t need, uint64_t 
 }
 
 // Writes the final ascending unit list (lead units, the sorted selected units,
-// tail units) expanded to tokens, and the count.
-template <int NT>
-__device__ void write_units(const Geo& g, const uint32_t* sel, int nsel, int32_t* idx_row,
-                            int32_t* count_row) {
+// tail units) expanded to tokens, and the count: thread t of nt threads.
+__device__ void write_units_by(const Geo& g, const uint32_t* sel, int nsel, int32_t* idx_row,
+                               int32_t* count_row, int t, int nt) {
   const int ntail = (int)(g.n_units - g.tail);
   const int nunits = g.lead + nsel + ntail;
   const int blk = g.block;
   const int total = nunits * blk;  // <= idx_stride < 2^31
   const int ntok = (int)g.n_tokens;
-  for (int p = threadIdx.x; p < total; p += NT) {
-    const int ui = blk == 1 ? p : p / blk;
+  const int sh = (blk & (blk - 1)) == 0 ? __ffs(blk) - 1 : -1;  // power-of-two blocks shift
+#pragma unroll 4
+  for (int p = t; p < total; p += nt) {
+    const int ui = sh >= 0 ? p >> sh : p / blk;
     const int off = p - ui * blk;
     const int u = ui < g.lead ? ui : (ui < g.lead + nsel ? (int)sel[ui - g.lead]
                                                         : g.tail + (ui - g.lead - nsel));
     const int tok = u * blk + off;
     if (tok < ntok) idx_row[p] = tok;
   }
-  if (threadIdx.x == 0) {
+  if (t == 0) {
     const bool last_in = ntail > 0 || (nsel > 0 && (int64_t)sel[nsel - 1] == g.n_units - 1) ||
                          (nsel == 0 && ntail == 0 && g.lead == g.n_units);
     int64_t cnt = total;
     if (last_in) cnt -= (g.n_units * g.block - g.n_tokens);
     *count_row = (int32_t)cnt;
   }
+}
+
+template <int NT>
+__device__ void write_units(const Geo& g, const uint32_t* sel, int nsel, int32_t* idx_row,
+                            int32_t* count_row) {
+  write_units_by(g, sel, nsel, idx_row, count_row, threadIdx.x, NT);
 }
 
 // Shared memory of a finishing CTA.
@@ -370,6 +378,195 @@ topk_small_kernel(const void* __restrict__ scores, Geo g, int32_t* __restrict__ 
   sort_units<kFinThreads>(S.sel, nsel, bits_of((uint32_t)(g.n_units - 1)), S.hist,
                           reinterpret_cast<uint32_t*>(S.C));
   write_units<kFinThreads>(g, S.sel, nsel, idx_row, count + row);
+}
+
+// --------------------------------------------------------------------------------------
+// Rows of at most kRegRow candidates: one CTA of 4 warps per row, keys in registers.
+// --------------------------------------------------------------------------------------
+// Warp w holds candidates [w * 32 JW, (w + 1) * 32 JW); candidate i = w * 32 JW +
+// j * 32 + lane sits in key[j] of that lane (coalesced loads).  The k-th largest
+// key T is found bit by bit from the most significant bit in which the row's keys
+// differ: T | bit is kept while at least k keys are >= it.  Each lane counts with
+// borrow arithmetic (no compares, no predicates), each warp sums its lanes, and the
+// four warp sums meet in a double-buffered shared slot behind one barrier per bit.
+// Every key > T is taken, and of the keys == T the lowest-indexed k - #(key > T):
+// the composite order of the other kernels, with no 64-bit keys.  One exchange of
+// per-warp counts then gives each warp the place of its first taken unit and its
+// first tie's rank; walking j upward, ballots place each taken unit, so the units
+// come out ascending with no sort, and the lane that takes a unit writes its tokens.
+// A single warp per row is latency-bound here (about one instruction per three
+// cycles with no other warp to switch to), hence four.
+constexpr int kRegRow = 2048;
+constexpr int kRegWarps = 4;
+
+// 1 if a < b (unsigned), from the borrow of a - b: no compare, no predicate
+__device__ __forceinline__ uint32_t borrow_of(uint32_t a, uint32_t b) {
+  return ((~a & b) | (~(a ^ b) & (a - b))) >> 31;
+}
+
+// Tokens of unit u at output position pos (units are blk tokens; the last may be
+// cut at ntok): 16-byte stores when the row allows them.
+__device__ __forceinline__ void put_unit(int32_t* idx_row, int pos, int u, int blk, int ntok,
+                                         bool vec) {
+  const int t0 = u * blk;
+  int32_t* dst = idx_row + (int64_t)pos * blk;
+  if (vec && t0 + blk <= ntok) {
+    for (int o = 0; o < blk; o += 4)
+      *reinterpret_cast<int4*>(dst + o) = make_int4(t0 + o, t0 + o + 1, t0 + o + 2, t0 + o + 3);
+  } else {
+    for (int o = 0; o < blk && t0 + o < ntok; ++o) dst[o] = t0 + o;
+  }
+}
+
+template <bool F32, int JW>
+__global__ void __launch_bounds__(kRegWarps * 32)
+topk_reg_kernel(const void* __restrict__ scores, Geo g, int32_t* __restrict__ idx,
+                int64_t idx_stride, int32_t* __restrict__ count) {
+  __shared__ uint32_t xch[2][kRegWarps];            // per-bit warp sums, double-buffered
+  __shared__ uint32_t mm[2][kRegWarps];             // warp minima and maxima
+  __shared__ uint32_t gt_tie[2][kRegWarps];         // warp counts of key > T and key == T
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t row = blockIdx.x;
+  const int M = g.M;
+  const int u0 = w * 32 * JW;  // this warp's first candidate
+  const int64_t base = row * g.n_units + g.lead;
+  uint32_t key[JW];
+  bool nan = false;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0;
+  if (M > 0) {
+    // addresses clamped into the row, so no load waits on a branch: all in flight
+#pragma unroll
+    for (int j = 0; j < JW; ++j) {
+      const int i = u0 + j * 32 + lane;
+      const bool valid = i < M;
+      bool nj = false;
+      const uint32_t kk = load_key<F32>(scores, base + min(i, M - 1), nj);
+      nan = nan || (nj && valid);
+      key[j] = valid ? kk : 0u;
+      mn = valid ? min(mn, kk) : mn;
+      mx = valid ? max(mx, kk) : mx;
+    }
+  }
+  if (__syncthreads_or(nan)) {
+    if (threadIdx.x == 0) count[row] = -1;
+    return;
+  }
+  const bool all = M <= g.k;  // every candidate is taken
+  int ties = 0, nsel = 0;     // ties and taken units before this warp's first candidate
+  uint32_t T = 0;
+  int need = 0;               // keys == T taken, lowest index first
+  if (!all) {                 // M >= 1 here
+    mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if (lane == 0) { mm[0][w] = mn; mm[1][w] = mx; }
+    __syncthreads();
+#pragma unroll
+    for (int v = 0; v < kRegWarps; ++v) { mn = min(mn, mm[0][v]); mx = max(mx, mm[1][v]); }
+    if (mn == mx) {
+      T = mn;
+    } else {
+      // every key shares the bits of mn above hb, so the k-th largest does too;
+      // T | bit >= 1 counts the zero padding of i >= M as below it
+      const int hb = 31 - __clz(mn ^ mx);
+      T = hb == 31 ? 0u : mn & ~((2u << hb) - 1u);
+      const int max_below = kRegWarps * 32 * JW - g.k;  // keep T | bit while #(key < it) <= this
+      for (int b = hb; b >= 0; --b) {
+        const uint32_t c = T | (1u << b);
+        uint32_t n_lt[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < JW; ++j) n_lt[j & 1] += borrow_of(key[j], c);
+        const uint32_t n = __reduce_add_sync(0xFFFFFFFFu, n_lt[0] + n_lt[1]);
+        if (lane == 0) xch[b & 1][w] = n;
+        __syncthreads();  // a slot is rewritten two bits later, after another barrier
+        uint32_t tot = 0;
+#pragma unroll
+        for (int v = 0; v < kRegWarps; ++v) tot += xch[b & 1][v];
+        if ((int)tot <= max_below) T = c;
+      }
+    }
+    uint32_t n_gt = 0, n_tie = 0;
+#pragma unroll
+    for (int j = 0; j < JW; ++j) {
+      n_gt += key[j] > T ? 1u : 0u;
+      n_tie += (key[j] == T && u0 + j * 32 + lane < M) ? 1u : 0u;
+    }
+    n_gt = __reduce_add_sync(0xFFFFFFFFu, n_gt);
+    n_tie = __reduce_add_sync(0xFFFFFFFFu, n_tie);
+    if (lane == 0) { gt_tie[0][w] = n_gt; gt_tie[1][w] = n_tie; }
+    __syncthreads();
+    int gt_all = 0;
+#pragma unroll
+    for (int v = 0; v < kRegWarps; ++v) gt_all += (int)gt_tie[0][v];
+    need = g.k - gt_all;
+    for (int v = 0; v < w; ++v) {
+      const int tv = (int)gt_tie[1][v];
+      nsel += (int)gt_tie[0][v] + max(0, min(tv, need - ties));
+      ties += tv;
+    }
+  } else {
+    nsel = min(M, u0);
+  }
+  const int nsel_all = min(M, g.k);
+  int32_t* idx_row = idx + row * idx_stride;
+  const int blk = g.block, ntok = (int)g.n_tokens;
+  const bool vec = (blk & 3) == 0 && (reinterpret_cast<uintptr_t>(idx_row) & 15) == 0;
+  const uint32_t lt = (1u << lane) - 1u;
+  const bool last_cand = g.tail == g.n_units && M > 0;  // the row's last unit competes
+  bool last_taken = false;
+#pragma unroll
+  for (int j = 0; j < JW; ++j) {
+    const int i = u0 + j * 32 + lane;
+    const bool valid = i < M;
+    bool take;
+    if (all) {
+      take = valid;
+    } else {
+      const bool tie = valid && key[j] == T;
+      const uint32_t bt = __ballot_sync(0xFFFFFFFFu, tie);
+      take = valid && (key[j] > T || (tie && ties + __popc(bt & lt) < need));
+      ties += __popc(bt);
+    }
+    const uint32_t bs = __ballot_sync(0xFFFFFFFFu, take);
+    if (take) put_unit(idx_row, g.lead + nsel + __popc(bs & lt), g.lead + i, blk, ntok, vec);
+    if (take && i == M - 1) last_taken = true;
+    nsel += __popc(bs);
+  }
+  // the forced windows: units [0, lead) first, then [tail, n_units) after the taken
+  const int lead_tok = g.lead * blk;
+  for (int p = threadIdx.x; p < lead_tok && p < ntok; p += kRegWarps * 32) idx_row[p] = p;
+  const int ntail = (int)(g.n_units - g.tail);
+  const int tail0 = (g.lead + nsel_all) * blk, tail_tok = ntail * blk;
+  for (int q = threadIdx.x; q < tail_tok && g.tail * blk + q < ntok; q += kRegWarps * 32)
+    idx_row[tail0 + q] = g.tail * blk + q;
+  // the count: less the cut of the last unit when that unit is in the output
+  const int64_t cut = g.n_units * g.block - g.n_tokens;
+  const int64_t total = (int64_t)(g.lead + nsel_all + ntail) * blk;
+  if (last_cand) {
+    const int owner = (M - 1) / (32 * JW) * 32 + (M - 1) % 32;  // thread holding candidate M - 1
+    if ((int)threadIdx.x == owner) count[row] = (int32_t)(last_taken ? total - cut : total);
+  } else if (threadIdx.x == 0) {
+    const bool last_in = ntail > 0 || (M == 0 && g.lead == g.n_units);
+    count[row] = (int32_t)(last_in ? total - cut : total);
+  }
+}
+
+template <bool F32, int JW>
+static int launch_topk_reg(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
+                           int64_t idx_stride, int32_t* count, cudaStream_t st) {
+  topk_reg_kernel<F32, JW><<<(unsigned)rows, kRegWarps * 32, 0, st>>>(scores, g, idx, idx_stride,
+                                                                      count);
+  note_launches(1);
+  return check_launch("topk_reg");
+}
+
+template <bool F32>
+static int topk_reg(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
+                    int64_t idx_stride, int32_t* count, cudaStream_t st) {
+  if (g.M <= 128) return launch_topk_reg<F32, 1>(scores, rows, g, idx, idx_stride, count, st);
+  if (g.M <= 256) return launch_topk_reg<F32, 2>(scores, rows, g, idx, idx_stride, count, st);
+  if (g.M <= 512) return launch_topk_reg<F32, 4>(scores, rows, g, idx, idx_stride, count, st);
+  if (g.M <= 1024) return launch_topk_reg<F32, 8>(scores, rows, g, idx, idx_stride, count, st);
+  return launch_topk_reg<F32, 16>(scores, rows, g, idx, idx_stride, count, st);
 }
 
 // --------------------------------------------------------------------------------------
@@ -1267,6 +1464,8 @@ template <bool F32>
 static int topk_t(const void* scores, int64_t rows, const Geo& g, int32_t* idx,
                   int64_t idx_stride, int32_t* count, void* wsp, cudaStream_t st) {
   const size_t smem = sizeof(FinSmem);
+  if (g.n_units <= kSmallRow && g.M <= kRegRow)
+    return topk_reg<F32>(scores, rows, g, idx, idx_stride, count, st);
   if (g.n_units <= kSmallRow) {
     auto kern = topk_small_kernel<F32>;
     if (int rc_ = set_smem_limit((const void*)kern, smem, "topk: smem attribute")) return rc_;

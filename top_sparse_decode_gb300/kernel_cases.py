@@ -28,6 +28,8 @@ the cases fix those.  Cases:
                 maxima (sd_topk_wmax), as in the long-context step
   attend_1m     gather-attend of 8 rows x 512 selected tokens (sd_gather_attend), the
                 long-context step's shape; K/V of 131,072 tokens
+  topk_quest    top-128 of 1,024 block scores (16-token blocks, last block forced) in
+                each of 64 x 8 rows (sd_topk), the Quest step's selection
 """
 from __future__ import annotations
 
@@ -209,6 +211,17 @@ def make_case(name: str):
         ws = torch.empty(max(sd.sd_topk_workspace_size(Hkv, n, sel), 256), dtype=torch.uint8,
                          device=DEV)
         return lambda: sd.sd_topk_wmax(scores, wmax, Hkv, n, sel, idx, stride, cnt, ws)
+    if name == "topk_quest":  # the Quest step's block selection: 512 rows of 1,024 blocks
+        rows, nb, blk = 64 * 8, 1024, 16
+        scores = torch.randn((rows, nb), device=DEV, generator=gen)
+        sel = sd.make_select(128, 0, 1, blk)
+        stride = 129 * blk
+        idx = torch.empty((rows, stride), dtype=torch.int32, device=DEV)
+        cnt = torch.empty((rows,), dtype=torch.int32, device=DEV)
+        ws = torch.empty(max(sd.sd_topk_workspace_size(rows, nb, sel), 256), dtype=torch.uint8,
+                         device=DEV)
+        return lambda: sd.sd_topk(sd.SD_SCORE_F32, scores, rows, nb, nb * blk, sel, idx, stride,
+                                  cnt, ws)
     if name == "attend_1m":  # the long-context step's gather-attend: 8 rows of 512 tokens
         Hkv, G, n, c = 8, 4, 1 << 17, 512
         K = _bf16((1, Hkv, n, 128), gen)
