@@ -2,9 +2,10 @@
 
     python -m top_sparse_decode_gb300.kernel_cases <case> [--reps R]
 
-Each case allocates inputs larger than the GB300's 129 MB L2 but at most a few GB
-of device memory, runs the case's library call R times (default 3) and waits for
-the device.  Values are random (normal keys and queries, random signatures and
+Each bandwidth case allocates inputs larger than the GB300's 129 MB L2 but at most
+a few GB of device memory; the latency cases (topk_wmax, topk_quest, merge) use the
+step's own, smaller shapes.  A case runs its library call R times (default 3) and
+waits for the device.  Values are random (normal keys and queries, random signatures and
 summaries); what a kernel reads and writes depends on the shapes and the plan, and
 the cases fix those.  Cases:
 
