@@ -209,7 +209,8 @@ int sd_score(int kind, const sd_shape* shape, const void* index0, const void* in
  *   each unit expanded to tokens [u*block, min((u+1)*block, n_tokens));
  *   count int32 [rows] = tokens written (-1 if the row holds a NaN score).
  *   Entries past count are not written.  idx_stride must be at least
- *   min(n_units, sink + local + k) * block.  Limits: 1 <= k <= 4096.
+ *   min(n_units, sink + local + k) * block.  Limits: 1 <= k <= 4096; n_tokens and
+ *   min(n_units, sink + local + k) * block below 2^31 (SD_ERR_UNSUPPORTED).
  *   Workspace: sd_topk_workspace_size() bytes (device), contents need not be
  *   initialised; calls sharing a workspace must not overlap.
  */

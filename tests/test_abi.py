@@ -152,6 +152,12 @@ def test_argument_checks(sd):
     selb = sd.make_select(4, 0, 1, 16)
     assert lib.sd_topk(1, P, 1, 10, 200, ctypes.byref(selb), P, 80, P, None, 0, None) == \
         sd.SD_ERR_INVALID_ARG
+    # token indices are int32: a row's tokens and its output must stay below 2^31
+    selh = sd.make_select(2, 0, 0, 1 << 30)
+    assert lib.sd_topk(1, P, 1, 3, (1 << 31) + 5, ctypes.byref(selh), P, 1 << 31, P, None, 0,
+                       None) == sd.SD_ERR_UNSUPPORTED
+    assert lib.sd_topk(1, P, 1, 2, (1 << 30) + 5, ctypes.byref(selh), P, 1 << 31, P, None, 0,
+                       None) == sd.SD_ERR_UNSUPPORTED
     # gather-attend workspace
     wsz = sd.sd_gather_attend_workspace_size(shp, 200)
     assert wsz > 0

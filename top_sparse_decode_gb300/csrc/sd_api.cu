@@ -261,6 +261,9 @@ int sd_topk(int score_type, const void* scores, int64_t rows, int64_t n_units,
     return fail(SD_ERR_INVALID_ARG, "sd_topk: n_tokens does not match n_units * block");
   int64_t max_units = n_units < (int64_t)sel->sink + sel->local + sel->k
                           ? n_units : (int64_t)sel->sink + sel->local + sel->k;
+  if (n_tokens >= ((int64_t)1 << 31) || max_units * sel->block >= ((int64_t)1 << 31))
+    return fail(SD_ERR_UNSUPPORTED, "sd_topk: %lld tokens or %lld output entries per row (limit 2^31 - 1)",
+                (long long)n_tokens, (long long)(max_units * sel->block));
   if (idx_stride < max_units * sel->block)
     return fail(SD_ERR_INVALID_ARG, "sd_topk: idx_stride %lld < %lld", (long long)idx_stride,
                 (long long)(max_units * sel->block));
