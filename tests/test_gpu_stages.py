@@ -406,6 +406,30 @@ def test_topk_reg_rows_block_mode_last_unit(sd):
         assert np.array_equal(gi[r, :gc[r]], ri[r, :rc[r]]), r
 
 
+def test_topk_reg_rows_odd_blocks_and_strides(sd):
+    # 6-token blocks (scalar token writes, a division per position in the windows'
+    # writer) with a cut last block, and 16-token blocks with a row stride that is not
+    # a multiple of 4 entries (no 16-byte stores)
+    for blk, extra in ((6, 0), (16, 1), (4, 3)):
+        nblk = 700
+        s = synth.make_scores(90 + blk, 9, nblk, "f32ties", 5)
+        s[::3, nblk - 1] = 10.0  # the cut last block is taken in rows 0, 3, 6
+        n_tokens = nblk * blk - (blk - 1)
+        sel = sd.make_select(50, 2, 0, blk)
+        stride = (2 + 50) * blk + extra
+        idx = torch.full((9, stride), -7, dtype=torch.int32, device="cuda")
+        cnt = empty((9,), np.int32)
+        sd.sd_topk(sd.SD_SCORE_F32, dev(s), 9, nblk, n_tokens, sel, idx, stride, cnt, None)
+        torch.cuda.synchronize()
+        gi, gc = host(idx, np.int32), host(cnt, np.int32)
+        ri, rc = oracle.topk(s, 50, 2, 0, block=blk, n_tokens=n_tokens)
+        assert np.array_equal(gc, rc), (blk, gc, rc)
+        assert gc[0] == 52 * blk - (blk - 1) and gc[1] == 52 * blk
+        for r in range(9):
+            assert np.array_equal(gi[r, :gc[r]], ri[r, :rc[r]]), (blk, r)
+            assert (gi[r, gc[r]:] == -7).all(), (blk, r)  # nothing written past count
+
+
 def test_topk_reg_rows_signed_zeros_infinities_nan(sd):
     rng = np.random.default_rng(11)
     s = rng.standard_normal((8, 1000)).astype(np.float32)
